@@ -1,0 +1,201 @@
+"""Python loader for the fp64 CPU oracle (``nsa_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the smoke check and by
+the benchmark's CPU-baseline leg.  The product library never imports it.
+
+Every wrapper takes numpy-convertible arrays (torch CPU tensors work), turns
+the floating-point ones into contiguous fp64 and returns fp64 numpy arrays.
+Layouts follow the C file: fixed length [B, H, T, D] when ``cu_seqlens`` is
+None, packed [total, H, D] otherwise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_i64 = C.c_int64
+_dbl = C.c_double
+_ptr = C.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with the host C compiler (gcc/cc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cc = os.environ.get("CC", "gcc")
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([cc, "-O2", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = C.CDLL(_LIB)
+        L.oracle_validate_index.restype = C.c_int
+        L.oracle_validate_index.argtypes = [_i64] * 5 + [_ptr, _ptr]
+        common = [_i64] * 7 + [_dbl, _ptr]
+        L.oracle_sel_fwd.restype = None
+        L.oracle_sel_fwd.argtypes = common + [_ptr] * 6
+        L.oracle_sel_bwd.restype = None
+        L.oracle_sel_bwd.argtypes = common + [_ptr] * 10
+        L.oracle_inverse_index.restype = None
+        L.oracle_inverse_index.argtypes = [_i64] * 5 + [_ptr, _ptr, _i64, _ptr, _ptr]
+        L.oracle_do_dot.restype = None
+        L.oracle_do_dot.argtypes = [_i64] * 4 + [_ptr] * 4
+        L.oracle_count_pairs.restype = _i64
+        L.oracle_count_pairs.argtypes = [_i64] * 6 + [_ptr, _ptr]
+        L.oracle_sel_rows.restype = None
+        L.oracle_sel_rows.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 6
+        L.oracle_sel_keys.restype = None
+        L.oracle_sel_keys.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5
+        _lib = L
+    return _lib
+
+
+def _f64(x):
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _shape(q, k, idx, cu_seqlens):
+    """(B, Hq, Hkv, T, D, S) from the tensors' shapes."""
+    if cu_seqlens is None:
+        B, Hq, T, D = q.shape
+        Hkv = k.shape[1]
+        S = idx.shape[3]
+    else:
+        T, Hq, D = q.shape  # T = packed total
+        Hkv = k.shape[1]
+        S = idx.shape[2]
+        B = len(cu_seqlens) - 1
+    return B, Hq, Hkv, T, D, S
+
+
+def sel_fwd(q, k, v, idx, bs, scale=None, cu_seqlens=None):
+    """Returns (O, LSE) in fp64."""
+    q, k, v, idx, cu = _f64(q), _f64(k), _f64(v), _i32(idx), _i32(cu_seqlens)
+    B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros_like(q)
+    lse = np.zeros(q.shape[:-1], dtype=np.float64)
+    lib().oracle_sel_fwd(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                         _p(o), _p(lse))
+    return o, lse
+
+
+def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False):
+    """Returns dict with dq, dk, dv, o, lse (and dsum = row sums of dS)."""
+    q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
+    B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.zeros(q.shape[:-1], dtype=np.float64)
+    dsum = np.zeros(q.shape[:-1], dtype=np.float64) if want_dsum else None
+    lib().oracle_sel_bwd(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                         _p(dO), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(dsum))
+    out = dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse)
+    if want_dsum:
+        out["dsum"] = dsum
+    return out
+
+
+def validate_index(idx, bs, cu_seqlens=None, T=None):
+    """0 when the index is valid, 3 (bad index) otherwise."""
+    idx, cu = _i32(idx), _i32(cu_seqlens)
+    if cu is None:
+        B, Hkv, T, S = idx.shape
+    else:
+        T, Hkv, S = idx.shape
+        B = len(cu) - 1
+    return int(lib().oracle_validate_index(B, Hkv, T, bs, S, _p(cu), _p(idx)))
+
+
+def inverse_index(idx, bs, cu_seqlens=None):
+    """Returns (offsets int32 [B*Hkv*nbmax + 1], rows int32 [nnz], nbmax)."""
+    idx, cu = _i32(idx), _i32(cu_seqlens)
+    if cu is None:
+        B, Hkv, T, S = idx.shape
+        maxlen = T
+    else:
+        T, Hkv, S = idx.shape
+        B = len(cu) - 1
+        maxlen = int(np.max(np.diff(cu))) if B > 0 else 0
+    nbmax = (maxlen + bs - 1) // bs
+    offsets = np.zeros(B * Hkv * nbmax + 1, dtype=np.int32)
+    rows = np.zeros(max(1, idx.size), dtype=np.int32)
+    lib().oracle_inverse_index(B, Hkv, T, bs, S, _p(cu), _p(idx), nbmax, _p(offsets), _p(rows))
+    return offsets, rows[: offsets[-1]].copy(), nbmax
+
+
+def do_dot(o, dO, cu_seqlens=None):
+    o, dO, cu = _f64(o), _f64(dO), _i32(cu_seqlens)
+    if cu is None:
+        B, H, T, D = o.shape
+    else:
+        T, H, D = o.shape
+        B = len(cu) - 1
+    out = np.zeros(o.shape[:-1], dtype=np.float64)
+    lib().oracle_do_dot(B, H, T, D, _p(cu), _p(o), _p(dO), _p(out))
+    return out
+
+
+def count_pairs(idx, Hq, bs, cu_seqlens=None):
+    idx, cu = _i32(idx), _i32(cu_seqlens)
+    if cu is None:
+        B, Hkv, T, S = idx.shape
+    else:
+        T, Hkv, S = idx.shape
+        B = len(cu) - 1
+    return int(lib().oracle_count_pairs(B, Hq, Hkv, T, bs, S, _p(cu), _p(idx)))
+
+
+def sel_rows(q, k, v, idx, dO, bs, rows, scale=None, cu_seqlens=None):
+    """rows: int array [n, 3] of (b, h, t).  Returns (o [n,D], lse [n], dq [n,D])."""
+    q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
+    B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    rb, rh, rt = (np.ascontiguousarray(rows[:, i]) for i in range(3))
+    n = rows.shape[0]
+    o, lse, dq = np.zeros((n, D)), np.zeros(n), np.zeros((n, D))
+    lib().oracle_sel_rows(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                          _p(dO), n, _p(rb), _p(rh), _p(rt), _p(o), _p(lse), _p(dq))
+    return o, lse, dq
+
+
+def sel_keys(q, k, v, idx, dO, bs, keys, scale=None, cu_seqlens=None):
+    """keys: int array [n, 3] of (b, g, key).  Returns (dk [n,D], dv [n,D])."""
+    q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
+    B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64).reshape(-1, 3))
+    kb, kg, kk = (np.ascontiguousarray(keys[:, i]) for i in range(3))
+    n = keys.shape[0]
+    dk, dv = np.zeros((n, D)), np.zeros((n, D))
+    lib().oracle_sel_keys(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                          _p(dO), n, _p(kb), _p(kg), _p(kk), _p(dk), _p(dv))
+    return dk, dv

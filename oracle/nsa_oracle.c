@@ -1,0 +1,470 @@
+/*
+ * nsa_oracle.c -- plain fp64 CPU oracle for Native-Sparse-Attention block
+ * selection (forward and analytic backward) under grouped-query attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this file:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg load
+ * it.  It shares no code with the CUDA library.
+ *
+ * What it computes (the gradcheck-gate page, "test_kernel_backward.py":
+ * run_one builds q,k,v [B,H,T,D], idx = make_block_idx(B,Hkv,T,bs,S) and
+ * compares dQ/dK/dV of selection attention against autograd through the
+ * plain torch forward; the definitions below are that forward and its exact
+ * derivative, written out per output element):
+ *
+ *   G = Hq / Hkv, query head h reads kv head g = h / G.
+ *   sel(t)  = { idx[b,g,t,s] : 0 <= s < S, idx != -1 }
+ *   key k is attended by row (b,h,t) iff k <= t and k / bs is in sel(t)
+ *   s_tk    = scale * <q_t, k_k>
+ *   LSE_t   = log sum_k exp(s_tk)        (max-shifted; -inf for an empty row)
+ *   P_tk    = exp(s_tk - LSE_t)
+ *   O_t     = sum_k P_tk v_k             (0 for an empty row)
+ *   D_t     = <dO_t, O_t>
+ *   dP_tk   = <dO_t, v_k>
+ *   dS_tk   = P_tk (dP_tk - D_t)
+ *   dQ_t    = scale * sum_k dS_tk k_k
+ *   dK_k    = scale * sum_{h in group, t} dS_tk q_t
+ *   dV_k    = sum_{h in group, t} P_tk dO_t
+ *
+ * Readings of points the pages leave open: scale is passed in (callers use
+ * 1/sqrt(D)); keys after t inside the own block are masked (causal); -1
+ * slots are ignored wherever they sit; an index is invalid if it is < -1,
+ * lies in the future (> t / bs), or repeats within a row.
+ *
+ * Layouts.  Fixed length ("BHTD"): q,o,dO,dq [B,Hq,T,D]; k,v,dk,dv
+ * [B,Hkv,T,D]; idx [B,Hkv,T,S]; lse [B,Hq,T].  Packed variable length
+ * ("THD", cu_seqlens != NULL, B = number of sequences): q [total,Hq,D],
+ * k [total,Hkv,D], idx [total,Hkv,S] holding sequence-local block ids,
+ * lse [total,Hq]; causality and block numbering are local to a sequence.
+ *
+ * Build: cc -O2 -fopenmp -fPIC -shared nsa_oracle.c -o liboracle.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int64_t B, Hq, Hkv, T, D, bs, S;
+    double scale;
+    const int32_t *cu; /* NULL: fixed length */
+} prob_t;
+
+static prob_t mk(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D,
+                 int64_t bs, int64_t S, double scale, const int32_t *cu)
+{
+    prob_t p = {B, Hq, Hkv, T, D, bs, S, scale, cu};
+    return p;
+}
+
+static int64_t seq_len(const prob_t *p, int64_t b)
+{
+    return p->cu ? (int64_t)p->cu[b + 1] - p->cu[b] : p->T;
+}
+
+/* element offset of the D-vector of (b, head, t) in a tensor with H heads */
+static int64_t row_off(const prob_t *p, int64_t H, int64_t b, int64_t h, int64_t t)
+{
+    if (p->cu)
+        return (((int64_t)p->cu[b] + t) * H + h) * p->D;
+    return ((b * H + h) * p->T + t) * p->D;
+}
+
+/* offset of a per-row scalar (lse, row sums) */
+static int64_t stat_off(const prob_t *p, int64_t H, int64_t b, int64_t h, int64_t t)
+{
+    if (p->cu)
+        return ((int64_t)p->cu[b] + t) * H + h;
+    return (b * H + h) * p->T + t;
+}
+
+static const int32_t *idx_row(const prob_t *p, const int32_t *idx, int64_t b, int64_t g, int64_t t)
+{
+    if (p->cu)
+        return idx + (((int64_t)p->cu[b] + t) * p->Hkv + g) * p->S;
+    return idx + ((b * p->Hkv + g) * p->T + t) * p->S;
+}
+
+static double dot(const double *a, const double *b, int64_t n)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        s += a[i] * b[i];
+    return s;
+}
+
+/* 1 if block j is one of the row's selected blocks */
+static int selects(const prob_t *p, const int32_t *row, int64_t j)
+{
+    for (int64_t s = 0; s < p->S; ++s)
+        if (row[s] == j)
+            return 1;
+    return 0;
+}
+
+/*
+ * Index validation.  Returns 0 when every entry is -1 or a distinct block id
+ * in [0, t / bs]; 3 otherwise (the library's "bad index" status).
+ */
+int oracle_validate_index(int64_t B, int64_t Hkv, int64_t T, int64_t bs, int64_t S,
+                          const int32_t *cu, const int32_t *idx)
+{
+    prob_t p = mk(B, Hkv, Hkv, T, 1, bs, S, 1.0, cu);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                const int32_t *row = idx_row(&p, idx, b, g, t);
+                for (int64_t s = 0; s < S; ++s) {
+                    int64_t j = row[s];
+                    if (j == -1)
+                        continue;
+                    if (j < -1 || j > t / bs)
+                        return 3;
+                    for (int64_t s2 = 0; s2 < s; ++s2)
+                        if (row[s2] == j)
+                            return 3;
+                }
+            }
+    return 0;
+}
+
+/*
+ * Scores of one row over its attended keys.  Fills keys[] (sequence-local key
+ * positions) and sc[] (scale * q.k); returns the number of attended keys.
+ * Keys come block by block in slot order; the set is what matters.
+ */
+static int64_t row_scores(const prob_t *p, const double *q, const double *k, const int32_t *idx,
+                          int64_t b, int64_t h, int64_t t, int64_t *keys, double *sc)
+{
+    const int64_t G = p->Hq / p->Hkv, g = h / G;
+    const int32_t *row = idx_row(p, idx, b, g, t);
+    const double *qt = q + row_off(p, p->Hq, b, h, t);
+    int64_t n = 0;
+    for (int64_t s = 0; s < p->S; ++s) {
+        int64_t j = row[s];
+        if (j < 0)
+            continue;
+        for (int64_t kk = j * p->bs; kk < (j + 1) * p->bs && kk <= t; ++kk) {
+            keys[n] = kk;
+            sc[n] = p->scale * dot(qt, k + row_off(p, p->Hkv, b, g, kk), p->D);
+            ++n;
+        }
+    }
+    return n;
+}
+
+/* log-sum-exp of sc[0..n) with the max shift; -inf when n == 0 */
+static double lse_of(const double *sc, int64_t n)
+{
+    if (n == 0)
+        return -INFINITY;
+    double m = sc[0];
+    for (int64_t i = 1; i < n; ++i)
+        if (sc[i] > m)
+            m = sc[i];
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        l += exp(sc[i] - m);
+    return m + log(l);
+}
+
+/* forward of one row: writes o (D values) and returns LSE */
+static double row_forward(const prob_t *p, const double *q, const double *k, const double *v,
+                          const int32_t *idx, int64_t b, int64_t h, int64_t t, double *o,
+                          int64_t *keys, double *sc)
+{
+    const int64_t G = p->Hq / p->Hkv, g = h / G;
+    int64_t n = row_scores(p, q, k, idx, b, h, t, keys, sc);
+    double lse = lse_of(sc, n);
+    for (int64_t d = 0; d < p->D; ++d)
+        o[d] = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double pk = exp(sc[i] - lse);
+        const double *vk = v + row_off(p, p->Hkv, b, g, keys[i]);
+        for (int64_t d = 0; d < p->D; ++d)
+            o[d] += pk * vk[d];
+    }
+    return lse;
+}
+
+static int64_t max_keys(const prob_t *p) { return p->S * p->bs + 1; }
+
+static int64_t n_rows_total(const prob_t *p)
+{
+    int64_t n = 0;
+    for (int64_t b = 0; b < p->B; ++b)
+        n += seq_len(p, b);
+    return n;
+}
+
+/* Forward: o (layout of q) and lse. */
+void oracle_sel_fwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                    int64_t S, double scale, const int32_t *cu, const double *q,
+                    const double *k, const double *v, const int32_t *idx, double *o,
+                    double *lse)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+#pragma omp parallel
+    {
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
+        double *sc = (double *)malloc(sizeof(double) * max_keys(&p));
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t h = 0; h < Hq; ++h)
+                for (int64_t t = 0; t < seq_len(&p, b); ++t)
+                    lse[stat_off(&p, Hq, b, h, t)] =
+                        row_forward(&p, q, k, v, idx, b, h, t, o + row_off(&p, Hq, b, h, t),
+                                    keys, sc);
+        free(keys);
+        free(sc);
+    }
+}
+
+/*
+ * Backward.  Recomputes the forward in fp64 (O, LSE), then
+ *   pass 1, one query row at a time: D_t, dQ_t and (optionally) sum_k dS_tk;
+ *   pass 2, one key at a time: dK_k and dV_k as sums over every row (h, t) of
+ *           the group that attends k.
+ * o_out / lse_out / dsum_out may be NULL.
+ */
+void oracle_sel_bwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                    int64_t S, double scale, const int32_t *cu, const double *q,
+                    const double *k, const double *v, const int32_t *idx, const double *dO,
+                    double *dq, double *dk, double *dv, double *o_out, double *lse_out,
+                    double *dsum_out)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    const int64_t G = Hq / Hkv;
+    const int64_t nrow = n_rows_total(&p) * Hq;
+    double *O = o_out ? o_out : (double *)malloc(sizeof(double) * nrow * D);
+    double *L = lse_out ? lse_out : (double *)malloc(sizeof(double) * nrow);
+    double *Dt = (double *)malloc(sizeof(double) * nrow);
+
+    /* pass 1: per query row */
+#pragma omp parallel
+    {
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
+        double *sc = (double *)malloc(sizeof(double) * max_keys(&p));
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t h = 0; h < Hq; ++h)
+                for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                    const int64_t ro = row_off(&p, Hq, b, h, t), so = stat_off(&p, Hq, b, h, t);
+                    const int64_t g = h / G;
+                    double lse = row_forward(&p, q, k, v, idx, b, h, t, O + ro, keys, sc);
+                    L[so] = lse;
+                    const double *dOt = dO + ro;
+                    double Dv = dot(dOt, O + ro, D);
+                    Dt[so] = Dv;
+                    int64_t n = row_scores(&p, q, k, idx, b, h, t, keys, sc);
+                    double *dqt = dq + ro;
+                    for (int64_t d = 0; d < D; ++d)
+                        dqt[d] = 0.0;
+                    double dsum = 0.0;
+                    for (int64_t i = 0; i < n; ++i) {
+                        const double *kk = k + row_off(&p, Hkv, b, g, keys[i]);
+                        const double *vk = v + row_off(&p, Hkv, b, g, keys[i]);
+                        double P = exp(sc[i] - lse);
+                        double dP = dot(dOt, vk, D);
+                        double dS = P * (dP - Dv);
+                        dsum += dS;
+                        for (int64_t d = 0; d < D; ++d)
+                            dqt[d] += scale * dS * kk[d];
+                    }
+                    if (dsum_out)
+                        dsum_out[so] = dsum;
+                }
+        free(keys);
+        free(sc);
+    }
+
+    /* pass 2: per key, sum over every row of the group that attends it */
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t kk = 0; kk < seq_len(&p, b); ++kk) {
+                const int64_t ko = row_off(&p, Hkv, b, g, kk);
+                const double *kv = k + ko, *vv = v + ko;
+                double *dkk = dk + ko, *dvk = dv + ko;
+                for (int64_t d = 0; d < D; ++d) {
+                    dkk[d] = 0.0;
+                    dvk[d] = 0.0;
+                }
+                const int64_t j = kk / bs;
+                for (int64_t t = kk; t < seq_len(&p, b); ++t) {
+                    if (!selects(&p, idx_row(&p, idx, b, g, t), j))
+                        continue;
+                    for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                        const int64_t ro = row_off(&p, Hq, b, h, t), so = stat_off(&p, Hq, b, h, t);
+                        const double *qt = q + ro, *dOt = dO + ro;
+                        double s = scale * dot(qt, kv, D);
+                        double P = exp(s - L[so]);
+                        double dP = dot(dOt, vv, D);
+                        double dS = P * (dP - Dt[so]);
+                        for (int64_t d = 0; d < D; ++d) {
+                            dkk[d] += scale * dS * qt[d];
+                            dvk[d] += P * dOt[d];
+                        }
+                    }
+                }
+            }
+
+    if (!o_out)
+        free(O);
+    if (!lse_out)
+        free(L);
+    free(Dt);
+}
+
+/*
+ * Inverse index (block -> selecting tokens), by brute force.
+ * offsets has B*Hkv*nbmax + 1 entries, nbmax = ceil(max sequence length / bs);
+ * entry (b,g,j) lists, in ascending order, every sequence-local token t whose
+ * row selects block j.  Blocks past a sequence's end have empty lists.
+ * rows must hold offsets[B*Hkv*nbmax] entries (at most total_tokens*Hkv*S).
+ */
+void oracle_inverse_index(int64_t B, int64_t Hkv, int64_t T, int64_t bs, int64_t S,
+                          const int32_t *cu, const int32_t *idx, int64_t nbmax,
+                          int32_t *offsets, int32_t *rows)
+{
+    prob_t p = mk(B, Hkv, Hkv, T, 1, bs, S, 1.0, cu);
+    int64_t n = 0;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t j = 0; j < nbmax; ++j) {
+                offsets[(b * Hkv + g) * nbmax + j] = (int32_t)n;
+                for (int64_t t = 0; t < seq_len(&p, b); ++t)
+                    if (selects(&p, idx_row(&p, idx, b, g, t), j))
+                        rows[n++] = (int32_t)t;
+            }
+    offsets[B * Hkv * nbmax] = (int32_t)n;
+}
+
+/* D_t = <dO_t, O_t> for every row (layout of lse) */
+void oracle_do_dot(int64_t B, int64_t Hq, int64_t T, int64_t D, const int32_t *cu,
+                   const double *o, const double *dO, double *out)
+{
+    prob_t p = mk(B, Hq, Hq, T, D, 1, 1, 1.0, cu);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < Hq; ++h)
+            for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                int64_t ro = row_off(&p, Hq, b, h, t);
+                out[stat_off(&p, Hq, b, h, t)] = dot(dO + ro, o + ro, D);
+            }
+}
+
+/* Number of (query row, attended key) pairs summed over query heads. */
+int64_t oracle_count_pairs(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t bs, int64_t S,
+                           const int32_t *cu, const int32_t *idx)
+{
+    prob_t p = mk(B, Hq, Hkv, T, 1, bs, S, 1.0, cu);
+    const int64_t G = Hq / Hkv;
+    int64_t n = 0;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                const int32_t *row = idx_row(&p, idx, b, g, t);
+                for (int64_t s = 0; s < S; ++s) {
+                    int64_t j = row[s];
+                    if (j < 0)
+                        continue;
+                    int64_t hi = (j + 1) * bs - 1;
+                    if (hi > t)
+                        hi = t;
+                    if (hi >= j * bs)
+                        n += G * (hi - j * bs + 1);
+                }
+            }
+    return n;
+}
+
+/*
+ * Sampled outputs, for problems too large to run whole: the same definitions
+ * evaluated only at the requested rows / keys.
+ *
+ * oracle_sel_rows: for each (b, h, t) in the list, O_t, LSE_t and dQ_t.
+ */
+void oracle_sel_rows(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                     int64_t S, double scale, const int32_t *cu, const double *q,
+                     const double *k, const double *v, const int32_t *idx, const double *dO,
+                     int64_t n, const int64_t *rb, const int64_t *rh, const int64_t *rt,
+                     double *o_out, double *lse_out, double *dq_out)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel
+    {
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
+        double *sc = (double *)malloc(sizeof(double) * max_keys(&p));
+#pragma omp for schedule(dynamic)
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t b = rb[i], h = rh[i], t = rt[i], g = h / G;
+            double *o = o_out + i * D, *dqt = dq_out + i * D;
+            const double *dOt = dO + row_off(&p, Hq, b, h, t);
+            double lse = row_forward(&p, q, k, v, idx, b, h, t, o, keys, sc);
+            lse_out[i] = lse;
+            double Dv = dot(dOt, o, D);
+            int64_t m = row_scores(&p, q, k, idx, b, h, t, keys, sc);
+            for (int64_t d = 0; d < D; ++d)
+                dqt[d] = 0.0;
+            for (int64_t c = 0; c < m; ++c) {
+                const int64_t ko = row_off(&p, Hkv, b, g, keys[c]);
+                double P = exp(sc[c] - lse);
+                double dS = P * (dot(dOt, v + ko, D) - Dv);
+                for (int64_t d = 0; d < D; ++d)
+                    dqt[d] += scale * dS * k[ko + d];
+            }
+        }
+        free(keys);
+        free(sc);
+    }
+}
+
+/*
+ * oracle_sel_keys: for each (b, g, key) in the list, dK and dV of that key;
+ * LSE_t and D_t of every attending row are recomputed from scratch.
+ */
+void oracle_sel_keys(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                     int64_t S, double scale, const int32_t *cu, const double *q,
+                     const double *k, const double *v, const int32_t *idx, const double *dO,
+                     int64_t n, const int64_t *kb, const int64_t *kg, const int64_t *kk_,
+                     double *dk_out, double *dv_out)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel
+    {
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
+        double *sc = (double *)malloc(sizeof(double) * max_keys(&p));
+        double *o = (double *)malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic)
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t b = kb[i], g = kg[i], kk = kk_[i], j = kk / bs;
+            const int64_t ko = row_off(&p, Hkv, b, g, kk);
+            double *dkk = dk_out + i * D, *dvk = dv_out + i * D;
+            for (int64_t d = 0; d < D; ++d) {
+                dkk[d] = 0.0;
+                dvk[d] = 0.0;
+            }
+            for (int64_t t = kk; t < seq_len(&p, b); ++t) {
+                if (!selects(&p, idx_row(&p, idx, b, g, t), j))
+                    continue;
+                for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                    const int64_t ro = row_off(&p, Hq, b, h, t);
+                    const double *qt = q + ro, *dOt = dO + ro;
+                    double lse = row_forward(&p, q, k, v, idx, b, h, t, o, keys, sc);
+                    double Dv = dot(dOt, o, D);
+                    double P = exp(scale * dot(qt, k + ko, D) - lse);
+                    double dS = P * (dot(dOt, v + ko, D) - Dv);
+                    for (int64_t d = 0; d < D; ++d) {
+                        dkk[d] += scale * dS * qt[d];
+                        dvk[d] += P * dOt[d];
+                    }
+                }
+            }
+        }
+        free(keys);
+        free(sc);
+        free(o);
+    }
+}

@@ -1,0 +1,332 @@
+"""Pins for the fp64 CPU oracle, against things other than itself.
+
+Each pin targets a mistake the oracle could plausibly make:
+
+* masked dense attention through torch's scaled_dot_product_attention +
+  autograd (a library routine; selection attention is by definition dense
+  attention under the mask "k <= t and k // bs in sel(t)", and the mask here
+  is built by brute force from the index) -- catches wrong key sets, wrong
+  GQA mapping, transposed operands, sign or scale errors in any gradient;
+* central finite differences of L = <dO, O> -- the backward is the derivative
+  of the forward;
+* the dense causal special case against SDPA(is_causal=True);
+* invariants fixed by the mathematics (sum_k dS = 0, sum dV = sum dO,
+  sum dK = 0 per group);
+* closed forms for rows with one attended key;
+* -1 padding wherever it sits, slot order, empty rows;
+* the inverse index against a pure-Python brute force;
+* index validation cases.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from block_sparse_attention_do_gb300 import inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _mask_from_idx(idx, T, bs):
+    """bool [B, Hkv, T, T] mask by brute force over the index rows."""
+    idx = idx.numpy()
+    B, Hkv = idx.shape[:2]
+    m = np.zeros((B, Hkv, T, T), dtype=bool)
+    for b in range(B):
+        for g in range(Hkv):
+            for t in range(T):
+                blocks = {int(j) for j in idx[b, g, t] if j >= 0}
+                for k in range(t + 1):
+                    if k // bs in blocks:
+                        m[b, g, t, k] = True
+    return torch.from_numpy(m)
+
+
+def _sdpa_reference(q, k, v, do, mask_kv, scale):
+    """fp64 masked attention + autograd via torch SDPA; mask per kv head."""
+    G = q.shape[1] // k.shape[1]
+    qr, kr, vr = (x.double().clone().requires_grad_(True) for x in (q, k, v))
+    ke = kr.repeat_interleave(G, dim=1)
+    ve = vr.repeat_interleave(G, dim=1)
+    mask = mask_kv.repeat_interleave(G, dim=1)
+    o = F.scaled_dot_product_attention(qr, ke, ve, attn_mask=mask, scale=scale)
+    o.backward(do.double())
+    return o.detach(), qr.grad, kr.grad, vr.grad
+
+
+CASES = [
+    # B, Hq, Hkv, T, D, bs, S
+    (1, 2, 1, 32, 8, 4, 3),     # G=2
+    (2, 3, 3, 29, 16, 8, 2),    # G=1, ragged tail (29 % 8)
+    (1, 6, 2, 40, 8, 8, 8),     # G=3, S > valid blocks for every row
+    (2, 4, 1, 33, 4, 16, 2),    # G=4, large block, ragged
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_matches_masked_sdpa(case):
+    B, Hq, Hkv, T, D, bs, S = case
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=7)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=3)
+    scale = 1.0 / math.sqrt(D)
+    mask = _mask_from_idx(idx, T, bs)
+    o_ref, dq_ref, dk_ref, dv_ref = _sdpa_reference(q, k, v, do, mask, scale)
+    o, lse = oracle.sel_fwd(q, k, v, idx, bs)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs)
+    np.testing.assert_allclose(o, o_ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["o"], o_ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dq"], dq_ref.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(r["dk"], dk_ref.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(r["dv"], dv_ref.numpy(), rtol=0, atol=1e-11)
+    # LSE: torch.logsumexp over the masked scores (library reduction)
+    G = Hq // Hkv
+    s = torch.einsum("bhtd,bhkd->bhtk", q.double(), k.double().repeat_interleave(G, 1)) * scale
+    s = s.masked_fill(~mask.repeat_interleave(G, 1), -math.inf)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_finite_differences():
+    """Central differences of L = <dO, O(q,k,v)> on every input coordinate."""
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 2, 12, 4, 4, 2
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=11)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=5)
+    idx[0, 1, 9, 1] = -1  # a padded row
+    q, k, v, do = (x.double().numpy() for x in (q, k, v, do))
+    r = oracle.sel_bwd(q, k, v, idx, do, bs)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.sel_fwd(qq, kk, vv, idx, bs)
+        return float(np.sum(o * do))
+
+    for name, x, g in (("q", q, r["dq"]), ("k", k, r["dk"]), ("v", v, r["dv"])):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            xp, xm = x.copy(), x.copy()
+            xp[i] += h
+            xm[i] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[i] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        np.testing.assert_allclose(g, fd, rtol=0, atol=2e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_dense_selection_is_causal_sdpa(G):
+    B, Hkv, T, D, bs = 2, 2, 37, 8, 8
+    Hq = Hkv * G
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=2)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    qr, kr, vr = (x.double().clone().requires_grad_(True) for x in (q, k, v))
+    o = F.scaled_dot_product_attention(qr, kr.repeat_interleave(G, 1), vr.repeat_interleave(G, 1),
+                                       is_causal=True)
+    o.backward(do.double())
+    r = oracle.sel_bwd(q, k, v, idx, do, bs)
+    np.testing.assert_allclose(r["o"], o.detach().numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(r["dq"], qr.grad.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dk"], kr.grad.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dv"], vr.grad.numpy(), atol=1e-11, rtol=0)
+
+
+def test_invariants():
+    B, Hq, Hkv, T, D, bs, S = 2, 6, 2, 96, 16, 8, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=4)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=4)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, want_dsum=True)
+    G = Hq // Hkv
+    assert np.max(np.abs(r["dsum"])) < 1e-12
+    dO = do.double().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            sum_dv = r["dv"][b, g].sum(axis=0)
+            sum_do = dO[b, g * G:(g + 1) * G].sum(axis=(0, 1))
+            np.testing.assert_allclose(sum_dv, sum_do, atol=1e-10, rtol=0)
+            assert np.max(np.abs(r["dk"][b, g].sum(axis=0))) < 1e-10
+    # O is a convex combination of the attended values
+    vmax = v.double().numpy().max()
+    vmin = v.double().numpy().min()
+    assert r["o"].max() <= vmax + 1e-12 and r["o"].min() >= vmin - 1e-12
+
+
+def test_single_key_rows_closed_form():
+    """S = 1 and t at a block start: the row attends only key t."""
+    B, Hq, Hkv, T, D, bs, S = 1, 2, 1, 16, 8, 4, 1
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=9)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs)
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    scale = 1 / math.sqrt(D)
+    for h in range(Hq):
+        for t in range(0, T, bs):
+            np.testing.assert_allclose(r["o"][0, h, t], vd[0, 0, t], atol=1e-14, rtol=0)
+            assert abs(r["lse"][0, h, t] - scale * qd[0, h, t] @ kd[0, 0, t]) < 1e-13
+            assert np.max(np.abs(r["dq"][0, h, t])) < 1e-14
+
+
+def test_two_key_row_closed_form():
+    """Row t = 1 attending keys {0, 1}: softmax of two scores is a sigmoid."""
+    B, Hq, Hkv, T, D, bs, S = 1, 1, 1, 2, 4, 2, 1
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=1)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S)
+    o, lse = oracle.sel_fwd(q, k, v, idx, bs)
+    qd, kd, vd = (x.double().numpy()[0, 0] for x in (q, k, v))
+    scale = 0.5
+    s0, s1 = scale * qd[1] @ kd[0], scale * qd[1] @ kd[1]
+    p1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    np.testing.assert_allclose(o[0, 0, 1], (1 - p1) * vd[0] + p1 * vd[1], atol=1e-14, rtol=0)
+    assert abs(lse[0, 0, 1] - (s1 + math.log1p(math.exp(s0 - s1)))) < 1e-13
+
+
+def test_padding_position_and_slot_order_do_not_matter():
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 2, 48, 8, 4, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=6)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=6)
+    base = oracle.sel_bwd(q, k, v, idx, do, bs)
+    rng = np.random.default_rng(0)
+    wide = np.full((B, Hkv, T, S + 3), -1, dtype=np.int32)
+    for b in range(B):
+        for g in range(Hkv):
+            for t in range(T):
+                perm = rng.permutation(S + 3)
+                wide[b, g, t, perm[:S]] = idx[b, g, t].numpy()
+    r = oracle.sel_bwd(q, k, v, torch.from_numpy(wide), do, bs)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_allclose(r[key], base[key], atol=1e-13, rtol=0, err_msg=key)
+
+
+def test_empty_row_contributes_nothing():
+    B, Hq, Hkv, T, D, bs, S = 1, 2, 1, 24, 8, 4, 3
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=8)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=8)
+    t0 = 13
+    idx_empty = idx.clone()
+    idx_empty[0, 0, t0] = -1
+    r = oracle.sel_bwd(q, k, v, idx_empty, do, bs)
+    assert np.all(r["o"][0, :, t0] == 0) and np.all(np.isneginf(r["lse"][0, :, t0]))
+    assert np.all(r["dq"][0, :, t0] == 0)
+    do_zero = do.clone()
+    do_zero[0, :, t0] = 0
+    ref = oracle.sel_bwd(q, k, v, idx, do_zero, bs)
+    np.testing.assert_allclose(r["dk"], ref["dk"], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(r["dv"], ref["dv"], atol=1e-13, rtol=0)
+
+
+def test_varlen_matches_per_sequence_sdpa():
+    lengths = [7, 33, 20]
+    Hq, Hkv, D, bs, S = 4, 2, 8, 8, 3
+    total = sum(lengths)
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, seed=12, layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=12)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, cu_seqlens=cu)
+    scale = 1 / math.sqrt(D)
+    for i, L in enumerate(lengths):
+        a, b_ = int(cu[i]), int(cu[i + 1])
+        to_bhtd = lambda x: x[a:b_].permute(1, 0, 2).unsqueeze(0)  # noqa: E731
+        idx_s = idx[a:b_].permute(1, 0, 2).unsqueeze(0)
+        mask = _mask_from_idx(idx_s, L, bs)
+        o_ref, dq_ref, dk_ref, dv_ref = _sdpa_reference(
+            to_bhtd(q), to_bhtd(k), to_bhtd(v), to_bhtd(do), mask, scale)
+        back = lambda x: x[0].permute(1, 0, 2).numpy()  # noqa: E731
+        np.testing.assert_allclose(r["o"][a:b_], back(o_ref), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(r["dq"][a:b_], back(dq_ref), atol=1e-11, rtol=0)
+        np.testing.assert_allclose(r["dk"][a:b_], back(dk_ref), atol=1e-11, rtol=0)
+        np.testing.assert_allclose(r["dv"][a:b_], back(dv_ref), atol=1e-11, rtol=0)
+
+
+def _csr_brute(idx_np, lengths, bs, nbmax):
+    offsets, rows = [], []
+    B = len(lengths)
+    Hkv = idx_np[0].shape[1]
+    for b in range(B):
+        for g in range(Hkv):
+            for j in range(nbmax):
+                offsets.append(len(rows))
+                for t in range(lengths[b]):
+                    if j in set(idx_np[b][t, g].tolist()):
+                        rows.append(t)
+    offsets.append(len(rows))
+    return np.array(offsets, dtype=np.int32), np.array(rows, dtype=np.int32)
+
+
+def test_inverse_index_bruteforce_fixed_and_varlen():
+    B, Hkv, T, bs, S = 2, 3, 50, 8, 4
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=13)
+    off, rows, nbmax = oracle.inverse_index(idx, bs)
+    per_b = [idx[b].permute(1, 0, 2).numpy() for b in range(B)]
+    ref_off, ref_rows = _csr_brute(per_b, [T] * B, bs, nbmax)
+    assert np.array_equal(off, ref_off) and np.array_equal(rows, ref_rows)
+    assert off[-1] == int((idx >= 0).sum())
+
+    lengths = [9, 40, 1, 17]
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    vidx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=2)
+    off, rows, nbmax = oracle.inverse_index(vidx, bs, cu_seqlens=cu)
+    per_b = [vidx[int(cu[i]):int(cu[i + 1])].numpy() for i in range(len(lengths))]
+    ref_off, ref_rows = _csr_brute(per_b, lengths, bs, nbmax)
+    assert np.array_equal(off, ref_off) and np.array_equal(rows, ref_rows)
+
+
+def test_validate_index_cases():
+    B, Hkv, T, bs, S = 1, 1, 16, 4, 3
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S)
+    assert oracle.validate_index(idx, bs) == 0
+    bad = idx.clone()
+    bad[0, 0, 5, 1] = 2          # future block for t=5 (own block is 1)
+    assert oracle.validate_index(bad, bs) == 3
+    bad = idx.clone()
+    bad[0, 0, 9, 2] = bad[0, 0, 9, 0]  # duplicate
+    assert oracle.validate_index(bad, bs) == 3
+    bad = idx.clone()
+    bad[0, 0, 3, 2] = -2
+    assert oracle.validate_index(bad, bs) == 3
+    ok = idx.clone()
+    ok[0, 0, 12] = torch.tensor([-1, 0, -1], dtype=torch.int32)  # own block omitted: allowed
+    assert oracle.validate_index(ok, bs) == 0
+
+
+def test_count_pairs_matches_mask():
+    B, Hq, Hkv, T, bs, S = 2, 6, 2, 45, 8, 3
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=1)
+    mask = _mask_from_idx(idx, T, bs)
+    assert oracle.count_pairs(idx, Hq, bs) == int(mask.sum()) * (Hq // Hkv)
+
+
+def test_do_dot_and_sampled_entries_agree_with_whole_problem():
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 2, 40, 8, 8, 3
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=21)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=21)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs)
+    dd = oracle.do_dot(r["o"], do)
+    np.testing.assert_allclose(dd, np.einsum("bhtd,bhtd->bht", r["o"], do.double().numpy()),
+                               atol=1e-13, rtol=0)
+    rows = [(0, 1, 0), (0, 3, 39), (0, 2, 17)]
+    o, lse, dq = oracle.sel_rows(q, k, v, idx, do, bs, rows)
+    for i, (b, h, t) in enumerate(rows):
+        np.testing.assert_allclose(o[i], r["o"][b, h, t], atol=1e-14, rtol=0)
+        np.testing.assert_allclose(dq[i], r["dq"][b, h, t], atol=1e-14, rtol=0)
+        assert abs(lse[i] - r["lse"][b, h, t]) < 1e-14
+    keys = [(0, 0, 0), (0, 1, 39), (0, 1, 8)]
+    dk, dv = oracle.sel_keys(q, k, v, idx, do, bs, keys)
+    for i, (b, g, kk) in enumerate(keys):
+        np.testing.assert_allclose(dk[i], r["dk"][b, g, kk], atol=1e-13, rtol=0)
+        np.testing.assert_allclose(dv[i], r["dv"][b, g, kk], atol=1e-13, rtol=0)
+
+
+def test_planted_mistake_is_caught(monkeypatch):
+    """A transposed GQA mapping (h % Hkv instead of h // G) must fail the SDPA pin."""
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 2, 24, 8, 4, 2
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=3)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=3)
+    mask = _mask_from_idx(idx, T, bs)
+    o_ref, *_ = _sdpa_reference(q, k, v, do, mask, 1 / math.sqrt(D))
+    # plant: permute heads so head h reads kv head h % Hkv
+    perm = [h for r in range(Hkv) for h in range(r, Hq, Hkv)]
+    o_bad, _ = oracle.sel_fwd(q[:, perm], k, v, idx, bs)
+    inv = np.argsort(perm)
+    assert np.max(np.abs(o_bad[:, inv] - o_ref.numpy())) > 1e-3
