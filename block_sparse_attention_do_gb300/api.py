@@ -1,0 +1,256 @@
+"""ctypes binding over libnsa.so (declared in include/nsa.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  torch provides device memory (outputs and the
+workspace) and the current CUDA stream.  There is no CPU fallback: if the
+library is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnsa.so")
+
+NSA_OK = 0
+STATUS = {0: "NSA_OK", 1: "NSA_ERR_INVALID_ARG", 2: "NSA_ERR_UNSUPPORTED", 3: "NSA_ERR_BAD_INDEX",
+          4: "NSA_ERR_DEVICE_TIMEOUT", 5: "NSA_ERR_CUDA", 6: "NSA_ERR_WORKSPACE"}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+LAYOUT_BHTD, LAYOUT_THD = 0, 1
+
+# every entry point of include/nsa.h
+SYMBOLS = (
+    "nsa_fwd_workspace_size", "nsa_bwd_workspace_size", "nsa_sel_fwd", "nsa_sel_bwd",
+    "nsa_dense_causal_fwd", "nsa_dense_causal_bwd", "nsa_sel_varlen_fwd", "nsa_sel_varlen_bwd",
+    "nsa_do_dot", "nsa_inverse_index_offsets_len", "nsa_build_inverse_index", "nsa_get_error",
+    "nsa_status_string", "nsa_count_pairs",
+)
+
+
+class Problem(C.Structure):
+    _fields_ = [("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("T", C.c_int32),
+                ("D", C.c_int32), ("block_size", C.c_int32), ("S", C.c_int32),
+                ("dtype", C.c_int32), ("layout", C.c_int32), ("total_tokens", C.c_int32),
+                ("scale", C.c_float)]
+
+
+class NsaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+_P = C.c_void_p
+
+
+def lib() -> C.CDLL:
+    """Load libnsa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libnsa.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        pp = C.POINTER(Problem)
+        L.nsa_fwd_workspace_size.restype = C.c_size_t
+        L.nsa_fwd_workspace_size.argtypes = [pp]
+        L.nsa_bwd_workspace_size.restype = C.c_size_t
+        L.nsa_bwd_workspace_size.argtypes = [pp]
+        L.nsa_sel_fwd.argtypes = [pp] + [_P] * 6 + [_P, C.c_size_t, _P]
+        L.nsa_sel_bwd.argtypes = [pp] + [_P] * 10 + [_P, C.c_size_t, _P]
+        L.nsa_dense_causal_fwd.argtypes = [pp] + [_P] * 5 + [_P, C.c_size_t, _P]
+        L.nsa_dense_causal_bwd.argtypes = [pp] + [_P] * 9 + [_P, C.c_size_t, _P]
+        L.nsa_sel_varlen_fwd.argtypes = [pp] + [_P] * 7 + [_P, C.c_size_t, _P]
+        L.nsa_sel_varlen_bwd.argtypes = [pp] + [_P] * 11 + [_P, C.c_size_t, _P]
+        L.nsa_do_dot.argtypes = [pp] + [_P] * 4 + [_P]
+        L.nsa_inverse_index_offsets_len.restype = C.c_int64
+        L.nsa_inverse_index_offsets_len.argtypes = [pp]
+        L.nsa_build_inverse_index.argtypes = [pp] + [_P] * 4 + [_P, C.c_size_t, _P]
+        L.nsa_get_error.argtypes = [_P, _P, C.POINTER(C.c_int32)]
+        L.nsa_status_string.restype = C.c_char_p
+        L.nsa_status_string.argtypes = [C.c_int32]
+        L.nsa_count_pairs.argtypes = [pp] + [_P] * 3 + [_P]
+        for name in SYMBOLS:
+            fn = getattr(L, name)
+            if fn.restype is C.c_int:  # default restype: status enums
+                fn.restype = C.c_int32
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _check(status, where):
+    if status != NSA_OK:
+        raise NsaError(status, where)
+
+
+def problem(B, Hq, Hkv, T, D, block_size, S, dtype, layout=LAYOUT_BHTD, total_tokens=0,
+            scale=None) -> Problem:
+    return Problem(B, Hq, Hkv, T, D, block_size, S, DTYPE[dtype], layout, total_tokens,
+                   float(scale) if scale else 0.0)
+
+
+def problem_from(q, k, block_size, S, scale=None, cu_seqlens=None, max_seqlen=None) -> Problem:
+    if cu_seqlens is None:
+        B, Hq, T, D = q.shape
+        return problem(B, Hq, k.shape[1], T, D, block_size, S, q.dtype, scale=scale)
+    total, Hq, D = q.shape
+    B = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 1
+    return problem(B, Hq, k.shape[1], max(1, max_seqlen), D, block_size, S, q.dtype,
+                   layout=LAYOUT_THD, total_tokens=total, scale=scale)
+
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device, key="default") -> torch.Tensor:
+    """A cached device buffer of at least nbytes (256-byte aligned by torch)."""
+    ck = (key, str(device))
+    buf = _ws_cache.get(ck)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[ck] = buf
+    return buf
+
+
+def fwd_workspace_size(p: Problem) -> int:
+    return int(lib().nsa_fwd_workspace_size(C.byref(p)))
+
+
+def bwd_workspace_size(p: Problem) -> int:
+    return int(lib().nsa_bwd_workspace_size(C.byref(p)))
+
+
+def _lse_shape(q, cu_seqlens):
+    return q.shape[:-1]
+
+
+def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seqlen=None,
+            dense=False, ws=None, stream=None):
+    """Selection (or dense causal) forward through the C ABI: returns (o, lse)."""
+    S = 1 if dense else block_idx.shape[-1]
+    p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
+    o = torch.empty_like(q)
+    lse = torch.empty(_lse_shape(q, cu_seqlens), dtype=torch.float32, device=q.device)
+    n = fwd_workspace_size(p)
+    if n == 0:
+        raise NsaError(1, "nsa_fwd_workspace_size")
+    ws = workspace(n, q.device, "fwd") if ws is None else ws
+    L = lib()
+    st = _stream(stream)
+    if cu_seqlens is not None:
+        s = L.nsa_sel_varlen_fwd(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v),
+                                 _ptr(block_idx), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), st)
+    elif dense:
+        s = L.nsa_dense_causal_fwd(C.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                   _ptr(ws), ws.numel(), st)
+    else:
+        s = L.nsa_sel_fwd(C.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), _ptr(o),
+                          _ptr(lse), _ptr(ws), ws.numel(), st)
+    _check(s, "nsa fwd")
+    return o, lse
+
+
+def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=None,
+            max_seqlen=None, dense=False, ws=None, stream=None, out=None):
+    """Selection (or dense causal) backward through the C ABI: returns (dq, dk, dv)."""
+    S = 1 if dense else block_idx.shape[-1]
+    p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    n = bwd_workspace_size(p)
+    if n == 0:
+        raise NsaError(1, "nsa_bwd_workspace_size")
+    ws = workspace(n, q.device, "bwd") if ws is None else ws
+    L = lib()
+    st = _stream(stream)
+    if cu_seqlens is not None:
+        s = L.nsa_sel_varlen_bwd(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                 _ptr(dO), _ptr(lse), _ptr(block_idx), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(ws), ws.numel(), st)
+    elif dense:
+        s = L.nsa_dense_causal_bwd(C.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                   _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+                                   st)
+    else:
+        s = L.nsa_sel_bwd(C.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                          _ptr(block_idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), st)
+    _check(s, "nsa bwd")
+    return dq, dk, dv
+
+
+def do_dot(o, dO, cu_seqlens=None, stream=None):
+    p = problem_from(o, o, 16, 1, None, cu_seqlens)
+    delta = torch.empty(o.shape[:-1], dtype=torch.float32, device=o.device)
+    _check(lib().nsa_do_dot(C.byref(p), _ptr(cu_seqlens), _ptr(o), _ptr(dO), _ptr(delta),
+                            _stream(stream)), "nsa_do_dot")
+    return delta
+
+
+def build_inverse_index(block_idx, Hq, block_size, cu_seqlens=None, max_seqlen=None,
+                        stream=None):
+    """Returns (offsets, rows) device int32 tensors (rows trimmed on the host)."""
+    if cu_seqlens is None:
+        B, Hkv, T, S = block_idx.shape
+        p = problem(B, Hq, Hkv, T, 64, block_size, S, torch.bfloat16)
+        ntok = B * T
+    else:
+        total, Hkv, S = block_idx.shape
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+        p = problem(B, Hq, Hkv, max(1, max_seqlen), 64, block_size, S, torch.bfloat16,
+                    layout=LAYOUT_THD, total_tokens=total)
+        ntok = total
+    L = lib()
+    noff = int(L.nsa_inverse_index_offsets_len(C.byref(p)))
+    offsets = torch.empty(noff, dtype=torch.int32, device=block_idx.device)
+    rows = torch.empty(max(1, ntok * Hkv * S), dtype=torch.int32, device=block_idx.device)
+    ws = workspace(bwd_workspace_size(p), block_idx.device, "csr")
+    _check(L.nsa_build_inverse_index(C.byref(p), _ptr(cu_seqlens), _ptr(block_idx), _ptr(offsets),
+                                     _ptr(rows), _ptr(ws), ws.numel(), _stream(stream)),
+           "nsa_build_inverse_index")
+    return offsets, rows, ws
+
+
+def get_error(ws, stream=None) -> int:
+    out = C.c_int32(0)
+    _check(lib().nsa_get_error(_ptr(ws), _stream(stream), C.byref(out)), "nsa_get_error")
+    return int(out.value)
+
+
+def count_pairs(block_idx, Hq, block_size, cu_seqlens=None, max_seqlen=None, stream=None) -> int:
+    if cu_seqlens is None:
+        B, Hkv, T, S = block_idx.shape
+        p = problem(B, Hq, Hkv, T, 64, block_size, S, torch.bfloat16)
+    else:
+        total, Hkv, S = block_idx.shape
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+        p = problem(B, Hq, Hkv, max(1, max_seqlen), 64, block_size, S, torch.bfloat16,
+                    layout=LAYOUT_THD, total_tokens=total)
+    out = torch.zeros(1, dtype=torch.int64, device=block_idx.device)
+    _check(lib().nsa_count_pairs(C.byref(p), _ptr(cu_seqlens), _ptr(block_idx), _ptr(out),
+                                 _stream(stream)), "nsa_count_pairs")
+    return int(out.item())
+
+
+def default_scale(D):
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,424 @@
+// k_prep.cu -- the memory-bound steps around the attention kernels:
+//   * do_dot: delta_t = sum_d dO_td * O_td (the do_dot kernel of the backward
+//     chain on the cuDNN-frontend pull-request page);
+//   * index validation;
+//   * the block -> token inverse index (count, scan, ordered fill) that lets
+//     dK/dV accumulate per kv block without atomics on data;
+//   * the fixed-order reduction of split dK/dV blocks;
+//   * the (query row, key) pair count used for effective-FLOP reporting.
+#include "launch.h"
+
+namespace nsa {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+inline int grid_for(int64_t n, int per_block, int cap = 152 * 32)
+{
+    int64_t b = (n + per_block - 1) / per_block;
+    if (b < 1)
+        b = 1;
+    if (b > cap)
+        b = cap;
+    return (int)b;
+}
+
+// ---------------------------------------------------------------- do_dot
+// Rows are contiguous D-vectors in both layouts, and delta uses the row order
+// of o, so the kernel is a plain segmented dot product over rows.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) do_dot_kernel(const T *__restrict__ o,
+                                                          const T *__restrict__ dO,
+                                                          float *__restrict__ out, int64_t nrows,
+                                                          int D)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    const int tpr = D / VEC;  // threads per row (power of two, <= 32)
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / tpr, part = lane % tpr, rpw = 32 / tpr;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r0 = warp * rpw; r0 < nrows; r0 += nwarps * rpw) {
+        const int64_t r = r0 + sub;
+        float acc = 0.f;
+        if (r < nrows) {
+            uint4 a = __ldcs(reinterpret_cast<const uint4 *>(o + r * D + part * VEC));
+            uint4 b = __ldcs(reinterpret_cast<const uint4 *>(dO + r * D + part * VEC));
+            const T *ea = reinterpret_cast<const T *>(&a);
+            const T *eb = reinterpret_cast<const T *>(&b);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i)
+                acc = fmaf(to_f(ea[i]), to_f(eb[i]), acc);
+        }
+        for (int off = tpr >> 1; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (r < nrows && part == 0)
+            out[r] = acc;
+    }
+}
+
+// decode a linear index-row number into (b, kvh, t)
+__device__ __forceinline__ void decode_idx_row(const Geo &g, int64_t lin, int &b, int &kvh, int &t)
+{
+    if (g.thd) {
+        kvh = (int)(lin % g.Hkv);
+        int tok = (int)(lin / g.Hkv);
+        b = seq_of_token(g, tok);
+        t = tok - g.cu[b];
+    } else {
+        t = (int)(lin % g.T);
+        int64_t bk = lin / g.T;
+        kvh = (int)(bk % g.Hkv);
+        b = (int)(bk / g.Hkv);
+    }
+}
+
+// 0 = use, 1 = padding, 2 = invalid (reported), 3 = repeat (reported)
+__device__ __forceinline__ int classify(const int *row, int s, int t, int bs, int nbmax)
+{
+    const int j = row[s];
+    if (j == -1)
+        return 1;
+    if (j < -1 || j > t / bs || j >= nbmax)
+        return 2;
+    for (int s2 = 0; s2 < s; ++s2)
+        if (row[s2] == j)
+            return 3;
+    return 0;
+}
+
+__global__ void __launch_bounds__(kThreads) validate_kernel(Geo g, const int *__restrict__ idx,
+                                                            int *err)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
+         lin += (int64_t)gridDim.x * blockDim.x) {
+        int b, kvh, t;
+        decode_idx_row(g, lin, b, kvh, t);
+        const int *row = idx_row(g, idx, b, kvh, t);
+        for (int s = 0; s < g.S; ++s)
+            if (classify(row, s, t, g.bs, g.nbmax) >= 2)
+                set_error(err, NSA_ERR_BAD_INDEX);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) csr_count_kernel(Geo g, const int *__restrict__ idx,
+                                                             int *__restrict__ counts, int *err)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
+         lin += (int64_t)gridDim.x * blockDim.x) {
+        int b, kvh, t;
+        decode_idx_row(g, lin, b, kvh, t);
+        const int *row = idx_row(g, idx, b, kvh, t);
+        for (int s = 0; s < g.S; ++s) {
+            const int c = classify(row, s, t, g.bs, g.nbmax);
+            if (c == 0)
+                atomicAdd(&counts[((int64_t)b * g.Hkv + kvh) * g.nbmax + row[s]], 1);
+            else if (c >= 2)
+                set_error(err, NSA_ERR_BAD_INDEX);
+        }
+    }
+}
+
+// exclusive scan of one int per thread over a 1024-thread block
+__device__ __forceinline__ int block_scan_excl(int v, int &total, int *sm)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+    for (int off = 1; off < 32; off <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off)
+            x += y;
+    }
+    if (lane == 31)
+        sm[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = sm[lane];
+        int z = s;
+        for (int off = 1; off < 32; off <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, z, off);
+            if (lane >= off)
+                z += y;
+        }
+        sm[32 + lane] = z - s;  // exclusive prefix of warp totals
+        if (lane == 31)
+            sm[64] = z;
+    }
+    __syncthreads();
+    const int r = sm[32 + w] + x - v;
+    total = sm[64];
+    __syncthreads();
+    return r;
+}
+
+// One block of 1024 threads: offsets, the unit list (full-size chunks
+// first, then the shorter tails, so that a strided persistent schedule
+// starts with the longest work) and the per-block chunk/partial-slot table.
+__global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__restrict__ counts,
+                                                        int *__restrict__ offsets,
+                                                        Unit *__restrict__ units,
+                                                        int *__restrict__ blk_nchunk,
+                                                        int *__restrict__ blk_slot, WsHeader *hdr,
+                                                        int chunk)
+{
+    __shared__ int sm[80];
+    const int n = g.B * g.Hkv * g.nbmax;
+    // pass 1: totals of full chunks (to place the tails after them)
+    int full_total = 0;
+    for (int base = 0; base < n; base += 1024) {
+        const int i = base + threadIdx.x;
+        int cnt = 0;
+        if (i < n) {
+            if (g.dense) {
+                const int b = i / (g.Hkv * g.nbmax), j = i % g.nbmax;
+                const int L = seq_len(g, b);
+                cnt = j * g.bs < L ? L - j * g.bs : 0;
+            } else {
+                cnt = counts[i];
+            }
+        }
+        int tot;
+        block_scan_excl(cnt / chunk, tot, sm);
+        full_total += tot;
+    }
+    int c_off = 0, c_full = 0, c_tail = 0, c_slot = 0;
+    for (int base = 0; base < n; base += 1024) {
+        const int i = base + threadIdx.x;
+        int cnt = 0, b = 0, kvh = 0, j = 0;
+        if (i < n) {
+            j = i % g.nbmax;
+            kvh = (i / g.nbmax) % g.Hkv;
+            b = i / (g.Hkv * g.nbmax);
+            if (g.dense) {
+                const int L = seq_len(g, b);
+                cnt = j * g.bs < L ? L - j * g.bs : 0;
+            } else {
+                cnt = counts[i];
+            }
+        }
+        const int nfull = cnt / chunk, tail = (cnt % chunk) ? 1 : 0, nch = nfull + tail;
+        int t_off, t_full, t_tail, t_slot;
+        const int p_off = block_scan_excl(cnt, t_off, sm);
+        const int p_full = block_scan_excl(nfull, t_full, sm);
+        const int p_tail = block_scan_excl(tail, t_tail, sm);
+        const int p_slot = block_scan_excl(nch >= 2 ? nch : 0, t_slot, sm);
+        if (i < n) {
+            offsets[i] = c_off + p_off;
+            blk_nchunk[i] = nch;
+            const int slot0 = nch >= 2 ? c_slot + p_slot : -1;
+            blk_slot[i] = slot0;
+            const int bg = b * g.Hkv + kvh;
+            for (int c = 0; c < nfull; ++c) {
+                Unit u;
+                u.bg = bg;
+                u.j = j;
+                u.begin = c * chunk;
+                u.count = chunk;
+                u.slot = slot0 >= 0 ? slot0 + c : -1;
+                u.pad0 = u.pad1 = u.pad2 = 0;
+                units[c_full + p_full + c] = u;
+            }
+            if (tail) {
+                Unit u;
+                u.bg = bg;
+                u.j = j;
+                u.begin = nfull * chunk;
+                u.count = cnt - nfull * chunk;
+                u.slot = slot0 >= 0 ? slot0 + nfull : -1;
+                u.pad0 = u.pad1 = u.pad2 = 0;
+                units[full_total + c_tail + p_tail] = u;
+            }
+        }
+        c_off += t_off;
+        c_full += t_full;
+        c_tail += t_tail;
+        c_slot += t_slot;
+    }
+    if (threadIdx.x == 0) {
+        offsets[n] = c_off;
+        hdr->n_units = full_total + c_tail;
+    }
+}
+
+// One block per (b, kvh, j): walk the tokens that may select block j in
+// ascending order and append those that do.  Ascending order comes from the
+// block-wide ballot prefix, so the list is the same on every run.
+__global__ void __launch_bounds__(kThreads) csr_fill_kernel(Geo g, const int *__restrict__ idx,
+                                                            const int *__restrict__ offsets,
+                                                            int *__restrict__ rows)
+{
+    __shared__ int warp_tot[kThreads / 32];
+    __shared__ int carry;
+    const int i = blockIdx.x;
+    const int j = i % g.nbmax, kvh = (i / g.nbmax) % g.Hkv, b = i / (g.Hkv * g.nbmax);
+    const int begin = offsets[i], cnt = offsets[i + 1] - begin;
+    if (cnt == 0)
+        return;
+    const int L = seq_len(g, b);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0)
+        carry = 0;
+    __syncthreads();
+    for (int t0 = j * g.bs; t0 < L; t0 += kThreads) {
+        const int t = t0 + threadIdx.x;
+        const bool sel = t < L && row_selects(g, idx, b, kvh, t, j);
+        const unsigned m = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0)
+            warp_tot[w] = __popc(m);
+        __syncthreads();
+        int before = carry;
+        for (int x = 0; x < w; ++x)
+            before += warp_tot[x];
+        if (sel) {
+            const int pos = before + __popc(m & ((1u << lane) - 1u));
+            if (pos < cnt)
+                rows[begin + pos] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int s = 0;
+            for (int x = 0; x < kThreads / 32; ++x)
+                s += warp_tot[x];
+            carry += s;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int *__restrict__ nchunk,
+                                                               const int *__restrict__ slot,
+                                                               const float *__restrict__ partials,
+                                                               T *__restrict__ dk, T *__restrict__ dv)
+{
+    const int i = blockIdx.x;
+    const int nch = nchunk[i];
+    if (nch == 1)
+        return;  // written directly by the dK/dV kernel
+    const int j = i % g.nbmax, kvh = (i / g.nbmax) % g.Hkv, b = i / (g.Hkv * g.nbmax);
+    const int L = seq_len(g, b);
+    const int k0 = j * g.bs;
+    if (k0 >= L)
+        return;
+    const int nkeys = min(g.bs, L - k0);
+    const int64_t per = (int64_t)g.bs * g.D;
+    for (int e = threadIdx.x; e < nkeys * g.D; e += blockDim.x) {
+        const int kk = e / g.D, d = e % g.D;
+        float a = 0.f, c = 0.f;
+        if (nch >= 2) {
+            const float *p = partials + (int64_t)slot[i] * 2 * per;
+            for (int s = 0; s < nch; ++s) {  // fixed order: deterministic
+                a += p[(int64_t)s * 2 * per + kk * g.D + d];
+                c += p[(int64_t)s * 2 * per + per + kk * g.D + d];
+            }
+        }
+        const int64_t off = row_off(g, g.Hkv, b, kvh, k0 + kk) + d;
+        dk[off] = from_f<T>(a);
+        dv[off] = from_f<T>(c);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) count_pairs_kernel(Geo g, const int *__restrict__ idx,
+                                                               unsigned long long *out)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    unsigned long long local = 0;
+    for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
+         lin += (int64_t)gridDim.x * blockDim.x) {
+        int b, kvh, t;
+        decode_idx_row(g, lin, b, kvh, t);
+        const int *row = idx_row(g, idx, b, kvh, t);
+        for (int s = 0; s < g.S; ++s)
+            if (classify(row, s, t, g.bs, g.nbmax) == 0) {
+                const int j = row[s];
+                const int hi = min((j + 1) * g.bs - 1, t);
+                local += (unsigned long long)g.G * (hi - j * g.bs + 1);
+            }
+    }
+    for (int off = 16; off > 0; off >>= 1)
+        local += __shfl_xor_sync(0xffffffffu, local, off);
+    if ((threadIdx.x & 31) == 0 && local)
+        atomicAdd(out, local);
+}
+
+}  // namespace
+
+cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *delta, int dtype,
+                          cudaStream_t st)
+{
+    const int64_t nrows = (int64_t)g.ntok * g.Hq;
+    const int elems = dtype == NSA_DTYPE_BF16 ? 8 : 4;
+    const int rpw = 32 / (g.D / elems);
+    const int grid = grid_for(nrows, (kThreads / 32) * rpw);
+    if (dtype == NSA_DTYPE_BF16)
+        do_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+            (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta, nrows, g.D);
+    else
+        do_dot_kernel<float><<<grid, kThreads, 0, st>>>((const float *)o, (const float *)dO, delta,
+                                                        nrows, g.D);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_validate_index(const Geo &g, const int *idx, int *err, cudaStream_t st)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    validate_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr_count(const Geo &g, const int *idx, int *counts, int *err, cudaStream_t st)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    csr_count_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx, counts, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit *units,
+                            int *blk_nchunk, int *blk_slot, WsHeader *hdr, int chunk,
+                            cudaStream_t st)
+{
+    csr_scan_kernel<<<1, 1024, 0, st>>>(g, counts, offsets, units, blk_nchunk, blk_slot, hdr, chunk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, int *rows,
+                            cudaStream_t st)
+{
+    const int n = g.B * g.Hkv * g.nbmax;
+    if (n == 0)
+        return cudaSuccess;
+    csr_fill_kernel<<<n, kThreads, 0, st>>>(g, idx, offsets, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *blk_slot,
+                               const float *partials, void *dk, void *dv, int dtype,
+                               cudaStream_t st)
+{
+    const int n = g.B * g.Hkv * g.nbmax;
+    if (n == 0)
+        return cudaSuccess;
+    if (dtype == NSA_DTYPE_BF16)
+        dkdv_reduce_kernel<__nv_bfloat16><<<n, kThreads, 0, st>>>(
+            g, blk_nchunk, blk_slot, partials, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv);
+    else
+        dkdv_reduce_kernel<float><<<n, kThreads, 0, st>>>(g, blk_nchunk, blk_slot, partials,
+                                                          (float *)dk, (float *)dv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cudaStream_t st)
+{
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(long long), st);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    count_pairs_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx,
+                                                                   (unsigned long long *)out);
+    return cudaGetLastError();
+}
+
+}  // namespace nsa

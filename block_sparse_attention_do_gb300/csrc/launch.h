@@ -1,0 +1,53 @@
+// launch.h -- host-side launchers of the kernels, called by nsa_api.cu.
+// Every launcher enqueues on `st` and returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "nsa_common.cuh"
+
+namespace nsa {
+
+// ---- prep (k_prep.cu) ----------------------------------------------------
+cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *delta, int dtype,
+                          cudaStream_t st);
+cudaError_t launch_validate_index(const Geo &g, const int *idx, int *err, cudaStream_t st);
+// counts[B*Hkv*nbmax] must be zeroed by the caller
+cudaError_t launch_csr_count(const Geo &g, const int *idx, int *counts, int *err, cudaStream_t st);
+// offsets (B*Hkv*nbmax + 1), units, per-block chunk table; chunk = tokens per unit
+cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit *units,
+                            int *blk_nchunk, int *blk_slot, WsHeader *hdr, int chunk,
+                            cudaStream_t st);
+cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, int *rows,
+                            cudaStream_t st);
+// sums the fp32 partials of split blocks into dk/dv and zeroes unselected blocks
+cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *blk_slot,
+                               const float *partials, void *dk, void *dv, int dtype,
+                               cudaStream_t st);
+cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cudaStream_t st);
+
+// ---- SIMT kernels (k_simt.cu): any supported shape, fp32 or bf16 ----------
+cudaError_t launch_fwd_simt(const Geo &g, const void *q, const void *k, const void *v,
+                            const int *idx, void *o, float *lse, int dtype, cudaStream_t st);
+cudaError_t launch_dq_simt(const Geo &g, const void *q, const void *k, const void *v,
+                           const void *dO, const float *lse, const float *delta, const int *idx,
+                           void *dq, int dtype, cudaStream_t st);
+cudaError_t launch_dkdv_simt(const Geo &g, const void *q, const void *k, const void *v,
+                             const void *dO, const float *lse, const float *delta,
+                             const int *offsets, const int *rows, void *dk, void *dv, int dtype,
+                             cudaStream_t st);
+
+// ---- tensor-core kernels (bf16, D = 128, block_size = 64) -----------------
+bool tc_supported(const Geo &g, int dtype);
+cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v,
+                          const int *idx, void *o, float *lse, int *err, cudaStream_t st);
+cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,
+                         const void *dO, const float *lse, const float *delta, const int *idx,
+                         void *dq, int *err, cudaStream_t st);
+cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const void *v,
+                           const void *dO, const float *lse, const float *delta,
+                           const int *offsets, const int *rows, const Unit *units,
+                           const WsHeader *hdr, int max_units, float *partials, void *dk, void *dv,
+                           int *err, cudaStream_t st);
+
+}  // namespace nsa

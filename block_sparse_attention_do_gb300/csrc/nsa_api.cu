@@ -1,0 +1,398 @@
+// nsa_api.cu -- the C ABI of libnsa.so (include/nsa.h): argument checks,
+// workspace carving and the launch sequence of each entry point.  No entry
+// point allocates memory or synchronises; all work goes on the caller's
+// stream.
+#include <math.h>
+#include <string.h>
+
+#include "launch.h"
+
+using namespace nsa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+enum Mode { SPARSE = 0, DENSE = 1 };
+
+// Checks the problem and fills the device geometry.  `want_thd` is the
+// layout the entry point requires.
+nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g)
+{
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->T < 1)
+        return NSA_ERR_INVALID_ARG;
+    if (p->Hq % p->Hkv != 0)
+        return NSA_ERR_INVALID_ARG;
+    if (p->dtype != NSA_DTYPE_F32 && p->dtype != NSA_DTYPE_BF16)
+        return NSA_ERR_INVALID_ARG;
+    if (p->layout != (want_thd ? NSA_LAYOUT_THD : NSA_LAYOUT_BHTD))
+        return NSA_ERR_INVALID_ARG;
+    if (mode == SPARSE && p->S < 1)
+        return NSA_ERR_INVALID_ARG;
+    if (p->D != 32 && p->D != 64 && p->D != 128)
+        return NSA_ERR_UNSUPPORTED;
+    if (p->block_size != 16 && p->block_size != 32 && p->block_size != 64)
+        return NSA_ERR_UNSUPPORTED;
+    if (mode == SPARSE && p->S > 256)
+        return NSA_ERR_UNSUPPORTED;
+    if (want_thd) {
+        if (!cu || p->total_tokens < 0)
+            return NSA_ERR_INVALID_ARG;
+    }
+    const int64_t ntok = want_thd ? (int64_t)p->total_tokens : (int64_t)p->B * p->T;
+    if (ntok * p->Hq * (int64_t)p->D >= ((int64_t)1 << 40))
+        return NSA_ERR_UNSUPPORTED;
+    memset(&g, 0, sizeof(g));
+    g.B = p->B;
+    g.Hq = p->Hq;
+    g.Hkv = p->Hkv;
+    g.G = p->Hq / p->Hkv;
+    g.T = p->T;
+    g.D = p->D;
+    g.bs = p->block_size;
+    g.nbmax = (p->T + p->block_size - 1) / p->block_size;
+    g.S = mode == DENSE ? g.nbmax : p->S;
+    g.ntok = (int)ntok;
+    g.thd = want_thd ? 1 : 0;
+    g.dense = mode == DENSE ? 1 : 0;
+    g.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->D);
+    g.scale_l2 = g.scale * 1.4426950408889634f;
+    g.cu = cu;
+    return NSA_OK;
+}
+
+// Backward workspace carving.
+struct BwdWs {
+    size_t delta, counts, offsets, units, nchunk, slot, partials, total;
+    int chunk, max_units;
+};
+
+int tiles_tokens(const Geo &g) { return g.G >= 128 ? 1 : 128 / g.G; }
+
+BwdWs bwd_layout(const Geo &g, int dtype)
+{
+    BwdWs w;
+    const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
+    const bool tc = tc_supported(g, dtype);
+    // tokens per dK/dV unit: 64 row tiles of the tensor-core kernel
+    w.chunk = tiles_tokens(g) * 64;
+    const int64_t sel_total = (int64_t)g.ntok * g.Hkv * g.S;  // upper bound on list entries
+    w.max_units = (int)(nbgj + (sel_total + w.chunk - 1) / w.chunk);
+    size_t off = kAlign;  // header
+    w.delta = off;
+    off = align_up(off + sizeof(float) * (size_t)g.ntok * g.Hq);
+    w.counts = off;
+    off = align_up(off + sizeof(int) * (size_t)nbgj);
+    w.offsets = off;
+    off = align_up(off + sizeof(int) * (size_t)(nbgj + 1));
+    w.units = off;
+    off = align_up(off + sizeof(Unit) * (size_t)w.max_units);
+    w.nchunk = off;
+    off = align_up(off + sizeof(int) * (size_t)nbgj);
+    w.slot = off;
+    off = align_up(off + sizeof(int) * (size_t)nbgj);
+    w.partials = off;
+    if (tc)
+        off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.max_units);
+    // token lists of the inverse index (sparse only; dense lists are implicit)
+    w.total = off;
+    return w;
+}
+
+size_t bwd_rows_bytes(const Geo &g)
+{
+    return g.dense ? 0 : align_up(sizeof(int) * (size_t)g.ntok * g.Hkv * g.S);
+}
+
+inline nsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NSA_OK : NSA_ERR_CUDA; }
+
+#define NSA_TRY(expr)                                  \
+    do {                                               \
+        cudaError_t _e = (expr);                       \
+        if (_e != cudaSuccess)                         \
+            return NSA_ERR_CUDA;                       \
+    } while (0)
+
+nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws || ((uintptr_t)ws & (kAlign - 1)) || ws_bytes < need)
+        return NSA_ERR_WORKSPACE;
+    return NSA_OK;
+}
+
+nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
+                   const void *k, const void *v, const int32_t *idx, void *o, float *lse,
+                   void *ws, size_t ws_bytes, void *stream)
+{
+    Geo g;
+    nsa_status s = make_geo(p, thd, mode, cu, g);
+    if (s != NSA_OK)
+        return s;
+    if (!q || !k || !v || !o || !lse || (mode == SPARSE && !idx))
+        return NSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return NSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, nsa_fwd_workspace_size(p))) != NSA_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    WsHeader *hdr = (WsHeader *)ws;
+    NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+    if (g.ntok == 0)
+        return NSA_OK;
+    if (mode == SPARSE)
+        NSA_TRY(launch_validate_index(g, idx, &hdr->err, st));
+    if (tc_supported(g, p->dtype))
+        NSA_TRY(launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, st));
+    else
+        NSA_TRY(launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
+    return NSA_OK;
+}
+
+// the inverse index into (offsets, rows); counts is scratch of nbgj ints
+nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
+                     Unit *units, int *nchunk, int *slot, WsHeader *hdr, int chunk, cudaStream_t st)
+{
+    const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
+    if (!g.dense) {
+        NSA_TRY(cudaMemsetAsync(counts, 0, sizeof(int) * nbgj, st));
+        NSA_TRY(launch_csr_count(g, idx, counts, &hdr->err, st));
+    }
+    NSA_TRY(launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
+    if (!g.dense)
+        NSA_TRY(launch_csr_fill(g, idx, offsets, rows, st));
+    return NSA_OK;
+}
+
+nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
+                   const void *k, const void *v, const void *o, const void *dO, const float *lse,
+                   const int32_t *idx, void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                   void *stream)
+{
+    Geo g;
+    nsa_status s = make_geo(p, thd, mode, cu, g);
+    if (s != NSA_OK)
+        return s;
+    if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || (mode == SPARSE && !idx))
+        return NSA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+    for (const void *x : ptrs)
+        if (!aligned16(x))
+            return NSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, nsa_bwd_workspace_size(p))) != NSA_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *w8 = (char *)ws;
+    WsHeader *hdr = (WsHeader *)ws;
+    const BwdWs L = bwd_layout(g, p->dtype);
+    float *delta = (float *)(w8 + L.delta);
+    int *counts = (int *)(w8 + L.counts);
+    int *offsets = (int *)(w8 + L.offsets);
+    Unit *units = (Unit *)(w8 + L.units);
+    int *nchunk = (int *)(w8 + L.nchunk);
+    int *slot = (int *)(w8 + L.slot);
+    float *partials = (float *)(w8 + L.partials);
+    int *rows = (int *)(w8 + L.total);
+    NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+    if (g.ntok == 0)
+        return NSA_OK;
+    NSA_TRY(launch_do_dot(g, o, dO, delta, p->dtype, st));
+    if ((s = build_csr(g, idx, counts, offsets, rows, units, nchunk, slot, hdr, L.chunk, st)) != NSA_OK)
+        return s;
+    if (tc_supported(g, p->dtype)) {
+        NSA_TRY(launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, hdr, L.max_units,
+                               partials, dk, dv, &hdr->err, st));
+        NSA_TRY(launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
+        NSA_TRY(launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, st));
+    } else {
+        NSA_TRY(launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
+        NSA_TRY(launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));
+    }
+    return NSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nsa_fwd_workspace_size(const nsa_problem *p)
+{
+    Geo g;
+    if (!p)
+        return 0;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    // dense and sparse forwards share the layout: the header only
+    if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK &&
+        make_geo(p, thd, DENSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
+        return 0;
+    return kAlign;
+}
+
+size_t nsa_bwd_workspace_size(const nsa_problem *p)
+{
+    Geo g;
+    if (!p)
+        return 0;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    const int32_t *fake_cu = thd ? (const int32_t *)16 : nullptr;
+    if (make_geo(p, thd, SPARSE, fake_cu, g) == NSA_OK) {
+        // the dense entry uses S = nbmax; size for the larger of the two
+        Geo gd;
+        make_geo(p, thd, DENSE, fake_cu, gd);
+        const BwdWs a = bwd_layout(g, p->dtype), b = bwd_layout(gd, p->dtype);
+        const size_t sa = a.total + bwd_rows_bytes(g), sb = b.total + bwd_rows_bytes(gd);
+        return sa > sb ? sa : sb;
+    }
+    if (make_geo(p, thd, DENSE, fake_cu, g) == NSA_OK)
+        return bwd_layout(g, p->dtype).total;
+    return 0;
+}
+
+nsa_status nsa_sel_fwd(const nsa_problem *p, const void *q, const void *k, const void *v,
+                       const int32_t *block_idx, void *o, float *lse, void *ws, size_t ws_bytes,
+                       void *stream)
+{
+    return run_fwd(p, false, SPARSE, nullptr, q, k, v, block_idx, o, lse, ws, ws_bytes, stream);
+}
+
+nsa_status nsa_sel_bwd(const nsa_problem *p, const void *q, const void *k, const void *v,
+                       const void *o, const void *dO, const float *lse, const int32_t *block_idx,
+                       void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream)
+{
+    return run_bwd(p, false, SPARSE, nullptr, q, k, v, o, dO, lse, block_idx, dq, dk, dv, ws,
+                   ws_bytes, stream);
+}
+
+nsa_status nsa_dense_causal_fwd(const nsa_problem *p, const void *q, const void *k,
+                                const void *v, void *o, float *lse, void *ws, size_t ws_bytes,
+                                void *stream)
+{
+    return run_fwd(p, false, DENSE, nullptr, q, k, v, nullptr, o, lse, ws, ws_bytes, stream);
+}
+
+nsa_status nsa_dense_causal_bwd(const nsa_problem *p, const void *q, const void *k,
+                                const void *v, const void *o, const void *dO, const float *lse,
+                                void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                                void *stream)
+{
+    return run_bwd(p, false, DENSE, nullptr, q, k, v, o, dO, lse, nullptr, dq, dk, dv, ws,
+                   ws_bytes, stream);
+}
+
+nsa_status nsa_sel_varlen_fwd(const nsa_problem *p, const int32_t *cu_seqlens, const void *q,
+                              const void *k, const void *v, const int32_t *block_idx, void *o,
+                              float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    return run_fwd(p, true, SPARSE, cu_seqlens, q, k, v, block_idx, o, lse, ws, ws_bytes, stream);
+}
+
+nsa_status nsa_sel_varlen_bwd(const nsa_problem *p, const int32_t *cu_seqlens, const void *q,
+                              const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, const int32_t *block_idx, void *dq, void *dk,
+                              void *dv, void *ws, size_t ws_bytes, void *stream)
+{
+    return run_bwd(p, true, SPARSE, cu_seqlens, q, k, v, o, dO, lse, block_idx, dq, dk, dv, ws,
+                   ws_bytes, stream);
+}
+
+nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,
+                      const void *dO, float *delta, void *stream)
+{
+    Geo g;
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    nsa_status s = make_geo(p, thd, DENSE, cu_seqlens, g);
+    if (s != NSA_OK)
+        return s;
+    if (!o || !dO || !delta || !aligned16(o) || !aligned16(dO))
+        return NSA_ERR_INVALID_ARG;
+    if (g.ntok == 0)
+        return NSA_OK;
+    return cuda_status(launch_do_dot(g, o, dO, delta, p->dtype, (cudaStream_t)stream));
+}
+
+int64_t nsa_inverse_index_offsets_len(const nsa_problem *p)
+{
+    if (!p || p->block_size < 1 || p->T < 1)
+        return 0;
+    return (int64_t)p->B * p->Hkv * ((p->T + p->block_size - 1) / p->block_size) + 1;
+}
+
+nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqlens,
+                                   const int32_t *block_idx, int32_t *offsets, int32_t *rows,
+                                   void *ws, size_t ws_bytes, void *stream)
+{
+    Geo g;
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    nsa_status s = make_geo(p, thd, SPARSE, cu_seqlens, g);
+    if (s != NSA_OK)
+        return s;
+    if (!block_idx || !offsets || !rows)
+        return NSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, nsa_bwd_workspace_size(p))) != NSA_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *w8 = (char *)ws;
+    WsHeader *hdr = (WsHeader *)ws;
+    const BwdWs L = bwd_layout(g, p->dtype);
+    NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+    return build_csr(g, block_idx, (int *)(w8 + L.counts), offsets, rows, (Unit *)(w8 + L.units),
+                     (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, L.chunk, st);
+}
+
+nsa_status nsa_get_error(void *ws, void *stream, int32_t *out)
+{
+    if (!ws || !out)
+        return NSA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    *out = v;
+    return NSA_OK;
+}
+
+const char *nsa_status_string(int32_t s)
+{
+    switch (s) {
+    case NSA_OK: return "NSA_OK";
+    case NSA_ERR_INVALID_ARG: return "NSA_ERR_INVALID_ARG";
+    case NSA_ERR_UNSUPPORTED: return "NSA_ERR_UNSUPPORTED";
+    case NSA_ERR_BAD_INDEX: return "NSA_ERR_BAD_INDEX";
+    case NSA_ERR_DEVICE_TIMEOUT: return "NSA_ERR_DEVICE_TIMEOUT";
+    case NSA_ERR_CUDA: return "NSA_ERR_CUDA";
+    case NSA_ERR_WORKSPACE: return "NSA_ERR_WORKSPACE";
+    default: return "NSA_ERR_UNKNOWN";
+    }
+}
+
+nsa_status nsa_count_pairs(const nsa_problem *p, const int32_t *cu_seqlens,
+                           const int32_t *block_idx, int64_t *out_pairs, void *stream)
+{
+    Geo g;
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    nsa_status s = make_geo(p, thd, SPARSE, cu_seqlens, g);
+    if (s != NSA_OK)
+        return s;
+    if (!block_idx || !out_pairs)
+        return NSA_ERR_INVALID_ARG;
+    return cuda_status(launch_count_pairs(g, block_idx, (long long *)out_pairs, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// nsa_common.cuh -- problem geometry, addressing and the device error word,
+// shared by every kernel of libnsa.
+//
+// Addressing follows the two layouts of the C ABI (include/nsa.h): BHTD
+// (fixed length) and THD (packed variable length with cu_seqlens).  A query
+// or key row is named by (sequence b, head h, sequence-local token t).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nsa.h"
+
+namespace nsa {
+
+// Device-side view of an nsa_problem plus derived quantities.
+struct Geo {
+    int B, Hq, Hkv, G, T, D, bs, S;
+    int nbmax;       // ceil(T / bs): blocks of the longest sequence
+    int ntok;        // B*T (BHTD) or total_tokens (THD)
+    int thd;         // 1 for the packed layout
+    int dense;       // 1: every row selects blocks 0..t/bs (no index read)
+    float scale;     // softmax scale
+    float scale_l2;  // scale * log2(e)
+    const int *cu;   // cu_seqlens (THD) or nullptr
+};
+
+__device__ __forceinline__ int seq_len(const Geo &g, int b) { return g.thd ? g.cu[b + 1] - g.cu[b] : g.T; }
+
+// element offset of the D-vector of (b, head, t) in a tensor with H heads
+__device__ __forceinline__ int64_t row_off(const Geo &g, int H, int b, int h, int t)
+{
+    if (g.thd)
+        return ((int64_t)(g.cu[b] + t) * H + h) * g.D;
+    return (((int64_t)b * H + h) * g.T + t) * g.D;
+}
+
+// offset of a per-row scalar (lse, delta) of (b, query head h, t)
+__device__ __forceinline__ int64_t stat_off(const Geo &g, int b, int h, int t)
+{
+    if (g.thd)
+        return (int64_t)(g.cu[b] + t) * g.Hq + h;
+    return ((int64_t)b * g.Hq + h) * g.T + t;
+}
+
+__device__ __forceinline__ const int *idx_row(const Geo &g, const int *idx, int b, int kvh, int t)
+{
+    if (g.thd)
+        return idx + ((int64_t)(g.cu[b] + t) * g.Hkv + kvh) * g.S;
+    return idx + (((int64_t)b * g.Hkv + kvh) * g.T + t) * g.S;
+}
+
+// sequence holding packed token `tok` (THD); binary search over cu_seqlens
+__device__ __forceinline__ int seq_of_token(const Geo &g, int tok)
+{
+    int lo = 0, hi = g.B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (g.cu[mid] <= tok)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// does row (b, kvh, t) select block j?  (dense: every block up to t/bs)
+__device__ __forceinline__ bool row_selects(const Geo &g, const int *idx, int b, int kvh, int t, int j)
+{
+    if (g.dense)
+        return j <= t / g.bs;
+    const int *r = idx_row(g, idx, b, kvh, t);
+    for (int s = 0; s < g.S; ++s)
+        if (r[s] == j)
+            return true;
+    return false;
+}
+
+// The first error recorded wins; later ones are dropped.
+__device__ __forceinline__ void set_error(int *err, int code)
+{
+    if (err)
+        atomicCAS(err, 0, code);
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// A dK/dV work unit: rows [begin, begin + count) of the token list of
+// (bg = b*Hkv + kvh, block j); slot >= 0 names the fp32 partial buffer the
+// unit writes when the block is split into several units, -1 = write the
+// final dK/dV directly.
+struct Unit {
+    int bg, j, begin, count, slot, pad0, pad1, pad2;
+};
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    int err;      // nsa_status recorded by the device
+    int n_units;  // number of dK/dV units built for the current call
+    int pad[62];
+};
+
+}  // namespace nsa

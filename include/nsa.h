@@ -1,0 +1,191 @@
+/*
+ * nsa.h -- C ABI of libnsa.so: Native-Sparse-Attention block-selection
+ * attention (forward producing O and LSE, backward producing dQ, dK, dV)
+ * under grouped-query attention, on one NVIDIA GB300 (sm_103a).
+ *
+ * Where the operation is defined.  The gradcheck-gate page
+ * ("test_kernel_backward.py", functions run_one and main) fixes the
+ * operation: q [B,Hq,T,D], k and v [B,Hkv,T,D], a per-token block index
+ * idx = make_block_idx(B, Hkv, T, block_size, S), o = selection forward of
+ * (q, k, v, idx, block_size), and dQ, dK, dV = the gradient of <dO, o>.
+ * The cuDNN-frontend pull-request page ("port the SM80 backward onto
+ * SdpaBwdDsl ...", its description and the review of the THD path) supplies
+ * the dense causal backward, the packed THD variable-length form
+ * (cum_seqlen tensors), the do_dot pre-pass, caller-owned workspace with no
+ * per-call allocation, and respecting the caller's stream.
+ *
+ * Definitions (G = Hq/Hkv; query head h reads kv head h/G; every index row
+ * is shared by the G query heads of its kv head):
+ *   sel(t)   = { idx[b,g,t,s] : s < S, idx != -1 }
+ *   key k is attended by row t  iff  k <= t  and  k/block_size in sel(t)
+ *   P_tk     = exp(scale*q_t.k_k - LSE_t),  LSE_t = log sum_k exp(scale*q_t.k_k)
+ *   O_t      = sum_k P_tk v_k
+ *   dS_tk    = P_tk (dO_t.v_k - dO_t.O_t)
+ *   dQ_t     = scale sum_k dS_tk k_k
+ *   dK_k     = scale sum_{h in group, t} dS_tk q_t,   dV_k = sum_{h, t} P_tk dO_t
+ * LSE is the natural-log sum.  A row with no attended key gets O = 0,
+ * LSE = -inf and contributes no gradient.
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, dense in
+ *    the layout named by nsa_problem.layout, 16-byte aligned.  The library
+ *    never allocates or frees memory and never synchronises: work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Shape, dtype and layout errors are returned synchronously before any
+ *    launch.  Errors found on the device (a bad index entry, a wait that
+ *    timed out) are recorded in the workspace and read back with
+ *    nsa_get_error.  After any error the outputs are unspecified.
+ *  - `ws` is a caller-provided device workspace of at least the size the
+ *    matching *_workspace_size function returns (256-byte aligned).  Its
+ *    contents on entry do not matter; it must not be shared by calls that
+ *    can run at the same time.
+ *  - dtype NSA_DTYPE_BF16: q,k,v,o,dO,dq,dk,dv are bfloat16; NSA_DTYPE_F32:
+ *    they are float.  lse is always float; idx and cu_seqlens are int32.
+ *    Accumulation is fp32 in both cases; results are rounded once.
+ */
+#ifndef NSA_H
+#define NSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nsa_status {
+    NSA_OK = 0,
+    NSA_ERR_INVALID_ARG = 1,    /* null pointer, bad shape, misaligned pointer */
+    NSA_ERR_UNSUPPORTED = 2,    /* valid problem this build does not handle */
+    NSA_ERR_BAD_INDEX = 3,      /* (device) index entry < -1, in the future, or repeated in a row */
+    NSA_ERR_DEVICE_TIMEOUT = 4, /* (device) a bounded wait inside a kernel gave up */
+    NSA_ERR_CUDA = 5,           /* a CUDA runtime call failed (launch, tensor map) */
+    NSA_ERR_WORKSPACE = 6       /* ws is NULL, too small or misaligned */
+} nsa_status;
+
+enum { NSA_DTYPE_F32 = 0, NSA_DTYPE_BF16 = 1 };
+
+/*
+ * Layouts.  BHTD: q,o,dO,dq [B,Hq,T,D]; k,v,dk,dv [B,Hkv,T,D];
+ * idx [B,Hkv,T,S]; lse [B,Hq,T].
+ * THD (packed variable length, only through the *_varlen_* entry points):
+ * q,o,dO,dq [total,Hq,D]; k,v,dk,dv [total,Hkv,D]; idx [total,Hkv,S] with
+ * sequence-local block ids; lse [total,Hq]; cu_seqlens [B+1] int32 with
+ * cu_seqlens[0] = 0 and cu_seqlens[B] = total.  Causality and block
+ * numbering restart at every sequence (query and key lengths are equal).
+ */
+enum { NSA_LAYOUT_BHTD = 0, NSA_LAYOUT_THD = 1 };
+
+typedef struct nsa_problem {
+    int32_t B;            /* batch size (BHTD) or number of sequences (THD) */
+    int32_t Hq;           /* query heads */
+    int32_t Hkv;          /* key/value heads; Hq % Hkv == 0 */
+    int32_t T;            /* BHTD: sequence length; THD: upper bound on every sequence length */
+    int32_t D;            /* head dimension: 32, 64 or 128 */
+    int32_t block_size;   /* keys per selectable block: 16, 32 or 64 */
+    int32_t S;            /* slots per index row (ignored by the dense entry points) */
+    int32_t dtype;        /* NSA_DTYPE_* */
+    int32_t layout;       /* NSA_LAYOUT_*; the varlen entry points require THD, the others BHTD */
+    int32_t total_tokens; /* THD: cu_seqlens[B]; ignored for BHTD */
+    float scale;          /* softmax scale; <= 0 selects 1/sqrt(D) */
+} nsa_problem;
+
+/* Workspace bytes needed by the forward / backward entry points (0 on an invalid problem). */
+size_t nsa_fwd_workspace_size(const nsa_problem *p);
+size_t nsa_bwd_workspace_size(const nsa_problem *p);
+
+/*
+ * Selection forward (gradcheck-gate page: the selection forward called in
+ * run_one with (q, k, v, idx, block_size)).  Writes o (layout of q) and
+ * lse.  idx rows may hold -1 anywhere; entries are validated on the device.
+ */
+nsa_status nsa_sel_fwd(const nsa_problem *p, const void *q, const void *k, const void *v,
+                       const int32_t *block_idx, void *o, float *lse, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/*
+ * Selection backward (gradcheck-gate page: o.backward(dO) through the
+ * selection forward; cuDNN-frontend page: the backward chain do_dot ->
+ * main -> dQ -> GQA reduction).  Inputs are the forward's inputs plus its
+ * o and lse and the upstream gradient dO; writes dq, dk, dv (layouts of q
+ * and k).  Runs: D_t = rowsum(dO*O); the block -> token inverse index;
+ * dK/dV per (kv block, kv head) summed over the G query heads in-kernel with
+ * a fixed summation order (deterministic, no atomics on data); dQ per query
+ * tile.  Every output element is written exactly once.
+ */
+nsa_status nsa_sel_bwd(const nsa_problem *p, const void *q, const void *k, const void *v,
+                       const void *o, const void *dO, const float *lse, const int32_t *block_idx,
+                       void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Dense causal attention (cuDNN-frontend page: the SDPA backward with
+ * is_causal) as the special case where every row selects all of its blocks
+ * 0..t/block_size.  Same arguments as the selection calls without an index;
+ * p->S is ignored.
+ */
+nsa_status nsa_dense_causal_fwd(const nsa_problem *p, const void *q, const void *k,
+                                const void *v, void *o, float *lse, void *ws, size_t ws_bytes,
+                                void *stream);
+nsa_status nsa_dense_causal_bwd(const nsa_problem *p, const void *q, const void *k,
+                                const void *v, const void *o, const void *dO, const float *lse,
+                                void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/*
+ * Packed variable-length selection attention (cuDNN-frontend page: the THD
+ * path with cum_seqlen_q / cum_seqlen_k; here both are the same array).
+ * p->layout must be NSA_LAYOUT_THD, p->B the number of sequences, p->T an
+ * upper bound on every sequence length and p->total_tokens = cu_seqlens[B].
+ */
+nsa_status nsa_sel_varlen_fwd(const nsa_problem *p, const int32_t *cu_seqlens, const void *q,
+                              const void *k, const void *v, const int32_t *block_idx, void *o,
+                              float *lse, void *ws, size_t ws_bytes, void *stream);
+nsa_status nsa_sel_varlen_bwd(const nsa_problem *p, const int32_t *cu_seqlens, const void *q,
+                              const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, const int32_t *block_idx, void *dq, void *dk,
+                              void *dv, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * do_dot pre-pass (cuDNN-frontend page: the do_dot kernel of the backward
+ * chain): delta_t = sum_d dO_td * O_td for every query row, in fp32, layout
+ * of lse.  cu_seqlens is NULL for BHTD.
+ */
+nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,
+                      const void *dO, float *delta, void *stream);
+
+/*
+ * Inverse index (block -> selecting tokens), the step the backward uses so
+ * that dK/dV accumulate without atomics.  Canonical form: offsets has
+ * nsa_inverse_index_offsets_len(p) entries, an exclusive scan over
+ * (b, g, j) in lexicographic order with j < ceil(T / block_size); the list
+ * of (b, g, j) holds every sequence-local token t whose row selects block j,
+ * ascending.  rows must have room for (tokens * Hkv * S) entries, where
+ * tokens is B*T (BHTD) or total_tokens (THD).  ws is a backward workspace.
+ * Bad entries are skipped and reported through nsa_get_error.
+ */
+int64_t nsa_inverse_index_offsets_len(const nsa_problem *p);
+nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqlens,
+                                   const int32_t *block_idx, int32_t *offsets, int32_t *rows,
+                                   void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Reads the device error word of a workspace used by the calls above,
+ * after synchronising `stream`, into *out (an nsa_status value), and clears
+ * it.  Returns NSA_ERR_CUDA if the read itself fails.
+ */
+nsa_status nsa_get_error(void *ws, void *stream, int32_t *out);
+
+/* Static string naming a status. */
+const char *nsa_status_string(int32_t status);
+
+/* Number of (query row, attended key) pairs summed over query heads; the
+ * unit of the effective-FLOP count (10*D per pair for the backward).
+ * Computed on the device into *out_pairs (device int64), on `stream`. */
+nsa_status nsa_count_pairs(const nsa_problem *p, const int32_t *cu_seqlens,
+                           const int32_t *block_idx, int64_t *out_pairs, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NSA_H */

@@ -1,0 +1,82 @@
+"""The C ABI library loads on a machine without a GPU and exports every
+function include/nsa.h declares; host-side argument checks return the
+documented statuses without touching a device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_do_gb300 import api, build
+
+    build.build()
+    return api.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "nsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from block_sparse_attention_do_gb300 import api
+
+    declared = _declared()
+    assert len(declared) >= 14
+    assert sorted(api.SYMBOLS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.nsa_status_string(0) == b"NSA_OK"
+    assert lib.nsa_status_string(3) == b"NSA_ERR_BAD_INDEX"
+    assert lib.nsa_status_string(99) == b"NSA_ERR_UNKNOWN"
+
+
+def _p(**kw):
+    import torch
+
+    from block_sparse_attention_do_gb300 import api
+
+    base = dict(B=1, Hq=4, Hkv=2, T=256, D=128, block_size=64, S=4, dtype=torch.bfloat16)
+    base.update(kw)
+    return api.problem(**base)
+
+
+def test_workspace_sizes_and_validation(lib):
+    from block_sparse_attention_do_gb300 import api
+
+    p = _p()
+    assert api.fwd_workspace_size(p) >= 256
+    assert api.bwd_workspace_size(p) > 256 + 4 * 256 * 4
+    assert api.bwd_workspace_size(_p(Hq=3)) == 0          # Hq % Hkv != 0
+    assert api.bwd_workspace_size(_p(D=96)) == 0          # unsupported head dim
+    assert api.bwd_workspace_size(_p(block_size=48)) == 0
+    # a call with null tensors fails before any launch
+    ws = C.c_void_p(256)
+    s = lib.nsa_sel_fwd(C.byref(p), None, None, None, None, None, None, ws, 1 << 20, None)
+    assert s == 1
+    s = lib.nsa_sel_bwd(C.byref(_p(D=96)), *([C.c_void_p(256)] * 10), ws, 1 << 20, None)
+    assert s == 2
+    # workspace too small / misaligned
+    args = [C.c_void_p(256)] * 6
+    assert lib.nsa_sel_fwd(C.byref(p), *args, C.c_void_p(256), 16, None) == 6
+    assert lib.nsa_sel_fwd(C.byref(p), *args, C.c_void_p(272), 1 << 20, None) == 6
+    # misaligned tensor
+    bad = [C.c_void_p(258)] + [C.c_void_p(256)] * 5
+    assert lib.nsa_sel_fwd(C.byref(p), *bad, C.c_void_p(256), 1 << 20, None) == 1
+    # wrong layout for the entry point
+    pt = api.problem(1, 4, 2, 256, 128, 64, 4, __import__("torch").bfloat16, layout=1,
+                     total_tokens=256)
+    assert lib.nsa_sel_fwd(C.byref(pt), *args, C.c_void_p(256), 1 << 20, None) == 1
+
+
+def test_offsets_len(lib):
+    assert lib.nsa_inverse_index_offsets_len(C.byref(_p(B=2, Hkv=2, T=130, block_size=64))) == 2 * 2 * 3 + 1

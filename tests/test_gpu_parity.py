@@ -1,0 +1,202 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Inputs are seeded and synthetic (block_sparse_attention_do_gb300.inputs); the
+oracle reads the same dtype-rounded values.  The gate is the gradcheck page's
+TOL table applied as a max-abs bound (tests/golden/gate_tolerances.json):
+2e-3 for fp32, 6e-2 for bf16; the inverse index must match bit-exactly.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_do_gb300 import api, inputs
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "gate_tolerances.json")))
+TOL = {torch.float32: GOLD["max_abs_gate"]["fp32"], torch.bfloat16: GOLD["max_abs_gate"]["bf16"]}
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_sparse_attention_do_gb300 import build
+
+    build.build()
+    api.lib()
+
+
+def _maxerr(got, ref):
+    return float(np.max(np.abs(got.double().cpu().numpy() - ref))) if ref.size else 0.0
+
+
+def _run(q, k, v, do, idx, bs, cu=None, dense=False):
+    g = [x.to(DEV) for x in (q, k, v, do)]
+    gi = None if dense else idx.to(DEV)
+    gcu = None if cu is None else cu.to(DEV)
+    o, lse = api.sel_fwd(g[0], g[1], g[2], gi, bs, cu_seqlens=gcu, dense=dense)
+    dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, gi, bs, cu_seqlens=gcu, dense=dense)
+    torch.cuda.synchronize()
+    return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def _compare(got, ref, dtype, names=("o", "dq", "dk", "dv")):
+    tol = TOL[dtype]
+    errs = {n: _maxerr(got[n], ref[n]) for n in names}
+    lse_ref = ref["lse"]
+    lse_got = got["lse"].double().cpu().numpy()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(lse_got)), "empty rows must give -inf"
+    errs["lse"] = float(np.max(np.abs(lse_got[fin] - lse_ref[fin]))) if fin.any() else 0.0
+    bad = {n: e for n, e in errs.items() if not e <= tol}
+    assert not bad, f"max-abs errors over {tol}: {errs}"
+    return errs
+
+
+SMALL = [
+    # B, Hq, Hkv, T, D, bs, S
+    (1, 2, 1, 128, 32, 16, 4),    # the small fp32 fwd+bwd workload
+    (1, 3, 3, 77, 64, 32, 3),     # G=1, ragged tail
+    (2, 6, 2, 200, 64, 32, 8),    # G=3, S above the valid count for early rows
+    (1, 4, 1, 150, 128, 64, 3),   # G=4, D=128, bs=64, ragged
+    (1, 16, 1, 256, 128, 64, 4),  # G=16
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("case", SMALL)
+def test_small_selection(case, dtype):
+    B, Hq, Hkv, T, D, bs, S = case
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=1)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=1)
+    got = _run(q, k, v, do, idx, bs)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_padding_anywhere_and_empty_rows(dtype):
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 2, 192, 64, 32, 5
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=5)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=5)
+    rng = np.random.default_rng(0)
+    a = idx.numpy()
+    for g in range(Hkv):
+        for t in range(T):
+            a[0, g, t] = a[0, g, t][rng.permutation(S)]  # -1 anywhere, own block anywhere
+    a[0, 0, 100] = -1      # an empty row
+    a[0, 1, 37, :] = -1
+    a[0, 1, 37, 2] = 0     # a row attending only an earlier block
+    idx = torch.from_numpy(a)
+    got = _run(q, k, v, do, idx, bs)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_dense_causal(dtype):
+    B, Hq, Hkv, T, D, bs = 2, 8, 2, 200, 128, 64
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=2)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    got = _run(q, k, v, do, None, bs, dense=True)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_varlen(dtype):
+    lengths = [130, 1, 64, 257, 90]
+    Hq, Hkv, D, bs, S = 8, 2, 128, 64, 3
+    total = sum(lengths)
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=dtype, seed=3, layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=3)
+    got = _run(q, k, v, do, idx, bs, cu=cu)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs, cu_seqlens=cu)
+    _compare(got, ref, dtype)
+
+
+def test_inverse_index_bit_exact():
+    for (B, Hkv, T, bs, S, lengths) in ((2, 3, 333, 32, 6, None), (0, 2, 0, 64, 5, [70, 1, 300])):
+        if lengths is None:
+            idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=4)
+            cu = None
+        else:
+            idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=4)
+            cu = inputs.cu_seqlens_from_lengths(lengths)
+        off, rows, ws = api.build_inverse_index(idx.to(DEV), Hkv * 2, bs,
+                                                cu_seqlens=None if cu is None else cu.to(DEV))
+        ref_off, ref_rows, _ = oracle.inverse_index(idx, bs, cu_seqlens=cu)
+        off = off.cpu().numpy()
+        assert np.array_equal(off, ref_off)
+        assert np.array_equal(rows[: off[-1]].cpu().numpy(), ref_rows)
+        assert api.get_error(ws) == 0
+
+
+def test_do_dot():
+    o = torch.randn(2, 3, 100, 128, dtype=torch.bfloat16)
+    do = torch.randn(2, 3, 100, 128, dtype=torch.bfloat16)
+    got = api.do_dot(o.to(DEV), do.to(DEV)).cpu().double().numpy()
+    ref = oracle.do_dot(o, do)
+    assert np.max(np.abs(got - ref)) < 1e-3
+
+
+def test_bad_index_is_reported():
+    B, Hq, Hkv, T, D, bs, S = 1, 2, 1, 128, 64, 32, 3
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S)
+    cases = []
+    bad = idx.clone()
+    bad[0, 0, 10, 1] = 3       # future block
+    cases.append(bad)
+    bad = idx.clone()
+    bad[0, 0, 100, 2] = bad[0, 0, 100, 0]  # repeated block
+    cases.append(bad)
+    bad = idx.clone()
+    bad[0, 0, 50, 1] = -7
+    cases.append(bad)
+    for bad in cases:
+        assert oracle.validate_index(bad, bs) == 3
+        g = [x.to(DEV) for x in (q, k, v, do, bad)]
+        ws = torch.empty(api.bwd_workspace_size(api.problem_from(g[0], g[1], bs, S)),
+                         dtype=torch.uint8, device=DEV)
+        o, lse = api.sel_fwd(g[0], g[1], g[2], g[4], bs, ws=ws)
+        assert api.get_error(ws) == 3
+        api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, g[4], bs, ws=ws)
+        assert api.get_error(ws) == 3
+        assert api.get_error(ws) == 0  # reading clears it
+
+
+def test_runs_on_the_callers_stream():
+    B, Hq, Hkv, T, D, bs, S = 1, 4, 1, 256, 128, 64, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=9)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=9)
+    g = [x.to(DEV) for x in (q, k, v, do, idx)]
+    ref = _run(q, k, v, do, idx, bs)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = api.sel_fwd(g[0], g[1], g[2], g[4], bs, stream=s)
+        dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, g[4], bs, stream=s)
+    s.synchronize()
+    for name, x in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(x, ref[name]), f"{name} differs between streams (must be deterministic)"
+
+
+def test_count_pairs():
+    B, Hq, Hkv, T, bs, S = 2, 6, 2, 500, 32, 6
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=6)
+    assert api.count_pairs(idx.to(DEV), Hq, bs) == oracle.count_pairs(idx, Hq, bs)
+
+
+def test_deterministic_bitwise():
+    B, Hq, Hkv, T, D, bs, S = 1, 16, 1, 512, 128, 64, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=10)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=10)
+    a = _run(q, k, v, do, idx, bs)
+    b = _run(q, k, v, do, idx, bs)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
