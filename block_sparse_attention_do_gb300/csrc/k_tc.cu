@@ -1,25 +1,104 @@
-// k_tc.cu -- placeholder until the tensor-core kernels land.
-#include "launch.h"
+// k_tc.cu -- host helpers of the tensor-core kernels: which problems they
+// take, the device's SM count and TMA tensor-map construction.
+#include <mutex>
+
+#include "tc_common.cuh"
 
 namespace nsa {
 
-bool tc_supported(const Geo &, int) { return false; }
+bool tc_supported(const Geo &g, int dtype)
+{
+    return dtype == NSA_DTYPE_BF16 && g.D == kHead && g.bs == kKeys && g.G >= 1 && g.G <= kRows;
+}
 
-cudaError_t launch_fwd_tc(const Geo &, const void *, const void *, const void *, const int *, void *,
-                          float *, int *, cudaStream_t)
+int num_sms()
 {
-    return cudaErrorNotSupported;
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
-cudaError_t launch_dq_tc(const Geo &, const void *, const void *, const void *, const void *,
-                         const float *, const float *, const int *, void *, int *, cudaStream_t)
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    return cudaErrorNotSupported;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    });
+    return fn;
 }
-cudaError_t launch_dkdv_tc(const Geo &, const void *, const void *, const void *, const void *,
-                           const float *, const float *, const int *, const int *, const Unit *,
-                           const WsHeader *, int, float *, void *, void *, int *, cudaStream_t)
+
+}  // namespace
+
+bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads)
 {
-    return cudaErrorNotSupported;
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+    cuuint32_t rank;
+    const cuuint64_t es = 2;  // bf16
+    if (g.thd) {
+        rank = 3;
+        dims[0] = g.D;
+        dims[1] = H;
+        dims[2] = g.ntok;
+        strides[0] = (cuuint64_t)g.D * es;
+        strides[1] = (cuuint64_t)H * g.D * es;
+        box[0] = 64;
+        box[1] = box_heads;
+        box[2] = box_tok;
+    } else {
+        rank = 4;
+        dims[0] = g.D;
+        dims[1] = g.T;
+        dims[2] = H;
+        dims[3] = g.B;
+        strides[0] = (cuuint64_t)g.D * es;
+        strides[1] = (cuuint64_t)g.T * g.D * es;
+        strides[2] = (cuuint64_t)H * g.T * g.D * es;
+        box[0] = 64;
+        box[1] = box_tok;
+        box[2] = box_heads;
+        box[3] = 1;
+    }
+    if (dims[rank - 1] == 0)
+        return false;
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// dQ and the forward on tensor cores are not in this build yet: the SIMT
+// kernels serve them.
+cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
+                          void *o, float *lse, int *, cudaStream_t st)
+{
+    return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
+}
+
+cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                         const float *lse, const float *delta, const int *idx, void *dq, int *,
+                         cudaStream_t st)
+{
+    return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
 }
 
 }  // namespace nsa

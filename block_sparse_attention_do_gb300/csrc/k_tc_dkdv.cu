@@ -1,0 +1,494 @@
+// k_tc_dkdv.cu -- dK/dV on the tcgen05 tensor cores (bf16, D = 128,
+// block_size = 64).
+//
+// One work unit is (sequence b, kv head g, kv block j, a run of the block's
+// token list from the inverse index).  Its rows are (token, query head) pairs
+// for the G query heads of the group, 128 rows per tile.  For every tile:
+//   S   = Q K_j^T,  dP = dO V_j^T                     (M=128 rows, N=64 keys, K=128)
+//   P   = exp(scale S - LSE) on the rows' attended keys, dS = P (dP - delta)
+//   dV_j^T += dO^T P,  dK_j^T += Q^T dS               (M=128 dims, N=64 keys, K=128 rows)
+// so the sum over the G heads (the GQA reduction) and over the tokens happens
+// inside the accumulator, in a fixed order.  A block whose list is split over
+// several units writes fp32 partials that a separate kernel adds in unit
+// order; a block held by one unit writes dK/dV directly.
+//
+// Roles (8 warps):  warps 0-1 load (TMA for K_j/V_j; Q/dO rows by TMA boxes of
+// one token x G heads when G % 8 == 0, else by 16-byte cp.async with the
+// swizzle applied by hand; LSE/delta/token ids by plain loads); warp 2 owns
+// TMEM and one thread issues every MMA; warps 4-7 compute P/dS for one row
+// each and run the epilogue.  Two Q/dO stages, two S/dP TMEM buffers, one
+// P/dS buffer.
+#include "tc_common.cuh"
+
+namespace nsa {
+
+namespace {
+
+using namespace tc;
+
+// shared-memory plan (bytes from a 1024-aligned base)
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + kKvBytes;
+constexpr int OFF_Q = OFF_V + kKvBytes;          // 2 stages
+constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;   // 2 stages
+constexpr int OFF_P = OFF_DO + 2 * kTileBytes;
+constexpr int OFF_DS = OFF_P + kRows * 128;
+constexpr int OFF_LSE = OFF_DS + kRows * 128;    // float [2][128], LSE * log2(e)
+constexpr int OFF_DLT = OFF_LSE + 2 * kRows * 4; // float [2][128]
+constexpr int OFF_TOK = OFF_DLT + 2 * kRows * 4; // int   [2][128]
+constexpr int OFF_BAR = OFF_TOK + 2 * kRows * 4;
+constexpr int NUM_BARS = 16;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+
+// barrier slots
+enum {
+    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE
+};
+
+// TMEM columns
+constexpr uint32_t TM_S = 0;     // S of buffer b at b*128, dP at b*128 + 64
+constexpr uint32_t TM_DV = 256;  // dV^T: 128 lanes (d) x 64 columns (keys)
+constexpr uint32_t TM_DK = 320;  // dK^T
+constexpr uint32_t TM_COLS = 512;
+
+constexpr int kProdThreads = 64;
+
+struct Params {
+    Geo g;
+    const __nv_bfloat16 *q, *dO;
+    const float *lse, *delta;
+    const int *offsets, *rows;
+    const Unit *units;
+    const WsHeader *hdr;
+    float *partials;
+    __nv_bfloat16 *dk, *dv;
+    int *err;
+};
+
+__device__ __forceinline__ int unit_token(const Params &p, const Unit &u, int pos)
+{
+    if (p.g.dense)
+        return u.j * p.g.bs + u.begin + pos;
+    return p.rows[p.offsets[u.bg * p.g.nbmax + u.j] + u.begin + pos];
+}
+
+template <bool GATHER_TMA>
+__global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                         const __grid_constant__ CUtensorMap tm_do,
+                                                         const __grid_constant__ CUtensorMap tm_k,
+                                                         const __grid_constant__ CUtensorMap tm_v,
+                                                         const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(sm + OFF_BAR);
+    volatile int *abort_flag = (volatile int *)(sm + OFF_MISC);
+    uint32_t *tmem_slot = (uint32_t *)(sm + OFF_MISC + 16);
+    float *lse_s = (float *)(sm + OFF_LSE);
+    float *dlt_s = (float *)(sm + OFF_DLT);
+    int *tok_s = (int *)(sm + OFF_TOK);
+
+    const Geo &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = g.G;
+    const int Tt = G >= kRows ? 1 : kRows / G;  // tokens per tile
+    const int nrows = Tt * G;                  // used rows per tile
+    const int n_units = p.hdr->n_units;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(&bars[B_FULL0], kProdThreads + (GATHER_TMA ? 1 : 0));
+        mbar_init(&bars[B_FULL1], kProdThreads + (GATHER_TMA ? 1 : 0));
+        mbar_init(&bars[B_EMPTY0], 1);
+        mbar_init(&bars[B_EMPTY1], 1);
+        mbar_init(&bars[B_KVFULL], 1);
+        mbar_init(&bars[B_KVEMPTY], 1);
+        mbar_init(&bars[B_SFULL0], 1);
+        mbar_init(&bars[B_SFULL1], 1);
+        mbar_init(&bars[B_SFREE0], kRows);
+        mbar_init(&bars[B_SFREE1], kRows);
+        mbar_init(&bars[B_PFULL], kRows);
+        mbar_init(&bars[B_PFREE], 1);
+        mbar_init(&bars[B_ACCFULL], 1);
+        mbar_init(&bars[B_ACCEMPTY], kRows);
+        mbar_init(&bars[B_DONE], 1);
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, TM_COLS);
+        tmem_relinquish();
+    }
+    // rows a tile never fills must hold finite values (they meet P = 0)
+    for (int i = threadIdx.x; i < (2 * kTileBytes * 2) / 16; i += blockDim.x)
+        *(uint4 *)(sm + OFF_Q + i * 16) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 2) {
+        // ------------------------------------------------------------ loader
+        const int pt = threadIdx.x;  // 0..63
+        const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
+        int it = 0, uc = 0;
+        int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
+        bool ok = true;
+        if (pt == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_do);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+        }
+        for (int ui = blockIdx.x; ui < n_units && ok; ui += gridDim.x, ++uc) {
+            const Unit u = p.units[ui];
+            const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
+            if (pt == 0) {
+                ok = mbar_wait(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag);
+                if (ok) {
+                    last_kv = uc;
+                    mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
+                    for (int h = 0; h < 2; ++h) {
+                        if (g.thd) {
+                            const int t0 = g.cu[b] + u.j * kKeys;
+                            tma_load_3d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64, kvh, t0);
+                            tma_load_3d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64, kvh, t0);
+                        } else {
+                            tma_load_4d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64,
+                                        u.j * kKeys, kvh, b);
+                            tma_load_4d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64,
+                                        u.j * kKeys, kvh, b);
+                        }
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp 0 only; warp 1 follows below
+            const int ntiles = (u.count + Tt - 1) / Tt;
+            for (int ti = 0; ti < ntiles && !*abort_flag; ++ti, ++it) {
+                const int st = it & 1;
+                if (!mbar_wait(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int ntok = min(Tt, u.count - ti * Tt);
+                // token ids, LSE and delta for the tile's rows (generic stores)
+                for (int tl = pt; tl < kRows; tl += kProdThreads)
+                    tok_s[st * kRows + tl] = tl < ntok ? unit_token(p, u, ti * Tt + tl) : -1;
+                for (int r = pt; r < kRows; r += kProdThreads) {
+                    const int tl = r / G, hh = r % G;
+                    float l2 = 0.f, dl = 0.f;
+                    if (r < nrows && tl < ntok) {
+                        const int t = unit_token(p, u, ti * Tt + tl);
+                        const int64_t so = stat_off(g, b, kvh * G + hh, t);
+                        l2 = p.lse[so] * 1.4426950408889634f;
+                        dl = p.delta[so];
+                    }
+                    lse_s[st * kRows + r] = l2;
+                    dlt_s[st * kRows + r] = dl;
+                }
+                if (GATHER_TMA) {
+                    if (pt == 0) {
+                        last_tile = it;
+                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
+                        for (int tl = 0; tl < Tt; ++tl) {
+                            // rows past the list repeat the last token (finite data, P = 0)
+                            const int t = unit_token(p, u, ti * Tt + min(tl, ntok - 1));
+                            uint8_t *qd = sm + OFF_Q + st * kTileBytes + tl * G * 128;
+                            uint8_t *od = sm + OFF_DO + st * kTileBytes + tl * G * 128;
+                            for (int h = 0; h < 2; ++h) {
+                                if (g.thd) {
+                                    tma_load_3d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, kvh * G,
+                                                g.cu[b] + t);
+                                    tma_load_3d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, kvh * G,
+                                                g.cu[b] + t);
+                                } else {
+                                    tma_load_4d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
+                                    tma_load_4d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
+                                }
+                            }
+                        }
+                    }
+                    mbar_arrive(&bars[B_FULL0 + st]);
+                } else {
+                    // 2 tensors x 128 rows x 16 chunks of 16 bytes
+                    for (int item = pt; item < 2 * kRows * 16; item += kProdThreads) {
+                        const int tensor = item / (kRows * 16);
+                        const int rem = item % (kRows * 16);
+                        const int r = rem >> 4, c = rem & 15;
+                        const int tl = r / G, hh = r % G;
+                        const bool valid = r < nrows && tl < ntok;
+                        const __nv_bfloat16 *base = tensor ? p.dO : p.q;
+                        const __nv_bfloat16 *src = base;
+                        if (valid) {
+                            const int t = unit_token(p, u, ti * Tt + tl);
+                            src = base + row_off(g, g.Hq, b, kvh * G + hh, t) + c * 8;
+                        }
+                        const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + (c >> 3) * kHalfBytes +
+                                             sw128_off(r, c & 7);
+                        cp_async_16(dst, src, valid ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    fence_async_smem();
+                    mbar_arrive(&bars[B_FULL0 + st]);
+                }
+            }
+            if (!ok)
+                break;
+        }
+        if (!GATHER_TMA)
+            cp_async_wait<0>();
+        if (*abort_flag && pt == 0) {
+            // let TMA copies still in flight land before the CTA exits
+            volatile int never = 0;
+            if (last_tile >= 0)
+                mbar_wait(&bars[B_FULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
+            if (last_kv >= 0)
+                mbar_wait(&bars[B_KVFULL], last_kv & 1, &never);
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, 64, false, false);
+            const uint32_t idV = idesc_bf16(128, 64, true, true);
+            const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
+            const uint32_t k_s = smem_u32(sm + OFF_K), v_s = smem_u32(sm + OFF_V);
+            const uint32_t p_s = smem_u32(sm + OFF_P), ds_s = smem_u32(sm + OFF_DS);
+            // cursor S issues S/dP, cursor V issues dV/dK; both walk (unit, tile)
+            int sU = blockIdx.x, sT = 0, sIt = 0, sUc = 0, sN = -1;
+            int vU = blockIdx.x, vT = 0, vIt = 0, vUc = 0, vN = -1;
+            auto ntiles_of = [&](int ui) { return (p.units[ui].count + Tt - 1) / Tt; };
+            if (sU < n_units)
+                sN = ntiles_of(sU);
+            if (vU < n_units)
+                vN = ntiles_of(vU);
+            const uint64_t t_start = globaltimer();
+            uint64_t t_last = t_start;
+            while (vU < n_units && !*abort_flag) {
+                bool progressed = false;
+                // dV/dK of the oldest tile whose P/dS are ready
+                if (vIt < sIt && mbar_try_wait(&bars[B_PFULL], vIt & 1) &&
+                    (vT > 0 || mbar_try_wait(&bars[B_ACCEMPTY], (vUc & 1) ^ 1))) {
+                    tc_fence_after();
+                    const int st = vIt & 1;
+                    for (int kr = 0; kr < kRows / 16; ++kr) {
+                        const uint32_t acc = (vT > 0 || kr > 0) ? 1u : 0u;
+                        mma_bf16(tmem + TM_DV, sdesc_sw128(do_s + st * kTileBytes + kr * 2048, kHalfBytes, 1024),
+                                 sdesc_sw128(p_s + kr * 2048, 8192, 1024), idV, acc);
+                        mma_bf16(tmem + TM_DK, sdesc_sw128(q_s + st * kTileBytes + kr * 2048, kHalfBytes, 1024),
+                                 sdesc_sw128(ds_s + kr * 2048, 8192, 1024), idV, acc);
+                    }
+                    mma_commit(&bars[B_PFREE]);
+                    mma_commit(&bars[B_EMPTY0 + st]);
+                    if (vT + 1 == vN) {
+                        mma_commit(&bars[B_ACCFULL]);
+                        vU += gridDim.x;
+                        vT = 0;
+                        ++vUc;
+                        vN = vU < n_units ? ntiles_of(vU) : -1;
+                    } else {
+                        ++vT;
+                    }
+                    ++vIt;
+                    progressed = true;
+                }
+                // S/dP of the next tile (at most two tiles ahead of dV/dK)
+                if (sU < n_units && sIt < vIt + 2 && mbar_try_wait(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
+                    mbar_try_wait(&bars[B_SFREE0 + (sIt & 1)], ((sIt >> 1) & 1) ^ 1) &&
+                    (sT > 0 || mbar_try_wait(&bars[B_KVFULL], sUc & 1))) {
+                    tc_fence_after();
+                    const int st = sIt & 1;
+                    const uint32_t dS_col = tmem + TM_S + st * 128;
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
+                        mma_bf16(dS_col, sdesc_sw128(q_s + st * kTileBytes + ao, 16, 1024),
+                                 sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
+                        mma_bf16(dS_col + 64, sdesc_sw128(do_s + st * kTileBytes + ao, 16, 1024),
+                                 sdesc_sw128(v_s + bo, 16, 1024), idS, kk > 0);
+                    }
+                    mma_commit(&bars[B_SFULL0 + st]);
+                    if (sT + 1 == sN) {
+                        mma_commit(&bars[B_KVEMPTY]);
+                        sU += gridDim.x;
+                        sT = 0;
+                        ++sUc;
+                        sN = sU < n_units ? ntiles_of(sU) : -1;
+                    } else {
+                        ++sT;
+                    }
+                    ++sIt;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = globaltimer();
+                } else if (globaltimer() - t_last > kWaitLimitNs) {
+                    *abort_flag = 1;
+                }
+            }
+            // every MMA issued must finish before TMEM is released
+            mma_commit(&bars[B_DONE]);
+            volatile int never = 0;
+            mbar_wait(&bars[B_DONE], 0, &never);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------- softmax / epilogue
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // tile row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t p_row = smem_u32(sm + OFF_P) + r * 128;
+        const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
+        int it = 0, uc = 0;
+        bool ok = true;
+        for (int ui = blockIdx.x; ui < n_units && ok; ui += gridDim.x, ++uc) {
+            const Unit u = p.units[ui];
+            const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
+            const int L = seq_len(g, b);
+            const int k0 = u.j * kKeys;
+            const int ntiles = (u.count + Tt - 1) / Tt;
+            for (int ti = 0; ti < ntiles; ++ti, ++it) {
+                const int st = it & 1;
+                if (!mbar_wait(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
+                    !mbar_wait(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sv[64], dv_[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&a)[16] = *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]);
+                    uint32_t (&bq)[16] = *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]);
+                    tmem_ld16(lane_base + TM_S + st * 128 + c * 16, a);
+                    tmem_ld16(lane_base + TM_S + st * 128 + 64 + c * 16, bq);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE0 + st]);
+
+                const int tl = r / G;
+                const int tok = (r < nrows) ? tok_s[st * kRows + tl] : -1;
+                const float l2 = lse_s[st * kRows + r], dl = dlt_s[st * kRows + r];
+                // keys k0 + c with c <= tok - k0 are attended (the token selected block j)
+                const int lim = tok < 0 ? -1 : tok - k0;
+                uint32_t pk[32], dk_[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (c <= lim)
+                        p0 = exp2f(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                    if (c + 1 <= lim)
+                        p1 = exp2f(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                    const float d0 = p0 * (__uint_as_float(dv_[c]) - dl);
+                    const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dl);
+                    pk[c >> 1] = pack_bf16(p0, p1);
+                    dk_[c >> 1] = pack_bf16(d0, d1);
+                }
+                if (!mbar_wait(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t o = ((c ^ (r & 7)) << 4);
+                    st_shared_v4(p_row + o, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    st_shared_v4(ds_row + o, dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
+                }
+                fence_async_smem();
+                mbar_arrive(&bars[B_PFULL]);
+            }
+            if (!ok)
+                break;
+            // ---- epilogue: lane = head dimension d, columns = keys
+            if (!mbar_wait(&bars[B_ACCFULL], uc & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int d = r;
+            const int nk = min(kKeys, L - k0);
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? TM_DK : TM_DV;
+                const float mul = which == 0 ? g.scale : 1.f;
+                uint32_t a[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld16(lane_base + col + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&a[c * 16]));
+                tmem_wait_ld();
+                if (u.slot >= 0) {
+                    float *dst = p.partials + ((int64_t)u.slot * 2 + which) * kKeys * kHead + d;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        dst[c * kHead] = __uint_as_float(a[c]) * mul;
+                } else {
+                    __nv_bfloat16 *out = which == 0 ? p.dk : p.dv;
+                    __nv_bfloat16 *o0 = out + row_off(g, g.Hkv, b, kvh, k0) + d;
+                    // distance between consecutive keys: D (BHTD) or Hkv*D (THD)
+                    const int64_t kstride = g.thd ? (int64_t)g.Hkv * kHead : kHead;
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c < nk)
+                            o0[c * kstride] = __float2bfloat16_rn(__uint_as_float(a[c]) * mul);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[B_ACCEMPTY]);
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0)
+        set_error(p.err, NSA_ERR_DEVICE_TIMEOUT);
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const void *v,
+                           const void *dO, const float *lse, const float *delta,
+                           const int *offsets, const int *rows, const Unit *units,
+                           const WsHeader *hdr, int max_units, float *partials, void *dk, void *dv,
+                           int *err, cudaStream_t st)
+{
+    CUtensorMap tq, tdo, tk, tv;
+    const bool gather_tma = (g.G % 8) == 0;
+    const int box_heads = gather_tma ? g.G : 1;
+    if (!make_tmap(&tq, q, g, g.Hq, 1, box_heads) || !make_tmap(&tdo, dO, g, g.Hq, 1, box_heads) ||
+        !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.g = g;
+    p.q = (const __nv_bfloat16 *)q;
+    p.dO = (const __nv_bfloat16 *)dO;
+    p.lse = lse;
+    p.delta = delta;
+    p.offsets = offsets;
+    p.rows = rows;
+    p.units = units;
+    p.hdr = hdr;
+    p.partials = partials;
+    p.dk = (__nv_bfloat16 *)dk;
+    p.dv = (__nv_bfloat16 *)dv;
+    p.err = err;
+    int grid = num_sms();
+    if (grid > max_units)
+        grid = max_units;
+    if (grid < 1)
+        grid = 1;
+    if (gather_tma) {
+        cudaFuncSetAttribute(dkdv_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        dkdv_tc_kernel<true><<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+    } else {
+        cudaFuncSetAttribute(dkdv_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        dkdv_tc_kernel<false><<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace nsa
