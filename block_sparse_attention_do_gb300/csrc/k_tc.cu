@@ -86,19 +86,4 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
     return r == CUDA_SUCCESS;
 }
 
-// dQ and the forward on tensor cores are not in this build yet: the SIMT
-// kernels serve them.
-cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
-                          void *o, float *lse, int *, cudaStream_t st)
-{
-    return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
-}
-
-cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
-                         const float *lse, const float *delta, const int *idx, void *dq, int *,
-                         cudaStream_t st)
-{
-    return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
-}
-
 }  // namespace nsa

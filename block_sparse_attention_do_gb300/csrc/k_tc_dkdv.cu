@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             const int ntiles = (u.count + Tt - 1) / Tt;
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
                 const int st = it & 1;
-                if (!mbar_wait(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
-                    !mbar_wait(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
+                    !mbar_wait_warp(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     pk[c >> 1] = pack_bf16(p0, p1);
                     dk_[c >> 1] = pack_bf16(d0, d1);
                 }
-                if (!mbar_wait(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             if (!ok)
                 break;
             // ---- epilogue: lane = head dimension d, columns = keys
-            if (!mbar_wait(&bars[B_ACCFULL], uc & 1, abort_flag)) {
+            if (!mbar_wait_warp(&bars[B_ACCFULL], uc & 1, abort_flag)) {
                 ok = false;
                 break;
             }

@@ -1,0 +1,351 @@
+// k_tc_dq.cu -- dQ on the tcgen05 tensor cores (bf16, D = 128, block_size
+// = 64).
+//
+// One CTA owns a query tile: Tq consecutive tokens of one sequence times the
+// G query heads of one kv head (Tq * G <= 128 rows, Tq = 128 / G).  It walks,
+// in ascending order, the union U of the blocks its tokens select, and for
+// every block j of U:
+//   S = Q K_j^T,  dP = dO V_j^T                       (M=128 rows, N=64 keys, K=128)
+//   P = exp(scale S - LSE) where the row's token selects j and key <= token,
+//   dS = P (dP - delta)
+//   dQ += dS K_j                                      (M=128 rows, N=128 dims, K=64 keys)
+// and writes dQ * scale once at the end.  Rows of a token that did not
+// select j get P = dS = 0, so the sum over j is exactly the sum over the
+// token's own blocks.
+//
+// Roles (8 warps): warp 0 lane 0 issues TMA (the Q/dO tile once, then K_j/V_j
+// double-buffered); warp 2 owns TMEM and issues the MMAs; warps 4-7 build the
+// block union, then form P/dS one row per thread and run the epilogue.
+#include "tc_common.cuh"
+
+namespace nsa {
+
+namespace {
+
+using namespace tc;
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_DO = OFF_Q + kTileBytes;
+constexpr int OFF_KV = OFF_DO + kTileBytes;   // 2 stages x (K | V)
+constexpr int OFF_DS = OFF_KV + 2 * 2 * kKvBytes;  // 2 buffers
+constexpr int OFF_MASK = OFF_DS + 2 * kRows * 128;
+constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
+constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
+constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
+constexpr int NUM_BARS = 16;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+
+enum {
+    B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
+    B_DSFULL0, B_DSFULL1, B_DSFREE0, B_DSFREE1, B_ACCFULL, B_DONE, B_LIST
+};
+
+constexpr uint32_t TM_S = 0;     // buffer b: S at b*128, dP at b*128 + 64
+constexpr uint32_t TM_DQ = 256;  // 128 lanes (rows) x 128 columns (dims)
+constexpr uint32_t TM_COLS = 512;
+
+struct Params {
+    Geo g;
+    const int *idx;
+    const float *lse, *delta;
+    __nv_bfloat16 *dq;
+    int *err;
+};
+
+__global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                       const __grid_constant__ CUtensorMap tm_do,
+                                                       const __grid_constant__ CUtensorMap tm_k,
+                                                       const __grid_constant__ CUtensorMap tm_v,
+                                                       const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(sm + OFF_BAR);
+    volatile int *abort_flag = (volatile int *)(sm + OFF_MISC);
+    uint32_t *tmem_slot = (uint32_t *)(sm + OFF_MISC + 16);
+    volatile int *n_list = (volatile int *)(sm + OFF_MISC + 32);
+    uint32_t *mask = (uint32_t *)(sm + OFF_MASK);
+    int *list = (int *)(sm + OFF_LIST);
+    uint32_t *ubits = (uint32_t *)(sm + OFF_UBITS);
+
+    const Geo &g = p.g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = g.G;
+    const int Tq = G >= kRows ? 1 : kRows / G;
+    const int nrows = Tq * G;
+    // heavier (later) tiles first
+    const int ntiles_seq = (g.T + Tq - 1) / Tq;
+    const int tile = ntiles_seq - 1 - (int)blockIdx.x;
+    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int L = seq_len(g, b);
+    const int t0 = tile * Tq;
+    if (t0 >= L)
+        return;
+    const int nvalid = min(Tq, L - t0);
+    const int words = (g.nbmax + 31) / 32;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(&bars[B_QFULL], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[B_KVFULL0 + s], 1);
+            mbar_init(&bars[B_KVEMPTY0 + s], 1);
+            mbar_init(&bars[B_SFULL0 + s], 1);
+            mbar_init(&bars[B_SFREE0 + s], kRows);
+            mbar_init(&bars[B_DSFULL0 + s], kRows);
+            mbar_init(&bars[B_DSFREE0 + s], 1);
+        }
+        mbar_init(&bars[B_ACCFULL], 1);
+        mbar_init(&bars[B_DONE], 1);
+        mbar_init(&bars[B_LIST], kRows);
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, TM_COLS);
+        tmem_relinquish();
+    }
+    // unused rows (Tq * G < 128) must hold finite values
+    if (nrows < kRows) {
+        for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += blockDim.x) {
+            const int r = (i * 16 % kHalfBytes) / 128;
+            if (r >= nrows)
+                *(uint4 *)(sm + OFF_Q + i * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------- TMA
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(&bars[B_QFULL], 2 * nrows * 128 * 2);
+            for (int h = 0; h < 2; ++h) {
+                if (g.thd) {
+                    tma_load_3d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                    tma_load_3d(sm + OFF_DO + h * kHalfBytes, &tm_do, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                } else {
+                    tma_load_4d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                    tma_load_4d(sm + OFF_DO + h * kHalfBytes, &tm_do, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                }
+            }
+            bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag);
+            const int U = ok ? *n_list : 0;
+            int last = -1;
+            for (int i = 0; i < U && ok; ++i) {
+                const int s = i & 1;
+                if (!mbar_wait(&bars[B_KVEMPTY0 + s], ((i >> 1) & 1) ^ 1, abort_flag))
+                    break;
+                const int j = list[i];
+                uint8_t *kd = sm + OFF_KV + s * 2 * kKvBytes;
+                uint8_t *vd = kd + kKvBytes;
+                mbar_arrive_expect_tx(&bars[B_KVFULL0 + s], 2 * kKvBytes);
+                last = i;
+                for (int h = 0; h < 2; ++h) {
+                    if (g.thd) {
+                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, kvh,
+                                    g.cu[b] + j * kKeys);
+                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, kvh,
+                                    g.cu[b] + j * kKeys);
+                    } else {
+                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
+                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
+                    }
+                }
+            }
+            // copies in flight must land before the CTA may exit
+            volatile int never = 0;
+            mbar_wait(&bars[B_QFULL], 0, &never);
+            if (*abort_flag && last >= 0)
+                mbar_wait(&bars[B_KVFULL0 + (last & 1)], (last >> 1) & 1, &never);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // -------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, 64, false, false);
+            const uint32_t idQ = idesc_bf16(128, 128, false, true);
+            const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
+            const uint32_t kv_s = smem_u32(sm + OFF_KV), ds_s = smem_u32(sm + OFF_DS);
+            bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
+            const int U = ok ? *n_list : 0;
+            int si = 0, qi = 0;  // next S/dP block, next dQ block
+            uint64_t t_last = globaltimer();
+            while (ok && qi < U && !*abort_flag) {
+                bool progressed = false;
+                if (qi < si && mbar_try_wait(&bars[B_DSFULL0 + (qi & 1)], (qi >> 1) & 1)) {
+                    tc_fence_after();
+                    const int s = qi & 1;
+                    const uint32_t k_s = kv_s + s * 2 * kKvBytes;
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        mma_bf16(tmem + TM_DQ, sdesc_sw128(ds_s + s * kRows * 128 + kk * 32, 16, 1024),
+                                 sdesc_sw128(k_s + kk * 2048, kKvHalfBytes, 1024), idQ, (qi > 0 || kk > 0));
+                    mma_commit(&bars[B_DSFREE0 + s]);
+                    mma_commit(&bars[B_KVEMPTY0 + s]);
+                    ++qi;
+                    progressed = true;
+                }
+                if (si < U && si < qi + 2 && mbar_try_wait(&bars[B_KVFULL0 + (si & 1)], (si >> 1) & 1) &&
+                    mbar_try_wait(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1)) {
+                    tc_fence_after();
+                    const int s = si & 1;
+                    const uint32_t k_s = kv_s + s * 2 * kKvBytes, v_s = k_s + kKvBytes;
+                    const uint32_t d = tmem + TM_S + s * 128;
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
+                        mma_bf16(d, sdesc_sw128(q_s + ao, 16, 1024), sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
+                        mma_bf16(d + 64, sdesc_sw128(do_s + ao, 16, 1024), sdesc_sw128(v_s + bo, 16, 1024), idS,
+                                 kk > 0);
+                    }
+                    mma_commit(&bars[B_SFULL0 + s]);
+                    ++si;
+                    progressed = true;
+                }
+                if (progressed)
+                    t_last = globaltimer();
+                else if (globaltimer() - t_last > kWaitLimitNs)
+                    *abort_flag = 1;
+            }
+            mma_commit(&bars[B_ACCFULL]);
+            mma_commit(&bars[B_DONE]);
+            volatile int never = 0;
+            mbar_wait(&bars[B_DONE], 0, &never);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------- union, softmax, epilogue
+        const int tid = threadIdx.x - 128;  // 0..127
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        // 1. block union and per-token masks
+        const int Un = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, tid, lane, wq);
+        if (tid == 0)
+            *n_list = Un;
+        mbar_arrive(&bars[B_LIST]);
+        const int U = Un;
+
+        // 2. per-row constants
+        int tl, hh;
+        qtile_row(g, Tq, r, tl, hh);
+        const bool rvalid = r < nrows && tl < nvalid;
+        const int t = t0 + tl;
+        float l2 = 0.f, dl = 0.f;
+        if (rvalid) {
+            const int64_t so = stat_off(g, b, kvh * G + hh, t);
+            l2 = p.lse[so] * 1.4426950408889634f;
+            dl = p.delta[so];
+        }
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
+        const uint32_t *my_mask = mask + (rvalid ? tl : 0) * words;
+        bool ok = true;
+        for (int i = 0; i < U; ++i) {
+            const int s = i & 1;
+            if (!mbar_wait_warp(&bars[B_SFULL0 + s], (i >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[64], dv_[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld16(lane_base + TM_S + s * 128 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
+                tmem_ld16(lane_base + TM_S + s * 128 + 64 + c * 16,
+                          *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars[B_SFREE0 + s]);
+            const int j = list[i];
+            const bool sel = rvalid && qtile_selects(g, my_mask, t, j);
+            const int lim = sel ? t - j * kKeys : -1;
+            uint32_t dk_[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                float p0 = 0.f, p1 = 0.f;
+                if (c <= lim)
+                    p0 = exp2f(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                if (c + 1 <= lim)
+                    p1 = exp2f(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+            }
+            if (!mbar_wait_warp(&bars[B_DSFREE0 + s], ((i >> 1) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint32_t row = ds_row + s * kRows * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
+            fence_async_smem();
+            mbar_arrive(&bars[B_DSFULL0 + s]);
+        }
+        // 3. epilogue: dQ row r = scale * TMEM lane r.  Every lane of the warp
+        //    runs the TMEM loads (.sync.aligned); only valid rows store.
+        if (ok && U > 0)
+            ok = mbar_wait_warp(&bars[B_ACCFULL], 0, abort_flag);
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) : nullptr;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t a[16];
+                tmem_ld16(lane_base + TM_DQ + c * 16, a);
+                tmem_wait_ld();
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    w[e] = U > 0 ? pack_bf16(__uint_as_float(a[2 * e]) * g.scale,
+                                             __uint_as_float(a[2 * e + 1]) * g.scale)
+                                 : 0u;
+                if (rvalid) {
+                    *(uint4 *)(dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(dst + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0)
+        set_error(p.err, NSA_ERR_DEVICE_TIMEOUT);
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                         const float *lse, const float *delta, const int *idx, void *dq, int *err,
+                         cudaStream_t st)
+{
+    if (!qtile_shape_ok(g))
+        return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
+    const int Tq = g.G >= kRows ? 1 : kRows / g.G;
+    CUtensorMap tq, tdo, tk, tv;
+    if (!make_tmap(&tq, q, g, g.Hq, Tq, g.G) || !make_tmap(&tdo, dO, g, g.Hq, Tq, g.G) ||
+        !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+        return cudaErrorInvalidValue;
+    Params p;
+    p.g = g;
+    p.idx = idx;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq = (__nv_bfloat16 *)dq;
+    p.err = err;
+    dim3 grid((g.T + Tq - 1) / Tq, g.Hkv, g.B);
+    cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    dq_tc_kernel<<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace nsa

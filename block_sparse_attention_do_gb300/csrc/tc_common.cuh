@@ -31,4 +31,94 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
 // the host launcher's view of the device: SM count (cached)
 int num_sms();
 
+// ---- query-tile kernels (forward, dQ): a tile is Tq consecutive tokens of
+// one sequence times the G query heads of one kv head.
+constexpr int MAX_BLOCKS = 2048;  // nbmax limit (union list and bitmap)
+constexpr int MASK_WORDS = 4096;  // per-token block bitmaps: Tq * ceil(nbmax/32) words
+
+__host__ __device__ inline int tile_tokens(int G) { return G >= kRows ? 1 : kRows / G; }
+
+inline bool qtile_shape_ok(const Geo &g)
+{
+    return g.nbmax <= MAX_BLOCKS && tile_tokens(g.G) * ((g.nbmax + 31) / 32) <= MASK_WORDS;
+}
+
+// tile row -> (token within tile, head within group).  The TMA box of a
+// tile is {64, Tq tokens, G heads} for BHTD (rows head-major) and
+// {64, G heads, Tq tokens} for THD (rows token-major).
+__device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, int &hh)
+{
+    if (g.thd) {
+        tl = r / g.G;
+        hh = r % g.G;
+    } else {
+        hh = r / Tq;
+        tl = r % Tq;
+    }
+}
+
+// Builds, with the 128 threads of warps 4-7 (named barrier 1), the ascending
+// list of blocks selected by any of the tile's tokens and one bitmap per
+// token.  Entries that are -1, out of range or in the future are skipped.
+// Returns the list length.
+__device__ __forceinline__ int qtile_union(const Geo &g, const int *idx, int b, int kvh, int t0, int nvalid,
+                                           uint32_t *mask, uint32_t *ubits, int *list, int tid, int lane,
+                                           int wq)
+{
+    const int words = (g.nbmax + 31) / 32;
+    for (int i = tid; i < tile_tokens(g.G) * words; i += 128)
+        mask[i] = 0;
+    for (int i = tid; i < words; i += 128)
+        ubits[i] = 0;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (g.dense) {
+        const int jmax = (t0 + nvalid - 1) / g.bs;
+        for (int j = tid; j <= jmax; j += 128)
+            atomicOr(&ubits[j >> 5], 1u << (j & 31));
+    } else {
+        for (int i = tid; i < nvalid * g.S; i += 128) {
+            const int tl = i / g.S, s = i % g.S;
+            const int t = t0 + tl;
+            const int j = idx_row(g, idx, b, kvh, t)[s];
+            if (j >= 0 && j <= t / g.bs && j < g.nbmax) {
+                atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
+                atomicOr(&ubits[j >> 5], 1u << (j & 31));
+            }
+        }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    __shared__ int n_out;
+    if (wq == 0) {  // ordered compaction by one warp
+        int base = 0;
+        for (int w0 = 0; w0 < words; w0 += 32) {
+            const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
+            const int cnt = __popc(bits);
+            int incl = cnt;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            int pos = base + incl - cnt;
+            uint32_t bb = bits;
+            while (bb) {
+                const int bit = __ffs(bb) - 1;
+                bb &= bb - 1;
+                list[pos++] = (w0 + lane) * 32 + bit;
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0)
+            n_out = base;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    return n_out;
+}
+
+// does the row's token select block j?  (valid rows only)
+__device__ __forceinline__ bool qtile_selects(const Geo &g, const uint32_t *my_mask, int t, int j)
+{
+    return g.dense ? (j <= t / g.bs) : (((my_mask[j >> 5] >> (j & 31)) & 1u) != 0);
+}
+
 }  // namespace nsa

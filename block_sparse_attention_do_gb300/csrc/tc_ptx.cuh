@@ -89,6 +89,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Same as mbar_wait, but the outcome is made uniform across the warp: the
+// caller may follow it with .sync.aligned tcgen05 instructions, which every
+// lane must execute together.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort)
+{
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
                                             int c1, int c2)
