@@ -27,7 +27,8 @@ SYMBOLS = (
     "nsa_fwd_workspace_size", "nsa_bwd_workspace_size", "nsa_sel_fwd", "nsa_sel_bwd",
     "nsa_dense_causal_fwd", "nsa_dense_causal_bwd", "nsa_sel_varlen_fwd", "nsa_sel_varlen_bwd",
     "nsa_do_dot", "nsa_inverse_index_offsets_len", "nsa_build_inverse_index", "nsa_get_error",
-    "nsa_status_string", "nsa_count_pairs",
+    "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
+    "nsa_trace_count", "nsa_trace_get",
 )
 
 
@@ -74,6 +75,12 @@ def lib() -> C.CDLL:
         L.nsa_status_string.restype = C.c_char_p
         L.nsa_status_string.argtypes = [C.c_int32]
         L.nsa_count_pairs.argtypes = [pp] + [_P] * 3 + [_P]
+        L.nsa_trace_enable.argtypes = [C.c_int32]
+        L.nsa_trace_reset.restype = None
+        L.nsa_trace_reset.argtypes = []
+        L.nsa_trace_count.restype = C.c_int32
+        L.nsa_trace_count.argtypes = []
+        L.nsa_trace_get.argtypes = [C.c_int32, C.POINTER(C.c_char_p), C.POINTER(C.c_float)]
         for name in SYMBOLS:
             fn = getattr(L, name)
             if fn.restype is C.c_int:  # default restype: status enums
@@ -250,6 +257,26 @@ def count_pairs(block_idx, Hq, block_size, cu_seqlens=None, max_seqlen=None, str
     _check(lib().nsa_count_pairs(C.byref(p), _ptr(cu_seqlens), _ptr(block_idx), _ptr(out),
                                  _stream(stream)), "nsa_count_pairs")
     return int(out.item())
+
+
+def trace_enable(max_records: int):
+    _check(lib().nsa_trace_enable(int(max_records)), "nsa_trace_enable")
+
+
+def trace_reset():
+    lib().nsa_trace_reset()
+
+
+def trace_records():
+    """[(kernel name, ms)] of the launches recorded since the last reset."""
+    L = lib()
+    out = []
+    name = C.c_char_p()
+    ms = C.c_float()
+    for i in range(int(L.nsa_trace_count())):
+        _check(L.nsa_trace_get(i, C.byref(name), C.byref(ms)), "nsa_trace_get")
+        out.append((name.value.decode(), float(ms.value)))
+    return out
 
 
 def default_scale(D):

@@ -119,6 +119,39 @@ inline nsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NSA_OK 
             return NSA_ERR_CUDA;                       \
     } while (0)
 
+// ---- opt-in per-kernel timing (nsa_trace_*): an event pair around every
+// kernel launch, recorded on the launch stream.  Off unless enabled.
+struct TraceRec {
+    const char *name;
+    cudaEvent_t start, stop;
+};
+TraceRec *g_trace = nullptr;
+int g_trace_cap = 0, g_trace_n = 0;
+
+struct TraceScope {
+    TraceRec *rec = nullptr;
+    cudaStream_t st;
+    TraceScope(const char *name, cudaStream_t s) : st(s)
+    {
+        if (g_trace && g_trace_n < g_trace_cap) {
+            rec = &g_trace[g_trace_n++];
+            rec->name = name;
+            cudaEventRecord(rec->start, st);
+        }
+    }
+    ~TraceScope()
+    {
+        if (rec)
+            cudaEventRecord(rec->stop, st);
+    }
+};
+
+#define NSA_LAUNCH(name, expr)                         \
+    do {                                               \
+        TraceScope _ts(name, st);                      \
+        NSA_TRY(expr);                                 \
+    } while (0)
+
 nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 {
     if (!ws || ((uintptr_t)ws & (kAlign - 1)) || ws_bytes < need)
@@ -146,11 +179,11 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (g.ntok == 0)
         return NSA_OK;
     if (mode == SPARSE)
-        NSA_TRY(launch_validate_index(g, idx, &hdr->err, st));
+        NSA_LAUNCH("validate_index", launch_validate_index(g, idx, &hdr->err, st));
     if (tc_supported(g, p->dtype))
-        NSA_TRY(launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, st));
+        NSA_LAUNCH("fwd_tc", launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, st));
     else
-        NSA_TRY(launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
+        NSA_LAUNCH("fwd_simt", launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
     return NSA_OK;
 }
 
@@ -161,11 +194,11 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     if (!g.dense) {
         NSA_TRY(cudaMemsetAsync(counts, 0, sizeof(int) * nbgj, st));
-        NSA_TRY(launch_csr_count(g, idx, counts, &hdr->err, st));
+        NSA_LAUNCH("csr_count", launch_csr_count(g, idx, counts, &hdr->err, st));
     }
-    NSA_TRY(launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
+    NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
     if (!g.dense)
-        NSA_TRY(launch_csr_fill(g, idx, offsets, rows, st));
+        NSA_LAUNCH("csr_fill", launch_csr_fill(g, idx, offsets, rows, st));
     return NSA_OK;
 }
 
@@ -201,17 +234,17 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     if (g.ntok == 0)
         return NSA_OK;
-    NSA_TRY(launch_do_dot(g, o, dO, delta, p->dtype, st));
+    NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
     if ((s = build_csr(g, idx, counts, offsets, rows, units, nchunk, slot, hdr, L.chunk, st)) != NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
-        NSA_TRY(launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, hdr, L.max_units,
+        NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, hdr, L.max_units,
                                partials, dk, dv, &hdr->err, st));
-        NSA_TRY(launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
-        NSA_TRY(launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, st));
+        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
+        NSA_LAUNCH("dq_tc", launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, st));
     } else {
-        NSA_TRY(launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
-        NSA_TRY(launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));
+        NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
+        NSA_LAUNCH("dq_simt", launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));
     }
     return NSA_OK;
 }
@@ -378,6 +411,46 @@ const char *nsa_status_string(int32_t s)
     case NSA_ERR_WORKSPACE: return "NSA_ERR_WORKSPACE";
     default: return "NSA_ERR_UNKNOWN";
     }
+}
+
+nsa_status nsa_trace_enable(int32_t max_records)
+{
+    if (g_trace) {
+        for (int i = 0; i < g_trace_cap; ++i) {
+            cudaEventDestroy(g_trace[i].start);
+            cudaEventDestroy(g_trace[i].stop);
+        }
+        delete[] g_trace;
+        g_trace = nullptr;
+        g_trace_cap = g_trace_n = 0;
+    }
+    if (max_records <= 0)
+        return NSA_OK;
+    g_trace = new TraceRec[max_records];
+    for (int i = 0; i < max_records; ++i) {
+        g_trace[i].name = "";
+        if (cudaEventCreate(&g_trace[i].start) != cudaSuccess || cudaEventCreate(&g_trace[i].stop) != cudaSuccess)
+            return NSA_ERR_CUDA;
+    }
+    g_trace_cap = max_records;
+    g_trace_n = 0;
+    return NSA_OK;
+}
+
+void nsa_trace_reset(void) { g_trace_n = 0; }
+
+int32_t nsa_trace_count(void) { return g_trace_n; }
+
+nsa_status nsa_trace_get(int32_t i, const char **name, float *ms)
+{
+    if (!g_trace || i < 0 || i >= g_trace_n || !name || !ms)
+        return NSA_ERR_INVALID_ARG;
+    if (cudaEventSynchronize(g_trace[i].stop) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    if (cudaEventElapsedTime(ms, g_trace[i].start, g_trace[i].stop) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    *name = g_trace[i].name;
+    return NSA_OK;
 }
 
 nsa_status nsa_count_pairs(const nsa_problem *p, const int32_t *cu_seqlens,

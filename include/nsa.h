@@ -184,6 +184,20 @@ const char *nsa_status_string(int32_t status);
 nsa_status nsa_count_pairs(const nsa_problem *p, const int32_t *cu_seqlens,
                            const int32_t *block_idx, int64_t *out_pairs, void *stream);
 
+/*
+ * Per-kernel timing (instrumentation, off by default).  nsa_trace_enable(n)
+ * creates n pairs of CUDA events (n <= 0 destroys them and turns timing
+ * off); while on, every kernel an entry point launches is bracketed by an
+ * event pair on the call's stream, until n launches have been recorded.
+ * nsa_trace_get(i, ...) waits for launch i to finish and returns the kernel
+ * name (static string) and its duration in milliseconds.  Not thread-safe:
+ * use from one host thread.
+ */
+nsa_status nsa_trace_enable(int32_t max_records);
+void nsa_trace_reset(void);
+int32_t nsa_trace_count(void);
+nsa_status nsa_trace_get(int32_t i, const char **name, float *ms);
+
 #ifdef __cplusplus
 }
 #endif
