@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of the NSA block-selection attention hot path on GB300.
+
+One step = one pass of the whole path over the workload: the selection
+forward (O, LSE) and the backward (do_dot, inverse index, dK/dV, dQ), all
+through the C ABI of libnsa.so.  The headline metric is the backward's
+effective throughput: 10 * D FLOP per (query row, attended key) pair summed
+over query heads (5 matmuls x 2 D), selected blocks only, divided by the time
+of the whole nsa_sel_bwd call.
+
+Workload: B=1, Hq=32, Hkv=2 (G=16), T=8192, D=128, block_size=64, S=16, bf16,
+q/k/v/dO ~ N(0,1), each token selecting its own causal block plus 15 earlier
+blocks drawn uniformly (seeded), as produced by
+block_sparse_attention_do_gb300.inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica (its own seed) of the
+workload on its own GPU: the problems share nothing, so there is no
+collective on the data path (weak scaling); rank 0 prints one JSON line.
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NSA-selection bwd effective TFLOP/s (selected blocks only) and % of bf16 tensor peak"
+WORKLOAD = dict(B=1, Hq=32, Hkv=2, T=8192, D=128, block_size=64, S=16)
+WORKLOAD_NAME = ("NSA selection fwd+bwd, bf16: B=1 Hq=32 Hkv=2 (G=16) T=8192 D=128 "
+                 "block_size=64 S=16, own block + 15 uniform earlier blocks per token")
+# FLOP per selected (query row, key) pair of each kernel's algorithmic work
+ALG_FLOP_PER_PAIR_PER_D = {"dkdv_tc": 8, "dq_tc": 6, "fwd_tc": 4,
+                           "dkdv_simt": 8, "dq_simt": 6, "fwd_simt": 4}
+FLUSH_BYTES = 256 << 20  # > the 129 MB L2
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def aggregate(local_time_ms: float, local_flop: float, device=None):
+    """Max of the time and sum of the work over ranks (identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_time_ms, local_flop
+    t = torch.tensor([local_time_ms], dtype=torch.float64, device=device)
+    w = torch.tensor([local_flop], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed loop runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[3:8]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names[1:], flags[1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def kernel_source_hash(name: str) -> str:
+    files = {"dkdv_tc": "k_tc_dkdv.cu", "dq_tc": "k_tc_dq.cu", "fwd_tc": "k_tc_fwd.cu"}
+    f = files.get(name)
+    if f is None:
+        return ""
+    with open(os.path.join(ROOT, "block_sparse_attention_do_gb300", "csrc", f), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def traffic_for(name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e or e.get("source_sha") != kernel_source_hash(name):
+        return None
+    return e.get("bytes_per_launch_full")
+
+
+def cpu_baseline_oracle(heads: int, T_prefix: int | None = None):
+    """Time the fp64 oracle's backward on a bounded sample of the workload:
+    kv group 0 of batch 0 with its first `heads` query heads (a self-contained
+    sub-problem of the same selection), optionally the first T_prefix tokens."""
+    import torch
+
+    import oracle
+    from block_sparse_attention_do_gb300 import inputs
+
+    W = WORKLOAD
+    T = W["T"] if T_prefix is None else T_prefix
+    q, k, v, do = inputs.make_qkv_do(W["B"], W["Hq"], W["Hkv"], W["T"], W["D"], dtype=torch.bfloat16,
+                                     seed=0)
+    idx = inputs.make_block_idx(W["B"], W["Hkv"], W["T"], W["block_size"], W["S"], seed=0)
+    q, do = q[:, :heads, :T], do[:, :heads, :T]
+    k, v, idx = k[:, :1, :T], v[:, :1, :T], idx[:, :1, :T]
+    pairs = oracle.count_pairs(idx, heads, W["block_size"])
+    t0 = time.perf_counter()
+    oracle.sel_bwd(q, k, v, idx, do, W["block_size"])
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    return dict(seconds=dt, pairs=pairs, flop=10 * W["D"] * pairs, cores=cores,
+                sample=f"kv group 0, query heads 0..{heads - 1}, tokens 0..{T - 1} "
+                       f"({pairs} pairs; fp64 backward incl. its forward recompute)")
+
+
+def prefix_pairs(T_prefix: int) -> int:
+    """Selected pairs of query head 0, kv group 0 over the first T_prefix tokens."""
+    import oracle
+    from block_sparse_attention_do_gb300 import inputs
+
+    W = WORKLOAD
+    idx = inputs.make_block_idx(W["B"], W["Hkv"], W["T"], W["block_size"], W["S"], seed=0)
+    return oracle.count_pairs(idx[:, :1, :T_prefix], 1, W["block_size"])
+
+
+def run_reference(args):
+    rank, _, world = env_rank()
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    # size one step's sample so that warm-up + steps take about 150 s: time
+    # a 1024-token prefix once, then take the longest prefix that fits
+    budget = min(12.0, 150.0 / (args.steps + args.warmup))
+    cal = cpu_baseline_oracle(1, 1024)
+    rate = cal["pairs"] / cal["seconds"]
+    T_prefix = 1024
+    while T_prefix < WORKLOAD["T"] and prefix_pairs(2 * T_prefix) <= budget * rate:
+        T_prefix *= 2
+    T_prefix = min(T_prefix, WORKLOAD["T"])
+    for _ in range(max(0, args.warmup - 1)):
+        cpu_baseline_oracle(1, T_prefix)
+    secs, flop = 0.0, 0.0
+    last = None
+    for _ in range(args.steps):
+        r = cpu_baseline_oracle(1, T_prefix)
+        secs += r["seconds"]
+        flop += r["flop"]
+        last = r
+    value = flop / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = env_rank()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from block_sparse_attention_do_gb300 import api, build, inputs
+
+    build.build()
+    W = WORKLOAD
+    B, Hq, Hkv, T, D, bs, S = (W[k] for k in ("B", "Hq", "Hkv", "T", "D", "block_size", "S"))
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=rank)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=rank)
+    q, k, v, do, idx = (x.to(dev) for x in (q, k, v, do, idx))
+    pairs = api.count_pairs(idx, Hq, bs)
+    bwd_flop = 10.0 * D * pairs
+
+    p = api.problem_from(q, k, bs, S)
+    ws_f = torch.empty(api.fwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(api.bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+
+    def step():
+        o, lse = api.sel_fwd(q, k, v, idx, bs, ws=ws_f)
+        return o, lse
+
+    for _ in range(args.warmup):
+        o, lse = step()
+        api.sel_bwd(q, k, v, o, do, lse, idx, bs, ws=ws_b, out=outs)
+    torch.cuda.synchronize()
+    if api.get_error(ws_b) != 0 or api.get_error(ws_f) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    api.trace_enable(K * 16)
+    api.trace_reset()
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        ev[i][0].record(st)
+        o, lse = api.sel_fwd(q, k, v, idx, bs, ws=ws_f)
+        ev[i][1].record(st)
+        api.sel_bwd(q, k, v, o, do, lse, idx, bs, ws=ws_b, out=outs)
+        ev[i][2].record(st)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+    recs = api.trace_records()
+    api.trace_enable(0)
+    err = api.get_error(ws_b) or api.get_error(ws_f)
+    if err:
+        raise RuntimeError(f"device error status {err} in the timed loop")
+
+    bwd_ms_max, flop_all = aggregate(bwd_ms, bwd_flop * K, dev)
+    step_ms_max, _ = aggregate(step_ms, 0.0, dev)
+    value = flop_all / (bwd_ms_max * 1e-3) / 1e12
+
+    # ---- per-kernel breakdown and roofline of the dominant kernel
+    kern = {}
+    for name, ms in recs:
+        e = kern.setdefault(name, {"ms_total": 0.0, "launches": 0})
+        e["ms_total"] += ms
+        e["launches"] += 1
+    total_k = sum(e["ms_total"] for e in kern.values()) or 1.0
+    for name, e in kern.items():
+        e["ms_avg"] = e["ms_total"] / e["launches"]
+        e["share"] = e["ms_total"] / total_k
+    peaks, peak_src = load_peaks()
+    dom = max(kern, key=lambda n: kern[n]["ms_total"])
+    roof = None
+    if dom in ALG_FLOP_PER_PAIR_PER_D:
+        alg = ALG_FLOP_PER_PAIR_PER_D[dom] * D * pairs
+        ach = alg / (kern[dom]["ms_avg"] * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic_for(dom),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                "algorithmic_flop_per_launch": alg}
+    pct = value / float(peaks["bf16_tflops"])
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if True:  # every rank: the aggregation below is collective
+        o, lse = step()
+        torch.cuda.synchronize()
+        host_in = [x.cpu().pin_memory() for x in (q, k, v, o, do, lse, idx)]
+        dev_in = [torch.empty_like(x, device=dev) for x in host_in]
+        host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        n_e2e = max(3, min(K, 20))
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_e2e + 2)]
+        for i in range(n_e2e + 2):
+            e_ev[i][0].record(st)
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            dq_, dk_, dv_ = api.sel_bwd(*dev_in[:6], dev_in[6], bs, ws=ws_b, out=outs)
+            for dsrc, hdst in zip(outs, host_out):
+                hdst.copy_(dsrc, non_blocking=True)
+            e_ev[i][1].record(st)
+        torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in e_ev[2:])  # first two are warm-up
+        e_ms_max, e_flop = aggregate(e_ms, bwd_flop * n_e2e, dev)
+        e2e = {"value": e_flop / (e_ms_max * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e2e,
+               "scope": "H2D of the backward's inputs (q,k,v,o,dO,lse,idx) from pinned memory, "
+                        "nsa_sel_bwd, D2H of dq,dk,dv to pinned memory"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = cpu_baseline_oracle(args.cpu_heads)
+        cpu = {"value": r["flop"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"], "seconds": r["seconds"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_ms_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "pairs": pairs,
+                       "bwd_flop_per_step": bwd_flop,
+                       "l2": "flushed between steps (256 MiB write outside the timed events); "
+                             "the bwd also reads 192 MiB of q/o/dO, more than L2",
+                       "parallelism": f"replicas x{world} (independent problems, no collective)"},
+            "pct_of_bf16_peak": pct,
+            "bwd_ms": bwd_ms / K, "fwd_ms": fwd_ms / K, "wall_s": t_wall,
+            "kernels": {n: {"ms_avg": e["ms_avg"], "launches": e["launches"], "share": e["share"]}
+                        for n, e in sorted(kern.items(), key=lambda kv: -kv[1]["ms_total"])},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": len(recs),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-heads", type=int, default=4, help="query heads in the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
