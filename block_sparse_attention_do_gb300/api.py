@@ -28,7 +28,7 @@ SYMBOLS = (
     "nsa_dense_causal_fwd", "nsa_dense_causal_bwd", "nsa_sel_varlen_fwd", "nsa_sel_varlen_bwd",
     "nsa_do_dot", "nsa_inverse_index_offsets_len", "nsa_build_inverse_index", "nsa_get_error",
     "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
-    "nsa_trace_count", "nsa_trace_get",
+    "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
 )
 
 
@@ -75,6 +75,7 @@ def lib() -> C.CDLL:
         L.nsa_status_string.restype = C.c_char_p
         L.nsa_status_string.argtypes = [C.c_int32]
         L.nsa_count_pairs.argtypes = [pp] + [_P] * 3 + [_P]
+        L.nsa_build_inverse_index_noalloc.argtypes = [pp] + [_P] * 5 + [_P]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []

@@ -251,6 +251,38 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 
 }  // namespace
 
+// ---- scratch for nsa_build_inverse_index_noalloc --------------------------
+// Some callers cannot allocate device memory at call time (see include/nsa.h),
+// so this one entry point keeps its scratch in a fixed array that every GPU
+// loading the library holds until the process exits.
+constexpr size_t kNoallocScratchBytes = (size_t)2 << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char nsa_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+
+// Device address of nsa_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name only stands in for the symbol;
+// handing it to a kernel directly would use the wrong memory.
+nsa_status noalloc_scratch_address(void **out)
+{
+    static void *addr[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NSA_ERR_CUDA;
+    if (dev < 0 || dev >= 128)
+        return NSA_ERR_UNSUPPORTED;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, nsa_noalloc_scratch) != cudaSuccess || !p)
+            return NSA_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return NSA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t nsa_fwd_workspace_size(const nsa_problem *p)
@@ -379,6 +411,46 @@ nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqle
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     return build_csr(g, block_idx, (int *)(w8 + L.counts), offsets, rows, (Unit *)(w8 + L.units),
                      (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, L.chunk, st);
+}
+
+nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *cu_seqlens,
+                                           const int32_t *block_idx, int32_t *offsets,
+                                           int32_t *rows, int32_t *status_out, void *stream)
+{
+    Geo g;
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    nsa_status s = make_geo(p, thd, SPARSE, cu_seqlens, g);
+    if (s != NSA_OK)
+        return s;
+    if (!block_idx || !offsets || !rows)
+        return NSA_ERR_INVALID_ARG;
+    // scratch plan: header | counts | unit list | chunks per block | partial slots
+    const BwdWs L = bwd_layout(g, p->dtype);
+    const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
+    const size_t off_counts = kAlign;
+    const size_t off_units = align_up(off_counts + sizeof(int) * nbgj);
+    const size_t off_nchunk = align_up(off_units + sizeof(Unit) * (size_t)L.max_units);
+    const size_t off_slot = align_up(off_nchunk + sizeof(int) * nbgj);
+    const size_t need = align_up(off_slot + sizeof(int) * nbgj);
+    if (need > kNoallocScratchBytes)
+        return NSA_ERR_UNSUPPORTED;
+    void *base = nullptr;
+    if ((s = noalloc_scratch_address(&base)) != NSA_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *w8 = (char *)base;
+    WsHeader *hdr = (WsHeader *)base;
+    // the array keeps the previous call's contents: clear the error word here;
+    // build_csr zeroes the per-block counts itself
+    NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+    if ((s = build_csr(g, block_idx, (int *)(w8 + off_counts), offsets, rows, (Unit *)(w8 + off_units),
+                       (int *)(w8 + off_nchunk), (int *)(w8 + off_slot), hdr, L.chunk, st)) != NSA_OK)
+        return s;
+    if (status_out)
+        NSA_TRY(cudaMemcpyAsync(status_out, &hdr->err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    return NSA_OK;
 }
 
 nsa_status nsa_get_error(void *ws, void *stream, int32_t *out)

@@ -169,6 +169,32 @@ nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqle
                                    void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * nsa_build_inverse_index without a caller workspace.  The pages describe
+ * nothing like it; it exists for callers that cannot allocate device memory
+ * when they call in -- for example a runtime whose memory is carved up once
+ * at start-up and may not grow afterwards, or code running where a
+ * cudaMalloc would stall or break the surrounding stream schedule.  Same
+ * arguments and results as nsa_build_inverse_index, except:
+ *  - the scratch is a 2 MiB array inside the library (every GPU that loads
+ *    the library holds it until the process exits).  A problem whose
+ *    scratch would not fit -- 256 + 12 * B*Hkv*ceil(T/block_size) bytes plus
+ *    32 bytes per dK/dV work unit, each part rounded up to 256 bytes --
+ *    returns NSA_ERR_UNSUPPORTED before any launch;
+ *  - the first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before
+ *    any stream capture;
+ *  - every call uses the same array and the call clears what must start at
+ *    zero, so calls that can overlap on the GPU (other streams, other host
+ *    threads) race and must not be issued;
+ *  - device-side index errors are copied into *status_out (device int32,
+ *    may be NULL) on `stream` instead of a workspace error word.
+ * Nothing is allocated or freed.
+ */
+nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *cu_seqlens,
+                                           const int32_t *block_idx, int32_t *offsets,
+                                           int32_t *rows, int32_t *status_out, void *stream);
+
+/*
  * Reads the device error word of a workspace used by the calls above,
  * after synchronising `stream`, into *out (an nsa_status value), and clears
  * it.  Returns NSA_ERR_CUDA if the read itself fails.
