@@ -131,23 +131,60 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
 
     if (warp < 2) {
         // ------------------------------------------------------------ loader
+        // Each of the 64 loader threads owns tile rows pt and pt + 64: it
+        // resolves their token (inverse-index list) and LSE/delta one tile
+        // ahead, into registers, while the stage it will fill is still busy.
         const int pt = threadIdx.x;  // 0..63
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
         int it = 0, uc = 0;
         int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
-        bool ok = true;
         if (pt == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_do);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        for (int ui = blockIdx.x; ui < n_units && ok; ui += gridDim.x, ++uc) {
-            const Unit u = p.units[ui];
-            const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
-            if (pt == 0) {
-                ok = mbar_wait(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag);
-                if (ok) {
+        int ui = blockIdx.x, ti = 0;
+        Unit u;
+        int b = 0, kvh = 0, csr0 = 0, ntiles = 0;
+        auto load_unit = [&]() {
+            u = p.units[ui];
+            b = u.bg / g.Hkv;
+            kvh = u.bg % g.Hkv;
+            csr0 = g.dense ? 0 : p.offsets[u.bg * g.nbmax + u.j] + u.begin;
+            ntiles = (u.count + Tt - 1) / Tt;
+        };
+        int tok_r[2];
+        float l2_r[2], dl_r[2];
+        auto fetch = [&]() {
+            const int ntok = min(Tt, u.count - ti * Tt);
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int r = pt + k2 * kProdThreads;
+                const int tl = r / G, hh = r % G;
+                tok_r[k2] = -1;
+                l2_r[k2] = 0.f;
+                dl_r[k2] = 0.f;
+                if (r < nrows && tl < ntok) {
+                    const int pos = ti * Tt + tl;
+                    const int t = g.dense ? u.j * g.bs + u.begin + pos : p.rows[csr0 + pos];
+                    const int64_t so = stat_off(g, b, kvh * G + hh, t);
+                    tok_r[k2] = t;
+                    l2_r[k2] = p.lse[so] * 1.4426950408889634f;
+                    dl_r[k2] = p.delta[so];
+                }
+            }
+        };
+        if (ui < n_units) {
+            load_unit();
+            fetch();
+        }
+        while (ui < n_units) {
+            const int st = it & 1;
+            bool okl = !*abort_flag;
+            if (okl && ti == 0 && pt == 0) {
+                okl = mbar_wait(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag);
+                if (okl) {
                     last_kv = uc;
                     mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
                     for (int h = 0; h < 2; ++h) {
@@ -164,79 +201,77 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     }
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp 0 only; warp 1 follows below
-            const int ntiles = (u.count + Tt - 1) / Tt;
-            for (int ti = 0; ti < ntiles && !*abort_flag; ++ti, ++it) {
-                const int st = it & 1;
-                if (!mbar_wait(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
+            if (okl)
+                okl = mbar_wait(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag);
+            if (okl) {
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int r = pt + k2 * kProdThreads;
+                    lse_s[st * kRows + r] = l2_r[k2];
+                    dlt_s[st * kRows + r] = dl_r[k2];
+                    if (r % G == 0 && r / G < Tt)
+                        tok_s[st * kRows + r / G] = tok_r[k2];
                 }
-                const int ntok = min(Tt, u.count - ti * Tt);
-                // token ids, LSE and delta for the tile's rows (generic stores)
-                for (int tl = pt; tl < kRows; tl += kProdThreads)
-                    tok_s[st * kRows + tl] = tl < ntok ? unit_token(p, u, ti * Tt + tl) : -1;
-                for (int r = pt; r < kRows; r += kProdThreads) {
-                    const int tl = r / G, hh = r % G;
-                    float l2 = 0.f, dl = 0.f;
-                    if (r < nrows && tl < ntok) {
-                        const int t = unit_token(p, u, ti * Tt + tl);
-                        const int64_t so = stat_off(g, b, kvh * G + hh, t);
-                        l2 = p.lse[so] * 1.4426950408889634f;
-                        dl = p.delta[so];
-                    }
-                    lse_s[st * kRows + r] = l2;
-                    dlt_s[st * kRows + r] = dl;
-                }
-                if (GATHER_TMA) {
-                    if (pt == 0) {
-                        last_tile = it;
-                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
-                        for (int tl = 0; tl < Tt; ++tl) {
-                            // rows past the list repeat the last token (finite data, P = 0)
-                            const int t = unit_token(p, u, ti * Tt + min(tl, ntok - 1));
-                            uint8_t *qd = sm + OFF_Q + st * kTileBytes + tl * G * 128;
-                            uint8_t *od = sm + OFF_DO + st * kTileBytes + tl * G * 128;
-                            for (int h = 0; h < 2; ++h) {
-                                if (g.thd) {
-                                    tma_load_3d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, kvh * G,
-                                                g.cu[b] + t);
-                                    tma_load_3d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, kvh * G,
-                                                g.cu[b] + t);
-                                } else {
-                                    tma_load_4d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
-                                    tma_load_4d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
-                                }
+            }
+            // all 64 loader threads agree to go on (and see each other's stores)
+            if (named_bar_any(2, kProdThreads, !okl))
+                break;
+            const int ntok = min(Tt, u.count - ti * Tt);
+            if (GATHER_TMA) {
+                if (pt == 0) {
+                    last_tile = it;
+                    mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
+                    for (int tl = 0; tl < Tt; ++tl) {
+                        // rows past the list repeat the last token (finite data, P = 0)
+                        const int t = tok_s[st * kRows + min(tl, ntok - 1)];
+                        uint8_t *qd = sm + OFF_Q + st * kTileBytes + tl * G * 128;
+                        uint8_t *od = sm + OFF_DO + st * kTileBytes + tl * G * 128;
+                        for (int h = 0; h < 2; ++h) {
+                            if (g.thd) {
+                                tma_load_3d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, kvh * G,
+                                            g.cu[b] + t);
+                                tma_load_3d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, kvh * G,
+                                            g.cu[b] + t);
+                            } else {
+                                tma_load_4d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
+                                tma_load_4d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
                             }
                         }
                     }
-                    mbar_arrive(&bars[B_FULL0 + st]);
-                } else {
-                    // 2 tensors x 128 rows x 16 chunks of 16 bytes
-                    for (int item = pt; item < 2 * kRows * 16; item += kProdThreads) {
-                        const int tensor = item / (kRows * 16);
-                        const int rem = item % (kRows * 16);
-                        const int r = rem >> 4, c = rem & 15;
-                        const int tl = r / G, hh = r % G;
-                        const bool valid = r < nrows && tl < ntok;
-                        const __nv_bfloat16 *base = tensor ? p.dO : p.q;
-                        const __nv_bfloat16 *src = base;
-                        if (valid) {
-                            const int t = unit_token(p, u, ti * Tt + tl);
-                            src = base + row_off(g, g.Hq, b, kvh * G + hh, t) + c * 8;
-                        }
-                        const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + (c >> 3) * kHalfBytes +
-                                             sw128_off(r, c & 7);
-                        cp_async_16(dst, src, valid ? 16u : 0u);
-                    }
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    fence_async_smem();
-                    mbar_arrive(&bars[B_FULL0 + st]);
                 }
+                mbar_arrive(&bars[B_FULL0 + st]);
+            } else {
+                // 2 tensors x 128 rows x 16 chunks of 16 bytes
+                for (int item = pt; item < 2 * kRows * 16; item += kProdThreads) {
+                    const int tensor = item / (kRows * 16);
+                    const int rem = item % (kRows * 16);
+                    const int r = rem >> 4, c = rem & 15;
+                    const int tl = r / G, hh = r % G;
+                    const bool valid = r < nrows && tl < ntok;
+                    const __nv_bfloat16 *base = tensor ? p.dO : p.q;
+                    const __nv_bfloat16 *src = base;
+                    if (valid)
+                        src = base + row_off(g, g.Hq, b, kvh * G + hh, tok_s[st * kRows + tl]) + c * 8;
+                    const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + (c >> 3) * kHalfBytes +
+                                         sw128_off(r, c & 7);
+                    cp_async_16(dst, src, valid ? 16u : 0u);
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+                fence_async_smem();
+                mbar_arrive(&bars[B_FULL0 + st]);
             }
-            if (!ok)
-                break;
+            // next tile (possibly of the next unit): resolve its rows now
+            ++it;
+            if (++ti == ntiles) {
+                ti = 0;
+                ui += gridDim.x;
+                ++uc;
+                if (ui < n_units)
+                    load_unit();
+            }
+            if (ui < n_units)
+                fetch();
         }
         if (!GATHER_TMA)
             cp_async_wait<0>();
@@ -379,9 +414,9 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 for (int c = 0; c < 64; c += 2) {
                     float p0 = 0.f, p1 = 0.f;
                     if (c <= lim)
-                        p0 = exp2f(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                        p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
                     if (c + 1 <= lim)
-                        p1 = exp2f(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                        p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
                     const float d0 = p0 * (__uint_as_float(dv_[c]) - dl);
                     const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dl);
                     pk[c >> 1] = pack_bf16(p0, p1);

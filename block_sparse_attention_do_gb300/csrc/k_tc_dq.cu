@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             for (int c = 0; c < 64; c += 2) {
                 float p0 = 0.f, p1 = 0.f;
                 if (c <= lim)
-                    p0 = exp2f(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                    p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
                 if (c + 1 <= lim)
-                    p1 = exp2f(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                    p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
                 dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
             }
             if (!mbar_wait_warp(&bars[B_DSFREE0 + s], ((i >> 1) & 1) ^ 1, abort_flag)) {

@@ -252,13 +252,13 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                     mb = fmaxf(mb, x);
             }
             const float mn = fmaxf(m, mb);
-            const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+            const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
             float rs = 0.f;
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
-                const float p0 = (c <= lim) ? exp2f(__uint_as_float(sv[c]) - mn) : 0.f;
-                const float p1 = (c + 1 <= lim) ? exp2f(__uint_as_float(sv[c + 1]) - mn) : 0.f;
+                const float p0 = (c <= lim) ? ex2(__uint_as_float(sv[c]) - mn) : 0.f;
+                const float p1 = (c + 1 <= lim) ? ex2(__uint_as_float(sv[c + 1]) - mn) : 0.f;
                 rs += p0 + p1;
                 pk[c >> 1] = pack_bf16(p0, p1);
             }

@@ -98,6 +98,19 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, v
     return __all_sync(0xffffffffu, ok);
 }
 
+// Named barrier `id` over `count` threads that also ORs a predicate across
+// them: every participant gets the same answer (used to agree on stopping).
+template <int ID, int COUNT> __device__ __forceinline__ bool named_bar_any_t(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(ID), "n"(COUNT)
+                 : "memory");
+    return r != 0;
+}
+#define named_bar_any(ID, COUNT, V) named_bar_any_t<(ID), (COUNT)>(V)
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
                                             int c1, int c2)
@@ -241,6 +254,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c)
 {
     return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+// 2^x by the SFU's approximate exponential (flush-to-zero); its relative
+// error is far below the bf16 rounding that P and dS receive next.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
