@@ -24,15 +24,17 @@ namespace {
 
 using namespace tc;
 
+constexpr int NS = 3;  // K/V stages
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTileBytes;
-constexpr int OFF_KV = OFF_DO + kTileBytes;   // 2 stages x (K | V)
-constexpr int OFF_DS = OFF_KV + 2 * 2 * kKvBytes;  // 2 buffers
+constexpr int OFF_KV = OFF_DO + kTileBytes;   // NS stages x (K | V)
+constexpr int OFF_DS = OFF_KV + NS * 2 * kKvBytes;  // 2 buffers
 constexpr int OFF_MASK = OFF_DS + 2 * kRows * 128;
 constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
 constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
 constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int NUM_BARS = 16;
+constexpr int KVF = 16, KVE = 16 + NS;  // barrier slots of the K/V ring
+constexpr int NUM_BARS = 16 + 2 * NS;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
@@ -89,8 +91,6 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         *abort_flag = 0;
         mbar_init(&bars[B_QFULL], 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_KVFULL0 + s], 1);
-            mbar_init(&bars[B_KVEMPTY0 + s], 1);
             mbar_init(&bars[B_SFULL0 + s], 1);
             mbar_init(&bars[B_SFREE0 + s], kRows);
             mbar_init(&bars[B_DSFULL0 + s], kRows);
@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
         mbar_init(&bars[B_LIST], kRows);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[KVF + s], 1);
+            mbar_init(&bars[KVE + s], 1);
+        }
         fence_barrier_init();
     }
     if (warp == 2) {
@@ -129,6 +133,13 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
                 if (g.thd) {
                     tma_load_3d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
                     tma_load_3d(sm + OFF_DO + h * kHalfBytes, &tm_do, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                } else if (qtile_token_major(g)) {
+                    for (int tl = 0; tl < Tq; ++tl) {
+                        tma_load_4d(sm + OFF_Q + h * kHalfBytes + tl * G * 128, &tm_q, &bars[B_QFULL], h * 64,
+                                    t0 + tl, kvh * G, b);
+                        tma_load_4d(sm + OFF_DO + h * kHalfBytes + tl * G * 128, &tm_do, &bars[B_QFULL], h * 64,
+                                    t0 + tl, kvh * G, b);
+                    }
                 } else {
                     tma_load_4d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, t0, kvh * G, b);
                     tma_load_4d(sm + OFF_DO + h * kHalfBytes, &tm_do, &bars[B_QFULL], h * 64, t0, kvh * G, b);
@@ -138,23 +149,23 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             const int U = ok ? *n_list : 0;
             int last = -1;
             for (int i = 0; i < U && ok; ++i) {
-                const int s = i & 1;
-                if (!mbar_wait(&bars[B_KVEMPTY0 + s], ((i >> 1) & 1) ^ 1, abort_flag))
+                const int s = i % NS;
+                if (!mbar_wait(&bars[KVE + s], ((i / NS) & 1) ^ 1, abort_flag))
                     break;
                 const int j = list[i];
                 uint8_t *kd = sm + OFF_KV + s * 2 * kKvBytes;
                 uint8_t *vd = kd + kKvBytes;
-                mbar_arrive_expect_tx(&bars[B_KVFULL0 + s], 2 * kKvBytes);
+                mbar_arrive_expect_tx(&bars[KVF + s], 2 * kKvBytes);
                 last = i;
                 for (int h = 0; h < 2; ++h) {
                     if (g.thd) {
-                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, kvh,
+                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, kvh,
                                     g.cu[b] + j * kKeys);
-                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, kvh,
+                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, kvh,
                                     g.cu[b] + j * kKeys);
                     } else {
-                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
-                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
+                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
+                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
                     }
                 }
             }
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
             if (*abort_flag && last >= 0)
-                mbar_wait(&bars[B_KVFULL0 + (last & 1)], (last >> 1) & 1, &never);
+                mbar_wait(&bars[KVF + last % NS], (last / NS) & 1, &never);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -180,21 +191,21 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
                 bool progressed = false;
                 if (qi < si && mbar_try_wait(&bars[B_DSFULL0 + (qi & 1)], (qi >> 1) & 1)) {
                     tc_fence_after();
-                    const int s = qi & 1;
-                    const uint32_t k_s = kv_s + s * 2 * kKvBytes;
+                    const int s = qi & 1, ks = qi % NS;
+                    const uint32_t k_s = kv_s + ks * 2 * kKvBytes;
                     for (int kk = 0; kk < kKeys / 16; ++kk)
                         mma_bf16(tmem + TM_DQ, sdesc_sw128(ds_s + s * kRows * 128 + kk * 32, 16, 1024),
                                  sdesc_sw128(k_s + kk * 2048, kKvHalfBytes, 1024), idQ, (qi > 0 || kk > 0));
                     mma_commit(&bars[B_DSFREE0 + s]);
-                    mma_commit(&bars[B_KVEMPTY0 + s]);
+                    mma_commit(&bars[KVE + ks]);
                     ++qi;
                     progressed = true;
                 }
-                if (si < U && si < qi + 2 && mbar_try_wait(&bars[B_KVFULL0 + (si & 1)], (si >> 1) & 1) &&
+                if (si < U && si < qi + 2 && mbar_try_wait(&bars[KVF + si % NS], (si / NS) & 1) &&
                     mbar_try_wait(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1)) {
                     tc_fence_after();
                     const int s = si & 1;
-                    const uint32_t k_s = kv_s + s * 2 * kKvBytes, v_s = k_s + kKvBytes;
+                    const uint32_t k_s = kv_s + (si % NS) * 2 * kKvBytes, v_s = k_s + kKvBytes;
                     const uint32_t d = tmem + TM_S + s * 128;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -266,14 +277,21 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             const bool sel = rvalid && qtile_selects(g, my_mask, t, j);
             const int lim = sel ? t - j * kKeys : -1;
             uint32_t dk_[32];
+            if (__any_sync(0xffffffffu, sel)) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                float p0 = 0.f, p1 = 0.f;
-                if (c <= lim)
-                    p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                if (c + 1 <= lim)
-                    p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
-                dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                for (int c = 0; c < 64; c += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (c <= lim)
+                        p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                    if (c + 1 <= lim)
+                        p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                    dk_[c >> 1] =
+                        pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    dk_[c] = 0u;
             }
             if (!mbar_wait_warp(&bars[B_DSFREE0 + s], ((i >> 1) & 1) ^ 1, abort_flag)) {
                 ok = false;
@@ -332,7 +350,8 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     const int Tq = g.G >= kRows ? 1 : kRows / g.G;
     CUtensorMap tq, tdo, tk, tv;
-    if (!make_tmap(&tq, q, g, g.Hq, Tq, g.G) || !make_tmap(&tdo, dO, g, g.Hq, Tq, g.G) ||
+    const int box_tok = (!g.thd && qtile_token_major(g)) ? 1 : Tq;
+    if (!make_tmap(&tq, q, g, g.Hq, box_tok, g.G) || !make_tmap(&tdo, dO, g, g.Hq, box_tok, g.G) ||
         !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;

@@ -3,12 +3,15 @@
 //
 // Same query tile as the dQ kernel (Tq tokens x G heads = 128 rows) walking
 // the ascending union of the tile's selected blocks.  For block j (step i):
-//   S_i  = Q K_j^T                               (M=128 rows, N=64 keys, K=128)
-//   m_i  = max(m_{i-1}, max of the row's attended scores),  P_i = exp(S_i - m_i)
-//   PV_i = P_i V_j  into a fresh TMEM buffer     (M=128 rows, N=128 dims, K=64)
-//   O    = O * exp(m_{i-1} - m_i) + PV_i         (fp32 registers, one row per thread)
-// so O is rescaled exactly once per block in registers and the MMA for PV_i
-// overlaps the softmax of block i+1.  At the end O /= l, LSE = m + log l.
+//   S_i = Q K_j^T                                (M=128 rows, N=64 keys, K=128)
+//   P_i = exp(S_i - m) on the row's attended keys, l += rowsum(P_i)
+//   O  += P_i V_j   accumulated in TMEM          (M=128 rows, N=128 dims, K=64)
+// m is a running reference that a row raises only when a block's maximum
+// exceeds it by more than 2^8; then that row's O (in TMEM) and l are scaled
+// by exp(m_old - m_new) before the block's P.V is issued.  Every term of O
+// and l carries the same reference, so O / l at the end is exact; P stays
+// below 2^8.  LSE = m + log l.  Warps whose rows all skip block j write
+// zero P without computing it.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -17,14 +20,16 @@ namespace {
 
 using namespace tc;
 
+constexpr int NS = 4;  // K/V stages
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + kTileBytes;          // 2 stages x (K | V)
-constexpr int OFF_P = OFF_KV + 2 * 2 * kKvBytes;     // 2 buffers of [128 rows][64 keys]
+constexpr int OFF_KV = OFF_Q + kTileBytes;          // NS stages x (K | V)
+constexpr int OFF_P = OFF_KV + NS * 2 * kKvBytes;     // 2 buffers of [128 rows][64 keys]
 constexpr int OFF_MASK = OFF_P + 2 * kRows * 128;
 constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
 constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
 constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int NUM_BARS = 16;
+constexpr int KVF = 16, KVE = 16 + NS;  // barrier slots of the K/V ring
+constexpr int NUM_BARS = 16 + 2 * NS;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
@@ -32,11 +37,11 @@ enum {
     B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
     B_PFULL0, B_PFULL1, B_PVFULL0, B_PVFULL1, B_OFREE0, B_OFREE1, B_LIST
 };
-constexpr int B_DONE = 16;  // extra slot (NUM_BARS covers 0..15; DONE uses the misc area)
 
 constexpr uint32_t TM_S = 0;    // buffer b at b*64
-constexpr uint32_t TM_O = 128;  // buffer b at 128 + b*128: 128 lanes (rows) x 128 columns (dims)
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_O = 128;  // 128 lanes (rows) x 128 columns (dims)
+constexpr uint32_t TM_COLS = 256;
+constexpr float kRescaleLog2 = 8.f;  // raise the reference only past a 2^8 growth
 
 struct Params {
     Geo g;
@@ -81,15 +86,16 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         *abort_flag = 0;
         mbar_init(&bars[B_QFULL], 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_KVFULL0 + s], 1);
-            mbar_init(&bars[B_KVEMPTY0 + s], 1);
             mbar_init(&bars[B_SFULL0 + s], 1);
             mbar_init(&bars[B_SFREE0 + s], kRows);
             mbar_init(&bars[B_PFULL0 + s], kRows);
             mbar_init(&bars[B_PVFULL0 + s], 1);
-            mbar_init(&bars[B_OFREE0 + s], kRows);
         }
         mbar_init(&bars[B_LIST], kRows);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars[KVF + s], 1);
+            mbar_init(&bars[KVE + s], 1);
+        }
         mbar_init(done_bar, 1);
         fence_barrier_init();
     }
@@ -119,6 +125,10 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             for (int h = 0; h < 2; ++h) {
                 if (g.thd)
                     tma_load_3d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                else if (qtile_token_major(g))
+                    for (int tl = 0; tl < Tq; ++tl)
+                        tma_load_4d(sm + OFF_Q + h * kHalfBytes + tl * G * 128, &tm_q, &bars[B_QFULL], h * 64,
+                                    t0 + tl, kvh * G, b);
                 else
                     tma_load_4d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, t0, kvh * G, b);
             }
@@ -126,30 +136,30 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             const int U = ok ? *n_list : 0;
             int last = -1;
             for (int i = 0; i < U && ok; ++i) {
-                const int s = i & 1;
-                if (!mbar_wait(&bars[B_KVEMPTY0 + s], ((i >> 1) & 1) ^ 1, abort_flag))
+                const int s = i % NS;
+                if (!mbar_wait(&bars[KVE + s], ((i / NS) & 1) ^ 1, abort_flag))
                     break;
                 const int j = list[i];
                 uint8_t *kd = sm + OFF_KV + s * 2 * kKvBytes;
                 uint8_t *vd = kd + kKvBytes;
-                mbar_arrive_expect_tx(&bars[B_KVFULL0 + s], 2 * kKvBytes);
+                mbar_arrive_expect_tx(&bars[KVF + s], 2 * kKvBytes);
                 last = i;
                 for (int h = 0; h < 2; ++h) {
                     if (g.thd) {
-                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, kvh,
+                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, kvh,
                                     g.cu[b] + j * kKeys);
-                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, kvh,
+                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, kvh,
                                     g.cu[b] + j * kKeys);
                     } else {
-                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
-                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL0 + s], h * 64, j * kKeys, kvh, b);
+                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
+                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
                     }
                 }
             }
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
             if (*abort_flag && last >= 0)
-                mbar_wait(&bars[B_KVFULL0 + (last & 1)], (last >> 1) & 1, &never);
+                mbar_wait(&bars[KVF + last % NS], (last / NS) & 1, &never);
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -164,24 +174,23 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             uint64_t t_last = globaltimer();
             while (ok && oi < U && !*abort_flag) {
                 bool progressed = false;
-                if (oi < si && mbar_try_wait(&bars[B_PFULL0 + (oi & 1)], (oi >> 1) & 1) &&
-                    mbar_try_wait(&bars[B_OFREE0 + (oi & 1)], ((oi >> 1) & 1) ^ 1)) {
+                if (oi < si && mbar_try_wait(&bars[B_PFULL0 + (oi & 1)], (oi >> 1) & 1)) {
                     tc_fence_after();
-                    const int s = oi & 1;
-                    const uint32_t v_s = kv_s + s * 2 * kKvBytes + kKvBytes;
+                    const int s = oi & 1, ks = oi % NS;
+                    const uint32_t v_s = kv_s + ks * 2 * kKvBytes + kKvBytes;
                     for (int kk = 0; kk < kKeys / 16; ++kk)
-                        mma_bf16(tmem + TM_O + s * 128, sdesc_sw128(p_s + s * kRows * 128 + kk * 32, 16, 1024),
-                                 sdesc_sw128(v_s + kk * 2048, kKvHalfBytes, 1024), idO, kk > 0);
+                        mma_bf16(tmem + TM_O, sdesc_sw128(p_s + s * kRows * 128 + kk * 32, 16, 1024),
+                                 sdesc_sw128(v_s + kk * 2048, kKvHalfBytes, 1024), idO, (oi > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&bars[B_PVFULL0 + s]);
-                    mma_commit(&bars[B_KVEMPTY0 + s]);
+                    mma_commit(&bars[KVE + ks]);
                     ++oi;
                     progressed = true;
                 }
-                if (si < U && si < oi + 2 && mbar_try_wait(&bars[B_KVFULL0 + (si & 1)], (si >> 1) & 1) &&
+                if (si < U && si < oi + 2 && mbar_try_wait(&bars[KVF + si % NS], (si / NS) & 1) &&
                     mbar_try_wait(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1)) {
                     tc_fence_after();
                     const int s = si & 1;
-                    const uint32_t k_s = kv_s + s * 2 * kKvBytes;
+                    const uint32_t k_s = kv_s + (si % NS) * 2 * kKvBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
@@ -220,11 +229,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t p_row = smem_u32(sm + OFF_P) + r * 128;
         const uint32_t *my_mask = mask + (rvalid ? tl : 0) * words;
-        float o[128];
-#pragma unroll
-        for (int e = 0; e < 128; ++e)
-            o[e] = 0.f;
-        float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+        float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int i = 0; i < U; ++i) {
             const int s = i & 1;
@@ -243,55 +248,69 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             const int j = list[i];
             const bool sel = rvalid && qtile_selects(g, my_mask, t, j);
             const int lim = sel ? t - j * kKeys : -1;
-            float mb = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float x = __uint_as_float(sv[c]) * g.scale_l2;
-                sv[c] = __float_as_uint(x);
-                if (c <= lim)
-                    mb = fmaxf(mb, x);
-            }
-            const float mn = fmaxf(m, mb);
-            const float alpha = (m == -INFINITY) ? 0.f : ex2(m - mn);
-            float rs = 0.f;
             uint32_t pk[32];
+            if (__any_sync(0xffffffffu, sel)) {
+                float mb = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                const float p0 = (c <= lim) ? ex2(__uint_as_float(sv[c]) - mn) : 0.f;
-                const float p1 = (c + 1 <= lim) ? ex2(__uint_as_float(sv[c + 1]) - mn) : 0.f;
-                rs += p0 + p1;
-                pk[c >> 1] = pack_bf16(p0, p1);
-            }
-            l = l * alpha + rs;
-            m = mn;
-            // fold PV of the previous block into O (this also frees P buffer s)
-            if (i > 0) {
-                const int sp = (i - 1) & 1;
-                if (!mbar_wait_warp(&bars[B_PVFULL0 + sp], ((i - 1) >> 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
+                for (int c = 0; c < 64; ++c) {
+                    const float x = __uint_as_float(sv[c]) * g.scale_l2;
+                    sv[c] = __float_as_uint(x);
+                    if (c <= lim)
+                        mb = fmaxf(mb, x);
                 }
-                tc_fence_after();
+                const bool raise = mb > m + kRescaleLog2;
+                if (__any_sync(0xffffffffu, raise)) {
+                    // O must hold every earlier block before it is rescaled
+                    if (i > 0 && !mbar_wait_warp(&bars[B_PVFULL0 + ((i - 1) & 1)], ((i - 1) >> 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float alpha = raise ? ex2(m - mb) : 1.f;  // 0 when m = -inf
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t a[16];
-                    tmem_ld16(lane_base + TM_O + sp * 128 + c * 16, a);
-                    tmem_wait_ld();
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t a[16];
+                        tmem_ld16(lane_base + TM_O + c * 16, a);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        o[c * 16 + e] = fmaf(o[c * 16 + e], alpha_prev, __uint_as_float(a[e]));
+                        for (int e = 0; e < 16; ++e)
+                            a[e] = __float_as_uint(__uint_as_float(a[e]) * alpha);
+                        tmem_st16(lane_base + TM_O + c * 16, a);
+                    }
+                    tmem_wait_st();
+                    if (raise) {
+                        l *= alpha;
+                        m = mb;
+                    }
                 }
-                tc_fence_before();
-                mbar_arrive(&bars[B_OFREE0 + sp]);
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const float p0 = (c <= lim) ? ex2(__uint_as_float(sv[c]) - m) : 0.f;
+                    const float p1 = (c + 1 <= lim) ? ex2(__uint_as_float(sv[c + 1]) - m) : 0.f;
+                    rs += p0 + p1;
+                    pk[c >> 1] = pack_bf16(p0, p1);
+                }
+                l += rs;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    pk[c] = 0u;
             }
-            alpha_prev = alpha;
+            // P buffer s was last read by the P.V of block i - 2
+            if (i >= 2 && !mbar_wait_warp(&bars[B_PVFULL0 + s], ((i >> 1) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 st_shared_v4(p_row + s * kRows * 128 + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1],
                              pk[4 * c + 2], pk[4 * c + 3]);
             fence_async_smem();
+            tc_fence_before();
             mbar_arrive(&bars[B_PFULL0 + s]);
         }
+        float o[128];
         if (ok && U > 0) {
             const int sp = (U - 1) & 1;
             if (!mbar_wait_warp(&bars[B_PVFULL0 + sp], ((U - 1) >> 1) & 1, abort_flag)) {
@@ -301,13 +320,17 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t a[16];
-                    tmem_ld16(lane_base + TM_O + sp * 128 + c * 16, a);
+                    tmem_ld16(lane_base + TM_O + c * 16, a);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        o[c * 16 + e] = fmaf(o[c * 16 + e], alpha_prev, __uint_as_float(a[e]));
+                        o[c * 16 + e] = __uint_as_float(a[e]);
                 }
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+                o[e] = 0.f;
         }
         if (ok && rvalid) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -343,7 +366,8 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
     CUtensorMap tq, tk, tv;
-    if (!make_tmap(&tq, q, g, g.Hq, Tq, g.G) || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) ||
+    const int box_tok = (!g.thd && qtile_token_major(g)) ? 1 : Tq;
+    if (!make_tmap(&tq, q, g, g.Hq, box_tok, g.G) || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) ||
         !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;

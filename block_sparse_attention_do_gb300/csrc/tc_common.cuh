@@ -43,12 +43,16 @@ inline bool qtile_shape_ok(const Geo &g)
     return g.nbmax <= MAX_BLOCKS && tile_tokens(g.G) * ((g.nbmax + 31) / 32) <= MASK_WORDS;
 }
 
-// tile row -> (token within tile, head within group).  The TMA box of a
-// tile is {64, Tq tokens, G heads} for BHTD (rows head-major) and
-// {64, G heads, Tq tokens} for THD (rows token-major).
+// Rows of a tile are token-major (row = token * G + head) for THD and, when
+// G % 8 == 0, for BHTD too (one TMA box of G heads per token, 1024-byte
+// aligned); otherwise BHTD rows are head-major (one box {64, Tq, G}).
+// Token-major rows let a whole warp skip a block none of its tokens chose.
+__host__ __device__ inline bool qtile_token_major(const Geo &g) { return g.thd || (g.G % 8) == 0; }
+
+// tile row -> (token within tile, head within group)
 __device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, int &hh)
 {
-    if (g.thd) {
+    if (qtile_token_major(g)) {
         tl = r / g.G;
         hh = r % g.G;
     } else {

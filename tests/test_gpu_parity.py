@@ -64,6 +64,8 @@ SMALL = [
     (2, 6, 2, 200, 64, 32, 8),    # G=3, S above the valid count for early rows
     (1, 4, 1, 150, 128, 64, 3),   # G=4, D=128, bs=64, ragged
     (1, 16, 1, 256, 128, 64, 4),  # G=16
+    (1, 32, 1, 300, 128, 64, 5),  # G=32, ragged
+    (2, 32, 2, 200, 128, 64, 3),  # G=16, two kv heads, batch 2
 ]
 
 
@@ -97,6 +99,27 @@ def test_padding_anywhere_and_empty_rows(dtype):
     _compare(got, ref, dtype)
 
 
+def test_padding_and_empty_rows_tensor_core_shapes():
+    """The bf16 tensor-core kernels (D=128, block 64, G=16) on -1 slots anywhere,
+    rows with no selected block and rows holding only an earlier block."""
+    B, Hq, Hkv, T, D, bs, S = 1, 32, 2, 320, 128, 64, 4
+    dtype = torch.bfloat16
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=15)
+    a = inputs.make_block_idx(B, Hkv, T, bs, S, seed=15).numpy()
+    rng = np.random.default_rng(1)
+    for g in range(Hkv):
+        for t in range(T):
+            a[0, g, t] = a[0, g, t][rng.permutation(S)]
+    a[0, 0, 200] = -1
+    a[0, 1, 7] = -1
+    a[0, 1, 300, :] = -1
+    a[0, 1, 300, 3] = 2
+    idx = torch.from_numpy(a)
+    got = _run(q, k, v, do, idx, bs)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, dtype)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_dense_causal(dtype):
     B, Hq, Hkv, T, D, bs = 2, 8, 2, 200, 128, 64
@@ -107,10 +130,10 @@ def test_dense_causal(dtype):
     _compare(got, ref, dtype)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_varlen(dtype):
+@pytest.mark.parametrize("dtype,Hq", [(torch.float32, 8), (torch.bfloat16, 8), (torch.bfloat16, 32)])
+def test_varlen(dtype, Hq):
     lengths = [130, 1, 64, 257, 90]
-    Hq, Hkv, D, bs, S = 8, 2, 128, 64, 3
+    Hkv, D, bs, S = 2, 128, 64, 3
     total = sum(lengths)
     cu = inputs.cu_seqlens_from_lengths(lengths)
     q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=dtype, seed=3, layout="thd")
