@@ -344,6 +344,123 @@ __global__ void __launch_bounds__(kThreads) count_pairs_kernel(Geo g, const int 
         atomicAdd(out, local);
 }
 
+// ---- inverse index by 256-token chunks (one warp per chunk) --------------
+// chunk_counts[(bg * nchunks + c) * nbmax + j] = tokens of chunk c selecting j.
+// A chunk's tokens are walked in order, 32 at a time, with a per-block lane
+// mask, so positions come out in ascending token order (deterministic).
+constexpr int kChunkTok = 256;
+constexpr int kChunkWarps = 2;
+
+__device__ __forceinline__ int chunk_seq_len(const Geo &g, int b) { return seq_len(g, b); }
+
+__global__ void __launch_bounds__(kChunkWarps * 32) csr_chunk_count_kernel(Geo g, const int *__restrict__ idx,
+                                                                           int *__restrict__ chunk_counts, int nchunks,
+                                                                           int *err)
+{
+    extern __shared__ int hist_all[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *hist = hist_all + w * g.nbmax;
+    const int item = blockIdx.x * kChunkWarps + w;  // (bg, chunk)
+    const int total = g.B * g.Hkv * nchunks;
+    if (item >= total)
+        return;
+    const int bg = item / nchunks, c = item % nchunks;
+    const int b = bg / g.Hkv, kvh = bg % g.Hkv;
+    for (int j = lane; j < g.nbmax; j += 32)
+        hist[j] = 0;
+    __syncwarp();
+    const int L = chunk_seq_len(g, b);
+    const int t_end = min(L, (c + 1) * kChunkTok);
+    for (int t = c * kChunkTok + lane; t < t_end; t += 32) {
+        const int *row = idx_row(g, idx, b, kvh, t);
+        for (int s = 0; s < g.S; ++s) {
+            const int cl = classify(row, s, t, g.bs, g.nbmax);
+            if (cl == 0)
+                atomicAdd(&hist[row[s]], 1);
+            else if (cl >= 2)
+                set_error(err, NSA_ERR_BAD_INDEX);
+        }
+    }
+    __syncwarp();
+    int *out = chunk_counts + (int64_t)item * g.nbmax;
+    for (int j = lane; j < g.nbmax; j += 32)
+        out[j] = hist[j];
+}
+
+// per (bg, j): exclusive prefix over chunks (in place) and the list length
+__global__ void __launch_bounds__(256) csr_chunk_prefix_kernel(Geo g, int *__restrict__ chunk_counts, int nchunks,
+                                                               int *__restrict__ counts)
+{
+    const int n = g.B * g.Hkv * g.nbmax;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int bg = i / g.nbmax, j = i % g.nbmax;
+        int acc = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            int *p = chunk_counts + ((int64_t)bg * nchunks + c) * g.nbmax + j;
+            const int v = *p;
+            *p = acc;
+            acc += v;
+        }
+        counts[i] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(kChunkWarps * 32) csr_chunk_fill_kernel(Geo g, const int *__restrict__ idx,
+                                                                          const int *__restrict__ chunk_prefix,
+                                                                          int nchunks, const int *__restrict__ offsets,
+                                                                          int *__restrict__ rows)
+{
+    extern __shared__ int sm_all[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *next = sm_all + w * 2 * g.nbmax;    // next list position per block
+    unsigned *mask = (unsigned *)(next + g.nbmax);  // lanes of the current batch selecting j
+    const int item = blockIdx.x * kChunkWarps + w;
+    const int total = g.B * g.Hkv * nchunks;
+    if (item >= total)
+        return;
+    const int bg = item / nchunks, c = item % nchunks;
+    const int b = bg / g.Hkv, kvh = bg % g.Hkv;
+    const int *pre = chunk_prefix + (int64_t)item * g.nbmax;
+    for (int j = lane; j < g.nbmax; j += 32) {
+        next[j] = offsets[bg * g.nbmax + j] + pre[j];
+        mask[j] = 0u;
+    }
+    __syncwarp();
+    const int L = chunk_seq_len(g, b);
+    const int t_end = min(L, (c + 1) * kChunkTok);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int t0 = c * kChunkTok; t0 < t_end; t0 += 32) {
+        const int t = t0 + lane;
+        const int *row = t < t_end ? idx_row(g, idx, b, kvh, t) : nullptr;
+        // pass 1: mark this lane in the mask of every block it selects
+        if (row)
+            for (int s = 0; s < g.S; ++s)
+                if (classify(row, s, t, g.bs, g.nbmax) == 0)
+                    atomicOr(&mask[row[s]], 1u << lane);
+        __syncwarp();
+        // pass 2: position = next[j] + earlier lanes selecting j
+        if (row)
+            for (int s = 0; s < g.S; ++s)
+                if (classify(row, s, t, g.bs, g.nbmax) == 0) {
+                    const int j = row[s];
+                    rows[next[j] + __popc(mask[j] & lt)] = t;
+                }
+        __syncwarp();
+        // pass 3: the lowest selecting lane advances next[j] and clears the mask
+        if (row)
+            for (int s = 0; s < g.S; ++s)
+                if (classify(row, s, t, g.bs, g.nbmax) == 0) {
+                    const int j = row[s];
+                    const unsigned m = mask[j];
+                    if ((m & lt) == 0u) {
+                        next[j] += __popc(m);
+                        mask[j] = 0u;
+                    }
+                }
+        __syncwarp();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *delta, int dtype,
@@ -381,6 +498,39 @@ cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit 
                             cudaStream_t st)
 {
     csr_scan_kernel<<<1, 1024, 0, st>>>(g, counts, offsets, units, blk_nchunk, blk_slot, hdr, chunk);
+    return cudaGetLastError();
+}
+
+int csr_nchunks(const Geo &g) { return (g.T + kChunkTok - 1) / kChunkTok; }
+
+bool csr_chunked_ok(const Geo &g) { return g.nbmax <= 4096; }
+
+cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_counts, int *counts, int *err,
+                                   cudaStream_t st)
+{
+    const int nchunks = csr_nchunks(g);
+    const int items = g.B * g.Hkv * nchunks;
+    const int grid = (items + kChunkWarps - 1) / kChunkWarps;
+    const size_t smem = sizeof(int) * kChunkWarps * g.nbmax;
+    csr_chunk_count_kernel<<<grid, kChunkWarps * 32, smem, st>>>(g, idx, chunk_counts, nchunks, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int n = g.B * g.Hkv * g.nbmax;
+    csr_chunk_prefix_kernel<<<grid_for(n, 256), 256, 0, st>>>(g, chunk_counts, nchunks, counts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk_prefix, const int *offsets,
+                                  int *rows, cudaStream_t st)
+{
+    const int nchunks = csr_nchunks(g);
+    const int items = g.B * g.Hkv * nchunks;
+    const int grid = (items + kChunkWarps - 1) / kChunkWarps;
+    const size_t smem = sizeof(int) * kChunkWarps * 2 * g.nbmax;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(csr_chunk_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    csr_chunk_fill_kernel<<<grid, kChunkWarps * 32, smem, st>>>(g, idx, chunk_prefix, nchunks, offsets, rows);
     return cudaGetLastError();
 }
 

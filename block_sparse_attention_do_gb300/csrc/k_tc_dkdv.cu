@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             while (vU < n_units && !*abort_flag) {
                 bool progressed = false;
                 // dV/dK of the oldest tile whose P/dS are ready
-                if (vIt < sIt && mbar_try_wait(&bars[B_PFULL], vIt & 1) &&
-                    (vT > 0 || mbar_try_wait(&bars[B_ACCEMPTY], (vUc & 1) ^ 1))) {
+                if (vIt < sIt && mbar_test(&bars[B_PFULL], vIt & 1) &&
+                    (vT > 0 || mbar_test(&bars[B_ACCEMPTY], (vUc & 1) ^ 1))) {
                     tc_fence_after();
                     const int st = vIt & 1;
                     for (int kr = 0; kr < kRows / 16; ++kr) {
@@ -330,9 +330,9 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     progressed = true;
                 }
                 // S/dP of the next tile (at most two tiles ahead of dV/dK)
-                if (sU < n_units && sIt < vIt + 2 && mbar_try_wait(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
-                    mbar_try_wait(&bars[B_SFREE0 + (sIt & 1)], ((sIt >> 1) & 1) ^ 1) &&
-                    (sT > 0 || mbar_try_wait(&bars[B_KVFULL], sUc & 1))) {
+                if (sU < n_units && sIt < vIt + 2 && mbar_test(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
+                    mbar_test(&bars[B_SFREE0 + (sIt & 1)], ((sIt >> 1) & 1) ^ 1) &&
+                    (sT > 0 || mbar_test(&bars[B_KVFULL], sUc & 1))) {
                     tc_fence_after();
                     const int st = sIt & 1;
                     const uint32_t dS_col = tmem + TM_S + st * 128;

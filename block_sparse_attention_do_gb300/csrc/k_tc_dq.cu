@@ -3,19 +3,24 @@
 //
 // One CTA owns a query tile: Tq consecutive tokens of one sequence times the
 // G query heads of one kv head (Tq * G <= 128 rows, Tq = 128 / G).  It walks,
-// in ascending order, the union U of the blocks its tokens select, and for
-// every block j of U:
-//   S = Q K_j^T,  dP = dO V_j^T                       (M=128 rows, N=64 keys, K=128)
-//   P = exp(scale S - LSE) where the row's token selects j and key <= token,
-//   dS = P (dP - delta)
-//   dQ += dS K_j                                      (M=128 rows, N=128 dims, K=64 keys)
-// and writes dQ * scale once at the end.  Rows of a token that did not
-// select j get P = dS = 0, so the sum over j is exactly the sum over the
-// token's own blocks.
+// two at a time, the ascending union U of the blocks its tokens select.  For
+// a pair (j_a, j_b) of U (128 keys):
+//   S = Q [K_a; K_b]^T,  dP = dO [V_a; V_b]^T           (M=128 rows, N=128 keys, K=128)
+//   P = exp(scale S - LSE) where the row's token selects the key's block and
+//   key <= token,  dS = P (dP - delta)
+//   dQ += dS [K_a; K_b]                                 (M=128 rows, N=128 dims, K=128 keys)
+// and writes dQ * scale once at the end.  Rows of a token that did not select
+// a block get P = dS = 0 there, so the sum over U is exactly the sum over the
+// token's own blocks.  Pairing keeps every MMA at N = 128: a tcgen05 MMA with
+// M = 128 costs about the same for N = 64 as for N = 128.
 //
-// Roles (8 warps): warp 0 lane 0 issues TMA (the Q/dO tile once, then K_j/V_j
-// double-buffered); warp 2 owns TMEM and issues the MMAs; warps 4-7 build the
-// block union, then form P/dS one row per thread and run the epilogue.
+// dS is written into the pair's V slot, free once dP is computed, so a K/V
+// stage (64 KB) carries the pair from load to the dQ MMA.
+//
+// Roles (8 warps): warp 0 lane 0 issues TMA (the Q/dO tile once, then the
+// K/V pairs, two stages); warp 2 owns TMEM and issues the MMAs; warps 4-7
+// build the block union, then form dS one row per thread and run the
+// epilogue.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -24,27 +29,27 @@ namespace {
 
 using namespace tc;
 
-constexpr int NS = 3;  // K/V stages
+constexpr int NS = 2;                       // K/V pair stages
+constexpr int kPairBytes = 2 * kTileBytes;  // K pair (32 KB) | V pair (32 KB, later dS)
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTileBytes;
-constexpr int OFF_KV = OFF_DO + kTileBytes;   // NS stages x (K | V)
-constexpr int OFF_DS = OFF_KV + NS * 2 * kKvBytes;  // 2 buffers
-constexpr int OFF_MASK = OFF_DS + 2 * kRows * 128;
+constexpr int OFF_KV = OFF_DO + kTileBytes;
+constexpr int OFF_MASK = OFF_KV + NS * kPairBytes;
 constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
 constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
 constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int KVF = 16, KVE = 16 + NS;  // barrier slots of the K/V ring
-constexpr int NUM_BARS = 16 + 2 * NS;
+constexpr int NUM_BARS = 16;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
-    B_QFULL = 0, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
-    B_DSFULL0, B_DSFULL1, B_DSFREE0, B_DSFREE1, B_ACCFULL, B_DONE, B_LIST
+    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE,
+    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1
 };
 
-constexpr uint32_t TM_S = 0;     // buffer b: S at b*128, dP at b*128 + 64
-constexpr uint32_t TM_DQ = 256;  // 128 lanes (rows) x 128 columns (dims)
+constexpr uint32_t TM_S = 0;     // S: 128 columns (keys)
+constexpr uint32_t TM_DP = 128;  // dP: 128 columns (keys)
+constexpr uint32_t TM_DQ = 256;  // dQ: 128 lanes (rows) x 128 columns (dims)
 constexpr uint32_t TM_COLS = 512;
 
 struct Params {
@@ -74,11 +79,10 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
     const Geo &g = p.g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = g.G;
-    const int Tq = G >= kRows ? 1 : kRows / G;
+    const int Tq = tile_tokens(G);
     const int nrows = Tq * G;
-    // heavier (later) tiles first
     const int ntiles_seq = (g.T + Tq - 1) / Tq;
-    const int tile = ntiles_seq - 1 - (int)blockIdx.x;
+    const int tile = ntiles_seq - 1 - (int)blockIdx.x;  // heavier (later) tiles first
     const int kvh = blockIdx.y, b = blockIdx.z;
     const int L = seq_len(g, b);
     const int t0 = tile * Tq;
@@ -90,18 +94,15 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(&bars[B_QFULL], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[B_SFULL0 + s], 1);
-            mbar_init(&bars[B_SFREE0 + s], kRows);
-            mbar_init(&bars[B_DSFULL0 + s], kRows);
-            mbar_init(&bars[B_DSFREE0 + s], 1);
-        }
+        mbar_init(&bars[B_LIST], kRows);
+        mbar_init(&bars[B_SFULL], 1);
+        mbar_init(&bars[B_SFREE], kRows);
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
-        mbar_init(&bars[B_LIST], kRows);
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[KVF + s], 1);
-            mbar_init(&bars[KVE + s], 1);
+            mbar_init(&bars[B_KVF0 + s], 1);
+            mbar_init(&bars[B_KVE0 + s], 1);
+            mbar_init(&bars[B_DSF0 + s], kRows);
         }
         fence_barrier_init();
     }
@@ -109,15 +110,14 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         tmem_alloc(tmem_slot, TM_COLS);
         tmem_relinquish();
     }
-    // unused rows (Tq * G < 128) must hold finite values
-    if (nrows < kRows) {
-        for (int i = threadIdx.x; i < 2 * kTileBytes / 16; i += blockDim.x) {
-            const int r = (i * 16 % kHalfBytes) / 128;
-            if (r >= nrows)
-                *(uint4 *)(sm + OFF_Q + i * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_async_smem();
+    // Finite values wherever a TMA may not write: tile rows past Tq * G and the
+    // K/V slots of a pair's missing second block (those keys meet P = dS = 0).
+    for (int i = threadIdx.x; i < (OFF_MASK - OFF_Q) / 16; i += blockDim.x) {
+        const int off = OFF_Q + i * 16;
+        if (off >= OFF_KV || (off % kHalfBytes) / 128 >= nrows)
+            *(uint4 *)(sm + off) = make_uint4(0, 0, 0, 0);
     }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -147,25 +147,28 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             }
             bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag);
             const int U = ok ? *n_list : 0;
+            const int npairs = (U + 1) >> 1;
             int last = -1;
-            for (int i = 0; i < U && ok; ++i) {
+            for (int i = 0; i < npairs && ok; ++i) {
                 const int s = i % NS;
-                if (!mbar_wait(&bars[KVE + s], ((i / NS) & 1) ^ 1, abort_flag))
+                if (!mbar_wait(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
                     break;
-                const int j = list[i];
-                uint8_t *kd = sm + OFF_KV + s * 2 * kKvBytes;
-                uint8_t *vd = kd + kKvBytes;
-                mbar_arrive_expect_tx(&bars[KVF + s], 2 * kKvBytes);
+                const int nb = min(2, U - 2 * i);
+                uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
+                mbar_arrive_expect_tx(&bars[B_KVF0 + s], nb * 2 * kKvBytes);
                 last = i;
-                for (int h = 0; h < 2; ++h) {
-                    if (g.thd) {
-                        tma_load_3d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, kvh,
-                                    g.cu[b] + j * kKeys);
-                        tma_load_3d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, kvh,
-                                    g.cu[b] + j * kKeys);
-                    } else {
-                        tma_load_4d(kd + h * kKvHalfBytes, &tm_k, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
-                        tma_load_4d(vd + h * kKvHalfBytes, &tm_v, &bars[KVF + s], h * 64, j * kKeys, kvh, b);
+                for (int e = 0; e < nb; ++e) {
+                    const int j = list[2 * i + e];
+                    for (int h = 0; h < 2; ++h) {
+                        uint8_t *kdst = kd + h * kHalfBytes + e * kKvHalfBytes;
+                        uint8_t *vdst = vd + h * kHalfBytes + e * kKvHalfBytes;
+                        if (g.thd) {
+                            tma_load_3d(kdst, &tm_k, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
+                            tma_load_3d(vdst, &tm_v, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
+                        } else {
+                            tma_load_4d(kdst, &tm_k, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
+                            tma_load_4d(vdst, &tm_v, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
+                        }
                     }
                 }
             }
@@ -173,48 +176,46 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
             if (*abort_flag && last >= 0)
-                mbar_wait(&bars[KVF + last % NS], (last / NS) & 1, &never);
+                mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
         }
         __syncwarp();
     } else if (warp == 2) {
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(128, 64, false, false);
+            const uint32_t idS = idesc_bf16(128, 128, false, false);
             const uint32_t idQ = idesc_bf16(128, 128, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
-            const uint32_t kv_s = smem_u32(sm + OFF_KV), ds_s = smem_u32(sm + OFF_DS);
+            const uint32_t kv_s = smem_u32(sm + OFF_KV);
             bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
             const int U = ok ? *n_list : 0;
-            int si = 0, qi = 0;  // next S/dP block, next dQ block
+            const int npairs = (U + 1) >> 1;
+            int si = 0, qi = 0;  // next pair for S/dP, next pair for dQ
             uint64_t t_last = globaltimer();
-            while (ok && qi < U && !*abort_flag) {
+            while (ok && qi < npairs && !*abort_flag) {
                 bool progressed = false;
-                if (qi < si && mbar_try_wait(&bars[B_DSFULL0 + (qi & 1)], (qi >> 1) & 1)) {
+                if (qi < si && mbar_test(&bars[B_DSF0 + qi % NS], (qi / NS) & 1)) {
                     tc_fence_after();
-                    const int s = qi & 1, ks = qi % NS;
-                    const uint32_t k_s = kv_s + ks * 2 * kKvBytes;
-                    for (int kk = 0; kk < kKeys / 16; ++kk)
-                        mma_bf16(tmem + TM_DQ, sdesc_sw128(ds_s + s * kRows * 128 + kk * 32, 16, 1024),
-                                 sdesc_sw128(k_s + kk * 2048, kKvHalfBytes, 1024), idQ, (qi > 0 || kk > 0));
-                    mma_commit(&bars[B_DSFREE0 + s]);
-                    mma_commit(&bars[KVE + ks]);
+                    const int s = qi % NS;
+                    const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
+                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
+                        mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars[B_KVE0 + s]);
                     ++qi;
                     progressed = true;
                 }
-                if (si < U && si < qi + 2 && mbar_try_wait(&bars[KVF + si % NS], (si / NS) & 1) &&
-                    mbar_try_wait(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1)) {
+                if (si < npairs && si < qi + NS && mbar_test(&bars[B_KVF0 + si % NS], (si / NS) & 1) &&
+                    mbar_test(&bars[B_SFREE], (si & 1) ^ 1)) {
                     tc_fence_after();
-                    const int s = si & 1;
-                    const uint32_t k_s = kv_s + (si % NS) * 2 * kKvBytes, v_s = k_s + kKvBytes;
-                    const uint32_t d = tmem + TM_S + s * 128;
+                    const uint32_t k_s = kv_s + (si % NS) * kPairBytes, v_s = k_s + kTileBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                        mma_bf16(d, sdesc_sw128(q_s + ao, 16, 1024), sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
-                        mma_bf16(d + 64, sdesc_sw128(do_s + ao, 16, 1024), sdesc_sw128(v_s + bo, 16, 1024), idS,
+                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
+                                 kk > 0);
+                        mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
                                  kk > 0);
                     }
-                    mma_commit(&bars[B_SFULL0 + s]);
+                    mma_commit(&bars[B_SFULL]);
                     ++si;
                     progressed = true;
                 }
@@ -234,14 +235,12 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         const int tid = threadIdx.x - 128;  // 0..127
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        // 1. block union and per-token masks
-        const int Un = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, tid, lane, wq);
+        const int U = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, tid, lane, wq);
         if (tid == 0)
-            *n_list = Un;
+            *n_list = U;
         mbar_arrive(&bars[B_LIST]);
-        const int U = Un;
+        const int npairs = (U + 1) >> 1;
 
-        // 2. per-row constants
         int tl, hh;
         qtile_row(g, Tq, r, tl, hh);
         const bool rvalid = r < nrows && tl < nvalid;
@@ -253,60 +252,61 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
             dl = p.delta[so];
         }
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
         const uint32_t *my_mask = mask + (rvalid ? tl : 0) * words;
         bool ok = true;
-        for (int i = 0; i < U; ++i) {
-            const int s = i & 1;
-            if (!mbar_wait_warp(&bars[B_SFULL0 + s], (i >> 1) & 1, abort_flag)) {
+        for (int i = 0; i < npairs; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sv[64], dv_[64];
+            // dS goes into this pair's V slot (dP is already computed)
+            const uint32_t ds_row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + r * 128;
+            for (int e = 0; e < 2; ++e) {
+                uint32_t sv[64], dv_[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld16(lane_base + TM_S + s * 128 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
-                tmem_ld16(lane_base + TM_S + s * 128 + 64 + c * 16,
-                          *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars[B_SFREE0 + s]);
-            const int j = list[i];
-            const bool sel = rvalid && qtile_selects(g, my_mask, t, j);
-            const int lim = sel ? t - j * kKeys : -1;
-            uint32_t dk_[32];
-            if (__any_sync(0xffffffffu, sel)) {
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (c <= lim)
-                        p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                    if (c + 1 <= lim)
-                        p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
-                    dk_[c >> 1] =
-                        pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld16(lane_base + TM_S + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
+                    tmem_ld16(lane_base + TM_DP + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
                 }
-            } else {
+                tmem_wait_ld();
+                if (e == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&bars[B_SFREE]);
+                }
+                const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
+                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+                const int lim = sel ? t - j * kKeys : -1;
+                uint32_t dk_[32];
+                if (__any_sync(0xffffffffu, sel)) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    dk_[c] = 0u;
-            }
-            if (!mbar_wait_warp(&bars[B_DSFREE0 + s], ((i >> 1) & 1) ^ 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const uint32_t row = ds_row + s * kRows * 128;
+                    for (int c = 0; c < 64; c += 2) {
+                        float p0 = 0.f, p1 = 0.f;
+                        if (c <= lim)
+                            p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                        if (c + 1 <= lim)
+                            p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                        dk_[c >> 1] =
+                            pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                    }
+                } else {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
+                    for (int c = 0; c < 32; ++c)
+                        dk_[c] = 0u;
+                }
+                const uint32_t row = ds_row + e * kHalfBytes;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
+                                 dk_[4 * c + 3]);
+            }
             fence_async_smem();
-            mbar_arrive(&bars[B_DSFULL0 + s]);
+            mbar_arrive(&bars[B_DSF0 + s]);
         }
-        // 3. epilogue: dQ row r = scale * TMEM lane r.  Every lane of the warp
-        //    runs the TMEM loads (.sync.aligned); only valid rows store.
-        if (ok && U > 0)
+        // epilogue: dQ row r = scale * TMEM lane r.  Every lane of the warp
+        // runs the TMEM loads (.sync.aligned); only valid rows store.
+        if (ok && npairs > 0)
             ok = mbar_wait_warp(&bars[B_ACCFULL], 0, abort_flag);
         if (ok) {
             tc_fence_after();
@@ -319,9 +319,9 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
                 uint32_t w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    w[e] = U > 0 ? pack_bf16(__uint_as_float(a[2 * e]) * g.scale,
-                                             __uint_as_float(a[2 * e + 1]) * g.scale)
-                                 : 0u;
+                    w[e] = npairs > 0 ? pack_bf16(__uint_as_float(a[2 * e]) * g.scale,
+                                                  __uint_as_float(a[2 * e + 1]) * g.scale)
+                                      : 0u;
                 if (rvalid) {
                     *(uint4 *)(dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     *(uint4 *)(dst + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -348,7 +348,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
 {
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
-    const int Tq = g.G >= kRows ? 1 : kRows / g.G;
+    const int Tq = tile_tokens(g.G);
     CUtensorMap tq, tdo, tk, tv;
     const int box_tok = (!g.thd && qtile_token_major(g)) ? 1 : Tq;
     if (!make_tmap(&tq, q, g, g.Hq, box_tok, g.G) || !make_tmap(&tdo, dO, g, g.Hq, box_tok, g.G) ||

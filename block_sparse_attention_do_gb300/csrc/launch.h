@@ -20,6 +20,15 @@ cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit 
                             cudaStream_t st);
 cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, int *rows,
                             cudaStream_t st);
+// the same inverse index by 256-token chunks: per-chunk histograms
+// (chunk_counts, B*Hkv*csr_nchunks(g)*nbmax ints, turned into per-chunk
+// prefixes in place; counts = list lengths), then an ordered per-chunk fill
+int csr_nchunks(const Geo &g);
+bool csr_chunked_ok(const Geo &g);
+cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_counts, int *counts, int *err,
+                                   cudaStream_t st);
+cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk_prefix, const int *offsets,
+                                  int *rows, cudaStream_t st);
 // sums the fp32 partials of split blocks into dk/dv and zeroes unselected blocks
 cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *blk_slot,
                                const float *partials, void *dk, void *dv, int dtype,

@@ -69,7 +69,7 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
 
 // Backward workspace carving.
 struct BwdWs {
-    size_t delta, counts, offsets, units, nchunk, slot, partials, total;
+    size_t delta, counts, offsets, units, nchunk, slot, chunkc, partials, total;
     int chunk, max_units;
 };
 
@@ -97,6 +97,10 @@ BwdWs bwd_layout(const Geo &g, int dtype)
     off = align_up(off + sizeof(int) * (size_t)nbgj);
     w.slot = off;
     off = align_up(off + sizeof(int) * (size_t)nbgj);
+    // per-chunk histograms of the inverse-index build (sparse only)
+    w.chunkc = off;
+    if (!g.dense)
+        off = align_up(off + sizeof(int) * (size_t)nbgj * csr_nchunks(g));
     w.partials = off;
     if (tc)
         off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.max_units);
@@ -188,10 +192,20 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 }
 
 // the inverse index into (offsets, rows); counts is scratch of nbgj ints
+// chunk_counts (nullable) selects the chunked build: per-chunk histograms
+// and an ordered per-chunk fill; otherwise one atomic count pass and one
+// ordered walk per block list.  Both give the same canonical lists.
 nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
-                     Unit *units, int *nchunk, int *slot, WsHeader *hdr, int chunk, cudaStream_t st)
+                     Unit *units, int *nchunk, int *slot, WsHeader *hdr, int chunk, cudaStream_t st,
+                     int *chunk_counts = nullptr)
 {
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
+    if (!g.dense && chunk_counts && csr_chunked_ok(g)) {
+        NSA_LAUNCH("csr_count", launch_csr_chunk_count(g, idx, chunk_counts, counts, &hdr->err, st));
+        NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
+        NSA_LAUNCH("csr_fill", launch_csr_chunk_fill(g, idx, chunk_counts, offsets, rows, st));
+        return NSA_OK;
+    }
     if (!g.dense) {
         NSA_TRY(cudaMemsetAsync(counts, 0, sizeof(int) * nbgj, st));
         NSA_LAUNCH("csr_count", launch_csr_count(g, idx, counts, &hdr->err, st));
@@ -235,7 +249,8 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (g.ntok == 0)
         return NSA_OK;
     NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
-    if ((s = build_csr(g, idx, counts, offsets, rows, units, nchunk, slot, hdr, L.chunk, st)) != NSA_OK)
+    if ((s = build_csr(g, idx, counts, offsets, rows, units, nchunk, slot, hdr, L.chunk, st,
+                       (int *)(w8 + L.chunkc))) != NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, hdr, L.max_units,
@@ -410,7 +425,7 @@ nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqle
     const BwdWs L = bwd_layout(g, p->dtype);
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     return build_csr(g, block_idx, (int *)(w8 + L.counts), offsets, rows, (Unit *)(w8 + L.units),
-                     (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, L.chunk, st);
+                     (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, L.chunk, st, (int *)(w8 + L.chunkc));
 }
 
 nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *cu_seqlens,

@@ -223,3 +223,126 @@ def test_deterministic_bitwise():
     b = _run(q, k, v, do, idx, bs)
     for n in ("o", "lse", "dq", "dk", "dv"):
         assert torch.equal(a[n], b[n]), n
+
+
+def test_realistic_sparsity_tensor_core_path():
+    """16 blocks, 4 slots: tiles walk a block union much larger than each
+    token's selection (the per-token bitmaps and warp skips matter)."""
+    B, Hq, Hkv, T, D, bs, S = 1, 16, 1, 1024, 128, 64, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=17)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=17)
+    got = _run(q, k, v, do, idx, bs)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, torch.bfloat16)
+    off, rows, ws = api.build_inverse_index(idx.to(DEV), Hq, bs)
+    ref_off, ref_rows, _ = oracle.inverse_index(idx, bs)
+    assert np.array_equal(off.cpu().numpy(), ref_off)
+    assert np.array_equal(rows[: int(ref_off[-1])].cpu().numpy(), ref_rows)
+
+
+def _sample_rows(rng, B, Hq, lengths, n):
+    rows = []
+    for i in range(n):
+        b = int(rng.integers(0, B))
+        L = lengths[b]
+        t = [0, L - 1, 63, 64, L // 2][i] if i < 5 else int(rng.integers(0, L))
+        rows.append((b, int(rng.integers(0, Hq)), min(t, L - 1)))
+    return rows
+
+
+def _full_size_check(q, k, v, do, idx, bs, cu=None, dense=False, n_rows=24, n_keys=12):
+    """Sampled outputs of a full-size run against the oracle, plus identities
+    that hold over the whole output."""
+    got = _run(q, k, v, do, idx, bs, cu=cu, dense=dense)
+    tol = TOL[torch.bfloat16]
+    thd = cu is not None
+    if thd:
+        lengths = [int(cu[i + 1] - cu[i]) for i in range(len(cu) - 1)]
+        B, Hq = len(lengths), q.shape[1]
+    else:
+        B, Hq, T = q.shape[0], q.shape[1], q.shape[2]
+        lengths = [T] * B
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    rng = np.random.default_rng(0)
+    rows = _sample_rows(rng, B, Hq, lengths, n_rows)
+    o, lse, dq = oracle.sel_rows(q, k, v, idx, do, bs, rows, cu_seqlens=cu)
+
+    def at(x, b, h, t):
+        return x[int(cu[b]) + t, h] if thd else x[b, h, t]
+
+    for i, (b, h, t) in enumerate(rows):
+        assert np.max(np.abs(at(got["o"], b, h, t).double().cpu().numpy() - o[i])) <= tol
+        assert np.max(np.abs(at(got["dq"], b, h, t).double().cpu().numpy() - dq[i])) <= tol
+        assert abs(float(at(got["lse"], b, h, t)) - lse[i]) <= tol
+    # keys in the last two blocks of a sequence: few attending rows
+    keys = []
+    for i in range(n_keys):
+        b = int(rng.integers(0, B))
+        L = lengths[b]
+        lo = max(0, (L - 1) // bs * bs - bs)
+        keys.append((b, int(rng.integers(0, Hkv)), int(rng.integers(lo, L))))
+    dk, dv = oracle.sel_keys(q, k, v, idx, do, bs, keys, cu_seqlens=cu)
+    for i, (b, g, kk) in enumerate(keys):
+        assert np.max(np.abs(at(got["dk"], b, g, kk).double().cpu().numpy() - dk[i])) <= tol
+        assert np.max(np.abs(at(got["dv"], b, g, kk).double().cpu().numpy() - dv[i])) <= tol
+    # identities over every output: sum_keys dV = sum of the group's dO over
+    # rows that attend anything; sum_keys dK = 0 (rows of P sum to 1 and
+    # rows of dS sum to 0)
+    dvs, dks, dos = got["dv"].double().cpu(), got["dk"].double().cpu(), do.double()
+    fin = torch.isfinite(got["lse"].cpu())
+    if thd:
+        for b in range(B):
+            a, e = int(cu[b]), int(cu[b + 1])
+            for g in range(Hkv):
+                sel = fin[a:e, g * G:(g + 1) * G].unsqueeze(-1)
+                want = (dos[a:e, g * G:(g + 1) * G] * sel).sum(dim=(0, 1))
+                assert torch.max(torch.abs(dvs[a:e, g].sum(0) - want)) < 0.5
+                assert torch.max(torch.abs(dks[a:e, g].sum(0))) < 0.5
+    else:
+        for b in range(B):
+            for g in range(Hkv):
+                sel = fin[b, g * G:(g + 1) * G].unsqueeze(-1)
+                want = (dos[b, g * G:(g + 1) * G] * sel).sum(dim=(0, 1))
+                assert torch.max(torch.abs(dvs[b, g].sum(0) - want)) < 0.5
+                assert torch.max(torch.abs(dks[b, g].sum(0))) < 0.5
+
+
+def test_full_size_long_sequence_sampled():
+    """B=1 Hq=32 Hkv=2 T=8192 D=128 block 64 S=16, bf16 (the benchmark workload)."""
+    B, Hq, Hkv, T, D, bs, S = 1, 32, 2, 8192, 128, 64, 16
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=0)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=0)
+    _full_size_check(q, k, v, do, idx, bs)
+
+
+def test_full_size_dense_causal_sampled():
+    """B=2 Hq=32 Hkv=8 T=4096 D=128 block 64, every valid block selected."""
+    B, Hq, Hkv, T, D, bs = 2, 32, 8, 4096, 128, 64
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=0)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    _full_size_check(q, k, v, do, idx, bs, dense=True)
+
+
+def test_full_size_varlen_sampled():
+    """8 packed sequences with lengths uniform in [128, 4096], Hq=32 Hkv=8
+    D=128 block 64 S=16."""
+    lengths = inputs.make_varlen_lengths(8, 128, 4096, seed=0)
+    Hq, Hkv, D, bs, S = 32, 8, 128, 64, 16
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, sum(lengths), D, dtype=torch.bfloat16, seed=0,
+                                     layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=0)
+    _full_size_check(q, k, v, do, idx, bs, cu=cu)
+
+
+def test_full_size_mid_size_fp32_and_bf16():
+    """B=2 Hq=6 Hkv=2 (G=3) T=1024 D=64 block 32 S=8 in fp32 and bf16, whole
+    outputs against the oracle."""
+    B, Hq, Hkv, T, D, bs, S = 2, 6, 2, 1024, 64, 32, 8
+    for dtype in (torch.float32, torch.bfloat16):
+        q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=0)
+        idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=0)
+        got = _run(q, k, v, do, idx, bs)
+        ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+        _compare(got, ref, dtype)
