@@ -344,119 +344,111 @@ __global__ void __launch_bounds__(kThreads) count_pairs_kernel(Geo g, const int 
         atomicAdd(out, local);
 }
 
-// ---- inverse index by 256-token chunks (one warp per chunk) --------------
-// chunk_counts[(bg * nchunks + c) * nbmax + j] = tokens of chunk c selecting j.
-// A chunk's tokens are walked in order, 32 at a time, with a per-block lane
-// mask, so positions come out in ascending token order (deterministic).
-constexpr int kChunkTok = 256;
-constexpr int kChunkWarps = 2;
+// ---- inverse index by 32-token chunks ------------------------------------
+// chunk_counts[(bg * nbmax + j) * nchunks + c] = tokens of chunk c (tokens
+// 32c .. 32c+31) selecting block j, turned in place into an exclusive prefix
+// over c.  The fill gives each (token, block) its rank among the chunk's
+// earlier tokens with a per-block lane mask, so every list comes out in
+// ascending token order (deterministic, no ordering by atomics).
+constexpr int kChunkTok = 32;
+constexpr int kFillWarps = 4;
 
-__device__ __forceinline__ int chunk_seq_len(const Geo &g, int b) { return seq_len(g, b); }
-
-__global__ void __launch_bounds__(kChunkWarps * 32) csr_chunk_count_kernel(Geo g, const int *__restrict__ idx,
-                                                                           int *__restrict__ chunk_counts, int nchunks,
-                                                                           int *err)
+// valid slots of a row, each block counted once (bit s set = use slot s)
+__device__ __forceinline__ unsigned valid_slots(const int *row, int S, int t, int bs, int nbmax, int *err)
 {
-    extern __shared__ int hist_all[];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *hist = hist_all + w * g.nbmax;
-    const int item = blockIdx.x * kChunkWarps + w;  // (bg, chunk)
-    const int total = g.B * g.Hkv * nchunks;
-    if (item >= total)
-        return;
-    const int bg = item / nchunks, c = item % nchunks;
-    const int b = bg / g.Hkv, kvh = bg % g.Hkv;
-    for (int j = lane; j < g.nbmax; j += 32)
-        hist[j] = 0;
-    __syncwarp();
-    const int L = chunk_seq_len(g, b);
-    const int t_end = min(L, (c + 1) * kChunkTok);
-    for (int t = c * kChunkTok + lane; t < t_end; t += 32) {
+    unsigned m = 0u;
+    for (int s = 0; s < S; ++s) {
+        const int c = classify(row, s, t, bs, nbmax);
+        if (c == 0)
+            m |= 1u << s;
+        else if (c >= 2)
+            set_error(err, NSA_ERR_BAD_INDEX);
+    }
+    return m;
+}
+
+__global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const int *__restrict__ idx,
+                                                                   int *__restrict__ chunk_counts, int nchunks,
+                                                                   int *err)
+{
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
+         lin += (int64_t)gridDim.x * blockDim.x) {
+        int b, kvh, t;
+        decode_idx_row(g, lin, b, kvh, t);
         const int *row = idx_row(g, idx, b, kvh, t);
-        for (int s = 0; s < g.S; ++s) {
-            const int cl = classify(row, s, t, g.bs, g.nbmax);
-            if (cl == 0)
-                atomicAdd(&hist[row[s]], 1);
-            else if (cl >= 2)
-                set_error(err, NSA_ERR_BAD_INDEX);
+        unsigned m = valid_slots(row, g.S, t, g.bs, g.nbmax, err);
+        const int64_t base = ((int64_t)b * g.Hkv + kvh) * g.nbmax;
+        while (m) {
+            const int s = __ffs(m) - 1;
+            m &= m - 1u;
+            atomicAdd(&chunk_counts[(base + row[s]) * nchunks + t / kChunkTok], 1);
         }
     }
-    __syncwarp();
-    int *out = chunk_counts + (int64_t)item * g.nbmax;
-    for (int j = lane; j < g.nbmax; j += 32)
-        out[j] = hist[j];
 }
 
-// per (bg, j): exclusive prefix over chunks (in place) and the list length
-__global__ void __launch_bounds__(256) csr_chunk_prefix_kernel(Geo g, int *__restrict__ chunk_counts, int nchunks,
-                                                               int *__restrict__ counts)
+// one warp per (bg, j): exclusive prefix over chunks, list length in counts
+__global__ void __launch_bounds__(kThreads) csr_chunk_prefix_kernel(Geo g, int *__restrict__ chunk_counts,
+                                                                    int nchunks, int *__restrict__ counts)
 {
+    const int lane = threadIdx.x & 31;
     const int n = g.B * g.Hkv * g.nbmax;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const int bg = i / g.nbmax, j = i % g.nbmax;
-        int acc = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            int *p = chunk_counts + ((int64_t)bg * nchunks + c) * g.nbmax + j;
-            const int v = *p;
-            *p = acc;
-            acc += v;
+    for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += (gridDim.x * blockDim.x) >> 5) {
+        int *p = chunk_counts + (int64_t)i * nchunks;
+        int carry = 0;
+        for (int c0 = 0; c0 < nchunks; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < nchunks ? p[c] : 0;
+            int x = v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off)
+                    x += y;
+            }
+            if (c < nchunks)
+                p[c] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        counts[i] = acc;
+        if (lane == 0)
+            counts[i] = carry;
     }
 }
 
-__global__ void __launch_bounds__(kChunkWarps * 32) csr_chunk_fill_kernel(Geo g, const int *__restrict__ idx,
-                                                                          const int *__restrict__ chunk_prefix,
-                                                                          int nchunks, const int *__restrict__ offsets,
-                                                                          int *__restrict__ rows)
+// one warp per (bg, chunk): lane = token
+__global__ void __launch_bounds__(kFillWarps * 32) csr_chunk_fill_kernel(Geo g, const int *__restrict__ idx,
+                                                                         const int *__restrict__ chunk_prefix,
+                                                                         int nchunks, const int *__restrict__ offsets,
+                                                                         int *__restrict__ rows)
 {
-    extern __shared__ int sm_all[];
+    extern __shared__ unsigned mask_all[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *next = sm_all + w * 2 * g.nbmax;    // next list position per block
-    unsigned *mask = (unsigned *)(next + g.nbmax);  // lanes of the current batch selecting j
-    const int item = blockIdx.x * kChunkWarps + w;
-    const int total = g.B * g.Hkv * nchunks;
-    if (item >= total)
-        return;
-    const int bg = item / nchunks, c = item % nchunks;
-    const int b = bg / g.Hkv, kvh = bg % g.Hkv;
-    const int *pre = chunk_prefix + (int64_t)item * g.nbmax;
-    for (int j = lane; j < g.nbmax; j += 32) {
-        next[j] = offsets[bg * g.nbmax + j] + pre[j];
+    unsigned *mask = mask_all + w * g.nbmax;  // lanes selecting block j
+    for (int j = lane; j < g.nbmax; j += 32)
         mask[j] = 0u;
-    }
     __syncwarp();
-    const int L = chunk_seq_len(g, b);
-    const int t_end = min(L, (c + 1) * kChunkTok);
     const unsigned lt = (1u << lane) - 1u;
-    for (int t0 = c * kChunkTok; t0 < t_end; t0 += 32) {
-        const int t = t0 + lane;
-        const int *row = t < t_end ? idx_row(g, idx, b, kvh, t) : nullptr;
-        // pass 1: mark this lane in the mask of every block it selects
-        if (row)
-            for (int s = 0; s < g.S; ++s)
-                if (classify(row, s, t, g.bs, g.nbmax) == 0)
-                    atomicOr(&mask[row[s]], 1u << lane);
+    const int total = g.B * g.Hkv * nchunks;
+    for (int item = blockIdx.x * kFillWarps + w; item < total; item += gridDim.x * kFillWarps) {
+        const int bg = item / nchunks, c = item % nchunks;
+        const int b = bg / g.Hkv, kvh = bg % g.Hkv;
+        const int t = c * kChunkTok + lane;
+        const int *row = nullptr;
+        unsigned m = 0u;
+        if (t < seq_len(g, b)) {
+            row = idx_row(g, idx, b, kvh, t);
+            m = valid_slots(row, g.S, t, g.bs, g.nbmax, nullptr);
+        }
+        for (unsigned mm = m; mm; mm &= mm - 1u)
+            atomicOr(&mask[row[__ffs(mm) - 1]], 1u << lane);
         __syncwarp();
-        // pass 2: position = next[j] + earlier lanes selecting j
-        if (row)
-            for (int s = 0; s < g.S; ++s)
-                if (classify(row, s, t, g.bs, g.nbmax) == 0) {
-                    const int j = row[s];
-                    rows[next[j] + __popc(mask[j] & lt)] = t;
-                }
+        for (unsigned mm = m; mm; mm &= mm - 1u) {
+            const int j = row[__ffs(mm) - 1];
+            const int64_t bgj = (int64_t)bg * g.nbmax + j;
+            rows[offsets[bgj] + chunk_prefix[bgj * nchunks + c] + __popc(mask[j] & lt)] = t;
+        }
         __syncwarp();
-        // pass 3: the lowest selecting lane advances next[j] and clears the mask
-        if (row)
-            for (int s = 0; s < g.S; ++s)
-                if (classify(row, s, t, g.bs, g.nbmax) == 0) {
-                    const int j = row[s];
-                    const unsigned m = mask[j];
-                    if ((m & lt) == 0u) {
-                        next[j] += __popc(m);
-                        mask[j] = 0u;
-                    }
-                }
+        for (unsigned mm = m; mm; mm &= mm - 1u)
+            mask[row[__ffs(mm) - 1]] = 0u;
         __syncwarp();
     }
 }
@@ -503,21 +495,24 @@ cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit 
 
 int csr_nchunks(const Geo &g) { return (g.T + kChunkTok - 1) / kChunkTok; }
 
-bool csr_chunked_ok(const Geo &g) { return g.nbmax <= 4096; }
+bool csr_chunked_ok(const Geo &g)
+{
+    return g.S <= 32 && g.nbmax <= 2048 && (int64_t)g.B * g.Hkv * g.nbmax * csr_nchunks(g) <= ((int64_t)1 << 24);
+}
 
 cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_counts, int *counts, int *err,
                                    cudaStream_t st)
 {
     const int nchunks = csr_nchunks(g);
-    const int items = g.B * g.Hkv * nchunks;
-    const int grid = (items + kChunkWarps - 1) / kChunkWarps;
-    const size_t smem = sizeof(int) * kChunkWarps * g.nbmax;
-    csr_chunk_count_kernel<<<grid, kChunkWarps * 32, smem, st>>>(g, idx, chunk_counts, nchunks, err);
-    cudaError_t e = cudaGetLastError();
+    const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
+    cudaError_t e = cudaMemsetAsync(chunk_counts, 0, sizeof(int) * nbgj * nchunks, st);
     if (e != cudaSuccess)
         return e;
-    const int n = g.B * g.Hkv * g.nbmax;
-    csr_chunk_prefix_kernel<<<grid_for(n, 256), 256, 0, st>>>(g, chunk_counts, nchunks, counts);
+    const int64_t n = (int64_t)g.ntok * g.Hkv;
+    csr_chunk_count_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    csr_chunk_prefix_kernel<<<grid_for(nbgj * 32, kThreads), kThreads, 0, st>>>(g, chunk_counts, nchunks, counts);
     return cudaGetLastError();
 }
 
@@ -526,11 +521,9 @@ cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk
 {
     const int nchunks = csr_nchunks(g);
     const int items = g.B * g.Hkv * nchunks;
-    const int grid = (items + kChunkWarps - 1) / kChunkWarps;
-    const size_t smem = sizeof(int) * kChunkWarps * 2 * g.nbmax;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(csr_chunk_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    csr_chunk_fill_kernel<<<grid, kChunkWarps * 32, smem, st>>>(g, idx, chunk_prefix, nchunks, offsets, rows);
+    const int grid = grid_for(items, kFillWarps);
+    const size_t smem = sizeof(unsigned) * kFillWarps * g.nbmax;
+    csr_chunk_fill_kernel<<<grid, kFillWarps * 32, smem, st>>>(g, idx, chunk_prefix, nchunks, offsets, rows);
     return cudaGetLastError();
 }
 

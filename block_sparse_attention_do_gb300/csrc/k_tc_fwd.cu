@@ -317,7 +317,10 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         }
         float o[128];
         if (ok && npairs > 0) {
-            if (!mbar_wait_warp(&bars[B_PVFULL], (npairs - 1) & 1, abort_flag)) {
+            // The last two P.V products may both still be running here, which
+            // a parity wait on PVFULL cannot tell apart; DONE is committed
+            // once, after the final MMA.
+            if (!mbar_wait_warp(&bars[B_DONE], 0, abort_flag)) {
                 ok = false;
             } else {
                 tc_fence_after();

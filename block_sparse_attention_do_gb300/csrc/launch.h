@@ -20,8 +20,8 @@ cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit 
                             cudaStream_t st);
 cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, int *rows,
                             cudaStream_t st);
-// the same inverse index by 256-token chunks: per-chunk histograms
-// (chunk_counts, B*Hkv*csr_nchunks(g)*nbmax ints, turned into per-chunk
+// the same inverse index by 32-token chunks: per-chunk histograms
+// (chunk_counts, B*Hkv*nbmax*csr_nchunks(g) ints, turned into per-chunk
 // prefixes in place; counts = list lengths), then an ordered per-chunk fill
 int csr_nchunks(const Geo &g);
 bool csr_chunked_ok(const Geo &g);

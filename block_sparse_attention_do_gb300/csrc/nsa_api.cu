@@ -99,7 +99,7 @@ BwdWs bwd_layout(const Geo &g, int dtype)
     off = align_up(off + sizeof(int) * (size_t)nbgj);
     // per-chunk histograms of the inverse-index build (sparse only)
     w.chunkc = off;
-    if (!g.dense)
+    if (!g.dense && csr_chunked_ok(g))
         off = align_up(off + sizeof(int) * (size_t)nbgj * csr_nchunks(g));
     w.partials = off;
     if (tc)
