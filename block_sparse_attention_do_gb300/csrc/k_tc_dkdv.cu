@@ -218,25 +218,24 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 break;
             const int ntok = min(Tt, u.count - ti * Tt);
             if (GATHER_TMA) {
-                if (pt == 0) {
-                    last_tile = it;
-                    mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
-                    for (int tl = 0; tl < Tt; ++tl) {
+                // one box (a token's G heads, one 64-column half, Q or dO) per
+                // lane of warp 0: issuing from one thread costs ~100 cycles a box
+                if (pt < 32) {
+                    if (pt == 0) {
+                        last_tile = it;
+                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
+                    }
+                    __syncwarp();
+                    for (int box = pt; box < 4 * Tt; box += 32) {
+                        const int tl = box >> 2, h = (box >> 1) & 1, tensor = box & 1;
                         // rows past the list repeat the last token (finite data, P = 0)
                         const int t = tok_s[st * kRows + min(tl, ntok - 1)];
-                        uint8_t *qd = sm + OFF_Q + st * kTileBytes + tl * G * 128;
-                        uint8_t *od = sm + OFF_DO + st * kTileBytes + tl * G * 128;
-                        for (int h = 0; h < 2; ++h) {
-                            if (g.thd) {
-                                tma_load_3d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, kvh * G,
-                                            g.cu[b] + t);
-                                tma_load_3d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, kvh * G,
-                                            g.cu[b] + t);
-                            } else {
-                                tma_load_4d(qd + h * kHalfBytes, &tm_q, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
-                                tma_load_4d(od + h * kHalfBytes, &tm_do, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
-                            }
-                        }
+                        uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + st * kTileBytes + tl * G * 128 + h * kHalfBytes;
+                        const CUtensorMap *map = tensor ? &tm_do : &tm_q;
+                        if (g.thd)
+                            tma_load_3d(dst, map, &bars[B_FULL0 + st], h * 64, kvh * G, g.cu[b] + t);
+                        else
+                            tma_load_4d(dst, map, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
                     }
                 }
                 mbar_arrive(&bars[B_FULL0 + st]);
