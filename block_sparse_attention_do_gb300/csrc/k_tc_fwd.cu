@@ -116,47 +116,57 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------------------- TMA
+        // One TMA box per lane: issuing them from a single thread serialises
+        // about a hundred cycles per box.
         if (lane == 0) {
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(&bars[B_QFULL], 2 * nrows * 128);
-            for (int h = 0; h < 2; ++h) {
+        }
+        __syncwarp();
+        {
+            const bool per_token = !g.thd && qtile_token_major(g);
+            const int nbox = per_token ? 2 * Tq : 2;
+            for (int box = lane; box < nbox; box += 32) {
+                const int h = box & 1, tl = box >> 1;
+                const CUtensorMap *map = &tm_q;
+                uint8_t *dst = sm + OFF_Q + h * kHalfBytes;
                 if (g.thd)
-                    tma_load_3d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
-                else if (qtile_token_major(g))
-                    for (int tl = 0; tl < Tq; ++tl)
-                        tma_load_4d(sm + OFF_Q + h * kHalfBytes + tl * G * 128, &tm_q, &bars[B_QFULL], h * 64,
-                                    t0 + tl, kvh * G, b);
+                    tma_load_3d(dst, map, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                else if (per_token)
+                    tma_load_4d(dst + tl * G * 128, map, &bars[B_QFULL], h * 64, t0 + tl, kvh * G, b);
                 else
-                    tma_load_4d(sm + OFF_Q + h * kHalfBytes, &tm_q, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                    tma_load_4d(dst, map, &bars[B_QFULL], h * 64, t0, kvh * G, b);
             }
-            bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag);
-            const int U = ok ? *n_list : 0;
-            const int npairs = (U + 1) >> 1;
-            int last = -1;
-            for (int i = 0; i < npairs && ok; ++i) {
-                const int s = i % NS;
-                if (!mbar_wait(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
-                    break;
-                const int nb = min(2, U - 2 * i);
-                uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
+        }
+        bool ok = mbar_wait_warp(&bars[B_LIST], 0, abort_flag);
+        const int U = ok ? *n_list : 0;
+        const int npairs = (U + 1) >> 1;
+        int last = -1;
+        for (int i = 0; i < npairs && ok; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait_warp(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
+                break;
+            const int nb = min(2, U - 2 * i);
+            uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
+            if (lane == 0)
                 mbar_arrive_expect_tx(&bars[B_KVF0 + s], nb * 2 * kKvBytes);
-                last = i;
-                for (int e = 0; e < nb; ++e) {
-                    const int j = list[2 * i + e];
-                    for (int h = 0; h < 2; ++h) {
-                        uint8_t *kdst = kd + h * kHalfBytes + e * kKvHalfBytes;
-                        uint8_t *vdst = vd + h * kHalfBytes + e * kKvHalfBytes;
-                        if (g.thd) {
-                            tma_load_3d(kdst, &tm_k, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
-                            tma_load_3d(vdst, &tm_v, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
-                        } else {
-                            tma_load_4d(kdst, &tm_k, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
-                            tma_load_4d(vdst, &tm_v, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
-                        }
-                    }
-                }
+            __syncwarp();
+            last = i;
+            // lane -> (block e of the pair, 64-column half h, K or V)
+            if (lane < 4 * nb) {
+                const int e = lane >> 2, h = (lane >> 1) & 1, isv = lane & 1;
+                const int j = list[2 * i + e];
+                uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
+                const CUtensorMap *map = isv ? &tm_v : &tm_k;
+                if (g.thd)
+                    tma_load_3d(dst, map, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
+                else
+                    tma_load_4d(dst, map, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
             }
+        }
+        // copies in flight must land before the CTA may exit
+        if (lane == 0) {
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
             if (*abort_flag && last >= 0)
