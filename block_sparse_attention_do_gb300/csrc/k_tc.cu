@@ -86,4 +86,39 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G)
+{
+    auto fn = encode_fn();
+    if (!fn || G % 8 != 0 || H % 8 != 0 || G / 8 > 256)
+        return false;
+    const cuuint64_t es = 2;  // bf16
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)(G / 8), 1}, estr[5] = {1, 1, 1, 1, 1};
+    dims[0] = 64;
+    dims[1] = 8;
+    dims[2] = 2;
+    strides[1] = 64 * es;  // the second 64-column half of a row
+    if (g.thd) {
+        // packed rows [token][H][D]
+        dims[3] = H / 8;
+        dims[4] = g.ntok;
+        strides[0] = (cuuint64_t)g.D * es;
+        strides[2] = 8 * (cuuint64_t)g.D * es;
+        strides[3] = (cuuint64_t)H * g.D * es;
+    } else {
+        // [B][H][T][D]: (b, head) flattens to one index of stride T*D
+        dims[3] = (cuuint64_t)g.B * H / 8;
+        dims[4] = g.T;
+        strides[0] = (cuuint64_t)g.T * g.D * es;
+        strides[2] = 8 * (cuuint64_t)g.T * g.D * es;
+        strides[3] = (cuuint64_t)g.D * es;
+    }
+    if (dims[3] == 0 || dims[4] == 0)
+        return false;
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace nsa

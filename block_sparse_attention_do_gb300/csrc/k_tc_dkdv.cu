@@ -12,12 +12,13 @@
 // several units writes fp32 partials that a separate kernel adds in unit
 // order; a block held by one unit writes dK/dV directly.
 //
-// Roles (8 warps):  warps 0-1 load (TMA for K_j/V_j; Q/dO rows by TMA boxes of
-// one token x G heads when G % 8 == 0, else by 16-byte cp.async with the
-// swizzle applied by hand; LSE/delta/token ids by plain loads); warp 2 owns
-// TMEM and one thread issues every MMA; warps 4-7 compute P/dS for one row
-// each and run the epilogue.  Two Q/dO stages, two S/dP TMEM buffers, one
-// P/dS buffer.
+// Roles (8 warps):  warp 0 loads (TMA for K_j/V_j; Q/dO rows by one TMA box
+// per token -- its G heads, both halves -- when G % 8 == 0, else by 16-byte
+// cp.async with the swizzle applied by hand); warp 1 resolves each tile's
+// token ids, LSE and delta a tile ahead; warp 2 owns TMEM and one thread
+// issues every MMA; warps 4-7 compute P/dS for one row each and run the
+// epilogue.  Two Q/dO stages (row-group layout, so that a token's box is
+// contiguous), two S/dP TMEM buffers, one P/dS buffer.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -37,14 +38,14 @@ constexpr int OFF_LSE = OFF_DS + kRows * 128;    // float [2][128], LSE * log2(e
 constexpr int OFF_DLT = OFF_LSE + 2 * kRows * 4; // float [2][128]
 constexpr int OFF_TOK = OFF_DLT + 2 * kRows * 4; // int   [2][128]
 constexpr int OFF_BAR = OFF_TOK + 2 * kRows * 4;
-constexpr int NUM_BARS = 16;
+constexpr int NUM_BARS = 20;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
 // barrier slots
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1
 };
 
 // TMEM columns
@@ -52,8 +53,6 @@ constexpr uint32_t TM_S = 0;     // S of buffer b at b*128, dP at b*128 + 64
 constexpr uint32_t TM_DV = 256;  // dV^T: 128 lanes (d) x 64 columns (keys)
 constexpr uint32_t TM_DK = 320;  // dK^T
 constexpr uint32_t TM_COLS = 512;
-
-constexpr int kProdThreads = 64;
 
 struct Params {
     Geo g;
@@ -66,13 +65,6 @@ struct Params {
     __nv_bfloat16 *dk, *dv;
     int *err;
 };
-
-__device__ __forceinline__ int unit_token(const Params &p, const Unit &u, int pos)
-{
-    if (p.g.dense)
-        return u.j * p.g.bs + u.begin + pos;
-    return p.rows[p.offsets[u.bg * p.g.nbmax + u.j] + u.begin + pos];
-}
 
 template <bool GATHER_TMA>
 __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -99,8 +91,10 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[B_FULL0], kProdThreads + (GATHER_TMA ? 1 : 0));
-        mbar_init(&bars[B_FULL1], kProdThreads + (GATHER_TMA ? 1 : 0));
+        mbar_init(&bars[B_FULL0], GATHER_TMA ? 1 : 32);
+        mbar_init(&bars[B_FULL1], GATHER_TMA ? 1 : 32);
+        mbar_init(&bars[B_IDX0], 32);
+        mbar_init(&bars[B_IDX1], 32);
         mbar_init(&bars[B_EMPTY0], 1);
         mbar_init(&bars[B_EMPTY1], 1);
         mbar_init(&bars[B_KVFULL], 1);
@@ -129,21 +123,111 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 2) {
-        // ------------------------------------------------------------ loader
-        // Each of the 64 loader threads owns tile rows pt and pt + 64: it
-        // resolves their token (inverse-index list) and LSE/delta one tile
-        // ahead, into registers, while the stage it will fill is still busy.
-        const int pt = threadIdx.x;  // 0..63
+    if (warp == 0) {
+        // ------------------------------------------------------- tile loader
+        // K_j / V_j once per unit; per tile, once the indexer has published
+        // the tile's tokens, the Q and dO rows: by TMA when G % 8 == 0 (one
+        // box per token and tensor, its G heads and both halves), else by
+        // 16-byte cp.async with the swizzle applied by hand.
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
-        int it = 0, uc = 0;
-        int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
-        if (pt == 0) {
+        if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_do);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
+        int it = 0, uc = 0;
+        int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
+        bool okl = true;
+        for (int ui = blockIdx.x; ui < n_units && okl; ui += gridDim.x, ++uc) {
+            const Unit u = p.units[ui];
+            const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
+            const int ntiles = (u.count + Tt - 1) / Tt;
+            if (!mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
+                okl = false;
+                break;
+            }
+            if (lane == 0) {
+                last_kv = uc;
+                mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
+                for (int h = 0; h < 2; ++h) {
+                    if (g.thd) {
+                        const int t0 = g.cu[b] + u.j * kKeys;
+                        tma_load_3d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64, kvh, t0);
+                        tma_load_3d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64, kvh, t0);
+                    } else {
+                        tma_load_4d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64, u.j * kKeys,
+                                    kvh, b);
+                        tma_load_4d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64, u.j * kKeys,
+                                    kvh, b);
+                    }
+                }
+            }
+            for (int ti = 0; ti < ntiles; ++ti, ++it) {
+                const int st = it & 1;
+                if (!mbar_wait_warp(&bars[B_IDX0 + st], (it >> 1) & 1, abort_flag)) {
+                    okl = false;
+                    break;
+                }
+                const int ntok = min(Tt, u.count - ti * Tt);
+                if (GATHER_TMA) {
+                    if (lane == 0) {
+                        last_tile = it;
+                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * nrows * 256);
+                    }
+                    __syncwarp();
+                    for (int bx = lane; bx < 2 * Tt; bx += 32) {
+                        const int tl = bx >> 1, tensor = bx & 1;
+                        // rows past the list repeat the last token (finite data, P = 0)
+                        const int t = tok_s[st * kRows + min(tl, ntok - 1)];
+                        uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + st * kTileBytes + tl * G * 256;
+                        const CUtensorMap *map = tensor ? &tm_do : &tm_q;
+                        if (g.thd)
+                            tma_load_5d(dst, map, &bars[B_FULL0 + st], 0, 0, 0, kvh * G / 8, g.cu[b] + t);
+                        else
+                            tma_load_5d(dst, map, &bars[B_FULL0 + st], 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
+                    }
+                } else {
+                    // 2 tensors x 128 rows x 16 chunks of 16 bytes
+                    for (int item = lane; item < 2 * kRows * 16; item += 32) {
+                        const int tensor = item / (kRows * 16);
+                        const int rem = item % (kRows * 16);
+                        const int r = rem >> 4, c = rem & 15;
+                        const int tl = r / G, hh = r % G;
+                        const bool valid = r < nrows && tl < ntok;
+                        const __nv_bfloat16 *base = tensor ? p.dO : p.q;
+                        const __nv_bfloat16 *src = base;
+                        if (valid)
+                            src = base + row_off(g, g.Hq, b, kvh * G + hh, tok_s[st * kRows + tl]) + c * 8;
+                        const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + rg_off(r, c >> 3) +
+                                             (((c & 7) ^ (r & 7)) << 4);
+                        cp_async_16(dst, src, valid ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    fence_async_smem();
+                    mbar_arrive(&bars[B_FULL0 + st]);
+                }
+            }
+        }
+        if (!GATHER_TMA)
+            cp_async_wait<0>();
+        if (*abort_flag && lane == 0) {
+            // let TMA copies still in flight land before the CTA exits
+            volatile int never = 0;
+            if (last_tile >= 0)
+                mbar_wait(&bars[B_FULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
+            if (last_kv >= 0)
+                mbar_wait(&bars[B_KVFULL], last_kv & 1, &never);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ indexer
+        // Resolves each tile's rows (token from the inverse index, LSE and
+        // delta) one tile ahead, into registers, while the stage it will fill
+        // is still busy; publishes them when the stage frees.  Lane l owns
+        // tile rows l, l + 32, l + 64, l + 96.
+        int it = 0;
         int ui = blockIdx.x, ti = 0;
         Unit u;
         int b = 0, kvh = 0, csr0 = 0, ntiles = 0;
@@ -154,24 +238,24 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             csr0 = g.dense ? 0 : p.offsets[u.bg * g.nbmax + u.j] + u.begin;
             ntiles = (u.count + Tt - 1) / Tt;
         };
-        int tok_r[2];
-        float l2_r[2], dl_r[2];
+        int tok_r[4];
+        float l2_r[4], dl_r[4];
         auto fetch = [&]() {
             const int ntok = min(Tt, u.count - ti * Tt);
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-                const int r = pt + k2 * kProdThreads;
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int r = lane + k4 * 32;
                 const int tl = r / G, hh = r % G;
-                tok_r[k2] = -1;
-                l2_r[k2] = 0.f;
-                dl_r[k2] = 0.f;
+                tok_r[k4] = -1;
+                l2_r[k4] = 0.f;
+                dl_r[k4] = 0.f;
                 if (r < nrows && tl < ntok) {
                     const int pos = ti * Tt + tl;
                     const int t = g.dense ? u.j * g.bs + u.begin + pos : p.rows[csr0 + pos];
                     const int64_t so = stat_off(g, b, kvh * G + hh, t);
-                    tok_r[k2] = t;
-                    l2_r[k2] = p.lse[so] * 1.4426950408889634f;
-                    dl_r[k2] = p.delta[so];
+                    tok_r[k4] = t;
+                    l2_r[k4] = p.lse[so] * 1.4426950408889634f;
+                    dl_r[k4] = p.delta[so];
                 }
             }
         };
@@ -181,106 +265,27 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         }
         while (ui < n_units) {
             const int st = it & 1;
-            bool okl = !*abort_flag;
-            if (okl && ti == 0 && pt == 0) {
-                okl = mbar_wait(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag);
-                if (okl) {
-                    last_kv = uc;
-                    mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
-                    for (int h = 0; h < 2; ++h) {
-                        if (g.thd) {
-                            const int t0 = g.cu[b] + u.j * kKeys;
-                            tma_load_3d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64, kvh, t0);
-                            tma_load_3d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64, kvh, t0);
-                        } else {
-                            tma_load_4d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64,
-                                        u.j * kKeys, kvh, b);
-                            tma_load_4d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64,
-                                        u.j * kKeys, kvh, b);
-                        }
-                    }
-                }
-            }
-            if (okl)
-                okl = mbar_wait(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag);
-            if (okl) {
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int r = pt + k2 * kProdThreads;
-                    lse_s[st * kRows + r] = l2_r[k2];
-                    dlt_s[st * kRows + r] = dl_r[k2];
-                    if (r % G == 0 && r / G < Tt)
-                        tok_s[st * kRows + r / G] = tok_r[k2];
-                }
-            }
-            // all 64 loader threads agree to go on (and see each other's stores)
-            if (named_bar_any(2, kProdThreads, !okl))
+            if (!mbar_wait_warp(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag))
                 break;
-            const int ntok = min(Tt, u.count - ti * Tt);
-            if (GATHER_TMA) {
-                // one box (a token's G heads, one 64-column half, Q or dO) per
-                // lane of warp 0: issuing from one thread costs ~100 cycles a box
-                if (pt < 32) {
-                    if (pt == 0) {
-                        last_tile = it;
-                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * kTileBytes);
-                    }
-                    __syncwarp();
-                    for (int box = pt; box < 4 * Tt; box += 32) {
-                        const int tl = box >> 2, h = (box >> 1) & 1, tensor = box & 1;
-                        // rows past the list repeat the last token (finite data, P = 0)
-                        const int t = tok_s[st * kRows + min(tl, ntok - 1)];
-                        uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + st * kTileBytes + tl * G * 128 + h * kHalfBytes;
-                        const CUtensorMap *map = tensor ? &tm_do : &tm_q;
-                        if (g.thd)
-                            tma_load_3d(dst, map, &bars[B_FULL0 + st], h * 64, kvh * G, g.cu[b] + t);
-                        else
-                            tma_load_4d(dst, map, &bars[B_FULL0 + st], h * 64, t, kvh * G, b);
-                    }
-                }
-                mbar_arrive(&bars[B_FULL0 + st]);
-            } else {
-                // 2 tensors x 128 rows x 16 chunks of 16 bytes
-                for (int item = pt; item < 2 * kRows * 16; item += kProdThreads) {
-                    const int tensor = item / (kRows * 16);
-                    const int rem = item % (kRows * 16);
-                    const int r = rem >> 4, c = rem & 15;
-                    const int tl = r / G, hh = r % G;
-                    const bool valid = r < nrows && tl < ntok;
-                    const __nv_bfloat16 *base = tensor ? p.dO : p.q;
-                    const __nv_bfloat16 *src = base;
-                    if (valid)
-                        src = base + row_off(g, g.Hq, b, kvh * G + hh, tok_s[st * kRows + tl]) + c * 8;
-                    const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + (c >> 3) * kHalfBytes +
-                                         sw128_off(r, c & 7);
-                    cp_async_16(dst, src, valid ? 16u : 0u);
-                }
-                cp_async_commit();
-                cp_async_wait<0>();
-                fence_async_smem();
-                mbar_arrive(&bars[B_FULL0 + st]);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int r = lane + k4 * 32;
+                lse_s[st * kRows + r] = l2_r[k4];
+                dlt_s[st * kRows + r] = dl_r[k4];
+                if (r % G == 0 && r / G < Tt)
+                    tok_s[st * kRows + r / G] = tok_r[k4];
             }
+            mbar_arrive(&bars[B_IDX0 + st]);
             // next tile (possibly of the next unit): resolve its rows now
             ++it;
             if (++ti == ntiles) {
                 ti = 0;
                 ui += gridDim.x;
-                ++uc;
                 if (ui < n_units)
                     load_unit();
             }
             if (ui < n_units)
                 fetch();
-        }
-        if (!GATHER_TMA)
-            cp_async_wait<0>();
-        if (*abort_flag && pt == 0) {
-            // let TMA copies still in flight land before the CTA exits
-            volatile int never = 0;
-            if (last_tile >= 0)
-                mbar_wait(&bars[B_FULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
-            if (last_kv >= 0)
-                mbar_wait(&bars[B_KVFULL], last_kv & 1, &never);
         }
     } else if (warp == 2) {
         // -------------------------------------------------------------- MMA
@@ -309,9 +314,12 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     const int st = vIt & 1;
                     for (int kr = 0; kr < kRows / 16; ++kr) {
                         const uint32_t acc = (vT > 0 || kr > 0) ? 1u : 0u;
-                        mma_bf16(tmem + TM_DV, sdesc_sw128(do_s + st * kTileBytes + kr * 2048, kHalfBytes, 1024),
+                        // 16 rows = two row groups; LBO steps the 64-dim halves (M)
+                        mma_bf16(tmem + TM_DV,
+                                 sdesc_sw128(do_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
                                  sdesc_sw128(p_s + kr * 2048, 8192, 1024), idV, acc);
-                        mma_bf16(tmem + TM_DK, sdesc_sw128(q_s + st * kTileBytes + kr * 2048, kHalfBytes, 1024),
+                        mma_bf16(tmem + TM_DK,
+                                 sdesc_sw128(q_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
                                  sdesc_sw128(ds_s + kr * 2048, 8192, 1024), idV, acc);
                     }
                     mma_commit(&bars[B_PFREE]);
@@ -336,11 +344,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     const int st = sIt & 1;
                     const uint32_t dS_col = tmem + TM_S + st * 128;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t ao = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
                         const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                        mma_bf16(dS_col, sdesc_sw128(q_s + st * kTileBytes + ao, 16, 1024),
+                        mma_bf16(dS_col, sdesc_sw128(q_s + st * kTileBytes + ao, 16, kRgStride),
                                  sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
-                        mma_bf16(dS_col + 64, sdesc_sw128(do_s + st * kTileBytes + ao, 16, 1024),
+                        mma_bf16(dS_col + 64, sdesc_sw128(do_s + st * kTileBytes + ao, 16, kRgStride),
                                  sdesc_sw128(v_s + bo, 16, 1024), idS, kk > 0);
                     }
                     mma_commit(&bars[B_SFULL0 + st]);
@@ -492,9 +500,9 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
 {
     CUtensorMap tq, tdo, tk, tv;
     const bool gather_tma = (g.G % 8) == 0;
-    const int box_heads = gather_tma ? g.G : 1;
-    if (!make_tmap(&tq, q, g, g.Hq, 1, box_heads) || !make_tmap(&tdo, dO, g, g.Hq, 1, box_heads) ||
-        !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    const bool qmaps = gather_tma ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
+                                  : make_tmap(&tq, q, g, g.Hq, 1, 1) && make_tmap(&tdo, dO, g, g.Hq, 1, 1);
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;

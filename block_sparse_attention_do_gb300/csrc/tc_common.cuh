@@ -28,6 +28,22 @@ constexpr int kKvBytes = 2 * kKvHalfBytes;
 // order.
 bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads);
 
+// Row-group tile layout (gathered rows of the dK/dV kernel): the tile's
+// rows go in groups of 8; group R/8 occupies 2048 bytes, its 64-column half h
+// the 1024 bytes at h * 1024, row R at (R % 8) * 128 inside it, 128B-swizzled.
+// Both halves of a group sit in one 2 KB span, so a TMA box covering a
+// token's G heads (G % 8 == 0) and both halves lands as one contiguous run.
+constexpr int kRgStride = 2048;
+constexpr int kRgHalf = 1024;
+__host__ __device__ inline int rg_off(int r, int half) { return (r >> 3) * kRgStride + half * kRgHalf + (r & 7) * 128; }
+
+// Tensor map whose box is one token's G consecutive query heads (G % 8 == 0,
+// H % 8 == 0), both 64-column halves, in the row-group layout above:
+// box {64 columns, 8 heads, 2 halves, G/8 head octets, 1 token}.
+// Coordinates: (0, 0, 0, octet, token) with octet = (b*H + head0)/8 (BHTD)
+// or head0/8 (THD, token = packed row).
+bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G);
+
 // the host launcher's view of the device: SM count (cached)
 int num_sms();
 
