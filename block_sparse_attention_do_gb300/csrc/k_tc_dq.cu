@@ -17,10 +17,11 @@
 // dS is written into the pair's V slot, free once dP is computed, so a K/V
 // stage (64 KB) carries the pair from load to the dQ MMA.
 //
-// Roles (8 warps): warp 0 lane 0 issues TMA (the Q/dO tile once, then the
-// K/V pairs, two stages); warp 2 owns TMEM and issues the MMAs; warps 4-7
-// build the block union, then form dS one row per thread and run the
-// epilogue.
+// Roles (12 warps): warp 0 issues TMA (the Q/dO tile once, then the K/V
+// pairs, two stages, one box per lane); warp 2 owns TMEM and one thread
+// issues the MMAs; warps 4-7 build the block union; then warps 4-7 form dS
+// of the pair's first block and warps 8-11 of its second, one row per
+// thread, and split the epilogue's columns the same way.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -60,7 +61,7 @@ struct Params {
     int *err;
 };
 
-__global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                        const __grid_constant__ CUtensorMap tm_do,
                                                        const __grid_constant__ CUtensorMap tm_k,
                                                        const __grid_constant__ CUtensorMap tm_v,
@@ -96,13 +97,13 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_LIST], kRows);
         mbar_init(&bars[B_SFULL], 1);
-        mbar_init(&bars[B_SFREE], kRows);
+        mbar_init(&bars[B_SFREE], 2 * kRows);
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[B_KVF0 + s], 1);
             mbar_init(&bars[B_KVE0 + s], 1);
-            mbar_init(&bars[B_DSF0 + s], kRows);
+            mbar_init(&bars[B_DSF0 + s], 2 * kRows);
         }
         fence_barrier_init();
     }
@@ -235,13 +236,22 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------- union, softmax, epilogue
-        const int tid = threadIdx.x - 128;  // 0..127
+        // Two warpgroups: warpgroup e (warps 4-7: e = 0, warps 8-11: e = 1)
+        // takes block e of every pair (S/dP columns e*64 .. e*64+63) and dQ
+        // columns e*64 .. e*64+63 in the epilogue; warp w reads TMEM lanes
+        // 32*(w%4) .. 32*(w%4)+31, so row r = 32*(w%4) + lane in both.
+        const int e = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int U = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, tid, lane, wq);
-        if (tid == 0)
-            *n_list = U;
-        mbar_arrive(&bars[B_LIST]);
+        int U;
+        if (e == 0) {
+            U = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, r, lane, wq);
+            if (r == 0)
+                *n_list = U;
+            mbar_arrive(&bars[B_LIST]);
+        } else {
+            U = mbar_wait_warp(&bars[B_LIST], 0, abort_flag) ? *n_list : 0;
+        }
         const int npairs = (U + 1) >> 1;
 
         int tl, hh;
@@ -264,66 +274,62 @@ __global__ void __launch_bounds__(256, 1) dq_tc_kernel(const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            // dS goes into this pair's V slot (dP is already computed)
-            const uint32_t ds_row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + r * 128;
-            for (int e = 0; e < 2; ++e) {
-                uint32_t sv[64], dv_[64];
+            uint32_t sv[64], dv_[64];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld16(lane_base + TM_S + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
-                    tmem_ld16(lane_base + TM_DP + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
-                }
-                tmem_wait_ld();
-                if (e == 1) {
-                    tc_fence_before();
-                    mbar_arrive(&bars[B_SFREE]);
-                }
-                const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
-                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
-                const int lim = sel ? t - j * kKeys : -1;
-                uint32_t dk_[32];
-                if (__any_sync(0xffffffffu, sel)) {
-#pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
-                        float p0 = 0.f, p1 = 0.f;
-                        if (c <= lim)
-                            p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                        if (c + 1 <= lim)
-                            p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
-                        dk_[c >> 1] =
-                            pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        dk_[c] = 0u;
-                }
-                const uint32_t row = ds_row + e * kHalfBytes;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
-                                 dk_[4 * c + 3]);
+            for (int c = 0; c < 4; ++c) {
+                tmem_ld16(lane_base + TM_S + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
+                tmem_ld16(lane_base + TM_DP + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
             }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars[B_SFREE]);
+            const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
+            const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+            const int lim = sel ? t - j * kKeys : -1;
+            uint32_t dk_[32];
+            if (__any_sync(0xffffffffu, sel)) {
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float p0 = 0.f, p1 = 0.f;
+                    if (c <= lim)
+                        p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
+                    if (c + 1 <= lim)
+                        p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
+                    dk_[c >> 1] =
+                        pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    dk_[c] = 0u;
+            }
+            // dS goes into this pair's V slot (dP is already computed), block e
+            // as the e-th 64-key K-chunk of the dQ MMA
+            const uint32_t row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + e * kHalfBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
             fence_async_smem();
             mbar_arrive(&bars[B_DSF0 + s]);
         }
-        // epilogue: dQ row r = scale * TMEM lane r.  Every lane of the warp
-        // runs the TMEM loads (.sync.aligned); only valid rows store.
+        // epilogue: dQ row r, columns e*64 .. e*64+63 = scale * TMEM.  Every
+        // lane of the warp runs the TMEM loads (.sync.aligned); only valid
+        // rows store.
         if (ok && npairs > 0)
             ok = mbar_wait_warp(&bars[B_ACCFULL], 0, abort_flag);
         if (ok) {
             tc_fence_after();
-            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) : nullptr;
+            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64 : nullptr;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t a[16];
-                tmem_ld16(lane_base + TM_DQ + c * 16, a);
+                tmem_ld16(lane_base + TM_DQ + e * 64 + c * 16, a);
                 tmem_wait_ld();
                 uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[e] = npairs > 0 ? pack_bf16(__uint_as_float(a[2 * e]) * g.scale,
-                                                  __uint_as_float(a[2 * e + 1]) * g.scale)
+                for (int x = 0; x < 8; ++x)
+                    w[x] = npairs > 0 ? pack_bf16(__uint_as_float(a[2 * x]) * g.scale,
+                                                  __uint_as_float(a[2 * x + 1]) * g.scale)
                                       : 0u;
                 if (rvalid) {
                     *(uint4 *)(dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -366,7 +372,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.err = err;
     dim3 grid((g.T + Tq - 1) / Tq, g.Hkv, g.B);
     cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    dq_tc_kernel<<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+    dq_tc_kernel<<<grid, 384, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError();
 }
 
