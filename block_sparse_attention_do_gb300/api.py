@@ -29,6 +29,7 @@ SYMBOLS = (
     "nsa_do_dot", "nsa_inverse_index_offsets_len", "nsa_build_inverse_index", "nsa_get_error",
     "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
     "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
+    "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
 )
 
 
@@ -76,6 +77,12 @@ def lib() -> C.CDLL:
         L.nsa_status_string.argtypes = [C.c_int32]
         L.nsa_count_pairs.argtypes = [pp] + [_P] * 3 + [_P]
         L.nsa_build_inverse_index_noalloc.argtypes = [pp] + [_P] * 5 + [_P]
+        L.nsa_plan_size.restype = C.c_size_t
+        L.nsa_plan_size.argtypes = [pp]
+        L.nsa_plan_build.argtypes = [pp, _P, _P, _P, C.c_size_t, _P]
+        L.nsa_bwd_planned_workspace_size.restype = C.c_size_t
+        L.nsa_bwd_planned_workspace_size.argtypes = [pp]
+        L.nsa_sel_bwd_planned.argtypes = [pp] + [_P] * 12 + [_P, C.c_size_t, _P]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []
@@ -173,20 +180,48 @@ def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
     return o, lse
 
 
+def build_plan(q, k, block_idx, block_size, scale=None, cu_seqlens=None, max_seqlen=None,
+               stream=None):
+    """A reusable backward plan (device uint8 tensor) of block_idx, for
+    sel_bwd(..., plan=...); q and k only give the problem's shapes."""
+    p = problem_from(q, k, block_size, block_idx.shape[-1], scale, cu_seqlens, max_seqlen)
+    L = lib()
+    n = int(L.nsa_plan_size(C.byref(p)))
+    if n == 0:
+        raise NsaError(1, "nsa_plan_size")
+    plan = torch.empty(n, dtype=torch.uint8, device=block_idx.device)
+    _check(L.nsa_plan_build(C.byref(p), _ptr(cu_seqlens), _ptr(block_idx), _ptr(plan), plan.numel(),
+                            _stream(stream)), "nsa_plan_build")
+    return plan
+
+
 def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=None,
-            max_seqlen=None, dense=False, ws=None, stream=None, out=None):
-    """Selection (or dense causal) backward through the C ABI: returns (dq, dk, dv)."""
+            max_seqlen=None, dense=False, ws=None, stream=None, out=None, plan=None):
+    """Selection (or dense causal) backward through the C ABI: returns (dq, dk, dv).
+    With `plan` (from build_plan on the same block_idx) the index build is skipped."""
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     else:
         dq, dk, dv = out
+    L = lib()
+    if plan is not None:
+        if dense:
+            raise ValueError("a plan serves the selection backward only")
+        n = int(L.nsa_bwd_planned_workspace_size(C.byref(p)))
+        if n == 0:
+            raise NsaError(1, "nsa_bwd_planned_workspace_size")
+        ws = workspace(n, q.device, "bwd_planned") if ws is None else ws
+        s = L.nsa_sel_bwd_planned(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                  _ptr(dO), _ptr(lse), _ptr(block_idx), _ptr(plan), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(ws), ws.numel(), _stream(stream))
+        _check(s, "nsa_sel_bwd_planned")
+        return dq, dk, dv
     n = bwd_workspace_size(p)
     if n == 0:
         raise NsaError(1, "nsa_bwd_workspace_size")
     ws = workspace(n, q.device, "bwd") if ws is None else ws
-    L = lib()
     st = _stream(stream)
     if cu_seqlens is not None:
         s = L.nsa_sel_varlen_bwd(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),

@@ -67,26 +67,26 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     return NSA_OK;
 }
 
-// Backward workspace carving.
-struct BwdWs {
-    size_t delta, counts, offsets, units, nchunk, slot, chunkc, partials, total;
+// Backward plan: the inverse index of one block_idx and its dK/dV work
+// units, in one region that starts with a header (n_units, index errors):
+// header | counts | offsets | unit list | per-block chunk count and partial
+// slot | per-chunk histograms (chunked build) | token lists (sparse only).
+struct PlanLayout {
+    size_t counts, offsets, units, nchunk, slot, chunkc, rows, total;
     int chunk, max_units;
 };
 
 int tiles_tokens(const Geo &g) { return g.G >= 128 ? 1 : 128 / g.G; }
 
-BwdWs bwd_layout(const Geo &g, int dtype)
+PlanLayout plan_layout(const Geo &g)
 {
-    BwdWs w;
+    PlanLayout w;
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
-    const bool tc = tc_supported(g, dtype);
     // tokens per dK/dV unit: 64 row tiles of the tensor-core kernel
     w.chunk = tiles_tokens(g) * 64;
     const int64_t sel_total = (int64_t)g.ntok * g.Hkv * g.S;  // upper bound on list entries
     w.max_units = (int)(nbgj + (sel_total + w.chunk - 1) / w.chunk);
     size_t off = kAlign;  // header
-    w.delta = off;
-    off = align_up(off + sizeof(float) * (size_t)g.ntok * g.Hq);
     w.counts = off;
     off = align_up(off + sizeof(int) * (size_t)nbgj);
     w.offsets = off;
@@ -97,21 +97,36 @@ BwdWs bwd_layout(const Geo &g, int dtype)
     off = align_up(off + sizeof(int) * (size_t)nbgj);
     w.slot = off;
     off = align_up(off + sizeof(int) * (size_t)nbgj);
-    // per-chunk histograms of the inverse-index build (sparse only)
     w.chunkc = off;
     if (!g.dense && csr_chunked_ok(g))
         off = align_up(off + sizeof(int) * (size_t)nbgj * csr_nchunks(g));
-    w.partials = off;
-    if (tc)
-        off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.max_units);
-    // token lists of the inverse index (sparse only; dense lists are implicit)
+    w.rows = off;
+    if (!g.dense)
+        off = align_up(off + sizeof(int) * (size_t)g.ntok * g.Hkv * g.S);
     w.total = off;
     return w;
 }
 
-size_t bwd_rows_bytes(const Geo &g)
+// Backward workspace: header (error word) | delta fp32 [rows] | fp32 dK/dV
+// partials (tensor-core path) | the plan, unless the call is given one.
+struct BwdWs {
+    size_t delta, partials, plan, total;
+    PlanLayout pl;
+};
+
+BwdWs bwd_layout(const Geo &g, int dtype)
 {
-    return g.dense ? 0 : align_up(sizeof(int) * (size_t)g.ntok * g.Hkv * g.S);
+    BwdWs w;
+    w.pl = plan_layout(g);
+    size_t off = kAlign;
+    w.delta = off;
+    off = align_up(off + sizeof(float) * (size_t)g.ntok * g.Hq);
+    w.partials = off;
+    if (tc_supported(g, dtype))
+        off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.pl.max_units);
+    w.plan = off;
+    w.total = off + w.pl.total;
+    return w;
 }
 
 inline nsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NSA_OK : NSA_ERR_CUDA; }
@@ -196,19 +211,19 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 // and an ordered per-chunk fill; otherwise one atomic count pass and one
 // ordered walk per block list.  Both give the same canonical lists.
 nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
-                     Unit *units, int *nchunk, int *slot, WsHeader *hdr, int chunk, cudaStream_t st,
+                     Unit *units, int *nchunk, int *slot, WsHeader *hdr, int *err, int chunk, cudaStream_t st,
                      int *chunk_counts = nullptr)
 {
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     if (!g.dense && chunk_counts && csr_chunked_ok(g)) {
-        NSA_LAUNCH("csr_count", launch_csr_chunk_count(g, idx, chunk_counts, counts, &hdr->err, st));
+        NSA_LAUNCH("csr_count", launch_csr_chunk_count(g, idx, chunk_counts, counts, err, st));
         NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
         NSA_LAUNCH("csr_fill", launch_csr_chunk_fill(g, idx, chunk_counts, offsets, rows, st));
         return NSA_OK;
     }
     if (!g.dense) {
         NSA_TRY(cudaMemsetAsync(counts, 0, sizeof(int) * nbgj, st));
-        NSA_LAUNCH("csr_count", launch_csr_count(g, idx, counts, &hdr->err, st));
+        NSA_LAUNCH("csr_count", launch_csr_count(g, idx, counts, err, st));
     }
     NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
     if (!g.dense)
@@ -216,10 +231,20 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
     return NSA_OK;
 }
 
+// Builds the plan of `idx` at `plan8` (layout L); index errors go to *err.
+nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanLayout &L, int *err, cudaStream_t st)
+{
+    WsHeader *phdr = (WsHeader *)plan8;
+    NSA_TRY(cudaMemsetAsync(phdr, 0, sizeof(WsHeader), st));
+    return build_csr(g, idx, (int *)(plan8 + L.counts), (int *)(plan8 + L.offsets), (int *)(plan8 + L.rows),
+                     (Unit *)(plan8 + L.units), (int *)(plan8 + L.nchunk), (int *)(plan8 + L.slot), phdr, err,
+                     L.chunk, st, (int *)(plan8 + L.chunkc));
+}
+
 nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
-                   const int32_t *idx, void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
-                   void *stream)
+                   const int32_t *idx, const void *plan, void *dq, void *dk, void *dv, void *ws,
+                   size_t ws_bytes, void *stream)
 {
     Geo g;
     nsa_status s = make_geo(p, thd, mode, cu, g);
@@ -231,29 +256,32 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     for (const void *x : ptrs)
         if (!aligned16(x))
             return NSA_ERR_INVALID_ARG;
-    if ((s = check_ws(ws, ws_bytes, nsa_bwd_workspace_size(p))) != NSA_OK)
+    if (plan && ((uintptr_t)plan & (kAlign - 1)))
+        return NSA_ERR_INVALID_ARG;
+    const BwdWs L = bwd_layout(g, p->dtype);
+    if ((s = check_ws(ws, ws_bytes, plan ? L.plan : nsa_bwd_workspace_size(p))) != NSA_OK)
         return s;
     cudaStream_t st = (cudaStream_t)stream;
     char *w8 = (char *)ws;
     WsHeader *hdr = (WsHeader *)ws;
-    const BwdWs L = bwd_layout(g, p->dtype);
+    char *pl8 = plan ? (char *)plan : w8 + L.plan;
+    const PlanLayout &P = L.pl;
     float *delta = (float *)(w8 + L.delta);
-    int *counts = (int *)(w8 + L.counts);
-    int *offsets = (int *)(w8 + L.offsets);
-    Unit *units = (Unit *)(w8 + L.units);
-    int *nchunk = (int *)(w8 + L.nchunk);
-    int *slot = (int *)(w8 + L.slot);
     float *partials = (float *)(w8 + L.partials);
-    int *rows = (int *)(w8 + L.total);
+    const int *offsets = (const int *)(pl8 + P.offsets);
+    const int *rows = (const int *)(pl8 + P.rows);
+    const Unit *units = (const Unit *)(pl8 + P.units);
+    const int *nchunk = (const int *)(pl8 + P.nchunk);
+    const int *slot = (const int *)(pl8 + P.slot);
+    const WsHeader *phdr = (const WsHeader *)pl8;
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     if (g.ntok == 0)
         return NSA_OK;
     NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
-    if ((s = build_csr(g, idx, counts, offsets, rows, units, nchunk, slot, hdr, L.chunk, st,
-                       (int *)(w8 + L.chunkc))) != NSA_OK)
+    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st)) != NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
-        NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, hdr, L.max_units,
+        NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                partials, dk, dv, &hdr->err, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
         NSA_LAUNCH("dq_tc", launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, st));
@@ -324,8 +352,7 @@ size_t nsa_bwd_workspace_size(const nsa_problem *p)
         // the dense entry uses S = nbmax; size for the larger of the two
         Geo gd;
         make_geo(p, thd, DENSE, fake_cu, gd);
-        const BwdWs a = bwd_layout(g, p->dtype), b = bwd_layout(gd, p->dtype);
-        const size_t sa = a.total + bwd_rows_bytes(g), sb = b.total + bwd_rows_bytes(gd);
+        const size_t sa = bwd_layout(g, p->dtype).total, sb = bwd_layout(gd, p->dtype).total;
         return sa > sb ? sa : sb;
     }
     if (make_geo(p, thd, DENSE, fake_cu, g) == NSA_OK)
@@ -344,7 +371,7 @@ nsa_status nsa_sel_bwd(const nsa_problem *p, const void *q, const void *k, const
                        const void *o, const void *dO, const float *lse, const int32_t *block_idx,
                        void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream)
 {
-    return run_bwd(p, false, SPARSE, nullptr, q, k, v, o, dO, lse, block_idx, dq, dk, dv, ws,
+    return run_bwd(p, false, SPARSE, nullptr, q, k, v, o, dO, lse, block_idx, nullptr, dq, dk, dv, ws,
                    ws_bytes, stream);
 }
 
@@ -360,7 +387,7 @@ nsa_status nsa_dense_causal_bwd(const nsa_problem *p, const void *q, const void 
                                 void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
                                 void *stream)
 {
-    return run_bwd(p, false, DENSE, nullptr, q, k, v, o, dO, lse, nullptr, dq, dk, dv, ws,
+    return run_bwd(p, false, DENSE, nullptr, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws,
                    ws_bytes, stream);
 }
 
@@ -376,8 +403,65 @@ nsa_status nsa_sel_varlen_bwd(const nsa_problem *p, const int32_t *cu_seqlens, c
                               const float *lse, const int32_t *block_idx, void *dq, void *dk,
                               void *dv, void *ws, size_t ws_bytes, void *stream)
 {
-    return run_bwd(p, true, SPARSE, cu_seqlens, q, k, v, o, dO, lse, block_idx, dq, dk, dv, ws,
+    return run_bwd(p, true, SPARSE, cu_seqlens, q, k, v, o, dO, lse, block_idx, nullptr, dq, dk, dv, ws,
                    ws_bytes, stream);
+}
+
+size_t nsa_plan_size(const nsa_problem *p)
+{
+    Geo g;
+    if (!p)
+        return 0;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
+        return 0;
+    return plan_layout(g).total;
+}
+
+size_t nsa_bwd_planned_workspace_size(const nsa_problem *p)
+{
+    Geo g;
+    if (!p)
+        return 0;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
+        return 0;
+    return bwd_layout(g, p->dtype).plan;
+}
+
+nsa_status nsa_plan_build(const nsa_problem *p, const int32_t *cu_seqlens, const int32_t *block_idx, void *plan,
+                          size_t plan_bytes, void *stream)
+{
+    Geo g;
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    nsa_status s = make_geo(p, thd, SPARSE, cu_seqlens, g);
+    if (s != NSA_OK)
+        return s;
+    if (!block_idx)
+        return NSA_ERR_INVALID_ARG;
+    const PlanLayout L = plan_layout(g);
+    if ((s = check_ws(plan, plan_bytes, L.total)) != NSA_OK)
+        return s;
+    char *pl8 = (char *)plan;
+    return build_plan(g, block_idx, pl8, L, &((WsHeader *)pl8)->err, (cudaStream_t)stream);
+}
+
+nsa_status nsa_sel_bwd_planned(const nsa_problem *p, const int32_t *cu_seqlens, const void *q, const void *k,
+                               const void *v, const void *o, const void *dO, const float *lse,
+                               const int32_t *block_idx, const void *plan, void *dq, void *dk, void *dv, void *ws,
+                               size_t ws_bytes, void *stream)
+{
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    if (!plan)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_bwd(p, thd, SPARSE, cu_seqlens, q, k, v, o, dO, lse, block_idx, plan, dq, dk, dv, ws, ws_bytes,
+                   stream);
 }
 
 nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,
@@ -422,10 +506,11 @@ nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqle
     cudaStream_t st = (cudaStream_t)stream;
     char *w8 = (char *)ws;
     WsHeader *hdr = (WsHeader *)ws;
-    const BwdWs L = bwd_layout(g, p->dtype);
+    const PlanLayout L = plan_layout(g);
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     return build_csr(g, block_idx, (int *)(w8 + L.counts), offsets, rows, (Unit *)(w8 + L.units),
-                     (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, L.chunk, st, (int *)(w8 + L.chunkc));
+                     (int *)(w8 + L.nchunk), (int *)(w8 + L.slot), hdr, &hdr->err, L.chunk, st,
+                     (int *)(w8 + L.chunkc));
 }
 
 nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *cu_seqlens,
@@ -442,7 +527,7 @@ nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *
     if (!block_idx || !offsets || !rows)
         return NSA_ERR_INVALID_ARG;
     // scratch plan: header | counts | unit list | chunks per block | partial slots
-    const BwdWs L = bwd_layout(g, p->dtype);
+    const PlanLayout L = plan_layout(g);
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     const size_t off_counts = kAlign;
     const size_t off_units = align_up(off_counts + sizeof(int) * nbgj);
@@ -461,7 +546,7 @@ nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *
     // build_csr zeroes the per-block counts itself
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     if ((s = build_csr(g, block_idx, (int *)(w8 + off_counts), offsets, rows, (Unit *)(w8 + off_units),
-                       (int *)(w8 + off_nchunk), (int *)(w8 + off_slot), hdr, L.chunk, st)) != NSA_OK)
+                       (int *)(w8 + off_nchunk), (int *)(w8 + off_slot), hdr, &hdr->err, L.chunk, st)) != NSA_OK)
         return s;
     if (status_out)
         NSA_TRY(cudaMemcpyAsync(status_out, &hdr->err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));

@@ -146,6 +146,38 @@ nsa_status nsa_sel_varlen_bwd(const nsa_problem *p, const int32_t *cu_seqlens, c
                               void *dv, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Reusable backward plan.  The pages build nothing like it: it is the inverse
+ * index of one block_idx tensor (block -> ascending list of the tokens that
+ * selected it, see nsa_build_inverse_index) together with the dK/dV work
+ * units cut from it, built once -- for example right after the selection is
+ * made, next to the forward -- and read by any number of backward calls on
+ * the same block_idx, which then skip the index build.
+ *  - nsa_plan_size: bytes of device memory a plan of problem p needs
+ *    (0 if p is not a valid selection problem).  The plan buffer is
+ *    caller-owned, 256-byte aligned.
+ *  - nsa_plan_build: checks the arguments, then on `stream` validates
+ *    block_idx and writes the plan.  cu_seqlens is NULL for BHTD (p->layout
+ *    NSA_LAYOUT_BHTD) and the packed-row offsets for THD.  Index errors are
+ *    read with nsa_get_error(plan, ...); bad entries are left out.
+ *  - nsa_bwd_planned_workspace_size / nsa_sel_bwd_planned: the selection
+ *    backward (nsa_sel_bwd, or nsa_sel_varlen_bwd when p->layout is THD and
+ *    cu_seqlens is given) taking the index from `plan`, which must have been
+ *    built from the same p, cu_seqlens and block_idx contents (not checked).
+ *    The call only reads the plan, so calls sharing one plan may run at the
+ *    same time (each with its own ws).  Returns NSA_ERR_INVALID_ARG for a
+ *    NULL or misaligned plan.
+ */
+size_t nsa_plan_size(const nsa_problem *p);
+nsa_status nsa_plan_build(const nsa_problem *p, const int32_t *cu_seqlens, const int32_t *block_idx,
+                          void *plan, size_t plan_bytes, void *stream);
+size_t nsa_bwd_planned_workspace_size(const nsa_problem *p);
+nsa_status nsa_sel_bwd_planned(const nsa_problem *p, const int32_t *cu_seqlens, const void *q,
+                               const void *k, const void *v, const void *o, const void *dO,
+                               const float *lse, const int32_t *block_idx, const void *plan,
+                               void *dq, void *dk, void *dv, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/*
  * do_dot pre-pass (cuDNN-frontend page: the do_dot kernel of the backward
  * chain): delta_t = sum_d dO_td * O_td for every query row, in fp32, layout
  * of lse.  cu_seqlens is NULL for BHTD.

@@ -244,6 +244,49 @@ def test_deterministic_bitwise():
         assert torch.equal(a[n], b[n]), n
 
 
+@pytest.mark.parametrize("dtype,shape", [
+    (torch.bfloat16, (1, 16, 1, 1024, 128, 64, 4)),   # tensor-core path
+    (torch.float32, (2, 6, 2, 300, 64, 32, 5)),       # SIMT path
+])
+def test_planned_backward_is_the_same_backward(dtype, shape):
+    """A plan built once gives bitwise the results of the plain backward, and
+    is only read: two calls on one plan agree."""
+    B, Hq, Hkv, T, D, bs, S = shape
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=12)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=12)
+    ref = _run(q, k, v, do, idx, bs)
+    g = [x.to(DEV) for x in (q, k, v, do, idx)]
+    plan = api.build_plan(g[0], g[1], g[4], bs)
+    assert api.get_error(plan) == 0
+    for _ in range(2):
+        dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], ref["o"], g[3], ref["lse"], g[4], bs, plan=plan)
+        torch.cuda.synchronize()
+        for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert torch.equal(x, ref[name]), name
+
+
+def test_planned_backward_varlen_and_bad_index():
+    Hq, Hkv, D, bs, S = 8, 2, 128, 64, 6
+    lengths = [130, 64, 257]
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    total = int(cu[-1])
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=torch.bfloat16, seed=13, layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=13)
+    ref = _run(q, k, v, do, idx, bs, cu=cu)
+    g = [x.to(DEV) for x in (q, k, v, do, idx)]
+    gcu = cu.to(DEV)
+    plan = api.build_plan(g[0], g[1], g[4], bs, cu_seqlens=gcu)
+    dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], ref["o"], g[3], ref["lse"], g[4], bs, cu_seqlens=gcu,
+                             plan=plan)
+    torch.cuda.synchronize()
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert torch.equal(x, ref[name]), name
+    bad = idx.clone()
+    bad[5, 0, 1] = 3  # a future block of the first sequence
+    plan = api.build_plan(g[0], g[1], bad.to(DEV), bs, cu_seqlens=gcu)
+    assert api.get_error(plan) == 3
+
+
 def test_realistic_sparsity_tensor_core_path():
     """16 blocks, 4 slots: tiles walk a block union much larger than each
     token's selection (the per-token bitmaps and warp skips matter)."""
