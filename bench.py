@@ -319,6 +319,33 @@ def run_ours(args):
                 "algorithmic_flop_per_launch": alg}
     pct = value / float(peaks["bf16_tflops"])
 
+    # ---- the same backward reading a plan built once for idx (nsa_plan_build):
+    # the inverse index leaves the backward's critical path
+    plan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    plan_ev[0].record(st)
+    plan = api.build_plan(q, k, idx, bs)
+    plan_ev[1].record(st)
+    ws_p = torch.empty(api.bwd_planned_workspace_size(p), dtype=torch.uint8, device=dev)
+    o, lse = step()
+    for _ in range(2):
+        api.sel_bwd(q, k, v, o, do, lse, idx, bs, ws=ws_p, out=outs, plan=plan)
+    n_pl = max(3, min(K, 50))
+    p_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pl)]
+    for i in range(n_pl):
+        flush.zero_()
+        p_ev[i][0].record(st)
+        api.sel_bwd(q, k, v, o, do, lse, idx, bs, ws=ws_p, out=outs, plan=plan)
+        p_ev[i][1].record(st)
+    torch.cuda.synchronize()
+    if api.get_error(ws_p) or api.get_error(plan):
+        raise RuntimeError("device error in the planned backward")
+    pl_ms = sum(a.elapsed_time(b) for a, b in p_ev)
+    pl_ms_max, pl_flop = aggregate(pl_ms, bwd_flop * n_pl, dev)
+    planned = {"value": pl_flop / (pl_ms_max * 1e-3) / 1e12, "unit": "TFLOP/s", "bwd_ms": pl_ms / n_pl,
+               "plan_build_ms": plan_ev[0].elapsed_time(plan_ev[1]), "steps": n_pl,
+               "scope": "nsa_sel_bwd_planned with a plan built once for idx (nsa_plan_build, timed "
+                        "apart); same L2 flush between steps"}
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if True:  # every rank: the aggregation below is collective
@@ -368,7 +395,7 @@ def run_ours(args):
             "bwd_ms": bwd_ms / K, "fwd_ms": fwd_ms / K, "wall_s": t_wall,
             "kernels": {n: {"ms_avg": e["ms_avg"], "launches": e["launches"], "share": e["share"]}
                         for n, e in sorted(kern.items(), key=lambda kv: -kv[1]["ms_total"])},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": len(recs),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "planned": planned, "gpu_launches": len(recs),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -150,6 +150,10 @@ def bwd_workspace_size(p: Problem) -> int:
     return int(lib().nsa_bwd_workspace_size(C.byref(p)))
 
 
+def bwd_planned_workspace_size(p: Problem) -> int:
+    return int(lib().nsa_bwd_planned_workspace_size(C.byref(p)))
+
+
 def _lse_shape(q, cu_seqlens):
     return q.shape[:-1]
 
@@ -209,7 +213,7 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
     if plan is not None:
         if dense:
             raise ValueError("a plan serves the selection backward only")
-        n = int(L.nsa_bwd_planned_workspace_size(C.byref(p)))
+        n = bwd_planned_workspace_size(p)
         if n == 0:
             raise NsaError(1, "nsa_bwd_planned_workspace_size")
         ws = workspace(n, q.device, "bwd_planned") if ws is None else ws
