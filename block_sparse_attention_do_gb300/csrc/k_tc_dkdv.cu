@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[B_FULL0], GATHER_TMA ? 1 : 32);
-        mbar_init(&bars[B_FULL1], GATHER_TMA ? 1 : 32);
+        mbar_init(&bars[B_FULL0], GATHER_TMA ? 2 : 32);
+        mbar_init(&bars[B_FULL1], GATHER_TMA ? 2 : 32);
         mbar_init(&bars[B_IDX0], 32);
         mbar_init(&bars[B_IDX1], 32);
         mbar_init(&bars[B_EMPTY0], 1);
@@ -123,12 +123,15 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp == 0 || (GATHER_TMA && warp == 3)) {
         // ------------------------------------------------------- tile loader
-        // K_j / V_j once per unit; per tile, once the indexer has published
-        // the tile's tokens, the Q and dO rows: by TMA when G % 8 == 0 (one
-        // box per token and tensor, its G heads and both halves), else by
-        // 16-byte cp.async with the swizzle applied by hand.
+        // K_j / V_j once per unit (warp 0); per tile, once the indexer has
+        // published the tile's tokens, the Q and dO rows: by TMA when G % 8 ==
+        // 0, one box per token (its G heads, both halves), warp 0 the Q boxes
+        // and warp 3 the dO boxes (a box takes ~85 cycles to issue, so two
+        // warps halve the time to the tile's last one); else by 16-byte
+        // cp.async from warp 0 with the swizzle applied by hand.
+        const int tensor = warp == 3 ? 1 : 0;
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -143,11 +146,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int ntiles = (u.count + Tt - 1) / Tt;
-            if (!mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
+            if (tensor == 0 && !mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
                 okl = false;
                 break;
             }
-            if (lane == 0) {
+            if (tensor == 0 && lane == 0) {
                 last_kv = uc;
                 mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
                 for (int h = 0; h < 2; ++h) {
@@ -173,11 +176,10 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 if (GATHER_TMA) {
                     if (lane == 0) {
                         last_tile = it;
-                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], 2 * nrows * 256);
+                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], nrows * 256);
                     }
                     __syncwarp();
-                    for (int bx = lane; bx < 2 * Tt; bx += 32) {
-                        const int tl = bx >> 1, tensor = bx & 1;
+                    for (int tl = lane; tl < Tt; tl += 32) {
                         // rows past the list repeat the last token (finite data, P = 0)
                         const int t = tok_s[st * kRows + min(tl, ntok - 1)];
                         uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + st * kTileBytes + tl * G * 256;
