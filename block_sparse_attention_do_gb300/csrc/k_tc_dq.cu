@@ -195,19 +195,23 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const int npairs = (U + 1) >> 1;
             int si = 0, qi = 0;  // next pair for S/dP, next pair for dQ
             uint64_t t_last = globaltimer();
+            // dQ += dS K of the oldest pair whose dS is in shared memory; its
+            // commit frees the pair's K/V stage for the loader
+            auto try_dq = [&]() -> bool {
+                if (!(qi < si && mbar_test(&bars[B_DSF0 + qi % NS], (qi / NS) & 1)))
+                    return false;
+                tc_fence_after();
+                const int s = qi % NS;
+                const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
+                for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
+                    mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                             sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars[B_KVE0 + s]);
+                ++qi;
+                return true;
+            };
             while (ok && qi < npairs && !*abort_flag) {
-                bool progressed = false;
-                if (qi < si && mbar_test(&bars[B_DSF0 + qi % NS], (qi / NS) & 1)) {
-                    tc_fence_after();
-                    const int s = qi % NS;
-                    const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
-                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
-                        mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars[B_KVE0 + s]);
-                    ++qi;
-                    progressed = true;
-                }
+                bool progressed = try_dq();
                 if (si < npairs && si < qi + NS && mbar_test(&bars[B_KVF0 + si % NS], (si / NS) & 1) &&
                     mbar_test(&bars[B_SFREE], (si & 1) ^ 1)) {
                     tc_fence_after();
@@ -216,6 +220,13 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
                                  kk > 0);
+                    }
+                    // a dQ that became ready meanwhile goes between S and dP:
+                    // issuing blocks while the tensor pipe is busy, and the dQ
+                    // commit is what frees a K/V stage
+                    try_dq();
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
                                  kk > 0);
                     }
@@ -287,7 +298,24 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
             const int lim = sel ? t - j * kKeys : -1;
             uint32_t dk_[32];
-            if (__any_sync(0xffffffffu, sel)) {
+            if (__all_sync(0xffffffffu, lim < 0 || lim >= kKeys - 1)) {
+                // no row of the warp ends inside the block: a row attends all
+                // of it or none; none gets a +inf bias (exp2(-inf) = 0)
+                if (__any_sync(0xffffffffu, sel)) {
+                    const float bias = sel ? l2 : __int_as_float(0x7f800000);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[c]), g.scale_l2, -bias));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), g.scale_l2, -bias));
+                        dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl),
+                                                p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        dk_[c] = 0u;
+                }
+            } else if (__any_sync(0xffffffffu, sel)) {
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     float p0 = 0.f, p1 = 0.f;
