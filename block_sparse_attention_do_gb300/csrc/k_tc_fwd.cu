@@ -265,13 +265,27 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             }
             uint32_t pk[64];
             if (__any_sync(0xffffffffu, anysel)) {
+                // no row of the warp ends inside either block: a row attends a
+                // whole block or none of it; none gets a -inf bias
+                const bool whole = __all_sync(0xffffffffu, (lim[0] < 0 || lim[0] >= kKeys - 1) &&
+                                                               (lim[1] < 0 || lim[1] >= kKeys - 1));
                 float mb = -INFINITY;
+                if (whole) {
+                    const float b0 = lim[0] >= 0 ? 0.f : -INFINITY, b1 = lim[1] >= 0 ? 0.f : -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float x = __uint_as_float(sv[c]) * g.scale_l2;
-                    sv[c] = __float_as_uint(x);
-                    if ((c & 63) <= lim[c >> 6])
+                    for (int c = 0; c < 128; ++c) {
+                        const float x = fmaf(__uint_as_float(sv[c]), g.scale_l2, c < 64 ? b0 : b1);
+                        sv[c] = __float_as_uint(x);
                         mb = fmaxf(mb, x);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const float x = __uint_as_float(sv[c]) * g.scale_l2;
+                        sv[c] = __float_as_uint(x);
+                        if ((c & 63) <= lim[c >> 6])
+                            mb = fmaxf(mb, x);
+                    }
                 }
                 const bool raise = mb > m + kRescaleLog2;
                 if (__any_sync(0xffffffffu, raise)) {
@@ -299,13 +313,26 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                     }
                 }
                 float rs = 0.f;
+                if (whole) {
+                    // a row with nothing attended so far has m = -inf and only
+                    // -inf scores: subtract 0 there so that exp2 gives 0, not NaN
+                    const float ms = m == -INFINITY ? 0.f : m;
 #pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const int lm = lim[c >> 6];
-                    const float p0 = ((c & 63) <= lm) ? ex2(__uint_as_float(sv[c]) - m) : 0.f;
-                    const float p1 = (((c + 1) & 63) <= lm) ? ex2(__uint_as_float(sv[c + 1]) - m) : 0.f;
-                    rs += p0 + p1;
-                    pk[c >> 1] = pack_bf16(p0, p1);
+                    for (int c = 0; c < 128; c += 2) {
+                        const float p0 = ex2(__uint_as_float(sv[c]) - ms);
+                        const float p1 = ex2(__uint_as_float(sv[c + 1]) - ms);
+                        rs += p0 + p1;
+                        pk[c >> 1] = pack_bf16(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; c += 2) {
+                        const int lm = lim[c >> 6];
+                        const float p0 = ((c & 63) <= lm) ? ex2(__uint_as_float(sv[c]) - m) : 0.f;
+                        const float p1 = (((c + 1) & 63) <= lm) ? ex2(__uint_as_float(sv[c + 1]) - m) : 0.f;
+                        rs += p0 + p1;
+                        pk[c >> 1] = pack_bf16(p0, p1);
+                    }
                 }
                 l += rs;
             } else {
