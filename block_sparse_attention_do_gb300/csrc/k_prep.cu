@@ -288,13 +288,17 @@ __global__ void __launch_bounds__(kThreads) csr_fill_kernel(Geo g, const int *__
     }
 }
 
+// dK/dV of blocks whose token list was split over several units: the sum of
+// the units' fp32 partials in unit order (deterministic); blocks nobody
+// selected get zeros.  One CTA per (b, kv head, block, quarter of its keys);
+// a thread takes 4 consecutive dims of one key.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int *__restrict__ nchunk,
                                                                const int *__restrict__ slot,
                                                                const float *__restrict__ partials,
                                                                T *__restrict__ dk, T *__restrict__ dv)
 {
-    const int i = blockIdx.x;
+    const int i = blockIdx.x >> 2, quarter = blockIdx.x & 3;
     const int nch = nchunk[i];
     if (nch == 1)
         return;  // written directly by the dK/dV kernel
@@ -305,19 +309,40 @@ __global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int 
         return;
     const int nkeys = min(g.bs, L - k0);
     const int64_t per = (int64_t)g.bs * g.D;
-    for (int e = threadIdx.x; e < nkeys * g.D; e += blockDim.x) {
-        const int kk = e / g.D, d = e % g.D;
-        float a = 0.f, c = 0.f;
-        if (nch >= 2) {
-            const float *p = partials + (int64_t)slot[i] * 2 * per;
-            for (int s = 0; s < nch; ++s) {  // fixed order: deterministic
-                a += p[(int64_t)s * 2 * per + kk * g.D + d];
-                c += p[(int64_t)s * 2 * per + per + kk * g.D + d];
-            }
+    const int kq = g.bs / 4, d4 = g.D / 4;
+    const float *base = partials + (nch >= 2 ? (int64_t)slot[i] * 2 * per : 0);
+    for (int e = threadIdx.x; e < kq * d4; e += blockDim.x) {
+        const int kk = quarter * kq + e / d4, d = (e % d4) * 4;
+        if (kk >= nkeys)
+            continue;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+        const float *p = base + kk * g.D + d;
+        int s = 0;
+        for (; s + 2 <= nch; s += 2) {  // fixed order: deterministic
+            const float4 a0 = *reinterpret_cast<const float4 *>(p + (int64_t)s * 2 * per);
+            const float4 c0 = *reinterpret_cast<const float4 *>(p + (int64_t)s * 2 * per + per);
+            const float4 a1 = *reinterpret_cast<const float4 *>(p + (int64_t)(s + 1) * 2 * per);
+            const float4 c1 = *reinterpret_cast<const float4 *>(p + (int64_t)(s + 1) * 2 * per + per);
+            a.x += a0.x; a.y += a0.y; a.z += a0.z; a.w += a0.w;
+            c.x += c0.x; c.y += c0.y; c.z += c0.z; c.w += c0.w;
+            a.x += a1.x; a.y += a1.y; a.z += a1.z; a.w += a1.w;
+            c.x += c1.x; c.y += c1.y; c.z += c1.z; c.w += c1.w;
+        }
+        if (s < nch) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(p + (int64_t)s * 2 * per);
+            const float4 c0 = *reinterpret_cast<const float4 *>(p + (int64_t)s * 2 * per + per);
+            a.x += a0.x; a.y += a0.y; a.z += a0.z; a.w += a0.w;
+            c.x += c0.x; c.y += c0.y; c.z += c0.z; c.w += c0.w;
         }
         const int64_t off = row_off(g, g.Hkv, b, kvh, k0 + kk) + d;
-        dk[off] = from_f<T>(a);
-        dv[off] = from_f<T>(c);
+        dk[off] = from_f<T>(a.x);
+        dk[off + 1] = from_f<T>(a.y);
+        dk[off + 2] = from_f<T>(a.z);
+        dk[off + 3] = from_f<T>(a.w);
+        dv[off] = from_f<T>(c.x);
+        dv[off + 1] = from_f<T>(c.y);
+        dv[off + 2] = from_f<T>(c.z);
+        dv[off + 3] = from_f<T>(c.w);
     }
 }
 
@@ -545,11 +570,11 @@ cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *b
     if (n == 0)
         return cudaSuccess;
     if (dtype == NSA_DTYPE_BF16)
-        dkdv_reduce_kernel<__nv_bfloat16><<<n, kThreads, 0, st>>>(
+        dkdv_reduce_kernel<__nv_bfloat16><<<4 * n, kThreads, 0, st>>>(
             g, blk_nchunk, blk_slot, partials, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv);
     else
-        dkdv_reduce_kernel<float><<<n, kThreads, 0, st>>>(g, blk_nchunk, blk_slot, partials,
-                                                          (float *)dk, (float *)dv);
+        dkdv_reduce_kernel<float><<<4 * n, kThreads, 0, st>>>(g, blk_nchunk, blk_slot, partials,
+                                                              (float *)dk, (float *)dv);
     return cudaGetLastError();
 }
 
