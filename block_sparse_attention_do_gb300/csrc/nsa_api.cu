@@ -84,7 +84,9 @@ PlanLayout plan_layout(const Geo &g)
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
     // tokens per dK/dV unit: 64 row tiles of the tensor-core kernel
     w.chunk = tiles_tokens(g) * 64;
-    const int64_t sel_total = (int64_t)g.ntok * g.Hkv * g.S;  // upper bound on list entries
+    // upper bound on list entries; dense: a row of sequence-local token t
+    // attends t/bs + 1 <= nbmax/2 + 1 blocks on average over a sequence
+    const int64_t sel_total = g.dense ? (int64_t)g.ntok * g.Hkv * (g.nbmax / 2 + 1) : (int64_t)g.ntok * g.Hkv * g.S;
     w.max_units = (int)(nbgj + (sel_total + w.chunk - 1) / w.chunk);
     size_t off = kAlign;  // header
     w.counts = off;
