@@ -44,7 +44,7 @@ constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
-    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE,
+    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE, B_DONEQ,
     B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1
 };
 
@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_SFREE], 2 * kRows);
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
+        mbar_init(&bars[B_DONEQ], 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[B_KVF0 + s], 1);
             mbar_init(&bars[B_KVE0 + s], 1);
@@ -183,66 +184,63 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // -------------------------------------------------------------- MMA
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- MMA
+        // Two issuing threads, so that a pair's dQ MMAs enter the tensor pipe
+        // as soon as its dS is ready instead of queueing behind the next
+        // pair's S/dP issue: warp 2 issues S and dP, warp 3 dQ (their TMEM
+        // columns are disjoint; each commit covers its own thread's MMAs).
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(128, 128, false, false);
-            const uint32_t idQ = idesc_bf16(128, 128, false, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
             const uint32_t kv_s = smem_u32(sm + OFF_KV);
             bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
             const int U = ok ? *n_list : 0;
             const int npairs = (U + 1) >> 1;
-            int si = 0, qi = 0;  // next pair for S/dP, next pair for dQ
-            uint64_t t_last = globaltimer();
-            // dQ += dS K of the oldest pair whose dS is in shared memory; its
-            // commit frees the pair's K/V stage for the loader
-            auto try_dq = [&]() -> bool {
-                if (!(qi < si && mbar_test(&bars[B_DSF0 + qi % NS], (qi / NS) & 1)))
-                    return false;
-                tc_fence_after();
-                const int s = qi % NS;
-                const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
-                for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
-                    mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                             sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bars[B_KVE0 + s]);
-                ++qi;
-                return true;
-            };
-            while (ok && qi < npairs && !*abort_flag) {
-                bool progressed = try_dq();
-                if (si < npairs && si < qi + NS && mbar_test(&bars[B_KVF0 + si % NS], (si / NS) & 1) &&
-                    mbar_test(&bars[B_SFREE], (si & 1) ^ 1)) {
+            if (warp == 2) {
+                const uint32_t idS = idesc_bf16(128, 128, false, false);
+                for (int si = 0; si < npairs && ok; ++si) {
+                    // the pair's K/V have landed; the softmax holds the previous S/dP in registers
+                    if (!mbar_wait(&bars[B_KVF0 + si % NS], (si / NS) & 1, abort_flag) ||
+                        !mbar_wait(&bars[B_SFREE], (si & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t k_s = kv_s + (si % NS) * kPairBytes, v_s = k_s + kTileBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
                                  kk > 0);
-                    }
-                    // a dQ that became ready meanwhile goes between S and dP:
-                    // issuing blocks while the tensor pipe is busy, and the dQ
-                    // commit is what frees a K/V stage
-                    try_dq();
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
                                  kk > 0);
                     }
                     mma_commit(&bars[B_SFULL]);
-                    ++si;
-                    progressed = true;
                 }
-                if (progressed)
-                    t_last = globaltimer();
-                else if (globaltimer() - t_last > kWaitLimitNs)
-                    *abort_flag = 1;
+                mma_commit(&bars[B_DONE]);
+                volatile int never = 0;
+                mbar_wait(&bars[B_DONE], 0, &never);
+            } else {
+                const uint32_t idQ = idesc_bf16(128, 128, false, true);
+                for (int qi = 0; qi < npairs && ok; ++qi) {
+                    // dQ += dS K once the pair's dS is in shared memory; the
+                    // commit frees the pair's K/V stage for the loader
+                    if (!mbar_wait(&bars[B_DSF0 + qi % NS], (qi / NS) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int s = qi % NS;
+                    const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
+                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
+                        mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars[B_KVE0 + s]);
+                }
+                mma_commit(&bars[B_ACCFULL]);
+                mma_commit(&bars[B_DONEQ]);
+                volatile int never = 0;
+                mbar_wait(&bars[B_DONEQ], 0, &never);
             }
-            mma_commit(&bars[B_ACCFULL]);
-            mma_commit(&bars[B_DONE]);
-            volatile int never = 0;
-            mbar_wait(&bars[B_DONE], 0, &never);
         }
         __syncwarp();
     } else if (warp >= 4) {
