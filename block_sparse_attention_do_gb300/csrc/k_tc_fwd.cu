@@ -14,6 +14,11 @@
 // below 2^8.  LSE = m + log l.  Warps whose rows all skip a pair write zero P
 // without computing it.  P is written into the pair's K slot, free once S is
 // computed.
+//
+// Roles (8 warps): warp 0 issues the TMA copies (the Q tile once, then the
+// K/V pairs, one box per lane); warp 2 issues the S MMAs and warp 3 the P.V
+// MMAs (one thread each); warps 4-7 build the block union, then run the
+// online softmax one row per thread and the epilogue.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -36,7 +41,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
     B_QFULL = 0, B_LIST, B_DONE, B_PVFULL, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
-    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_PF0, B_PF1
+    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_PF0, B_PF1, B_DONES
 };
 
 constexpr uint32_t TM_S = 0;    // buffer b at b*128 (keys of the pair)
@@ -87,6 +92,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_LIST], kRows);
         mbar_init(&bars[B_DONE], 1);
+        mbar_init(&bars[B_DONES], 1);
         mbar_init(&bars[B_PVFULL], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[B_SFULL0 + s], 1);
@@ -173,33 +179,28 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                 mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // -------------------------------------------------------------- MMA
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- MMA
+        // Two issuing threads: warp 2 issues S of each pair, warp 3 the P.V
+        // products (whose completion frees a K/V stage), so a ready P.V never
+        // queues behind the next pair's S issue.  TMEM columns are disjoint
+        // (S buffers vs O); each commit covers its own thread's MMAs.
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(128, 128, false, false);
-            const uint32_t idO = idesc_bf16(128, 128, false, true);
-            const uint32_t q_s = smem_u32(sm + OFF_Q), kv_s = smem_u32(sm + OFF_KV);
+            const uint32_t kv_s = smem_u32(sm + OFF_KV);
             bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
             const int U = ok ? *n_list : 0;
             const int npairs = (U + 1) >> 1;
-            int si = 0, oi = 0;
-            uint64_t t_last = globaltimer();
-            while (ok && oi < npairs && !*abort_flag) {
-                bool progressed = false;
-                if (oi < si && mbar_test(&bars[B_PF0 + oi % NS], (oi / NS) & 1)) {
-                    tc_fence_after();
-                    const int s = oi % NS;
-                    const uint32_t p_s = kv_s + s * kPairBytes, v_s = p_s + kTileBytes;
-                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: P (K-major, 2 halves) x V pair (MN-major)
-                        mma_bf16(tmem + TM_O, sdesc_sw128(p_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(v_s + kk * 2048, kHalfBytes, 1024), idO, (oi > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars[B_PVFULL]);
-                    mma_commit(&bars[B_KVE0 + s]);
-                    ++oi;
-                    progressed = true;
-                }
-                if (si < npairs && si < oi + 2 && mbar_test(&bars[B_KVF0 + si % NS], (si / NS) & 1) &&
-                    mbar_test(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1)) {
+            if (warp == 2) {
+                const uint32_t idS = idesc_bf16(128, 128, false, false);
+                const uint32_t q_s = smem_u32(sm + OFF_Q);
+                for (int si = 0; si < npairs && ok; ++si) {
+                    // the pair's K/V have landed; the softmax has taken S of
+                    // pair si - 2 out of this TMEM buffer
+                    if (!mbar_wait(&bars[B_KVF0 + si % NS], (si / NS) & 1, abort_flag) ||
+                        !mbar_wait(&bars[B_SFREE0 + (si & 1)], ((si >> 1) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t k_s = kv_s + (si % NS) * kPairBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
@@ -208,17 +209,31 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                                  sdesc_sw128(k_s + o, 16, 1024), idS, kk > 0);
                     }
                     mma_commit(&bars[B_SFULL0 + (si & 1)]);
-                    ++si;
-                    progressed = true;
                 }
-                if (progressed)
-                    t_last = globaltimer();
-                else if (globaltimer() - t_last > kWaitLimitNs)
-                    *abort_flag = 1;
+                mma_commit(&bars[B_DONES]);
+                volatile int never = 0;
+                mbar_wait(&bars[B_DONES], 0, &never);
+            } else {
+                const uint32_t idO = idesc_bf16(128, 128, false, true);
+                for (int oi = 0; oi < npairs && ok; ++oi) {
+                    if (!mbar_wait(&bars[B_PF0 + oi % NS], (oi / NS) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int s = oi % NS;
+                    const uint32_t p_s = kv_s + s * kPairBytes, v_s = p_s + kTileBytes;
+                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: P (K-major, 2 halves) x V pair (MN-major)
+                        mma_bf16(tmem + TM_O, sdesc_sw128(p_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(v_s + kk * 2048, kHalfBytes, 1024), idO, (oi > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars[B_PVFULL]);
+                    mma_commit(&bars[B_KVE0 + s]);
+                }
+                // O is final once this commit completes
+                mma_commit(&bars[B_DONE]);
+                volatile int never = 0;
+                mbar_wait(&bars[B_DONE], 0, &never);
             }
-            mma_commit(&bars[B_DONE]);
-            volatile int never = 0;
-            mbar_wait(&bars[B_DONE], 0, &never);
         }
         __syncwarp();
     } else if (warp >= 4) {
