@@ -44,20 +44,20 @@ def lib():
         L.oracle_validate_index.restype = C.c_int
         L.oracle_validate_index.argtypes = [_i64] * 5 + [_ptr, _ptr]
         common = [_i64] * 7 + [_dbl, _ptr]
-        L.oracle_sel_fwd.restype = None
-        L.oracle_sel_fwd.argtypes = common + [_ptr] * 6
-        L.oracle_sel_bwd.restype = None
-        L.oracle_sel_bwd.argtypes = common + [_ptr] * 10
+        L.oracle_sel_fwd_w.restype = None
+        L.oracle_sel_fwd_w.argtypes = common + [_ptr] * 6 + [_i64]
+        L.oracle_sel_bwd_w.restype = None
+        L.oracle_sel_bwd_w.argtypes = common + [_ptr] * 11 + [_i64]
         L.oracle_inverse_index.restype = None
         L.oracle_inverse_index.argtypes = [_i64] * 5 + [_ptr, _ptr, _i64, _ptr, _ptr]
         L.oracle_do_dot.restype = None
         L.oracle_do_dot.argtypes = [_i64] * 4 + [_ptr] * 4
-        L.oracle_count_pairs.restype = _i64
-        L.oracle_count_pairs.argtypes = [_i64] * 6 + [_ptr, _ptr]
-        L.oracle_sel_rows.restype = None
-        L.oracle_sel_rows.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 6
-        L.oracle_sel_keys.restype = None
-        L.oracle_sel_keys.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5
+        L.oracle_count_pairs_w.restype = _i64
+        L.oracle_count_pairs_w.argtypes = [_i64] * 6 + [_ptr, _ptr, _i64]
+        L.oracle_sel_rows_w.restype = None
+        L.oracle_sel_rows_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 6 + [_i64]
+        L.oracle_sel_keys_w.restype = None
+        L.oracle_sel_keys_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5 + [_i64]
         _lib = L
     return _lib
 
@@ -94,19 +94,19 @@ def _shape(q, k, idx, cu_seqlens):
     return B, Hq, Hkv, T, D, S
 
 
-def sel_fwd(q, k, v, idx, bs, scale=None, cu_seqlens=None):
-    """Returns (O, LSE) in fp64."""
+def sel_fwd(q, k, v, idx, bs, scale=None, cu_seqlens=None, window=0):
+    """Returns (O, LSE) in fp64.  window > 0: keys k with t - k < window only."""
     q, k, v, idx, cu = _f64(q), _f64(k), _f64(v), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
     o = np.zeros_like(q)
     lse = np.zeros(q.shape[:-1], dtype=np.float64)
-    lib().oracle_sel_fwd(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                         _p(o), _p(lse))
+    lib().oracle_sel_fwd_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                           _p(o), _p(lse), int(window))
     return o, lse
 
 
-def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False):
+def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False, window=0):
     """Returns dict with dq, dk, dv, o, lse (and dsum = row sums of dS)."""
     q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
@@ -115,8 +115,8 @@ def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False):
     o = np.zeros_like(q)
     lse = np.zeros(q.shape[:-1], dtype=np.float64)
     dsum = np.zeros(q.shape[:-1], dtype=np.float64) if want_dsum else None
-    lib().oracle_sel_bwd(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                         _p(dO), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(dsum))
+    lib().oracle_sel_bwd_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                           _p(dO), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(dsum), int(window))
     out = dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse)
     if want_dsum:
         out["dsum"] = dsum
@@ -163,17 +163,17 @@ def do_dot(o, dO, cu_seqlens=None):
     return out
 
 
-def count_pairs(idx, Hq, bs, cu_seqlens=None):
+def count_pairs(idx, Hq, bs, cu_seqlens=None, window=0):
     idx, cu = _i32(idx), _i32(cu_seqlens)
     if cu is None:
         B, Hkv, T, S = idx.shape
     else:
         T, Hkv, S = idx.shape
         B = len(cu) - 1
-    return int(lib().oracle_count_pairs(B, Hq, Hkv, T, bs, S, _p(cu), _p(idx)))
+    return int(lib().oracle_count_pairs_w(B, Hq, Hkv, T, bs, S, _p(cu), _p(idx), int(window)))
 
 
-def sel_rows(q, k, v, idx, dO, bs, rows, scale=None, cu_seqlens=None):
+def sel_rows(q, k, v, idx, dO, bs, rows, scale=None, cu_seqlens=None, window=0):
     """rows: int array [n, 3] of (b, h, t).  Returns (o [n,D], lse [n], dq [n,D])."""
     q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
@@ -182,12 +182,12 @@ def sel_rows(q, k, v, idx, dO, bs, rows, scale=None, cu_seqlens=None):
     rb, rh, rt = (np.ascontiguousarray(rows[:, i]) for i in range(3))
     n = rows.shape[0]
     o, lse, dq = np.zeros((n, D)), np.zeros(n), np.zeros((n, D))
-    lib().oracle_sel_rows(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                          _p(dO), n, _p(rb), _p(rh), _p(rt), _p(o), _p(lse), _p(dq))
+    lib().oracle_sel_rows_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                            _p(dO), n, _p(rb), _p(rh), _p(rt), _p(o), _p(lse), _p(dq), int(window))
     return o, lse, dq
 
 
-def sel_keys(q, k, v, idx, dO, bs, keys, scale=None, cu_seqlens=None):
+def sel_keys(q, k, v, idx, dO, bs, keys, scale=None, cu_seqlens=None, window=0):
     """keys: int array [n, 3] of (b, g, key).  Returns (dk [n,D], dv [n,D])."""
     q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
@@ -196,6 +196,6 @@ def sel_keys(q, k, v, idx, dO, bs, keys, scale=None, cu_seqlens=None):
     kb, kg, kk = (np.ascontiguousarray(keys[:, i]) for i in range(3))
     n = keys.shape[0]
     dk, dv = np.zeros((n, D)), np.zeros((n, D))
-    lib().oracle_sel_keys(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                          _p(dO), n, _p(kb), _p(kg), _p(kk), _p(dk), _p(dv))
+    lib().oracle_sel_keys_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                            _p(dO), n, _p(kb), _p(kg), _p(kk), _p(dk), _p(dv), int(window))
     return dk, dv

@@ -15,6 +15,7 @@
  *   G = Hq / Hkv, query head h reads kv head g = h / G.
  *   sel(t)  = { idx[b,g,t,s] : 0 <= s < S, idx != -1 }
  *   key k is attended by row (b,h,t) iff k <= t and k / bs is in sel(t)
+ *   (and, with a sliding window W >= 1, t - k < W)
  *   s_tk    = scale * <q_t, k_k>
  *   LSE_t   = log sum_k exp(s_tk)        (max-shifted; -inf for an empty row)
  *   P_tk    = exp(s_tk - LSE_t)
@@ -25,6 +26,10 @@
  *   dQ_t    = scale * sum_k dS_tk k_k
  *   dK_k    = scale * sum_{h in group, t} dS_tk q_t
  *   dV_k    = sum_{h in group, t} P_tk dO_t
+ *
+ * The window is the sliding-window option of the cuDNN-frontend page's
+ * dense causal backward (SWA); W = 0 means no window.  The *_w entry points
+ * take it; the others use W = 0.
  *
  * Readings of points the pages leave open: scale is passed in (callers use
  * 1/sqrt(D)); keys after t inside the own block are masked (causal); -1
@@ -48,14 +53,18 @@ typedef struct {
     int64_t B, Hq, Hkv, T, D, bs, S;
     double scale;
     const int32_t *cu; /* NULL: fixed length */
+    int64_t window;    /* 0: none; else keys k with t - k < window only */
 } prob_t;
 
 static prob_t mk(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D,
                  int64_t bs, int64_t S, double scale, const int32_t *cu)
 {
-    prob_t p = {B, Hq, Hkv, T, D, bs, S, scale, cu};
+    prob_t p = {B, Hq, Hkv, T, D, bs, S, scale, cu, 0};
     return p;
 }
+
+/* 1 if the window lets row t see key kk (kk <= t is checked elsewhere) */
+static int in_window(const prob_t *p, int64_t t, int64_t kk) { return p->window <= 0 || t - kk < p->window; }
 
 static int64_t seq_len(const prob_t *p, int64_t b)
 {
@@ -145,6 +154,8 @@ static int64_t row_scores(const prob_t *p, const double *q, const double *k, con
         if (j < 0)
             continue;
         for (int64_t kk = j * p->bs; kk < (j + 1) * p->bs && kk <= t; ++kk) {
+            if (!in_window(p, t, kk))
+                continue;
             keys[n] = kk;
             sc[n] = p->scale * dot(qt, k + row_off(p, p->Hkv, b, g, kk), p->D);
             ++n;
@@ -198,12 +209,13 @@ static int64_t n_rows_total(const prob_t *p)
 }
 
 /* Forward: o (layout of q) and lse. */
-void oracle_sel_fwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
-                    int64_t S, double scale, const int32_t *cu, const double *q,
-                    const double *k, const double *v, const int32_t *idx, double *o,
-                    double *lse)
+void oracle_sel_fwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                      int64_t S, double scale, const int32_t *cu, const double *q,
+                      const double *k, const double *v, const int32_t *idx, double *o,
+                      double *lse, int64_t window)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    p.window = window;
 #pragma omp parallel
     {
         int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
@@ -227,13 +239,14 @@ void oracle_sel_fwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, in
  *           the group that attends k.
  * o_out / lse_out / dsum_out may be NULL.
  */
-void oracle_sel_bwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
-                    int64_t S, double scale, const int32_t *cu, const double *q,
-                    const double *k, const double *v, const int32_t *idx, const double *dO,
-                    double *dq, double *dk, double *dv, double *o_out, double *lse_out,
-                    double *dsum_out)
+void oracle_sel_bwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                      int64_t S, double scale, const int32_t *cu, const double *q,
+                      const double *k, const double *v, const int32_t *idx, const double *dO,
+                      double *dq, double *dk, double *dv, double *o_out, double *lse_out,
+                      double *dsum_out, int64_t window)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    p.window = window;
     const int64_t G = Hq / Hkv;
     const int64_t nrow = n_rows_total(&p) * Hq;
     double *O = o_out ? o_out : (double *)malloc(sizeof(double) * nrow * D);
@@ -291,7 +304,7 @@ void oracle_sel_bwd(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, in
                     dvk[d] = 0.0;
                 }
                 const int64_t j = kk / bs;
-                for (int64_t t = kk; t < seq_len(&p, b); ++t) {
+                for (int64_t t = kk; t < seq_len(&p, b) && in_window(&p, t, kk); ++t) {
                     if (!selects(&p, idx_row(&p, idx, b, g, t), j))
                         continue;
                     for (int64_t h = g * G; h < (g + 1) * G; ++h) {
@@ -354,10 +367,11 @@ void oracle_do_dot(int64_t B, int64_t Hq, int64_t T, int64_t D, const int32_t *c
 }
 
 /* Number of (query row, attended key) pairs summed over query heads. */
-int64_t oracle_count_pairs(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t bs, int64_t S,
-                           const int32_t *cu, const int32_t *idx)
+int64_t oracle_count_pairs_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t bs, int64_t S,
+                             const int32_t *cu, const int32_t *idx, int64_t window)
 {
     prob_t p = mk(B, Hq, Hkv, T, 1, bs, S, 1.0, cu);
+    p.window = window;
     const int64_t G = Hq / Hkv;
     int64_t n = 0;
     for (int64_t b = 0; b < B; ++b)
@@ -368,11 +382,13 @@ int64_t oracle_count_pairs(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_
                     int64_t j = row[s];
                     if (j < 0)
                         continue;
-                    int64_t hi = (j + 1) * bs - 1;
+                    int64_t hi = (j + 1) * bs - 1, lo = j * bs;
                     if (hi > t)
                         hi = t;
-                    if (hi >= j * bs)
-                        n += G * (hi - j * bs + 1);
+                    if (window > 0 && lo < t - window + 1)
+                        lo = t - window + 1;
+                    if (hi >= lo)
+                        n += G * (hi - lo + 1);
                 }
             }
     return n;
@@ -384,13 +400,14 @@ int64_t oracle_count_pairs(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_
  *
  * oracle_sel_rows: for each (b, h, t) in the list, O_t, LSE_t and dQ_t.
  */
-void oracle_sel_rows(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
-                     int64_t S, double scale, const int32_t *cu, const double *q,
-                     const double *k, const double *v, const int32_t *idx, const double *dO,
-                     int64_t n, const int64_t *rb, const int64_t *rh, const int64_t *rt,
-                     double *o_out, double *lse_out, double *dq_out)
+void oracle_sel_rows_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                       int64_t S, double scale, const int32_t *cu, const double *q,
+                       const double *k, const double *v, const int32_t *idx, const double *dO,
+                       int64_t n, const int64_t *rb, const int64_t *rh, const int64_t *rt,
+                       double *o_out, double *lse_out, double *dq_out, int64_t window)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    p.window = window;
     const int64_t G = Hq / Hkv;
 #pragma omp parallel
     {
@@ -424,13 +441,14 @@ void oracle_sel_rows(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, i
  * oracle_sel_keys: for each (b, g, key) in the list, dK and dV of that key;
  * LSE_t and D_t of every attending row are recomputed from scratch.
  */
-void oracle_sel_keys(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
-                     int64_t S, double scale, const int32_t *cu, const double *q,
-                     const double *k, const double *v, const int32_t *idx, const double *dO,
-                     int64_t n, const int64_t *kb, const int64_t *kg, const int64_t *kk_,
-                     double *dk_out, double *dv_out)
+void oracle_sel_keys_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                       int64_t S, double scale, const int32_t *cu, const double *q,
+                       const double *k, const double *v, const int32_t *idx, const double *dO,
+                       int64_t n, const int64_t *kb, const int64_t *kg, const int64_t *kk_,
+                       double *dk_out, double *dv_out, int64_t window)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    p.window = window;
     const int64_t G = Hq / Hkv;
 #pragma omp parallel
     {
@@ -446,7 +464,7 @@ void oracle_sel_keys(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, i
                 dkk[d] = 0.0;
                 dvk[d] = 0.0;
             }
-            for (int64_t t = kk; t < seq_len(&p, b); ++t) {
+            for (int64_t t = kk; t < seq_len(&p, b) && in_window(&p, t, kk); ++t) {
                 if (!selects(&p, idx_row(&p, idx, b, g, t), j))
                     continue;
                 for (int64_t h = g * G; h < (g + 1) * G; ++h) {

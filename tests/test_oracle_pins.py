@@ -15,7 +15,11 @@ Each pin targets a mistake the oracle could plausibly make:
 * closed forms for rows with one attended key;
 * -1 padding wherever it sits, slot order, empty rows;
 * the inverse index against a pure-Python brute force;
-* index validation cases.
+* index validation cases;
+* the sliding window (cuDNN-frontend page: the SDPA backward's window option)
+  against SDPA with a brute-force band mask, its two limits (W >= T is plain
+  causal attention, W = 1 attends the row's own key only), pair counts and
+  sampled entries.
 """
 import math
 
@@ -330,3 +334,71 @@ def test_planted_mistake_is_caught(monkeypatch):
     o_bad, _ = oracle.sel_fwd(q[:, perm], k, v, idx, bs)
     inv = np.argsort(perm)
     assert np.max(np.abs(o_bad[:, inv] - o_ref.numpy())) > 1e-3
+
+
+def _band_mask(B, Hkv, T, W):
+    """bool [B, Hkv, T, T]: k <= t and t - k < W, by brute force."""
+    m = np.zeros((B, Hkv, T, T), dtype=bool)
+    for t in range(T):
+        for k in range(T):
+            if k <= t and t - k < W:
+                m[:, :, t, k] = True
+    return torch.from_numpy(m)
+
+
+@pytest.mark.parametrize("W,G", [(5, 1), (13, 2), (8, 3), (1, 2)])
+def test_window_matches_band_masked_sdpa(W, G):
+    """Dense causal attention limited to the W most recent keys."""
+    B, Hkv, T, D, bs = 2, 2, 37, 8, 8
+    Hq = Hkv * G
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=4)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    scale = 1 / math.sqrt(D)
+    o_ref, dq_ref, dk_ref, dv_ref = _sdpa_reference(q, k, v, do, _band_mask(B, Hkv, T, W), scale)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, window=W)
+    np.testing.assert_allclose(r["o"], o_ref.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(r["dq"], dq_ref.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dk"], dk_ref.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dv"], dv_ref.numpy(), atol=1e-11, rtol=0)
+    o, lse = oracle.sel_fwd(q, k, v, idx, bs, window=W)
+    np.testing.assert_allclose(o, o_ref.numpy(), atol=1e-12, rtol=0)
+    assert oracle.count_pairs(idx, Hq, bs, window=W) == int(_band_mask(B, Hkv, T, W).sum()) * G
+
+
+def test_window_limits():
+    B, Hq, Hkv, T, D, bs = 1, 4, 2, 30, 8, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=6)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    full = oracle.sel_bwd(q, k, v, idx, do, bs)
+    wide = oracle.sel_bwd(q, k, v, idx, do, bs, window=T)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(wide[n], full[n])
+    # W = 1: each row sees its own key: O_t = v_t, LSE_t = scale q_t.k_t,
+    # P = 1 so dS = 0: no dQ / dK; dV_k = sum over the group's heads of dO_k
+    one = oracle.sel_bwd(q, k, v, idx, do, bs, window=1)
+    G = Hq // Hkv
+    vv = v.double().repeat_interleave(G, 1).numpy()
+    np.testing.assert_allclose(one["o"], vv, atol=1e-14, rtol=0)
+    sc = (q.double() * k.double().repeat_interleave(G, 1)).sum(-1).numpy() / math.sqrt(D)
+    np.testing.assert_allclose(one["lse"], sc, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(one["dq"], 0.0, atol=1e-14)
+    np.testing.assert_allclose(one["dk"], 0.0, atol=1e-14)
+    dv_ref = do.double().reshape(B, Hkv, G, T, D).sum(2).numpy()
+    np.testing.assert_allclose(one["dv"], dv_ref, atol=1e-13, rtol=0)
+
+
+def test_window_sampled_entries_agree_with_whole_problem():
+    B, Hq, Hkv, T, D, bs, W = 1, 4, 2, 41, 8, 8, 11
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=8)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, window=W)
+    rows = [(0, 0, 0), (0, 3, 10), (0, 1, 11), (0, 2, 40)]
+    o, lse, dq = oracle.sel_rows(q, k, v, idx, do, bs, rows, window=W)
+    for i, (b, h, t) in enumerate(rows):
+        np.testing.assert_allclose(o[i], r["o"][b, h, t], atol=1e-13, rtol=0)
+        np.testing.assert_allclose(dq[i], r["dq"][b, h, t], atol=1e-13, rtol=0)
+    keys = [(0, 0, 0), (0, 1, 29), (0, 0, 30), (0, 1, 40)]
+    dk, dv = oracle.sel_keys(q, k, v, idx, do, bs, keys, window=W)
+    for i, (b, g, kk) in enumerate(keys):
+        np.testing.assert_allclose(dk[i], r["dk"][b, g, kk], atol=1e-13, rtol=0)
+        np.testing.assert_allclose(dv[i], r["dv"][b, g, kk], atol=1e-13, rtol=0)
