@@ -30,6 +30,7 @@ SYMBOLS = (
     "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
     "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
     "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
+    "nsa_swa_fwd", "nsa_swa_bwd",
 )
 
 
@@ -83,6 +84,8 @@ def lib() -> C.CDLL:
         L.nsa_bwd_planned_workspace_size.restype = C.c_size_t
         L.nsa_bwd_planned_workspace_size.argtypes = [pp]
         L.nsa_sel_bwd_planned.argtypes = [pp] + [_P] * 12 + [_P, C.c_size_t, _P]
+        L.nsa_swa_fwd.argtypes = [pp, C.c_int32] + [_P] * 6 + [_P, C.c_size_t, _P]
+        L.nsa_swa_bwd.argtypes = [pp, C.c_int32] + [_P] * 10 + [_P, C.c_size_t, _P]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []
@@ -159,8 +162,10 @@ def _lse_shape(q, cu_seqlens):
 
 
 def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seqlen=None,
-            dense=False, ws=None, stream=None):
-    """Selection (or dense causal) forward through the C ABI: returns (o, lse)."""
+            dense=False, ws=None, stream=None, window=None):
+    """Selection (or dense causal, or with `window` sliding-window causal)
+    forward through the C ABI: returns (o, lse)."""
+    dense = dense or window is not None
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     o = torch.empty_like(q)
@@ -171,7 +176,10 @@ def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
     ws = workspace(n, q.device, "fwd") if ws is None else ws
     L = lib()
     st = _stream(stream)
-    if cu_seqlens is not None:
+    if window is not None:
+        s = L.nsa_swa_fwd(C.byref(p), int(window), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                          _ptr(lse), _ptr(ws), ws.numel(), st)
+    elif cu_seqlens is not None:
         s = L.nsa_sel_varlen_fwd(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v),
                                  _ptr(block_idx), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), st)
     elif dense:
@@ -200,9 +208,11 @@ def build_plan(q, k, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
 
 
 def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=None,
-            max_seqlen=None, dense=False, ws=None, stream=None, out=None, plan=None):
-    """Selection (or dense causal) backward through the C ABI: returns (dq, dk, dv).
-    With `plan` (from build_plan on the same block_idx) the index build is skipped."""
+            max_seqlen=None, dense=False, ws=None, stream=None, out=None, plan=None, window=None):
+    """Selection (or dense causal, or with `window` sliding-window causal)
+    backward through the C ABI: returns (dq, dk, dv).  With `plan` (from
+    build_plan on the same block_idx) the index build is skipped."""
+    dense = dense or window is not None
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     if out is None:
@@ -227,7 +237,10 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
         raise NsaError(1, "nsa_bwd_workspace_size")
     ws = workspace(n, q.device, "bwd") if ws is None else ws
     st = _stream(stream)
-    if cu_seqlens is not None:
+    if window is not None:
+        s = L.nsa_swa_bwd(C.byref(p), int(window), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                          _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), st)
+    elif cu_seqlens is not None:
         s = L.nsa_sel_varlen_bwd(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                                  _ptr(dO), _ptr(lse), _ptr(block_idx), _ptr(dq), _ptr(dk),
                                  _ptr(dv), _ptr(ws), ws.numel(), st)

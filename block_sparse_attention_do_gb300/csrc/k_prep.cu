@@ -75,6 +75,17 @@ __device__ __forceinline__ void decode_idx_row(const Geo &g, int64_t lin, int &b
 }
 
 // 0 = use, 1 = padding, 2 = invalid (reported), 3 = repeat (reported)
+// dense mode: tokens attending block j form the run [j*bs, end) of the
+// sequence, end = L, or with a window the last token whose window still
+// reaches the block's last key: t <= (j+1)*bs - 1 + window - 1
+__device__ __forceinline__ int dense_count(const Geo &g, int L, int j)
+{
+    int end = L;
+    if (g.window > 0)
+        end = min(end, (j + 1) * g.bs + g.window - 1);
+    return j * g.bs < end ? end - j * g.bs : 0;
+}
+
 __device__ __forceinline__ int classify(const int *row, int s, int t, int bs, int nbmax)
 {
     const int j = row[s];
@@ -174,8 +185,7 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
         if (i < n) {
             if (g.dense) {
                 const int b = i / (g.Hkv * g.nbmax), j = i % g.nbmax;
-                const int L = seq_len(g, b);
-                cnt = j * g.bs < L ? L - j * g.bs : 0;
+                cnt = dense_count(g, seq_len(g, b), j);
             } else {
                 cnt = counts[i];
             }
@@ -193,8 +203,7 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
             kvh = (i / g.nbmax) % g.Hkv;
             b = i / (g.Hkv * g.nbmax);
             if (g.dense) {
-                const int L = seq_len(g, b);
-                cnt = j * g.bs < L ? L - j * g.bs : 0;
+                cnt = dense_count(g, seq_len(g, b), j);
             } else {
                 cnt = counts[i];
             }

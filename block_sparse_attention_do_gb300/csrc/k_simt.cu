@@ -91,12 +91,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__re
         float m = -INFINITY, l = 0.f;
         const int *row = g.dense ? nullptr : idx_row(g, idx, b, kvh, t);
         const int ns = n_slots(g, t);
+        const int klo = key_lo(g, t);
         for (int s = 0; s < ns; ++s) {
             const int j = slot_block(g, row, s, t);
             if (j < 0)
                 continue;
             const int kend = min((j + 1) * g.bs, t + 1);
-            for (int kk = j * g.bs; kk < kend; ++kk) {
+            for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
                 const int64_t ko = row_off(g, g.Hkv, b, kvh, kk);
                 float part = 0.f;
 #pragma unroll
@@ -153,12 +154,13 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(Geo g, const T *__res
         if (L != -INFINITY) {
             const int *row = g.dense ? nullptr : idx_row(g, idx, b, kvh, t);
             const int ns = n_slots(g, t);
+            const int klo = key_lo(g, t);
             for (int s = 0; s < ns; ++s) {
                 const int j = slot_block(g, row, s, t);
                 if (j < 0)
                     continue;
                 const int kend = min((j + 1) * g.bs, t + 1);
-                for (int kk = j * g.bs; kk < kend; ++kk) {
+                for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
                     const int64_t ko = row_off(g, g.Hkv, b, kvh, kk);
                     float ps = 0.f, pd = 0.f;
                     float kv[DPL];
@@ -230,6 +232,8 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
             const int t = g.dense ? beg + e : rows[beg + e];
             if (t < kk)
                 continue;
+            if (g.window > 0 && t - kk >= g.window)
+                break;  // tokens ascend: the rest are past the window too
             for (int h = kvh * g.G; h < (kvh + 1) * g.G; ++h) {
                 const int64_t qo = row_off(g, g.Hq, b, h, t);
                 const int64_t so = stat_off(g, b, h, t);

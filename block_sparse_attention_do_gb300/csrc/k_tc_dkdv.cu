@@ -418,10 +418,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 const float l2 = lse_s[st * kRows + r], dl = dlt_s[st * kRows + r];
                 // keys k0 + c with c <= tok - k0 are attended (the token selected block j)
                 const int lim = tok < 0 ? -1 : tok - k0;
+                const int lo = tok < 0 ? 0 : key_lo(g, tok) - k0;  // window's left edge
                 uint32_t pk[32], dk_[32];
-                if (__all_sync(0xffffffffu, lim < 0 || lim >= kKeys - 1)) {
-                    // no row of the warp ends inside the block: a row attends
-                    // all of it or none; none gets a +inf bias (exp2(-inf) = 0)
+                if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
+                    // no row of the warp ends or starts inside the block: a row
+                    // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                     const float bias = lim >= 0 ? l2 : __int_as_float(0x7f800000);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
@@ -435,9 +436,9 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
                         float p0 = 0.f, p1 = 0.f;
-                        if (c <= lim)
+                        if (c <= lim && c >= lo)
                             p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                        if (c + 1 <= lim)
+                        if (c + 1 <= lim && c + 1 >= lo)
                             p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
                         const float d0 = p0 * (__uint_as_float(dv_[c]) - dl);
                         const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dl);

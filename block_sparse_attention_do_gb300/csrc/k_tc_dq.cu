@@ -294,11 +294,13 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             mbar_arrive(&bars[B_SFREE]);
             const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
             const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+            // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
             const int lim = sel ? t - j * kKeys : -1;
+            const int lo = key_lo(g, t) - j * kKeys;
             uint32_t dk_[32];
-            if (__all_sync(0xffffffffu, lim < 0 || lim >= kKeys - 1)) {
-                // no row of the warp ends inside the block: a row attends all
-                // of it or none; none gets a +inf bias (exp2(-inf) = 0)
+            if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
+                // no row of the warp ends or starts inside the block: a row
+                // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                 if (__any_sync(0xffffffffu, sel)) {
                     const float bias = sel ? l2 : __int_as_float(0x7f800000);
 #pragma unroll
@@ -317,9 +319,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     float p0 = 0.f, p1 = 0.f;
-                    if (c <= lim)
+                    if (c <= lim && c >= lo)
                         p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                    if (c + 1 <= lim)
+                    if (c + 1 <= lim && c + 1 >= lo)
                         p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
                     dk_[c >> 1] =
                         pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));

@@ -269,21 +269,23 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bars[B_SFREE0 + s]);
-            int lim[2];
+            // block e: the row attends keys j*64 + c, lo[e] <= c <= lim[e]
+            int lim[2], lo[2];
             bool anysel = false;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
                 const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
                 lim[e] = sel ? t - j * kKeys : -1;
+                lo[e] = key_lo(g, t) - j * kKeys;
                 anysel |= sel;
             }
             uint32_t pk[64];
             if (__any_sync(0xffffffffu, anysel)) {
                 // no row of the warp ends inside either block: a row attends a
                 // whole block or none of it; none gets a -inf bias
-                const bool whole = __all_sync(0xffffffffu, (lim[0] < 0 || lim[0] >= kKeys - 1) &&
-                                                               (lim[1] < 0 || lim[1] >= kKeys - 1));
+                const bool whole = __all_sync(0xffffffffu, (lim[0] < 0 || (lim[0] >= kKeys - 1 && lo[0] <= 0)) &&
+                                                               (lim[1] < 0 || (lim[1] >= kKeys - 1 && lo[1] <= 0)));
                 float mb = -INFINITY;
                 if (whole) {
                     const float b0 = lim[0] >= 0 ? 0.f : -INFINITY, b1 = lim[1] >= 0 ? 0.f : -INFINITY;
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                     for (int c = 0; c < 128; ++c) {
                         const float x = __uint_as_float(sv[c]) * g.scale_l2;
                         sv[c] = __float_as_uint(x);
-                        if ((c & 63) <= lim[c >> 6])
+                        if ((c & 63) <= lim[c >> 6] && (c & 63) >= lo[c >> 6])
                             mb = fmaxf(mb, x);
                     }
                 }
@@ -342,9 +344,11 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                 } else {
 #pragma unroll
                     for (int c = 0; c < 128; c += 2) {
-                        const int lm = lim[c >> 6];
-                        const float p0 = ((c & 63) <= lm) ? ex2(__uint_as_float(sv[c]) - m) : 0.f;
-                        const float p1 = (((c + 1) & 63) <= lm) ? ex2(__uint_as_float(sv[c + 1]) - m) : 0.f;
+                        const int lm = lim[c >> 6], lw = lo[c >> 6];
+                        const float p0 = ((c & 63) <= lm && (c & 63) >= lw) ? ex2(__uint_as_float(sv[c]) - m) : 0.f;
+                        const float p1 = (((c + 1) & 63) <= lm && ((c + 1) & 63) >= lw)
+                                             ? ex2(__uint_as_float(sv[c + 1]) - m)
+                                             : 0.f;
                         rs += p0 + p1;
                         pk[c >> 1] = pack_bf16(p0, p1);
                     }

@@ -21,8 +21,10 @@ enum Mode { SPARSE = 0, DENSE = 1 };
 
 // Checks the problem and fills the device geometry.  `want_thd` is the
 // layout the entry point requires.
-nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g)
+nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g, int window = 0)
 {
+    if (window < 0 || (window > 0 && mode != DENSE))
+        return NSA_ERR_INVALID_ARG;
     if (!p)
         return NSA_ERR_INVALID_ARG;
     if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->T < 1)
@@ -61,6 +63,7 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     g.ntok = (int)ntok;
     g.thd = want_thd ? 1 : 0;
     g.dense = mode == DENSE ? 1 : 0;
+    g.window = window;
     g.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->D);
     g.scale_l2 = g.scale * 1.4426950408889634f;
     g.cu = cu;
@@ -182,10 +185,10 @@ nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 
 nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const int32_t *idx, void *o, float *lse,
-                   void *ws, size_t ws_bytes, void *stream)
+                   void *ws, size_t ws_bytes, void *stream, int window = 0)
 {
     Geo g;
-    nsa_status s = make_geo(p, thd, mode, cu, g);
+    nsa_status s = make_geo(p, thd, mode, cu, g, window);
     if (s != NSA_OK)
         return s;
     if (!q || !k || !v || !o || !lse || (mode == SPARSE && !idx))
@@ -246,10 +249,10 @@ nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanL
 nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
                    const int32_t *idx, const void *plan, void *dq, void *dk, void *dv, void *ws,
-                   size_t ws_bytes, void *stream)
+                   size_t ws_bytes, void *stream, int window = 0)
 {
     Geo g;
-    nsa_status s = make_geo(p, thd, mode, cu, g);
+    nsa_status s = make_geo(p, thd, mode, cu, g, window);
     if (s != NSA_OK)
         return s;
     if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || (mode == SPARSE && !idx))
@@ -464,6 +467,30 @@ nsa_status nsa_sel_bwd_planned(const nsa_problem *p, const int32_t *cu_seqlens, 
         return NSA_ERR_INVALID_ARG;
     return run_bwd(p, thd, SPARSE, cu_seqlens, q, k, v, o, dO, lse, block_idx, plan, dq, dk, dv, ws, ws_bytes,
                    stream);
+}
+
+nsa_status nsa_swa_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const void *q,
+                       const void *k, const void *v, void *o, float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!p || window < 1)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_fwd(p, thd, DENSE, cu_seqlens, q, k, v, nullptr, o, lse, ws, ws_bytes, stream, window);
+}
+
+nsa_status nsa_swa_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const void *q,
+                       const void *k, const void *v, const void *o, const void *dO, const float *lse, void *dq,
+                       void *dk, void *dv, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!p || window < 1)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_bwd(p, thd, DENSE, cu_seqlens, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws, ws_bytes,
+                   stream, window);
 }
 
 nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,

@@ -21,12 +21,19 @@ struct Geo {
     int ntok;        // B*T (BHTD) or total_tokens (THD)
     int thd;         // 1 for the packed layout
     int dense;       // 1: every row selects blocks 0..t/bs (no index read)
+    int window;      // > 0: keys k with t - k < window only (sliding window); 0: none
     float scale;     // softmax scale
     float scale_l2;  // scale * log2(e)
     const int *cu;   // cu_seqlens (THD) or nullptr
 };
 
 __device__ __forceinline__ int seq_len(const Geo &g, int b) { return g.thd ? g.cu[b + 1] - g.cu[b] : g.T; }
+
+// first key row t may attend (the sliding window's left edge; 0 without one)
+__host__ __device__ __forceinline__ int key_lo(const Geo &g, int t)
+{
+    return (g.window > 0 && t - g.window + 1 > 0) ? t - g.window + 1 : 0;
+}
 
 // element offset of the D-vector of (b, head, t) in a tensor with H heads
 __device__ __forceinline__ int64_t row_off(const Geo &g, int H, int b, int h, int t)
@@ -65,11 +72,12 @@ __device__ __forceinline__ int seq_of_token(const Geo &g, int tok)
     return lo;
 }
 
-// does row (b, kvh, t) select block j?  (dense: every block up to t/bs)
+// does row (b, kvh, t) select block j?  (dense: every block up to t/bs that
+// reaches into the window)
 __device__ __forceinline__ bool row_selects(const Geo &g, const int *idx, int b, int kvh, int t, int j)
 {
     if (g.dense)
-        return j <= t / g.bs;
+        return j <= t / g.bs && j >= key_lo(g, t) / g.bs;
     const int *r = idx_row(g, idx, b, kvh, t);
     for (int s = 0; s < g.S; ++s)
         if (r[s] == j)

@@ -92,8 +92,8 @@ __device__ __forceinline__ int qtile_union(const Geo &g, const int *idx, int b, 
         ubits[i] = 0;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (g.dense) {
-        const int jmax = (t0 + nvalid - 1) / g.bs;
-        for (int j = tid; j <= jmax; j += 128)
+        const int jmin = key_lo(g, t0) / g.bs, jmax = (t0 + nvalid - 1) / g.bs;
+        for (int j = jmin + tid; j <= jmax; j += 128)
             atomicOr(&ubits[j >> 5], 1u << (j & 31));
     } else {
         for (int i = tid; i < nvalid * g.S; i += 128) {
@@ -138,7 +138,7 @@ __device__ __forceinline__ int qtile_union(const Geo &g, const int *idx, int b, 
 // does the row's token select block j?  (valid rows only)
 __device__ __forceinline__ bool qtile_selects(const Geo &g, const uint32_t *my_mask, int t, int j)
 {
-    return g.dense ? (j <= t / g.bs) : (((my_mask[j >> 5] >> (j & 31)) & 1u) != 0);
+    return g.dense ? (j <= t / g.bs && j >= key_lo(g, t) / g.bs) : (((my_mask[j >> 5] >> (j & 31)) & 1u) != 0);
 }
 
 }  // namespace nsa

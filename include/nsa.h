@@ -146,6 +146,24 @@ nsa_status nsa_sel_varlen_bwd(const nsa_problem *p, const int32_t *cu_seqlens, c
                               void *dv, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Sliding-window causal attention (cuDNN-frontend page: the dense causal
+ * SDPA backward's sliding-window option; NSA's sliding-window branch): the
+ * dense causal case restricted to each row's `window` most recent keys,
+ * k in (t - window, t].  window >= 1 (else NSA_ERR_INVALID_ARG); a window of
+ * T or more is the dense causal case.  cu_seqlens is NULL for BHTD
+ * (p->layout NSA_LAYOUT_BHTD) and the packed-row offsets for THD, where the
+ * window applies within each sequence.  p->S is ignored; the workspaces are
+ * the dense ones (nsa_fwd_workspace_size, nsa_bwd_workspace_size).
+ */
+nsa_status nsa_swa_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens,
+                       const void *q, const void *k, const void *v, void *o, float *lse,
+                       void *ws, size_t ws_bytes, void *stream);
+nsa_status nsa_swa_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens,
+                       const void *q, const void *k, const void *v, const void *o,
+                       const void *dO, const float *lse, void *dq, void *dk, void *dv,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Reusable backward plan.  The pages build nothing like it: it is the inverse
  * index of one block_idx tensor (block -> ascending list of the tokens that
  * selected it, see nsa_build_inverse_index) together with the dK/dV work

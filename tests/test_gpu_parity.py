@@ -49,12 +49,13 @@ def _maxerr(got, ref):
     return float(np.max(err))
 
 
-def _run(q, k, v, do, idx, bs, cu=None, dense=False):
+def _run(q, k, v, do, idx, bs, cu=None, dense=False, window=None):
     g = [x.to(DEV) for x in (q, k, v, do)]
-    gi = None if dense else idx.to(DEV)
+    gi = None if (dense or window is not None) else idx.to(DEV)
     gcu = None if cu is None else cu.to(DEV)
-    o, lse = api.sel_fwd(g[0], g[1], g[2], gi, bs, cu_seqlens=gcu, dense=dense)
-    dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, gi, bs, cu_seqlens=gcu, dense=dense)
+    o, lse = api.sel_fwd(g[0], g[1], g[2], gi, bs, cu_seqlens=gcu, dense=dense, window=window)
+    dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, gi, bs, cu_seqlens=gcu, dense=dense,
+                             window=window)
     torch.cuda.synchronize()
     return dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
@@ -159,6 +160,43 @@ def test_varlen(dtype, Hq):
     idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=3)
     got = _run(q, k, v, do, idx, bs, cu=cu)
     ref = oracle.sel_bwd(q, k, v, idx, do, bs, cu_seqlens=cu)
+    _compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype,shape,W", [
+    (torch.bfloat16, (1, 16, 1, 300, 128, 64, 1), 100),  # tensor cores; the window edge cuts blocks
+    (torch.bfloat16, (1, 16, 1, 300, 128, 64, 1), 64),   # window = one block
+    (torch.bfloat16, (2, 32, 2, 200, 128, 64, 1), 1),    # own key only
+    (torch.bfloat16, (1, 16, 1, 300, 128, 64, 1), 1000), # wider than T: dense causal
+    (torch.float32, (2, 6, 2, 150, 64, 32, 1), 45),      # SIMT
+    (torch.bfloat16, (1, 4, 1, 150, 128, 64, 1), 70),    # G = 4: head-major tiles, cp.async gathers
+])
+def test_sliding_window(dtype, shape, W):
+    B, Hq, Hkv, T, D, bs, _ = shape
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=14)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    got = _run(q, k, v, do, None, bs, window=W)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs, window=W)
+    _compare(got, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sliding_window_varlen(dtype):
+    lengths = [130, 1, 64, 257, 90]
+    Hq, Hkv, D, bs, W = 16, 1, 128, 64, 75
+    total = sum(lengths)
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=dtype, seed=15, layout="thd")
+    nb = (max(lengths) + bs - 1) // bs
+    # the oracle's dense index: every block up to the token's own
+    dense = np.full((total, Hkv, nb), -1, dtype=np.int32)
+    off = 0
+    for L in lengths:
+        for t in range(L):
+            dense[off + t, :, : t // bs + 1] = np.arange(t // bs + 1)
+        off += L
+    got = _run(q, k, v, do, None, bs, cu=cu, window=W)
+    ref = oracle.sel_bwd(q, k, v, torch.from_numpy(dense), do, bs, cu_seqlens=cu, window=W)
     _compare(got, ref, dtype)
 
 
