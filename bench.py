@@ -43,6 +43,7 @@ WORKLOAD_NAME = ("NSA selection fwd+bwd, bf16: B=1 Hq=32 Hkv=2 (G=16) T=8192 D=1
 ALG_FLOP_PER_PAIR_PER_D = {"dkdv_tc": 8, "dq_tc": 6, "fwd_tc": 4,
                            "dkdv_simt": 8, "dq_simt": 6, "fwd_simt": 4}
 FLUSH_BYTES = 256 << 20  # > the 129 MB L2
+SWA_WINDOW = 512  # sliding-window leg: keys (t - 512, t]
 
 
 def env_rank():
@@ -346,6 +347,32 @@ def run_ours(args):
                "scope": "nsa_sel_bwd_planned with a plan built once for idx (nsa_plan_build, timed "
                         "apart); same L2 flush between steps"}
 
+    # ---- sliding-window causal attention (nsa_swa_fwd / nsa_swa_bwd) on the
+    # same tensors: every row attends its SWA_WINDOW most recent keys
+    Wn = SWA_WINDOW
+    swa_pairs = B * Hq * sum(min(t + 1, Wn) for t in range(T))
+    o_w, lse_w = api.sel_fwd(q, k, v, None, bs, window=Wn, ws=ws_f)
+    for _ in range(2):
+        api.sel_bwd(q, k, v, o_w, do, lse_w, None, bs, window=Wn, ws=ws_b, out=outs)
+    n_sw = max(3, min(K, 20))
+    w_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_sw)]
+    for i in range(n_sw):
+        flush.zero_()
+        w_ev[i][0].record(st)
+        o_w, lse_w = api.sel_fwd(q, k, v, None, bs, window=Wn, ws=ws_f)
+        w_ev[i][1].record(st)
+        api.sel_bwd(q, k, v, o_w, do, lse_w, None, bs, window=Wn, ws=ws_b, out=outs)
+        w_ev[i][2].record(st)
+    torch.cuda.synchronize()
+    if api.get_error(ws_b) or api.get_error(ws_f):
+        raise RuntimeError("device error in the sliding-window leg")
+    sw_bwd = sum(e[1].elapsed_time(e[2]) for e in w_ev)
+    sw_fwd = sum(e[0].elapsed_time(e[1]) for e in w_ev)
+    sw_bwd_max, sw_flop = aggregate(sw_bwd, 10.0 * D * swa_pairs * n_sw, dev)
+    swa = {"window": Wn, "pairs": swa_pairs, "value": sw_flop / (sw_bwd_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "bwd_ms": sw_bwd / n_sw, "fwd_ms": sw_fwd / n_sw, "steps": n_sw,
+           "scope": "nsa_swa_fwd + nsa_swa_bwd, same shapes, 10*D*pairs / backward time, L2 flushed"}
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if True:  # every rank: the aggregation below is collective
@@ -395,7 +422,8 @@ def run_ours(args):
             "bwd_ms": bwd_ms / K, "fwd_ms": fwd_ms / K, "wall_s": t_wall,
             "kernels": {n: {"ms_avg": e["ms_avg"], "launches": e["launches"], "share": e["share"]}
                         for n, e in sorted(kern.items(), key=lambda kv: -kv[1]["ms_total"])},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "planned": planned, "gpu_launches": len(recs),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "planned": planned, "swa": swa,
+            "gpu_launches": len(recs),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
