@@ -166,8 +166,9 @@ __device__ __forceinline__ int block_scan_excl(int v, int &total, int *sm)
 }
 
 // One block of 1024 threads: offsets, the unit list (full-size chunks
-// first, then the shorter tails, so that a strided persistent schedule
-// starts with the longest work) and the per-block chunk/partial-slot table.
+// first, then the shorter tails, longest first, so that the dK/dV kernel's
+// snake schedule of units over CTAs starts with the longest work and ends
+// balanced) and the per-block chunk/partial-slot table.
 __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__restrict__ counts,
                                                         int *__restrict__ offsets,
                                                         Unit *__restrict__ units,
@@ -175,45 +176,93 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
                                                         int *__restrict__ blk_slot, WsHeader *hdr,
                                                         int chunk)
 {
+    // Tails (each block's last, partial chunk) go after the full chunks,
+    // longest first by kTailBins bins (stable within a bin), so that the
+    // dK/dV kernel's snake assignment of units to CTAs balances their work.
+    constexpr int kTailBins = 16;
     __shared__ int sm[80];
+    __shared__ int wbin[32][kTailBins];
+    __shared__ int binbase[kTailBins];
     const int n = g.B * g.Hkv * g.nbmax;
-    // pass 1: totals of full chunks (to place the tails after them)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    auto block_count = [&](int i) {
+        if (i >= n)
+            return 0;
+        if (g.dense) {
+            const int b = i / (g.Hkv * g.nbmax), j = i % g.nbmax;
+            return dense_count(g, seq_len(g, b), j);
+        }
+        return counts[i];
+    };
+    auto tail_bin = [&](int cnt) {
+        const int r = cnt % chunk;  // tail length, 1 .. chunk-1
+        return r ? (kTailBins - 1) - (int)(((int64_t)(r - 1) * kTailBins) / chunk) : -1;
+    };
+    // pass 1: totals of full chunks (to place the tails after them) and the
+    // tails' bin sizes
+    if (threadIdx.x < kTailBins)
+        binbase[threadIdx.x] = 0;
+    __syncthreads();
     int full_total = 0;
     for (int base = 0; base < n; base += 1024) {
-        const int i = base + threadIdx.x;
-        int cnt = 0;
-        if (i < n) {
-            if (g.dense) {
-                const int b = i / (g.Hkv * g.nbmax), j = i % g.nbmax;
-                cnt = dense_count(g, seq_len(g, b), j);
-            } else {
-                cnt = counts[i];
-            }
-        }
+        const int cnt = block_count(base + threadIdx.x);
+        const int bin = tail_bin(cnt);
+        if (bin >= 0)
+            atomicAdd(&binbase[bin], 1);
         int tot;
         block_scan_excl(cnt / chunk, tot, sm);
         full_total += tot;
     }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // bin sizes -> first position of each bin
+        int run = 0;
+        for (int k = 0; k < kTailBins; ++k) {
+            const int c = binbase[k];
+            binbase[k] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
     int c_off = 0, c_full = 0, c_tail = 0, c_slot = 0;
     for (int base = 0; base < n; base += 1024) {
         const int i = base + threadIdx.x;
-        int cnt = 0, b = 0, kvh = 0, j = 0;
+        int b = 0, kvh = 0, j = 0;
+        const int cnt = block_count(i);
         if (i < n) {
             j = i % g.nbmax;
             kvh = (i / g.nbmax) % g.Hkv;
             b = i / (g.Hkv * g.nbmax);
-            if (g.dense) {
-                cnt = dense_count(g, seq_len(g, b), j);
-            } else {
-                cnt = counts[i];
-            }
         }
         const int nfull = cnt / chunk, tail = (cnt % chunk) ? 1 : 0, nch = nfull + tail;
         int t_off, t_full, t_tail, t_slot;
         const int p_off = block_scan_excl(cnt, t_off, sm);
         const int p_full = block_scan_excl(nfull, t_full, sm);
-        const int p_tail = block_scan_excl(tail, t_tail, sm);
+        block_scan_excl(tail, t_tail, sm);
         const int p_slot = block_scan_excl(nch >= 2 ? nch : 0, t_slot, sm);
+        // rank of this tail among the tails of its bin, in block order
+        const int bin = tail_bin(cnt);
+        for (int x = threadIdx.x; x < 32 * kTailBins; x += blockDim.x)
+            (&wbin[0][0])[x] = 0;
+        __syncthreads();
+        const unsigned same = __match_any_sync(0xffffffffu, bin);
+        const int rank_w = __popc(same & ((1u << lane) - 1u));
+        if (bin >= 0 && rank_w == 0)
+            wbin[w][bin] = __popc(same);
+        __syncthreads();
+        if (w < kTailBins) {  // warp k: exclusive scan of bin k over the 32 warps
+            const int v = wbin[lane][w];
+            int x = v;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off)
+                    x += y;
+            }
+            wbin[lane][w] = binbase[w] + x - v;
+            __syncwarp();
+            if (lane == 31)
+                binbase[w] += x;
+        }
+        __syncthreads();
         if (i < n) {
             offsets[i] = c_off + p_off;
             blk_nchunk[i] = nch;
@@ -238,13 +287,14 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
                 u.count = cnt - nfull * chunk;
                 u.slot = slot0 >= 0 ? slot0 + nfull : -1;
                 u.pad0 = u.pad1 = u.pad2 = 0;
-                units[full_total + c_tail + p_tail] = u;
+                units[full_total + wbin[w][bin] + rank_w] = u;
             }
         }
         c_off += t_off;
         c_full += t_full;
         c_tail += t_tail;
         c_slot += t_slot;
+        __syncthreads();  // wbin is cleared for the next round
     }
     if (threadIdx.x == 0) {
         offsets[n] = c_off;

@@ -66,6 +66,16 @@ struct Params {
     int *err;
 };
 
+// The CTA's k-th work unit, or -1 past the end.  Units are dealt to the CTAs
+// in a snake (row k left to right for even k, right to left for odd k);
+// with the unit list's longest-first order this balances the CTAs' work.
+__device__ __forceinline__ int unit_of(int k, int n_units)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    const int64_t ui = (int64_t)k * G + ((k & 1) ? G - 1 - c : c);
+    return ui < n_units ? (int)ui : -1;
+}
+
 template <bool GATHER_TMA>
 __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_do,
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         int it = 0, uc = 0;
         int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
         bool okl = true;
-        for (int ui = blockIdx.x; ui < n_units && okl; ui += gridDim.x, ++uc) {
+        for (int ui; (ui = unit_of(uc, n_units)) >= 0 && okl; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int ntiles = (u.count + Tt - 1) / Tt;
@@ -230,7 +240,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         // is still busy; publishes them when the stage frees.  Lane l owns
         // tile rows l, l + 32, l + 64, l + 96.
         int it = 0;
-        int ui = blockIdx.x, ti = 0;
+        int ku = 0, ti = 0;
+        int ui = unit_of(0, n_units);
         Unit u;
         int b = 0, kvh = 0, csr0 = 0, ntiles = 0;
         auto load_unit = [&]() {
@@ -261,11 +272,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 }
             }
         };
-        if (ui < n_units) {
+        if (ui >= 0) {
             load_unit();
             fetch();
         }
-        while (ui < n_units) {
+        while (ui >= 0) {
             const int st = it & 1;
             if (!mbar_wait_warp(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag))
                 break;
@@ -282,11 +293,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             ++it;
             if (++ti == ntiles) {
                 ti = 0;
-                ui += gridDim.x;
-                if (ui < n_units)
+                ui = unit_of(++ku, n_units);
+                if (ui >= 0)
                     load_unit();
             }
-            if (ui < n_units)
+            if (ui >= 0)
                 fetch();
         }
     } else if (warp == 2) {
@@ -298,16 +309,16 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             const uint32_t k_s = smem_u32(sm + OFF_K), v_s = smem_u32(sm + OFF_V);
             const uint32_t p_s = smem_u32(sm + OFF_P), ds_s = smem_u32(sm + OFF_DS);
             // cursor S issues S/dP, cursor V issues dV/dK; both walk (unit, tile)
-            int sU = blockIdx.x, sT = 0, sIt = 0, sUc = 0, sN = -1;
-            int vU = blockIdx.x, vT = 0, vIt = 0, vUc = 0, vN = -1;
+            int sU = unit_of(0, n_units), sT = 0, sIt = 0, sUc = 0, sN = -1;
+            int vU = sU, vT = 0, vIt = 0, vUc = 0, vN = -1;
             auto ntiles_of = [&](int ui) { return (p.units[ui].count + Tt - 1) / Tt; };
-            if (sU < n_units)
+            if (sU >= 0)
                 sN = ntiles_of(sU);
-            if (vU < n_units)
+            if (vU >= 0)
                 vN = ntiles_of(vU);
             const uint64_t t_start = globaltimer();
             uint64_t t_last = t_start;
-            while (vU < n_units && !*abort_flag) {
+            while (vU >= 0 && !*abort_flag) {
                 bool progressed = false;
                 // dV/dK of the oldest tile whose P/dS are ready
                 if (vIt < sIt && mbar_test(&bars[B_PFULL], vIt & 1) &&
@@ -328,10 +339,9 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     mma_commit(&bars[B_EMPTY0 + st]);
                     if (vT + 1 == vN) {
                         mma_commit(&bars[B_ACCFULL]);
-                        vU += gridDim.x;
+                        vU = unit_of(++vUc, n_units);
                         vT = 0;
-                        ++vUc;
-                        vN = vU < n_units ? ntiles_of(vU) : -1;
+                        vN = vU >= 0 ? ntiles_of(vU) : -1;
                     } else {
                         ++vT;
                     }
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     progressed = true;
                 }
                 // S/dP of the next tile (at most two tiles ahead of dV/dK)
-                if (sU < n_units && sIt < vIt + 2 && mbar_test(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
+                if (sU >= 0 && sIt < vIt + 2 && mbar_test(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
                     mbar_test(&bars[B_SFREE0 + (sIt & 1)], ((sIt >> 1) & 1) ^ 1) &&
                     (sT > 0 || mbar_test(&bars[B_KVFULL], sUc & 1))) {
                     tc_fence_after();
@@ -356,10 +366,9 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     mma_commit(&bars[B_SFULL0 + st]);
                     if (sT + 1 == sN) {
                         mma_commit(&bars[B_KVEMPTY]);
-                        sU += gridDim.x;
+                        sU = unit_of(++sUc, n_units);
                         sT = 0;
-                        ++sUc;
-                        sN = sU < n_units ? ntiles_of(sU) : -1;
+                        sN = sU >= 0 ? ntiles_of(sU) : -1;
                     } else {
                         ++sT;
                     }
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
         int it = 0, uc = 0;
         bool ok = true;
-        for (int ui = blockIdx.x; ui < n_units && ok; ui += gridDim.x, ++uc) {
+        for (int ui; (ui = unit_of(uc, n_units)) >= 0 && ok; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int L = seq_len(g, b);
