@@ -107,13 +107,14 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         tmem_alloc(tmem_slot, TM_COLS);
         tmem_relinquish();
     }
-    // Finite values wherever a TMA may not write: tile rows past Tq * G and the
-    // K/V slots of a pair's missing second block (those keys meet P = 0).
-    for (int i = threadIdx.x; i < (OFF_MASK - OFF_Q) / 16; i += blockDim.x) {
-        const int off = OFF_Q + i * 16;
-        if (off >= OFF_KV || (off % kHalfBytes) / 128 >= nrows)
-            *(uint4 *)(sm + off) = make_uint4(0, 0, 0, 0);
-    }
+    // Tile rows past Tq * G receive no data; they meet P = 0 but must be
+    // finite.  (A pair's missing second block is loaded as a copy of its first.)
+    if (nrows < kRows)
+        for (int i = threadIdx.x; i < 2 * (kRows - nrows) * 8; i += blockDim.x) {
+            const int part = i / ((kRows - nrows) * 8), rem = i % ((kRows - nrows) * 8);
+            *(uint4 *)(sm + OFF_Q + part * kHalfBytes + (nrows + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -153,16 +154,16 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             const int s = i % NS;
             if (!mbar_wait_warp(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
                 break;
-            const int nb = min(2, U - 2 * i);
             uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
             if (lane == 0)
-                mbar_arrive_expect_tx(&bars[B_KVF0 + s], nb * 2 * kKvBytes);
+                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * 2 * kKvBytes);
             __syncwarp();
             last = i;
-            // lane -> (block e of the pair, 64-column half h, K or V)
-            if (lane < 4 * nb) {
+            // lane -> (block e of the pair, 64-column half h, K or V); a
+            // missing second block repeats the first (finite data, P = 0)
+            if (lane < 8) {
                 const int e = lane >> 2, h = (lane >> 1) & 1, isv = lane & 1;
-                const int j = list[2 * i + e];
+                const int j = list[min(2 * i + e, U - 1)];
                 uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
                 const CUtensorMap *map = isv ? &tm_v : &tm_k;
                 if (g.thd)
