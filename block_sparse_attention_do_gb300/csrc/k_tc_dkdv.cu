@@ -45,8 +45,9 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 // barrier slots
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1, B_COUNT
 };
+static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;     // S of buffer b at b*128, dP at b*128 + 64

@@ -45,8 +45,9 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
     B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE, B_DONEQ,
-    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1
+    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1, B_VF0, B_VF1, B_COUNT  // B_KVF*: the pair's K (its V: B_VF*)
 };
+static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
 constexpr uint32_t TM_S = 0;     // S: 128 columns (keys)
 constexpr uint32_t TM_DP = 128;  // dP: 128 columns (keys)
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_DONEQ], 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[B_KVF0 + s], 1);
+            mbar_init(&bars[B_VF0 + s], 1);
             mbar_init(&bars[B_KVE0 + s], 1);
             mbar_init(&bars[B_DSF0 + s], 2 * kRows);
         }
@@ -160,29 +162,35 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!mbar_wait_warp(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
                 break;
             uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * 2 * kKvBytes);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * kKvBytes);
+                mbar_arrive_expect_tx(&bars[B_VF0 + s], 2 * kKvBytes);
+            }
             __syncwarp();
             last = i;
-            // lane -> (block e of the pair, 64-column half h, K or V); a
-            // missing second block repeats the first (finite data, P = 0)
+            // lane -> (K or V, block e of the pair, 64-column half h), the K
+            // boxes first: S can start while V is still landing.  A missing
+            // second block repeats the first (finite data, P = dS = 0).
             if (lane < 8) {
-                const int e = lane >> 2, h = (lane >> 1) & 1, isv = lane & 1;
+                const int isv = lane >> 2, e = (lane >> 1) & 1, h = lane & 1;
                 const int j = list[min(2 * i + e, U - 1)];
                 uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
                 const CUtensorMap *map = isv ? &tm_v : &tm_k;
+                uint64_t *bar = &bars[(isv ? B_VF0 : B_KVF0) + s];
                 if (g.thd)
-                    tma_load_3d(dst, map, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
+                    tma_load_3d(dst, map, bar, h * 64, kvh, g.cu[b] + j * kKeys);
                 else
-                    tma_load_4d(dst, map, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
+                    tma_load_4d(dst, map, bar, h * 64, j * kKeys, kvh, b);
             }
         }
         // copies in flight must land before the CTA may exit
         if (lane == 0) {
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
-            if (*abort_flag && last >= 0)
+            if (*abort_flag && last >= 0) {
                 mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
+                mbar_wait(&bars[B_VF0 + last % NS], (last / NS) & 1, &never);
+            }
         }
         __syncwarp();
     } else if (warp == 2 || warp == 3) {
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (warp == 2) {
                 const uint32_t idS = idesc_bf16(128, 128, false, false);
                 for (int si = 0; si < npairs && ok; ++si) {
-                    // the pair's K/V have landed; the softmax holds the previous S/dP in registers
+                    // the pair's K has landed; the softmax holds the previous S/dP in registers
                     if (!mbar_wait(&bars[B_KVF0 + si % NS], (si / NS) & 1, abort_flag) ||
                         !mbar_wait(&bars[B_SFREE], (si & 1) ^ 1, abort_flag)) {
                         ok = false;
@@ -212,6 +220,14 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
                                  kk > 0);
+                    }
+                    if (!mbar_wait(&bars[B_VF0 + si % NS], (si / NS) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
                                  kk > 0);
                     }

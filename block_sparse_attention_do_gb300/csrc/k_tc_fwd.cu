@@ -35,14 +35,15 @@ constexpr int OFF_MASK = OFF_KV + NS * kPairBytes;
 constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
 constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
 constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int NUM_BARS = 16;
+constexpr int NUM_BARS = 20;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
     B_QFULL = 0, B_LIST, B_DONE, B_PVFULL, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
-    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_PF0, B_PF1, B_DONES
+    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_PF0, B_PF1, B_DONES, B_VF0, B_VF1, B_COUNT  // B_KVF*: the pair's K (its V: B_VF*)
 };
+static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
 constexpr uint32_t TM_S = 0;    // buffer b at b*128 (keys of the pair)
 constexpr uint32_t TM_O = 256;  // 128 lanes (rows) x 128 columns (dims)
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             mbar_init(&bars[B_SFULL0 + s], 1);
             mbar_init(&bars[B_SFREE0 + s], kRows);
             mbar_init(&bars[B_KVF0 + s], 1);
+            mbar_init(&bars[B_VF0 + s], 1);
             mbar_init(&bars[B_KVE0 + s], 1);
             mbar_init(&bars[B_PF0 + s], kRows);
         }
@@ -155,29 +157,35 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             if (!mbar_wait_warp(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
                 break;
             uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * 2 * kKvBytes);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * kKvBytes);
+                mbar_arrive_expect_tx(&bars[B_VF0 + s], 2 * kKvBytes);
+            }
             __syncwarp();
             last = i;
-            // lane -> (block e of the pair, 64-column half h, K or V); a
-            // missing second block repeats the first (finite data, P = 0)
+            // lane -> (K or V, block e of the pair, 64-column half h), the K
+            // boxes first (S needs K only; V is read by the later P.V).  A
+            // missing second block repeats the first (finite data, P = 0).
             if (lane < 8) {
-                const int e = lane >> 2, h = (lane >> 1) & 1, isv = lane & 1;
+                const int isv = lane >> 2, e = (lane >> 1) & 1, h = lane & 1;
                 const int j = list[min(2 * i + e, U - 1)];
                 uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
                 const CUtensorMap *map = isv ? &tm_v : &tm_k;
+                uint64_t *bar = &bars[(isv ? B_VF0 : B_KVF0) + s];
                 if (g.thd)
-                    tma_load_3d(dst, map, &bars[B_KVF0 + s], h * 64, kvh, g.cu[b] + j * kKeys);
+                    tma_load_3d(dst, map, bar, h * 64, kvh, g.cu[b] + j * kKeys);
                 else
-                    tma_load_4d(dst, map, &bars[B_KVF0 + s], h * 64, j * kKeys, kvh, b);
+                    tma_load_4d(dst, map, bar, h * 64, j * kKeys, kvh, b);
             }
         }
         // copies in flight must land before the CTA may exit
         if (lane == 0) {
             volatile int never = 0;
             mbar_wait(&bars[B_QFULL], 0, &never);
-            if (*abort_flag && last >= 0)
+            if (*abort_flag && last >= 0) {
                 mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
+                mbar_wait(&bars[B_VF0 + last % NS], (last / NS) & 1, &never);
+            }
         }
         __syncwarp();
     } else if (warp == 2 || warp == 3) {
@@ -217,7 +225,8 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             } else {
                 const uint32_t idO = idesc_bf16(128, 128, false, true);
                 for (int oi = 0; oi < npairs && ok; ++oi) {
-                    if (!mbar_wait(&bars[B_PF0 + oi % NS], (oi / NS) & 1, abort_flag)) {
+                    if (!mbar_wait(&bars[B_PF0 + oi % NS], (oi / NS) & 1, abort_flag) ||
+                        !mbar_wait(&bars[B_VF0 + oi % NS], (oi / NS) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
