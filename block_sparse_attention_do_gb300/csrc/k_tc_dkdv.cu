@@ -434,13 +434,16 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     // no row of the warp ends or starts inside the block: a row
                     // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                     const float bias = lim >= 0 ? l2 : __int_as_float(0x7f800000);
+                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias), nd2 = f2(-dl, -dl);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[c]), g.scale_l2, -bias));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), g.scale_l2, -bias));
+                        float x0, x1, d0, d1;
+                        f2_split(f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nb2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
                         pk[c >> 1] = pack_bf16(p0, p1);
-                        dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl),
-                                                p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                        f2_split(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
+                                 d0, d1);
+                        dk_[c >> 1] = pack_bf16(d0, d1);
                     }
                 } else {
 #pragma unroll

@@ -320,12 +320,15 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                 if (__any_sync(0xffffffffu, sel)) {
                     const float bias = sel ? l2 : __int_as_float(0x7f800000);
+                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias), nd2 = f2(-dl, -dl);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[c]), g.scale_l2, -bias));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), g.scale_l2, -bias));
-                        dk_[c >> 1] = pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl),
-                                                p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                        float x0, x1, d0, d1;
+                        f2_split(f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nb2), x0, x1);
+                        const uint64_t pp = f2(ex2(x0), ex2(x1));
+                        f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
+                                 d0, d1);
+                        dk_[c >> 1] = pack_bf16(d0, d1);
                     }
                 } else {
 #pragma unroll
