@@ -299,11 +299,15 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                 float mb = -INFINITY;
                 if (whole) {
                     const float b0 = lim[0] >= 0 ? 0.f : -INFINITY, b1 = lim[1] >= 0 ? 0.f : -INFINITY;
+                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), bb0 = f2(b0, b0), bb1 = f2(b1, b1);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const float x = fmaf(__uint_as_float(sv[c]), g.scale_l2, c < 64 ? b0 : b1);
-                        sv[c] = __float_as_uint(x);
-                        mb = fmaxf(mb, x);
+                    for (int c = 0; c < 128; c += 2) {
+                        float x0, x1;
+                        f2_split(f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, c < 64 ? bb0 : bb1),
+                                 x0, x1);
+                        sv[c] = __float_as_uint(x0);
+                        sv[c + 1] = __float_as_uint(x1);
+                        mb = fmaxf(mb, fmaxf(x0, x1));
                     }
                 } else {
 #pragma unroll
@@ -344,13 +348,19 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                     // a row with nothing attended so far has m = -inf and only
                     // -inf scores: subtract 0 there so that exp2 gives 0, not NaN
                     const float ms = m == -INFINITY ? 0.f : m;
+                    const uint64_t nms2 = f2(-ms, -ms);
+                    uint64_t rs2 = f2(0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < 128; c += 2) {
-                        const float p0 = ex2(__uint_as_float(sv[c]) - ms);
-                        const float p1 = ex2(__uint_as_float(sv[c + 1]) - ms);
-                        rs += p0 + p1;
+                        float x0, x1;
+                        f2_split(f2_add(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nms2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        rs2 = f2_add(rs2, f2(p0, p1));
                         pk[c >> 1] = pack_bf16(p0, p1);
                     }
+                    float r0, r1;
+                    f2_split(rs2, r0, r1);
+                    rs = r0 + r1;
                 } else {
 #pragma unroll
                     for (int c = 0; c < 128; c += 2) {
