@@ -412,13 +412,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                 }
                 tc_fence_after();
                 uint32_t sv[64], dv_[64];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t (&a)[16] = *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]);
-                    uint32_t (&bq)[16] = *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]);
-                    tmem_ld16(lane_base + TM_S + st * 128 + c * 16, a);
-                    tmem_ld16(lane_base + TM_S + st * 128 + 64 + c * 16, bq);
-                }
+                tmem_ld64(lane_base + TM_S + st * 128, sv);
+                tmem_ld64(lane_base + TM_S + st * 128 + 64, dv_);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE0 + st]);

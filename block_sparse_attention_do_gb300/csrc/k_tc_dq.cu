@@ -301,11 +301,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             }
             tc_fence_after();
             uint32_t sv[64], dv_[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld16(lane_base + TM_S + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
-                tmem_ld16(lane_base + TM_DP + e * 64 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&dv_[c * 16]));
-            }
+            tmem_ld64(lane_base + TM_S + e * 64, sv);
+            tmem_ld64(lane_base + TM_DP + e * 64, dv_);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bars[B_SFREE]);

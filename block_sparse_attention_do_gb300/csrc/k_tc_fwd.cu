@@ -273,9 +273,8 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             }
             tc_fence_after();
             uint32_t sv[128];
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                tmem_ld16(lane_base + TM_S + s * 128 + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[c * 16]));
+            tmem_ld64(lane_base + TM_S + s * 128, *reinterpret_cast<uint32_t(*)[64]>(&sv[0]));
+            tmem_ld64(lane_base + TM_S + s * 128 + 64, *reinterpret_cast<uint32_t(*)[64]>(&sv[64]));
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bars[B_SFREE0 + s]);
