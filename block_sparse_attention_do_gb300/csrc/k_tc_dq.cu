@@ -39,12 +39,12 @@ constexpr int OFF_MASK = OFF_KV + NS * kPairBytes;
 constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
 constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
 constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int NUM_BARS = 16;
+constexpr int NUM_BARS = 20;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 
 enum {
-    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE, B_DONEQ,
+    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE, B_DONEQ, B_DPFULL, B_DPFREE,
     B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1, B_VF0, B_VF1, B_COUNT  // B_KVF*: the pair's K (its V: B_VF*)
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_LIST], kRows);
         mbar_init(&bars[B_SFULL], 1);
         mbar_init(&bars[B_SFREE], 2 * kRows);
+        mbar_init(&bars[B_DPFULL], 1);
+        mbar_init(&bars[B_DPFREE], 2 * kRows);
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
         mbar_init(&bars[B_DONEQ], 1);
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (warp == 2) {
                 const uint32_t idS = idesc_bf16(128, 128, false, false);
                 for (int si = 0; si < npairs && ok; ++si) {
-                    // the pair's K has landed; the softmax holds the previous S/dP in registers
+                    // the pair's K has landed; the softmax has taken the previous S
                     if (!mbar_wait(&bars[B_KVF0 + si % NS], (si / NS) & 1, abort_flag) ||
                         !mbar_wait(&bars[B_SFREE], (si & 1) ^ 1, abort_flag)) {
                         ok = false;
@@ -221,7 +223,10 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
                                  kk > 0);
                     }
-                    if (!mbar_wait(&bars[B_VF0 + si % NS], (si / NS) & 1, abort_flag)) {
+                    mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
+                    // the V has landed; the softmax has taken the previous dP
+                    if (!mbar_wait(&bars[B_VF0 + si % NS], (si / NS) & 1, abort_flag) ||
+                        !mbar_wait(&bars[B_DPFREE], (si & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
                                  kk > 0);
                     }
-                    mma_commit(&bars[B_SFULL]);
+                    mma_commit(&bars[B_DPFULL]);
                 }
                 mma_commit(&bars[B_DONE]);
                 volatile int never = 0;
@@ -295,53 +300,65 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         bool ok = true;
         for (int i = 0; i < npairs; ++i) {
             const int s = i % NS;
-            if (!mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sv[64], dv_[64];
-            tmem_ld64(lane_base + TM_S + e * 64, sv);
-            tmem_ld64(lane_base + TM_DP + e * 64, dv_);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars[B_SFREE]);
             const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
             const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
             // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
             const int lim = sel ? t - j * kKeys : -1;
             const int lo = key_lo(g, t) - j * kKeys;
-            uint32_t dk_[32];
-            if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
-                // no row of the warp ends or starts inside the block: a row
-                // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
-                if (__any_sync(0xffffffffu, sel)) {
+            // no row of the warp ends or starts inside the block: a row attends
+            // all of it or none; none gets a +inf bias (exp2(-inf) = 0)
+            const bool whole = __all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0));
+            const bool any = __any_sync(0xffffffffu, sel);
+            // P = exp2(scale S - LSE) on the attended keys, while dP is still running
+            if (!mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t pv[64];
+            tmem_ld64(lane_base + TM_S + e * 64, pv);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars[B_SFREE]);
+            if (any) {
+                if (whole) {
                     const float bias = sel ? l2 : __int_as_float(0x7f800000);
-                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias), nd2 = f2(-dl, -dl);
+                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        float x0, x1, d0, d1;
-                        f2_split(f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nb2), x0, x1);
-                        const uint64_t pp = f2(ex2(x0), ex2(x1));
-                        f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
-                                 d0, d1);
-                        dk_[c >> 1] = pack_bf16(d0, d1);
+                        float x0, x1;
+                        f2_split(f2_fma(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sc2, nb2), x0, x1);
+                        pv[c] = __float_as_uint(ex2(x0));
+                        pv[c + 1] = __float_as_uint(ex2(x1));
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        dk_[c] = 0u;
+                    for (int c = 0; c < 64; ++c)
+                        pv[c] = __float_as_uint((c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
+                                                                      : 0.f);
                 }
-            } else if (__any_sync(0xffffffffu, sel)) {
+            }
+            // dS = P (dP - delta)
+            if (!mbar_wait_warp(&bars[B_DPFULL], i & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t dv_[64];
+            tmem_ld64(lane_base + TM_DP + e * 64, dv_);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bars[B_DPFREE]);
+            uint32_t dk_[32];
+            if (any) {
+                const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    float p0 = 0.f, p1 = 0.f;
-                    if (c <= lim && c >= lo)
-                        p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                    if (c + 1 <= lim && c + 1 >= lo)
-                        p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
-                    dk_[c >> 1] =
-                        pack_bf16(p0 * (__uint_as_float(dv_[c]) - dl), p1 * (__uint_as_float(dv_[c + 1]) - dl));
+                    float d0, d1;
+                    f2_split(f2_mul(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                    f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
+                             d0, d1);
+                    dk_[c >> 1] = pack_bf16(d0, d1);
                 }
             } else {
 #pragma unroll
