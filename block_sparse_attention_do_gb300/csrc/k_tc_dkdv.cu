@@ -45,7 +45,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 // barrier slots
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1, B_COUNT
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1, B_DPFULL0, B_DPFULL1, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         mbar_init(&bars[B_KVFULL], 1);
         mbar_init(&bars[B_KVEMPTY], 1);
         mbar_init(&bars[B_SFULL0], 1);
+        mbar_init(&bars[B_DPFULL0], 1);
+        mbar_init(&bars[B_DPFULL1], 1);
         mbar_init(&bars[B_SFULL1], 1);
         mbar_init(&bars[B_SFREE0], kRows);
         mbar_init(&bars[B_SFREE1], kRows);
@@ -361,10 +363,15 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                         const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
                         mma_bf16(dS_col, sdesc_sw128(q_s + st * kTileBytes + ao, 16, kRgStride),
                                  sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
+                    }
+                    mma_commit(&bars[B_SFULL0 + st]);  // the softmax starts on P while dP runs
+                    for (int kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
+                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
                         mma_bf16(dS_col + 64, sdesc_sw128(do_s + st * kTileBytes + ao, 16, kRgStride),
                                  sdesc_sw128(v_s + bo, 16, 1024), idS, kk > 0);
                     }
-                    mma_commit(&bars[B_SFULL0 + st]);
+                    mma_commit(&bars[B_DPFULL0 + st]);
                     if (sT + 1 == sN) {
                         mma_commit(&bars[B_KVEMPTY]);
                         sU = unit_of(++sUc, n_units);
@@ -411,48 +418,54 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                uint32_t sv[64], dv_[64];
-                tmem_ld64(lane_base + TM_S + st * 128, sv);
-                tmem_ld64(lane_base + TM_S + st * 128 + 64, dv_);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bars[B_SFREE0 + st]);
-
                 const int tl = r / G;
                 const int tok = (r < nrows) ? tok_s[st * kRows + tl] : -1;
                 const float l2 = lse_s[st * kRows + r], dl = dlt_s[st * kRows + r];
-                // keys k0 + c with c <= tok - k0 are attended (the token selected block j)
+                // keys k0 + c with lo <= c <= tok - k0 are attended (the token selected block j)
                 const int lim = tok < 0 ? -1 : tok - k0;
                 const int lo = tok < 0 ? 0 : key_lo(g, tok) - k0;  // window's left edge
-                uint32_t pk[32], dk_[32];
+                // P from S while dP is still running
+                uint32_t pv[64];
+                tmem_ld64(lane_base + TM_S + st * 128, pv);
+                tmem_wait_ld();
                 if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
                     // no row of the warp ends or starts inside the block: a row
                     // attends all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                     const float bias = lim >= 0 ? l2 : __int_as_float(0x7f800000);
-                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias), nd2 = f2(-dl, -dl);
+                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        float x0, x1, d0, d1;
-                        f2_split(f2_fma(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nb2), x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
-                        pk[c >> 1] = pack_bf16(p0, p1);
-                        f2_split(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
-                                 d0, d1);
-                        dk_[c >> 1] = pack_bf16(d0, d1);
+                        float x0, x1;
+                        f2_split(f2_fma(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sc2, nb2), x0, x1);
+                        pv[c] = __float_as_uint(ex2(x0));
+                        pv[c + 1] = __float_as_uint(ex2(x1));
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
-                        float p0 = 0.f, p1 = 0.f;
-                        if (c <= lim && c >= lo)
-                            p0 = ex2(__uint_as_float(sv[c]) * g.scale_l2 - l2);
-                        if (c + 1 <= lim && c + 1 >= lo)
-                            p1 = ex2(__uint_as_float(sv[c + 1]) * g.scale_l2 - l2);
-                        const float d0 = p0 * (__uint_as_float(dv_[c]) - dl);
-                        const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dl);
-                        pk[c >> 1] = pack_bf16(p0, p1);
-                        dk_[c >> 1] = pack_bf16(d0, d1);
-                    }
+                    for (int c = 0; c < 64; ++c)
+                        pv[c] = __float_as_uint((c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
+                                                                      : 0.f);
+                }
+                // dS = P (dP - delta)
+                if (!mbar_wait_warp(&bars[B_DPFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t dv_[64];
+                tmem_ld64(lane_base + TM_S + st * 128 + 64, dv_);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE0 + st]);
+                uint32_t pk[32], dk_[32];
+                const uint64_t nd2 = f2(-dl, -dl);
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float d0, d1;
+                    const uint64_t pp = f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
+                    f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)), d0, d1);
+                    pk[c >> 1] = pack_bf16(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
+                    dk_[c >> 1] = pack_bf16(d0, d1);
                 }
                 if (!mbar_wait_warp(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
                     ok = false;
