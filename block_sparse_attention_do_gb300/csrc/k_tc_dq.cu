@@ -17,11 +17,13 @@
 // dS is written into the pair's V slot, free once dP is computed, so a K/V
 // stage (64 KB) carries the pair from load to the dQ MMA.
 //
-// Roles (12 warps): warp 0 issues TMA (the Q/dO tile once, then the K/V
-// pairs, two stages, one box per lane); warp 2 owns TMEM and one thread
-// issues the MMAs; warps 4-7 build the block union; then warps 4-7 form dS
-// of the pair's first block and warps 8-11 of its second, one row per
-// thread, and split the epilogue's columns the same way.
+// Roles (12 warps): warp 0 issues the TMA copies (the Q/dO tile once, then
+// each pair's K boxes and then its V boxes, two stages, one box per lane);
+// warp 2 owns TMEM and one thread issues S and dP, one thread of warp 3 the
+// dQ MMAs; warps 4-7 build the block union; then warps 4-7 form dS of the
+// pair's first block and warps 8-11 of its second, one row per thread (P
+// from S while dP still runs), and split the epilogue's columns the same
+// way.
 #include "tc_common.cuh"
 
 namespace nsa {
