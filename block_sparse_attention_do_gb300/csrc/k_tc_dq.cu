@@ -120,11 +120,16 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
     }
     // Tile rows past Tq * G receive no data; they meet P = dS = 0 but must be
     // finite.  (A pair's missing second block is loaded as a copy of its first.)
+    // With G % 8 == 0 in BHTD the Q and dO tiles are in the row-group layout
+    // (one TMA box per token: its G heads, both halves), else rows of 128
+    // bytes per half.
+    const bool rg = !g.thd && (G % 8) == 0;
     if (nrows < kRows)
         for (int i = threadIdx.x; i < 4 * (kRows - nrows) * 8; i += blockDim.x) {
             const int part = i / ((kRows - nrows) * 8), rem = i % ((kRows - nrows) * 8);
-            *(uint4 *)(sm + OFF_Q + part * kHalfBytes + (nrows + (rem >> 3)) * 128 + (rem & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int row = nrows + (rem >> 3), half = part & 1, tensor = part >> 1;
+            *(uint4 *)(sm + OFF_Q + tensor * kTileBytes + (rg ? rg_off(row, half) : half * kHalfBytes + row * 128) +
+                       (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
     fence_async_smem();
     tc_fence_before();
@@ -143,18 +148,22 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         }
         __syncwarp();
         {
-            const bool per_token = !g.thd && qtile_token_major(g);
-            const int nbox = per_token ? 4 * Tq : 4;
+            const int nbox = rg ? 2 * Tq : 4;
             for (int box = lane; box < nbox; box += 32) {
-                const int h = (box >> 1) & 1, tensor = box & 1, tl = box >> 2;
+                const int tensor = box & 1;
                 const CUtensorMap *map = tensor ? &tm_do : &tm_q;
-                uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + h * kHalfBytes;
-                if (g.thd)
-                    tma_load_3d(dst, map, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
-                else if (per_token)
-                    tma_load_4d(dst + tl * G * 128, map, &bars[B_QFULL], h * 64, t0 + tl, kvh * G, b);
-                else
-                    tma_load_4d(dst, map, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
+                    const int tl = box >> 1;
+                    tma_load_5d(sm + (tensor ? OFF_DO : OFF_Q) + tl * G * 256, map, &bars[B_QFULL], 0, 0, 0,
+                                (b * g.Hq + kvh * G) / 8, t0 + tl);
+                } else {
+                    const int h = box >> 1;
+                    uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + h * kHalfBytes;
+                    if (g.thd)
+                        tma_load_3d(dst, map, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                    else
+                        tma_load_4d(dst, map, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                }
             }
         }
         bool ok = mbar_wait_warp(&bars[B_LIST], 0, abort_flag);
@@ -206,6 +215,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         if (lane == 0) {
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
             const uint32_t kv_s = smem_u32(sm + OFF_KV);
+            // Q/dO tiles: 64-column halves and 8-row groups apart by these
+            const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
             bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
             const int U = ok ? *n_list : 0;
             const int npairs = (U + 1) >> 1;
@@ -222,8 +233,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     const uint32_t k_s = kv_s + (si % NS) * kPairBytes, v_s = k_s + kTileBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_S, sdesc_sw128(q_s + o, 16, 1024), sdesc_sw128(k_s + o, 16, 1024), idS,
-                                 kk > 0);
+                        const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
+                        mma_bf16(tmem + TM_S, sdesc_sw128(q_s + oq, 16, qsbo), sdesc_sw128(k_s + o, 16, 1024),
+                                 idS, kk > 0);
                     }
                     mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
                     // the V has landed; the softmax has taken the previous dP
@@ -235,8 +247,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     tc_fence_after();
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + o, 16, 1024), sdesc_sw128(v_s + o, 16, 1024), idS,
-                                 kk > 0);
+                        const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
+                        mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + oq, 16, qsbo), sdesc_sw128(v_s + o, 16, 1024),
+                                 idS, kk > 0);
                     }
                     mma_commit(&bars[B_DPFULL]);
                 }
@@ -423,8 +436,10 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
     CUtensorMap tq, tdo, tk, tv;
-    const int box_tok = (!g.thd && qtile_token_major(g)) ? 1 : Tq;
-    if (!make_tmap(&tq, q, g, g.Hq, box_tok, g.G) || !make_tmap(&tdo, dO, g, g.Hq, box_tok, g.G) ||
+    const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q/dO tiles, one box per token and tensor
+    const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
+                          : make_tmap(&tq, q, g, g.Hq, Tq, g.G) && make_tmap(&tdo, dO, g, g.Hq, Tq, g.G);
+    if (!qmaps ||
         !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;

@@ -111,10 +111,14 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
     }
     // Tile rows past Tq * G receive no data; they meet P = 0 but must be
     // finite.  (A pair's missing second block is loaded as a copy of its first.)
+    // With G % 8 == 0 in BHTD the tile is in the row-group layout (one TMA
+    // box per token: its G heads, both halves), else rows of 128 bytes per half.
+    const bool rg = !g.thd && (G % 8) == 0;
     if (nrows < kRows)
         for (int i = threadIdx.x; i < 2 * (kRows - nrows) * 8; i += blockDim.x) {
-            const int part = i / ((kRows - nrows) * 8), rem = i % ((kRows - nrows) * 8);
-            *(uint4 *)(sm + OFF_Q + part * kHalfBytes + (nrows + (rem >> 3)) * 128 + (rem & 7) * 16) =
+            const int half = i / ((kRows - nrows) * 8), rem = i % ((kRows - nrows) * 8);
+            const int row = nrows + (rem >> 3);
+            *(uint4 *)(sm + OFF_Q + (rg ? rg_off(row, half) : half * kHalfBytes + row * 128) + (rem & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
     fence_async_smem();
@@ -134,18 +138,18 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
         }
         __syncwarp();
         {
-            const bool per_token = !g.thd && qtile_token_major(g);
-            const int nbox = per_token ? 2 * Tq : 2;
+            const int nbox = rg ? Tq : 2;
             for (int box = lane; box < nbox; box += 32) {
-                const int h = box & 1, tl = box >> 1;
-                const CUtensorMap *map = &tm_q;
-                uint8_t *dst = sm + OFF_Q + h * kHalfBytes;
-                if (g.thd)
-                    tma_load_3d(dst, map, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
-                else if (per_token)
-                    tma_load_4d(dst + tl * G * 128, map, &bars[B_QFULL], h * 64, t0 + tl, kvh * G, b);
-                else
-                    tma_load_4d(dst, map, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
+                    tma_load_5d(sm + OFF_Q + box * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, (b * g.Hq + kvh * G) / 8,
+                                t0 + box);
+                } else {
+                    uint8_t *dst = sm + OFF_Q + box * kHalfBytes;
+                    if (g.thd)
+                        tma_load_3d(dst, &tm_q, &bars[B_QFULL], box * 64, kvh * G, g.cu[b] + t0);
+                    else
+                        tma_load_4d(dst, &tm_q, &bars[B_QFULL], box * 64, t0, kvh * G, b);
+                }
             }
         }
         bool ok = mbar_wait_warp(&bars[B_LIST], 0, abort_flag);
@@ -202,6 +206,8 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
             if (warp == 2) {
                 const uint32_t idS = idesc_bf16(128, 128, false, false);
                 const uint32_t q_s = smem_u32(sm + OFF_Q);
+                // Q tile: 64-column halves and 8-row groups apart by these
+                const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
                 for (int si = 0; si < npairs && ok; ++si) {
                     // the pair's K/V have landed; the softmax has taken S of
                     // pair si - 2 out of this TMEM buffer
@@ -214,7 +220,8 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(const __grid_constant__ 
                     const uint32_t k_s = kv_s + (si % NS) * kPairBytes;
                     for (int kk = 0; kk < kHead / 16; ++kk) {
                         const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_S + (si & 1) * 128, sdesc_sw128(q_s + o, 16, 1024),
+                        const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
+                        mma_bf16(tmem + TM_S + (si & 1) * 128, sdesc_sw128(q_s + oq, 16, qsbo),
                                  sdesc_sw128(k_s + o, 16, 1024), idS, kk > 0);
                     }
                     mma_commit(&bars[B_SFULL0 + (si & 1)]);
@@ -448,9 +455,9 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
     CUtensorMap tq, tk, tv;
-    const int box_tok = (!g.thd && qtile_token_major(g)) ? 1 : Tq;
-    if (!make_tmap(&tq, q, g, g.Hq, box_tok, g.G) || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) ||
-        !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q tile, one box per token
+    const bool qmap = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) : make_tmap(&tq, q, g, g.Hq, Tq, g.G);
+    if (!qmap || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;
