@@ -1,10 +1,10 @@
 // k_tc_dq.cu -- dQ on the tcgen05 tensor cores (bf16, D = 128, block_size
 // = 64).
 //
-// One CTA owns a query tile: Tq consecutive tokens of one sequence times the
-// G query heads of one kv head (Tq * G <= 128 rows, Tq = 128 / G).  It walks,
-// two at a time, the ascending union U of the blocks its tokens select.  For
-// a pair (j_a, j_b) of U (128 keys):
+// Work is cut into query tiles: Tq consecutive tokens of one sequence times
+// the G query heads of one kv head (Tq * G <= 128 rows, Tq = 128 / G).  A
+// tile walks, two at a time, the ascending union U of the blocks its tokens
+// select.  For a pair (j_a, j_b) of U (128 keys):
 //   S = Q [K_a; K_b]^T,  dP = dO [V_a; V_b]^T           (M=128 rows, N=128 keys, K=128)
 //   P = exp(scale S - LSE) where the row's token selects the key's block and
 //   key <= token,  dS = P (dP - delta)
@@ -14,16 +14,21 @@
 // token's own blocks.  Pairing keeps every MMA at N = 128: a tcgen05 MMA with
 // M = 128 costs about the same for N = 64 as for N = 128.
 //
-// dS is written into the pair's V slot, free once dP is computed, so a K/V
-// stage (64 KB) carries the pair from load to the dQ MMA.
+// The kernel is persistent: one CTA per SM walks its share of the tiles,
+// heaviest (latest tokens) first, dealt to the CTAs in a snake.  The next
+// tile's block union, its Q/dO load and its first K/V pairs overlap the
+// current tile's last pairs and epilogue: the union sits in one of two
+// shared-memory buffers (one when two do not fit), the dQ accumulator in one
+// of two TMEM buffers, and the two K/V pair stages form one ring across
+// tiles.  dS is written into the pair's V slot, free once dP is computed.
 //
-// Roles (12 warps): warp 0 issues the TMA copies (the Q/dO tile once, then
-// each pair's K boxes and then its V boxes, two stages, one box per lane);
-// warp 2 owns TMEM and one thread issues S and dP, one thread of warp 3 the
-// dQ MMAs; warps 4-7 build the block union; then warps 4-7 form dS of the
-// pair's first block and warps 8-11 of its second, one row per thread (P
-// from S while dP still runs), and split the epilogue's columns the same
-// way.
+// Roles (12 warps): warp 1 picks the tiles and builds their block unions,
+// publishing each tile's coordinates with its union; warp 0 issues the TMA
+// copies (each tile's Q and dO, then its pairs' K boxes and V boxes, one box
+// per lane); warp 2 owns TMEM and one thread issues S and dP, one thread of
+// warp 3 the dQ MMAs; warps 4-7 form dS of each pair's first block and warps
+// 8-11 of its second, one row per thread (P from S while dP still runs),
+// and split the epilogue's columns the same way.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -37,24 +42,43 @@ constexpr int kPairBytes = 2 * kTileBytes;  // K pair (32 KB) | V pair (32 KB, l
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTileBytes;
 constexpr int OFF_KV = OFF_DO + kTileBytes;
-constexpr int OFF_MASK = OFF_KV + NS * kPairBytes;
-constexpr int OFF_LIST = OFF_MASK + MASK_WORDS * 4;
-constexpr int OFF_UBITS = OFF_LIST + MAX_BLOCKS * 4;
-constexpr int OFF_BAR = OFF_UBITS + (MAX_BLOCKS / 32) * 4;
-constexpr int NUM_BARS = 20;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+constexpr int OFF_UNION = OFF_KV + NS * kPairBytes;  // union buffers, sized at launch
+constexpr int NUM_BARS = 28;
+constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
 enum {
-    B_QFULL = 0, B_LIST, B_SFULL, B_SFREE, B_ACCFULL, B_DONE, B_DONEQ, B_DPFULL, B_DPFREE,
-    B_KVF0, B_KVF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1, B_VF0, B_VF1, B_COUNT  // B_KVF*: the pair's K (its V: B_VF*)
+    B_QFULL = 0, B_QEMPTY, B_DOFULL, B_DOEMPTY, B_SFULL, B_SFREE, B_DPFULL, B_DPFREE,
+    B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_ACCFULL0, B_ACCFULL1, B_ACCEMPTY0, B_ACCEMPTY1,
+    B_KVF0, B_KVF1, B_VF0, B_VF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1,  // B_KVF*: a pair's K (its V: B_VF*)
+    B_DONE, B_DONEQ, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
+// threads releasing a tile's union: the loader warp, the two MMA threads and
+// the 256 softmax threads
+constexpr int kUnionUsers = 32 + 2 + 2 * kRows;
 
 constexpr uint32_t TM_S = 0;     // S: 128 columns (keys)
 constexpr uint32_t TM_DP = 128;  // dP: 128 columns (keys)
-constexpr uint32_t TM_DQ = 256;  // dQ: 128 lanes (rows) x 128 columns (dims)
+constexpr uint32_t TM_DQ = 256;  // dQ of even / odd tiles: 128 lanes (rows) x 128 columns (dims) each
 constexpr uint32_t TM_COLS = 512;
+
+// One union buffer: the tile's coordinates and list length (8 ints), the
+// per-token block bitmaps, the union bitmap and the ascending list.
+struct UnionPlan {
+    int mask_words, ubits_words, list_ints, bytes;
+};
+
+__host__ __device__ inline UnionPlan union_plan(const Geo &g)
+{
+    UnionPlan u;
+    const int words = (g.nbmax + 31) / 32;
+    u.mask_words = tile_tokens(g.G) * words;
+    u.ubits_words = (words + 3) & ~3;
+    u.list_ints = (g.nbmax + 3) & ~3;
+    u.bytes = ((8 + u.mask_words + u.ubits_words + u.list_ints) * 4 + 127) & ~127;
+    return u;
+}
+enum { H_B = 0, H_KVH, H_T0, H_NVALID, H_COUNT };  // header ints; count < 0: no more tiles
 
 struct Params {
     Geo g;
@@ -62,6 +86,8 @@ struct Params {
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     int *err;
+    int ntiles;  // query tiles over all (b, kv head)
+    int nub;     // union buffers (1 or 2)
 };
 
 __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -72,40 +98,44 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = (uint64_t *)(sm + OFF_BAR);
-    volatile int *abort_flag = (volatile int *)(sm + OFF_MISC);
-    uint32_t *tmem_slot = (uint32_t *)(sm + OFF_MISC + 16);
-    volatile int *n_list = (volatile int *)(sm + OFF_MISC + 32);
-    uint32_t *mask = (uint32_t *)(sm + OFF_MASK);
-    int *list = (int *)(sm + OFF_LIST);
-    uint32_t *ubits = (uint32_t *)(sm + OFF_UBITS);
-
     const Geo &g = p.g;
+    const UnionPlan up = union_plan(g);
+    const int nub = p.nub;
+    const int off_bar = OFF_UNION + nub * up.bytes;
+    uint64_t *bars = (uint64_t *)(sm + off_bar);
+    volatile int *abort_flag = (volatile int *)(sm + off_bar + NUM_BARS * 8);
+    uint32_t *tmem_slot = (uint32_t *)(sm + off_bar + NUM_BARS * 8 + 16);
+    // union buffer of this CTA's k-th tile, and the parity of its phase
+    auto u_hdr = [&](int k) { return (volatile int *)(sm + OFF_UNION + (k % nub) * up.bytes); };
+    auto u_mask = [&](int k) { return (uint32_t *)(u_hdr(k) + 8); };
+    auto u_ubits = [&](int k) { return u_mask(k) + up.mask_words; };
+    auto u_list = [&](int k) { return (int *)(u_ubits(k) + up.ubits_words); };
+    auto u_par = [&](int k) { return (uint32_t)((k / nub) & 1); };
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = g.G;
     const int Tq = tile_tokens(G);
     const int nrows = Tq * G;
-    const int ntiles_seq = (g.T + Tq - 1) / Tq;
-    const int tile = ntiles_seq - 1 - (int)blockIdx.x;  // heavier (later) tiles first
-    const int kvh = blockIdx.y, b = blockIdx.z;
-    const int L = seq_len(g, b);
-    const int t0 = tile * Tq;
-    if (t0 >= L)
-        return;
-    const int nvalid = min(Tq, L - t0);
     const int words = (g.nbmax + 31) / 32;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(&bars[B_QFULL], 1);
-        mbar_init(&bars[B_LIST], kRows);
+        mbar_init(&bars[B_QEMPTY], 1);
+        mbar_init(&bars[B_DOFULL], 1);
+        mbar_init(&bars[B_DOEMPTY], 1);
         mbar_init(&bars[B_SFULL], 1);
         mbar_init(&bars[B_SFREE], 2 * kRows);
         mbar_init(&bars[B_DPFULL], 1);
         mbar_init(&bars[B_DPFREE], 2 * kRows);
-        mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_DONE], 1);
         mbar_init(&bars[B_DONEQ], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars[B_UFULL0 + x], 32);
+            mbar_init(&bars[B_UEMPTY0 + x], kUnionUsers);
+            mbar_init(&bars[B_ACCFULL0 + x], 1);
+            mbar_init(&bars[B_ACCEMPTY0 + x], 2 * kRows);
+        }
         for (int s = 0; s < NS; ++s) {
             mbar_init(&bars[B_KVF0 + s], 1);
             mbar_init(&bars[B_VF0 + s], 1);
@@ -142,70 +172,186 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         // One TMA box per lane: issuing them from a single thread serialises
         // about a hundred cycles per box.
         if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_do);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(&bars[B_QFULL], 2 * nrows * 128 * 2);
         }
-        __syncwarp();
-        {
-            const int nbox = rg ? 2 * Tq : 4;
-            for (int box = lane; box < nbox; box += 32) {
-                const int tensor = box & 1;
+        int lastq = -1, lastd = -1, last = -1, gi = 0;
+        for (int k = 0;; ++k) {
+            if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+                break;
+            const volatile int *hdr = u_hdr(k);
+            const int U = hdr[H_COUNT];
+            if (U < 0)
+                break;
+            const int b = hdr[H_B], kvh = hdr[H_KVH], t0 = hdr[H_T0];
+            const int *list = u_list(k);
+            // Q once the previous tile's last S has run, dO once its last dP has
+            bool ok = true;
+            for (int tensor = 0; tensor < 2 && ok; ++tensor) {
+                if (!mbar_wait_warp(&bars[tensor ? B_DOEMPTY : B_QEMPTY], (k & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t *bar = &bars[tensor ? B_DOFULL : B_QFULL];
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar, nrows * 128 * 2);
+                __syncwarp();
+                (tensor ? lastd : lastq) = k;
                 const CUtensorMap *map = tensor ? &tm_do : &tm_q;
+                uint8_t *base = sm + (tensor ? OFF_DO : OFF_Q);
                 if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
-                    const int tl = box >> 1;
-                    tma_load_5d(sm + (tensor ? OFF_DO : OFF_Q) + tl * G * 256, map, &bars[B_QFULL], 0, 0, 0,
-                                (b * g.Hq + kvh * G) / 8, t0 + tl);
-                } else {
-                    const int h = box >> 1;
-                    uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + h * kHalfBytes;
+                    for (int tl = lane; tl < Tq; tl += 32)
+                        tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t0 + tl);
+                } else if (lane < 2) {
+                    const int h = lane;
                     if (g.thd)
-                        tma_load_3d(dst, map, &bars[B_QFULL], h * 64, kvh * G, g.cu[b] + t0);
+                        tma_load_3d(base + h * kHalfBytes, map, bar, h * 64, kvh * G, g.cu[b] + t0);
                     else
-                        tma_load_4d(dst, map, &bars[B_QFULL], h * 64, t0, kvh * G, b);
+                        tma_load_4d(base + h * kHalfBytes, map, bar, h * 64, t0, kvh * G, b);
                 }
             }
-        }
-        bool ok = mbar_wait_warp(&bars[B_LIST], 0, abort_flag);
-        const int U = ok ? *n_list : 0;
-        const int npairs = (U + 1) >> 1;
-        int last = -1;
-        for (int i = 0; i < npairs && ok; ++i) {
-            const int s = i % NS;
-            if (!mbar_wait_warp(&bars[B_KVE0 + s], ((i / NS) & 1) ^ 1, abort_flag))
+            if (!ok)
                 break;
-            uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * kKvBytes);
-                mbar_arrive_expect_tx(&bars[B_VF0 + s], 2 * kKvBytes);
+            for (int i = 0; i < (U + 1) >> 1; ++i, ++gi) {
+                const int s = gi % NS;
+                if (!mbar_wait_warp(&bars[B_KVE0 + s], ((gi / NS) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * kKvBytes);
+                    mbar_arrive_expect_tx(&bars[B_VF0 + s], 2 * kKvBytes);
+                }
+                __syncwarp();
+                last = gi;
+                // lane -> (K or V, block e of the pair, 64-column half h), the K
+                // boxes first: S can start while V is still landing.  A missing
+                // second block repeats the first (finite data, P = dS = 0).
+                if (lane < 8) {
+                    const int isv = lane >> 2, e = (lane >> 1) & 1, h = lane & 1;
+                    const int j = list[min(2 * i + e, U - 1)];
+                    uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
+                    const CUtensorMap *map = isv ? &tm_v : &tm_k;
+                    uint64_t *bar = &bars[(isv ? B_VF0 : B_KVF0) + s];
+                    if (g.thd)
+                        tma_load_3d(dst, map, bar, h * 64, kvh, g.cu[b] + j * kKeys);
+                    else
+                        tma_load_4d(dst, map, bar, h * 64, j * kKeys, kvh, b);
+                }
             }
-            __syncwarp();
-            last = i;
-            // lane -> (K or V, block e of the pair, 64-column half h), the K
-            // boxes first: S can start while V is still landing.  A missing
-            // second block repeats the first (finite data, P = dS = 0).
-            if (lane < 8) {
-                const int isv = lane >> 2, e = (lane >> 1) & 1, h = lane & 1;
-                const int j = list[min(2 * i + e, U - 1)];
-                uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
-                const CUtensorMap *map = isv ? &tm_v : &tm_k;
-                uint64_t *bar = &bars[(isv ? B_VF0 : B_KVF0) + s];
-                if (g.thd)
-                    tma_load_3d(dst, map, bar, h * 64, kvh, g.cu[b] + j * kKeys);
-                else
-                    tma_load_4d(dst, map, bar, h * 64, j * kKeys, kvh, b);
-            }
+            if (!ok)
+                break;
+            mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
         }
         // copies in flight must land before the CTA may exit
-        if (lane == 0) {
+        if (lane == 0 && *abort_flag) {
             volatile int never = 0;
-            mbar_wait(&bars[B_QFULL], 0, &never);
-            if (*abort_flag && last >= 0) {
+            if (lastq >= 0)
+                mbar_wait(&bars[B_QFULL], lastq & 1, &never);
+            if (lastd >= 0)
+                mbar_wait(&bars[B_DOFULL], lastd & 1, &never);
+            if (last >= 0) {
                 mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
                 mbar_wait(&bars[B_VF0 + last % NS], (last / NS) & 1, &never);
             }
         }
         __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ union
+        // Deals the tiles (numbered heaviest first, in a snake over the CTAs,
+        // those past a sequence's end skipped) and builds, a tile ahead of
+        // its use, the ascending union of the blocks the tile's tokens select
+        // and each token's bitmap.  After the last tile a header with count
+        // -1 tells the other roles to stop.
+        const int Gc = gridDim.x, c = blockIdx.x;
+        const int per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
+        int r = 0;
+        for (int k = 0;; ++k) {
+            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+            bool more = false;
+            for (;; ++r) {
+                const int64_t L = (int64_t)r * Gc + ((r & 1) ? Gc - 1 - c : c);
+                if (L >= p.ntiles)
+                    break;
+                const int bg = (int)(L % nbg), tile = per_seq - 1 - (int)(L / nbg);
+                b = bg / g.Hkv;
+                kvh = bg % g.Hkv;
+                t0 = tile * Tq;
+                const int len = seq_len(g, b);
+                if (t0 < len) {
+                    nvalid = min(Tq, len - t0);
+                    more = true;
+                    ++r;
+                    break;
+                }
+            }
+            if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
+                break;
+            volatile int *hdr = u_hdr(k);
+            if (!more) {
+                if (lane == 0)
+                    hdr[H_COUNT] = -1;
+                __syncwarp();
+                mbar_arrive(&bars[B_UFULL0 + k % nub]);
+                break;
+            }
+            uint32_t *mask = u_mask(k), *ubits = u_ubits(k);
+            int *list = u_list(k);
+            if (!g.dense)
+                for (int x = lane; x < up.mask_words; x += 32)
+                    mask[x] = 0u;
+            for (int x = lane; x < words; x += 32)
+                ubits[x] = 0u;
+            __syncwarp();
+            if (g.dense) {
+                const int jmin = key_lo(g, t0) / g.bs, jmax = (t0 + nvalid - 1) / g.bs;
+                for (int j = jmin + lane; j <= jmax; j += 32)
+                    atomicOr(&ubits[j >> 5], 1u << (j & 31));
+            } else {
+                for (int x = lane; x < nvalid * g.S; x += 32) {
+                    const int tl = x / g.S, s = x % g.S;
+                    const int t = t0 + tl;
+                    const int j = idx_row(g, p.idx, b, kvh, t)[s];
+                    if (j >= 0 && j <= t / g.bs && j < g.nbmax) {
+                        atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
+                        atomicOr(&ubits[j >> 5], 1u << (j & 31));
+                    }
+                }
+            }
+            __syncwarp();
+            // ordered compaction
+            int base = 0;
+            for (int w0 = 0; w0 < words; w0 += 32) {
+                const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
+                const int cnt = __popc(bits);
+                int incl = cnt;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off)
+                        incl += y;
+                }
+                int pos = base + incl - cnt;
+                uint32_t bb = bits;
+                while (bb) {
+                    const int bit = __ffs(bb) - 1;
+                    bb &= bb - 1;
+                    list[pos++] = (w0 + lane) * 32 + bit;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                hdr[H_B] = b;
+                hdr[H_KVH] = kvh;
+                hdr[H_T0] = t0;
+                hdr[H_NVALID] = nvalid;
+                hdr[H_COUNT] = base;
+            }
+            __syncwarp();
+            mbar_arrive(&bars[B_UFULL0 + k % nub]);
+        }
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- MMA
         // Two issuing threads, so that a pair's dQ MMAs enter the tensor pipe
@@ -217,71 +363,110 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const uint32_t kv_s = smem_u32(sm + OFF_KV);
             // Q/dO tiles: 64-column halves and 8-row groups apart by these
             const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
-            bool ok = mbar_wait(&bars[B_LIST], 0, abort_flag) && mbar_wait(&bars[B_QFULL], 0, abort_flag);
-            const int U = ok ? *n_list : 0;
-            const int npairs = (U + 1) >> 1;
+            int gi = 0;
+            bool ok = true;
             if (warp == 2) {
                 const uint32_t idS = idesc_bf16(128, 128, false, false);
-                for (int si = 0; si < npairs && ok; ++si) {
-                    // the pair's K has landed; the softmax has taken the previous S
-                    if (!mbar_wait(&bars[B_KVF0 + si % NS], (si / NS) & 1, abort_flag) ||
-                        !mbar_wait(&bars[B_SFREE], (si & 1) ^ 1, abort_flag)) {
-                        ok = false;
+                for (int k = 0; ok; ++k) {
+                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                         break;
-                    }
-                    tc_fence_after();
-                    const uint32_t k_s = kv_s + (si % NS) * kPairBytes, v_s = k_s + kTileBytes;
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_S, sdesc_sw128(q_s + oq, 16, qsbo), sdesc_sw128(k_s + o, 16, 1024),
-                                 idS, kk > 0);
-                    }
-                    mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
-                    // the V has landed; the softmax has taken the previous dP
-                    if (!mbar_wait(&bars[B_VF0 + si % NS], (si / NS) & 1, abort_flag) ||
-                        !mbar_wait(&bars[B_DPFREE], (si & 1) ^ 1, abort_flag)) {
-                        ok = false;
+                    const int U = u_hdr(k)[H_COUNT];
+                    if (U < 0)
                         break;
+                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
+                    const int npairs = (U + 1) >> 1;
+                    // the tile's Q (and, before its first dP, dO) has landed
+                    if (!mbar_wait(&bars[B_QFULL], k & 1, abort_flag))
+                        break;
+                    for (int i = 0; i < npairs; ++i, ++gi) {
+                        // the pair's K has landed; the softmax has taken the previous S
+                        if (!mbar_wait(&bars[B_KVF0 + gi % NS], (gi / NS) & 1, abort_flag) ||
+                            !mbar_wait(&bars[B_SFREE], (gi & 1) ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t k_s = kv_s + (gi % NS) * kPairBytes, v_s = k_s + kTileBytes;
+                        for (int kk = 0; kk < kHead / 16; ++kk) {
+                            const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
+                            mma_bf16(tmem + TM_S, sdesc_sw128(q_s + oq, 16, qsbo), sdesc_sw128(k_s + o, 16, 1024),
+                                     idS, kk > 0);
+                        }
+                        mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
+                        if (i == npairs - 1)
+                            mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
+                        // the V (and dO) has landed; the softmax has taken the previous dP
+                        if ((i == 0 && !mbar_wait(&bars[B_DOFULL], k & 1, abort_flag)) ||
+                            !mbar_wait(&bars[B_VF0 + gi % NS], (gi / NS) & 1, abort_flag) ||
+                            !mbar_wait(&bars[B_DPFREE], (gi & 1) ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        for (int kk = 0; kk < kHead / 16; ++kk) {
+                            const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
+                            mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + oq, 16, qsbo), sdesc_sw128(v_s + o, 16, 1024),
+                                     idS, kk > 0);
+                        }
+                        mma_commit(&bars[B_DPFULL]);
                     }
-                    tc_fence_after();
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
-                        mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + oq, 16, qsbo), sdesc_sw128(v_s + o, 16, 1024),
-                                 idS, kk > 0);
+                    if (!ok)
+                        break;
+                    if (npairs == 0) {  // a tile with no blocks still releases its Q/dO once they land
+                        if (!mbar_wait(&bars[B_DOFULL], k & 1, abort_flag))
+                            break;
+                        mma_commit(&bars[B_QEMPTY]);
                     }
-                    mma_commit(&bars[B_DPFULL]);
+                    mma_commit(&bars[B_DOEMPTY]);
                 }
-                mma_commit(&bars[B_DONE]);
-                volatile int never = 0;
-                mbar_wait(&bars[B_DONE], 0, &never);
             } else {
                 const uint32_t idQ = idesc_bf16(128, 128, false, true);
-                for (int qi = 0; qi < npairs && ok; ++qi) {
-                    // dQ += dS K once the pair's dS is in shared memory; the
-                    // commit frees the pair's K/V stage for the loader
-                    if (!mbar_wait(&bars[B_DSF0 + qi % NS], (qi / NS) & 1, abort_flag)) {
-                        ok = false;
+                for (int k = 0; ok; ++k) {
+                    const int a = k & 1;  // the tile's dQ accumulator
+                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                         break;
-                    }
+                    const int U = u_hdr(k)[H_COUNT];
+                    if (U < 0)
+                        break;
+                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
+                    const int npairs = (U + 1) >> 1;
+                    // the epilogue has read this accumulator's previous tile
+                    if (!mbar_wait(&bars[B_ACCEMPTY0 + a], ((k >> 1) & 1) ^ 1, abort_flag))
+                        break;
                     tc_fence_after();
-                    const int s = qi % NS;
-                    const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
-                    for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
-                        mma_bf16(tmem + TM_DQ, sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ, (qi > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars[B_KVE0 + s]);
+                    for (int i = 0; i < npairs; ++i, ++gi) {
+                        // dQ += dS K once the pair's dS is in shared memory; the
+                        // commit frees the pair's K/V stage for the loader
+                        if (!mbar_wait(&bars[B_DSF0 + gi % NS], (gi / NS) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int s = gi % NS;
+                        const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
+                        for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
+                            mma_bf16(tmem + TM_DQ + a * 128,
+                                     sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                                     sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ,
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bars[B_KVE0 + s]);
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&bars[B_ACCFULL0 + a]);
                 }
-                mma_commit(&bars[B_ACCFULL]);
-                mma_commit(&bars[B_DONEQ]);
-                volatile int never = 0;
-                mbar_wait(&bars[B_DONEQ], 0, &never);
             }
+            // every MMA of this thread completes before TMEM is freed
+            uint64_t *done = &bars[warp == 2 ? B_DONE : B_DONEQ];
+            mma_commit(done);
+            volatile int never = 0;
+            mbar_wait(done, 0, &never);
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------------- union, softmax, epilogue
+        // ----------------------------------------------------- softmax, epilogue
         // Two warpgroups: warpgroup e (warps 4-7: e = 0, warps 8-11: e = 1)
         // takes block e of every pair (S/dP columns e*64 .. e*64+63) and dQ
         // columns e*64 .. e*64+63 in the epilogue; warp w reads TMEM lanes
@@ -289,132 +474,139 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         const int e = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        int U;
-        if (e == 0) {
-            U = qtile_union(g, p.idx, b, kvh, t0, nvalid, mask, ubits, list, r, lane, wq);
-            if (r == 0)
-                *n_list = U;
-            mbar_arrive(&bars[B_LIST]);
-        } else {
-            U = mbar_wait_warp(&bars[B_LIST], 0, abort_flag) ? *n_list : 0;
-        }
-        const int npairs = (U + 1) >> 1;
-
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         int tl, hh;
         qtile_row(g, Tq, r, tl, hh);
-        const bool rvalid = r < nrows && tl < nvalid;
-        const int t = t0 + tl;
-        float l2 = 0.f, dl = 0.f;
-        if (rvalid) {
-            const int64_t so = stat_off(g, b, kvh * G + hh, t);
-            l2 = p.lse[so] * 1.4426950408889634f;
-            dl = p.delta[so];
-        }
-        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t *my_mask = mask + (rvalid ? tl : 0) * words;
-        bool ok = true;
-        for (int i = 0; i < npairs; ++i) {
-            const int s = i % NS;
-            const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
-            const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
-            // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
-            const int lim = sel ? t - j * kKeys : -1;
-            const int lo = key_lo(g, t) - j * kKeys;
-            // no row of the warp ends or starts inside the block: a row attends
-            // all of it or none; none gets a +inf bias (exp2(-inf) = 0)
-            const bool whole = __all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0));
-            const bool any = __any_sync(0xffffffffu, sel);
-            // P = exp2(scale S - LSE) on the attended keys, while dP is still running
-            if (!mbar_wait_warp(&bars[B_SFULL], i & 1, abort_flag)) {
-                ok = false;
+        int gi = 0;
+        for (int k = 0;; ++k) {
+            const int a = k & 1;
+            if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                 break;
+            const volatile int *hdr = u_hdr(k);
+            const int U = hdr[H_COUNT];
+            if (U < 0)
+                break;
+            const int b = hdr[H_B], kvh = hdr[H_KVH], t0 = hdr[H_T0], nvalid = hdr[H_NVALID];
+            const int *list = u_list(k);
+            const int npairs = (U + 1) >> 1;
+            const bool rvalid = r < nrows && tl < nvalid;
+            const int t = t0 + tl;
+            float l2 = 0.f, dl = 0.f;
+            __nv_bfloat16 *dst = nullptr;  // the row's dQ columns e*64 .. e*64+63
+            if (rvalid) {
+                const int64_t so = stat_off(g, b, kvh * G + hh, t);
+                l2 = p.lse[so] * 1.4426950408889634f;
+                dl = p.delta[so];
+                dst = p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64;
             }
-            tc_fence_after();
-            uint32_t pv[64];
-            tmem_ld64(lane_base + TM_S + e * 64, pv);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars[B_SFREE]);
-            if (any) {
-                if (whole) {
-                    const float bias = sel ? l2 : __int_as_float(0x7f800000);
-                    const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias);
+            const uint32_t *my_mask = u_mask(k) + (rvalid ? tl : 0) * words;
+            bool ok = true;
+            for (int i = 0; i < npairs; ++i, ++gi) {
+                const int s = gi % NS;
+                const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
+                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+                // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
+                const int lim = sel ? t - j * kKeys : -1;
+                const int lo = key_lo(g, t) - j * kKeys;
+                // no row of the warp ends or starts inside the block: a row attends
+                // all of it or none; none gets a +inf bias (exp2(-inf) = 0)
+                const bool whole = __all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0));
+                const bool any = __any_sync(0xffffffffu, sel);
+                // P = exp2(scale S - LSE) on the attended keys, while dP is still running
+                if (!mbar_wait_warp(&bars[B_SFULL], gi & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t pv[64];
+                tmem_ld64(lane_base + TM_S + e * 64, pv);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars[B_SFREE]);
+                if (any) {
+                    if (whole) {
+                        const float bias = sel ? l2 : __int_as_float(0x7f800000);
+                        const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias);
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            float x0, x1;
+                            f2_split(f2_fma(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sc2, nb2), x0,
+                                     x1);
+                            pv[c] = __float_as_uint(ex2(x0));
+                            pv[c + 1] = __float_as_uint(ex2(x1));
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            pv[c] = __float_as_uint(
+                                (c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2) : 0.f);
+                    }
+                }
+                // dS = P (dP - delta)
+                if (!mbar_wait_warp(&bars[B_DPFULL], gi & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t dv_[64];
+                tmem_ld64(lane_base + TM_DP + e * 64, dv_);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars[B_DPFREE]);
+                uint32_t dk_[32];
+                if (any) {
+                    const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        float x0, x1;
-                        f2_split(f2_fma(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sc2, nb2), x0, x1);
-                        pv[c] = __float_as_uint(ex2(x0));
-                        pv[c + 1] = __float_as_uint(ex2(x1));
+                        float d0, d1;
+                        f2_split(f2_mul(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                        f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
+                                 d0, d1);
+                        dk_[c >> 1] = pack_bf16(d0, d1);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        pv[c] = __float_as_uint((c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
-                                                                      : 0.f);
+                    for (int c = 0; c < 32; ++c)
+                        dk_[c] = 0u;
                 }
+                // dS goes into this pair's V slot (dP is already computed), block e
+                // as the e-th 64-key K-chunk of the dQ MMA
+                const uint32_t row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + e * kHalfBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
+                                 dk_[4 * c + 3]);
+                fence_async_smem();
+                mbar_arrive(&bars[B_DSF0 + s]);
             }
-            // dS = P (dP - delta)
-            if (!mbar_wait_warp(&bars[B_DPFULL], i & 1, abort_flag)) {
-                ok = false;
+            if (!ok)
                 break;
-            }
+            mbar_arrive(&bars[B_UEMPTY0 + k % nub]);  // the union buffer may be rebuilt
+            // epilogue: dQ row r, columns e*64 .. e*64+63 = scale * TMEM.  Every
+            // lane of the warp runs the TMEM loads (.sync.aligned); only valid
+            // rows store.
+            if (!mbar_wait_warp(&bars[B_ACCFULL0 + a], (k >> 1) & 1, abort_flag))
+                break;
             tc_fence_after();
-            uint32_t dv_[64];
-            tmem_ld64(lane_base + TM_DP + e * 64, dv_);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bars[B_DPFREE]);
-            uint32_t dk_[32];
-            if (any) {
-                const uint64_t nd2 = f2(-dl, -dl);
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float d0, d1;
-                    f2_split(f2_mul(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
-                                    f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)),
-                             d0, d1);
-                    dk_[c >> 1] = pack_bf16(d0, d1);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    dk_[c] = 0u;
-            }
-            // dS goes into this pair's V slot (dP is already computed), block e
-            // as the e-th 64-key K-chunk of the dQ MMA
-            const uint32_t row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + e * kHalfBytes + r * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
-            fence_async_smem();
-            mbar_arrive(&bars[B_DSF0 + s]);
-        }
-        // epilogue: dQ row r, columns e*64 .. e*64+63 = scale * TMEM.  Every
-        // lane of the warp runs the TMEM loads (.sync.aligned); only valid
-        // rows store.
-        if (ok && npairs > 0)
-            ok = mbar_wait_warp(&bars[B_ACCFULL], 0, abort_flag);
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64 : nullptr;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t a[16];
-                tmem_ld16(lane_base + TM_DQ + e * 64 + c * 16, a);
+                uint32_t acc[16];
+                tmem_ld16(lane_base + TM_DQ + a * 128 + e * 64 + c * 16, acc);
                 tmem_wait_ld();
                 uint32_t w[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
-                    w[x] = npairs > 0 ? pack_bf16(__uint_as_float(a[2 * x]) * g.scale,
-                                                  __uint_as_float(a[2 * x + 1]) * g.scale)
+                    w[x] = npairs > 0 ? pack_bf16(__uint_as_float(acc[2 * x]) * g.scale,
+                                                  __uint_as_float(acc[2 * x + 1]) * g.scale)
                                       : 0u;
                 if (rvalid) {
                     *(uint4 *)(dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                     *(uint4 *)(dst + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&bars[B_ACCEMPTY0 + a]);
         }
-        tc_fence_before();
     }
 
     __syncthreads();
@@ -435,12 +627,17 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
+    const UnionPlan up = union_plan(g);
+    const int fixed = OFF_UNION + NUM_BARS * 8 + 64 + 1024;  // + alignment slack
+    const int nub = fixed + 2 * up.bytes <= kSmemLimit ? 2 : 1;
+    const int smem = fixed + nub * up.bytes;
+    if (smem > kSmemLimit)
+        return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     CUtensorMap tq, tdo, tk, tv;
     const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q/dO tiles, one box per token and tensor
     const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
                           : make_tmap(&tq, q, g, g.Hq, Tq, g.G) && make_tmap(&tdo, dO, g, g.Hq, Tq, g.G);
-    if (!qmaps ||
-        !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;
@@ -449,9 +646,15 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.delta = delta;
     p.dq = (__nv_bfloat16 *)dq;
     p.err = err;
-    dim3 grid((g.T + Tq - 1) / Tq, g.Hkv, g.B);
-    cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    dq_tc_kernel<<<grid, 384, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+    p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
+    p.nub = nub;
+    int grid = num_sms();
+    if (grid > p.ntiles)
+        grid = p.ntiles;
+    if (grid < 1)
+        return cudaSuccess;
+    cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    dq_tc_kernel<<<grid, 384, smem, st>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError();
 }
 
