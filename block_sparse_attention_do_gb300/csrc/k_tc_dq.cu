@@ -62,24 +62,6 @@ constexpr uint32_t TM_DP = 128;  // dP: 128 columns (keys)
 constexpr uint32_t TM_DQ = 256;  // dQ of even / odd tiles: 128 lanes (rows) x 128 columns (dims) each
 constexpr uint32_t TM_COLS = 512;
 
-// One union buffer: the tile's coordinates and list length (8 ints), the
-// per-token block bitmaps, the union bitmap and the ascending list.
-struct UnionPlan {
-    int mask_words, ubits_words, list_ints, bytes;
-};
-
-__host__ __device__ inline UnionPlan union_plan(const Geo &g)
-{
-    UnionPlan u;
-    const int words = (g.nbmax + 31) / 32;
-    u.mask_words = tile_tokens(g.G) * words;
-    u.ubits_words = (words + 3) & ~3;
-    u.list_ints = (g.nbmax + 3) & ~3;
-    u.bytes = ((8 + u.mask_words + u.ubits_words + u.list_ints) * 4 + 127) & ~127;
-    return u;
-}
-enum { H_B = 0, H_KVH, H_T0, H_NVALID, H_COUNT };  // header ints; count < 0: no more tiles
-
 struct Params {
     Geo g;
     const int *idx;
@@ -99,17 +81,15 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
-    const UnionPlan up = union_plan(g);
+    const UnionBuf up = union_buf(g);
     const int nub = p.nub;
     const int off_bar = OFF_UNION + nub * up.bytes;
     uint64_t *bars = (uint64_t *)(sm + off_bar);
     volatile int *abort_flag = (volatile int *)(sm + off_bar + NUM_BARS * 8);
     uint32_t *tmem_slot = (uint32_t *)(sm + off_bar + NUM_BARS * 8 + 16);
     // union buffer of this CTA's k-th tile, and the parity of its phase
-    auto u_hdr = [&](int k) { return (volatile int *)(sm + OFF_UNION + (k % nub) * up.bytes); };
-    auto u_mask = [&](int k) { return (uint32_t *)(u_hdr(k) + 8); };
-    auto u_ubits = [&](int k) { return u_mask(k) + up.mask_words; };
-    auto u_list = [&](int k) { return (int *)(u_ubits(k) + up.ubits_words); };
+    auto u_buf = [&](int k) { return (int *)(sm + OFF_UNION + (k % nub) * up.bytes); };
+    auto u_hdr = [&](int k) { return (volatile int *)u_buf(k); };
     auto u_par = [&](int k) { return (uint32_t)((k / nub) & 1); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,11 +162,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                 break;
             const volatile int *hdr = u_hdr(k);
-            const int U = hdr[H_COUNT];
+            const int U = hdr[UH_COUNT];
             if (U < 0)
                 break;
-            const int b = hdr[H_B], kvh = hdr[H_KVH], t0 = hdr[H_T0];
-            const int *list = u_list(k);
+            const int b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0];
+            const int *list = union_list(u_buf(k), up);
             // Q once the previous tile's last S has run, dO once its last dP has
             bool ok = true;
             for (int tensor = 0; tensor < 2 && ok; ++tensor) {
@@ -261,96 +241,25 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ union
-        // Deals the tiles (numbered heaviest first, in a snake over the CTAs,
-        // those past a sequence's end skipped) and builds, a tile ahead of
-        // its use, the ascending union of the blocks the tile's tokens select
-        // and each token's bitmap.  After the last tile a header with count
-        // -1 tells the other roles to stop.
-        const int Gc = gridDim.x, c = blockIdx.x;
-        const int per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
+        // Deals the tiles and builds each one's block union a tile ahead of
+        // its use; after the last tile a header with a negative count tells
+        // the other roles to stop.
         int r = 0;
         for (int k = 0;; ++k) {
             int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            bool more = false;
-            for (;; ++r) {
-                const int64_t L = (int64_t)r * Gc + ((r & 1) ? Gc - 1 - c : c);
-                if (L >= p.ntiles)
-                    break;
-                const int bg = (int)(L % nbg), tile = per_seq - 1 - (int)(L / nbg);
-                b = bg / g.Hkv;
-                kvh = bg % g.Hkv;
-                t0 = tile * Tq;
-                const int len = seq_len(g, b);
-                if (t0 < len) {
-                    nvalid = min(Tq, len - t0);
-                    more = true;
-                    ++r;
-                    break;
-                }
-            }
+            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
-            volatile int *hdr = u_hdr(k);
-            if (!more) {
-                if (lane == 0)
-                    hdr[H_COUNT] = -1;
-                __syncwarp();
-                mbar_arrive(&bars[B_UFULL0 + k % nub]);
-                break;
-            }
-            uint32_t *mask = u_mask(k), *ubits = u_ubits(k);
-            int *list = u_list(k);
-            if (!g.dense)
-                for (int x = lane; x < up.mask_words; x += 32)
-                    mask[x] = 0u;
-            for (int x = lane; x < words; x += 32)
-                ubits[x] = 0u;
-            __syncwarp();
-            if (g.dense) {
-                const int jmin = key_lo(g, t0) / g.bs, jmax = (t0 + nvalid - 1) / g.bs;
-                for (int j = jmin + lane; j <= jmax; j += 32)
-                    atomicOr(&ubits[j >> 5], 1u << (j & 31));
+            if (more) {
+                qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
             } else {
-                for (int x = lane; x < nvalid * g.S; x += 32) {
-                    const int tl = x / g.S, s = x % g.S;
-                    const int t = t0 + tl;
-                    const int j = idx_row(g, p.idx, b, kvh, t)[s];
-                    if (j >= 0 && j <= t / g.bs && j < g.nbmax) {
-                        atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
-                        atomicOr(&ubits[j >> 5], 1u << (j & 31));
-                    }
-                }
+                if (lane == 0)
+                    u_hdr(k)[UH_COUNT] = -1;
+                __syncwarp();
             }
-            __syncwarp();
-            // ordered compaction
-            int base = 0;
-            for (int w0 = 0; w0 < words; w0 += 32) {
-                const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
-                const int cnt = __popc(bits);
-                int incl = cnt;
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off)
-                        incl += y;
-                }
-                int pos = base + incl - cnt;
-                uint32_t bb = bits;
-                while (bb) {
-                    const int bit = __ffs(bb) - 1;
-                    bb &= bb - 1;
-                    list[pos++] = (w0 + lane) * 32 + bit;
-                }
-                base += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (lane == 0) {
-                hdr[H_B] = b;
-                hdr[H_KVH] = kvh;
-                hdr[H_T0] = t0;
-                hdr[H_NVALID] = nvalid;
-                hdr[H_COUNT] = base;
-            }
-            __syncwarp();
             mbar_arrive(&bars[B_UFULL0 + k % nub]);
+            if (!more)
+                break;
         }
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- MMA
@@ -370,7 +279,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 for (int k = 0; ok; ++k) {
                     if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                         break;
-                    const int U = u_hdr(k)[H_COUNT];
+                    const int U = u_hdr(k)[UH_COUNT];
                     if (U < 0)
                         break;
                     mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
@@ -427,7 +336,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     const int a = k & 1;  // the tile's dQ accumulator
                     if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                         break;
-                    const int U = u_hdr(k)[H_COUNT];
+                    const int U = u_hdr(k)[UH_COUNT];
                     if (U < 0)
                         break;
                     mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
@@ -483,11 +392,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                 break;
             const volatile int *hdr = u_hdr(k);
-            const int U = hdr[H_COUNT];
+            const int U = hdr[UH_COUNT];
             if (U < 0)
                 break;
-            const int b = hdr[H_B], kvh = hdr[H_KVH], t0 = hdr[H_T0], nvalid = hdr[H_NVALID];
-            const int *list = u_list(k);
+            const int b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0], nvalid = hdr[UH_NVALID];
+            const int *list = union_list(u_buf(k), up);
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
             const int t = t0 + tl;
@@ -499,7 +408,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 dl = p.delta[so];
                 dst = p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64;
             }
-            const uint32_t *my_mask = u_mask(k) + (rvalid ? tl : 0) * words;
+            const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
             bool ok = true;
             for (int i = 0; i < npairs; ++i, ++gi) {
                 const int s = gi % NS;
@@ -627,7 +536,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
-    const UnionPlan up = union_plan(g);
+    const UnionBuf up = union_buf(g);
     const int fixed = OFF_UNION + NUM_BARS * 8 + 64 + 1024;  // + alignment slack
     const int nub = fixed + 2 * up.bytes <= kSmemLimit ? 2 : 1;
     const int smem = fixed + nub * up.bytes;

@@ -77,27 +77,82 @@ __device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, 
     }
 }
 
-// Builds, with the 128 threads of warps 4-7 (named barrier 1), the ascending
-// list of blocks selected by any of the tile's tokens and one bitmap per
-// token.  Entries that are -1, out of range or in the future are skipped.
-// Returns the list length.
-__device__ __forceinline__ int qtile_union(const Geo &g, const int *idx, int b, int kvh, int t0, int nvalid,
-                                           uint32_t *mask, uint32_t *ubits, int *list, int tid, int lane,
-                                           int wq)
+// ---- persistent query-tile kernels: tiles are dealt to the CTAs in a snake,
+// heaviest (latest tokens) first, and one warp per CTA builds each tile's
+// block union a tile ahead of its use into one of (up to) two buffers.
+
+// A union buffer: UH_INTS header ints (the tile's coordinates and the list
+// length; a negative length ends the walk), the per-token block bitmaps, the
+// union bitmap and the ascending list.
+enum { UH_B = 0, UH_KVH, UH_T0, UH_NVALID, UH_COUNT, UH_INTS = 8 };
+struct UnionBuf {
+    int mask_words, ubits_words, list_ints, bytes;
+};
+__host__ __device__ inline UnionBuf union_buf(const Geo &g)
+{
+    UnionBuf u;
+    const int words = (g.nbmax + 31) / 32;
+    u.mask_words = tile_tokens(g.G) * words;
+    u.ubits_words = (words + 3) & ~3;
+    u.list_ints = (g.nbmax + 3) & ~3;
+    u.bytes = ((UH_INTS + u.mask_words + u.ubits_words + u.list_ints) * 4 + 127) & ~127;
+    return u;
+}
+__device__ __forceinline__ uint32_t *union_mask(int *buf) { return (uint32_t *)(buf + UH_INTS); }
+__device__ __forceinline__ int *union_list(int *buf, const UnionBuf &u)
+{
+    return buf + UH_INTS + u.mask_words + u.ubits_words;
+}
+
+// The CTA's next tile, cursor r (start at 0): tile numbers L = r * grid +
+// (c or grid-1-c, alternating), tile L covering (b, kv head) = L % (B*Hkv)
+// and the (L / (B*Hkv))-th tile from the end of the sequence; tiles past a
+// sequence's end are skipped.  False once L passes the tile count.
+__device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int &r, int &b, int &kvh, int &t0,
+                                           int &nvalid)
+{
+    const int Gc = gridDim.x, c = blockIdx.x;
+    const int Tq = tile_tokens(g.G), per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
+    for (;; ++r) {
+        const int64_t L = (int64_t)r * Gc + ((r & 1) ? Gc - 1 - c : c);
+        if (L >= ntiles)
+            return false;
+        const int bg = (int)(L % nbg), tile = per_seq - 1 - (int)(L / nbg);
+        b = bg / g.Hkv;
+        kvh = bg % g.Hkv;
+        t0 = tile * Tq;
+        const int len = seq_len(g, b);
+        if (t0 < len) {
+            nvalid = min(Tq, len - t0);
+            ++r;
+            return true;
+        }
+    }
+}
+
+// One warp fills buf for a tile: each token's block bitmap, the ascending
+// list of blocks selected by any of its tokens, then the header (written
+// last, with the list length).  Entries that are -1, out of range or in the
+// future are skipped.  The caller orders the writes before its release.
+__device__ __forceinline__ void qtile_union_warp(const Geo &g, const int *idx, const UnionBuf &u, int *buf, int b,
+                                                 int kvh, int t0, int nvalid, int lane)
 {
     const int words = (g.nbmax + 31) / 32;
-    for (int i = tid; i < tile_tokens(g.G) * words; i += 128)
-        mask[i] = 0;
-    for (int i = tid; i < words; i += 128)
-        ubits[i] = 0;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    uint32_t *mask = union_mask(buf), *ubits = mask + u.mask_words;
+    int *list = union_list(buf, u);
+    if (!g.dense)
+        for (int x = lane; x < u.mask_words; x += 32)
+            mask[x] = 0u;
+    for (int x = lane; x < words; x += 32)
+        ubits[x] = 0u;
+    __syncwarp();
     if (g.dense) {
         const int jmin = key_lo(g, t0) / g.bs, jmax = (t0 + nvalid - 1) / g.bs;
-        for (int j = jmin + tid; j <= jmax; j += 128)
+        for (int j = jmin + lane; j <= jmax; j += 32)
             atomicOr(&ubits[j >> 5], 1u << (j & 31));
     } else {
-        for (int i = tid; i < nvalid * g.S; i += 128) {
-            const int tl = i / g.S, s = i % g.S;
+        for (int x = lane; x < nvalid * g.S; x += 32) {
+            const int tl = x / g.S, s = x % g.S;
             const int t = t0 + tl;
             const int j = idx_row(g, idx, b, kvh, t)[s];
             if (j >= 0 && j <= t / g.bs && j < g.nbmax) {
@@ -106,33 +161,35 @@ __device__ __forceinline__ int qtile_union(const Geo &g, const int *idx, int b, 
             }
         }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    __shared__ int n_out;
-    if (wq == 0) {  // ordered compaction by one warp
-        int base = 0;
-        for (int w0 = 0; w0 < words; w0 += 32) {
-            const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
-            const int cnt = __popc(bits);
-            int incl = cnt;
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off)
-                    incl += y;
-            }
-            int pos = base + incl - cnt;
-            uint32_t bb = bits;
-            while (bb) {
-                const int bit = __ffs(bb) - 1;
-                bb &= bb - 1;
-                list[pos++] = (w0 + lane) * 32 + bit;
-            }
-            base += __shfl_sync(0xffffffffu, incl, 31);
+    __syncwarp();
+    // ordered compaction
+    int base = 0;
+    for (int w0 = 0; w0 < words; w0 += 32) {
+        const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
+        const int cnt = __popc(bits);
+        int incl = cnt;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += y;
         }
-        if (lane == 0)
-            n_out = base;
+        int pos = base + incl - cnt;
+        uint32_t bb = bits;
+        while (bb) {
+            const int bit = __ffs(bb) - 1;
+            bb &= bb - 1;
+            list[pos++] = (w0 + lane) * 32 + bit;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    return n_out;
+    if (lane == 0) {
+        buf[UH_B] = b;
+        buf[UH_KVH] = kvh;
+        buf[UH_T0] = t0;
+        buf[UH_NVALID] = nvalid;
+        buf[UH_COUNT] = base;
+    }
+    __syncwarp();
 }
 
 // does the row's token select block j?  (valid rows only)
