@@ -18,17 +18,22 @@
 // heaviest (latest tokens) first, dealt to the CTAs in a snake.  The next
 // tile's block union, its Q/dO load and its first K/V pairs overlap the
 // current tile's last pairs and epilogue: the union sits in one of two
-// shared-memory buffers (one when two do not fit), the dQ accumulator in one
-// of two TMEM buffers, and the two K/V pair stages form one ring across
-// tiles.  dS is written into the pair's V slot, free once dP is computed.
+// shared-memory buffers (one when two do not fit).
+//
+// dP has two TMEM buffers, so dP of the next pair runs while the softmax
+// works on this one; dS (bf16 pairs) is written over the first 32 columns
+// of its dP block and read from there as the A operand of dQ += dS K.  So K
+// and V have rings of their own, carried across tiles: V is held from its
+// load to dP, K from its load to the dQ product (three stages when they
+// fit, else two).
 //
 // Roles (12 warps): warp 1 picks the tiles and builds their block unions,
 // publishing each tile's coordinates with its union; warp 0 issues the TMA
-// copies (each tile's Q and dO, then its pairs' K boxes and V boxes, one box
-// per lane); warp 2 owns TMEM and one thread issues S and dP, one thread of
-// warp 3 the dQ MMAs; warps 4-7 form dS of each pair's first block and warps
-// 8-11 of its second, one row per thread (P from S while dP still runs),
-// and split the epilogue's columns the same way.
+// copies (each tile's Q and dO, then per pair its K boxes and its V boxes,
+// one box per lane); warp 2 owns TMEM and one thread issues S and dP, one
+// thread of warp 3 the dQ MMAs; warps 4-7 form dS of each pair's first block
+// and warps 8-11 of its second, one row per thread (P from S while dP still
+// runs), and split the epilogue's columns the same way.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -37,20 +42,18 @@ namespace {
 
 using namespace tc;
 
-constexpr int NS = 2;                       // K/V pair stages
-constexpr int kPairBytes = 2 * kTileBytes;  // K pair (32 KB) | V pair (32 KB, later dS)
+constexpr int kMaxNK = 3;  // K pair stages (32 KB each)
+constexpr int NV = 2;      // V pair stages (32 KB each)
 constexpr int OFF_Q = 0;
 constexpr int OFF_DO = OFF_Q + kTileBytes;
-constexpr int OFF_KV = OFF_DO + kTileBytes;
-constexpr int OFF_UNION = OFF_KV + NS * kPairBytes;  // union buffers, sized at launch
-constexpr int NUM_BARS = 28;
+constexpr int OFF_K = OFF_DO + kTileBytes;  // then the V ring, then the union buffers (sized at launch)
+constexpr int NUM_BARS = 32;
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
 enum {
-    B_QFULL = 0, B_QEMPTY, B_DOFULL, B_DOEMPTY, B_SFULL, B_SFREE, B_DPFULL, B_DPFREE,
-    B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_ACCFULL0, B_ACCFULL1, B_ACCEMPTY0, B_ACCEMPTY1,
-    B_KVF0, B_KVF1, B_VF0, B_VF1, B_KVE0, B_KVE1, B_DSF0, B_DSF1,  // B_KVF*: a pair's K (its V: B_VF*)
-    B_DONE, B_DONEQ, B_COUNT
+    B_QFULL = 0, B_QEMPTY, B_DOFULL, B_DOEMPTY, B_SFULL, B_SFREE, B_DPFULL0, B_DPFULL1, B_DPFREE0, B_DPFREE1,
+    B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_ACCFULL, B_ACCEMPTY, B_DONE, B_DONEQ, B_DSF0, B_DSF1,
+    B_KF0, B_KE0 = B_KF0 + kMaxNK, B_VF0 = B_KE0 + kMaxNK, B_VE0 = B_VF0 + NV, B_COUNT = B_VE0 + NV
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 // threads releasing a tile's union: the loader warp, the two MMA threads and
@@ -58,8 +61,8 @@ static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 constexpr int kUnionUsers = 32 + 2 + 2 * kRows;
 
 constexpr uint32_t TM_S = 0;     // S: 128 columns (keys)
-constexpr uint32_t TM_DP = 128;  // dP: 128 columns (keys)
-constexpr uint32_t TM_DQ = 256;  // dQ of even / odd tiles: 128 lanes (rows) x 128 columns (dims) each
+constexpr uint32_t TM_DP = 128;  // dP buffer x at 128 + x*128 (keys); dS of block e over its columns e*64 .. +31
+constexpr uint32_t TM_DQ = 384;  // dQ: 128 lanes (rows) x 128 columns (dims)
 constexpr uint32_t TM_COLS = 512;
 
 struct Params {
@@ -70,6 +73,7 @@ struct Params {
     int *err;
     int ntiles;  // query tiles over all (b, kv head)
     int nub;     // union buffers (1 or 2)
+    int nk;      // K pair stages (2 or 3)
 };
 
 __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -82,7 +86,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
     const UnionBuf up = union_buf(g);
-    const int nub = p.nub;
+    const int nub = p.nub, NK = p.nk;
+    const int OFF_V = OFF_K + NK * kTileBytes, OFF_UNION = OFF_V + NV * kTileBytes;
     const int off_bar = OFF_UNION + nub * up.bytes;
     uint64_t *bars = (uint64_t *)(sm + off_bar);
     volatile int *abort_flag = (volatile int *)(sm + off_bar + NUM_BARS * 8);
@@ -106,21 +111,26 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         mbar_init(&bars[B_DOEMPTY], 1);
         mbar_init(&bars[B_SFULL], 1);
         mbar_init(&bars[B_SFREE], 2 * kRows);
-        mbar_init(&bars[B_DPFULL], 1);
-        mbar_init(&bars[B_DPFREE], 2 * kRows);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars[B_DPFULL0 + x], 1);
+            mbar_init(&bars[B_DPFREE0 + x], 1);
+        }
         mbar_init(&bars[B_DONE], 1);
         mbar_init(&bars[B_DONEQ], 1);
+        mbar_init(&bars[B_ACCFULL], 1);
+        mbar_init(&bars[B_ACCEMPTY], 2 * kRows);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&bars[B_UFULL0 + x], 32);
             mbar_init(&bars[B_UEMPTY0 + x], kUnionUsers);
-            mbar_init(&bars[B_ACCFULL0 + x], 1);
-            mbar_init(&bars[B_ACCEMPTY0 + x], 2 * kRows);
+            mbar_init(&bars[B_DSF0 + x], 2 * kRows);
         }
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars[B_KVF0 + s], 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(&bars[B_KF0 + s], 1);
+            mbar_init(&bars[B_KE0 + s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
             mbar_init(&bars[B_VF0 + s], 1);
-            mbar_init(&bars[B_KVE0 + s], 1);
-            mbar_init(&bars[B_DSF0 + s], 2 * kRows);
+            mbar_init(&bars[B_VE0 + s], 1);
         }
         fence_barrier_init();
     }
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int lastq = -1, lastd = -1, last = -1, gi = 0;
+        int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0;
         for (int k = 0;; ++k) {
             if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                 break;
@@ -195,32 +205,33 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!ok)
                 break;
             for (int i = 0; i < (U + 1) >> 1; ++i, ++gi) {
-                const int s = gi % NS;
-                if (!mbar_wait_warp(&bars[B_KVE0 + s], ((gi / NS) & 1) ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *kd = sm + OFF_KV + s * kPairBytes, *vd = kd + kTileBytes;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[B_KVF0 + s], 2 * kKvBytes);
-                    mbar_arrive_expect_tx(&bars[B_VF0 + s], 2 * kKvBytes);
-                }
-                __syncwarp();
-                last = gi;
-                // lane -> (K or V, block e of the pair, 64-column half h), the K
-                // boxes first: S can start while V is still landing.  A missing
+                // lane -> (block e of the pair, 64-column half h); K first (S
+                // needs K only), then V once its stage is free.  A missing
                 // second block repeats the first (finite data, P = dS = 0).
-                if (lane < 8) {
-                    const int isv = lane >> 2, e = (lane >> 1) & 1, h = lane & 1;
-                    const int j = list[min(2 * i + e, U - 1)];
-                    uint8_t *dst = (isv ? vd : kd) + h * kHalfBytes + e * kKvHalfBytes;
-                    const CUtensorMap *map = isv ? &tm_v : &tm_k;
-                    uint64_t *bar = &bars[(isv ? B_VF0 : B_KVF0) + s];
-                    if (g.thd)
-                        tma_load_3d(dst, map, bar, h * 64, kvh, g.cu[b] + j * kKeys);
-                    else
-                        tma_load_4d(dst, map, bar, h * 64, j * kKeys, kvh, b);
+                const int e = lane >> 1, h = lane & 1;
+                const int j = list[min(2 * i + (e & 1), U - 1)];
+                for (int isv = 0; isv < 2; ++isv) {
+                    const int ns = isv ? NV : NK, st = gi % ns;
+                    uint64_t *full = &bars[(isv ? B_VF0 : B_KF0) + st];
+                    if (!mbar_wait_warp(&bars[(isv ? B_VE0 : B_KE0) + st], ((gi / ns) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(full, 2 * kKvBytes);
+                    __syncwarp();
+                    (isv ? lastv : last) = gi;
+                    if (lane < 4) {
+                        uint8_t *dst = sm + (isv ? OFF_V : OFF_K) + st * kTileBytes + h * kHalfBytes + e * kKvHalfBytes;
+                        const CUtensorMap *map = isv ? &tm_v : &tm_k;
+                        if (g.thd)
+                            tma_load_3d(dst, map, full, h * 64, kvh, g.cu[b] + j * kKeys);
+                        else
+                            tma_load_4d(dst, map, full, h * 64, j * kKeys, kvh, b);
+                    }
                 }
+                if (!ok)
+                    break;
             }
             if (!ok)
                 break;
@@ -233,10 +244,10 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 mbar_wait(&bars[B_QFULL], lastq & 1, &never);
             if (lastd >= 0)
                 mbar_wait(&bars[B_DOFULL], lastd & 1, &never);
-            if (last >= 0) {
-                mbar_wait(&bars[B_KVF0 + last % NS], (last / NS) & 1, &never);
-                mbar_wait(&bars[B_VF0 + last % NS], (last / NS) & 1, &never);
-            }
+            if (last >= 0)
+                mbar_wait(&bars[B_KF0 + last % NK], (last / NK) & 1, &never);
+            if (lastv >= 0)
+                mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, &never);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -265,11 +276,12 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         // ---------------------------------------------------------------- MMA
         // Two issuing threads, so that a pair's dQ MMAs enter the tensor pipe
         // as soon as its dS is ready instead of queueing behind the next
-        // pair's S/dP issue: warp 2 issues S and dP, warp 3 dQ (their TMEM
-        // columns are disjoint; each commit covers its own thread's MMAs).
+        // pair's S/dP issue: warp 2 issues S and dP (dP's completion frees the
+        // V stage), warp 3 dQ (whose completion frees the K stage and the dP
+        // buffer holding dS).  Each commit covers its own thread's MMAs.
         if (lane == 0) {
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
-            const uint32_t kv_s = smem_u32(sm + OFF_KV);
+            const uint32_t k_ring = smem_u32(sm + OFF_K), v_ring = smem_u32(sm + OFF_V);
             // Q/dO tiles: 64-column halves and 8-row groups apart by these
             const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
             int gi = 0;
@@ -289,13 +301,13 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         break;
                     for (int i = 0; i < npairs; ++i, ++gi) {
                         // the pair's K has landed; the softmax has taken the previous S
-                        if (!mbar_wait(&bars[B_KVF0 + gi % NS], (gi / NS) & 1, abort_flag) ||
+                        if (!mbar_wait(&bars[B_KF0 + gi % NK], (gi / NK) & 1, abort_flag) ||
                             !mbar_wait(&bars[B_SFREE], (gi & 1) ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t k_s = kv_s + (gi % NS) * kPairBytes, v_s = k_s + kTileBytes;
+                        const uint32_t k_s = k_ring + (gi % NK) * kTileBytes, v_s = v_ring + (gi % NV) * kTileBytes;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
@@ -305,10 +317,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
                         if (i == npairs - 1)
                             mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
-                        // the V (and dO) has landed; the softmax has taken the previous dP
+                        // the V (and dO) has landed; dQ of pair gi - 2 has read its
+                        // dS out of this dP buffer
                         if ((i == 0 && !mbar_wait(&bars[B_DOFULL], k & 1, abort_flag)) ||
-                            !mbar_wait(&bars[B_VF0 + gi % NS], (gi / NS) & 1, abort_flag) ||
-                            !mbar_wait(&bars[B_DPFREE], (gi & 1) ^ 1, abort_flag)) {
+                            !mbar_wait(&bars[B_VF0 + gi % NV], (gi / NV) & 1, abort_flag) ||
+                            !mbar_wait(&bars[B_DPFREE0 + (gi & 1)], ((gi >> 1) & 1) ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -316,10 +329,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
-                            mma_bf16(tmem + TM_DP, sdesc_sw128(do_s + oq, 16, qsbo), sdesc_sw128(v_s + o, 16, 1024),
-                                     idS, kk > 0);
+                            mma_bf16(tmem + TM_DP + (gi & 1) * 128, sdesc_sw128(do_s + oq, 16, qsbo),
+                                     sdesc_sw128(v_s + o, 16, 1024), idS, kk > 0);
                         }
-                        mma_commit(&bars[B_DPFULL]);
+                        mma_commit(&bars[B_DPFULL0 + (gi & 1)]);
+                        mma_commit(&bars[B_VE0 + gi % NV]);
                     }
                     if (!ok)
                         break;
@@ -333,7 +347,6 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             } else {
                 const uint32_t idQ = idesc_bf16(128, 128, false, true);
                 for (int k = 0; ok; ++k) {
-                    const int a = k & 1;  // the tile's dQ accumulator
                     if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                         break;
                     const int U = u_hdr(k)[UH_COUNT];
@@ -341,30 +354,30 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         break;
                     mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
                     const int npairs = (U + 1) >> 1;
-                    // the epilogue has read this accumulator's previous tile
-                    if (!mbar_wait(&bars[B_ACCEMPTY0 + a], ((k >> 1) & 1) ^ 1, abort_flag))
+                    // the epilogue has read the previous tile's dQ
+                    if (!mbar_wait(&bars[B_ACCEMPTY], (k & 1) ^ 1, abort_flag))
                         break;
                     tc_fence_after();
                     for (int i = 0; i < npairs; ++i, ++gi) {
-                        // dQ += dS K once the pair's dS is in shared memory; the
-                        // commit frees the pair's K/V stage for the loader
-                        if (!mbar_wait(&bars[B_DSF0 + gi % NS], (gi / NS) & 1, abort_flag)) {
+                        // dQ += dS K once the pair's dS is in TMEM; the commits free
+                        // the K stage and the dP buffer
+                        const int db = gi & 1, sk = gi % NK;
+                        if (!mbar_wait(&bars[B_DSF0 + db], (gi >> 1) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const int s = gi % NS;
-                        const uint32_t k_s = kv_s + s * kPairBytes, d_s = k_s + kTileBytes;
-                        for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (K-major, 2 halves) x K pair (MN-major)
-                            mma_bf16(tmem + TM_DQ + a * 128,
-                                     sdesc_sw128(d_s + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                                     sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ,
-                                     (i > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bars[B_KVE0 + s]);
+                        const uint32_t k_s = k_ring + sk * kTileBytes;
+                        for (int kk = 0; kk < 8; ++kk)  // 128 keys: dS (TMEM) x K pair (MN-major)
+                            mma_bf16_ts(tmem + TM_DQ, tmem + TM_DP + db * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                                        sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), idQ,
+                                        (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bars[B_KE0 + sk]);
+                        mma_commit(&bars[B_DPFREE0 + db]);
                     }
                     if (!ok)
                         break;
-                    mma_commit(&bars[B_ACCFULL0 + a]);
+                    mma_commit(&bars[B_ACCFULL]);
                 }
             }
             // every MMA of this thread completes before TMEM is freed
@@ -388,7 +401,6 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         qtile_row(g, Tq, r, tl, hh);
         int gi = 0;
         for (int k = 0;; ++k) {
-            const int a = k & 1;
             if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                 break;
             const volatile int *hdr = u_hdr(k);
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
             bool ok = true;
             for (int i = 0; i < npairs; ++i, ++gi) {
-                const int s = gi % NS;
+                const int db = gi & 1;  // dP buffer
                 const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
                 const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
                 // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
@@ -452,16 +464,14 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     }
                 }
                 // dS = P (dP - delta)
-                if (!mbar_wait_warp(&bars[B_DPFULL], gi & 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_DPFULL0 + db], (gi >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t dv_[64];
-                tmem_ld64(lane_base + TM_DP + e * 64, dv_);
+                tmem_ld64(lane_base + TM_DP + db * 128 + e * 64, dv_);
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bars[B_DPFREE]);
                 uint32_t dk_[32];
                 if (any) {
                     const uint64_t nd2 = f2(-dl, -dl);
@@ -478,15 +488,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     for (int c = 0; c < 32; ++c)
                         dk_[c] = 0u;
                 }
-                // dS goes into this pair's V slot (dP is already computed), block e
-                // as the e-th 64-key K-chunk of the dQ MMA
-                const uint32_t row = smem_u32(sm + OFF_KV + s * kPairBytes + kTileBytes) + e * kHalfBytes + r * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
-                                 dk_[4 * c + 3]);
-                fence_async_smem();
-                mbar_arrive(&bars[B_DSF0 + s]);
+                // dS over the first half of this block's dP columns
+                tmem_st32(lane_base + TM_DP + db * 128 + e * 64, dk_);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[B_DSF0 + db]);
             }
             if (!ok)
                 break;
@@ -494,13 +500,13 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             // epilogue: dQ row r, columns e*64 .. e*64+63 = scale * TMEM.  Every
             // lane of the warp runs the TMEM loads (.sync.aligned); only valid
             // rows store.
-            if (!mbar_wait_warp(&bars[B_ACCFULL0 + a], (k >> 1) & 1, abort_flag))
+            if (!mbar_wait_warp(&bars[B_ACCFULL], k & 1, abort_flag))
                 break;
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t acc[16];
-                tmem_ld16(lane_base + TM_DQ + a * 128 + e * 64 + c * 16, acc);
+                tmem_ld16(lane_base + TM_DQ + e * 64 + c * 16, acc);
                 tmem_wait_ld();
                 uint32_t w[8];
 #pragma unroll
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars[B_ACCEMPTY0 + a]);
+            mbar_arrive(&bars[B_ACCEMPTY]);
         }
     }
 
@@ -537,11 +543,19 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
     const int Tq = tile_tokens(g.G);
     const UnionBuf up = union_buf(g);
-    const int fixed = OFF_UNION + NUM_BARS * 8 + 64 + 1024;  // + alignment slack
-    const int nub = fixed + 2 * up.bytes <= kSmemLimit ? 2 : 1;
-    const int smem = fixed + nub * up.bytes;
-    if (smem > kSmemLimit)
+    // three K stages and two union buffers when they fit, else fewer
+    const int base = OFF_K + NV * kTileBytes + NUM_BARS * 8 + 64 + 1024;  // + alignment slack
+    int nk = 0, nub = 0;
+    for (int c = 0; c < 4 && !nk; ++c) {
+        const int k_ = c < 2 ? 3 : 2, u_ = 2 - (c & 1);
+        if (base + k_ * kTileBytes + u_ * up.bytes <= kSmemLimit) {
+            nk = k_;
+            nub = u_;
+        }
+    }
+    if (!nk)
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
+    const int smem = base + nk * kTileBytes + nub * up.bytes;
     CUtensorMap tq, tdo, tk, tv;
     const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q/dO tiles, one box per token and tensor
     const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
@@ -557,6 +571,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.err = err;
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
+    p.nk = nk;
     int grid = num_sms();
     if (grid > p.ntiles)
         grid = p.ntiles;
