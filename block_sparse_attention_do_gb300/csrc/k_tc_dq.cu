@@ -27,13 +27,12 @@
 // load to dP, K from its load to the dQ product (three stages when they
 // fit, else two).
 //
-// Roles (12 warps): warp 1 picks the tiles and builds their block unions,
-// publishing each tile's coordinates with its union; warp 0 issues the TMA
-// copies (each tile's Q and dO, then per pair its K boxes and its V boxes,
-// one box per lane); warp 2 owns TMEM and one thread issues S and dP, one
-// thread of warp 3 the dQ MMAs; warps 4-7 form dS of each pair's first block
-// and warps 8-11 of its second, one row per thread (P from S while dP still
-// runs), and split the epilogue's columns the same way.
+// Roles (12 warps): warp 0 deals the tiles, builds each tile's block union
+// and issues the TMA copies (the tile's Q and dO, then per pair its K boxes
+// and its V boxes, one box per lane); one thread each of warps 2, 1 and 3
+// issues the S, dP and dQ MMAs (warp 2 owns TMEM); warps 4-7 form dS of each
+// pair's first block and warps 8-11 of its second, one row per thread (P
+// from S while dP still runs), and split the epilogue's columns the same way.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -52,13 +51,13 @@ constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
 enum {
     B_QFULL = 0, B_QEMPTY, B_DOFULL, B_DOEMPTY, B_SFULL, B_SFREE, B_DPFULL0, B_DPFULL1, B_DPFREE0, B_DPFREE1,
-    B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_ACCFULL, B_ACCEMPTY, B_DONE, B_DONEQ, B_DSF0, B_DSF1,
+    B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_ACCFULL, B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_DSF0, B_DSF1,
     B_KF0, B_KE0 = B_KF0 + kMaxNK, B_VF0 = B_KE0 + kMaxNK, B_VE0 = B_VF0 + NV, B_COUNT = B_VE0 + NV
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
-// threads releasing a tile's union: the loader warp, the two MMA threads and
-// the 256 softmax threads
-constexpr int kUnionUsers = 32 + 2 + 2 * kRows;
+// threads releasing a tile's union: the loader warp, the three MMA threads
+// and the 256 softmax threads
+constexpr int kUnionUsers = 32 + 3 + 2 * kRows;
 
 constexpr uint32_t TM_S = 0;     // S: 128 columns (keys)
 constexpr uint32_t TM_DP = 128;  // dP buffer x at 128 + x*128 (keys); dS of block e over its columns e*64 .. +31
@@ -115,8 +114,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             mbar_init(&bars[B_DPFULL0 + x], 1);
             mbar_init(&bars[B_DPFREE0 + x], 1);
         }
-        mbar_init(&bars[B_DONE], 1);
-        mbar_init(&bars[B_DONEQ], 1);
+        for (int x = 0; x < 3; ++x)
+            mbar_init(&bars[B_DONE0 + x], 1);
         mbar_init(&bars[B_ACCFULL], 1);
         mbar_init(&bars[B_ACCEMPTY], 2 * kRows);
         for (int x = 0; x < 2; ++x) {
@@ -167,15 +166,27 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0;
+        int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0, r = 0;
         for (int k = 0;; ++k) {
-            if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+            // The tile and its block union: this warp deals the tiles and builds
+            // each union after issuing the previous tile's copies, while the
+            // K/V rings still hold several of that tile's pairs; after the last
+            // tile a header with a negative count tells the other roles to stop.
+            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
+            if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
-            const volatile int *hdr = u_hdr(k);
-            const int U = hdr[UH_COUNT];
-            if (U < 0)
+            if (more) {
+                qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
+            } else {
+                if (lane == 0)
+                    u_hdr(k)[UH_COUNT] = -1;
+                __syncwarp();
+            }
+            mbar_arrive(&bars[B_UFULL0 + k % nub]);
+            if (!more)
                 break;
-            const int b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0];
+            const int U = u_hdr(k)[UH_COUNT];
             const int *list = union_list(u_buf(k), up);
             // Q once the previous tile's last S has run, dO once its last dP has
             bool ok = true;
@@ -250,53 +261,31 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, &never);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ union
-        // Deals the tiles and builds each one's block union a tile ahead of
-        // its use; after the last tile a header with a negative count tells
-        // the other roles to stop.
-        int r = 0;
-        for (int k = 0;; ++k) {
-            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
-            if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
-                break;
-            if (more) {
-                qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
-            } else {
-                if (lane == 0)
-                    u_hdr(k)[UH_COUNT] = -1;
-                __syncwarp();
-            }
-            mbar_arrive(&bars[B_UFULL0 + k % nub]);
-            if (!more)
-                break;
-        }
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp <= 3) {
         // ---------------------------------------------------------------- MMA
-        // Two issuing threads, so that a pair's dQ MMAs enter the tensor pipe
-        // as soon as its dS is ready instead of queueing behind the next
-        // pair's S/dP issue: warp 2 issues S and dP (dP's completion frees the
-        // V stage), warp 3 dQ (whose completion frees the K stage and the dP
-        // buffer holding dS).  Each commit covers its own thread's MMAs.
+        // Three issuing threads in three warps (one thread issues a tcgen05 MMA
+        // only every ~150 cycles): warp 2 issues S, warp 1 dP (whose completion
+        // frees the V stage), warp 3 dQ (whose completion frees the K stage
+        // and the dP buffer holding dS), so a ready product never queues behind
+        // another's issue.  Each commit covers its own thread's MMAs.
         if (lane == 0) {
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
             const uint32_t k_ring = smem_u32(sm + OFF_K), v_ring = smem_u32(sm + OFF_V);
             // Q/dO tiles: 64-column halves and 8-row groups apart by these
             const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
+            const uint32_t idS = idesc_bf16(128, 128, false, false), idQ = idesc_bf16(128, 128, false, true);
             int gi = 0;
             bool ok = true;
-            if (warp == 2) {
-                const uint32_t idS = idesc_bf16(128, 128, false, false);
-                for (int k = 0; ok; ++k) {
-                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
-                        break;
-                    const int U = u_hdr(k)[UH_COUNT];
-                    if (U < 0)
-                        break;
-                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
-                    const int npairs = (U + 1) >> 1;
-                    // the tile's Q (and, before its first dP, dO) has landed
+            for (int k = 0; ok; ++k) {
+                if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+                    break;
+                const int U = u_hdr(k)[UH_COUNT];
+                if (U < 0)
+                    break;
+                mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
+                const int npairs = (U + 1) >> 1;
+                if (warp == 2) {
+                    // S = Q K^T, once the tile's Q has landed
                     if (!mbar_wait(&bars[B_QFULL], k & 1, abort_flag))
                         break;
                     for (int i = 0; i < npairs; ++i, ++gi) {
@@ -307,25 +296,32 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t k_s = k_ring + (gi % NK) * kTileBytes, v_s = v_ring + (gi % NV) * kTileBytes;
+                        const uint32_t k_s = k_ring + (gi % NK) * kTileBytes;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
                             mma_bf16(tmem + TM_S, sdesc_sw128(q_s + oq, 16, qsbo), sdesc_sw128(k_s + o, 16, 1024),
                                      idS, kk > 0);
                         }
-                        mma_commit(&bars[B_SFULL]);  // the softmax starts on P while dP runs
-                        if (i == npairs - 1)
-                            mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
-                        // the V (and dO) has landed; dQ of pair gi - 2 has read its
-                        // dS out of this dP buffer
-                        if ((i == 0 && !mbar_wait(&bars[B_DOFULL], k & 1, abort_flag)) ||
-                            !mbar_wait(&bars[B_VF0 + gi % NV], (gi / NV) & 1, abort_flag) ||
+                        mma_commit(&bars[B_SFULL]);
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
+                } else if (warp == 1) {
+                    // dP = dO V^T, once the tile's dO has landed
+                    if (!mbar_wait(&bars[B_DOFULL], k & 1, abort_flag))
+                        break;
+                    for (int i = 0; i < npairs; ++i, ++gi) {
+                        // the V has landed; dQ of pair gi - 2 has read its dS out
+                        // of this dP buffer
+                        if (!mbar_wait(&bars[B_VF0 + gi % NV], (gi / NV) & 1, abort_flag) ||
                             !mbar_wait(&bars[B_DPFREE0 + (gi & 1)], ((gi >> 1) & 1) ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        const uint32_t v_s = v_ring + (gi % NV) * kTileBytes;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t o = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * qhalf + (kk & 3) * 32;
@@ -337,23 +333,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                     }
                     if (!ok)
                         break;
-                    if (npairs == 0) {  // a tile with no blocks still releases its Q/dO once they land
-                        if (!mbar_wait(&bars[B_DOFULL], k & 1, abort_flag))
-                            break;
-                        mma_commit(&bars[B_QEMPTY]);
-                    }
-                    mma_commit(&bars[B_DOEMPTY]);
-                }
-            } else {
-                const uint32_t idQ = idesc_bf16(128, 128, false, true);
-                for (int k = 0; ok; ++k) {
-                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
-                        break;
-                    const int U = u_hdr(k)[UH_COUNT];
-                    if (U < 0)
-                        break;
-                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
-                    const int npairs = (U + 1) >> 1;
+                    mma_commit(&bars[B_DOEMPTY]);  // the next tile's dO may land
+                } else {
                     // the epilogue has read the previous tile's dQ
                     if (!mbar_wait(&bars[B_ACCEMPTY], (k & 1) ^ 1, abort_flag))
                         break;
@@ -381,7 +362,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 }
             }
             // every MMA of this thread completes before TMEM is freed
-            uint64_t *done = &bars[warp == 2 ? B_DONE : B_DONEQ];
+            uint64_t *done = &bars[B_DONE0 + warp - 1];
             mma_commit(done);
             volatile int never = 0;
             mbar_wait(done, 0, &never);
