@@ -12,13 +12,14 @@
 // several units writes fp32 partials that a separate kernel adds in unit
 // order; a block held by one unit writes dK/dV directly.
 //
-// Roles (8 warps):  warp 0 loads (TMA for K_j/V_j; Q/dO rows by one TMA box
+// Roles (11 warps):  warp 0 loads (TMA for K_j/V_j; Q/dO rows by one TMA box
 // per token -- its G heads, both halves -- when G % 8 == 0, else by 16-byte
 // cp.async with the swizzle applied by hand); warp 1 resolves each tile's
-// token ids, LSE and delta a tile ahead; warp 2 owns TMEM and one thread
-// issues every MMA; warps 4-7 compute P/dS for one row each and run the
-// epilogue.  Two Q/dO stages (row-group layout, so that a token's box is
-// contiguous), two S/dP TMEM buffers, one P/dS buffer.
+// token ids, LSE and delta a tile ahead; warp 2 owns TMEM; one thread each
+// of warps 2, 8, 9 and 10 issues the S, dP, dV^T and dK^T MMAs; warps 4-7
+// compute P/dS for one row each and run the epilogue.  Two Q/dO stages
+// (row-group layout, so that a token's box is contiguous), two S/dP TMEM
+// buffers, one P/dS buffer.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -38,14 +39,15 @@ constexpr int OFF_LSE = OFF_DS + kRows * 128;    // float [2][128], LSE * log2(e
 constexpr int OFF_DLT = OFF_LSE + 2 * kRows * 4; // float [2][128]
 constexpr int OFF_TOK = OFF_DLT + 2 * kRows * 4; // int   [2][128]
 constexpr int OFF_BAR = OFF_TOK + 2 * kRows * 4;
-constexpr int NUM_BARS = 20;
+constexpr int NUM_BARS = 24;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
 // barrier slots
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DONE, B_IDX0, B_IDX1, B_DPFULL0, B_DPFULL1, B_COUNT
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_IDX0, B_IDX1, B_DPFULL0, B_DPFULL1,
+    B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
@@ -78,7 +80,7 @@ __device__ __forceinline__ int unit_of(int k, int n_units)
 }
 
 template <bool GATHER_TMA>
-__global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_do,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v,
@@ -106,10 +108,10 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         mbar_init(&bars[B_FULL1], GATHER_TMA ? 2 : 32);
         mbar_init(&bars[B_IDX0], 32);
         mbar_init(&bars[B_IDX1], 32);
-        mbar_init(&bars[B_EMPTY0], 1);
-        mbar_init(&bars[B_EMPTY1], 1);
+        mbar_init(&bars[B_EMPTY0], 2);
+        mbar_init(&bars[B_EMPTY1], 2);
         mbar_init(&bars[B_KVFULL], 1);
-        mbar_init(&bars[B_KVEMPTY], 1);
+        mbar_init(&bars[B_KVEMPTY], 2);
         mbar_init(&bars[B_SFULL0], 1);
         mbar_init(&bars[B_DPFULL0], 1);
         mbar_init(&bars[B_DPFULL1], 1);
@@ -117,10 +119,11 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
         mbar_init(&bars[B_SFREE0], kRows);
         mbar_init(&bars[B_SFREE1], kRows);
         mbar_init(&bars[B_PFULL], kRows);
-        mbar_init(&bars[B_PFREE], 1);
-        mbar_init(&bars[B_ACCFULL], 1);
+        mbar_init(&bars[B_PFREE], 2);
+        mbar_init(&bars[B_ACCFULL], 2);
         mbar_init(&bars[B_ACCEMPTY], kRows);
-        mbar_init(&bars[B_DONE], 1);
+        for (int x = 0; x < 4; ++x)
+            mbar_init(&bars[B_DONE0 + x], 1);
         fence_barrier_init();
     }
     if (warp == 2) {
@@ -303,99 +306,78 @@ __global__ void __launch_bounds__(256, 1) dkdv_tc_kernel(const __grid_constant__
             if (ui >= 0)
                 fetch();
         }
-    } else if (warp == 2) {
+    } else if (warp == 2 || warp >= 8) {
         // -------------------------------------------------------------- MMA
+        // Four issuing threads in four warps (one thread issues a tcgen05 MMA
+        // only every ~150 cycles): warp 2 issues S, warp 8 dP, warp 9 dV^T and
+        // warp 10 dK^T; each walks every (unit, tile).  Barriers shared by two
+        // of them count two commits: KVEMPTY (S and dP), EMPTY, PFREE and
+        // ACCFULL (dV and dK).
         if (lane == 0) {
+            const int role = warp == 2 ? 0 : warp - 7;  // 0 S, 1 dP, 2 dV, 3 dK
             const uint32_t idS = idesc_bf16(128, 64, false, false);
             const uint32_t idV = idesc_bf16(128, 64, true, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
             const uint32_t k_s = smem_u32(sm + OFF_K), v_s = smem_u32(sm + OFF_V);
             const uint32_t p_s = smem_u32(sm + OFF_P), ds_s = smem_u32(sm + OFF_DS);
-            // cursor S issues S/dP, cursor V issues dV/dK; both walk (unit, tile)
-            int sU = unit_of(0, n_units), sT = 0, sIt = 0, sUc = 0, sN = -1;
-            int vU = sU, vT = 0, vIt = 0, vUc = 0, vN = -1;
-            auto ntiles_of = [&](int ui) { return (p.units[ui].count + Tt - 1) / Tt; };
-            if (sU >= 0)
-                sN = ntiles_of(sU);
-            if (vU >= 0)
-                vN = ntiles_of(vU);
-            const uint64_t t_start = globaltimer();
-            uint64_t t_last = t_start;
-            while (vU >= 0 && !*abort_flag) {
-                bool progressed = false;
-                // dV/dK of the oldest tile whose P/dS are ready
-                if (vIt < sIt && mbar_test(&bars[B_PFULL], vIt & 1) &&
-                    (vT > 0 || mbar_test(&bars[B_ACCEMPTY], (vUc & 1) ^ 1))) {
-                    tc_fence_after();
-                    const int st = vIt & 1;
-                    for (int kr = 0; kr < kRows / 16; ++kr) {
-                        const uint32_t acc = (vT > 0 || kr > 0) ? 1u : 0u;
-                        // 16 rows = two row groups; LBO steps the 64-dim halves (M)
-                        mma_bf16(tmem + TM_DV,
-                                 sdesc_sw128(do_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
-                                 sdesc_sw128(p_s + kr * 2048, 8192, 1024), idV, acc);
-                        mma_bf16(tmem + TM_DK,
-                                 sdesc_sw128(q_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
-                                 sdesc_sw128(ds_s + kr * 2048, 8192, 1024), idV, acc);
-                    }
-                    mma_commit(&bars[B_PFREE]);
-                    mma_commit(&bars[B_EMPTY0 + st]);
-                    if (vT + 1 == vN) {
-                        mma_commit(&bars[B_ACCFULL]);
-                        vU = unit_of(++vUc, n_units);
-                        vT = 0;
-                        vN = vU >= 0 ? ntiles_of(vU) : -1;
+            // S / dP: A = Q / dO (row-group tile), B = K_j / V_j
+            const uint32_t a_s = role == 1 || role == 2 ? do_s : q_s;
+            const uint32_t b_s = role == 1 ? v_s : k_s;
+            int it = 0, uc = 0;
+            bool ok = true;
+            for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
+                const int ntiles = (p.units[ui].count + Tt - 1) / Tt;
+                for (int ti = 0; ti < ntiles; ++ti, ++it) {
+                    const int st = it & 1;
+                    if (role <= 1) {
+                        // the tile's rows (and at a unit's start K_j / V_j) have
+                        // landed; the softmax has loaded S/dP of tile it - 2
+                        if (!mbar_wait(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
+                            !mbar_wait(&bars[B_SFREE0 + st], ((it >> 1) & 1) ^ 1, abort_flag) ||
+                            (ti == 0 && !mbar_wait(&bars[B_KVFULL], uc & 1, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t col = tmem + TM_S + st * 128 + role * 64;
+                        for (int kk = 0; kk < kHead / 16; ++kk) {
+                            const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
+                            const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
+                            mma_bf16(col, sdesc_sw128(a_s + st * kTileBytes + ao, 16, kRgStride),
+                                     sdesc_sw128(b_s + bo, 16, 1024), idS, kk > 0);
+                        }
+                        mma_commit(&bars[(role == 0 ? B_SFULL0 : B_DPFULL0) + st]);
+                        if (ti + 1 == ntiles)
+                            mma_commit(&bars[B_KVEMPTY]);
                     } else {
-                        ++vT;
+                        // P (dV) or dS (dK) of the tile is in shared memory; at a
+                        // unit's start the epilogue has read the accumulators
+                        if (!mbar_wait(&bars[B_PFULL], it & 1, abort_flag) ||
+                            (ti == 0 && !mbar_wait(&bars[B_ACCEMPTY], (uc & 1) ^ 1, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t col = tmem + (role == 2 ? TM_DV : TM_DK);
+                        const uint32_t pb = role == 2 ? p_s : ds_s;
+                        for (int kr = 0; kr < kRows / 16; ++kr)
+                            // 16 rows = two row groups; LBO steps the 64-dim halves (M)
+                            mma_bf16(col, sdesc_sw128(a_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
+                                     sdesc_sw128(pb + kr * 2048, 8192, 1024), idV, (ti > 0 || kr > 0) ? 1u : 0u);
+                        mma_commit(&bars[B_PFREE]);
+                        mma_commit(&bars[B_EMPTY0 + st]);
+                        if (ti + 1 == ntiles)
+                            mma_commit(&bars[B_ACCFULL]);
                     }
-                    ++vIt;
-                    progressed = true;
-                }
-                // S/dP of the next tile (at most two tiles ahead of dV/dK)
-                if (sU >= 0 && sIt < vIt + 2 && mbar_test(&bars[B_FULL0 + (sIt & 1)], (sIt >> 1) & 1) &&
-                    mbar_test(&bars[B_SFREE0 + (sIt & 1)], ((sIt >> 1) & 1) ^ 1) &&
-                    (sT > 0 || mbar_test(&bars[B_KVFULL], sUc & 1))) {
-                    tc_fence_after();
-                    const int st = sIt & 1;
-                    const uint32_t dS_col = tmem + TM_S + st * 128;
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
-                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                        mma_bf16(dS_col, sdesc_sw128(q_s + st * kTileBytes + ao, 16, kRgStride),
-                                 sdesc_sw128(k_s + bo, 16, 1024), idS, kk > 0);
-                    }
-                    mma_commit(&bars[B_SFULL0 + st]);  // the softmax starts on P while dP runs
-                    for (int kk = 0; kk < kHead / 16; ++kk) {
-                        const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
-                        const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                        mma_bf16(dS_col + 64, sdesc_sw128(do_s + st * kTileBytes + ao, 16, kRgStride),
-                                 sdesc_sw128(v_s + bo, 16, 1024), idS, kk > 0);
-                    }
-                    mma_commit(&bars[B_DPFULL0 + st]);
-                    if (sT + 1 == sN) {
-                        mma_commit(&bars[B_KVEMPTY]);
-                        sU = unit_of(++sUc, n_units);
-                        sT = 0;
-                        sN = sU >= 0 ? ntiles_of(sU) : -1;
-                    } else {
-                        ++sT;
-                    }
-                    ++sIt;
-                    progressed = true;
-                }
-                if (progressed) {
-                    t_last = globaltimer();
-                } else if (globaltimer() - t_last > kWaitLimitNs) {
-                    *abort_flag = 1;
                 }
             }
             // every MMA issued must finish before TMEM is released
-            mma_commit(&bars[B_DONE]);
+            mma_commit(&bars[B_DONE0 + role]);
             volatile int never = 0;
-            mbar_wait(&bars[B_DONE], 0, &never);
+            mbar_wait(&bars[B_DONE0 + role], 0, &never);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------- softmax / epilogue
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // tile row = TMEM lane
@@ -563,10 +545,10 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
         grid = 1;
     if (gather_tma) {
         cudaFuncSetAttribute(dkdv_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        dkdv_tc_kernel<true><<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+        dkdv_tc_kernel<true><<<grid, 352, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
     } else {
         cudaFuncSetAttribute(dkdv_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        dkdv_tc_kernel<false><<<grid, 256, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+        dkdv_tc_kernel<false><<<grid, 352, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
     }
     return cudaGetLastError();
 }
