@@ -155,6 +155,12 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // registers: the role warps (warpgroup 0) need few, the softmax warps many
+    // (launch: 384 x 168 = 64512; after: 128 x 96 + 256 x 200 = 63488)
+    if (warp < 4)
+        setmaxnreg_dec<96>();
+    else
+        setmaxnreg_inc<200>();
 
     if (warp == 0) {
         // ------------------------------------------------------------- TMA
