@@ -28,11 +28,12 @@
 // the current tile; S (with P) is double-buffered in TMEM and the K and V
 // rings carry across tiles.
 //
-// Roles (12 warps): warp 1 deals the tiles and builds their block unions;
-// warp 0 issues the TMA copies (each tile's Q, then per pair its K boxes and
-// its V boxes, one box per lane); warp 2 owns TMEM and one thread issues S,
-// one thread of warp 3 the P.V products; warps 4-7 and 8-11 are softmax
-// warpgroups 0 and 1, one row per thread, and split the epilogue's columns.
+// Roles (12 warps): warp 0 deals the tiles, builds each tile's block union
+// and issues the TMA copies (the tile's Q, then per pair its K boxes and its
+// V boxes, one box per lane); one thread of warp 2 (which owns TMEM) issues
+// S, one thread each of warps 1 and 3 the P.V products of blocks 0 and 1;
+// warps 4-7 and 8-11 are softmax warpgroups 0 and 1, one row per thread,
+// and split the epilogue's columns.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -48,19 +49,19 @@ constexpr int OFF_K = OFF_Q + kTileBytes;
 constexpr int OFF_V = OFF_K + NK * kTileBytes;
 constexpr int OFF_UNION = OFF_V + NV * kTileBytes;  // union buffers, sized at launch
 constexpr int kXchgBytes = 2 * 2 * kRows * 8;       // row (m, l) of both warpgroups, two tiles
-constexpr int NUM_BARS = 32;
+constexpr int NUM_BARS = 40;
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
 enum {
-    B_QFULL = 0, B_QEMPTY, B_ACCFULL, B_ACCEMPTY, B_DONE, B_DONES,
-    B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PF0, B_PF1, B_PVFULL0, B_PVFULL1,
+    B_QFULL = 0, B_QEMPTY, B_ACCFULL, B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1,
+    B_PF00, B_PF01, B_PF10, B_PF11, B_PVFULL00, B_PVFULL01, B_PVFULL10, B_PVFULL11,  // [warpgroup][buffer]
     B_UFULL0, B_UFULL1, B_UEMPTY0, B_UEMPTY1, B_XCHG0, B_XCHG1,
     B_KF0, B_KE0 = B_KF0 + NK, B_VF0 = B_KE0 + NK, B_VE0 = B_VF0 + NV, B_COUNT = B_VE0 + NV
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
-// threads releasing a tile's union: the loader warp, the two MMA threads and
-// the 256 softmax threads
-constexpr int kUnionUsers = 32 + 2 + 2 * kRows;
+// threads releasing a tile's union: the loader warp, the three MMA threads
+// and the 256 softmax threads
+constexpr int kUnionUsers = 32 + 3 + 2 * kRows;
 
 constexpr uint32_t TM_S = 0;    // S buffer x at x*128 (the pair's 128 keys); P_e over its columns e*64 .. +31
 constexpr uint32_t TM_O = 256;  // O_e at 256 + e*128: 128 lanes (rows) x 128 columns (dims)
@@ -108,15 +109,17 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
         *abort_flag = 0;
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QEMPTY], 1);
-        mbar_init(&bars[B_ACCFULL], 1);
+        mbar_init(&bars[B_ACCFULL], 2);
         mbar_init(&bars[B_ACCEMPTY], 2 * kRows);
-        mbar_init(&bars[B_DONE], 1);
-        mbar_init(&bars[B_DONES], 1);
+        for (int x = 0; x < 3; ++x)
+            mbar_init(&bars[B_DONE0 + x], 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&bars[B_SFULL0 + x], 1);
-            mbar_init(&bars[B_SFREE0 + x], 1);
-            mbar_init(&bars[B_PF0 + x], 2 * kRows);
-            mbar_init(&bars[B_PVFULL0 + x], 1);
+            mbar_init(&bars[B_SFREE0 + x], 2);
+            mbar_init(&bars[B_PF00 + x], kRows);
+            mbar_init(&bars[B_PF10 + x], kRows);
+            mbar_init(&bars[B_PVFULL00 + x], 1);
+            mbar_init(&bars[B_PVFULL10 + x], 1);
             mbar_init(&bars[B_UFULL0 + x], 32);
             mbar_init(&bars[B_UEMPTY0 + x], kUnionUsers);
             mbar_init(&bars[B_XCHG0 + x], 2 * kRows);
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(&bars[B_VF0 + s], 1);
-            mbar_init(&bars[B_VE0 + s], 1);
+            mbar_init(&bars[B_VE0 + s], 2);
         }
         fence_barrier_init();
     }
@@ -162,15 +165,27 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int lastq = -1, last = -1, lastv = -1, gi = 0;
+        int lastq = -1, last = -1, lastv = -1, gi = 0, r = 0;
         for (int k = 0;; ++k) {
-            if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+            // The tile and its block union: this warp deals the tiles and builds
+            // each union after issuing the previous tile's copies, while the
+            // K/V rings still hold several of that tile's pairs; after the last
+            // tile a header with a negative count tells the other roles to stop.
+            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
+            if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
-            const volatile int *hdr = u_hdr(k);
-            const int U = hdr[UH_COUNT];
-            if (U < 0)
+            if (more) {
+                qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
+            } else {
+                if (lane == 0)
+                    u_hdr(k)[UH_COUNT] = -1;
+                __syncwarp();
+            }
+            mbar_arrive(&bars[B_UFULL0 + k % nub]);
+            if (!more)
                 break;
-            const int b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0];
+            const int U = u_hdr(k)[UH_COUNT];
             const int *list = union_list(u_buf(k), up);
             // the tile's Q, once the previous tile's last S has run
             if (!mbar_wait_warp(&bars[B_QEMPTY], (k & 1) ^ 1, abort_flag))
@@ -235,51 +250,31 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                 mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, &never);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ union
-        // Deals the tiles and builds each one's block union a tile ahead of
-        // its use; after the last tile a header with a negative count tells
-        // the other roles to stop.
-        int r = 0;
-        for (int k = 0;; ++k) {
-            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
-            if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
-                break;
-            if (more) {
-                qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
-            } else {
-                if (lane == 0)
-                    u_hdr(k)[UH_COUNT] = -1;
-                __syncwarp();
-            }
-            mbar_arrive(&bars[B_UFULL0 + k % nub]);
-            if (!more)
-                break;
-        }
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp <= 3) {
         // ---------------------------------------------------------------- MMA
-        // Two issuing threads: warp 2 issues S of each pair (whose completion
-        // frees its K stage), warp 3 the P.V products (whose completion frees
-        // the V stage and the S buffer holding P), so a ready P.V never
-        // queues behind the next pair's S issue.  Each commit covers its own
-        // thread's MMAs.
+        // Three issuing threads in three warps (one thread issues a tcgen05 MMA
+        // only every ~150 cycles): warp 2 issues S of each pair (whose
+        // completion frees its K stage), warps 1 and 3 the P.V products of
+        // blocks 0 and 1 (O_0 and O_1; both completions free the V stage and
+        // the S buffer holding P), so a ready product never queues behind
+        // another's issue.  Each commit covers its own thread's MMAs.
         if (lane == 0) {
+            const int e = warp == 3 ? 1 : 0;  // the P.V threads' block
+            const uint32_t idS = idesc_bf16(128, 128, false, false), idO = idesc_bf16(128, 128, false, true);
+            const uint32_t q_s = smem_u32(sm + OFF_Q);
+            // Q tile: 64-column halves and 8-row groups apart by these
+            const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
             int gi = 0;
             bool ok = true;
-            if (warp == 2) {
-                const uint32_t idS = idesc_bf16(128, 128, false, false);
-                const uint32_t q_s = smem_u32(sm + OFF_Q);
-                // Q tile: 64-column halves and 8-row groups apart by these
-                const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
-                for (int k = 0; ok; ++k) {
-                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
-                        break;
-                    const int U = u_hdr(k)[UH_COUNT];
-                    if (U < 0)
-                        break;
-                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
-                    const int npairs = (U + 1) >> 1;
+            for (int k = 0; ok; ++k) {
+                if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+                    break;
+                const int U = u_hdr(k)[UH_COUNT];
+                if (U < 0)
+                    break;
+                mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
+                const int npairs = (U + 1) >> 1;
+                if (warp == 2) {
                     if (!mbar_wait(&bars[B_QFULL], k & 1, abort_flag))
                         break;
                     for (int i = 0; i < npairs; ++i, ++gi) {
@@ -300,32 +295,18 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                         }
                         mma_commit(&bars[B_SFULL0 + (gi & 1)]);
                         mma_commit(&bars[B_KE0 + gi % NK]);
-                        if (i == npairs - 1)
-                            mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
                     }
-                    if (ok && npairs == 0)
-                        mma_commit(&bars[B_QEMPTY]);
-                }
-                mma_commit(&bars[B_DONES]);
-                volatile int never = 0;
-                mbar_wait(&bars[B_DONES], 0, &never);
-            } else {
-                const uint32_t idO = idesc_bf16(128, 128, false, true);
-                for (int k = 0; ok; ++k) {
-                    if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
+                    if (!ok)
                         break;
-                    const int U = u_hdr(k)[UH_COUNT];
-                    if (U < 0)
-                        break;
-                    mbar_arrive(&bars[B_UEMPTY0 + k % nub]);
-                    const int npairs = (U + 1) >> 1;
-                    // the epilogue has read the previous tile's O
+                    mma_commit(&bars[B_QEMPTY]);  // the next tile's Q may land
+                } else {
+                    // the epilogue has read the previous tile's O_e
                     if (!mbar_wait(&bars[B_ACCEMPTY], (k & 1) ^ 1, abort_flag))
                         break;
                     tc_fence_after();
                     for (int i = 0; i < npairs; ++i, ++gi) {
                         const int sb = gi & 1, sv = gi % NV;
-                        if (!mbar_wait(&bars[B_PF0 + sb], (gi >> 1) & 1, abort_flag) ||
+                        if (!mbar_wait(&bars[B_PF00 + e * 2 + sb], (gi >> 1) & 1, abort_flag) ||
                             !mbar_wait(&bars[B_VF0 + sv], (gi / NV) & 1, abort_flag)) {
                             ok = false;
                             break;
@@ -333,12 +314,11 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                         tc_fence_after();
                         const uint32_t v_s = smem_u32(sm + OFF_V) + sv * kTileBytes;
                         // O_e += P_e V_e: 64 keys, P from TMEM x the block's V (MN-major)
-                        for (int e = 0; e < 2; ++e)
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ts(tmem + TM_O + e * 128, tmem + TM_S + sb * 128 + e * 64 + kk * 8,
-                                            sdesc_sw128(v_s + (e * 4 + kk) * 2048, kHalfBytes, 1024), idO,
-                                            (i > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bars[B_PVFULL0 + sb]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ts(tmem + TM_O + e * 128, tmem + TM_S + sb * 128 + e * 64 + kk * 8,
+                                        sdesc_sw128(v_s + (e * 4 + kk) * 2048, kHalfBytes, 1024), idO,
+                                        (i > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bars[B_PVFULL00 + e * 2 + sb]);
                         mma_commit(&bars[B_VE0 + sv]);
                         mma_commit(&bars[B_SFREE0 + sb]);
                     }
@@ -346,10 +326,12 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                         break;
                     mma_commit(&bars[B_ACCFULL]);
                 }
-                mma_commit(&bars[B_DONE]);
-                volatile int never = 0;
-                mbar_wait(&bars[B_DONE], 0, &never);
             }
+            // every MMA of this thread completes before TMEM is freed
+            uint64_t *done = &bars[B_DONE0 + warp - 1];
+            mma_commit(done);
+            volatile int never = 0;
+            mbar_wait(done, 0, &never);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -429,7 +411,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                         const float alpha = raise ? ex2(m - mb) : 1.f;  // 0 when m = -inf
                         if (i > 0) {
                             // O_e must hold every earlier pair of the tile before it is rescaled
-                            if (!mbar_wait_warp(&bars[B_PVFULL0 + ((gi - 1) & 1)], ((gi - 1) >> 1) & 1,
+                            if (!mbar_wait_warp(&bars[B_PVFULL00 + e * 2 + ((gi - 1) & 1)], ((gi - 1) >> 1) & 1,
                                                 abort_flag)) {
                                 ok = false;
                                 break;
@@ -489,7 +471,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                 tmem_st32(lane_base + TM_S + sb * 128 + e * 64, pk);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars[B_PF0 + sb]);
+                mbar_arrive(&bars[B_PF00 + e * 2 + sb]);
             }
             if (!ok)
                 break;
