@@ -387,26 +387,34 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         int tl, hh;
         qtile_row(g, Tq, r, tl, hh);
         int gi = 0;
-        for (int k = 0;; ++k) {
+        // A tile's header and this row's LSE / delta, fetched while the
+        // previous tile's dQ products complete (the first tile's here); the
+        // header stays in the union buffer until the tile releases it.
+        int nU = -1;
+        float nl2 = 0.f, ndl = 0.f;
+        auto fetch = [&](int k) {
+            nU = -1;
             if (!mbar_wait_warp(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
-                break;
+                return;
             const volatile int *hdr = u_hdr(k);
-            const int U = hdr[UH_COUNT];
-            if (U < 0)
-                break;
-            const int b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0], nvalid = hdr[UH_NVALID];
+            nU = hdr[UH_COUNT];
+            if (nU >= 0 && r < nrows && tl < hdr[UH_NVALID]) {
+                const int64_t so = stat_off(g, hdr[UH_B], hdr[UH_KVH] * G + hh, hdr[UH_T0] + tl);
+                nl2 = p.lse[so] * 1.4426950408889634f;
+                ndl = p.delta[so];
+            }
+        };
+        fetch(0);
+        for (int k = 0; nU >= 0; ++k) {
+            const volatile int *hdr = u_hdr(k);
+            const int U = nU, b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0], nvalid = hdr[UH_NVALID];
+            const float l2 = nl2, dl = ndl;
             const int *list = union_list(u_buf(k), up);
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
             const int t = t0 + tl;
-            float l2 = 0.f, dl = 0.f;
-            __nv_bfloat16 *dst = nullptr;  // the row's dQ columns e*64 .. e*64+63
-            if (rvalid) {
-                const int64_t so = stat_off(g, b, kvh * G + hh, t);
-                l2 = p.lse[so] * 1.4426950408889634f;
-                dl = p.delta[so];
-                dst = p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64;
-            }
+            // the row's dQ columns e*64 .. e*64+63
+            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64 : nullptr;
             const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
             bool ok = true;
             for (int i = 0; i < npairs; ++i, ++gi) {
@@ -484,6 +492,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!ok)
                 break;
             mbar_arrive(&bars[B_UEMPTY0 + k % nub]);  // the union buffer may be rebuilt
+            fetch(k + 1);
             // epilogue: dQ row r, columns e*64 .. e*64+63 = scale * TMEM.  Every
             // lane of the warp runs the TMEM loads (.sync.aligned); only valid
             // rows store.
