@@ -39,7 +39,7 @@ constexpr int OFF_LSE = OFF_DS + kRows * 128;    // float [2][128], LSE * log2(e
 constexpr int OFF_DLT = OFF_LSE + 2 * kRows * 4; // float [2][128]
 constexpr int OFF_TOK = OFF_DLT + 2 * kRows * 4; // int   [2][128]
 constexpr int OFF_BAR = OFF_TOK + 2 * kRows * 4;
-constexpr int NUM_BARS = 24;
+constexpr int NUM_BARS = 28;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
@@ -47,7 +47,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 enum {
     B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
     B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_IDX0, B_IDX1, B_DPFULL0, B_DPFULL1,
-    B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_COUNT
+    B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 
@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         mbar_init(&bars[B_SFREE0], kRows);
         mbar_init(&bars[B_SFREE1], kRows);
         mbar_init(&bars[B_PFULL], kRows);
-        mbar_init(&bars[B_PFREE], 2);
+        mbar_init(&bars[B_PFREE], 1);
+        mbar_init(&bars[B_DSFULL], kRows);
+        mbar_init(&bars[B_DSFREE], 1);
         mbar_init(&bars[B_ACCFULL], 2);
         mbar_init(&bars[B_ACCEMPTY], kRows);
         for (int x = 0; x < 4; ++x)
@@ -309,10 +311,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     } else if (warp == 2 || warp >= 8) {
         // -------------------------------------------------------------- MMA
         // Four issuing threads in four warps (one thread issues a tcgen05 MMA
-        // only every ~150 cycles): warp 2 issues S, warp 8 dP, warp 9 dV^T and
-        // warp 10 dK^T; each walks every (unit, tile).  Barriers shared by two
-        // of them count two commits: KVEMPTY (S and dP), EMPTY, PFREE and
-        // ACCFULL (dV and dK).
+        // only every ~150 cycles): warp 2 issues S, warp 8 dP, warp 9 dV^T (as
+        // soon as P is in shared memory) and warp 10 dK^T (once dS is); each
+        // walks every (unit, tile).  Barriers shared by two of them count two
+        // commits: KVEMPTY (S and dP), EMPTY and ACCFULL (dV and dK).
         if (lane == 0) {
             const int role = warp == 2 ? 0 : warp - 7;  // 0 S, 1 dP, 2 dV, 3 dK
             const uint32_t idS = idesc_bf16(128, 64, false, false);
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     } else {
                         // P (dV) or dS (dK) of the tile is in shared memory; at a
                         // unit's start the epilogue has read the accumulators
-                        if (!mbar_wait(&bars[B_PFULL], it & 1, abort_flag) ||
+                        if (!mbar_wait(&bars[role == 2 ? B_PFULL : B_DSFULL], it & 1, abort_flag) ||
                             (ti == 0 && !mbar_wait(&bars[B_ACCEMPTY], (uc & 1) ^ 1, abort_flag))) {
                             ok = false;
                             break;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             // 16 rows = two row groups; LBO steps the 64-dim halves (M)
                             mma_bf16(col, sdesc_sw128(a_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
                                      sdesc_sw128(pb + kr * 2048, 8192, 1024), idV, (ti > 0 || kr > 0) ? 1u : 0u);
-                        mma_commit(&bars[B_PFREE]);
+                        mma_commit(&bars[role == 2 ? B_PFREE : B_DSFREE]);
                         mma_commit(&bars[B_EMPTY0 + st]);
                         if (ti + 1 == ntiles)
                             mma_commit(&bars[B_ACCFULL]);
@@ -428,6 +430,21 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         pv[c] = __float_as_uint((c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
                                                                       : 0.f);
                 }
+                // P (bf16) to shared memory as soon as the dV product of the
+                // previous tile has read it: dV^T += dO^T P starts while dS forms
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2)
+                    pk[c >> 1] = pack_bf16(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
+                if (!mbar_wait_warp(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_async_smem();
+                mbar_arrive(&bars[B_PFULL]);
                 // dS = P (dP - delta)
                 if (!mbar_wait_warp(&bars[B_DPFULL0 + st], (it >> 1) & 1, abort_flag)) {
                     ok = false;
@@ -439,28 +456,25 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE0 + st]);
-                uint32_t pk[32], dk_[32];
+                uint32_t dk_[32];
                 const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     float d0, d1;
                     const uint64_t pp = f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
                     f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)), d0, d1);
-                    pk[c >> 1] = pack_bf16(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
                     dk_[c >> 1] = pack_bf16(d0, d1);
                 }
-                if (!mbar_wait_warp(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_DSFREE], (it & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t o = ((c ^ (r & 7)) << 4);
-                    st_shared_v4(p_row + o, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    st_shared_v4(ds_row + o, dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
-                }
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
+                                 dk_[4 * c + 3]);
                 fence_async_smem();
-                mbar_arrive(&bars[B_PFULL]);
+                mbar_arrive(&bars[B_DSFULL]);
             }
             if (!ok)
                 break;
