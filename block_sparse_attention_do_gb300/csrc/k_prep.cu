@@ -86,6 +86,8 @@ __device__ __forceinline__ int dense_count(const Geo &g, int L, int j)
     return j * g.bs < end ? end - j * g.bs : 0;
 }
 
+// slot s of an index row: 0 use it, 1 padding (-1), 2 out of range or in the
+// future, 3 a repeat of an earlier slot
 __device__ __forceinline__ int classify(const int *row, int s, int t, int bs, int nbmax)
 {
     const int j = row[s];
@@ -99,6 +101,39 @@ __device__ __forceinline__ int classify(const int *row, int s, int t, int bs, in
     return 0;
 }
 
+// The slots of one index row that name a block to use (bit s set), each
+// block once; `bad` reports a slot that is out of range, in the future or a
+// repeat of an earlier slot (-1 is padding).  The row is read into registers
+// once (S <= 32).
+__device__ __forceinline__ unsigned row_slots(const int *row, int S, int t, int bs, int nbmax, bool &bad)
+{
+    int v[32];
+#pragma unroll
+    for (int s = 0; s < 32; ++s)
+        v[s] = s < S ? row[s] : -1;
+    const int jmax = min(t / bs, nbmax - 1);
+    unsigned m = 0u;
+    bool b = false;
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+        if (s >= S)
+            break;
+        const int j = v[s];
+        if (j == -1)
+            continue;
+        bool dup = false;
+#pragma unroll
+        for (int s2 = 0; s2 < s; ++s2)
+            dup |= v[s2] == j;
+        if (j < 0 || j > jmax || dup)
+            b = true;
+        else
+            m |= 1u << s;
+    }
+    bad = b;
+    return m;
+}
+
 __global__ void __launch_bounds__(kThreads) validate_kernel(Geo g, const int *__restrict__ idx,
                                                             int *err)
 {
@@ -108,9 +143,14 @@ __global__ void __launch_bounds__(kThreads) validate_kernel(Geo g, const int *__
         int b, kvh, t;
         decode_idx_row(g, lin, b, kvh, t);
         const int *row = idx_row(g, idx, b, kvh, t);
-        for (int s = 0; s < g.S; ++s)
-            if (classify(row, s, t, g.bs, g.nbmax) >= 2)
-                set_error(err, NSA_ERR_BAD_INDEX);
+        bool bad = false;
+        if (g.S <= 32)
+            row_slots(row, g.S, t, g.bs, g.nbmax, bad);
+        else
+            for (int s = 0; s < g.S; ++s)
+                bad |= classify(row, s, t, g.bs, g.nbmax) >= 2;
+        if (bad)
+            set_error(err, NSA_ERR_BAD_INDEX);
     }
 }
 
@@ -123,13 +163,21 @@ __global__ void __launch_bounds__(kThreads) csr_count_kernel(Geo g, const int *_
         int b, kvh, t;
         decode_idx_row(g, lin, b, kvh, t);
         const int *row = idx_row(g, idx, b, kvh, t);
-        for (int s = 0; s < g.S; ++s) {
-            const int c = classify(row, s, t, g.bs, g.nbmax);
-            if (c == 0)
-                atomicAdd(&counts[((int64_t)b * g.Hkv + kvh) * g.nbmax + row[s]], 1);
-            else if (c >= 2)
-                set_error(err, NSA_ERR_BAD_INDEX);
+        int *cnt = counts + ((int64_t)b * g.Hkv + kvh) * g.nbmax;
+        bool bad = false;
+        if (g.S <= 32) {
+            for (unsigned m = row_slots(row, g.S, t, g.bs, g.nbmax, bad); m; m &= m - 1u)
+                atomicAdd(&cnt[row[__ffs(m) - 1]], 1);
+        } else {
+            for (int s = 0; s < g.S; ++s) {
+                const int c = classify(row, s, t, g.bs, g.nbmax);
+                if (c == 0)
+                    atomicAdd(&cnt[row[s]], 1);
+                bad |= c >= 2;
+            }
         }
+        if (bad)
+            set_error(err, NSA_ERR_BAD_INDEX);
     }
 }
 
@@ -415,12 +463,16 @@ __global__ void __launch_bounds__(kThreads) count_pairs_kernel(Geo g, const int 
         int b, kvh, t;
         decode_idx_row(g, lin, b, kvh, t);
         const int *row = idx_row(g, idx, b, kvh, t);
-        for (int s = 0; s < g.S; ++s)
-            if (classify(row, s, t, g.bs, g.nbmax) == 0) {
-                const int j = row[s];
-                const int hi = min((j + 1) * g.bs - 1, t);
-                local += (unsigned long long)g.G * (hi - j * g.bs + 1);
-            }
+        auto add = [&](int j) { local += (unsigned long long)g.G * (min((j + 1) * g.bs - 1, t) - j * g.bs + 1); };
+        if (g.S <= 32) {
+            bool bad;
+            for (unsigned m = row_slots(row, g.S, t, g.bs, g.nbmax, bad); m; m &= m - 1u)
+                add(row[__ffs(m) - 1]);
+        } else {
+            for (int s = 0; s < g.S; ++s)
+                if (classify(row, s, t, g.bs, g.nbmax) == 0)
+                    add(row[s]);
+        }
     }
     for (int off = 16; off > 0; off >>= 1)
         local += __shfl_xor_sync(0xffffffffu, local, off);
@@ -440,14 +492,10 @@ constexpr int kFillWarps = 4;
 // valid slots of a row, each block counted once (bit s set = use slot s)
 __device__ __forceinline__ unsigned valid_slots(const int *row, int S, int t, int bs, int nbmax, int *err)
 {
-    unsigned m = 0u;
-    for (int s = 0; s < S; ++s) {
-        const int c = classify(row, s, t, bs, nbmax);
-        if (c == 0)
-            m |= 1u << s;
-        else if (c >= 2)
-            set_error(err, NSA_ERR_BAD_INDEX);
-    }
+    bool bad;
+    const unsigned m = row_slots(row, S, t, bs, nbmax, bad);
+    if (bad && err)
+        set_error(err, NSA_ERR_BAD_INDEX);
     return m;
 }
 

@@ -86,6 +86,7 @@ SMALL = [
     (1, 48, 2, 260, 128, 64, 5),  # G=24: 5 tokens, 120 of 128 rows used
     (1, 64, 1, 130, 128, 64, 3),  # G=64: 2 tokens a tile
     (1, 128, 1, 70, 128, 64, 2),  # G=128: one token a tile
+    (1, 4, 1, 1100, 64, 16, 40),  # S above 32: the per-slot index checks
 ]
 
 
@@ -225,8 +226,9 @@ def test_do_dot():
     assert np.max(np.abs(got - ref)) < 1e-3
 
 
-def test_bad_index_is_reported():
-    B, Hq, Hkv, T, D, bs, S = 1, 2, 1, 128, 64, 32, 3
+@pytest.mark.parametrize("S", [3, 40])
+def test_bad_index_is_reported(S):
+    B, Hq, Hkv, T, D, bs = 1, 2, 1, 128, 64, 32
     q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16)
     idx = inputs.make_block_idx(B, Hkv, T, bs, S)
     cases = []
