@@ -14,8 +14,8 @@
 // token's own blocks.  Pairing keeps every MMA at N = 128: a tcgen05 MMA with
 // M = 128 costs about the same for N = 64 as for N = 128.
 //
-// The kernel is persistent: one CTA per SM walks its share of the tiles,
-// heaviest (latest tokens) first, dealt to the CTAs in a snake.  The next
+// The kernel is persistent: one CTA per SM takes tiles from a launch-wide
+// counter, heaviest (latest tokens) first.  The next
 // tile's block union, its Q/dO load and its first K/V pairs overlap the
 // current tile's last pairs and epilogue: the union sits in one of two
 // shared-memory buffers (one when two do not fit).
@@ -70,7 +70,8 @@ struct Params {
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     int *err;
-    int ntiles;  // query tiles over all (b, kv head)
+    int ntiles;      // query tiles over all (b, kv head)
+    int *tile_next;  // work counter, zero at launch
     int nub;     // union buffers (1 or 2)
     int nk;      // K pair stages (2 or 3)
 };
@@ -172,14 +173,14 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0, r = 0;
+        int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0;
         for (int k = 0;; ++k) {
             // The tile and its block union: this warp deals the tiles and builds
             // each union after issuing the previous tile's copies, while the
             // K/V rings still hold several of that tile's pairs; after the last
             // tile a header with a negative count tells the other roles to stop.
             int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
+            const bool more = qtile_next(g, p.ntiles, p.tile_next, lane, b, kvh, t0, nvalid);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
             if (more) {
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
 
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
                          const float *lse, const float *delta, const int *idx, void *dq, int *err,
-                         cudaStream_t st)
+                         int *tile_next, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
@@ -568,6 +569,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
     p.nk = nk;
+    p.tile_next = tile_next;
     int grid = num_sms();
     if (grid > p.ntiles)
         grid = p.ntiles;

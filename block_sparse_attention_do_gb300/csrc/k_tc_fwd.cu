@@ -23,8 +23,8 @@
 // pair's K is free as soon as S is computed, and K and V have rings of their
 // own: K is held only from its load to S, V from its load to P.V.
 //
-// The kernel is persistent like the dQ kernel: one CTA per SM, tiles dealt
-// heaviest first in a snake, the next tile's union and Q load overlapping
+// The kernel is persistent like the dQ kernel: one CTA per SM, tiles taken
+// heaviest first from a launch-wide counter, the next tile's union and Q load overlapping
 // the current tile; S (with P) is double-buffered in TMEM and the K and V
 // rings carry across tiles.
 //
@@ -74,7 +74,8 @@ struct Params {
     __nv_bfloat16 *o;
     float *lse;
     int *err;
-    int ntiles;  // query tiles over all (b, kv head)
+    int ntiles;      // query tiles over all (b, kv head)
+    int *tile_next;  // work counter, zero at launch
     int nub;     // union buffers (1 or 2)
 };
 
@@ -165,14 +166,14 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int lastq = -1, last = -1, lastv = -1, gi = 0, r = 0;
+        int lastq = -1, last = -1, lastv = -1, gi = 0;
         for (int k = 0;; ++k) {
             // The tile and its block union: this warp deals the tiles and builds
             // each union after issuing the previous tile's copies, while the
             // K/V rings still hold several of that tile's pairs; after the last
             // tile a header with a negative count tells the other roles to stop.
             int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, r, b, kvh, t0, nvalid);
+            const bool more = qtile_next(g, p.ntiles, p.tile_next, lane, b, kvh, t0, nvalid);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
             if (more) {
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
-                          void *o, float *lse, int *err, cudaStream_t st)
+                          void *o, float *lse, int *err, int *tile_next, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
@@ -556,6 +557,7 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     p.err = err;
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
+    p.tile_next = tile_next;
     int grid = num_sms();
     if (grid > p.ntiles)
         grid = p.ntiles;

@@ -110,9 +110,10 @@ struct Unit {
 
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
-    int err;      // nsa_status recorded by the device
-    int n_units;  // number of dK/dV units built for the current call
-    int pad[62];
+    int err;        // nsa_status recorded by the device
+    int n_units;    // number of dK/dV units built for the current call
+    int tile_next;  // the query-tile kernels' work counter (zeroed with the header)
+    int pad[61];
 };
 
 }  // namespace nsa

@@ -77,9 +77,9 @@ __device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, 
     }
 }
 
-// ---- persistent query-tile kernels: tiles are dealt to the CTAs in a snake,
-// heaviest (latest tokens) first, and one warp per CTA builds each tile's
-// block union a tile ahead of its use into one of (up to) two buffers.
+// ---- persistent query-tile kernels: tiles are taken from a launch-wide
+// counter, heaviest (latest tokens) first, and one warp per CTA builds each
+// tile's block union a tile ahead of its use into one of (up to) two buffers.
 
 // A union buffer: UH_INTS header ints (the tile's coordinates and the list
 // length; a negative length ends the walk), the per-token block bitmaps, the
@@ -104,27 +104,30 @@ __device__ __forceinline__ int *union_list(int *buf, const UnionBuf &u)
     return buf + UH_INTS + u.mask_words + u.ubits_words;
 }
 
-// The CTA's next tile, cursor r (start at 0): tile numbers L = r * grid +
-// (c or grid-1-c, alternating), tile L covering (b, kv head) = L % (B*Hkv)
-// and the (L / (B*Hkv))-th tile from the end of the sequence; tiles past a
-// sequence's end are skipped.  False once L passes the tile count.
-__device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int &r, int &b, int &kvh, int &t0,
-                                           int &nvalid)
+// The next tile for the calling warp's CTA from the launch-wide counter
+// *next (zero at launch): tile L covers (b, kv head) = L % (B*Hkv) and is the
+// (L / (B*Hkv))-th from the end of the sequence, so the heaviest tiles (the
+// latest tokens) go first and a CTA that finishes early takes more.  Tiles
+// past a sequence's end are skipped.  False once the counter passes the tile
+// count.  Called by all lanes of one warp.
+__device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int *next, int lane, int &b, int &kvh,
+                                           int &t0, int &nvalid)
 {
-    const int Gc = gridDim.x, c = blockIdx.x;
     const int Tq = tile_tokens(g.G), per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
-    for (;; ++r) {
-        const int64_t L = (int64_t)r * Gc + ((r & 1) ? Gc - 1 - c : c);
+    for (;;) {
+        int L = 0;
+        if (lane == 0)
+            L = atomicAdd(next, 1);
+        L = __shfl_sync(0xffffffffu, L, 0);
         if (L >= ntiles)
             return false;
-        const int bg = (int)(L % nbg), tile = per_seq - 1 - (int)(L / nbg);
+        const int bg = L % nbg, tile = per_seq - 1 - L / nbg;
         b = bg / g.Hkv;
         kvh = bg % g.Hkv;
         t0 = tile * Tq;
         const int len = seq_len(g, b);
         if (t0 < len) {
             nvalid = min(Tq, len - t0);
-            ++r;
             return true;
         }
     }
