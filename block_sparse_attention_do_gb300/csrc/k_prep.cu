@@ -27,18 +27,17 @@ inline int grid_for(int64_t n, int per_block, int cap = 152 * 32)
 // ---------------------------------------------------------------- do_dot
 // Rows are contiguous D-vectors in both layouts, and delta uses the row order
 // of o, so the kernel is a plain segmented dot product over rows.
+// blocks blk of nblk (grid-stride)
 template <typename T>
-__global__ void __launch_bounds__(kThreads) do_dot_kernel(const T *__restrict__ o,
-                                                          const T *__restrict__ dO,
-                                                          float *__restrict__ out, int64_t nrows,
-                                                          int D)
+__device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__restrict__ dO, float *__restrict__ out,
+                                            int64_t nrows, int D, int blk, int nblk)
 {
     constexpr int VEC = 16 / sizeof(T);
     const int tpr = D / VEC;  // threads per row (power of two, <= 32)
     const int lane = threadIdx.x & 31;
     const int sub = lane / tpr, part = lane % tpr, rpw = 32 / tpr;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t warp = ((int64_t)blk * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)nblk * blockDim.x) >> 5;
     for (int64_t r0 = warp * rpw; r0 < nrows; r0 += nwarps * rpw) {
         const int64_t r = r0 + sub;
         float acc = 0.f;
@@ -56,6 +55,13 @@ __global__ void __launch_bounds__(kThreads) do_dot_kernel(const T *__restrict__ 
         if (r < nrows && part == 0)
             out[r] = acc;
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) do_dot_kernel(const T *__restrict__ o, const T *__restrict__ dO,
+                                                          float *__restrict__ out, int64_t nrows, int D)
+{
+    do_dot_body<T>(o, dO, out, nrows, D, blockIdx.x, gridDim.x);
 }
 
 // decode a linear index-row number into (b, kvh, t)
@@ -499,13 +505,11 @@ __device__ __forceinline__ unsigned valid_slots(const int *row, int S, int t, in
     return m;
 }
 
-__global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const int *__restrict__ idx,
-                                                                   int *__restrict__ chunk_counts, int nchunks,
-                                                                   int *err)
+__device__ __forceinline__ void chunk_count_body(const Geo &g, const int *__restrict__ idx, int *__restrict__ chunk_counts,
+                                                 int nchunks, int *err, int blk, int nblk)
 {
     const int64_t n = (int64_t)g.ntok * g.Hkv;
-    for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
-         lin += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t lin = (int64_t)blk * blockDim.x + threadIdx.x; lin < n; lin += (int64_t)nblk * blockDim.x) {
         int b, kvh, t;
         decode_idx_row(g, lin, b, kvh, t);
         const int *row = idx_row(g, idx, b, kvh, t);
@@ -517,6 +521,29 @@ __global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const 
             atomicAdd(&chunk_counts[(base + row[s]) * nchunks + t / kChunkTok], 1);
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const int *__restrict__ idx,
+                                                                   int *__restrict__ chunk_counts, int nchunks,
+                                                                   int *err)
+{
+    chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, gridDim.x);
+}
+
+// The chunk count and delta = rowsum(dO * O) in one launch: they are
+// independent, the first latency-bound and the second bandwidth-bound, so
+// the count's blocks (the first count_blocks) run under the dot's.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const int *__restrict__ idx,
+                                                                   int *__restrict__ chunk_counts, int nchunks,
+                                                                   int *err, int count_blocks, const T *__restrict__ o,
+                                                                   const T *__restrict__ dO, float *__restrict__ out,
+                                                                   int64_t nrows)
+{
+    if ((int)blockIdx.x < count_blocks)
+        chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, count_blocks);
+    else
+        do_dot_body<T>(o, dO, out, nrows, g.D, blockIdx.x - count_blocks, gridDim.x - count_blocks);
 }
 
 // one warp per (bg, j): exclusive prefix over chunks, list length in counts
@@ -633,7 +660,7 @@ bool csr_chunked_ok(const Geo &g)
 }
 
 cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_counts, int *counts, int *err,
-                                   cudaStream_t st)
+                                   cudaStream_t st, const DotArgs *dot)
 {
     const int nchunks = csr_nchunks(g);
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
@@ -641,7 +668,23 @@ cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_coun
     if (e != cudaSuccess)
         return e;
     const int64_t n = (int64_t)g.ntok * g.Hkv;
-    csr_chunk_count_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err);
+    const int cblocks = grid_for(n, kThreads);
+    if (dot) {
+        const int64_t nrows = (int64_t)g.ntok * g.Hq;
+        const int elems = dot->dtype == NSA_DTYPE_BF16 ? 8 : 4;
+        const int rpw = 32 / (g.D / elems);
+        const int grid = cblocks + grid_for(nrows, (kThreads / 32) * rpw);
+        if (dot->dtype == NSA_DTYPE_BF16)
+            chunk_count_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+                g, idx, chunk_counts, nchunks, err, cblocks, (const __nv_bfloat16 *)dot->o,
+                (const __nv_bfloat16 *)dot->dO, dot->delta, nrows);
+        else
+            chunk_count_dot_kernel<float><<<grid, kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err, cblocks,
+                                                                     (const float *)dot->o, (const float *)dot->dO,
+                                                                     dot->delta, nrows);
+    } else {
+        csr_chunk_count_kernel<<<cblocks, kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     csr_chunk_prefix_kernel<<<grid_for(nbgj * 32, kThreads), kThreads, 0, st>>>(g, chunk_counts, nchunks, counts);

@@ -25,8 +25,15 @@ cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, in
 // prefixes in place; counts = list lengths), then an ordered per-chunk fill
 int csr_nchunks(const Geo &g);
 bool csr_chunked_ok(const Geo &g);
+// delta = rowsum(dO * O) riding along the chunk count (see below)
+struct DotArgs {
+    const void *o, *dO;
+    float *delta;
+    int dtype;
+};
+// dot (nullable): also computes delta in the same launch
 cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_counts, int *counts, int *err,
-                                   cudaStream_t st);
+                                   cudaStream_t st, const DotArgs *dot = nullptr);
 cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk_prefix, const int *offsets,
                                   int *rows, cudaStream_t st);
 // sums the fp32 partials of split blocks into dk/dv and zeroes unselected blocks

@@ -215,13 +215,15 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 // chunk_counts (nullable) selects the chunked build: per-chunk histograms
 // and an ordered per-chunk fill; otherwise one atomic count pass and one
 // ordered walk per block list.  Both give the same canonical lists.
+// dot (nullable, chunked build only): delta computed in the count's launch
 nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
                      Unit *units, int *nchunk, int *slot, WsHeader *hdr, int *err, int chunk, cudaStream_t st,
-                     int *chunk_counts = nullptr)
+                     int *chunk_counts = nullptr, const DotArgs *dot = nullptr)
 {
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     if (!g.dense && chunk_counts && csr_chunked_ok(g)) {
-        NSA_LAUNCH("csr_count", launch_csr_chunk_count(g, idx, chunk_counts, counts, err, st));
+        NSA_LAUNCH(dot ? "do_dot+csr_count" : "csr_count",
+                   launch_csr_chunk_count(g, idx, chunk_counts, counts, err, st, dot));
         NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
         NSA_LAUNCH("csr_fill", launch_csr_chunk_fill(g, idx, chunk_counts, offsets, rows, st));
         return NSA_OK;
@@ -237,14 +239,19 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
 }
 
 // Builds the plan of `idx` at `plan8` (layout L); index errors go to *err.
-nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanLayout &L, int *err, cudaStream_t st)
+// With dot, delta is computed in the same pass (see build_csr).
+nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanLayout &L, int *err, cudaStream_t st,
+                      const DotArgs *dot = nullptr)
 {
     WsHeader *phdr = (WsHeader *)plan8;
     NSA_TRY(cudaMemsetAsync(phdr, 0, sizeof(WsHeader), st));
     return build_csr(g, idx, (int *)(plan8 + L.counts), (int *)(plan8 + L.offsets), (int *)(plan8 + L.rows),
                      (Unit *)(plan8 + L.units), (int *)(plan8 + L.nchunk), (int *)(plan8 + L.slot), phdr, err,
-                     L.chunk, st, (int *)(plan8 + L.chunkc));
+                     L.chunk, st, (int *)(plan8 + L.chunkc), dot);
 }
+
+// whether build_plan takes the chunked path (which can carry the dot)
+bool plan_is_chunked(const Geo &g) { return !g.dense && csr_chunked_ok(g); }
 
 nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
@@ -282,8 +289,13 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
     if (g.ntok == 0)
         return NSA_OK;
-    NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
-    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st)) != NSA_OK)
+    // delta = rowsum(dO * O): in the index count's launch when the index is
+    // built here by chunks, else on its own
+    const DotArgs dot{o, dO, delta, p->dtype};
+    const bool fused = !plan && plan_is_chunked(g);
+    if (!fused)
+        NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
+    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr)) != NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
