@@ -48,6 +48,10 @@ def lib():
         L.oracle_sel_fwd_w.argtypes = common + [_ptr] * 6 + [_i64]
         L.oracle_sel_bwd_w.restype = None
         L.oracle_sel_bwd_w.argtypes = common + [_ptr] * 11 + [_i64]
+        L.oracle_sel_fwd_s.restype = None
+        L.oracle_sel_fwd_s.argtypes = common + [_ptr] * 6 + [_i64, _ptr]
+        L.oracle_sel_bwd_s.restype = None
+        L.oracle_sel_bwd_s.argtypes = common + [_ptr] * 11 + [_i64, _ptr, _ptr]
         L.oracle_inverse_index.restype = None
         L.oracle_inverse_index.argtypes = [_i64] * 5 + [_ptr, _ptr, _i64, _ptr, _ptr]
         L.oracle_do_dot.restype = None
@@ -94,32 +98,40 @@ def _shape(q, k, idx, cu_seqlens):
     return B, Hq, Hkv, T, D, S
 
 
-def sel_fwd(q, k, v, idx, bs, scale=None, cu_seqlens=None, window=0):
-    """Returns (O, LSE) in fp64.  window > 0: keys k with t - k < window only."""
+def sel_fwd(q, k, v, idx, bs, scale=None, cu_seqlens=None, window=0, sinks=None):
+    """Returns (O, LSE) in fp64.  window > 0: keys k with t - k < window only.
+    sinks: one logit per query head in every row's softmax denominator."""
     q, k, v, idx, cu = _f64(q), _f64(k), _f64(v), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    sk = None if sinks is None else _f64(sinks)
     o = np.zeros_like(q)
     lse = np.zeros(q.shape[:-1], dtype=np.float64)
-    lib().oracle_sel_fwd_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                           _p(o), _p(lse), int(window))
+    lib().oracle_sel_fwd_s(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                           _p(o), _p(lse), int(window), _p(sk))
     return o, lse
 
 
-def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False, window=0):
-    """Returns dict with dq, dk, dv, o, lse (and dsum = row sums of dS)."""
+def sel_bwd(q, k, v, idx, dO, bs, scale=None, cu_seqlens=None, want_dsum=False, window=0, sinks=None):
+    """Returns dict with dq, dk, dv, o, lse (and dsum = row sums of dS; with
+    sinks, dsinks = the gradient of the sink logits)."""
     q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    sk = None if sinks is None else _f64(sinks)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     o = np.zeros_like(q)
     lse = np.zeros(q.shape[:-1], dtype=np.float64)
     dsum = np.zeros(q.shape[:-1], dtype=np.float64) if want_dsum else None
-    lib().oracle_sel_bwd_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
-                           _p(dO), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(dsum), int(window))
+    dsk = None if sk is None else np.zeros_like(sk)
+    lib().oracle_sel_bwd_s(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                           _p(dO), _p(dq), _p(dk), _p(dv), _p(o), _p(lse), _p(dsum), int(window), _p(sk),
+                           _p(dsk))
     out = dict(dq=dq, dk=dk, dv=dv, o=o, lse=lse)
     if want_dsum:
         out["dsum"] = dsum
+    if dsk is not None:
+        out["dsinks"] = dsk
     return out
 
 

@@ -31,6 +31,15 @@
  * dense causal backward (SWA); W = 0 means no window.  The *_w entry points
  * take it; the others use W = 0.
  *
+ * Attention sinks (the *_s entry points; the same page's backward chain ends
+ * in a dSink kernel but does not define the sink, so this is the plainest
+ * reading): one logit sigma_h per query head joins every row's softmax
+ * denominator and carries no value,
+ *   LSE_t   = log( sum_k exp(s_tk) + exp(sigma_h) )   (= sigma_h for an empty row)
+ *   P_tk, O_t, dS_tk, dQ, dK, dV as above with this LSE
+ *   dsigma_h = - sum_{b,t} exp(sigma_h - LSE_t) D_t
+ * (the sink's probability exp(sigma_h - LSE_t) times dP = 0 minus D_t).
+ *
  * Readings of points the pages leave open: scale is passed in (callers use
  * 1/sqrt(D)); keys after t inside the own block are masked (causal); -1
  * slots are ignored wherever they sit; an index is invalid if it is < -1,
@@ -52,14 +61,15 @@
 typedef struct {
     int64_t B, Hq, Hkv, T, D, bs, S;
     double scale;
-    const int32_t *cu; /* NULL: fixed length */
-    int64_t window;    /* 0: none; else keys k with t - k < window only */
+    const int32_t *cu;    /* NULL: fixed length */
+    int64_t window;       /* 0: none; else keys k with t - k < window only */
+    const double *sinks;  /* NULL: none; else one logit per query head */
 } prob_t;
 
 static prob_t mk(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D,
                  int64_t bs, int64_t S, double scale, const int32_t *cu)
 {
-    prob_t p = {B, Hq, Hkv, T, D, bs, S, scale, cu, 0};
+    prob_t p = {B, Hq, Hkv, T, D, bs, S, scale, cu, 0, NULL};
     return p;
 }
 
@@ -164,16 +174,18 @@ static int64_t row_scores(const prob_t *p, const double *q, const double *k, con
     return n;
 }
 
-/* log-sum-exp of sc[0..n) with the max shift; -inf when n == 0 */
-static double lse_of(const double *sc, int64_t n)
+/* log-sum-exp of sc[0..n) and, with sinks, head h's sink logit, with the
+ * max shift; -inf when there is nothing to sum */
+static double lse_of(const prob_t *p, int64_t h, const double *sc, int64_t n)
 {
-    if (n == 0)
+    const int has = p->sinks != NULL;
+    if (n == 0 && !has)
         return -INFINITY;
-    double m = sc[0];
-    for (int64_t i = 1; i < n; ++i)
+    double m = has ? p->sinks[h] : sc[0];
+    for (int64_t i = 0; i < n; ++i)
         if (sc[i] > m)
             m = sc[i];
-    double l = 0.0;
+    double l = has ? exp(p->sinks[h] - m) : 0.0;
     for (int64_t i = 0; i < n; ++i)
         l += exp(sc[i] - m);
     return m + log(l);
@@ -186,7 +198,7 @@ static double row_forward(const prob_t *p, const double *q, const double *k, con
 {
     const int64_t G = p->Hq / p->Hkv, g = h / G;
     int64_t n = row_scores(p, q, k, idx, b, h, t, keys, sc);
-    double lse = lse_of(sc, n);
+    double lse = lse_of(p, h, sc, n);
     for (int64_t d = 0; d < p->D; ++d)
         o[d] = 0.0;
     for (int64_t i = 0; i < n; ++i) {
@@ -208,14 +220,15 @@ static int64_t n_rows_total(const prob_t *p)
     return n;
 }
 
-/* Forward: o (layout of q) and lse. */
-void oracle_sel_fwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+/* Forward: o (layout of q) and lse; sinks NULL or one logit per query head. */
+void oracle_sel_fwd_s(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
                       int64_t S, double scale, const int32_t *cu, const double *q,
                       const double *k, const double *v, const int32_t *idx, double *o,
-                      double *lse, int64_t window)
+                      double *lse, int64_t window, const double *sinks)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
     p.window = window;
+    p.sinks = sinks;
 #pragma omp parallel
     {
         int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
@@ -232,6 +245,14 @@ void oracle_sel_fwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, 
     }
 }
 
+void oracle_sel_fwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                      int64_t S, double scale, const int32_t *cu, const double *q,
+                      const double *k, const double *v, const int32_t *idx, double *o,
+                      double *lse, int64_t window)
+{
+    oracle_sel_fwd_s(B, Hq, Hkv, T, D, bs, S, scale, cu, q, k, v, idx, o, lse, window, NULL);
+}
+
 /*
  * Backward.  Recomputes the forward in fp64 (O, LSE), then
  *   pass 1, one query row at a time: D_t, dQ_t and (optionally) sum_k dS_tk;
@@ -239,14 +260,15 @@ void oracle_sel_fwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, 
  *           the group that attends k.
  * o_out / lse_out / dsum_out may be NULL.
  */
-void oracle_sel_bwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+void oracle_sel_bwd_s(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
                       int64_t S, double scale, const int32_t *cu, const double *q,
                       const double *k, const double *v, const int32_t *idx, const double *dO,
                       double *dq, double *dk, double *dv, double *o_out, double *lse_out,
-                      double *dsum_out, int64_t window)
+                      double *dsum_out, int64_t window, const double *sinks, double *dsinks_out)
 {
     prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
     p.window = window;
+    p.sinks = sinks;
     const int64_t G = Hq / Hkv;
     const int64_t nrow = n_rows_total(&p) * Hq;
     double *O = o_out ? o_out : (double *)malloc(sizeof(double) * nrow * D);
@@ -291,6 +313,18 @@ void oracle_sel_bwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, 
         free(sc);
     }
 
+    /* the sinks' gradient: each row's term, then a sum per head in (b, t) order */
+    if (sinks && dsinks_out)
+        for (int64_t h = 0; h < Hq; ++h) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < B; ++b)
+                for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                    const int64_t so = stat_off(&p, Hq, b, h, t);
+                    acc -= exp(sinks[h] - L[so]) * Dt[so];
+                }
+            dsinks_out[h] = acc;
+        }
+
     /* pass 2: per key, sum over every row of the group that attends it */
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int64_t b = 0; b < B; ++b)
@@ -327,6 +361,16 @@ void oracle_sel_bwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, 
     if (!lse_out)
         free(L);
     free(Dt);
+}
+
+void oracle_sel_bwd_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                      int64_t S, double scale, const int32_t *cu, const double *q,
+                      const double *k, const double *v, const int32_t *idx, const double *dO,
+                      double *dq, double *dk, double *dv, double *o_out, double *lse_out,
+                      double *dsum_out, int64_t window)
+{
+    oracle_sel_bwd_s(B, Hq, Hkv, T, D, bs, S, scale, cu, q, k, v, idx, dO, dq, dk, dv, o_out, lse_out,
+                     dsum_out, window, NULL, NULL);
 }
 
 /*

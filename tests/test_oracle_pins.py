@@ -402,3 +402,82 @@ def test_window_sampled_entries_agree_with_whole_problem():
     for i, (b, g, kk) in enumerate(keys):
         np.testing.assert_allclose(dk[i], r["dk"][b, g, kk], atol=1e-13, rtol=0)
         np.testing.assert_allclose(dv[i], r["dv"][b, g, kk], atol=1e-13, rtol=0)
+
+
+# ---- attention sinks: one logit per query head in every row's denominator
+
+
+def _sink_reference(q, k, v, do, mask_kv, sinks, scale):
+    """fp64 attention with a sink column appended to the scores, by plain
+    torch ops + autograd (softmax over [scores | sink], the sink's
+    probability dropped before P.V)."""
+    G = q.shape[1] // k.shape[1]
+    qr, kr, vr = (x.double().clone().requires_grad_(True) for x in (q, k, v))
+    sr = torch.as_tensor(sinks, dtype=torch.float64).clone().requires_grad_(True)
+    ke = kr.repeat_interleave(G, dim=1)
+    ve = vr.repeat_interleave(G, dim=1)
+    mask = mask_kv.repeat_interleave(G, dim=1)
+    s = torch.einsum("bhtd,bhkd->bhtk", qr, ke) * scale
+    s = s.masked_fill(~mask, float("-inf"))
+    B, Hq, T, _ = s.shape
+    col = sr.view(1, Hq, 1, 1).expand(B, Hq, T, 1)
+    p = torch.softmax(torch.cat([s, col], dim=-1), dim=-1)[..., :T]
+    o = torch.einsum("bhtk,bhkd->bhtd", p, ve)
+    lse = torch.logsumexp(torch.cat([s, col], dim=-1), dim=-1)
+    o.backward(do.double())
+    return o.detach(), lse.detach(), qr.grad, kr.grad, vr.grad, sr.grad
+
+
+@pytest.mark.parametrize("W,G", [(0, 2), (7, 1), (0, 3)])
+def test_sinks_match_autograd(W, G):
+    """Dense causal (optionally windowed) attention with sinks against plain
+    torch fp64 attention with an appended sink column and its autograd."""
+    B, Hkv, T, D, bs = 2, 2, 29, 8, 4
+    Hq = Hkv * G
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=8)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    sinks = np.random.default_rng(3).normal(0.0, 2.0, Hq)
+    scale = 1 / math.sqrt(D)
+    mask = _band_mask(B, Hkv, T, W if W else T + 1)
+    o_ref, lse_ref, dq_ref, dk_ref, dv_ref, ds_ref = _sink_reference(q, k, v, do, mask, sinks, scale)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, window=W, sinks=sinks)
+    np.testing.assert_allclose(r["o"], o_ref.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(r["lse"], lse_ref.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(r["dq"], dq_ref.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dk"], dk_ref.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dv"], dv_ref.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(r["dsinks"], ds_ref.numpy(), atol=1e-10, rtol=0)
+    o, lse = oracle.sel_fwd(q, k, v, idx, bs, window=W, sinks=sinks)
+    np.testing.assert_array_equal(o, r["o"])
+    np.testing.assert_array_equal(lse, r["lse"])
+
+
+def test_sinks_closed_forms_and_finite_differences():
+    B, Hq, Hkv, T, D, bs = 1, 2, 1, 12, 4, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=10)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    sinks = np.array([0.7, -1.3])
+    scale = 1 / math.sqrt(D)
+    r = oracle.sel_bwd(q, k, v, idx, do, bs, sinks=sinks)
+    # row t = 0 sees key 0 only: LSE = log(e^s + e^sigma), O = v_0 / (1 + e^(sigma - s))
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    for h in range(Hq):
+        s00 = scale * float(qd[0, h, 0] @ kd[0, 0, 0])
+        assert abs(r["lse"][0, h, 0] - np.logaddexp(s00, sinks[h])) < 1e-13
+        np.testing.assert_allclose(r["o"][0, h, 0], vd[0, 0, 0] / (1 + math.exp(sinks[h] - s00)), atol=1e-13)
+    # sigma -> -inf: no sink at all
+    none = oracle.sel_bwd(q, k, v, idx, do, bs)
+    far = oracle.sel_bwd(q, k, v, idx, do, bs, sinks=np.full(Hq, -np.inf))
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(far[n], none[n])
+    np.testing.assert_array_equal(far["dsinks"], np.zeros(Hq))
+    # central differences of <dO, O(sigma)>
+    dod = do.double().numpy()
+    eps = 1e-6
+    for h in range(Hq):
+        sp, sm = sinks.copy(), sinks.copy()
+        sp[h] += eps
+        sm[h] -= eps
+        fp = float((oracle.sel_fwd(q, k, v, idx, bs, sinks=sp)[0] * dod).sum())
+        fm = float((oracle.sel_fwd(q, k, v, idx, bs, sinks=sm)[0] * dod).sum())
+        assert abs((fp - fm) / (2 * eps) - r["dsinks"][h]) < 1e-7
