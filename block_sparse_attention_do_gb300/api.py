@@ -30,7 +30,7 @@ SYMBOLS = (
     "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
     "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
     "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
-    "nsa_swa_fwd", "nsa_swa_bwd",
+    "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd",
 )
 
 
@@ -86,6 +86,8 @@ def lib() -> C.CDLL:
         L.nsa_sel_bwd_planned.argtypes = [pp] + [_P] * 12 + [_P, C.c_size_t, _P]
         L.nsa_swa_fwd.argtypes = [pp, C.c_int32] + [_P] * 6 + [_P, C.c_size_t, _P]
         L.nsa_swa_bwd.argtypes = [pp, C.c_int32] + [_P] * 10 + [_P, C.c_size_t, _P]
+        L.nsa_sink_fwd.argtypes = [pp, C.c_int32] + [_P] * 7 + [_P, C.c_size_t, _P]
+        L.nsa_sink_bwd.argtypes = [pp, C.c_int32] + [_P] * 12 + [_P, C.c_size_t, _P]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []
@@ -162,10 +164,11 @@ def _lse_shape(q, cu_seqlens):
 
 
 def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seqlen=None,
-            dense=False, ws=None, stream=None, window=None):
+            dense=False, ws=None, stream=None, window=None, sinks=None):
     """Selection (or dense causal, or with `window` sliding-window causal)
-    forward through the C ABI: returns (o, lse)."""
-    dense = dense or window is not None
+    forward through the C ABI: returns (o, lse).  `sinks` (fp32, one logit
+    per query head, dense entry only) adds attention sinks."""
+    dense = dense or window is not None or sinks is not None
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     o = torch.empty_like(q)
@@ -176,7 +179,10 @@ def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
     ws = workspace(n, q.device, "fwd") if ws is None else ws
     L = lib()
     st = _stream(stream)
-    if window is not None:
+    if sinks is not None:
+        s = L.nsa_sink_fwd(C.byref(p), int(window or 0), _ptr(cu_seqlens), _ptr(sinks), _ptr(q), _ptr(k),
+                           _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), st)
+    elif window is not None:
         s = L.nsa_swa_fwd(C.byref(p), int(window), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                           _ptr(lse), _ptr(ws), ws.numel(), st)
     elif cu_seqlens is not None:
@@ -208,11 +214,14 @@ def build_plan(q, k, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
 
 
 def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=None,
-            max_seqlen=None, dense=False, ws=None, stream=None, out=None, plan=None, window=None):
+            max_seqlen=None, dense=False, ws=None, stream=None, out=None, plan=None, window=None,
+            sinks=None):
     """Selection (or dense causal, or with `window` sliding-window causal)
-    backward through the C ABI: returns (dq, dk, dv).  With `plan` (from
-    build_plan on the same block_idx) the index build is skipped."""
-    dense = dense or window is not None
+    backward through the C ABI: returns (dq, dk, dv), and dsinks as a fourth
+    value with `sinks` (dense entry only; o and lse as the sink forward wrote
+    them).  With `plan` (from build_plan on the same block_idx) the index
+    build is skipped."""
+    dense = dense or window is not None or sinks is not None
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     if out is None:
@@ -237,6 +246,13 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
         raise NsaError(1, "nsa_bwd_workspace_size")
     ws = workspace(n, q.device, "bwd") if ws is None else ws
     st = _stream(stream)
+    if sinks is not None:
+        dsinks = torch.empty_like(sinks)
+        s = L.nsa_sink_bwd(C.byref(p), int(window or 0), _ptr(cu_seqlens), _ptr(sinks), _ptr(q), _ptr(k),
+                           _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsinks),
+                           _ptr(ws), ws.numel(), st)
+        _check(s, "nsa_sink_bwd")
+        return dq, dk, dv, dsinks
     if window is not None:
         s = L.nsa_swa_bwd(C.byref(p), int(window), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                           _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), st)

@@ -612,6 +612,69 @@ __global__ void __launch_bounds__(kFillWarps * 32) csr_chunk_fill_kernel(Geo g, 
     }
 }
 
+// ---- attention sinks
+// Row i of o / lse (the same linear row order in both layouts) belongs to
+// query head (i / T) % Hq (BHTD) or i % Hq (THD).
+__device__ __forceinline__ int row_head(const Geo &g, int64_t i)
+{
+    return g.thd ? (int)(i % g.Hq) : (int)((i / g.T) % g.Hq);
+}
+
+// Folds each head's sink into the forward's rows, one warp per row:
+// LSE' = log(e^LSE + e^sink), O' = O e^(LSE - LSE') (an empty row, LSE =
+// -inf, becomes LSE' = sink, O' = 0).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) sink_fwd_kernel(Geo g, const float *__restrict__ sinks, T *__restrict__ o,
+                                                            float *__restrict__ lse, int64_t nrows)
+{
+    const int lane = threadIdx.x & 31;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < nrows;
+         i += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const float sk = sinks[row_head(g, i)], L = lse[i];
+        float Ln, f;
+        if (L == -INFINITY) {
+            Ln = sk;
+            f = 0.f;
+        } else {
+            const float m = fmaxf(L, sk);
+            Ln = m + log1pf(expf(-fabsf(L - sk)));
+            f = expf(L - Ln);
+        }
+        T *row = o + i * g.D;
+        for (int d = lane; d < g.D; d += 32)
+            row[d] = from_f<T>(to_f(row[d]) * f);
+        if (lane == 0)
+            lse[i] = Ln;
+    }
+}
+
+// dsinks[h] = - sum over the head's rows of exp(sink - LSE) * delta: one
+// block per head, a fixed split over threads and a fixed tree (deterministic).
+__global__ void __launch_bounds__(kThreads) sink_bwd_kernel(Geo g, const float *__restrict__ sinks,
+                                                            const float *__restrict__ lse,
+                                                            const float *__restrict__ delta, float *__restrict__ dsinks)
+{
+    __shared__ double part[kThreads];
+    const int h = blockIdx.x;
+    const float sk = sinks[h];
+    const int64_t per_head = g.thd ? (int64_t)g.ntok : (int64_t)g.B * g.T;
+    double acc = 0.0;
+    for (int64_t x = threadIdx.x; x < per_head; x += blockDim.x) {
+        // the x-th row of head h: token x (THD) or (b, t) = (x / T, x % T)
+        const int64_t i = g.thd ? x * g.Hq + h : ((x / g.T) * g.Hq + h) * g.T + x % g.T;
+        acc -= (double)expf(sk - lse[i]) * (double)delta[i];
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w)
+            part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        dsinks[h] = (float)part[0];
+}
+
 }  // namespace
 
 cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *delta, int dtype,
@@ -736,6 +799,24 @@ cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cud
     const int64_t n = (int64_t)g.ntok * g.Hkv;
     count_pairs_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(g, idx,
                                                                    (unsigned long long *)out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sink_fwd(const Geo &g, const float *sinks, void *o, float *lse, int dtype, cudaStream_t st)
+{
+    const int64_t nrows = (int64_t)g.ntok * g.Hq;
+    const int grid = grid_for(nrows, kThreads / 32);
+    if (dtype == NSA_DTYPE_BF16)
+        sink_fwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(g, sinks, (__nv_bfloat16 *)o, lse, nrows);
+    else
+        sink_fwd_kernel<float><<<grid, kThreads, 0, st>>>(g, sinks, (float *)o, lse, nrows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sink_bwd(const Geo &g, const float *sinks, const float *lse, const float *delta, float *dsinks,
+                            cudaStream_t st)
+{
+    sink_bwd_kernel<<<g.Hq, kThreads, 0, st>>>(g, sinks, lse, delta, dsinks);
     return cudaGetLastError();
 }
 

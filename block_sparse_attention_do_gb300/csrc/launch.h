@@ -41,6 +41,11 @@ cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *b
                                const float *partials, void *dk, void *dv, int dtype,
                                cudaStream_t st);
 cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cudaStream_t st);
+// attention sinks: fold sinks[h] into the forward's o and lse in place; and
+// dsinks[h] = -sum over head h's rows of exp(sinks[h] - lse) * delta
+cudaError_t launch_sink_fwd(const Geo &g, const float *sinks, void *o, float *lse, int dtype, cudaStream_t st);
+cudaError_t launch_sink_bwd(const Geo &g, const float *sinks, const float *lse, const float *delta, float *dsinks,
+                            cudaStream_t st);
 
 // ---- SIMT kernels (k_simt.cu): any supported shape, fp32 or bf16 ----------
 cudaError_t launch_fwd_simt(const Geo &g, const void *q, const void *k, const void *v,

@@ -185,7 +185,7 @@ nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 
 nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const int32_t *idx, void *o, float *lse,
-                   void *ws, size_t ws_bytes, void *stream, int window = 0)
+                   void *ws, size_t ws_bytes, void *stream, int window = 0, const float *sinks = nullptr)
 {
     Geo g;
     nsa_status s = make_geo(p, thd, mode, cu, g, window);
@@ -208,6 +208,8 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         NSA_LAUNCH("fwd_tc", launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, &hdr->tile_next, st));
     else
         NSA_LAUNCH("fwd_simt", launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
+    if (sinks)
+        NSA_LAUNCH("sink_fwd", launch_sink_fwd(g, sinks, o, lse, p->dtype, st));
     return NSA_OK;
 }
 
@@ -256,7 +258,8 @@ bool plan_is_chunked(const Geo &g) { return !g.dense && csr_chunked_ok(g); }
 nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
                    const int32_t *idx, const void *plan, void *dq, void *dk, void *dv, void *ws,
-                   size_t ws_bytes, void *stream, int window = 0)
+                   size_t ws_bytes, void *stream, int window = 0, const float *sinks = nullptr,
+                   float *dsinks = nullptr)
 {
     Geo g;
     nsa_status s = make_geo(p, thd, mode, cu, g, window);
@@ -287,8 +290,11 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     const int *slot = (const int *)(pl8 + P.slot);
     const WsHeader *phdr = (const WsHeader *)pl8;
     NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
-    if (g.ntok == 0)
+    if (g.ntok == 0) {
+        if (sinks)
+            NSA_TRY(cudaMemsetAsync(dsinks, 0, sizeof(float) * g.Hq, st));
         return NSA_OK;
+    }
     // delta = rowsum(dO * O): in the index count's launch when the index is
     // built here by chunks, else on its own
     const DotArgs dot{o, dO, delta, p->dtype};
@@ -306,6 +312,8 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
         NSA_LAUNCH("dq_simt", launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));
     }
+    if (sinks)
+        NSA_LAUNCH("sink_bwd", launch_sink_bwd(g, sinks, lse, delta, dsinks, st));
     return NSA_OK;
 }
 
@@ -503,6 +511,32 @@ nsa_status nsa_swa_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_s
         return NSA_ERR_INVALID_ARG;
     return run_bwd(p, thd, DENSE, cu_seqlens, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws, ws_bytes,
                    stream, window);
+}
+
+nsa_status nsa_sink_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const float *sinks,
+                        const void *q, const void *k, const void *v, void *o, float *lse, void *ws,
+                        size_t ws_bytes, void *stream)
+{
+    if (!p || window < 0 || !sinks || ((uintptr_t)sinks & 3))
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_fwd(p, thd, DENSE, cu_seqlens, q, k, v, nullptr, o, lse, ws, ws_bytes, stream, window, sinks);
+}
+
+nsa_status nsa_sink_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const float *sinks,
+                        const void *q, const void *k, const void *v, const void *o, const void *dO,
+                        const float *lse, void *dq, void *dk, void *dv, float *dsinks, void *ws,
+                        size_t ws_bytes, void *stream)
+{
+    if (!p || window < 0 || !sinks || !dsinks || ((uintptr_t)sinks & 3) || ((uintptr_t)dsinks & 3))
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_bwd(p, thd, DENSE, cu_seqlens, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws, ws_bytes,
+                   stream, window, sinks, dsinks);
 }
 
 nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,

@@ -164,6 +164,28 @@ nsa_status nsa_swa_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_s
                        void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Dense causal attention with attention sinks (the cuDNN-frontend page's
+ * backward chain ends in a dSink kernel; the page does not define the sink,
+ * and the plainest reading is taken): one fp32 logit sinks[h] per query head
+ * joins every row's softmax denominator and carries no value, so
+ *   LSE_t = log( sum_k exp(s_tk) + exp(sinks[h]) ),  P_tk = exp(s_tk - LSE_t),
+ *   O_t = sum_k P_tk v_k,  dsinks[h] = - sum_{b,t} exp(sinks[h] - LSE_t) D_t
+ * with D_t = <dO_t, O_t>; dQ/dK/dV keep their form with this LSE.  window = 0
+ * is plain causal, >= 1 the sliding window of nsa_swa_*.  cu_seqlens as for
+ * nsa_swa_*.  sinks (device, Hq floats) is read, dsinks (device, Hq floats)
+ * is written (overwritten, not accumulated).  The forward writes o and lse
+ * with the sink included; the backward takes them as the forward wrote them.
+ * Workspaces as for the dense entries.
+ */
+nsa_status nsa_sink_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const float *sinks,
+                        const void *q, const void *k, const void *v, void *o, float *lse, void *ws,
+                        size_t ws_bytes, void *stream);
+nsa_status nsa_sink_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens, const float *sinks,
+                        const void *q, const void *k, const void *v, const void *o, const void *dO,
+                        const float *lse, void *dq, void *dk, void *dv, float *dsinks, void *ws,
+                        size_t ws_bytes, void *stream);
+
+/*
  * Reusable backward plan.  The pages build nothing like it: it is the inverse
  * index of one block_idx tensor (block -> ascending list of the tokens that
  * selected it, see nsa_build_inverse_index) together with the dK/dV work

@@ -448,3 +448,52 @@ def test_full_size_mid_size_fp32_and_bf16():
         got = _run(q, k, v, do, idx, bs)
         ref = oracle.sel_bwd(q, k, v, idx, do, bs)
         _compare(got, ref, dtype)
+
+
+# ---- attention sinks on the dense entry (tensor-core path for bf16 D=128
+# bs=64, SIMT otherwise), against the oracle with the same sinks
+
+SINK_CASES = [
+    # dtype, (B, Hq, Hkv, T, D, bs), window, thd
+    (torch.bfloat16, (1, 16, 1, 300, 128, 64), 0, False),
+    (torch.bfloat16, (2, 8, 2, 200, 128, 64), 96, False),
+    (torch.float32, (1, 4, 2, 150, 64, 32), 0, False),
+    (torch.bfloat16, (0, 16, 2, 0, 128, 64), 0, True),  # THD, lengths below
+]
+
+
+@pytest.mark.parametrize("dtype,shape,window,thd", SINK_CASES)
+def test_sinks_dense(dtype, shape, window, thd):
+    B, Hq, Hkv, T, D, bs = shape
+    sinks = torch.from_numpy(np.random.default_rng(11).normal(0.0, 2.0, Hq).astype(np.float32))
+    if thd:
+        lens = [130, 1, 257, 64]
+        cu = inputs.cu_seqlens_from_lengths(lens)
+        total = sum(lens)
+        q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=dtype, seed=12, layout="thd")
+        nb = (max(lens) + bs - 1) // bs
+        dense = np.full((total, Hkv, nb), -1, dtype=np.int32)  # every block up to the token's own
+        off = 0
+        for L in lens:
+            for t in range(L):
+                dense[off + t, :, : t // bs + 1] = np.arange(t // bs + 1)
+            off += L
+        ref = oracle.sel_bwd(q, k, v, torch.from_numpy(dense), do, bs, cu_seqlens=cu, window=window,
+                             sinks=sinks.numpy())
+        gcu = cu.to(DEV)
+    else:
+        q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=12)
+        ref = oracle.sel_bwd(q, k, v, inputs.make_dense_block_idx(B, Hkv, T, bs), do, bs, window=window,
+                             sinks=sinks.numpy())
+        gcu = None
+    g = [x.to(DEV) for x in (q, k, v, do)]
+    gs = sinks.to(DEV)
+    o, lse = api.sel_fwd(g[0], g[1], g[2], None, bs, cu_seqlens=gcu, window=window or None, sinks=gs)
+    dq, dk, dv, dsinks = api.sel_bwd(g[0], g[1], g[2], o, g[3], lse, None, bs, cu_seqlens=gcu,
+                                     window=window or None, sinks=gs)
+    torch.cuda.synchronize()
+    _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, dtype)
+    got = dsinks.cpu().double().numpy()
+    tol = TOL[dtype]
+    assert np.all(np.abs(got - ref["dsinks"]) <= tol * np.maximum(1.0, np.abs(ref["dsinks"]))), \
+        (got, ref["dsinks"])
