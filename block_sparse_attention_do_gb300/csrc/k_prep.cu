@@ -27,8 +27,9 @@ inline int grid_for(int64_t n, int per_block, int cap = 152 * 32)
 // ---------------------------------------------------------------- do_dot
 // Rows are contiguous D-vectors in both layouts, and delta uses the row order
 // of o, so the kernel is a plain segmented dot product over rows.
-// blocks blk of nblk (grid-stride); each warp takes two row groups per step,
-// so that four 16-byte loads per thread are in flight
+// blocks blk of nblk (grid-stride); each warp takes kDotU row groups per
+// step, so that 2 * kDotU 16-byte loads per thread are in flight
+constexpr int kDotU = 4;
 template <typename T>
 __device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__restrict__ dO, float *__restrict__ out,
                                             int64_t nrows, int D, int blk, int nblk)
@@ -39,10 +40,10 @@ __device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__
     const int sub = lane / tpr, part = lane % tpr, rpw = 32 / tpr;
     const int64_t warp = ((int64_t)blk * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)nblk * blockDim.x) >> 5;
-    for (int64_t r0 = warp * 2 * rpw; r0 < nrows; r0 += nwarps * 2 * rpw) {
-        uint4 a[2], b[2];
+    for (int64_t r0 = warp * kDotU * rpw; r0 < nrows; r0 += nwarps * kDotU * rpw) {
+        uint4 a[kDotU], b[kDotU];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kDotU; ++u) {
             const int64_t r = r0 + u * rpw + sub;
             a[u] = b[u] = make_uint4(0, 0, 0, 0);
             if (r < nrows) {
@@ -51,7 +52,7 @@ __device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kDotU; ++u) {
             const int64_t r = r0 + u * rpw + sub;
             const T *ea = reinterpret_cast<const T *>(&a[u]);
             const T *eb = reinterpret_cast<const T *>(&b[u]);
@@ -693,7 +694,7 @@ cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *de
     const int64_t nrows = (int64_t)g.ntok * g.Hq;
     const int elems = dtype == NSA_DTYPE_BF16 ? 8 : 4;
     const int rpw = 32 / (g.D / elems);
-    const int grid = grid_for(nrows, (kThreads / 32) * 2 * rpw);
+    const int grid = grid_for(nrows, (kThreads / 32) * kDotU * rpw);
     if (dtype == NSA_DTYPE_BF16)
         do_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta, nrows, g.D);
@@ -746,7 +747,7 @@ cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_coun
         const int64_t nrows = (int64_t)g.ntok * g.Hq;
         const int elems = dot->dtype == NSA_DTYPE_BF16 ? 8 : 4;
         const int rpw = 32 / (g.D / elems);
-        const int grid = cblocks + grid_for(nrows, (kThreads / 32) * 2 * rpw);
+        const int grid = cblocks + grid_for(nrows, (kThreads / 32) * kDotU * rpw);
         if (dot->dtype == NSA_DTYPE_BF16)
             chunk_count_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
                 g, idx, chunk_counts, nchunks, err, cblocks, (const __nv_bfloat16 *)dot->o,
