@@ -67,20 +67,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking test of a phase (mbarrier.test_wait).  try_wait may suspend
-// the thread for a while when the phase is incomplete, so loops that poll
-// several barriers use this instead.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for the phase with the given parity to complete.  Returns false if
 // it did not complete within kWaitLimitNs or if *abort became non-zero (some
 // other role gave up first); the caller then winds down.
@@ -111,19 +97,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, v
     const bool ok = mbar_wait(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
 }
-
-// Named barrier `id` over `count` threads that also ORs a predicate across
-// them: every participant gets the same answer (used to agree on stopping).
-template <int ID, int COUNT> __device__ __forceinline__ bool named_bar_any_t(bool v)
-{
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(r)
-                 : "r"((uint32_t)v), "n"(ID), "n"(COUNT)
-                 : "memory");
-    return r != 0;
-}
-#define named_bar_any(ID, COUNT, V) named_bar_any_t<(ID), (COUNT)>(V)
 
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
@@ -161,23 +134,11 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
-// bring the 128-byte line holding `p` into L2
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // ----------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
 
@@ -366,11 +327,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// byte offset of 16-byte chunk c of row r inside a 128B-swizzled tile
-__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c)
-{
-    return r * 128u + ((c ^ (r & 7u)) << 4);
-}
 
 // 2^x by the SFU's approximate exponential (flush-to-zero); its relative
 // error is far below the bf16 rounding that P and dS receive next.
