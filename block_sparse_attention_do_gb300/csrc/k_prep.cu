@@ -154,6 +154,8 @@ __device__ __forceinline__ unsigned row_slots(const int *row, int S, int t, int 
 __global__ void __launch_bounds__(kThreads) validate_kernel(Geo g, const int *__restrict__ idx,
                                                             int *err)
 {
+    // the forward kernel launched next does not wait for this check
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t n = (int64_t)g.ntok * g.Hkv;
     for (int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; lin < n;
          lin += (int64_t)gridDim.x * blockDim.x) {

@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The dQ kernel, launched next as a programmatic dependent, reads nothing
+    // this kernel writes: let it take each SM as this kernel's CTA there ends.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || (GATHER_TMA && warp == 3)) {
         // ------------------------------------------------------- tile loader

@@ -528,6 +528,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
     }
+    // As a programmatic dependent this kernel may have started before
+    // the dK/dV kernel ended: its completion implies that one's (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -576,8 +579,10 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     if (grid < 1)
         return cudaSuccess;
     cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    dq_tc_kernel<<<grid, 384, smem, st>>>(tq, tdo, tk, tv, p);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel before it on the stream (the dK/dV
+    // kernel, whose outputs it does not read): its CTAs start as that kernel's
+    // CTAs end; everything it reads was written by earlier, completed launches
+    return launch_dependent(dq_tc_kernel, dim3(grid), dim3(384), smem, st, tq, tdo, tk, tv, p);
 }
 
 }  // namespace nsa

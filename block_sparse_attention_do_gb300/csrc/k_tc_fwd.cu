@@ -528,12 +528,15 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
     }
+    // As a programmatic dependent this kernel may have started before
+    // the index validation ended: its completion implies that one's (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
-                          void *o, float *lse, int *err, int *tile_next, cudaStream_t st)
+                          void *o, float *lse, int *err, int *tile_next, bool after_validate, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
@@ -564,6 +567,10 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     if (grid < 1)
         return cudaSuccess;
     cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // After the index validation, a programmatic dependent of it (the check
+    // only reports errors; this kernel skips invalid entries by itself).
+    if (after_validate)
+        return launch_dependent(fwd_tc_kernel, dim3(grid), dim3(384), smem, st, tq, tk, tv, p);
     fwd_tc_kernel<<<grid, 384, smem, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }

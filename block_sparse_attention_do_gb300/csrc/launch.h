@@ -60,9 +60,12 @@ cudaError_t launch_dkdv_simt(const Geo &g, const void *q, const void *k, const v
 
 // ---- tensor-core kernels (bf16, D = 128, block_size = 64) -----------------
 bool tc_supported(const Geo &g, int dtype);
-// tile_next: a device int that is zero when the kernel starts (its work counter)
+// tile_next: a device int that is zero when the kernel starts (its work counter).
+// after_validate: the launch directly follows the index validation kernel,
+// and becomes its programmatic dependent
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v,
-                          const int *idx, void *o, float *lse, int *err, int *tile_next, cudaStream_t st);
+                          const int *idx, void *o, float *lse, int *err, int *tile_next, bool after_validate,
+                          cudaStream_t st);
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,
                          const void *dO, const float *lse, const float *delta, const int *idx,
                          void *dq, int *err, int *tile_next, cudaStream_t st);

@@ -205,7 +205,7 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (mode == SPARSE)
         NSA_LAUNCH("validate_index", launch_validate_index(g, idx, &hdr->err, st));
     if (tc_supported(g, p->dtype))
-        NSA_LAUNCH("fwd_tc", launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, &hdr->tile_next, st));
+        NSA_LAUNCH("fwd_tc", launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, &hdr->tile_next, mode == SPARSE, st));
     else
         NSA_LAUNCH("fwd_simt", launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
     if (sinks)
@@ -306,8 +306,9 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (tc_supported(g, p->dtype)) {
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                partials, dk, dv, &hdr->err, st));
-        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
+        // dQ right after dK/dV: it is that kernel's programmatic dependent
         NSA_LAUNCH("dq_tc", launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, &hdr->tile_next, st));
+        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else {
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
         NSA_LAUNCH("dq_simt", launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <utility>
+
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -46,6 +48,28 @@ bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int
 
 // the host launcher's view of the device: SM count (cached)
 int num_sms();
+
+// Launches kernel as a programmatic dependent of the previous kernel on st:
+// it may start before that kernel completes (once that kernel's CTAs have
+// executed griddepcontrol.launch_dependents and resources free up), so it
+// must not read what that kernel writes.  Later launches on st still wait
+// for both.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- query-tile kernels (forward, dQ): a tile is Tq consecutive tokens of
 // one sequence times the G query heads of one kv head.
