@@ -592,6 +592,8 @@ __global__ void __launch_bounds__(kFillWarps * 32) csr_chunk_fill_kernel(Geo g, 
                                                                          int nchunks, const int *__restrict__ offsets,
                                                                          int *__restrict__ rows)
 {
+    // the dK/dV kernel launched next may start its set-up (it waits before reading the index)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned mask_all[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned *mask = mask_all + w * g.nbmax;  // lanes selecting block j

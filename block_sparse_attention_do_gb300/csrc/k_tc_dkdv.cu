@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     const int G = g.G;
     const int Tt = G >= kRows ? 1 : kRows / G;  // tokens per tile
     const int nrows = Tt * G;                  // used rows per tile
-    const int n_units = p.hdr->n_units;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -140,6 +139,11 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the kernel before it (the index
+    // build or delta): everything above overlapped that kernel; nothing it
+    // writes is read before this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_units = p.hdr->n_units;
     // The dQ kernel, launched next as a programmatic dependent, reads nothing
     // this kernel writes: let it take each SM as this kernel's CTA there ends.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -560,14 +564,14 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
         grid = max_units;
     if (grid < 1)
         grid = 1;
+    // a programmatic dependent of the kernel before it (see the kernel's wait)
     if (gather_tma) {
         cudaFuncSetAttribute(dkdv_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        dkdv_tc_kernel<true><<<grid, 352, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+        return launch_dependent(dkdv_tc_kernel<true>, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
     } else {
         cudaFuncSetAttribute(dkdv_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        dkdv_tc_kernel<false><<<grid, 352, SMEM_BYTES, st>>>(tq, tdo, tk, tv, p);
+        return launch_dependent(dkdv_tc_kernel<false>, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace nsa
