@@ -390,24 +390,29 @@ def _full_size_check(q, k, v, do, idx, bs, cu=None, dense=False, n_rows=24, n_ke
         assert np.max(np.abs(at(got["dv"], b, g, kk).double().cpu().numpy() - dv[i])) <= tol
     # identities over every output: sum_keys dV = sum of the group's dO over
     # rows that attend anything; sum_keys dK = 0 (rows of P sum to 1 and
-    # rows of dS sum to 0)
+    # rows of dS sum to 0).  Each dK/dV entry carries its bf16 rounding (at
+    # most 2^-9 of itself), so a sum may be off by up to 2^-9 sum_k |entry|:
+    # allowed twice that, and never less than 0.5.
     dvs, dks, dos = got["dv"].double().cpu(), got["dk"].double().cpu(), do.double()
     fin = torch.isfinite(got["lse"].cpu())
+
+    def check(dv_keys, dk_keys, want):
+        tv = torch.clamp(2.0 ** -8 * dv_keys.abs().sum(0), min=0.5)
+        tk = torch.clamp(2.0 ** -8 * dk_keys.abs().sum(0), min=0.5)
+        assert torch.all(torch.abs(dv_keys.sum(0) - want) <= tv)
+        assert torch.all(torch.abs(dk_keys.sum(0)) <= tk)
+
     if thd:
         for b in range(B):
             a, e = int(cu[b]), int(cu[b + 1])
             for g in range(Hkv):
                 sel = fin[a:e, g * G:(g + 1) * G].unsqueeze(-1)
-                want = (dos[a:e, g * G:(g + 1) * G] * sel).sum(dim=(0, 1))
-                assert torch.max(torch.abs(dvs[a:e, g].sum(0) - want)) < 0.5
-                assert torch.max(torch.abs(dks[a:e, g].sum(0))) < 0.5
+                check(dvs[a:e, g], dks[a:e, g], (dos[a:e, g * G:(g + 1) * G] * sel).sum(dim=(0, 1)))
     else:
         for b in range(B):
             for g in range(Hkv):
                 sel = fin[b, g * G:(g + 1) * G].unsqueeze(-1)
-                want = (dos[b, g * G:(g + 1) * G] * sel).sum(dim=(0, 1))
-                assert torch.max(torch.abs(dvs[b, g].sum(0) - want)) < 0.5
-                assert torch.max(torch.abs(dks[b, g].sum(0))) < 0.5
+                check(dvs[b, g], dks[b, g], (dos[b, g * G:(g + 1) * G] * sel).sum(dim=(0, 1)))
 
 
 def test_full_size_long_sequence_sampled():
@@ -415,6 +420,16 @@ def test_full_size_long_sequence_sampled():
     B, Hq, Hkv, T, D, bs, S = 1, 32, 2, 8192, 128, 64, 16
     q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=0)
     idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=0)
+    _full_size_check(q, k, v, do, idx, bs)
+
+
+def test_full_size_very_long_sequence_sampled():
+    """B=1 Hq=16 Hkv=1 T=65536 D=128 block 64 S=16, bf16: 1024 selectable
+    blocks per row, so the query-tile kernels' union buffers no longer fit
+    twice beside three K stages (the fewer-stage / single-buffer layouts)."""
+    B, Hq, Hkv, T, D, bs, S = 1, 16, 1, 65536, 128, 64, 16
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=3)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=3)
     _full_size_check(q, k, v, do, idx, bs)
 
 
