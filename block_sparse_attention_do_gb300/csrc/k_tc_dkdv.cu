@@ -12,14 +12,17 @@
 // several units writes fp32 partials that a separate kernel adds in unit
 // order; a block held by one unit writes dK/dV directly.
 //
-// Roles (11 warps):  warp 0 loads (TMA for K_j/V_j; Q/dO rows by one TMA box
-// per token -- its G heads, both halves -- when G % 8 == 0, else by 16-byte
-// cp.async with the swizzle applied by hand); warp 1 resolves each tile's
-// token ids, LSE and delta a tile ahead; warp 2 owns TMEM; one thread each
-// of warps 2, 8, 9 and 10 issues the S, dP, dV^T and dK^T MMAs; warps 4-7
-// compute P/dS for one row each and run the epilogue.  Two Q/dO stages
-// (row-group layout, so that a token's box is contiguous), two S/dP TMEM
-// buffers, one P/dS buffer.
+// Roles (11 warps):  warps 0 and 3 load (TMA for K_j/V_j; Q rows from warp 0
+// and dO rows from warp 3 by one TMA box per token -- its G heads, both
+// halves -- when G % 8 == 0, else both by 16-byte cp.async from warp 0 with
+// the swizzle applied by hand); warp 1 resolves each tile's token ids a tile
+// ahead; warp 2 owns TMEM; one thread each of warps 2, 8, 9 and 10 issues the
+// S, dP, dV^T and dK^T MMAs; warps 4-7 compute P/dS for one row each (reading
+// the row's LSE and delta themselves) and run the epilogue.  Q has three
+// stages and dO two (row-group layout, so that a token's box is contiguous):
+// a tile's Q is held from its load until dK^T has read it, its dO only from
+// its load until dV^T has, so the dO ring refills later and needs fewer
+// slots.  Two S/dP TMEM buffers, one P and one dS buffer.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -31,25 +34,27 @@ using namespace tc;
 // shared-memory plan (bytes from a 1024-aligned base)
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKvBytes;
-constexpr int OFF_Q = OFF_V + kKvBytes;          // 2 stages
-constexpr int OFF_DO = OFF_Q + 2 * kTileBytes;   // 2 stages
-constexpr int OFF_P = OFF_DO + 2 * kTileBytes;
+constexpr int NQ = 3;                            // Q stages
+constexpr int NDO = 2;                           // dO stages
+constexpr int OFF_Q = OFF_V + kKvBytes;
+constexpr int OFF_DO = OFF_Q + NQ * kTileBytes;
+constexpr int OFF_P = OFF_DO + NDO * kTileBytes;
 constexpr int OFF_DS = OFF_P + kRows * 128;
-constexpr int OFF_LSE = OFF_DS + kRows * 128;    // float [2][128], LSE * log2(e)
-constexpr int OFF_DLT = OFF_LSE + 2 * kRows * 4; // float [2][128]
-constexpr int OFF_TOK = OFF_DLT + 2 * kRows * 4; // int   [2][128]
-constexpr int OFF_BAR = OFF_TOK + 2 * kRows * 4;
-constexpr int NUM_BARS = 28;
+constexpr int OFF_TOK = OFF_DS + kRows * 128;    // int [NQ][128]: a tile's token ids, one slot per Q stage
+constexpr int OFF_BAR = OFF_TOK + NQ * kRows * 4;
+constexpr int NUM_BARS = 32;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
-// barrier slots
+// barrier slots (QFULL/QEMPTY/IDX per Q stage, DOFULL/DOEMPTY per dO stage)
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KVFULL, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_IDX0, B_IDX1, B_DPFULL0, B_DPFULL1,
+    B_QFULL0 = 0, B_QEMPTY0 = B_QFULL0 + NQ, B_IDX0 = B_QEMPTY0 + NQ, B_DOFULL0 = B_IDX0 + NQ,
+    B_DOEMPTY0 = B_DOFULL0 + NDO, B_KVFULL = B_DOEMPTY0 + NDO, B_KVEMPTY, B_SFULL0, B_SFULL1,
+    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DPFULL0, B_DPFULL1,
     B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
+static_assert(OFF_MISC + 64 + 1024 <= 232448, "shared memory");
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;     // S of buffer b at b*128, dP at b*128 + 64
@@ -91,8 +96,6 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     uint64_t *bars = (uint64_t *)(sm + OFF_BAR);
     volatile int *abort_flag = (volatile int *)(sm + OFF_MISC);
     uint32_t *tmem_slot = (uint32_t *)(sm + OFF_MISC + 16);
-    float *lse_s = (float *)(sm + OFF_LSE);
-    float *dlt_s = (float *)(sm + OFF_DLT);
     int *tok_s = (int *)(sm + OFF_TOK);
 
     const Geo &g = p.g;
@@ -103,12 +106,15 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[B_FULL0], GATHER_TMA ? 2 : 32);
-        mbar_init(&bars[B_FULL1], GATHER_TMA ? 2 : 32);
-        mbar_init(&bars[B_IDX0], 32);
-        mbar_init(&bars[B_IDX1], 32);
-        mbar_init(&bars[B_EMPTY0], 2);
-        mbar_init(&bars[B_EMPTY1], 2);
+        for (int x = 0; x < NQ; ++x) {
+            mbar_init(&bars[B_QFULL0 + x], GATHER_TMA ? 1 : 32);
+            mbar_init(&bars[B_QEMPTY0 + x], 1);  // dK^T's commit
+            mbar_init(&bars[B_IDX0 + x], 32);
+        }
+        for (int x = 0; x < NDO; ++x) {
+            mbar_init(&bars[B_DOFULL0 + x], GATHER_TMA ? 1 : 32);
+            mbar_init(&bars[B_DOEMPTY0 + x], 2);  // dP's and dV^T's commits
+        }
         mbar_init(&bars[B_KVFULL], 1);
         mbar_init(&bars[B_KVEMPTY], 2);
         mbar_init(&bars[B_SFULL0], 1);
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         tmem_relinquish();
     }
     // rows a tile never fills must hold finite values (they meet P = 0)
-    for (int i = threadIdx.x; i < (2 * kTileBytes * 2) / 16; i += blockDim.x)
+    for (int i = threadIdx.x; i < ((NQ + NDO) * kTileBytes) / 16; i += blockDim.x)
         *(uint4 *)(sm + OFF_Q + i * 16) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
@@ -151,11 +157,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     if (warp == 0 || (GATHER_TMA && warp == 3)) {
         // ------------------------------------------------------- tile loader
         // K_j / V_j once per unit (warp 0); per tile, once the indexer has
-        // published the tile's tokens, the Q and dO rows: by TMA when G % 8 ==
-        // 0, one box per token (its G heads, both halves), warp 0 the Q boxes
-        // and warp 3 the dO boxes (a box takes ~85 cycles to issue, so two
-        // warps halve the time to the tile's last one); else by 16-byte
-        // cp.async from warp 0 with the swizzle applied by hand.
+        // published the tile's tokens (it does so when the tile's Q stage is
+        // free), the Q and dO rows: by TMA when G % 8 == 0, one box per token
+        // (its G heads, both halves), warp 0 the Q boxes and warp 3 the dO
+        // boxes once the tile's dO stage is free (a box takes ~85 cycles to
+        // issue, so two warps halve the time to the tile's last one); else
+        // both by 16-byte cp.async from warp 0 with the swizzle applied by hand.
         const int tensor = warp == 3 ? 1 : 0;
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
         if (lane == 0) {
@@ -164,8 +171,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
         }
-        int it = 0, uc = 0;
-        int last_tile = -1, last_kv = -1;  // newest TMA batches (for the abort path)
+        int it = 0, uc = 0, qs = 0, qph = 0;  // tile count; its Q stage and that stage's phase
+        int last_tile = -1, last_kv = -1;     // newest TMA batches (for the abort path)
         bool okl = true;
         for (int ui; (ui = unit_of(uc, n_units)) >= 0 && okl; ++uc) {
             const Unit u = p.units[ui];
@@ -192,27 +199,31 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 }
             }
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
-                const int st = it & 1;
-                if (!mbar_wait_warp(&bars[B_IDX0 + st], (it >> 1) & 1, abort_flag)) {
+                const int ds = it & 1;  // dO stage
+                if (!mbar_wait_warp(&bars[B_IDX0 + qs], qph, abort_flag) ||
+                    ((tensor == 1 || !GATHER_TMA) &&
+                     !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag))) {
                     okl = false;
                     break;
                 }
                 const int ntok = min(Tt, u.count - ti * Tt);
+                const int *tok = tok_s + qs * kRows;
                 if (GATHER_TMA) {
+                    uint64_t *full = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
                     if (lane == 0) {
                         last_tile = it;
-                        mbar_arrive_expect_tx(&bars[B_FULL0 + st], nrows * 256);
+                        mbar_arrive_expect_tx(full, nrows * 256);
                     }
                     __syncwarp();
                     for (int tl = lane; tl < Tt; tl += 32) {
                         // rows past the list repeat the last token (finite data, P = 0)
-                        const int t = tok_s[st * kRows + min(tl, ntok - 1)];
-                        uint8_t *dst = sm + (tensor ? OFF_DO : OFF_Q) + st * kTileBytes + tl * G * 256;
+                        const int t = tok[min(tl, ntok - 1)];
+                        uint8_t *dst = sm + (tensor ? OFF_DO + ds * kTileBytes : OFF_Q + qs * kTileBytes) + tl * G * 256;
                         const CUtensorMap *map = tensor ? &tm_do : &tm_q;
                         if (g.thd)
-                            tma_load_5d(dst, map, &bars[B_FULL0 + st], 0, 0, 0, kvh * G / 8, g.cu[b] + t);
+                            tma_load_5d(dst, map, full, 0, 0, 0, kvh * G / 8, g.cu[b] + t);
                         else
-                            tma_load_5d(dst, map, &bars[B_FULL0 + st], 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
+                            tma_load_5d(dst, map, full, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
                     }
                 } else {
                     // 2 tensors x 128 rows x 16 chunks of 16 bytes
@@ -225,15 +236,20 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         const __nv_bfloat16 *base = tensor ? p.dO : p.q;
                         const __nv_bfloat16 *src = base;
                         if (valid)
-                            src = base + row_off(g, g.Hq, b, kvh * G + hh, tok_s[st * kRows + tl]) + c * 8;
-                        const uint32_t dst = (tensor ? do_s : q_s) + st * kTileBytes + rg_off(r, c >> 3) +
-                                             (((c & 7) ^ (r & 7)) << 4);
+                            src = base + row_off(g, g.Hq, b, kvh * G + hh, tok[tl]) + c * 8;
+                        const uint32_t dst = (tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes) +
+                                             rg_off(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4);
                         cp_async_16(dst, src, valid ? 16u : 0u);
                     }
                     cp_async_commit();
                     cp_async_wait<0>();
                     fence_async_smem();
-                    mbar_arrive(&bars[B_FULL0 + st]);
+                    mbar_arrive(&bars[B_QFULL0 + qs]);
+                    mbar_arrive(&bars[B_DOFULL0 + ds]);
+                }
+                if (++qs == NQ) {
+                    qs = 0;
+                    qph ^= 1;
                 }
             }
         }
@@ -242,48 +258,42 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         if (*abort_flag && lane == 0) {
             // let TMA copies still in flight land before the CTA exits
             volatile int never = 0;
-            if (last_tile >= 0)
-                mbar_wait(&bars[B_FULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
+            if (last_tile >= 0) {
+                if (tensor)
+                    mbar_wait(&bars[B_DOFULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
+                else
+                    mbar_wait(&bars[B_QFULL0 + last_tile % NQ], (last_tile / NQ) & 1, &never);
+            }
             if (last_kv >= 0)
                 mbar_wait(&bars[B_KVFULL], last_kv & 1, &never);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ indexer
-        // Resolves each tile's rows (token from the inverse index, LSE and
-        // delta) one tile ahead, into registers, while the stage it will fill
-        // is still busy; publishes them when the stage frees.  Lane l owns
-        // tile rows l, l + 32, l + 64, l + 96.
-        int it = 0;
+        // Resolves each tile's token ids from the inverse index one tile
+        // ahead, into registers, while the Q stage it will fill is still
+        // busy; publishes them when that stage frees.  Lane l owns the
+        // tile's tokens l, l + 32, l + 64, l + 96.
+        int qs = 0, qph = 0;
         int ku = 0, ti = 0;
         int ui = unit_of(0, n_units);
         Unit u;
-        int b = 0, kvh = 0, csr0 = 0, ntiles = 0;
+        int csr0 = 0, ntiles = 0;
         auto load_unit = [&]() {
             u = p.units[ui];
-            b = u.bg / g.Hkv;
-            kvh = u.bg % g.Hkv;
             csr0 = g.dense ? 0 : p.offsets[u.bg * g.nbmax + u.j] + u.begin;
             ntiles = (u.count + Tt - 1) / Tt;
         };
         int tok_r[4];
-        float l2_r[4], dl_r[4];
         auto fetch = [&]() {
             const int ntok = min(Tt, u.count - ti * Tt);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-                const int r = lane + k4 * 32;
-                const int tl = r / G, hh = r % G;
+                const int tl = lane + k4 * 32;
                 tok_r[k4] = -1;
-                l2_r[k4] = 0.f;
-                dl_r[k4] = 0.f;
-                if (r < nrows && tl < ntok) {
+                if (tl < ntok) {
                     const int pos = ti * Tt + tl;
-                    const int t = g.dense ? u.j * g.bs + u.begin + pos : p.rows[csr0 + pos];
-                    const int64_t so = stat_off(g, b, kvh * G + hh, t);
-                    tok_r[k4] = t;
-                    l2_r[k4] = p.lse[so] * 1.4426950408889634f;
-                    dl_r[k4] = p.delta[so];
+                    tok_r[k4] = g.dense ? u.j * g.bs + u.begin + pos : p.rows[csr0 + pos];
                 }
             }
         };
@@ -292,20 +302,18 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             fetch();
         }
         while (ui >= 0) {
-            const int st = it & 1;
-            if (!mbar_wait_warp(&bars[B_EMPTY0 + st], ((it >> 1) & 1) ^ 1, abort_flag))
+            if (!mbar_wait_warp(&bars[B_QEMPTY0 + qs], qph ^ 1, abort_flag))
                 break;
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int r = lane + k4 * 32;
-                lse_s[st * kRows + r] = l2_r[k4];
-                dlt_s[st * kRows + r] = dl_r[k4];
-                if (r % G == 0 && r / G < Tt)
-                    tok_s[st * kRows + r / G] = tok_r[k4];
+            for (int k4 = 0; k4 < 4; ++k4)
+                if (lane + k4 * 32 < Tt)
+                    tok_s[qs * kRows + lane + k4 * 32] = tok_r[k4];
+            mbar_arrive(&bars[B_IDX0 + qs]);
+            // next tile (possibly of the next unit): resolve its tokens now
+            if (++qs == NQ) {
+                qs = 0;
+                qph ^= 1;
             }
-            mbar_arrive(&bars[B_IDX0 + st]);
-            // next tile (possibly of the next unit): resolve its rows now
-            ++it;
             if (++ti == ntiles) {
                 ti = 0;
                 ui = unit_of(++ku, n_units);
@@ -320,8 +328,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         // Four issuing threads in four warps (one thread issues a tcgen05 MMA
         // only every ~150 cycles): warp 2 issues S, warp 8 dP, warp 9 dV^T (as
         // soon as P is in shared memory) and warp 10 dK^T (once dS is); each
-        // walks every (unit, tile).  Barriers shared by two of them count two
-        // commits: KVEMPTY (S and dP), EMPTY and ACCFULL (dV and dK).
+        // walks every (unit, tile).  KVEMPTY counts the S and dP commits,
+        // ACCFULL the dV and dK ones; a Q stage is free once dK^T of its tile
+        // is done, a dO stage once dP and dV^T of its tile are.
         if (lane == 0) {
             const int role = warp == 2 ? 0 : warp - 7;  // 0 S, 1 dP, 2 dV, 3 dK
             const uint32_t idS = idesc_bf16(128, 64, false, false);
@@ -330,18 +339,21 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const uint32_t k_s = smem_u32(sm + OFF_K), v_s = smem_u32(sm + OFF_V);
             const uint32_t p_s = smem_u32(sm + OFF_P), ds_s = smem_u32(sm + OFF_DS);
             // S / dP: A = Q / dO (row-group tile), B = K_j / V_j
-            const uint32_t a_s = role == 1 || role == 2 ? do_s : q_s;
+            const bool on_do = role == 1 || role == 2;
             const uint32_t b_s = role == 1 ? v_s : k_s;
-            int it = 0, uc = 0;
+            int it = 0, uc = 0, qs = 0, qph = 0;
             bool ok = true;
             for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
                 const int ntiles = (p.units[ui].count + Tt - 1) / Tt;
                 for (int ti = 0; ti < ntiles; ++ti, ++it) {
-                    const int st = it & 1;
+                    const int st = it & 1;  // S/dP TMEM buffer, and the dO stage
+                    const uint32_t a_s = on_do ? do_s + st * kTileBytes : q_s + qs * kTileBytes;
                     if (role <= 1) {
-                        // the tile's rows (and at a unit's start K_j / V_j) have
-                        // landed; the softmax has loaded S/dP of tile it - 2
-                        if (!mbar_wait(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
+                        // the tile's Q (S) or dO (dP) rows, and at a unit's start
+                        // K_j / V_j, have landed; the softmax has loaded S/dP of
+                        // tile it - 2
+                        if (!(role == 0 ? mbar_wait(&bars[B_QFULL0 + qs], qph, abort_flag)
+                                        : mbar_wait(&bars[B_DOFULL0 + st], (it >> 1) & 1, abort_flag)) ||
                             !mbar_wait(&bars[B_SFREE0 + st], ((it >> 1) & 1) ^ 1, abort_flag) ||
                             (ti == 0 && !mbar_wait(&bars[B_KVFULL], uc & 1, abort_flag))) {
                             ok = false;
@@ -352,16 +364,20 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
                             const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                            mma_bf16(col, sdesc_sw128(a_s + st * kTileBytes + ao, 16, kRgStride),
-                                     sdesc_sw128(b_s + bo, 16, 1024), idS, kk > 0);
+                            mma_bf16(col, sdesc_sw128(a_s + ao, 16, kRgStride), sdesc_sw128(b_s + bo, 16, 1024), idS,
+                                     kk > 0);
                         }
                         mma_commit(&bars[(role == 0 ? B_SFULL0 : B_DPFULL0) + st]);
+                        if (role == 1)
+                            mma_commit(&bars[B_DOEMPTY0 + st]);
                         if (ti + 1 == ntiles)
                             mma_commit(&bars[B_KVEMPTY]);
                     } else {
-                        // P (dV) or dS (dK) of the tile is in shared memory; at a
-                        // unit's start the epilogue has read the accumulators
+                        // P (dV) or dS (dK) of the tile is in shared memory (and
+                        // for dV the tile's dO rows have landed); at a unit's
+                        // start the epilogue has read the accumulators
                         if (!mbar_wait(&bars[role == 2 ? B_PFULL : B_DSFULL], it & 1, abort_flag) ||
+                            (role == 2 && !mbar_wait(&bars[B_DOFULL0 + st], (it >> 1) & 1, abort_flag)) ||
                             (ti == 0 && !mbar_wait(&bars[B_ACCEMPTY], (uc & 1) ^ 1, abort_flag))) {
                             ok = false;
                             break;
@@ -371,12 +387,16 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         const uint32_t pb = role == 2 ? p_s : ds_s;
                         for (int kr = 0; kr < kRows / 16; ++kr)
                             // 16 rows = two row groups; LBO steps the 64-dim halves (M)
-                            mma_bf16(col, sdesc_sw128(a_s + st * kTileBytes + kr * 2 * kRgStride, kRgHalf, kRgStride),
+                            mma_bf16(col, sdesc_sw128(a_s + kr * 2 * kRgStride, kRgHalf, kRgStride),
                                      sdesc_sw128(pb + kr * 2048, 8192, 1024), idV, (ti > 0 || kr > 0) ? 1u : 0u);
                         mma_commit(&bars[role == 2 ? B_PFREE : B_DSFREE]);
-                        mma_commit(&bars[B_EMPTY0 + st]);
+                        mma_commit(&bars[role == 2 ? B_DOEMPTY0 + st : B_QEMPTY0 + qs]);
                         if (ti + 1 == ntiles)
                             mma_commit(&bars[B_ACCFULL]);
+                    }
+                    if (++qs == NQ) {
+                        qs = 0;
+                        qph ^= 1;
                     }
                 }
             }
@@ -393,9 +413,41 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t p_row = smem_u32(sm + OFF_P) + r * 128;
         const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
+        // The next tile's token and raw LSE / delta for this thread's row,
+        // read halfway through the tile before, so that the loads' latency
+        // stays off the softmax's path.  (pq, pph): the next tile's Q stage
+        // and phase; (pu, pti, p_ui): its unit and tile within the unit.
+        int pq = 0, pph = 0, pu = 0, pti = 0;
+        int p_ui = unit_of(0, n_units);
+        int ptok = -1;
+        float plse = 0.f, pdlt = 0.f;
+        auto prefetch = [&]() -> bool {
+            if (p_ui < 0)
+                return true;
+            const Unit nu = p.units[p_ui];
+            if (!mbar_wait_warp(&bars[B_IDX0 + pq], pph, abort_flag))
+                return false;
+            ptok = r < nrows ? tok_s[pq * kRows + r / G] : -1;
+            plse = 0.f;
+            pdlt = 0.f;
+            if (ptok >= 0) {
+                const int64_t so = stat_off(g, nu.bg / g.Hkv, (nu.bg % g.Hkv) * G + r % G, ptok);
+                plse = p.lse[so];
+                pdlt = p.delta[so];
+            }
+            if (++pq == NQ) {
+                pq = 0;
+                pph ^= 1;
+            }
+            if (++pti == (nu.count + Tt - 1) / Tt) {
+                pti = 0;
+                p_ui = unit_of(++pu, n_units);
+            }
+            return true;
+        };
         int it = 0, uc = 0;
-        bool ok = true;
-        for (int ui; (ui = unit_of(uc, n_units)) >= 0 && ok; ++uc) {
+        bool ok = prefetch();
+        for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int L = seq_len(g, b);
@@ -403,15 +455,13 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const int ntiles = (u.count + Tt - 1) / Tt;
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
                 const int st = it & 1;
-                if (!mbar_wait_warp(&bars[B_FULL0 + st], (it >> 1) & 1, abort_flag) ||
-                    !mbar_wait_warp(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                const int tok = ptok;
+                const float l2 = plse * 1.4426950408889634f, dl = pdlt;
+                if (!mbar_wait_warp(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int tl = r / G;
-                const int tok = (r < nrows) ? tok_s[st * kRows + tl] : -1;
-                const float l2 = lse_s[st * kRows + r], dl = dlt_s[st * kRows + r];
                 // keys k0 + c with lo <= c <= tok - k0 are attended (the token selected block j)
                 const int lim = tok < 0 ? -1 : tok - k0;
                 const int lo = tok < 0 ? 0 : key_lo(g, tok) - k0;  // window's left edge
@@ -452,6 +502,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 fence_async_smem();
                 mbar_arrive(&bars[B_PFULL]);
+                if (!prefetch()) {
+                    ok = false;
+                    break;
+                }
                 // dS = P (dP - delta)
                 if (!mbar_wait_warp(&bars[B_DPFULL0 + st], (it >> 1) & 1, abort_flag)) {
                     ok = false;
