@@ -22,7 +22,8 @@
 // stages and dO two (row-group layout, so that a token's box is contiguous):
 // a tile's Q is held from its load until dK^T has read it, its dO only from
 // its load until dV^T has, so the dO ring refills later and needs fewer
-// slots.  Two S/dP TMEM buffers, one P and one dS buffer.
+// slots.  Three S/dP TMEM buffers (so S and dP run up to two tiles ahead of
+// the softmax), one P and one dS buffer.
 #include "tc_common.cuh"
 
 namespace nsa {
@@ -36,30 +37,32 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKvBytes;
 constexpr int NQ = 3;                            // Q stages
 constexpr int NDO = 2;                           // dO stages
+constexpr int NSB = 3;                           // S/dP TMEM buffers
 constexpr int OFF_Q = OFF_V + kKvBytes;
 constexpr int OFF_DO = OFF_Q + NQ * kTileBytes;
 constexpr int OFF_P = OFF_DO + NDO * kTileBytes;
 constexpr int OFF_DS = OFF_P + kRows * 128;
 constexpr int OFF_TOK = OFF_DS + kRows * 128;    // int [NQ][128]: a tile's token ids, one slot per Q stage
 constexpr int OFF_BAR = OFF_TOK + NQ * kRows * 4;
-constexpr int NUM_BARS = 32;
+constexpr int NUM_BARS = 34;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
-// barrier slots (QFULL/QEMPTY/IDX per Q stage, DOFULL/DOEMPTY per dO stage)
+// barrier slots (QFULL/QEMPTY/IDX per Q stage, DOFULL/DOEMPTY per dO stage,
+// SFULL/SFREE/DPFULL per S/dP buffer)
 enum {
     B_QFULL0 = 0, B_QEMPTY0 = B_QFULL0 + NQ, B_IDX0 = B_QEMPTY0 + NQ, B_DOFULL0 = B_IDX0 + NQ,
-    B_DOEMPTY0 = B_DOFULL0 + NDO, B_KVFULL = B_DOEMPTY0 + NDO, B_KVEMPTY, B_SFULL0, B_SFULL1,
-    B_SFREE0, B_SFREE1, B_PFULL, B_PFREE, B_ACCFULL, B_ACCEMPTY, B_DPFULL0, B_DPFULL1,
-    B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_COUNT
+    B_DOEMPTY0 = B_DOFULL0 + NDO, B_KVFULL = B_DOEMPTY0 + NDO, B_KVEMPTY, B_SFULL0,
+    B_SFREE0 = B_SFULL0 + NSB, B_DPFULL0 = B_SFREE0 + NSB, B_PFULL = B_DPFULL0 + NSB, B_PFREE, B_ACCFULL,
+    B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 static_assert(OFF_MISC + 64 + 1024 <= 232448, "shared memory");
 
 // TMEM columns
-constexpr uint32_t TM_S = 0;     // S of buffer b at b*128, dP at b*128 + 64
-constexpr uint32_t TM_DV = 256;  // dV^T: 128 lanes (d) x 64 columns (keys)
-constexpr uint32_t TM_DK = 320;  // dK^T
+constexpr uint32_t TM_S = 0;                // S of buffer b at b*128, dP at b*128 + 64
+constexpr uint32_t TM_DV = NSB * 128;       // dV^T: 128 lanes (d) x 64 columns (keys)
+constexpr uint32_t TM_DK = TM_DV + 64;      // dK^T
 constexpr uint32_t TM_COLS = 512;
 
 struct Params {
@@ -117,12 +120,11 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         }
         mbar_init(&bars[B_KVFULL], 1);
         mbar_init(&bars[B_KVEMPTY], 2);
-        mbar_init(&bars[B_SFULL0], 1);
-        mbar_init(&bars[B_DPFULL0], 1);
-        mbar_init(&bars[B_DPFULL1], 1);
-        mbar_init(&bars[B_SFULL1], 1);
-        mbar_init(&bars[B_SFREE0], kRows);
-        mbar_init(&bars[B_SFREE1], kRows);
+        for (int x = 0; x < NSB; ++x) {
+            mbar_init(&bars[B_SFULL0 + x], 1);
+            mbar_init(&bars[B_DPFULL0 + x], 1);
+            mbar_init(&bars[B_SFREE0 + x], kRows);
+        }
         mbar_init(&bars[B_PFULL], kRows);
         mbar_init(&bars[B_PFREE], 1);
         mbar_init(&bars[B_DSFULL], kRows);
@@ -341,33 +343,33 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             // S / dP: A = Q / dO (row-group tile), B = K_j / V_j
             const bool on_do = role == 1 || role == 2;
             const uint32_t b_s = role == 1 ? v_s : k_s;
-            int it = 0, uc = 0, qs = 0, qph = 0;
+            int it = 0, uc = 0, qs = 0, qph = 0, tb = 0, tph = 0;  // (tb, tph): S/dP buffer and its phase
             bool ok = true;
             for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
                 const int ntiles = (p.units[ui].count + Tt - 1) / Tt;
                 for (int ti = 0; ti < ntiles; ++ti, ++it) {
-                    const int st = it & 1;  // S/dP TMEM buffer, and the dO stage
+                    const int st = it & 1;  // dO stage
                     const uint32_t a_s = on_do ? do_s + st * kTileBytes : q_s + qs * kTileBytes;
                     if (role <= 1) {
                         // the tile's Q (S) or dO (dP) rows, and at a unit's start
                         // K_j / V_j, have landed; the softmax has loaded S/dP of
-                        // tile it - 2
+                        // tile it - NSB
                         if (!(role == 0 ? mbar_wait(&bars[B_QFULL0 + qs], qph, abort_flag)
                                         : mbar_wait(&bars[B_DOFULL0 + st], (it >> 1) & 1, abort_flag)) ||
-                            !mbar_wait(&bars[B_SFREE0 + st], ((it >> 1) & 1) ^ 1, abort_flag) ||
+                            !mbar_wait(&bars[B_SFREE0 + tb], tph ^ 1, abort_flag) ||
                             (ti == 0 && !mbar_wait(&bars[B_KVFULL], uc & 1, abort_flag))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t col = tmem + TM_S + st * 128 + role * 64;
+                        const uint32_t col = tmem + TM_S + tb * 128 + role * 64;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
                             const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
                             mma_bf16(col, sdesc_sw128(a_s + ao, 16, kRgStride), sdesc_sw128(b_s + bo, 16, 1024), idS,
                                      kk > 0);
                         }
-                        mma_commit(&bars[(role == 0 ? B_SFULL0 : B_DPFULL0) + st]);
+                        mma_commit(&bars[(role == 0 ? B_SFULL0 : B_DPFULL0) + tb]);
                         if (role == 1)
                             mma_commit(&bars[B_DOEMPTY0 + st]);
                         if (ti + 1 == ntiles)
@@ -397,6 +399,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     if (++qs == NQ) {
                         qs = 0;
                         qph ^= 1;
+                    }
+                    if (++tb == NSB) {
+                        tb = 0;
+                        tph ^= 1;
                     }
                 }
             }
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             }
             return true;
         };
-        int it = 0, uc = 0;
+        int it = 0, uc = 0, tb = 0, tph = 0;  // (tb, tph): S/dP buffer and its phase
         bool ok = prefetch();
         for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
             const Unit u = p.units[ui];
@@ -454,10 +460,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const int k0 = u.j * kKeys;
             const int ntiles = (u.count + Tt - 1) / Tt;
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
-                const int st = it & 1;
                 const int tok = ptok;
                 const float l2 = plse * 1.4426950408889634f, dl = pdlt;
-                if (!mbar_wait_warp(&bars[B_SFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_SFULL0 + tb], tph, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 const int lo = tok < 0 ? 0 : key_lo(g, tok) - k0;  // window's left edge
                 // P from S while dP is still running
                 uint32_t pv[64];
-                tmem_ld64(lane_base + TM_S + st * 128, pv);
+                tmem_ld64(lane_base + TM_S + tb * 128, pv);
                 tmem_wait_ld();
                 if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
                     // no row of the warp ends or starts inside the block: a row
@@ -507,16 +512,20 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     break;
                 }
                 // dS = P (dP - delta)
-                if (!mbar_wait_warp(&bars[B_DPFULL0 + st], (it >> 1) & 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_DPFULL0 + tb], tph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 uint32_t dv_[64];
-                tmem_ld64(lane_base + TM_S + st * 128 + 64, dv_);
+                tmem_ld64(lane_base + TM_S + tb * 128 + 64, dv_);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&bars[B_SFREE0 + st]);
+                mbar_arrive(&bars[B_SFREE0 + tb]);
+                if (++tb == NSB) {
+                    tb = 0;
+                    tph ^= 1;
+                }
                 uint32_t dk_[32];
                 const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
