@@ -44,7 +44,7 @@ constexpr int OFF_P = OFF_DO + NDO * kTileBytes;
 constexpr int OFF_DS = OFF_P + kRows * 128;
 constexpr int OFF_TOK = OFF_DS + kRows * 128;    // int [NQ][128]: a tile's token ids, one slot per Q stage
 constexpr int OFF_BAR = OFF_TOK + NQ * kRows * 4;
-constexpr int NUM_BARS = 34;
+constexpr int NUM_BARS = 36;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
@@ -54,7 +54,7 @@ enum {
     B_QFULL0 = 0, B_QEMPTY0 = B_QFULL0 + NQ, B_IDX0 = B_QEMPTY0 + NQ, B_DOFULL0 = B_IDX0 + NQ,
     B_DOEMPTY0 = B_DOFULL0 + NDO, B_KVFULL = B_DOEMPTY0 + NDO, B_KVEMPTY, B_SFULL0,
     B_SFREE0 = B_SFULL0 + NSB, B_DPFULL0 = B_SFREE0 + NSB, B_PFULL = B_DPFULL0 + NSB, B_PFREE, B_ACCFULL,
-    B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_COUNT
+    B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_STAGED, B_COPIED, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 static_assert(OFF_MISC + 64 + 1024 <= 232448, "shared memory");
@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         mbar_init(&bars[B_DSFREE], 1);
         mbar_init(&bars[B_ACCFULL], 2);
         mbar_init(&bars[B_ACCEMPTY], kRows);
+        mbar_init(&bars[B_STAGED], kRows);
+        mbar_init(&bars[B_COPIED], kRows);
         for (int x = 0; x < 4; ++x)
             mbar_init(&bars[B_DONE0 + x], 1);
         fence_barrier_init();
@@ -452,6 +454,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             return true;
         };
         int it = 0, uc = 0, tb = 0, tph = 0;  // (tb, tph): S/dP buffer and its phase
+        int ep = 0;                           // staged (direct) epilogues so far
         bool ok = prefetch();
         for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
             const Unit u = p.units[ui];
@@ -548,7 +551,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             }
             if (!ok)
                 break;
-            // ---- epilogue: lane = head dimension d, columns = keys
+            // ---- epilogue: lane = head dimension d, columns = keys.  A split
+            // block's fp32 partials go out directly (each warp store covers
+            // 128 contiguous bytes); a whole block's bf16 dK/dV rows are first
+            // staged in the idle dS / P buffers (thread d writes column d) and
+            // then written as whole 256-byte rows with 16-byte stores, since
+            // 2-byte stores, 64 bytes per warp, drain many times slower.
             if (!mbar_wait_warp(&bars[B_ACCFULL], uc & 1, abort_flag)) {
                 ok = false;
                 break;
@@ -556,6 +564,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             tc_fence_after();
             const int d = r;
             const int nk = min(kKeys, L - k0);
+            const bool direct = u.slot < 0;
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which == 0 ? TM_DK : TM_DV;
                 const float mul = which == 0 ? g.scale : 1.f;
@@ -564,21 +573,44 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 for (int c = 0; c < 4; ++c)
                     tmem_ld16(lane_base + col + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&a[c * 16]));
                 tmem_wait_ld();
-                if (u.slot >= 0) {
+                if (!direct) {
                     float *dst = p.partials + ((int64_t)u.slot * 2 + which) * kKeys * kHead + d;
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
                         dst[c * kHead] = __uint_as_float(a[c]) * mul;
                 } else {
-                    __nv_bfloat16 *out = which == 0 ? p.dk : p.dv;
-                    __nv_bfloat16 *o0 = out + row_off(g, g.Hkv, b, kvh, k0) + d;
-                    // distance between consecutive keys: D (BHTD) or Hkv*D (THD)
-                    const int64_t kstride = g.thd ? (int64_t)g.Hkv * kHead : kHead;
+                    // dS buffer holds dK, P buffer dV: [64 keys][128 dims] bf16
+                    __nv_bfloat16 *stage = (__nv_bfloat16 *)(sm + (which == 0 ? OFF_DS : OFF_P)) + d;
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (c < nk)
-                            o0[c * kstride] = __float2bfloat16_rn(__uint_as_float(a[c]) * mul);
+                        stage[c * kHead] = __float2bfloat16_rn(__uint_as_float(a[c]) * mul);
                 }
+            }
+            if (direct) {
+                // every row staged: copy both tensors out, 16 bytes per thread and step
+                mbar_arrive(&bars[B_STAGED]);
+                if (!mbar_wait_warp(&bars[B_STAGED], ep & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // distance between consecutive keys: D (BHTD) or Hkv*D (THD)
+                const int64_t kstride = g.thd ? (int64_t)g.Hkv * kHead : kHead;
+#pragma unroll 4
+                for (int q = r; q < 2 * kKeys * 16; q += kRows) {
+                    const int which = q / (kKeys * 16), c = (q >> 4) & (kKeys - 1), ch = q & 15;
+                    if (c < nk) {
+                        __nv_bfloat16 *out = (which == 0 ? p.dk : p.dv) + row_off(g, g.Hkv, b, kvh, k0) + c * kstride;
+                        *(uint4 *)(out + ch * 8) =
+                            *(const uint4 *)(sm + (which == 0 ? OFF_DS : OFF_P) + c * (kHead * 2) + ch * 16);
+                    }
+                }
+                // the buffers take the next unit's P and dS only after every thread's copy
+                mbar_arrive(&bars[B_COPIED]);
+                if (!mbar_wait_warp(&bars[B_COPIED], ep & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++ep;
             }
             tc_fence_before();
             mbar_arrive(&bars[B_ACCEMPTY]);

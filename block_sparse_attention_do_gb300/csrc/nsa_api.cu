@@ -85,8 +85,10 @@ PlanLayout plan_layout(const Geo &g)
 {
     PlanLayout w;
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
-    // tokens per dK/dV unit: 64 row tiles of the tensor-core kernel
-    w.chunk = tiles_tokens(g) * 64;
+    // tokens per dK/dV unit: 128 row tiles of the tensor-core kernel (longer
+    // units mean fewer accumulator drains and split-block partials; the dQ
+    // kernel launched behind dK/dV takes the SMs its uneven end leaves)
+    w.chunk = tiles_tokens(g) * 128;
     // upper bound on list entries; dense: a row of sequence-local token t
     // attends t/bs + 1 <= nbmax/2 + 1 blocks on average over a sequence
     const int64_t sel_total = g.dense ? (int64_t)g.ntok * g.Hkv * (g.nbmax / 2 + 1) : (int64_t)g.ntok * g.Hkv * g.S;
