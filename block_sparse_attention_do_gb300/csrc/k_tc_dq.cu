@@ -174,13 +174,15 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             prefetch_tmap(&tm_v);
         }
         int lastq = -1, lastd = -1, last = -1, lastv = -1, gi = 0;
+        int claimed = qtile_claim(p.tile_next, lane);
         for (int k = 0;; ++k) {
-            // The tile and its block union: this warp deals the tiles and builds
-            // each union after issuing the previous tile's copies, while the
-            // K/V rings still hold several of that tile's pairs; after the last
-            // tile a header with a negative count tells the other roles to stop.
+            // The tile and its block union: this warp deals the tiles (each
+            // claimed a tile ahead) and builds each union after issuing the
+            // previous tile's copies, while the K/V rings still hold several of
+            // that tile's pairs; after the last tile a header with a negative
+            // count tells the other roles to stop.
             int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, p.tile_next, lane, b, kvh, t0, nvalid);
+            const bool more = qtile_take(g, p.ntiles, p.tile_next, lane, claimed, b, kvh, t0, nvalid);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
             if (more) {
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             mbar_arrive(&bars[B_UFULL0 + k % nub]);
             if (!more)
                 break;
+            claimed = qtile_claim(p.tile_next, lane);
             const int U = u_hdr(k)[UH_COUNT];
             const int *list = union_list(u_buf(k), up);
             // Q once the previous tile's last S has run, dO once its last dP has
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             nU = hdr[UH_COUNT];
             if (nU >= 0 && r < nrows && tl < hdr[UH_NVALID]) {
                 const int64_t so = stat_off(g, hdr[UH_B], hdr[UH_KVH] * G + hh, hdr[UH_T0] + tl);
-                nl2 = p.lse[so] * 1.4426950408889634f;
+                nl2 = p.lse[so];  // scaled by log2(e) at use, so the load does not stall here
                 ndl = p.delta[so];
             }
         };
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         for (int k = 0; nU >= 0; ++k) {
             const volatile int *hdr = u_hdr(k);
             const int U = nU, b = hdr[UH_B], kvh = hdr[UH_KVH], t0 = hdr[UH_T0], nvalid = hdr[UH_NVALID];
-            const float l2 = nl2, dl = ndl;
+            const float l2 = nl2 * 1.4426950408889634f, dl = ndl;
             const int *list = union_list(u_buf(k), up);
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;

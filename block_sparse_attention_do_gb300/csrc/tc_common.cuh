@@ -134,15 +134,19 @@ __device__ __forceinline__ int *union_list(int *buf, const UnionBuf &u)
 // latest tokens) go first and a CTA that finishes early takes more.  Tiles
 // past a sequence's end are skipped.  False once the counter passes the tile
 // count.  Called by all lanes of one warp.
-__device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int *next, int lane, int &b, int &kvh,
-                                           int &t0, int &nvalid)
+// Claims a tile index from the launch-wide counter *next: lane 0's value,
+// 0 on the other lanes.  A claim issued early keeps the counter's round trip
+// off the path; qtile_take turns it into a tile.
+__device__ __forceinline__ int qtile_claim(int *next, int lane) { return lane == 0 ? atomicAdd(next, 1) : 0; }
+
+// The tile of a claim (lane 0's `claimed`), claiming again past tiles that
+// lie beyond a shorter sequence's end; false once the tiles are used up.
+__device__ __forceinline__ bool qtile_take(const Geo &g, int ntiles, int *next, int lane, int claimed, int &b,
+                                           int &kvh, int &t0, int &nvalid)
 {
     const int Tq = tile_tokens(g.G), per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
     for (;;) {
-        int L = 0;
-        if (lane == 0)
-            L = atomicAdd(next, 1);
-        L = __shfl_sync(0xffffffffu, L, 0);
+        const int L = __shfl_sync(0xffffffffu, claimed, 0);
         if (L >= ntiles)
             return false;
         const int bg = L % nbg, tile = per_seq - 1 - L / nbg;
@@ -154,7 +158,14 @@ __device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int *next, 
             nvalid = min(Tq, len - t0);
             return true;
         }
+        claimed = qtile_claim(next, lane);
     }
+}
+
+__device__ __forceinline__ bool qtile_next(const Geo &g, int ntiles, int *next, int lane, int &b, int &kvh,
+                                           int &t0, int &nvalid)
+{
+    return qtile_take(g, ntiles, next, lane, qtile_claim(next, lane), b, kvh, t0, nvalid);
 }
 
 // One warp fills buf for a tile: each token's block bitmap, the ascending
@@ -178,13 +189,24 @@ __device__ __forceinline__ void qtile_union_warp(const Geo &g, const int *idx, c
         for (int j = jmin + lane; j <= jmax; j += 32)
             atomicOr(&ubits[j >> 5], 1u << (j & 31));
     } else {
-        for (int x = lane; x < nvalid * g.S; x += 32) {
-            const int tl = x / g.S, s = x % g.S;
-            const int t = t0 + tl;
-            const int j = idx_row(g, idx, b, kvh, t)[s];
-            if (j >= 0 && j <= t / g.bs && j < g.nbmax) {
-                atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
-                atomicOr(&ubits[j >> 5], 1u << (j & 31));
+        // four index entries per lane read at a time, all loads in flight
+        // together, then recorded
+        const int n = nvalid * g.S;
+        for (int x0 = 0; x0 < n; x0 += 128) {
+            int jv[4];
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int x = x0 + u4 * 32 + lane;
+                jv[u4] = x < n ? idx_row(g, idx, b, kvh, t0 + x / g.S)[x % g.S] : -1;
+            }
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int x = x0 + u4 * 32 + lane;
+                const int tl = x / g.S, t = t0 + tl, j = jv[u4];
+                if (x < n && j >= 0 && j <= t / g.bs && j < g.nbmax) {
+                    atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
+                    atomicOr(&ubits[j >> 5], 1u << (j & 31));
+                }
             }
         }
     }
