@@ -149,9 +149,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Launched as a programmatic dependent of the kernel before it (the index
-    // build or delta): everything above overlapped that kernel; nothing it
-    // writes is read before this wait.
+    // Launched as a programmatic dependent of the kernel before it (the
+    // query-tile unions, whose completion implies the index build's; or the
+    // index build or delta): everything above overlapped that kernel; nothing
+    // it or an earlier launch writes is read before this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_units = p.hdr->n_units;
     // The dQ kernel, launched next as a programmatic dependent, reads nothing

@@ -67,6 +67,7 @@ constexpr uint32_t TM_COLS = 512;
 struct Params {
     Geo g;
     const int *idx;
+    const int *utable;  // every tile's union buffer, built by qtile_union_kernel (null: built here)
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     int *err;
@@ -181,11 +182,20 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             // previous tile's copies, while the K/V rings still hold several of
             // that tile's pairs; after the last tile a header with a negative
             // count tells the other roles to stop.
-            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_take(g, p.ntiles, p.tile_next, lane, claimed, b, kvh, t0, nvalid);
+            int b = 0, kvh = 0, t0 = 0, nvalid = 0, L = 0;
+            const bool more = qtile_take(g, p.ntiles, p.tile_next, lane, claimed, b, kvh, t0, nvalid, &L);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
-            if (more) {
+            if (more && p.utable) {
+                // the union was built before this kernel (qtile_union_kernel):
+                // copy its buffer in, 16 bytes per lane and step
+                const uint4 *src = (const uint4 *)(p.utable + (int64_t)L * (up.bytes / 4));
+                uint4 *dst = (uint4 *)u_buf(k);
+                for (int x = lane; x < up.bytes / 16; x += 32)
+                    dst[x] = src[x];
+                __syncwarp();
+            } else if (more) {
+                // a dense entry's union is a block range: cheap to build here
                 qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
             } else {
                 if (lane == 0)
@@ -538,9 +548,61 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
 
 }  // namespace
 
+namespace {
+
+// Every query tile's union buffer, one warp per tile (built in shared memory,
+// then copied out whole).  A programmatic dependent of the kernel before it:
+// it reads only the index, so it runs alongside that kernel, and waits for
+// it at the end so that its own completion implies that kernel's.
+__global__ void __launch_bounds__(256) qtile_union_kernel(Geo g, const int *__restrict__ idx, int ntiles,
+                                                          UnionBuf up, int *__restrict__ utable)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ int ubuf_all[];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *buf = ubuf_all + w * (up.bytes / 4);
+    for (int L = blockIdx.x * (blockDim.x >> 5) + w; L < ntiles; L += gridDim.x * (blockDim.x >> 5)) {
+        int b, kvh, t0, nvalid;
+        if (!qtile_of(g, L, b, kvh, t0, nvalid))
+            continue;  // never taken
+        qtile_union_warp(g, idx, up, buf, b, kvh, t0, nvalid, lane);
+        uint4 *dst = (uint4 *)(utable + (int64_t)L * (up.bytes / 4));
+        for (int x = lane; x < up.bytes / 16; x += 32)
+            dst[x] = ((const uint4 *)buf)[x];
+        __syncwarp();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace
+
+size_t qtile_union_table_bytes(const Geo &g)
+{
+    if (g.dense || !qtile_shape_ok(g))
+        return 0;
+    const int Tq = tile_tokens(g.G);
+    return (size_t)((g.T + Tq - 1) / Tq) * g.B * g.Hkv * union_buf(g).bytes;
+}
+
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st)
+{
+    if (qtile_union_table_bytes(g) == 0)
+        return cudaSuccess;
+    const int Tq = tile_tokens(g.G);
+    const int ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
+    const UnionBuf up = union_buf(g);
+    const int grid = (ntiles + 7) / 8;
+    if (grid < 1)
+        return cudaSuccess;
+    const size_t smem = (size_t)8 * up.bytes;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(qtile_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return launch_dependent(qtile_union_kernel, dim3(grid), dim3(256), smem, st, g, idx, ntiles, up, utable);
+}
+
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
-                         const float *lse, const float *delta, const int *idx, void *dq, int *err,
-                         int *tile_next, cudaStream_t st)
+                         const float *lse, const float *delta, const int *idx, const int *utable, void *dq,
+                         int *err, int *tile_next, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
@@ -568,6 +630,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     Params p;
     p.g = g;
     p.idx = idx;
+    p.utable = utable;
     p.lse = lse;
     p.delta = delta;
     p.dq = (__nv_bfloat16 *)dq;

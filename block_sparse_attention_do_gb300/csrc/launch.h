@@ -66,9 +66,16 @@ bool tc_supported(const Geo &g, int dtype);
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v,
                           const int *idx, void *o, float *lse, int *err, int *tile_next, bool after_validate,
                           cudaStream_t st);
+// every query tile's block union for the dQ kernel, into utable
+// (qtile_union_table_bytes(g) bytes; 0, and no launch, for the dense entries,
+// whose unions are block ranges the dQ kernel builds itself); a
+// programmatic dependent of the kernel before it on st
+size_t qtile_union_table_bytes(const Geo &g);
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st);
+// utable: the union table launch_qtile_unions wrote, or null (dense entries)
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,
                          const void *dO, const float *lse, const float *delta, const int *idx,
-                         void *dq, int *err, int *tile_next, cudaStream_t st);
+                         const int *utable, void *dq, int *err, int *tile_next, cudaStream_t st);
 cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const void *v,
                            const void *dO, const float *lse, const float *delta,
                            const int *offsets, const int *rows, const Unit *units,

@@ -117,7 +117,7 @@ PlanLayout plan_layout(const Geo &g)
 // Backward workspace: header (error word) | delta fp32 [rows] | fp32 dK/dV
 // partials (tensor-core path) | the plan, unless the call is given one.
 struct BwdWs {
-    size_t delta, partials, plan, total;
+    size_t delta, partials, utable, plan, total;
     PlanLayout pl;
 };
 
@@ -131,6 +131,9 @@ BwdWs bwd_layout(const Geo &g, int dtype)
     w.partials = off;
     if (tc_supported(g, dtype))
         off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.pl.max_units);
+    w.utable = off;  // the dQ kernel's query-tile unions
+    if (tc_supported(g, dtype))
+        off = align_up(off + qtile_union_table_bytes(g));
     w.plan = off;
     w.total = off + w.pl.total;
     return w;
@@ -306,10 +309,16 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr)) != NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
+        // the query-tile unions (sparse only): alongside the kernel before,
+        // since they read only the index
+        int *utable = qtile_union_table_bytes(g) ? (int *)(w8 + L.utable) : nullptr;
+        if (utable)
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st));
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                partials, dk, dv, &hdr->err, st));
         // dQ right after dK/dV: it is that kernel's programmatic dependent
-        NSA_LAUNCH("dq_tc", launch_dq_tc(g, q, k, v, dO, lse, delta, idx, dq, &hdr->err, &hdr->tile_next, st));
+        NSA_LAUNCH("dq_tc",
+                   launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, dq, &hdr->err, &hdr->tile_next, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else {
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));

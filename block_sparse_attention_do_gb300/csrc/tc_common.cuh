@@ -139,23 +139,34 @@ __device__ __forceinline__ int *union_list(int *buf, const UnionBuf &u)
 // off the path; qtile_take turns it into a tile.
 __device__ __forceinline__ int qtile_claim(int *next, int lane) { return lane == 0 ? atomicAdd(next, 1) : 0; }
 
-// The tile of a claim (lane 0's `claimed`), claiming again past tiles that
-// lie beyond a shorter sequence's end; false once the tiles are used up.
-__device__ __forceinline__ bool qtile_take(const Geo &g, int ntiles, int *next, int lane, int claimed, int &b,
-                                           int &kvh, int &t0, int &nvalid)
+// Tile L's coordinates: (b, kv head) = L % (B*Hkv), tokens t0 .. t0+nvalid-1
+// counted from the sequence's end; false for a tile past a shorter
+// sequence's end (nothing to do).
+__device__ __forceinline__ bool qtile_of(const Geo &g, int L, int &b, int &kvh, int &t0, int &nvalid)
 {
     const int Tq = tile_tokens(g.G), per_seq = (g.T + Tq - 1) / Tq, nbg = g.B * g.Hkv;
+    const int bg = L % nbg, tile = per_seq - 1 - L / nbg;
+    b = bg / g.Hkv;
+    kvh = bg % g.Hkv;
+    t0 = tile * Tq;
+    const int len = seq_len(g, b);
+    nvalid = t0 < len ? min(Tq, len - t0) : 0;
+    return nvalid > 0;
+}
+
+// The tile of a claim (lane 0's `claimed`), claiming again past tiles that
+// lie beyond a shorter sequence's end; false once the tiles are used up.
+// *Lout (if given) receives the tile's index.
+__device__ __forceinline__ bool qtile_take(const Geo &g, int ntiles, int *next, int lane, int claimed, int &b,
+                                           int &kvh, int &t0, int &nvalid, int *Lout = nullptr)
+{
     for (;;) {
         const int L = __shfl_sync(0xffffffffu, claimed, 0);
         if (L >= ntiles)
             return false;
-        const int bg = L % nbg, tile = per_seq - 1 - L / nbg;
-        b = bg / g.Hkv;
-        kvh = bg % g.Hkv;
-        t0 = tile * Tq;
-        const int len = seq_len(g, b);
-        if (t0 < len) {
-            nvalid = min(Tq, len - t0);
+        if (qtile_of(g, L, b, kvh, t0, nvalid)) {
+            if (Lout)
+                *Lout = L;
             return true;
         }
         claimed = qtile_claim(next, lane);
