@@ -71,6 +71,7 @@ constexpr float kRescaleLog2 = 8.f;  // raise the reference only past a 2^8 grow
 struct Params {
     Geo g;
     const int *idx;
+    const int *utable;  // every tile's union buffer, built by the union kernel (null: built here)
     __nv_bfloat16 *o;
     float *lse;
     int *err;
@@ -167,16 +168,28 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             prefetch_tmap(&tm_v);
         }
         int lastq = -1, last = -1, lastv = -1, gi = 0;
+        // The union table is written by the kernel this one depends on.
+        if (p.utable)
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+        int claimed = qtile_claim(p.tile_next, lane);
         for (int k = 0;; ++k) {
-            // The tile and its block union: this warp deals the tiles and builds
-            // each union after issuing the previous tile's copies, while the
+            // The tile and its block union: this warp deals the tiles (each
+            // claimed a tile ahead) and takes each union from the table (or
+            // builds it) after issuing the previous tile's copies, while the
             // K/V rings still hold several of that tile's pairs; after the last
             // tile a header with a negative count tells the other roles to stop.
-            int b = 0, kvh = 0, t0 = 0, nvalid = 0;
-            const bool more = qtile_next(g, p.ntiles, p.tile_next, lane, b, kvh, t0, nvalid);
+            int b = 0, kvh = 0, t0 = 0, nvalid = 0, L = 0;
+            const bool more = qtile_take(g, p.ntiles, p.tile_next, lane, claimed, b, kvh, t0, nvalid, &L);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))
                 break;
-            if (more) {
+            if (more && p.utable) {
+                // copy the tile's union buffer in, 16 bytes per lane and step
+                const uint4 *src = (const uint4 *)(p.utable + (int64_t)L * (up.bytes / 4));
+                uint4 *dst = (uint4 *)u_buf(k);
+                for (int x = lane; x < up.bytes / 16; x += 32)
+                    dst[x] = src[x];
+                __syncwarp();
+            } else if (more) {
                 qtile_union_warp(g, p.idx, up, u_buf(k), b, kvh, t0, nvalid, lane);
             } else {
                 if (lane == 0)
@@ -186,6 +199,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             mbar_arrive(&bars[B_UFULL0 + k % nub]);
             if (!more)
                 break;
+            claimed = qtile_claim(p.tile_next, lane);
             const int U = u_hdr(k)[UH_COUNT];
             const int *list = union_list(u_buf(k), up);
             // the tile's Q, once the previous tile's last S has run
@@ -536,7 +550,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
-                          void *o, float *lse, int *err, int *tile_next, bool after_validate, cudaStream_t st)
+                          const int *utable, void *o, float *lse, int *err, int *tile_next, bool after_kernel,
+                          cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
@@ -555,6 +570,7 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     Params p;
     p.g = g;
     p.idx = idx;
+    p.utable = utable;
     p.o = (__nv_bfloat16 *)o;
     p.lse = lse;
     p.err = err;
@@ -569,7 +585,7 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     // After the index validation, a programmatic dependent of it (the check
     // only reports errors; this kernel skips invalid entries by itself).
-    if (after_validate)
+    if (after_kernel)
         return launch_dependent(fwd_tc_kernel, dim3(grid), dim3(384), smem, st, tq, tk, tv, p);
     fwd_tc_kernel<<<grid, 384, smem, st>>>(tq, tk, tv, p);
     return cudaGetLastError();

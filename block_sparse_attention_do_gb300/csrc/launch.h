@@ -61,11 +61,13 @@ cudaError_t launch_dkdv_simt(const Geo &g, const void *q, const void *k, const v
 // ---- tensor-core kernels (bf16, D = 128, block_size = 64) -----------------
 bool tc_supported(const Geo &g, int dtype);
 // tile_next: a device int that is zero when the kernel starts (its work counter).
-// after_validate: the launch directly follows the index validation kernel,
-// and becomes its programmatic dependent
+// utable: the query-tile union table (launch_qtile_unions), or null (the kernel
+// builds the unions); after_kernel: the launch directly follows a kernel of
+// this library (the index validation or the union build) and becomes its
+// programmatic dependent (it waits for it before reading utable)
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v,
-                          const int *idx, void *o, float *lse, int *err, int *tile_next, bool after_validate,
-                          cudaStream_t st);
+                          const int *idx, const int *utable, void *o, float *lse, int *err, int *tile_next,
+                          bool after_kernel, cudaStream_t st);
 // every query tile's block union for the dQ kernel, into utable
 // (qtile_union_table_bytes(g) bytes; 0, and no launch, for the dense entries,
 // whose unions are block ranges the dQ kernel builds itself); a

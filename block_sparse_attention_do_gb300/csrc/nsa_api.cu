@@ -209,8 +209,14 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         return NSA_OK;
     if (mode == SPARSE)
         NSA_LAUNCH("validate_index", launch_validate_index(g, idx, &hdr->err, st));
-    if (tc_supported(g, p->dtype))
-        NSA_LAUNCH("fwd_tc", launch_fwd_tc(g, q, k, v, idx, o, lse, &hdr->err, &hdr->tile_next, mode == SPARSE, st));
+    if (tc_supported(g, p->dtype)) {
+        // the query-tile unions (sparse only), alongside the validation
+        int *utable = mode == SPARSE && qtile_union_table_bytes(g) ? (int *)((char *)ws + kAlign) : nullptr;
+        if (utable)
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st));
+        NSA_LAUNCH("fwd_tc",
+                   launch_fwd_tc(g, q, k, v, idx, utable, o, lse, &hdr->err, &hdr->tile_next, mode == SPARSE, st));
+    }
     else
         NSA_LAUNCH("fwd_simt", launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
     if (sinks)
@@ -371,9 +377,11 @@ size_t nsa_fwd_workspace_size(const nsa_problem *p)
     if (!p)
         return 0;
     const bool thd = p->layout == NSA_LAYOUT_THD;
-    // dense and sparse forwards share the layout: the header only
-    if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK &&
-        make_geo(p, thd, DENSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
+    // dense and sparse forwards share the layout: the header, then (sparse,
+    // tensor-core path) the query-tile union table
+    if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) == NSA_OK)
+        return kAlign + (tc_supported(g, p->dtype) ? align_up(qtile_union_table_bytes(g)) : 0);
+    if (make_geo(p, thd, DENSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
         return 0;
     return kAlign;
 }
