@@ -15,8 +15,10 @@
 // M = 128 costs about the same for N = 64 as for N = 128.
 //
 // The kernel is persistent: one CTA per SM takes tiles from a launch-wide
-// counter, heaviest (latest tokens) first.  The next
-// tile's block union, its Q/dO load and its first K/V pairs overlap the
+// counter, heaviest (latest tokens) first, each claimed a tile ahead.  A
+// selection tile's block union comes from a table built before the kernel
+// (qtile_union_kernel, below); a dense tile's is a block range built here.
+// The next tile's union, its Q/dO load and its first K/V pairs overlap the
 // current tile's last pairs and epilogue: the union sits in one of two
 // shared-memory buffers (one when two do not fit).
 //
@@ -27,8 +29,8 @@
 // load to dP, K from its load to the dQ product (three stages when they
 // fit, else two).
 //
-// Roles (12 warps): warp 0 deals the tiles, builds each tile's block union
-// and issues the TMA copies (the tile's Q and dO, then per pair its K boxes
+// Roles (12 warps): warp 0 deals the tiles, copies in (or builds) each
+// tile's block union and issues the TMA copies (the tile's Q and dO, then per pair its K boxes
 // and its V boxes, one box per lane); one thread each of warps 2, 1 and 3
 // issues the S, dP and dQ MMAs (warp 2 owns TMEM); warps 4-7 form dS of each
 // pair's first block and warps 8-11 of its second, one row per thread (P
@@ -178,10 +180,10 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         int claimed = qtile_claim(p.tile_next, lane);
         for (int k = 0;; ++k) {
             // The tile and its block union: this warp deals the tiles (each
-            // claimed a tile ahead) and builds each union after issuing the
-            // previous tile's copies, while the K/V rings still hold several of
-            // that tile's pairs; after the last tile a header with a negative
-            // count tells the other roles to stop.
+            // claimed a tile ahead) and copies in (or builds) each union after
+            // issuing the previous tile's copies, while the K/V rings still
+            // hold several of that tile's pairs; after the last tile a header
+            // with a negative count tells the other roles to stop.
             int b = 0, kvh = 0, t0 = 0, nvalid = 0, L = 0;
             const bool more = qtile_take(g, p.ntiles, p.tile_next, lane, claimed, b, kvh, t0, nvalid, &L);
             if (!mbar_wait_warp(&bars[B_UEMPTY0 + k % nub], u_par(k) ^ 1, abort_flag))

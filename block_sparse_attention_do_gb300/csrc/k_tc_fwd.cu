@@ -24,12 +24,14 @@
 // own: K is held only from its load to S, V from its load to P.V.
 //
 // The kernel is persistent like the dQ kernel: one CTA per SM, tiles taken
-// heaviest first from a launch-wide counter, the next tile's union and Q load overlapping
+// heaviest first from a launch-wide counter (each claimed a tile ahead), a
+// selection tile's union copied from the table qtile_union_kernel built
+// (a dense tile's built here), the next tile's union and Q load overlapping
 // the current tile; S (with P) is double-buffered in TMEM and the K and V
 // rings carry across tiles.
 //
-// Roles (12 warps): warp 0 deals the tiles, builds each tile's block union
-// and issues the TMA copies (the tile's Q, then per pair its K boxes and its
+// Roles (12 warps): warp 0 deals the tiles, copies in (or builds) each
+// tile's block union and issues the TMA copies (the tile's Q, then per pair its K boxes and its
 // V boxes, one box per lane); one thread of warp 2 (which owns TMEM) issues
 // S, one thread each of warps 1 and 3 the P.V products of blocks 0 and 1;
 // warps 4-7 and 8-11 are softmax warpgroups 0 and 1, one row per thread,

@@ -102,8 +102,9 @@ __device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, 
 }
 
 // ---- persistent query-tile kernels: tiles are taken from a launch-wide
-// counter, heaviest (latest tokens) first, and one warp per CTA builds each
-// tile's block union a tile ahead of its use into one of (up to) two buffers.
+// counter, heaviest (latest tokens) first, and one warp per CTA puts each
+// tile's block union (copied from the table qtile_union_kernel built, or
+// built in place) a tile ahead of its use into one of (up to) two buffers.
 
 // A union buffer: UH_INTS header ints (the tile's coordinates and the list
 // length; a negative length ends the walk), the per-token block bitmaps, the
