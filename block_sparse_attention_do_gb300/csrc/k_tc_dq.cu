@@ -76,6 +76,7 @@ struct Params {
     int ntiles;      // query tiles over all (b, kv head)
     int *tile_next;  // work counter, zero at launch
     int nub;     // union buffers (1 or 2)
+    int v8;      // dq is 32-byte aligned: the epilogue stores 32 bytes at a time
     int nk;      // K pair stages (2 or 3)
 };
 
@@ -515,24 +516,31 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             if (!mbar_wait_warp(&bars[B_ACCFULL], k & 1, abort_flag))
                 break;
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t acc[16];
-                tmem_ld16(lane_base + TM_DQ + e * 64 + c * 16, acc);
-                tmem_wait_ld();
-                uint32_t w[8];
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    w[x] = npairs > 0 ? pack_bf16(__uint_as_float(acc[2 * x]) * g.scale,
-                                                  __uint_as_float(acc[2 * x + 1]) * g.scale)
-                                      : 0u;
-                if (rvalid) {
-                    *(uint4 *)(dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *(uint4 *)(dst + c * 16 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-                }
-            }
+            // all 64 columns in one go; the accumulator is free for the next
+            // tile's dQ products before the stores
+            uint32_t acc[64];
+            tmem_ld64(lane_base + TM_DQ + e * 64, acc);
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bars[B_ACCEMPTY]);
+            uint32_t w[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+                w[x] = npairs > 0 ? pack_bf16(__uint_as_float(acc[2 * x]) * g.scale,
+                                              __uint_as_float(acc[2 * x + 1]) * g.scale)
+                                  : 0u;
+            if (rvalid) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (p.v8) {
+                        st_global_v8(dst + c * 16, w + 8 * c);
+                    } else {
+                        *(uint4 *)(dst + c * 16) = make_uint4(w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3]);
+                        *(uint4 *)(dst + c * 16 + 8) =
+                            make_uint4(w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
+                    }
+                }
+            }
         }
     }
 
@@ -640,6 +648,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
     p.nk = nk;
+    p.v8 = ((uintptr_t)dq & 31) == 0;
     p.tile_next = tile_next;
     int grid = num_sms();
     if (grid > p.ntiles)

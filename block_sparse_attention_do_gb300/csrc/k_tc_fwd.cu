@@ -80,6 +80,7 @@ struct Params {
     int ntiles;      // query tiles over all (b, kv head)
     int *tile_next;  // work counter, zero at launch
     int nub;     // union buffers (1 or 2)
+    int v8;      // o is 32-byte aligned: the epilogue stores 32 bytes at a time
 };
 
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -517,6 +518,11 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                 tmem_ld32(lane_base + TM_O + e * 64 + h * 32, o0);
                 tmem_ld32(lane_base + TM_O + 128 + e * 64 + h * 32, o1);
                 tmem_wait_ld();
+                if (h == 1) {
+                    // the accumulators are read: free for the next tile before the stores
+                    tc_fence_before();
+                    mbar_arrive(&bars[B_ACCEMPTY]);
+                }
                 uint32_t w[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
@@ -524,13 +530,18 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                     const float v1 = __uint_as_float(o0[2 * x + 1]) * c0 + __uint_as_float(o1[2 * x + 1]) * c1;
                     w[x] = npairs > 0 ? pack_bf16(v0, v1) : 0u;
                 }
-                if (rvalid)
+                if (rvalid) {
+                    if (p.v8) {
+                        st_global_v8(dst + h * 32, w);
+                        st_global_v8(dst + h * 32 + 16, w + 8);
+                    } else {
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        *(uint4 *)(dst + h * 32 + x * 8) = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                        for (int x = 0; x < 4; ++x)
+                            *(uint4 *)(dst + h * 32 + x * 8) =
+                                make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                    }
+                }
             }
-            tc_fence_before();
-            mbar_arrive(&bars[B_ACCEMPTY]);
             if (e == 0 && rvalid)
                 p.lse[stat_off(g, b, kvh * G + hh, t)] =
                     lsum > 0.f ? (mx + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
@@ -578,6 +589,7 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     p.err = err;
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
+    p.v8 = ((uintptr_t)o & 31) == 0;
     p.tile_next = tile_next;
     int grid = num_sms();
     if (grid > p.ntiles)

@@ -256,6 +256,14 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64])
         : "r"(taddr));
 }
 
+// 32 bytes (w[0..7]) to global memory in one 256-bit store; dst 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t *w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // the store counterpart of tmem_ld16

@@ -284,6 +284,37 @@ def test_deterministic_bitwise():
         assert torch.equal(a[n], b[n]), n
 
 
+def test_outputs_only_16_byte_aligned():
+    """o and dq at addresses 16- but not 32-byte aligned (all the API asks) take
+    the kernels' 16-byte store path: bitwise the results of the 32-byte one."""
+    import ctypes as C
+    B, Hq, Hkv, T, D, bs, S = 1, 16, 1, 1100, 128, 64, 16
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=12)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=12)
+    q, k, v, do, idx = (x.cuda() for x in (q, k, v, do, idx))
+    o_ref, lse_ref = api.sel_fwd(q, k, v, idx, bs)
+    dq_ref, dk_ref, dv_ref = api.sel_bwd(q, k, v, o_ref, do, lse_ref, idx, bs)[:3]
+
+    def shifted_like(x):  # 8 bf16 = 16 bytes past a 256-byte aligned allocation
+        y = torch.empty(x.numel() + 8, dtype=x.dtype, device=x.device)[8:].view_as(x)
+        assert y.data_ptr() % 32 == 16
+        return y
+
+    o2, lse2 = shifted_like(q), torch.empty_like(lse_ref)
+    p = api.problem_from(q, k, bs, S)
+    ws = torch.empty(api.fwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    s = api.lib().nsa_sel_fwd(C.byref(p), api._ptr(q), api._ptr(k), api._ptr(v), api._ptr(idx), api._ptr(o2),
+                              api._ptr(lse2), api._ptr(ws), ws.numel(), api._stream(None))
+    assert s == 0
+    torch.cuda.synchronize()
+    assert api.get_error(ws) == 0
+    assert torch.equal(o2, o_ref) and torch.equal(lse2, lse_ref)
+    dq2 = shifted_like(q)
+    api.sel_bwd(q, k, v, o_ref, do, lse_ref, idx, bs, out=(dq2, torch.empty_like(k), torch.empty_like(v)))
+    torch.cuda.synchronize()
+    assert torch.equal(dq2, dq_ref)
+
+
 @pytest.mark.parametrize("dtype,shape", [
     (torch.bfloat16, (1, 16, 1, 1024, 128, 64, 4)),   # tensor-core path
     (torch.float32, (2, 6, 2, 300, 64, 32, 5)),       # SIMT path
