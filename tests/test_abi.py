@@ -80,3 +80,31 @@ def test_workspace_sizes_and_validation(lib):
 
 def test_offsets_len(lib):
     assert lib.nsa_inverse_index_offsets_len(C.byref(_p(B=2, Hkv=2, T=130, block_size=64))) == 2 * 2 * 3 + 1
+
+
+def test_forward_workspace_holds_the_union_table(lib):
+    """The selection forward's workspace: a 256-byte header, then (bf16 on the
+    tensor-core kernels) one union record per 128-row query tile: 8 header
+    ints, a block bitmap per token, the union bitmap (words rounded up to 4)
+    and the block list (rounded up to 4 ints), 128-byte rounded."""
+    import torch
+
+    from block_sparse_attention_do_gb300 import api
+
+    def expected(B, Hq, Hkv, T, bs):
+        G, nb = Hq // Hkv, -(-T // bs)
+        words = -(-nb // 32)
+        tq = 128 // G
+        ints = 8 + tq * words + (words + 3) // 4 * 4 + (nb + 3) // 4 * 4
+        rec = -(-ints * 4 // 128) * 128
+        table = B * Hkv * -(-T // tq) * rec
+        return 256 + -(-table // 256) * 256
+
+    for B, Hq, Hkv, T in ((1, 32, 2, 8192), (2, 16, 1, 1100), (1, 64, 4, 65536)):
+        p = _p(B=B, Hq=Hq, Hkv=Hkv, T=T, S=16)
+        assert api.fwd_workspace_size(p) == expected(B, Hq, Hkv, T, 64), (B, Hq, Hkv, T)
+        # the backward's workspace carries the same table besides its own parts
+        assert api.bwd_workspace_size(p) > api.fwd_workspace_size(p)
+    # the CUDA-core kernels build no table
+    assert api.fwd_workspace_size(_p(dtype=torch.float32)) == 256
+    assert api.fwd_workspace_size(_p(D=64)) == 256
