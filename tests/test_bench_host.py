@@ -1,6 +1,7 @@
 """Host-side logic of bench.py: the multi-rank aggregation (max of time, sum
-of work) over a world-size-2 gloo group on CPU, and the reference arm's
-rank handling."""
+of work) over a world-size-2 gloo group on CPU, the reference arm's rank
+handling, and the DRAM-traffic figure taken from the committed profile only
+while it matches the kernel's source."""
 import os
 import socket
 
@@ -57,3 +58,25 @@ def test_warmup_floor(argv):
 
     with pytest.raises(SystemExit):
         bench.main(argv)
+
+
+def test_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+    import json
+    import shutil
+
+    import bench
+
+    src = os.path.join(bench.ROOT, "block_sparse_attention_do_gb300", "csrc", "k_tc_dkdv.cu")
+    os.makedirs(tmp_path / "profiles")
+    os.makedirs(tmp_path / "block_sparse_attention_do_gb300" / "csrc")
+    shutil.copy(src, tmp_path / "block_sparse_attention_do_gb300" / "csrc" / "k_tc_dkdv.cu")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_hash("dkdv_tc")
+    entry = {"dkdv_tc": {"source_sha": sha, "bytes_per_launch_full": 1234}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(entry))
+    assert bench.traffic_for("dkdv_tc") == 1234
+    assert bench.traffic_for("dq_tc") is None  # no entry
+    # the kernel changed since the capture: no figure
+    with open(tmp_path / "block_sparse_attention_do_gb300" / "csrc" / "k_tc_dkdv.cu", "a") as f:
+        f.write("// changed\n")
+    assert bench.traffic_for("dkdv_tc") is None
