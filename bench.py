@@ -83,7 +83,9 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples, beside the summary the JSON line carries
+        out_dir = os.environ.get("NSA_BENCH_OUT") or os.path.join(ROOT, "bench_out")
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
