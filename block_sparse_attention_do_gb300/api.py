@@ -30,7 +30,7 @@ SYMBOLS = (
     "nsa_status_string", "nsa_count_pairs", "nsa_trace_enable", "nsa_trace_reset",
     "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
     "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
-    "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd",
+    "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd", "nsa_debug_stall",
 )
 
 
@@ -88,6 +88,7 @@ def lib() -> C.CDLL:
         L.nsa_swa_bwd.argtypes = [pp, C.c_int32] + [_P] * 10 + [_P, C.c_size_t, _P]
         L.nsa_sink_fwd.argtypes = [pp, C.c_int32] + [_P] * 7 + [_P, C.c_size_t, _P]
         L.nsa_sink_bwd.argtypes = [pp, C.c_int32] + [_P] * 12 + [_P, C.c_size_t, _P]
+        L.nsa_debug_stall.argtypes = [C.c_int32, C.c_int32]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []
@@ -326,6 +327,13 @@ def count_pairs(block_idx, Hq, block_size, cu_seqlens=None, max_seqlen=None, str
     _check(lib().nsa_count_pairs(C.byref(p), _ptr(cu_seqlens), _ptr(block_idx), _ptr(out),
                                  _stream(stream)), "nsa_count_pairs")
     return int(out.item())
+
+
+def debug_stall(kernel: int, wait_limit_us: int):
+    """Self-test of the kernels' bounded waits (nsa_debug_stall): kernel 1
+    (forward), 2 (dK/dV) or 3 (dQ) runs with its S-product issuer idle and
+    every wait gives up after wait_limit_us; (0, 0) restores normal operation."""
+    _check(lib().nsa_debug_stall(int(kernel), int(wait_limit_us)), "nsa_debug_stall")
 
 
 def trace_enable(max_records: int):

@@ -75,6 +75,8 @@ struct Params {
     float *partials;
     __nv_bfloat16 *dk, *dv;
     int *err;
+    int wait_us;  // bounded-wait limit in microseconds (0: the default)
+    int stall;    // self-test: the S-product issuer stays idle (see wait_test)
 };
 
 // The CTA's k-th work unit, or -1 past the end.  Units are dealt to the CTAs
@@ -108,7 +110,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     const int nrows = Tt * G;                  // used rows per tile
 
     if (threadIdx.x == 0) {
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = p.wait_us;  // the wait limit (0: the default)
         for (int x = 0; x < NQ; ++x) {
             mbar_init(&bars[B_QFULL0 + x], GATHER_TMA ? 1 : 32);
             mbar_init(&bars[B_QEMPTY0 + x], 1);  // dK^T's commit
@@ -262,15 +265,15 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             cp_async_wait<0>();
         if (*abort_flag && lane == 0) {
             // let TMA copies still in flight land before the CTA exits
-            volatile int never = 0;
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
             if (last_tile >= 0) {
                 if (tensor)
-                    mbar_wait(&bars[B_DOFULL0 + (last_tile & 1)], (last_tile >> 1) & 1, &never);
+                    mbar_wait(&bars[B_DOFULL0 + (last_tile & 1)], (last_tile >> 1) & 1, never);
                 else
-                    mbar_wait(&bars[B_QFULL0 + last_tile % NQ], (last_tile / NQ) & 1, &never);
+                    mbar_wait(&bars[B_QFULL0 + last_tile % NQ], (last_tile / NQ) & 1, never);
             }
             if (last_kv >= 0)
-                mbar_wait(&bars[B_KVFULL], last_kv & 1, &never);
+                mbar_wait(&bars[B_KVFULL], last_kv & 1, never);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -347,7 +350,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const bool on_do = role == 1 || role == 2;
             const uint32_t b_s = role == 1 ? v_s : k_s;
             int it = 0, uc = 0, qs = 0, qph = 0, tb = 0, tph = 0;  // (tb, tph): S/dP buffer and its phase
-            bool ok = true;
+            // (self-test of the bounded waits: an idle S issuer makes the
+            // softmax's first wait run out)
+            bool ok = !(p.stall && role == 0);
             for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
                 const int ntiles = (p.units[ui].count + Tt - 1) / Tt;
                 for (int ti = 0; ti < ntiles; ++ti, ++it) {
@@ -411,8 +416,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             }
             // every MMA issued must finish before TMEM is released
             mma_commit(&bars[B_DONE0 + role]);
-            volatile int never = 0;
-            mbar_wait(&bars[B_DONE0 + role], 0, &never);
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
+            mbar_wait(&bars[B_DONE0 + role], 0, never);
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
@@ -655,6 +660,8 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
     p.dk = (__nv_bfloat16 *)dk;
     p.dv = (__nv_bfloat16 *)dv;
     p.err = err;
+    p.wait_us = wait_test().wait_us;
+    p.stall = wait_test().kernel == WAIT_TEST_DKDV;
     int grid = num_sms();
     if (grid > max_units)
         grid = max_units;

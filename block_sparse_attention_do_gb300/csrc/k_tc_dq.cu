@@ -78,6 +78,8 @@ struct Params {
     int nub;     // union buffers (1 or 2)
     int v8;      // dq is 32-byte aligned: the epilogue stores 32 bytes at a time
     int nk;      // K pair stages (2 or 3)
+    int wait_us;  // bounded-wait limit in microseconds (0: the default)
+    int stall;    // self-test: the S-product issuer stays idle (see wait_test)
 };
 
 __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -108,7 +110,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
     const int words = (g.nbmax + 31) / 32;
 
     if (threadIdx.x == 0) {
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = p.wait_us;  // the wait limit (0: the default)
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QEMPTY], 1);
         mbar_init(&bars[B_DOFULL], 1);
@@ -273,15 +276,15 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
         }
         // copies in flight must land before the CTA may exit
         if (lane == 0 && *abort_flag) {
-            volatile int never = 0;
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
             if (lastq >= 0)
-                mbar_wait(&bars[B_QFULL], lastq & 1, &never);
+                mbar_wait(&bars[B_QFULL], lastq & 1, never);
             if (lastd >= 0)
-                mbar_wait(&bars[B_DOFULL], lastd & 1, &never);
+                mbar_wait(&bars[B_DOFULL], lastd & 1, never);
             if (last >= 0)
-                mbar_wait(&bars[B_KF0 + last % NK], (last / NK) & 1, &never);
+                mbar_wait(&bars[B_KF0 + last % NK], (last / NK) & 1, never);
             if (lastv >= 0)
-                mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, &never);
+                mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, never);
         }
         __syncwarp();
     } else if (warp <= 3) {
@@ -298,7 +301,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
             const uint32_t idS = idesc_bf16(128, 128, false, false), idQ = idesc_bf16(128, 128, false, true);
             int gi = 0;
-            bool ok = true;
+            // (self-test of the bounded waits: an idle S issuer makes the
+            // softmax's first wait run out)
+            bool ok = !(p.stall && warp == 2);
             for (int k = 0; ok; ++k) {
                 if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                     break;
@@ -387,8 +392,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             // every MMA of this thread completes before TMEM is freed
             uint64_t *done = &bars[B_DONE0 + warp - 1];
             mma_commit(done);
-            volatile int never = 0;
-            mbar_wait(done, 0, &never);
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
+            mbar_wait(done, 0, never);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -650,6 +655,8 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.nk = nk;
     p.v8 = ((uintptr_t)dq & 31) == 0;
     p.tile_next = tile_next;
+    p.wait_us = wait_test().wait_us;
+    p.stall = wait_test().kernel == WAIT_TEST_DQ;
     int grid = num_sms();
     if (grid > p.ntiles)
         grid = p.ntiles;

@@ -81,6 +81,8 @@ struct Params {
     int *tile_next;  // work counter, zero at launch
     int nub;     // union buffers (1 or 2)
     int v8;      // o is 32-byte aligned: the epilogue stores 32 bytes at a time
+    int wait_us;  // bounded-wait limit in microseconds (0: the default)
+    int stall;    // self-test: the S-product issuer stays idle (see wait_test)
 };
 
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
     const int words = (g.nbmax + 31) / 32;
 
     if (threadIdx.x == 0) {
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = p.wait_us;  // the wait limit (0: the default)
         mbar_init(&bars[B_QFULL], 1);
         mbar_init(&bars[B_QEMPTY], 1);
         mbar_init(&bars[B_ACCFULL], 2);
@@ -259,13 +262,13 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
         }
         // copies in flight must land before the CTA may exit
         if (lane == 0 && *abort_flag) {
-            volatile int never = 0;
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
             if (lastq >= 0)
-                mbar_wait(&bars[B_QFULL], lastq & 1, &never);
+                mbar_wait(&bars[B_QFULL], lastq & 1, never);
             if (last >= 0)
-                mbar_wait(&bars[B_KF0 + last % NK], (last / NK) & 1, &never);
+                mbar_wait(&bars[B_KF0 + last % NK], (last / NK) & 1, never);
             if (lastv >= 0)
-                mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, &never);
+                mbar_wait(&bars[B_VF0 + lastv % NV], (lastv / NV) & 1, never);
         }
         __syncwarp();
     } else if (warp <= 3) {
@@ -283,7 +286,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             // Q tile: 64-column halves and 8-row groups apart by these
             const uint32_t qhalf = rg ? kRgHalf : kHalfBytes, qsbo = rg ? kRgStride : 1024;
             int gi = 0;
-            bool ok = true;
+            // (self-test of the bounded waits: an idle S issuer makes the
+            // softmax's first wait run out)
+            bool ok = !(p.stall && warp == 2);
             for (int k = 0; ok; ++k) {
                 if (!mbar_wait(&bars[B_UFULL0 + k % nub], u_par(k), abort_flag))
                     break;
@@ -348,8 +353,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             // every MMA of this thread completes before TMEM is freed
             uint64_t *done = &bars[B_DONE0 + warp - 1];
             mma_commit(done);
-            volatile int never = 0;
-            mbar_wait(done, 0, &never);
+            volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
+            mbar_wait(done, 0, never);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -591,6 +596,8 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     p.nub = nub;
     p.v8 = ((uintptr_t)o & 31) == 0;
     p.tile_next = tile_next;
+    p.wait_us = wait_test().wait_us;
+    p.stall = wait_test().kernel == WAIT_TEST_FWD;
     int grid = num_sms();
     if (grid > p.ntiles)
         grid = p.ntiles;

@@ -8,6 +8,16 @@
 
 namespace nsa {
 
+// Self-test of the tensor-core kernels' bounded waits (nsa_debug_stall): the
+// kernel whose S-product issuer stays idle, so that its first wait on S runs
+// out, and the wait limit of every tensor-core kernel in microseconds
+// (0: the default).  Both 0 in normal operation.
+enum { WAIT_TEST_NONE = 0, WAIT_TEST_FWD = 1, WAIT_TEST_DKDV = 2, WAIT_TEST_DQ = 3 };
+struct WaitTest {
+    int kernel, wait_us;
+};
+WaitTest wait_test();
+
 // ---- prep (k_prep.cu) ----------------------------------------------------
 cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *delta, int dtype,
                           cudaStream_t st);

@@ -3,6 +3,7 @@
 // point allocates memory or synchronises; all work goes on the caller's
 // stream.
 #include <math.h>
+#include <stdint.h>
 #include <string.h>
 
 #include "launch.h"
@@ -49,6 +50,13 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     }
     const int64_t ntok = want_thd ? (int64_t)p->total_tokens : (int64_t)p->B * p->T;
     if (ntok * p->Hq * (int64_t)p->D >= ((int64_t)1 << 40))
+        return NSA_ERR_UNSUPPORTED;
+    // the index-side sizes (list entries, per-block counters, work units) are
+    // held in int: refuse problems whose counts would not fit
+    const int64_t nb = (p->T + p->block_size - 1) / p->block_size;
+    if (ntok >= INT32_MAX || ntok * p->Hq >= INT32_MAX || (int64_t)p->B * p->Hkv * nb >= INT32_MAX)
+        return NSA_ERR_UNSUPPORTED;
+    if (mode == SPARSE && ntok * p->Hkv * p->S >= INT32_MAX)  // inverse-index entries
         return NSA_ERR_UNSUPPORTED;
     memset(&g, 0, sizeof(g));
     g.B = p->B;
@@ -335,7 +343,11 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     return NSA_OK;
 }
 
+WaitTest g_wait_test = {WAIT_TEST_NONE, 0};
+
 }  // namespace
+
+WaitTest nsa::wait_test() { return g_wait_test; }
 
 // ---- scratch for nsa_build_inverse_index_noalloc --------------------------
 // Some callers cannot allocate device memory at call time (see include/nsa.h),
@@ -619,7 +631,7 @@ nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *
     nsa_status s = make_geo(p, thd, SPARSE, cu_seqlens, g);
     if (s != NSA_OK)
         return s;
-    if (!block_idx || !offsets || !rows)
+    if (!block_idx || !offsets || !rows || ((uintptr_t)status_out & 3))
         return NSA_ERR_INVALID_ARG;
     // scratch plan: header | counts | unit list | chunks per block | partial slots
     const PlanLayout L = plan_layout(g);
@@ -645,6 +657,15 @@ nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *
         return s;
     if (status_out)
         NSA_TRY(cudaMemcpyAsync(status_out, &hdr->err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    return NSA_OK;
+}
+
+nsa_status nsa_debug_stall(int32_t kernel, int32_t wait_limit_us)
+{
+    if (kernel < WAIT_TEST_NONE || kernel > WAIT_TEST_DQ || wait_limit_us < 0 || wait_limit_us > 2000000)
+        return NSA_ERR_INVALID_ARG;
+    g_wait_test.kernel = kernel;
+    g_wait_test.wait_us = wait_limit_us;
     return NSA_OK;
 }
 

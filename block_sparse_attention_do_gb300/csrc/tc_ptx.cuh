@@ -28,7 +28,8 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-// A bounded wait gives up after this many nanoseconds.
+// A bounded wait gives up after this many nanoseconds unless the kernel's
+// wait context names a shorter limit.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // ---------------------------------------------------------------- mbarrier
@@ -67,22 +68,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// A wait context is two ints: ctx[0] the abort flag (non-zero once some role
+// of the CTA gave up) and ctx[1] the wait limit in microseconds (0 or less:
+// kWaitLimitNs).  The kernels keep theirs in shared memory.
+//
 // Waits for the phase with the given parity to complete.  Returns false if
-// it did not complete within kWaitLimitNs or if *abort became non-zero (some
-// other role gave up first); the caller then winds down.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+// it did not complete within the limit (the wait then raises the abort flag)
+// or if the abort flag became non-zero (some other role gave up first); the
+// caller then winds down.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *ctx)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = globaltimer();
+    const int lim_us = ctx[1];
+    const uint64_t limit = lim_us > 0 ? (uint64_t)lim_us * 1000ull : kWaitLimitNs;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
         if ((i & 63) == 0) {
-            if (*abort)
+            if (ctx[0])
                 return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                *abort = 1;
+            if (globaltimer() - t0 > limit) {
+                ctx[0] = 1;
                 return false;
             }
         }

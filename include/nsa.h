@@ -259,12 +259,35 @@ nsa_status nsa_build_inverse_index(const nsa_problem *p, const int32_t *cu_seqle
  *    zero, so calls that can overlap on the GPU (other streams, other host
  *    threads) race and must not be issued;
  *  - device-side index errors are copied into *status_out (device int32,
- *    may be NULL) on `stream` instead of a workspace error word.
+ *    4-byte aligned, may be NULL) on `stream` instead of a workspace error
+ *    word;
+ *  - the array's device address is looked up once per device and kept for
+ *    the life of the process: after cudaDeviceReset (or anything else that
+ *    destroys the device's primary context) this entry point must not be
+ *    called again in that process.
  * Nothing is allocated or freed.
  */
 nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *cu_seqlens,
                                            const int32_t *block_idx, int32_t *offsets,
                                            int32_t *rows, int32_t *status_out, void *stream);
+
+/*
+ * Self-test of the device-side timeout path (instrumentation, off by
+ * default; not thread-safe).  Every wait inside the tensor-core kernels is
+ * bounded: a wait that runs out makes the kernel stop its work, wait (again
+ * bounded) for its own copies and products in flight, free its tensor
+ * memory, and report NSA_ERR_DEVICE_TIMEOUT through the workspace error word,
+ * leaving the CUDA context usable.  nsa_debug_stall(kernel, wait_limit_us)
+ * lets a test run that path without any fault: while `kernel` is 1 (the
+ * forward), 2 (the dK/dV kernel) or 3 (the dQ kernel), that kernel is
+ * launched with the thread that issues its S = Q K^T products idle, so the
+ * first wait on S runs out; `wait_limit_us` (1 .. 2000000; 0 = the default
+ * of 2 s) replaces the limit of every tensor-core kernel's waits.
+ * nsa_debug_stall(0, 0) restores normal operation.  Returns
+ * NSA_ERR_INVALID_ARG for values out of range.  The CUDA-core kernels (fp32,
+ * other head dims and block sizes) have no waits and ignore it.
+ */
+nsa_status nsa_debug_stall(int32_t kernel, int32_t wait_limit_us);
 
 /*
  * Reads the device error word of a workspace used by the calls above,

@@ -62,6 +62,8 @@ def lib():
         L.oracle_sel_rows_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 6 + [_i64]
         L.oracle_sel_keys_w.restype = None
         L.oracle_sel_keys_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5 + [_i64]
+        L.oracle_sel_blocks_w.restype = None
+        L.oracle_sel_blocks_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5 + [_i64]
         _lib = L
     return _lib
 
@@ -210,4 +212,19 @@ def sel_keys(q, k, v, idx, dO, bs, keys, scale=None, cu_seqlens=None, window=0):
     dk, dv = np.zeros((n, D)), np.zeros((n, D))
     lib().oracle_sel_keys_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
                             _p(dO), n, _p(kb), _p(kg), _p(kk), _p(dk), _p(dv), int(window))
+    return dk, dv
+
+
+def sel_blocks(q, k, v, idx, dO, bs, blocks, scale=None, cu_seqlens=None, window=0):
+    """blocks: int array [n, 3] of (b, g, j).  Returns (dk [n,bs,D], dv [n,bs,D]):
+    dK and dV of the keys j*bs .. j*bs+bs-1 (zero past the sequence's end)."""
+    q, k, v, dO, idx, cu = _f64(q), _f64(k), _f64(v), _f64(dO), _i32(idx), _i32(cu_seqlens)
+    B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    blocks = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64).reshape(-1, 3))
+    jb, jg, jj = (np.ascontiguousarray(blocks[:, i]) for i in range(3))
+    n = blocks.shape[0]
+    dk, dv = np.zeros((n, bs, D)), np.zeros((n, bs, D))
+    lib().oracle_sel_blocks_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
+                              _p(dO), n, _p(jb), _p(jg), _p(jj), _p(dk), _p(dv), int(window))
     return dk, dv

@@ -54,6 +54,7 @@
  * Build: cc -O2 -fopenmp -fPIC -shared nsa_oracle.c -o liboracle.so -lm
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -528,5 +529,80 @@ void oracle_sel_keys_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D,
         free(keys);
         free(sc);
         free(o);
+    }
+}
+
+/*
+ * oracle_sel_blocks: for each (b, g, j) in the list, dK and dV of every key
+ * of block j (bs keys x D each, keys past the sequence's end left 0), by the
+ * same definitions as oracle_sel_keys.  Each attending row -- a token t of
+ * the block's sequence whose row selects j, with every query head of group
+ * g -- has its forward (LSE_t, O_t) recomputed once for the whole block
+ * instead of once per key, which is what makes whole heavily selected
+ * blocks of the long workloads affordable.
+ */
+void oracle_sel_blocks_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs,
+                         int64_t S, double scale, const int32_t *cu, const double *q,
+                         const double *k, const double *v, const int32_t *idx, const double *dO,
+                         int64_t n, const int64_t *jb, const int64_t *jg, const int64_t *jj,
+                         double *dk_out, double *dv_out, int64_t window)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, S, scale, cu);
+    p.window = window;
+    const int64_t G = Hq / Hkv;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t b = jb[i], g = jg[i], j = jj[i], L = seq_len(&p, b);
+        const int64_t k0 = j * bs, nk = (k0 + bs <= L ? bs : L - k0);
+        double *dkb = dk_out + i * bs * D, *dvb = dv_out + i * bs * D;
+        memset(dkb, 0, sizeof(double) * bs * D);
+        memset(dvb, 0, sizeof(double) * bs * D);
+        if (nk <= 0)
+            continue;
+        /* the attending rows' contributions, summed per thread, then added in
+           thread order */
+#pragma omp parallel
+        {
+            int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * max_keys(&p));
+            double *sc = (double *)malloc(sizeof(double) * max_keys(&p));
+            double *o = (double *)malloc(sizeof(double) * D);
+            double *acc_k = (double *)calloc((size_t)(bs * D), sizeof(double));
+            double *acc_v = (double *)calloc((size_t)(bs * D), sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = k0; t < L; ++t) {
+                if (!selects(&p, idx_row(&p, idx, b, g, t), j))
+                    continue;
+                for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                    const int64_t ro = row_off(&p, Hq, b, h, t);
+                    const double *qt = q + ro, *dOt = dO + ro;
+                    double lse = row_forward(&p, q, k, v, idx, b, h, t, o, keys, sc);
+                    double Dv = dot(dOt, o, D);
+                    for (int64_t c = 0; c < nk; ++c) {
+                        const int64_t kk = k0 + c;
+                        if (kk > t || !in_window(&p, t, kk))
+                            continue;
+                        const int64_t ko = row_off(&p, Hkv, b, g, kk);
+                        double P = exp(scale * dot(qt, k + ko, D) - lse);
+                        double dS = P * (dot(dOt, v + ko, D) - Dv);
+                        for (int64_t d = 0; d < D; ++d) {
+                            acc_k[c * D + d] += scale * dS * qt[d];
+                            acc_v[c * D + d] += P * dOt[d];
+                        }
+                    }
+                }
+            }
+#pragma omp for ordered schedule(static, 1)
+            for (int th = 0; th < omp_get_num_threads(); ++th) {
+#pragma omp ordered
+                for (int64_t x = 0; x < bs * D; ++x) {
+                    dkb[x] += acc_k[x];
+                    dvb[x] += acc_v[x];
+                }
+            }
+            free(keys);
+            free(sc);
+            free(o);
+            free(acc_k);
+            free(acc_v);
+        }
     }
 }

@@ -108,3 +108,35 @@ def test_forward_workspace_holds_the_union_table(lib):
     # the CUDA-core kernels build no table
     assert api.fwd_workspace_size(_p(dtype=torch.float32)) == 256
     assert api.fwd_workspace_size(_p(D=64)) == 256
+
+
+def test_index_sizes_beyond_int32_are_refused(lib):
+    """Inverse-index entries (tokens x kv heads x slots) are counted in int32:
+    a problem one slot past that limit is refused before any launch, the one
+    just inside it is accepted."""
+    from block_sparse_attention_do_gb300 import api
+
+    T = 1 << 24  # 16M tokens, 8 kv heads: 16 slots give 2^31 entries
+    inside = _p(B=1, Hq=8, Hkv=8, T=T, D=32, block_size=64, S=15)
+    over = _p(B=1, Hq=8, Hkv=8, T=T, D=32, block_size=64, S=16)
+    assert lib.nsa_plan_size(C.byref(inside)) > 0
+    assert lib.nsa_plan_size(C.byref(over)) == 0
+    dummy = C.c_void_p(256)
+    s = lib.nsa_sel_bwd(C.byref(over), *([dummy] * 10), dummy, 1 << 40, None)
+    assert s == 2  # NSA_ERR_UNSUPPORTED
+
+
+def test_debug_stall_checks_its_arguments(lib):
+    assert lib.nsa_debug_stall(4, 0) == 1
+    assert lib.nsa_debug_stall(1, -1) == 1
+    assert lib.nsa_debug_stall(2, 3000000) == 1
+    assert lib.nsa_debug_stall(0, 0) == 0
+
+
+def test_noalloc_status_pointer_alignment(lib):
+    from block_sparse_attention_do_gb300 import api
+
+    p = _p(B=1, Hkv=1, T=256, S=4)
+    dummy = C.c_void_p(256)
+    s = lib.nsa_build_inverse_index_noalloc(C.byref(p), None, dummy, dummy, dummy, C.c_void_p(258), None)
+    assert s == 1  # NSA_ERR_INVALID_ARG: status_out not 4-byte aligned

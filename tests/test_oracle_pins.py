@@ -481,3 +481,61 @@ def test_sinks_closed_forms_and_finite_differences():
         fp = float((oracle.sel_fwd(q, k, v, idx, bs, sinks=sp)[0] * dod).sum())
         fm = float((oracle.sel_fwd(q, k, v, idx, bs, sinks=sm)[0] * dod).sum())
         assert abs((fp - fm) / (2 * eps) - r["dsinks"][h]) < 1e-7
+
+
+# ---- whole-block sampling (oracle.sel_blocks), used where the full-size
+# workloads are too large for the whole-output oracle
+
+
+def test_sampled_blocks_against_masked_sdpa():
+    """dK/dV of whole blocks, against masked SDPA + autograd: the first block
+    (selected by nearly every row), a middle block, a ragged last block and a
+    block whose keys no row reaches (an empty list gives zeros)."""
+    B, Hq, Hkv, T, D, bs, S = 2, 6, 2, 45, 8, 8, 3
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=23)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=23)
+    idx[1, 0, :, :] = torch.where(idx[1, 0] == 2, torch.full_like(idx[1, 0], -1), idx[1, 0])  # nobody keeps block 2
+    mask = _mask_from_idx(idx, T, bs)
+    _, _, dk_ref, dv_ref = _sdpa_reference(q, k, v, do, mask, 1.0 / math.sqrt(D))
+    blocks = [(0, 0, 0), (0, 1, 3), (1, 1, 5), (1, 0, 2), (0, 1, 5)]
+    dk, dv = oracle.sel_blocks(q, k, v, idx, do, bs, blocks)
+    for i, (b, g, j) in enumerate(blocks):
+        n = min(bs, T - j * bs)
+        np.testing.assert_allclose(dk[i, :n], dk_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv[i, :n], dv_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+        assert not np.any(dk[i, n:]) and not np.any(dv[i, n:])
+    assert not np.any(dk[3]) and not np.any(dv[3])
+
+
+def test_sampled_blocks_varlen_and_window():
+    """The packed layout (per-sequence SDPA) and the sliding window (band
+    mask), block by block."""
+    lengths = [19, 5, 30]
+    Hq, Hkv, D, bs, S = 4, 2, 8, 8, 3
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    q, k, v, do = inputs.make_qkv_do(1, Hq, Hkv, sum(lengths), D, seed=24, layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=24)
+    blocks = [(0, 0, 0), (0, 1, 2), (1, 0, 0), (2, 1, 1), (2, 0, 3)]
+    dk, dv = oracle.sel_blocks(q, k, v, idx, do, bs, blocks, cu_seqlens=cu)
+    for i, (b, g, j) in enumerate(blocks):
+        a, L = int(cu[b]), lengths[b]
+        sub = lambda x: x[a:a + L].permute(1, 0, 2).unsqueeze(0)  # [1, H, L, D]
+        m = _mask_from_idx(idx[a:a + L].permute(1, 0, 2).unsqueeze(0), L, bs)
+        _, _, dk_ref, dv_ref = _sdpa_reference(sub(q), sub(k), sub(v), sub(do), m, 1.0 / math.sqrt(D))
+        n = min(bs, L - j * bs)
+        np.testing.assert_allclose(dk[i, :n], dk_ref[0, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv[i, :n], dv_ref[0, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+    # window 11 on the dense index, fixed length
+    B, T, W = 1, 41, 11
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=25)
+    idx = inputs.make_dense_block_idx(B, Hkv, T, bs)
+    band = torch.zeros(B, Hkv, T, T, dtype=torch.bool)
+    for t in range(T):
+        band[:, :, t, max(0, t - W + 1):t + 1] = True
+    _, _, dk_ref, dv_ref = _sdpa_reference(q, k, v, do, band, 1.0 / math.sqrt(D))
+    blocks = [(0, 0, 0), (0, 1, 2), (0, 0, 5)]
+    dk, dv = oracle.sel_blocks(q, k, v, idx, do, bs, blocks, window=W)
+    for i, (b, g, j) in enumerate(blocks):
+        n = min(bs, T - j * bs)
+        np.testing.assert_allclose(dk[i, :n], dk_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv[i, :n], dv_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
