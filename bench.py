@@ -176,14 +176,75 @@ def cpu_baseline_oracle(heads: int, T_prefix: int | None = None):
                        f"({pairs} pairs; fp64 backward incl. its forward recompute)")
 
 
-def prefix_pairs(T_prefix: int) -> int:
-    """Selected pairs of query head 0, kv group 0 over the first T_prefix tokens."""
-    import oracle
-    from block_sparse_attention_do_gb300 import inputs
+def dense_pairs(B, Hq, T):
+    """(query row, key) pairs of dense causal attention: every row t attends t + 1 keys."""
+    return B * Hq * T * (T + 1) // 2
 
-    W = WORKLOAD
-    idx = inputs.make_block_idx(W["B"], W["Hkv"], W["T"], W["block_size"], W["S"], seed=0)
-    return oracle.count_pairs(idx[:, :1, :T_prefix], 1, W["block_size"])
+
+def bench_extra(name, q, k, v, do, idx, bs, flush, st, steps, peaks, cu=None, dense=False, pairs=None):
+    """Times one more workload of the pages' configs through the C ABI: the
+    backward (median of `steps`, L2 flushed before each) and the forward, then
+    a traced pass for the per-kernel breakdown and the dominant kernel's
+    roofline (its own algorithmic FLOPs per pair)."""
+    import torch
+
+    from block_sparse_attention_do_gb300 import api
+
+    D, Hq = q.shape[-1], q.shape[-3] if cu is None else q.shape[1]
+    if pairs is None:
+        pairs = api.count_pairs(idx, Hq, bs, cu_seqlens=cu)
+    flop = 10.0 * D * pairs
+    gi = None if dense else idx
+    o, lse = api.sel_fwd(q, k, v, gi, bs, cu_seqlens=cu, dense=dense)
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    for _ in range(3):
+        o, lse = api.sel_fwd(q, k, v, gi, bs, cu_seqlens=cu, dense=dense)
+        api.sel_bwd(q, k, v, o, do, lse, gi, bs, cu_seqlens=cu, dense=dense, out=outs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(st)
+        o, lse = api.sel_fwd(q, k, v, gi, bs, cu_seqlens=cu, dense=dense)
+        ev[i][1].record(st)
+        api.sel_bwd(q, k, v, o, do, lse, gi, bs, cu_seqlens=cu, dense=dense, out=outs)
+        ev[i][2].record(st)
+    torch.cuda.synchronize()
+    bwd = sorted(e[1].elapsed_time(e[2]) for e in ev)
+    fwd = sorted(e[0].elapsed_time(e[1]) for e in ev)
+    med_b, med_f = statistics.median(bwd), statistics.median(fwd)
+    # traced pass: per-kernel times
+    api.trace_enable(steps * 16)
+    api.trace_reset()
+    for i in range(steps):
+        flush.zero_()
+        o, lse = api.sel_fwd(q, k, v, gi, bs, cu_seqlens=cu, dense=dense)
+        api.sel_bwd(q, k, v, o, do, lse, gi, bs, cu_seqlens=cu, dense=dense, out=outs)
+    torch.cuda.synchronize()
+    recs = api.trace_records()
+    api.trace_enable(0)
+    kern = {}
+    for kn, ms in recs:
+        e = kern.setdefault(kn, {"ms_total": 0.0, "launches": 0})
+        e["ms_total"] += ms
+        e["launches"] += 1
+    bwd_kernels = {kn: e for kn, e in kern.items() if not kn.startswith("fwd")}
+    for e in kern.values():
+        e["ms_avg"] = e["ms_total"] / e["launches"]
+    dom = max(bwd_kernels, key=lambda n: bwd_kernels[n]["ms_total"])
+    roof = None
+    if dom in ALG_FLOP_PER_PAIR_PER_D:
+        alg = ALG_FLOP_PER_PAIR_PER_D[dom] * D * pairs
+        ach = alg / (kern[dom]["ms_avg"] * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "algorithmic_flop_per_launch": alg}
+    return {"workload": name, "pairs": pairs, "bwd_flop": flop, "value": flop / (med_b * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "bwd_ms_median": med_b, "bwd_ms_mean": sum(bwd) / len(bwd),
+            "fwd_ms_median": med_f, "steps": steps, "pct_of_bf16_peak": flop / (med_b * 1e-3) / 1e12 / float(
+                peaks["bf16_tflops"]),
+            "kernels": {kn: {"ms_avg": e["ms_avg"], "launches": e["launches"] // steps}
+                        for kn, e in sorted(kern.items(), key=lambda kv: -kv[1]["ms_total"])},
+            "roofline": roof}
 
 
 def run_reference(args):
@@ -193,21 +254,18 @@ def run_reference(args):
     import oracle
 
     oracle.build()
-    # size one step's sample so that warm-up + steps take about 150 s: time
-    # a 1024-token prefix once, then take the longest prefix that fits
+    # one step = the oracle's backward on the same kind of sample as the
+    # cpu_baseline key of the GPU arm (kv group 0, the first `heads` query
+    # heads, full length), with as many heads as fit about 150 s for the run
     budget = min(12.0, 150.0 / (args.steps + args.warmup))
-    cal = cpu_baseline_oracle(1, 1024)
-    rate = cal["pairs"] / cal["seconds"]
-    T_prefix = 1024
-    while T_prefix < WORKLOAD["T"] and prefix_pairs(2 * T_prefix) <= budget * rate:
-        T_prefix *= 2
-    T_prefix = min(T_prefix, WORKLOAD["T"])
+    cal = cpu_baseline_oracle(1)
+    heads = max(1, min(16, int(budget / cal["seconds"])))
     for _ in range(max(0, args.warmup - 1)):
-        cpu_baseline_oracle(1, T_prefix)
+        cpu_baseline_oracle(heads)
     secs, flop = 0.0, 0.0
     last = None
     for _ in range(args.steps):
-        r = cpu_baseline_oracle(1, T_prefix)
+        r = cpu_baseline_oracle(heads)
         secs += r["seconds"]
         flop += r["flop"]
         last = r
@@ -287,6 +345,8 @@ def run_ours(args):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+    # the median of the K backward times (the headline) beside the mean
+    bwd_med = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     err = api.get_error(ws_b) or api.get_error(ws_f)
     if err:
         raise RuntimeError(f"device error status {err} in the timed loop")
@@ -310,8 +370,10 @@ def run_ours(args):
     traced_bwd_ms = sum(a.elapsed_time(b) for a, b in tr_ev) / K
 
     bwd_ms_max, flop_all = aggregate(bwd_ms, bwd_flop * K, dev)
+    med_max, flop_one = aggregate(bwd_med, bwd_flop, dev)
     step_ms_max, _ = aggregate(step_ms, 0.0, dev)
-    value = flop_all / (bwd_ms_max * 1e-3) / 1e12
+    value = flop_one / (med_max * 1e-3) / 1e12
+    value_mean = flop_all / (bwd_ms_max * 1e-3) / 1e12
 
     # ---- per-kernel breakdown and roofline of the dominant kernel
     kern = {}
@@ -389,6 +451,40 @@ def run_ours(args):
            "bwd_ms": sw_bwd / n_sw, "fwd_ms": sw_fwd / n_sw, "steps": n_sw,
            "scope": "nsa_swa_fwd + nsa_swa_bwd, same shapes, 10*D*pairs / backward time, L2 flushed"}
 
+    # ---- the pages' other workloads (single GPU only; rank 0 of a replica run
+    # times them too, each rank on its own GPU)
+    configs = {}
+    if not args.skip_configs:
+        n_x = max(5, min(K, 20))
+        # config 2 in bf16: B=2 Hq=6 Hkv=2 T=1024 D=64 block 32 S=8
+        q2, k2, v2, do2 = inputs.make_qkv_do(2, 6, 2, 1024, 64, dtype=torch.bfloat16, seed=rank)
+        idx2 = inputs.make_block_idx(2, 2, 1024, 32, 8, seed=rank)
+        configs["mid_bf16"] = bench_extra(
+            "NSA selection bwd, bf16: B=2 Hq=6 Hkv=2 (G=3) T=1024 D=64 block_size=32 S=8",
+            *(x.to(dev) for x in (q2, k2, v2, do2, idx2)), 32, flush, st, n_x, peaks)
+        del q2, k2, v2, do2, idx2
+        # config 4: dense causal B=2 Hq=32 Hkv=8 T=4096 D=128 block 64 (nsa_dense_causal_*)
+        q4, k4, v4, do4 = inputs.make_qkv_do(2, 32, 8, 4096, 128, dtype=torch.bfloat16, seed=rank)
+        configs["dense_causal"] = bench_extra(
+            "dense causal SDPA bwd as selection of all valid blocks, bf16: B=2 Hq=32 Hkv=8 (G=4) T=4096 "
+            "D=128 block_size=64", *(x.to(dev) for x in (q4, k4, v4, do4)), None, 64, flush, st, n_x, peaks,
+            dense=True, pairs=dense_pairs(2, 32, 4096))
+        del q4, k4, v4, do4
+        # config 5: THD, 8 sequences with lengths uniform in [128, 4096], Hq=32 Hkv=8 D=128 block 64 S=16
+        lens = inputs.make_varlen_lengths(8, 128, 4096, seed=rank)
+        cu5 = inputs.cu_seqlens_from_lengths(lens)
+        q5, k5, v5, do5 = inputs.make_qkv_do(1, 32, 8, sum(lens), 128, dtype=torch.bfloat16, seed=rank,
+                                             layout="thd")
+        idx5 = inputs.make_varlen_block_idx(lens, 8, 64, 16, seed=rank)
+        configs["varlen_thd"] = bench_extra(
+            f"THD varlen NSA selection bwd, bf16: 8 sequences (lengths {lens}), Hq=32 Hkv=8 (G=4) D=128 "
+            "block_size=64 S=16", *(x.to(dev) for x in (q5, k5, v5, do5, idx5)), 64, flush, st, n_x, peaks,
+            cu=cu5.to(dev))
+        del q5, k5, v5, do5, idx5
+        torch.cuda.synchronize()
+        if api.get_error(api.workspace(1, dev, "bwd")) or api.get_error(api.workspace(1, dev, "fwd")):
+            raise RuntimeError("device error in the extra workloads")
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if True:  # every rank: the aggregation below is collective
@@ -422,7 +518,9 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = cpu_baseline_oracle(args.cpu_heads)
         cpu = {"value": r["flop"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"],
-               "kind": "oracle", "sample": r["sample"], "seconds": r["seconds"]}
+               "kind": "oracle", "sample": r["sample"], "seconds": r["seconds"],
+               "note": "the stated CPU baseline; bench.py --impl reference times the same kind of sample "
+                       "(fewer heads per step)"}
 
     if rank == 0:
         line = {
@@ -435,13 +533,16 @@ def run_ours(args):
                              "the bwd also reads 192 MiB of q/o/dO, more than L2",
                        "parallelism": f"replicas x{world} (independent problems, no collective)"},
             "pct_of_bf16_peak": pct,
-            "bwd_ms": bwd_ms / K, "fwd_ms": fwd_ms / K, "wall_s": t_wall,
+            "value_is": "10*D*pairs / median backward time over the K timed steps",
+            "value_mean": value_mean,
+            "bwd_ms": bwd_med, "bwd_ms_mean": bwd_ms / K, "fwd_ms": fwd_ms / K, "wall_s": t_wall,
             "kernels": {n: {"ms_avg": e["ms_avg"], "launches": e["launches"], "share": e["share"]}
                         for n, e in sorted(kern.items(), key=lambda kv: -kv[1]["ms_total"])},
             "kernels_pass": {"what": "a second pass of the same K fwd+bwd steps with a CUDA event pair "
                                      "around every launch (the library's tracer); the roofline uses it",
                              "bwd_ms": traced_bwd_ms},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "planned": planned, "swa": swa,
+            "configs": configs,
             "gpu_launches": len(recs),
             "clocks": clocks,
         }
@@ -459,6 +560,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-heads", type=int, default=4, help="query heads in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true", help="time only the headline workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -38,7 +38,34 @@ class Problem(C.Structure):
     _fields_ = [("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("T", C.c_int32),
                 ("D", C.c_int32), ("block_size", C.c_int32), ("S", C.c_int32),
                 ("dtype", C.c_int32), ("layout", C.c_int32), ("total_tokens", C.c_int32),
-                ("scale", C.c_float)]
+                ("scale", C.c_float), ("reserved", C.c_int32),
+                ("q_stride", C.c_int64 * 3), ("kv_stride", C.c_int64 * 3), ("o_stride", C.c_int64 * 3),
+                ("dq_stride", C.c_int64 * 3), ("dkv_stride", C.c_int64 * 3)]
+
+
+def _bht_strides(t, thd):
+    """(batch, head, token) element strides of a [B, H, T, D] (or packed
+    [total, H, D]) tensor whose last dimension is contiguous."""
+    if t.stride(-1) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    if thd:
+        return (0, t.stride(1), t.stride(0))
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
+def declare_strides(p: Problem, thd: bool, q=None, k=None, o=None, dq=None, dk=None) -> Problem:
+    """Fills the problem's declared strides from the tensors given (k stands
+    for k and v, o for o and dO, dk for dk and dv)."""
+    for name, t in (("q_stride", q), ("kv_stride", k), ("o_stride", o), ("dq_stride", dq),
+                    ("dkv_stride", dk)):
+        if t is not None:
+            getattr(p, name)[:] = _bht_strides(t, thd)
+    return p
+
+
+def _same_strides(a, b, what):
+    if a is not None and b is not None and a.stride() != b.stride():
+        raise ValueError(f"{what} must have the same strides")
 
 
 class NsaError(RuntimeError):
@@ -172,7 +199,9 @@ def sel_fwd(q, k, v, block_idx, block_size, scale=None, cu_seqlens=None, max_seq
     dense = dense or window is not None or sinks is not None
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    _same_strides(k, v, "k and v")
+    declare_strides(p, cu_seqlens is not None, q=q, k=k, o=o)
     lse = torch.empty(_lse_shape(q, cu_seqlens), dtype=torch.float32, device=q.device)
     n = fwd_workspace_size(p)
     if n == 0:
@@ -226,9 +255,15 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
     S = 1 if dense else block_idx.shape[-1]
     p = problem_from(q, k, block_size, S, scale, cu_seqlens, max_seqlen)
     if out is None:
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+        dk = torch.empty(k.shape, dtype=k.dtype, device=k.device)
+        dv = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     else:
         dq, dk, dv = out
+    _same_strides(k, v, "k and v")
+    _same_strides(o, dO, "o and dO")
+    _same_strides(dk, dv, "dk and dv")
+    declare_strides(p, cu_seqlens is not None, q=q, k=k, o=o, dq=dq, dk=dk)
     L = lib()
     if plan is not None:
         if dense:
@@ -274,6 +309,8 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
 
 def do_dot(o, dO, cu_seqlens=None, stream=None):
     p = problem_from(o, o, 16, 1, None, cu_seqlens)
+    _same_strides(o, dO, "o and dO")
+    declare_strides(p, cu_seqlens is not None, o=o)
     delta = torch.empty(o.shape[:-1], dtype=torch.float32, device=o.device)
     _check(lib().nsa_do_dot(C.byref(p), _ptr(cu_seqlens), _ptr(o), _ptr(dO), _ptr(delta),
                             _stream(stream)), "nsa_do_dot")

@@ -25,14 +25,15 @@ inline int grid_for(int64_t n, int per_block, int cap = 152 * 32)
 }
 
 // ---------------------------------------------------------------- do_dot
-// Rows are contiguous D-vectors in both layouts, and delta uses the row order
-// of o, so the kernel is a plain segmented dot product over rows.
+// delta uses the row order of lse (BHTD (b*Hq + h)*T + t, THD token*Hq + h);
+// each row's D-vector of o and dO sits where the strides of o put it, so the
+// kernel is a segmented dot product over rows.
 // blocks blk of nblk (grid-stride); each warp takes kDotU row groups per
 // step, so that 2 * kDotU 16-byte loads per thread are in flight
 constexpr int kDotU = 4;
 template <typename T>
-__device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__restrict__ dO, float *__restrict__ out,
-                                            int64_t nrows, int D, int blk, int nblk)
+__device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ o, const T *__restrict__ dO,
+                                            float *__restrict__ out, int64_t nrows, int D, int blk, int nblk)
 {
     constexpr int VEC = 16 / sizeof(T);
     const int tpr = D / VEC;  // threads per row (power of two, <= 32)
@@ -47,8 +48,9 @@ __device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__
             const int64_t r = r0 + u * rpw + sub;
             a[u] = b[u] = make_uint4(0, 0, 0, 0);
             if (r < nrows) {
-                a[u] = __ldcs(reinterpret_cast<const uint4 *>(o + r * D + part * VEC));
-                b[u] = __ldcs(reinterpret_cast<const uint4 *>(dO + r * D + part * VEC));
+                const int64_t off = qrow_off(g, g.so, r) + part * VEC;
+                a[u] = __ldcs(reinterpret_cast<const uint4 *>(o + off));
+                b[u] = __ldcs(reinterpret_cast<const uint4 *>(dO + off));
             }
         }
 #pragma unroll
@@ -69,10 +71,10 @@ __device__ __forceinline__ void do_dot_body(const T *__restrict__ o, const T *__
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) do_dot_kernel(const T *__restrict__ o, const T *__restrict__ dO,
+__global__ void __launch_bounds__(kThreads) do_dot_kernel(Geo g, const T *__restrict__ o, const T *__restrict__ dO,
                                                           float *__restrict__ out, int64_t nrows, int D)
 {
-    do_dot_body<T>(o, dO, out, nrows, D, blockIdx.x, gridDim.x);
+    do_dot_body<T>(g, o, dO, out, nrows, D, blockIdx.x, gridDim.x);
 }
 
 // decode a linear index-row number into (b, kvh, t)
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int 
             a.x += a0.x; a.y += a0.y; a.z += a0.z; a.w += a0.w;
             c.x += c0.x; c.y += c0.y; c.z += c0.z; c.w += c0.w;
         }
-        const int64_t off = row_off(g, g.Hkv, b, kvh, k0 + kk) + d;
+        const int64_t off = dkv_off(g, b, kvh, k0 + kk) + d;
         dk[off] = from_f<T>(a.x);
         dk[off + 1] = from_f<T>(a.y);
         dk[off + 2] = from_f<T>(a.z);
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const 
     if ((int)blockIdx.x < count_blocks)
         chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, count_blocks);
     else
-        do_dot_body<T>(o, dO, out, nrows, g.D, blockIdx.x - count_blocks, gridDim.x - count_blocks);
+        do_dot_body<T>(g, o, dO, out, nrows, g.D, blockIdx.x - count_blocks, gridDim.x - count_blocks);
 }
 
 // one warp per (bg, j): exclusive prefix over chunks, list length in counts
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreads) sink_fwd_kernel(Geo g, const float *
             Ln = m + log1pf(expf(-fabsf(L - sk)));
             f = expf(L - Ln);
         }
-        T *row = o + i * g.D;
+        T *row = o + qrow_off(g, g.so, i);
         for (int d = lane; d < g.D; d += 32)
             row[d] = from_f<T>(to_f(row[d]) * f);
         if (lane == 0)
@@ -701,9 +703,9 @@ cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *de
     const int grid = grid_for(nrows, (kThreads / 32) * kDotU * rpw);
     if (dtype == NSA_DTYPE_BF16)
         do_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-            (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta, nrows, g.D);
+            g, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta, nrows, g.D);
     else
-        do_dot_kernel<float><<<grid, kThreads, 0, st>>>((const float *)o, (const float *)dO, delta,
+        do_dot_kernel<float><<<grid, kThreads, 0, st>>>(g, (const float *)o, (const float *)dO, delta,
                                                         nrows, g.D);
     return cudaGetLastError();
 }

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__re
         int b, h, t;
         decode_qrow(g, r, b, h, t);
         const int kvh = h / g.G;
-        const T *qp = q + row_off(g, g.Hq, b, h, t);
+        const T *qp = q + q_off(g, b, h, t);
         float qv[DPL], acc[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__re
                 continue;
             const int kend = min((j + 1) * g.bs, t + 1);
             for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
-                const int64_t ko = row_off(g, g.Hkv, b, kvh, kk);
+                const int64_t ko = kv_off(g, b, kvh, kk);
                 float part = 0.f;
 #pragma unroll
                 for (int i = 0; i < DPL; ++i)
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__re
                 m = mn;
             }
         }
-        T *op = o + row_off(g, g.Hq, b, h, t);
+        T *op = o + o_off(g, b, h, t);
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int i = 0; i < DPL; ++i)
@@ -141,14 +141,14 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(Geo g, const T *__res
         int b, h, t;
         decode_qrow(g, r, b, h, t);
         const int kvh = h / g.G;
-        const int64_t qo = row_off(g, g.Hq, b, h, t);
+        const int64_t qo = q_off(g, b, h, t), oo = o_off(g, b, h, t);
         const int64_t so = stat_off(g, b, h, t);
         const float L = lse[so], Dt = delta[so];
         float qv[DPL], ov[DPL], acc[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
             qv[i] = to_f(q[qo + lane + 32 * i]);
-            ov[i] = to_f(dO[qo + lane + 32 * i]);
+            ov[i] = to_f(dO[oo + lane + 32 * i]);
             acc[i] = 0.f;
         }
         if (L != -INFINITY) {
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(Geo g, const T *__res
                     continue;
                 const int kend = min((j + 1) * g.bs, t + 1);
                 for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
-                    const int64_t ko = row_off(g, g.Hkv, b, kvh, kk);
+                    const int64_t ko = kv_off(g, b, kvh, kk);
                     float ps = 0.f, pd = 0.f;
                     float kv[DPL];
 #pragma unroll
@@ -180,9 +180,10 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(Geo g, const T *__res
                 }
             }
         }
+        const int64_t dqo = dq_off(g, b, h, t);
 #pragma unroll
         for (int i = 0; i < DPL; ++i)
-            dq[qo + lane + 32 * i] = from_f<T>(acc[i] * g.scale);
+            dq[dqo + lane + 32 * i] = from_f<T>(acc[i] * g.scale);
     }
 }
 
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
         decode_krow(g, r, b, kvh, kk);
         const int j = kk / g.bs;
         const int L = seq_len(g, b);
-        const int64_t ko = row_off(g, g.Hkv, b, kvh, kk);
+        const int64_t ko = kv_off(g, b, kvh, kk);
         float kv[DPL], vv[DPL], ak[DPL], av[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
@@ -235,13 +236,13 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
             if (g.window > 0 && t - kk >= g.window)
                 break;  // tokens ascend: the rest are past the window too
             for (int h = kvh * g.G; h < (kvh + 1) * g.G; ++h) {
-                const int64_t qo = row_off(g, g.Hq, b, h, t);
+                const int64_t qo = q_off(g, b, h, t), oo = o_off(g, b, h, t);
                 const int64_t so = stat_off(g, b, h, t);
                 float qv[DPL], ov[DPL], ps = 0.f, pd = 0.f;
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) {
                     qv[i] = to_f(q[qo + lane + 32 * i]);
-                    ov[i] = to_f(dO[qo + lane + 32 * i]);
+                    ov[i] = to_f(dO[oo + lane + 32 * i]);
                     ps = fmaf(qv[i], kv[i], ps);
                     pd = fmaf(ov[i], vv[i], pd);
                 }
@@ -256,10 +257,11 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
                 }
             }
         }
+        const int64_t dko = dkv_off(g, b, kvh, kk);
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
-            dk[ko + lane + 32 * i] = from_f<T>(ak[i] * g.scale);
-            dv[ko + lane + 32 * i] = from_f<T>(av[i]);
+            dk[dko + lane + 32 * i] = from_f<T>(ak[i] * g.scale);
+            dv[dko + lane + 32 * i] = from_f<T>(av[i]);
         }
     }
 }

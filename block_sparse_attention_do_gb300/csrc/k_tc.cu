@@ -8,7 +8,12 @@ namespace nsa {
 
 bool tc_supported(const Geo &g, int dtype)
 {
-    return dtype == NSA_DTYPE_BF16 && g.D == kHead && g.bs == kKeys && g.G >= 1 && g.G <= kRows;
+    if (!(dtype == NSA_DTYPE_BF16 && g.D == kHead && g.bs == kKeys && g.G >= 1 && g.G <= kRows))
+        return false;
+    // the row-gather maps (G % 8 == 0) fold the batch index into the head or
+    // the token index: strides where neither folds go to the CUDA-core kernels
+    int bt;
+    return g.G % 8 != 0 || (rows_map_form(g, g.Hq, g.sq, bt) && rows_map_form(g, g.Hq, g.so, bt));
 }
 
 int num_sms()
@@ -45,7 +50,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 }  // namespace
 
-bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads)
+bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -59,8 +64,8 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
         dims[0] = g.D;
         dims[1] = H;
         dims[2] = g.ntok;
-        strides[0] = (cuuint64_t)g.D * es;
-        strides[1] = (cuuint64_t)H * g.D * es;
+        strides[0] = (cuuint64_t)s.h * es;
+        strides[1] = (cuuint64_t)s.t * es;
         box[0] = 64;
         box[1] = box_heads;
         box[2] = box_tok;
@@ -70,9 +75,9 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
         dims[1] = g.T;
         dims[2] = H;
         dims[3] = g.B;
-        strides[0] = (cuuint64_t)g.D * es;
-        strides[1] = (cuuint64_t)g.T * g.D * es;
-        strides[2] = (cuuint64_t)H * g.T * g.D * es;
+        strides[0] = (cuuint64_t)s.t * es;
+        strides[1] = (cuuint64_t)s.h * es;
+        strides[2] = (cuuint64_t)s.b * es;
         box[0] = 64;
         box[1] = box_tok;
         box[2] = box_heads;
@@ -86,7 +91,7 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
     return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G)
+bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G, const Strides &s, int bt)
 {
     auto fn = encode_fn();
     if (!fn || G % 8 != 0 || H % 8 != 0 || G / 8 > 256)
@@ -97,21 +102,25 @@ bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int
     dims[0] = 64;
     dims[1] = 8;
     dims[2] = 2;
-    strides[1] = 64 * es;  // the second 64-column half of a row
+    strides[0] = (cuuint64_t)s.h * es;      // the next head
+    strides[1] = 64 * es;                   // the second 64-column half of a row
+    strides[2] = 8 * (cuuint64_t)s.h * es;  // the next head octet
+    strides[3] = (cuuint64_t)s.t * es;      // the next token
     if (g.thd) {
-        // packed rows [token][H][D]
         dims[3] = H / 8;
         dims[4] = g.ntok;
-        strides[0] = (cuuint64_t)g.D * es;
-        strides[2] = 8 * (cuuint64_t)g.D * es;
-        strides[3] = (cuuint64_t)H * g.D * es;
+    } else if (bt) {
+        // (b, t) folded: token index b*T + t (needs s.b = T * s.t)
+        if (g.B > 1 && s.b != (int64_t)g.T * s.t)
+            return false;
+        dims[3] = H / 8;
+        dims[4] = (cuuint64_t)g.B * g.T;
     } else {
-        // [B][H][T][D]: (b, head) flattens to one index of stride T*D
+        // (b, head) folded into one octet index (needs s.b = H * s.h unless B = 1)
+        if (g.B > 1 && s.b != (int64_t)H * s.h)
+            return false;
         dims[3] = (cuuint64_t)g.B * H / 8;
         dims[4] = g.T;
-        strides[0] = (cuuint64_t)g.T * g.D * es;
-        strides[2] = 8 * (cuuint64_t)g.T * g.D * es;
-        strides[3] = (cuuint64_t)g.D * es;
     }
     if (dims[3] == 0 || dims[4] == 0)
         return false;

@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         const CUtensorMap *map = tensor ? &tm_do : &tm_q;
                         if (g.thd)
                             tma_load_5d(dst, map, full, 0, 0, 0, kvh * G / 8, g.cu[b] + t);
+                        else if (tensor ? g.o_bt : g.q_bt)  // batch folded into the token index
+                            tma_load_5d(dst, map, full, 0, 0, 0, kvh * G / 8, b * g.T + t);
                         else
                             tma_load_5d(dst, map, full, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
                     }
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         const __nv_bfloat16 *base = tensor ? p.dO : p.q;
                         const __nv_bfloat16 *src = base;
                         if (valid)
-                            src = base + row_off(g, g.Hq, b, kvh * G + hh, tok[tl]) + c * 8;
+                            src = base + (tensor ? o_off(g, b, kvh * G + hh, tok[tl]) : q_off(g, b, kvh * G + hh, tok[tl])) + c * 8;
                         const uint32_t dst = (tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes) +
                                              rg_off(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4);
                         cp_async_16(dst, src, valid ? 16u : 0u);
@@ -599,13 +601,13 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     ok = false;
                     break;
                 }
-                // distance between consecutive keys: D (BHTD) or Hkv*D (THD)
-                const int64_t kstride = g.thd ? (int64_t)g.Hkv * kHead : kHead;
+                // distance between consecutive keys (elements)
+                const int64_t kstride = g.sdkv.t;
 #pragma unroll 4
                 for (int q = r; q < 2 * kKeys * 16; q += kRows) {
                     const int which = q / (kKeys * 16), c = (q >> 4) & (kKeys - 1), ch = q & 15;
                     if (c < nk) {
-                        __nv_bfloat16 *out = (which == 0 ? p.dk : p.dv) + row_off(g, g.Hkv, b, kvh, k0) + c * kstride;
+                        __nv_bfloat16 *out = (which == 0 ? p.dk : p.dv) + dkv_off(g, b, kvh, k0) + c * kstride;
                         *(uint4 *)(out + ch * 8) =
                             *(const uint4 *)(sm + (which == 0 ? OFF_DS : OFF_P) + c * (kHead * 2) + ch * 16);
                     }
@@ -642,9 +644,10 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
 {
     CUtensorMap tq, tdo, tk, tv;
     const bool gather_tma = (g.G % 8) == 0;
-    const bool qmaps = gather_tma ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
-                                  : make_tmap(&tq, q, g, g.Hq, 1, 1) && make_tmap(&tdo, dO, g, g.Hq, 1, 1);
-    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    const bool qmaps = gather_tma ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) &&
+                                        make_tmap_rows(&tdo, dO, g, g.Hq, g.G, g.so, g.o_bt)
+                                  : make_tmap(&tq, q, g, g.Hq, 1, 1, g.sq) && make_tmap(&tdo, dO, g, g.Hq, 1, 1, g.so);
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;

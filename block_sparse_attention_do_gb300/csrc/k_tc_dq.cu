@@ -230,7 +230,10 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 uint8_t *base = sm + (tensor ? OFF_DO : OFF_Q);
                 if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
                     for (int tl = lane; tl < Tq; tl += 32)
-                        tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t0 + tl);
+                        if (tensor ? g.o_bt : g.q_bt)  // batch folded into the token index
+                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, kvh * G / 8, b * g.T + t0 + tl);
+                        else
+                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t0 + tl);
                 } else if (lane < 2) {
                     const int h = lane;
                     if (g.thd)
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const bool rvalid = r < nrows && tl < nvalid;
             const int t = t0 + tl;
             // the row's dQ columns e*64 .. e*64+63
-            __nv_bfloat16 *dst = rvalid ? p.dq + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64 : nullptr;
+            __nv_bfloat16 *dst = rvalid ? p.dq + dq_off(g, b, kvh * G + hh, t) + e * 64 : nullptr;
             const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
             bool ok = true;
             for (int i = 0; i < npairs; ++i, ++gi) {
@@ -638,9 +641,10 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     const int smem = base + nk * kTileBytes + nub * up.bytes;
     CUtensorMap tq, tdo, tk, tv;
     const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q/dO tiles, one box per token and tensor
-    const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G)
-                          : make_tmap(&tq, q, g, g.Hq, Tq, g.G) && make_tmap(&tdo, dO, g, g.Hq, Tq, g.G);
-    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) &&
+                                make_tmap_rows(&tdo, dO, g, g.Hq, g.G, g.so, g.o_bt)
+                          : make_tmap(&tq, q, g, g.Hq, Tq, g.G, g.sq) && make_tmap(&tdo, dO, g, g.Hq, Tq, g.G, g.so);
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;
@@ -653,7 +657,8 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
     p.nk = nk;
-    p.v8 = ((uintptr_t)dq & 31) == 0;
+    // 32-byte stores when every row of dq starts on a 32-byte boundary
+    p.v8 = ((uintptr_t)dq & 31) == 0 && (g.sdq.h % 16) == 0 && (g.sdq.t % 16) == 0 && (g.sdq.b % 16) == 0;
     p.tile_next = tile_next;
     p.wait_us = wait_test().wait_us;
     p.stall = wait_test().kernel == WAIT_TEST_DQ;

@@ -216,9 +216,14 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             __syncwarp();
             lastq = k;
             if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
-                for (int tl = lane; tl < Tq; tl += 32)
-                    tma_load_5d(sm + OFF_Q + tl * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, (b * g.Hq + kvh * G) / 8,
-                                t0 + tl);
+                for (int tl = lane; tl < Tq; tl += 32) {
+                    if (g.q_bt)  // batch folded into the token index
+                        tma_load_5d(sm + OFF_Q + tl * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, kvh * G / 8,
+                                    b * g.T + t0 + tl);
+                    else
+                        tma_load_5d(sm + OFF_Q + tl * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, (b * g.Hq + kvh * G) / 8,
+                                    t0 + tl);
+                }
             } else if (lane < 2) {
                 const int h = lane;
                 if (g.thd)
@@ -516,7 +521,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             if (!mbar_wait_warp(&bars[B_ACCFULL], k & 1, abort_flag))
                 break;
             tc_fence_after();
-            __nv_bfloat16 *dst = rvalid ? p.o + row_off(g, g.Hq, b, kvh * G + hh, t) + e * 64 : nullptr;
+            __nv_bfloat16 *dst = rvalid ? p.o + o_off(g, b, kvh * G + hh, t) + e * 64 : nullptr;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t o0[32], o1[32];
@@ -582,8 +587,8 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
     CUtensorMap tq, tk, tv;
     const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q tile, one box per token
-    const bool qmap = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G) : make_tmap(&tq, q, g, g.Hq, Tq, g.G);
-    if (!qmap || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1))
+    const bool qmap = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) : make_tmap(&tq, q, g, g.Hq, Tq, g.G, g.sq);
+    if (!qmap || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;
@@ -594,7 +599,8 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     p.err = err;
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     p.nub = nub;
-    p.v8 = ((uintptr_t)o & 31) == 0;
+    // 32-byte stores when every row of o starts on a 32-byte boundary
+    p.v8 = ((uintptr_t)o & 31) == 0 && (g.so.h % 16) == 0 && (g.so.t % 16) == 0 && (g.so.b % 16) == 0;
     p.tile_next = tile_next;
     p.wait_us = wait_test().wait_us;
     p.stall = wait_test().kernel == WAIT_TEST_FWD;

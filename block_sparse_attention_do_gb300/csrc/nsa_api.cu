@@ -20,6 +20,24 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 enum Mode { SPARSE = 0, DENSE = 1 };
 
+// One tensor's declared (batch, head, token) strides into `out`: all zero
+// selects the dense layout with H heads; otherwise every stride in use must
+// be positive, a multiple of 16 bytes and below 2^40 bytes (the tensor-map
+// limits).  THD ignores the batch entry.
+bool take_strides(const int64_t in[3], const nsa_problem *p, bool thd, int H, Strides &out)
+{
+    const int64_t D = p->D, es = p->dtype == NSA_DTYPE_BF16 ? 2 : 4;
+    if (in[0] == 0 && in[1] == 0 && in[2] == 0) {
+        out = thd ? Strides{0, D, (int64_t)H * D} : Strides{(int64_t)H * p->T * D, (int64_t)p->T * D, D};
+        return true;
+    }
+    for (int i = thd ? 1 : 0; i < 3; ++i)
+        if (in[i] <= 0 || (in[i] * es) % 16 != 0 || in[i] * es >= ((int64_t)1 << 40))
+            return false;
+    out = Strides{thd ? 0 : in[0], in[1], in[2]};
+    return true;
+}
+
 // Checks the problem and fills the device geometry.  `want_thd` is the
 // layout the entry point requires.
 nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g, int window = 0)
@@ -75,6 +93,17 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     g.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->D);
     g.scale_l2 = g.scale * 1.4426950408889634f;
     g.cu = cu;
+    if (!take_strides(p->q_stride, p, want_thd, p->Hq, g.sq) || !take_strides(p->kv_stride, p, want_thd, p->Hkv, g.skv) ||
+        !take_strides(p->o_stride, p, want_thd, p->Hq, g.so) || !take_strides(p->dq_stride, p, want_thd, p->Hq, g.sdq) ||
+        !take_strides(p->dkv_stride, p, want_thd, p->Hkv, g.sdkv))
+        return NSA_ERR_INVALID_ARG;
+    // the row-gather maps of q and o fold the batch into the token index when
+    // it does not fold into the head index (a packed [B, T, H, D] tensor)
+    auto bt = [&](const Strides &st, int H) {
+        return !want_thd && p->B > 1 && st.b != (int64_t)H * st.h && st.b == (int64_t)p->T * st.t;
+    };
+    g.q_bt = bt(g.sq, p->Hq);
+    g.o_bt = bt(g.so, p->Hq);
     return NSA_OK;
 }
 

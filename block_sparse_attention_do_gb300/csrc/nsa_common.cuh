@@ -14,6 +14,12 @@
 
 namespace nsa {
 
+// Element strides of (batch, head, token) of one tensor; the head dimension
+// is contiguous.  THD: `b` is unused and `t` steps one packed row.
+struct Strides {
+    int64_t b, h, t;
+};
+
 // Device-side view of an nsa_problem plus derived quantities.
 struct Geo {
     int B, Hq, Hkv, G, T, D, bs, S;
@@ -25,6 +31,12 @@ struct Geo {
     float scale;     // softmax scale
     float scale_l2;  // scale * log2(e)
     const int *cu;   // cu_seqlens (THD) or nullptr
+    Strides sq;      // q
+    Strides skv;     // k and v
+    Strides so;      // o and dO
+    Strides sdq;     // dq
+    Strides sdkv;    // dk and dv
+    int q_bt, o_bt;  // BHTD q / o: batch and token fold into one row index (b*T + t) for the row-gather maps
 };
 
 __device__ __forceinline__ int seq_len(const Geo &g, int b) { return g.thd ? g.cu[b + 1] - g.cu[b] : g.T; }
@@ -35,12 +47,27 @@ __host__ __device__ __forceinline__ int key_lo(const Geo &g, int t)
     return (g.window > 0 && t - g.window + 1 > 0) ? t - g.window + 1 : 0;
 }
 
-// element offset of the D-vector of (b, head, t) in a tensor with H heads
-__device__ __forceinline__ int64_t row_off(const Geo &g, int H, int b, int h, int t)
+// element offset of the D-vector of (b, head h, token t) in a tensor with strides s
+__device__ __forceinline__ int64_t vec_off(const Geo &g, const Strides &s, int b, int h, int t)
 {
     if (g.thd)
-        return ((int64_t)(g.cu[b] + t) * H + h) * g.D;
-    return (((int64_t)b * H + h) * g.T + t) * g.D;
+        return (int64_t)(g.cu[b] + t) * s.t + (int64_t)h * s.h;
+    return (int64_t)b * s.b + (int64_t)h * s.h + (int64_t)t * s.t;
+}
+__device__ __forceinline__ int64_t q_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sq, b, h, t); }
+__device__ __forceinline__ int64_t o_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.so, b, h, t); }
+__device__ __forceinline__ int64_t kv_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.skv, b, h, t); }
+__device__ __forceinline__ int64_t dq_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sdq, b, h, t); }
+__device__ __forceinline__ int64_t dkv_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sdkv, b, h, t); }
+
+// the D-vector of query row number r (the row order of lse and delta: BHTD
+// (b*Hq + h)*T + t, THD token*Hq + h) in a tensor with strides s
+__device__ __forceinline__ int64_t qrow_off(const Geo &g, const Strides &s, int64_t r)
+{
+    if (g.thd)
+        return (r / g.Hq) * s.t + (r % g.Hq) * s.h;
+    const int64_t bh = r / g.T;
+    return (bh / g.Hq) * s.b + (bh % g.Hq) * s.h + (r % g.T) * s.t;
 }
 
 // offset of a per-row scalar (lse, delta) of (b, query head h, t)

@@ -28,7 +28,7 @@ constexpr int kKvBytes = 2 * kKvHalfBytes;
 // `box_heads` heads x 64 columns; the smem result is box_tok*box_heads rows
 // of 128 bytes, 128B-swizzled, in (token-major for THD, head-major for BHTD)
 // order.
-bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads);
+bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s);
 
 // Row-group tile layout (gathered rows of the dK/dV kernel): the tile's
 // rows go in groups of 8; group R/8 occupies 2048 bytes, its 64-column half h
@@ -42,9 +42,25 @@ __host__ __device__ inline int rg_off(int r, int half) { return (r >> 3) * kRgSt
 // Tensor map whose box is one token's G consecutive query heads (G % 8 == 0,
 // H % 8 == 0), both 64-column halves, in the row-group layout above:
 // box {64 columns, 8 heads, 2 halves, G/8 head octets, 1 token}.
-// Coordinates: (0, 0, 0, octet, token) with octet = (b*H + head0)/8 (BHTD)
-// or head0/8 (THD, token = packed row).
-bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G);
+// Coordinates: (0, 0, 0, octet, token) with octet = (b*H + head0)/8 (BHTD,
+// batch and head folded into one index: needs s.b = H * s.h or B = 1), or
+// octet = head0/8 and token = b*T + t (BHTD with bt set: batch and token
+// folded, needs s.b = T * s.t) or the packed row (THD).
+bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G, const Strides &s, int bt);
+
+// Whether the row-gather map of a BHTD tensor with these strides can be
+// built, and in which form (bt: batch folded into the token index).
+inline bool rows_map_form(const Geo &g, int H, const Strides &s, int &bt)
+{
+    bt = 0;
+    if (g.thd || g.B == 1 || s.b == (int64_t)H * s.h)
+        return true;
+    if (s.b == (int64_t)g.T * s.t) {
+        bt = 1;
+        return true;
+    }
+    return false;
+}
 
 // the host launcher's view of the device: SM count (cached)
 int num_sms();

@@ -27,8 +27,9 @@
  * LSE = -inf and contributes no gradient.
  *
  * Conventions for every entry point:
- *  - All tensor arguments are DEVICE pointers owned by the caller, dense in
- *    the layout named by nsa_problem.layout, 16-byte aligned.  The library
+ *  - All tensor arguments are DEVICE pointers owned by the caller, in the
+ *    layout named by nsa_problem.layout with the strides the problem
+ *    declares (dense when they are 0), 16-byte aligned.  The library
  *    never allocates or frees memory and never synchronises: work is
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - Shape, dtype and layout errors are returned synchronously before any
@@ -88,6 +89,26 @@ typedef struct nsa_problem {
     int32_t layout;       /* NSA_LAYOUT_*; the varlen entry points require THD, the others BHTD */
     int32_t total_tokens; /* THD: cu_seqlens[B]; ignored for BHTD */
     float scale;          /* softmax scale; <= 0 selects 1/sqrt(D) */
+    int32_t reserved;     /* set to 0 */
+    /*
+     * Declared strides (cuDNN-frontend page: the SM80 port's "declared
+     * strides", no pad/gather copies of non-compact operands), in ELEMENTS,
+     * of (batch, head, token) for each tensor; the head dimension D is always
+     * contiguous.  All three 0 selects the dense layout of `layout` (the
+     * shapes listed above), so a zero-initialised struct describes dense
+     * tensors.  THD: the batch entry is ignored and the token entry is the
+     * step between packed rows.  Every stride in use must be positive, a
+     * multiple of 16 bytes (8 bf16 or 4 fp32 elements) and below 2^40 bytes,
+     * else the call returns NSA_ERR_INVALID_ARG.  Example: q, k, v sliced
+     * out of one packed [B, T, Hq + 2*Hkv, D] tensor have (batch, head, token)
+     * strides (T*(Hq+2*Hkv)*D, D, (Hq+2*Hkv)*D).  Outputs must not overlap
+     * each other or any input.
+     */
+    int64_t q_stride[3];   /* q */
+    int64_t kv_stride[3];  /* k and v */
+    int64_t o_stride[3];   /* o (written by the forward, read by the backward) and dO */
+    int64_t dq_stride[3];  /* dq */
+    int64_t dkv_stride[3]; /* dk and dv */
 } nsa_problem;
 
 /* Workspace bytes needed by the forward / backward entry points (0 on an invalid problem). */

@@ -222,6 +222,10 @@ def sel_blocks(q, k, v, idx, dO, bs, blocks, scale=None, cu_seqlens=None, window
     B, Hq, Hkv, T, D, S = _shape(q, k, idx, cu)
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
     blocks = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64).reshape(-1, 3))
+    nb = -(-T // bs) if cu is None else -(-int(np.max(np.diff(cu))) // bs)
+    if blocks.size and (blocks.min() < 0 or blocks[:, 0].max() >= B or blocks[:, 1].max() >= Hkv
+                        or blocks[:, 2].max() >= nb):
+        raise ValueError("sel_blocks: (b, g, j) out of range")
     jb, jg, jj = (np.ascontiguousarray(blocks[:, i]) for i in range(3))
     n = blocks.shape[0]
     dk, dv = np.zeros((n, bs, D)), np.zeros((n, bs, D))

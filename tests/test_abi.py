@@ -140,3 +140,33 @@ def test_noalloc_status_pointer_alignment(lib):
     dummy = C.c_void_p(256)
     s = lib.nsa_build_inverse_index_noalloc(C.byref(p), None, dummy, dummy, dummy, C.c_void_p(258), None)
     assert s == 1  # NSA_ERR_INVALID_ARG: status_out not 4-byte aligned
+
+
+def test_declared_strides_are_checked(lib):
+    """Strides must be positive multiples of 16 bytes; all-zero strides mean
+    the dense layout (the other tests pass zero-initialised problems)."""
+    from block_sparse_attention_do_gb300 import api
+
+    p = _p()
+    n_dense = api.bwd_workspace_size(p)
+    assert n_dense > 0
+    args = [C.c_void_p(256)] * 6
+    ws = C.c_void_p(256)
+    # a token stride of D + 1 bf16 elements: not a 16-byte multiple
+    p.q_stride[:] = (4 * 256 * 129, 256 * 129, 129)
+    assert lib.nsa_sel_fwd(C.byref(p), *args, ws, 1 << 30, None) == 1
+    assert api.bwd_workspace_size(p) == 0
+    # a zero head stride among non-zero ones
+    p.q_stride[:] = (4 * 256 * 128, 0, 128)
+    assert lib.nsa_sel_fwd(C.byref(p), *args, ws, 1 << 30, None) == 1
+    # the dense strides written out equal the zero default
+    p.q_stride[:] = (4 * 256 * 128, 256 * 128, 128)
+    assert api.bwd_workspace_size(p) == n_dense
+    # THD ignores the batch entry
+    pt = api.problem(2, 4, 2, 256, 128, 64, 4, __import__("torch").bfloat16, layout=1, total_tokens=300)
+    pt.kv_stride[:] = (7, 128, 4 * 128)
+    assert api.fwd_workspace_size(pt) > 0
+    pt.kv_stride[:] = (0, 129, 4 * 128)
+    assert api.fwd_workspace_size(pt) == 0
+    assert lib.nsa_sel_varlen_fwd(C.byref(pt), C.c_void_p(256), *([C.c_void_p(256)] * 6), ws, 1 << 30,
+                                  None) == 1

@@ -412,7 +412,7 @@ def _list_lengths(idx, bs, cu=None):
     """[(b, g, j, number of tokens selecting block j)] from the oracle's
     inverse index."""
     off, _, nb = oracle.inverse_index(idx, bs, cu_seqlens=cu)
-    Hkv = idx.shape[-2]
+    Hkv = idx.shape[1]  # [B, Hkv, T, S] or packed [total, Hkv, S]
     n = np.diff(off.astype(np.int64))
     out = []
     for x, c in enumerate(n):
@@ -455,9 +455,10 @@ def _sample_blocks(rng, lists, G, bs, lengths, n_split=4):
     blocks.add((0, 0, 0))
     for x in rng.permutation(len(split))[:n_split]:
         blocks.add(split[int(x)])
+    Hkv = max(g for _, g, _, _ in lists) + 1
     for b, L in enumerate(lengths[:2]):
         last = (L - 1) // bs
-        blocks.add((b, int(rng.integers(0, lists[-1][1] + 1)), last))
+        blocks.add((b, int(rng.integers(0, Hkv)), last))
         if last > 0:
             blocks.add((b, 0, last - 1))
     return sorted(blocks), len(split)
@@ -669,3 +670,77 @@ def test_sinks_dense(dtype, shape, window, thd):
     tol = TOL[dtype]
     assert np.all(np.abs(got - ref["dsinks"]) <= tol * np.maximum(1.0, np.abs(ref["dsinks"]))), \
         (got, ref["dsinks"])
+
+
+# ---- declared strides: q, k, v (and dq, dk, dv) as views of packed tensors
+
+
+def _packed_views(x_q, x_k, x_v, thd, pad_tokens=0):
+    """q, k, v copied into one packed tensor ([B, T(+pad), Hq + 2 Hkv, D], or
+    [total, Hq + 2 Hkv, D]) and returned as non-contiguous views of it."""
+    if thd:
+        total, Hq, D = x_q.shape
+        Hkv = x_k.shape[1]
+        pk = torch.empty(total, Hq + 2 * Hkv, D, dtype=x_q.dtype, device=DEV)
+        q, k, v = pk[:, :Hq], pk[:, Hq:Hq + Hkv], pk[:, Hq + Hkv:]
+    else:
+        B, Hq, T, D = x_q.shape
+        Hkv = x_k.shape[1]
+        pk = torch.zeros(B, T + pad_tokens, Hq + 2 * Hkv, D, dtype=x_q.dtype, device=DEV)
+        q = pk[:, :T, :Hq].transpose(1, 2)
+        k = pk[:, :T, Hq:Hq + Hkv].transpose(1, 2)
+        v = pk[:, :T, Hq + Hkv:].transpose(1, 2)
+    q.copy_(x_q)
+    k.copy_(x_k)
+    v.copy_(x_v)
+    assert not q.is_contiguous() and not k.is_contiguous()
+    return q, k, v
+
+
+@pytest.mark.parametrize("dtype,shape,pad", [
+    (torch.bfloat16, (2, 32, 2, 300, 128, 64, 4), 0),  # tensor cores, row-gather maps (batch folded into tokens)
+    (torch.bfloat16, (2, 8, 2, 200, 128, 64, 3), 0),   # tensor cores, G = 4: tile maps and cp.async gathers
+    (torch.float32, (2, 6, 2, 150, 64, 32, 3), 0),     # CUDA cores
+    (torch.bfloat16, (2, 16, 1, 130, 128, 64, 3), 8),  # padded token capacity: batch folds nowhere (CUDA cores)
+])
+def test_declared_strides_packed_qkv(dtype, shape, pad):
+    """q, k, v are views of one packed [B, T, Hq + 2 Hkv, D] tensor and
+    dq, dk, dv views of another: the kernels read and write them in place
+    through the declared strides, and the results match the oracle."""
+    B, Hq, Hkv, T, D, bs, S = shape
+    xq, xk, xv, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=26)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=26)
+    q, k, v = _packed_views(xq.to(DEV), xk.to(DEV), xv.to(DEV), False, pad)
+    dq, dk, dv = _packed_views(torch.zeros_like(xq, device=DEV), torch.zeros_like(xk, device=DEV),
+                               torch.zeros_like(xv, device=DEV), False, pad)
+    gi, gdo = idx.to(DEV), do.to(DEV)
+    o, lse = api.sel_fwd(q, k, v, gi, bs)
+    api.sel_bwd(q, k, v, o, gdo, lse, gi, bs, out=(dq, dk, dv))
+    torch.cuda.synchronize()
+    ref = oracle.sel_bwd(xq, xk, xv, idx, do, bs)
+    _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, dtype)
+
+
+def test_declared_strides_packed_thd():
+    """The packed variable-length layout with q, k, v (and the gradients) as
+    views of one [total, Hq + 2 Hkv, D] tensor; o and dO as views too."""
+    lengths = [130, 1, 64, 257, 90]
+    Hq, Hkv, D, bs, S = 32, 2, 128, 64, 4
+    cu = inputs.cu_seqlens_from_lengths(lengths)
+    total = sum(lengths)
+    xq, xk, xv, do = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=torch.bfloat16, seed=27, layout="thd")
+    idx = inputs.make_varlen_block_idx(lengths, Hkv, bs, S, seed=27)
+    q, k, v = _packed_views(xq.to(DEV), xk.to(DEV), xv.to(DEV), True)
+    dq, dk, dv = _packed_views(torch.zeros_like(xq, device=DEV), torch.zeros_like(xk, device=DEV),
+                               torch.zeros_like(xv, device=DEV), True)
+    # o and dO interleaved in one [total, 2 Hq, D] tensor
+    od = torch.empty(total, 2 * Hq, D, dtype=torch.bfloat16, device=DEV)
+    o_view, do_view = od[:, :Hq], od[:, Hq:]
+    do_view.copy_(do.to(DEV))
+    gi, gcu = idx.to(DEV), cu.to(DEV)
+    o, lse = api.sel_fwd(q, k, v, gi, bs, cu_seqlens=gcu)
+    o_view.copy_(o)
+    api.sel_bwd(q, k, v, o_view, do_view, lse, gi, bs, cu_seqlens=gcu, out=(dq, dk, dv))
+    torch.cuda.synchronize()
+    ref = oracle.sel_bwd(xq, xk, xv, idx, do, bs, cu_seqlens=cu)
+    _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, torch.bfloat16)
