@@ -35,16 +35,17 @@ using namespace tc;
 // shared-memory plan (bytes from a 1024-aligned base)
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKvBytes;
-constexpr int NQ = 3;                            // Q stages
+constexpr int NQ = 2;                            // Q stages
 constexpr int NDO = 2;                           // dO stages
 constexpr int NSB = 3;                           // S/dP TMEM buffers
 constexpr int OFF_Q = OFF_V + kKvBytes;
 constexpr int OFF_DO = OFF_Q + NQ * kTileBytes;
-constexpr int OFF_P = OFF_DO + NDO * kTileBytes;
-constexpr int OFF_DS = OFF_P + kRows * 128;
-constexpr int OFF_TOK = OFF_DS + kRows * 128;    // int [NQ][128]: a tile's token ids, one slot per Q stage
+constexpr int NPB = 2;                           // P and dS shared-memory buffers
+constexpr int OFF_P = OFF_DO + NDO * kTileBytes; // P buffer x at OFF_P + x * kRows * 128
+constexpr int OFF_DS = OFF_P + NPB * kRows * 128;
+constexpr int OFF_TOK = OFF_DS + NPB * kRows * 128;  // int [NQ][128]: a tile's token ids, one slot per Q stage
 constexpr int OFF_BAR = OFF_TOK + NQ * kRows * 4;
-constexpr int NUM_BARS = 36;
+constexpr int NUM_BARS = 40;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 
@@ -53,8 +54,9 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
 enum {
     B_QFULL0 = 0, B_QEMPTY0 = B_QFULL0 + NQ, B_IDX0 = B_QEMPTY0 + NQ, B_DOFULL0 = B_IDX0 + NQ,
     B_DOEMPTY0 = B_DOFULL0 + NDO, B_KVFULL = B_DOEMPTY0 + NDO, B_KVEMPTY, B_SFULL0,
-    B_SFREE0 = B_SFULL0 + NSB, B_DPFULL0 = B_SFREE0 + NSB, B_PFULL = B_DPFULL0 + NSB, B_PFREE, B_ACCFULL,
-    B_ACCEMPTY, B_DONE0, B_DONE1, B_DONE2, B_DONE3, B_DSFULL, B_DSFREE, B_STAGED, B_COPIED, B_COUNT
+    B_SFREE0 = B_SFULL0 + NSB, B_DPFULL0 = B_SFREE0 + NSB, B_PFULL0 = B_DPFULL0 + NSB, B_PFREE0 = B_PFULL0 + NPB,
+    B_DSFULL0 = B_PFREE0 + NPB, B_DSFREE0 = B_DSFULL0 + NPB, B_ACCFULL = B_DSFREE0 + NPB, B_ACCEMPTY, B_DONE0,
+    B_DONE1, B_DONE2, B_DONE3, B_STAGED, B_COPIED, B_COUNT
 };
 static_assert(B_COUNT <= NUM_BARS, "barrier slots");
 static_assert(OFF_MISC + 64 + 1024 <= 232448, "shared memory");
@@ -128,10 +130,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             mbar_init(&bars[B_DPFULL0 + x], 1);
             mbar_init(&bars[B_SFREE0 + x], kRows);
         }
-        mbar_init(&bars[B_PFULL], kRows);
-        mbar_init(&bars[B_PFREE], 1);
-        mbar_init(&bars[B_DSFULL], kRows);
-        mbar_init(&bars[B_DSFREE], 1);
+        for (int x = 0; x < NPB; ++x) {
+            mbar_init(&bars[B_PFULL0 + x], kRows);
+            mbar_init(&bars[B_PFREE0 + x], 1);
+            mbar_init(&bars[B_DSFULL0 + x], kRows);
+            mbar_init(&bars[B_DSFREE0 + x], 1);
+        }
         mbar_init(&bars[B_ACCFULL], 2);
         mbar_init(&bars[B_ACCEMPTY], kRows);
         mbar_init(&bars[B_STAGED], kRows);
@@ -388,7 +392,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         // P (dV) or dS (dK) of the tile is in shared memory (and
                         // for dV the tile's dO rows have landed); at a unit's
                         // start the epilogue has read the accumulators
-                        if (!mbar_wait(&bars[role == 2 ? B_PFULL : B_DSFULL], it & 1, abort_flag) ||
+                        const int pbuf = it % NPB;  // the tile's P / dS buffer
+                        if (!mbar_wait(&bars[(role == 2 ? B_PFULL0 : B_DSFULL0) + pbuf], (it / NPB) & 1, abort_flag) ||
                             (role == 2 && !mbar_wait(&bars[B_DOFULL0 + st], (it >> 1) & 1, abort_flag)) ||
                             (ti == 0 && !mbar_wait(&bars[B_ACCEMPTY], (uc & 1) ^ 1, abort_flag))) {
                             ok = false;
@@ -396,12 +401,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         }
                         tc_fence_after();
                         const uint32_t col = tmem + (role == 2 ? TM_DV : TM_DK);
-                        const uint32_t pb = role == 2 ? p_s : ds_s;
+                        const uint32_t pb = (role == 2 ? p_s : ds_s) + pbuf * (kRows * 128);
                         for (int kr = 0; kr < kRows / 16; ++kr)
                             // 16 rows = two row groups; LBO steps the 64-dim halves (M)
                             mma_bf16(col, sdesc_sw128(a_s + kr * 2 * kRgStride, kRgHalf, kRgStride),
                                      sdesc_sw128(pb + kr * 2048, 8192, 1024), idV, (ti > 0 || kr > 0) ? 1u : 0u);
-                        mma_commit(&bars[role == 2 ? B_PFREE : B_DSFREE]);
+                        mma_commit(&bars[(role == 2 ? B_PFREE0 : B_DSFREE0) + pbuf]);
                         mma_commit(&bars[role == 2 ? B_DOEMPTY0 + st : B_QEMPTY0 + qs]);
                         if (ti + 1 == ntiles)
                             mma_commit(&bars[B_ACCFULL]);
@@ -509,15 +514,17 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
 #pragma unroll
                 for (int c = 0; c < 64; c += 2)
                     pk[c >> 1] = pack_bf16(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
-                if (!mbar_wait_warp(&bars[B_PFREE], (it & 1) ^ 1, abort_flag)) {
+                const int pbuf = it % NPB;  // this tile's P / dS buffer
+                if (!mbar_wait_warp(&bars[B_PFREE0 + pbuf], ((it / NPB) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_shared_v4(p_row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    st_shared_v4(p_row + pbuf * (kRows * 128) + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                                 pk[4 * c + 2], pk[4 * c + 3]);
                 fence_async_smem();
-                mbar_arrive(&bars[B_PFULL]);
+                mbar_arrive(&bars[B_PFULL0 + pbuf]);
                 if (!prefetch()) {
                     ok = false;
                     break;
@@ -546,16 +553,16 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)), d0, d1);
                     dk_[c >> 1] = pack_bf16(d0, d1);
                 }
-                if (!mbar_wait_warp(&bars[B_DSFREE], (it & 1) ^ 1, abort_flag)) {
+                if (!mbar_wait_warp(&bars[B_DSFREE0 + pbuf], ((it / NPB) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_shared_v4(ds_row + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
+                    st_shared_v4(ds_row + pbuf * (kRows * 128) + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
                                  dk_[4 * c + 3]);
                 fence_async_smem();
-                mbar_arrive(&bars[B_DSFULL]);
+                mbar_arrive(&bars[B_DSFULL0 + pbuf]);
             }
             if (!ok)
                 break;
