@@ -14,8 +14,9 @@
 //
 // Roles (11 warps):  warps 0 and 3 load (TMA for K_j/V_j; Q rows from warp 0
 // and dO rows from warp 3 by one TMA box per token -- its G heads, both
-// halves -- when G % 8 == 0, else both by 16-byte cp.async from warp 0 with
-// the swizzle applied by hand); warp 1 resolves each tile's token ids a tile
+// halves -- when G % 8 == 0; else by 16-byte cp.async, two whole rows per
+// warp instruction with the swizzle applied by hand, each tile released once
+// the next tile's copies are out); warp 1 resolves each tile's token ids a tile
 // ahead; warp 2 owns TMEM; one thread each of warps 2, 8, 9 and 10 issues the
 // S, dP, dV^T and dK^T MMAs; warps 4-7 compute P/dS for one row each (reading
 // the row's LSE and delta themselves) and run the epilogue.  Q has three
@@ -35,12 +36,12 @@ using namespace tc;
 // shared-memory plan (bytes from a 1024-aligned base)
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + kKvBytes;
-constexpr int NQ = 2;                            // Q stages
+constexpr int NQ = 3;                            // Q stages
 constexpr int NDO = 2;                           // dO stages
 constexpr int NSB = 3;                           // S/dP TMEM buffers
 constexpr int OFF_Q = OFF_V + kKvBytes;
 constexpr int OFF_DO = OFF_Q + NQ * kTileBytes;
-constexpr int NPB = 2;                           // P and dS shared-memory buffers
+constexpr int NPB = 1;                           // P and dS shared-memory buffers (a second one measured slower: it costs a Q stage)
 constexpr int OFF_P = OFF_DO + NDO * kTileBytes; // P buffer x at OFF_P + x * kRows * 128
 constexpr int OFF_DS = OFF_P + NPB * kRows * 128;
 constexpr int OFF_TOK = OFF_DS + NPB * kRows * 128;  // int [NQ][128]: a tile's token ids, one slot per Q stage
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     // this kernel writes: let it take each SM as this kernel's CTA there ends.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0 || (GATHER_TMA && warp == 3)) {
+    if (warp == 0 || warp == 3) {
         // ------------------------------------------------------- tile loader
         // K_j / V_j once per unit (warp 0); per tile, once the indexer has
         // published the tile's tokens (it does so when the tile's Q stage is
@@ -185,11 +186,24 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         }
         int it = 0, uc = 0, qs = 0, qph = 0;  // tile count; its Q stage and that stage's phase
         int last_tile = -1, last_kv = -1;     // newest TMA batches (for the abort path)
+        uint64_t *pend = nullptr;             // cp.async gather: the tile whose release is still due
+        // releases the pending cp.async tile (all of this lane's copies landed)
+        auto flush = [&]() {
+            if (!GATHER_TMA && pend) {
+                cp_async_wait<0>();
+                fence_async_smem();
+                mbar_arrive(pend);
+                pend = nullptr;
+            }
+        };
         bool okl = true;
         for (int ui; (ui = unit_of(uc, n_units)) >= 0 && okl; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int ntiles = (u.count + Tt - 1) / Tt;
+            // the K/V stage frees once the previous unit's last S and dP have
+            // run, which needs that unit's last tile released first
+            flush();
             if (tensor == 0 && !mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
                 okl = false;
                 break;
@@ -213,8 +227,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
                 const int ds = it & 1;  // dO stage
                 if (!mbar_wait_warp(&bars[B_IDX0 + qs], qph, abort_flag) ||
-                    ((tensor == 1 || !GATHER_TMA) &&
-                     !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag))) {
+                    (tensor == 1 && !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag))) {
                     okl = false;
                     break;
                 }
@@ -240,26 +253,42 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             tma_load_5d(dst, map, full, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
                     }
                 } else {
-                    // 2 tensors x 128 rows x 16 chunks of 16 bytes
-                    for (int item = lane; item < 2 * kRows * 16; item += 32) {
-                        const int tensor = item / (kRows * 16);
-                        const int rem = item % (kRows * 16);
-                        const int r = rem >> 4, c = rem & 15;
-                        const int tl = r / G, hh = r % G;
+                    // this warp's tensor: 128 rows x 16 chunks of 16 bytes, two
+                    // whole rows (256 contiguous bytes each) per warp
+                    // instruction; rows past the tile's tokens are zero-filled.
+                    // Each lane's arrival lands once its copies have.
+                    const __nv_bfloat16 *base = tensor ? p.dO : p.q;
+                    const Strides &str = tensor ? g.so : g.sq;
+                    const uint32_t tile_s = tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes;
+                    const int c = lane & 15;
+                    const int64_t hbase = (int64_t)(kvh * G) * str.h + c * 8;
+                    const int64_t cu_b = g.thd ? (int64_t)g.cu[b] : 0;
+                    // row r = token tl * G + head hh, stepped two rows at a time
+                    int tl = (lane >> 4) / G, hh = (lane >> 4) % G;
+                    for (int r = lane >> 4; r < kRows; r += 2, hh += 2) {
+                        while (hh >= G) {
+                            hh -= G;
+                            ++tl;
+                        }
                         const bool valid = r < nrows && tl < ntok;
-                        const __nv_bfloat16 *base = tensor ? p.dO : p.q;
                         const __nv_bfloat16 *src = base;
-                        if (valid)
-                            src = base + (tensor ? o_off(g, b, kvh * G + hh, tok[tl]) : q_off(g, b, kvh * G + hh, tok[tl])) + c * 8;
-                        const uint32_t dst = (tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes) +
-                                             rg_off(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4);
-                        cp_async_16(dst, src, valid ? 16u : 0u);
+                        if (valid) {
+                            const int64_t t = tok[tl];
+                            src = base + hbase + (int64_t)hh * str.h +
+                                  (g.thd ? (cu_b + t) * str.t : (int64_t)b * str.b + t * str.t);
+                        }
+                        cp_async_16(tile_s + rg_off(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
                     }
                     cp_async_commit();
-                    cp_async_wait<0>();
-                    fence_async_smem();
-                    mbar_arrive(&bars[B_QFULL0 + qs]);
-                    mbar_arrive(&bars[B_DOFULL0 + ds]);
+                    // the previous tile's rows have landed once only this
+                    // tile's group is outstanding: make them visible to the
+                    // tensor cores (async proxy), then release that tile
+                    if (pend) {
+                        cp_async_wait<1>();
+                        fence_async_smem();
+                        mbar_arrive(pend);
+                    }
+                    pend = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
                 }
                 if (++qs == NQ) {
                     qs = 0;
@@ -267,6 +296,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 }
             }
         }
+        if (okl && !*abort_flag)
+            flush();
         if (!GATHER_TMA)
             cp_async_wait<0>();
         if (*abort_flag && lane == 0) {

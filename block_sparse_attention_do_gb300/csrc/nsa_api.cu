@@ -104,6 +104,10 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     };
     g.q_bt = bt(g.sq, p->Hq);
     g.o_bt = bt(g.so, p->Hq);
+    Strides dense_o;
+    const int64_t zero[3] = {0, 0, 0};
+    take_strides(zero, p, want_thd, p->Hq, dense_o);
+    g.o_lin = (want_thd || g.so.b == dense_o.b) && g.so.h == dense_o.h && g.so.t == dense_o.t;
     return NSA_OK;
 }
 

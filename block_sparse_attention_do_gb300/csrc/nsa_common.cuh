@@ -37,6 +37,7 @@ struct Geo {
     Strides sdq;     // dq
     Strides sdkv;    // dk and dv
     int q_bt, o_bt;  // BHTD q / o: batch and token fold into one row index (b*T + t) for the row-gather maps
+    int o_lin;       // o and dO are dense: query row r's vector sits at r * D
 };
 
 __device__ __forceinline__ int seq_len(const Geo &g, int b) { return g.thd ? g.cu[b + 1] - g.cu[b] : g.T; }
@@ -64,6 +65,8 @@ __device__ __forceinline__ int64_t dkv_off(const Geo &g, int b, int h, int t) { 
 // (b*Hq + h)*T + t, THD token*Hq + h) in a tensor with strides s
 __device__ __forceinline__ int64_t qrow_off(const Geo &g, const Strides &s, int64_t r)
 {
+    if (g.o_lin && &s == &g.so)
+        return r * g.D;
     if (g.thd)
         return (r / g.Hq) * s.t + (r % g.Hq) * s.h;
     const int64_t bh = r / g.T;

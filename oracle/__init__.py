@@ -232,3 +232,41 @@ def sel_blocks(q, k, v, idx, dO, bs, blocks, scale=None, cu_seqlens=None, window
     lib().oracle_sel_blocks_w(B, Hq, Hkv, T, D, bs, S, scale, _p(cu), _p(q), _p(k), _p(v), _p(idx),
                               _p(dO), n, _p(jb), _p(jg), _p(jj), _p(dk), _p(dv), int(window))
     return dk, dv
+
+
+def causal(q, k, v, dO=None, scale=None, cu_seqlens_q=None, cu_seqlens_k=None, window=0,
+           bottom_right=False):
+    """Dense causal attention with separate query and key lengths: row t of a
+    sequence with Lq queries and Lk keys attends keys k <= c_t (c_t = t, or
+    t + Lk - Lq with bottom_right), k < Lk, and c_t - k < window when
+    window > 0.  Fixed length: q [B,Hq,Tq,D], k/v [B,Hkv,Tk,D]; packed:
+    q [total_q,Hq,D], k/v [total_k,Hkv,D] with cu_seqlens_q / cu_seqlens_k.
+    Returns dict(o, lse) and, with dO, dq, dk, dv (fp64)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    dOa = None if dO is None else _f64(dO)
+    cuq, cuk = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    if (cuq is None) != (cuk is None):
+        raise ValueError("give both cu_seqlens or neither")
+    if cuq is None:
+        B, Hq, Tq, D = q.shape
+        Hkv, Tk = k.shape[1], k.shape[2]
+    else:
+        B = len(cuq) - 1
+        Tq, Hq, D = q.shape
+        Tk, Hkv = k.shape[0], k.shape[1]
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    L = lib()
+    if not hasattr(L, "_causal_set"):
+        L.oracle_causal.restype = None
+        L.oracle_causal.argtypes = [_i64] * 6 + [_dbl, _ptr, _ptr, _i64, _i64] + [_ptr] * 9
+        L._causal_set = True
+    o = np.zeros_like(q)
+    lse = np.zeros(q.shape[:-1], dtype=np.float64)
+    out = dict(o=o, lse=lse)
+    dq = dk = dv = None
+    if dOa is not None:
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        out.update(dq=dq, dk=dk, dv=dv)
+    L.oracle_causal(B, Hq, Hkv, Tq, Tk, D, scale, _p(cuq), _p(cuk), int(window), int(bool(bottom_right)),
+                    _p(q), _p(k), _p(v), _p(dOa), _p(o), _p(lse), _p(dq), _p(dk), _p(dv))
+    return out

@@ -606,3 +606,178 @@ void oracle_sel_blocks_w(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t 
         }
     }
 }
+
+/*
+ * Dense causal attention with separate query and key lengths (the
+ * cuDNN-frontend page: the SDPA backward's THD path takes cum_seqlen_q and
+ * cum_seqlen_k, and its causal mask comes in two alignments,
+ * causal_bottom_right beside plain causal, each optionally with a sliding
+ * window).  For sequence b with Lq query rows and Lk keys, row t sits at
+ * key position
+ *     c_t = t                 (top-left alignment)
+ *     c_t = t + Lk - Lq       (bottom-right alignment)
+ * and attends key k iff 0 <= k <= c_t, k < Lk and (window W > 0) c_t - k < W.
+ * A row with no such key gets O = 0, LSE = -inf and no gradient.  Everything
+ * else is the plain softmax attention of the header, per query head h with
+ * kv head h / G.
+ *
+ * Layouts: fixed length (cu_q = cu_k = NULL): q, o, dO, dq [B,Hq,Tq,D],
+ * k, v, dk, dv [B,Hkv,Tk,D], lse [B,Hq,Tq]; packed: q [cu_q[B],Hq,D],
+ * k [cu_k[B],Hkv,D], lse [cu_q[B],Hq].
+ */
+typedef struct {
+    int64_t B, Hq, Hkv, Tq, Tk, D, window, bottom_right;
+    double scale;
+    const int32_t *cu_q, *cu_k;
+} cprob_t;
+
+static int64_t c_lq(const cprob_t *p, int64_t b) { return p->cu_q ? (int64_t)p->cu_q[b + 1] - p->cu_q[b] : p->Tq; }
+static int64_t c_lk(const cprob_t *p, int64_t b) { return p->cu_k ? (int64_t)p->cu_k[b + 1] - p->cu_k[b] : p->Tk; }
+
+static int64_t c_qoff(const cprob_t *p, int64_t H, int64_t b, int64_t h, int64_t t)
+{
+    if (p->cu_q)
+        return (((int64_t)p->cu_q[b] + t) * H + h) * p->D;
+    return ((b * H + h) * p->Tq + t) * p->D;
+}
+
+static int64_t c_koff(const cprob_t *p, int64_t b, int64_t g, int64_t kk)
+{
+    if (p->cu_k)
+        return (((int64_t)p->cu_k[b] + kk) * p->Hkv + g) * p->D;
+    return ((b * p->Hkv + g) * p->Tk + kk) * p->D;
+}
+
+static int64_t c_soff(const cprob_t *p, int64_t b, int64_t h, int64_t t)
+{
+    if (p->cu_q)
+        return ((int64_t)p->cu_q[b] + t) * p->Hq + h;
+    return (b * p->Hq + h) * p->Tq + t;
+}
+
+/* 1 if row t of sequence b attends key kk */
+static int c_attends(const cprob_t *p, int64_t b, int64_t t, int64_t kk)
+{
+    const int64_t Lk = c_lk(p, b);
+    const int64_t c = p->bottom_right ? t + Lk - c_lq(p, b) : t;
+    return kk >= 0 && kk < Lk && kk <= c && (p->window <= 0 || c - kk < p->window);
+}
+
+/* forward of one row: o (D values) and the returned LSE */
+static double c_row_forward(const cprob_t *p, const double *q, const double *k, const double *v, int64_t b,
+                            int64_t h, int64_t t, double *o, double *sc)
+{
+    const int64_t g = h / (p->Hq / p->Hkv), Lk = c_lk(p, b);
+    const double *qt = q + c_qoff(p, p->Hq, b, h, t);
+    double m = -INFINITY;
+    for (int64_t kk = 0; kk < Lk; ++kk) {
+        sc[kk] = c_attends(p, b, t, kk) ? p->scale * dot(qt, k + c_koff(p, b, g, kk), p->D) : -INFINITY;
+        if (sc[kk] > m)
+            m = sc[kk];
+    }
+    for (int64_t d = 0; d < p->D; ++d)
+        o[d] = 0.0;
+    if (m == -INFINITY)
+        return -INFINITY;
+    double l = 0.0;
+    for (int64_t kk = 0; kk < Lk; ++kk)
+        if (sc[kk] != -INFINITY)
+            l += exp(sc[kk] - m);
+    const double lse = m + log(l);
+    for (int64_t kk = 0; kk < Lk; ++kk)
+        if (sc[kk] != -INFINITY) {
+            const double pk = exp(sc[kk] - lse);
+            const double *vk = v + c_koff(p, b, g, kk);
+            for (int64_t d = 0; d < p->D; ++d)
+                o[d] += pk * vk[d];
+        }
+    return lse;
+}
+
+static int64_t c_maxlen(const int32_t *cu, int64_t B, int64_t T)
+{
+    if (!cu)
+        return T;
+    int64_t m = 0;
+    for (int64_t b = 0; b < B; ++b)
+        if (cu[b + 1] - cu[b] > m)
+            m = cu[b + 1] - cu[b];
+    return m;
+}
+
+/*
+ * Forward and backward together: o, lse, dq, dk, dv (dO may be NULL for the
+ * forward only; then dq, dk, dv are not touched).  Pass 1 per query row
+ * (LSE, O, D_t, dQ), pass 2 per key (dK, dV over every attending row of the
+ * key's group).
+ */
+void oracle_causal(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, int64_t D, double scale,
+                   const int32_t *cu_q, const int32_t *cu_k, int64_t window, int64_t bottom_right, const double *q,
+                   const double *k, const double *v, const double *dO, double *o, double *lse, double *dq, double *dk,
+                   double *dv)
+{
+    cprob_t p = {B, Hq, Hkv, Tq, Tk, D, window, bottom_right, scale, cu_q, cu_k};
+    const int64_t G = Hq / Hkv, mk_ = c_maxlen(cu_k, B, Tk) + 1;
+    int64_t nq = 0;
+    for (int64_t b = 0; b < B; ++b)
+        nq += c_lq(&p, b);
+    double *Dt = (double *)calloc((size_t)(nq * Hq + 1), sizeof(double));
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * mk_);
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t h = 0; h < Hq; ++h)
+                for (int64_t t = 0; t < c_lq(&p, b); ++t) {
+                    const int64_t ro = c_qoff(&p, Hq, b, h, t), so = c_soff(&p, b, h, t), g = h / G;
+                    const double L = c_row_forward(&p, q, k, v, b, h, t, o + ro, sc);
+                    lse[so] = L;
+                    if (!dO)
+                        continue;
+                    const double *dOt = dO + ro;
+                    const double Dv = dot(dOt, o + ro, D);
+                    Dt[so] = Dv;
+                    double *dqt = dq + ro;
+                    for (int64_t d = 0; d < D; ++d)
+                        dqt[d] = 0.0;
+                    for (int64_t kk = 0; kk < c_lk(&p, b); ++kk) {
+                        if (sc[kk] == -INFINITY)
+                            continue;
+                        const int64_t ko = c_koff(&p, b, g, kk);
+                        const double P = exp(sc[kk] - L);
+                        const double dS = P * (dot(dOt, v + ko, D) - Dv);
+                        for (int64_t d = 0; d < D; ++d)
+                            dqt[d] += scale * dS * k[ko + d];
+                    }
+                }
+        free(sc);
+    }
+    if (dO) {
+#pragma omp parallel for collapse(2) schedule(dynamic)
+        for (int64_t b = 0; b < B; ++b)
+            for (int64_t g = 0; g < Hkv; ++g)
+                for (int64_t kk = 0; kk < c_lk(&p, b); ++kk) {
+                    const int64_t ko = c_koff(&p, b, g, kk);
+                    double *dkk = dk + ko, *dvk = dv + ko;
+                    for (int64_t d = 0; d < D; ++d) {
+                        dkk[d] = 0.0;
+                        dvk[d] = 0.0;
+                    }
+                    for (int64_t t = 0; t < c_lq(&p, b); ++t) {
+                        if (!c_attends(&p, b, t, kk))
+                            continue;
+                        for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                            const int64_t ro = c_qoff(&p, Hq, b, h, t), so = c_soff(&p, b, h, t);
+                            const double *qt = q + ro, *dOt = dO + ro;
+                            const double P = exp(scale * dot(qt, k + ko, D) - lse[so]);
+                            const double dS = P * (dot(dOt, v + ko, D) - Dt[so]);
+                            for (int64_t d = 0; d < D; ++d) {
+                                dkk[d] += scale * dS * qt[d];
+                                dvk[d] += P * dOt[d];
+                            }
+                        }
+                    }
+                }
+    }
+    free(Dt);
+}

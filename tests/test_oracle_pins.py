@@ -539,3 +539,100 @@ def test_sampled_blocks_varlen_and_window():
         n = min(bs, T - j * bs)
         np.testing.assert_allclose(dk[i, :n], dk_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
         np.testing.assert_allclose(dv[i, :n], dv_ref[b, g, j * bs:j * bs + n].numpy(), rtol=0, atol=1e-12)
+
+
+# ---- dense causal attention with separate query and key lengths (top-left
+# and bottom-right alignment of the diagonal, optional window): oracle.causal
+
+
+def _sdpa_bias(q, k, v, do, mask):
+    """fp64 SDPA + autograd, GQA by repeating kv heads; mask [Tq, Tk] bool or
+    a torch attention-bias object."""
+    G = q.shape[1] // k.shape[1]
+    qr, kr, vr = (x.double().clone().requires_grad_(True) for x in (q, k, v))
+    o = F.scaled_dot_product_attention(qr, kr.repeat_interleave(G, 1), vr.repeat_interleave(G, 1), attn_mask=mask)
+    o.backward(do.double())
+    return o.detach(), qr.grad, kr.grad, vr.grad
+
+
+@pytest.mark.parametrize("Tq,Tk", [(5, 12), (12, 12), (9, 30)])
+def test_causal_bottom_right_matches_torch_lower_right_bias(Tq, Tk):
+    """Bottom-right alignment (Lk >= Lq: every row attends something) against
+    torch's own lower-right causal bias, forward and gradients."""
+    from torch.nn.attention.bias import causal_lower_right
+
+    B, Hq, Hkv, D = 2, 4, 2, 8
+    q, _, _, do = inputs.make_qkv_do(B, Hq, Hkv, Tq, D, seed=40)
+    _, k, v, _ = inputs.make_qkv_do(B, Hq, Hkv, Tk, D, seed=41)
+    r = oracle.causal(q, k, v, do, bottom_right=True)
+    o, dq, dk, dv = _sdpa_bias(q, k, v, do, causal_lower_right(Tq, Tk))
+    for name, ref in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(r[name], ref.numpy(), rtol=0, atol=1e-12, err_msg=name)
+
+
+@pytest.mark.parametrize("Tq,Tk", [(5, 12), (12, 7)])
+def test_causal_top_left_matches_sdpa_is_causal(Tq, Tk):
+    """Top-left alignment with unequal lengths: SDPA's is_causal (the
+    upper-left diagonal)."""
+    B, Hq, Hkv, D = 1, 4, 1, 8
+    q, _, _, do = inputs.make_qkv_do(B, Hq, Hkv, Tq, D, seed=42)
+    _, k, v, _ = inputs.make_qkv_do(B, Hq, Hkv, Tk, D, seed=43)
+    r = oracle.causal(q, k, v, do, bottom_right=False)
+    G = Hq // Hkv
+    qr, kr, vr = (x.double().clone().requires_grad_(True) for x in (q, k, v))
+    o = F.scaled_dot_product_attention(qr, kr.repeat_interleave(G, 1), vr.repeat_interleave(G, 1), is_causal=True)
+    o.backward(do.double())
+    for name, ref in (("o", o.detach()), ("dq", qr.grad), ("dk", kr.grad), ("dv", vr.grad)):
+        np.testing.assert_allclose(r[name], ref.numpy(), rtol=0, atol=1e-12, err_msg=name)
+
+
+def test_causal_bottom_right_empty_rows_and_window():
+    """Lq > Lk, bottom-right: the first Lq - Lk rows attend nothing (O = 0,
+    LSE = -inf, no gradient); the others match SDPA on a brute-force mask
+    c_t = t + Lk - Lq, with a window of 3 keys."""
+    B, Hq, Hkv, D, Tq, Tk, W = 1, 2, 1, 8, 10, 6, 3
+    q, _, _, do = inputs.make_qkv_do(B, Hq, Hkv, Tq, D, seed=44)
+    _, k, v, _ = inputs.make_qkv_do(B, Hq, Hkv, Tk, D, seed=45)
+    r = oracle.causal(q, k, v, do, bottom_right=True, window=W)
+    shift = Tk - Tq
+    mask = torch.zeros(Tq, Tk, dtype=torch.bool)
+    for t in range(Tq):
+        for kk in range(Tk):
+            c = t + shift
+            mask[t, kk] = kk <= c and c - kk < W
+    live = mask.any(1)
+    assert not live[: Tq - Tk].any() and live[Tq - Tk:].all()
+    assert np.all(r["o"][:, :, ~live.numpy()] == 0) and np.all(np.isneginf(r["lse"][:, :, ~live.numpy()]))
+    assert np.all(r["dq"][:, :, ~live.numpy()] == 0)
+    ql, dol = q[:, :, live], do[:, :, live]
+    o, dq, dk, dv = _sdpa_bias(ql, k, v, dol, mask[live])
+    np.testing.assert_allclose(r["o"][:, :, live.numpy()], o.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dq"][:, :, live.numpy()], dq.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dk"], dk.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["dv"], dv.numpy(), rtol=0, atol=1e-12)
+
+
+def test_causal_packed_sequences_and_equal_length_reduction():
+    """Packed sequences with their own Lq, Lk against the fixed-length oracle
+    per sequence; and with Lq = Lk both alignments reduce to the selection
+    oracle's dense case."""
+    lq, lk = [3, 7, 5], [8, 7, 2]
+    Hq, Hkv, D = 4, 2, 8
+    cuq, cuk = inputs.cu_seqlens_from_lengths(lq), inputs.cu_seqlens_from_lengths(lk)
+    q, _, _, do = inputs.make_qkv_do(1, Hq, Hkv, sum(lq), D, seed=46, layout="thd")
+    _, k, v, _ = inputs.make_qkv_do(1, Hq, Hkv, sum(lk), D, seed=47, layout="thd")
+    for br in (False, True):
+        r = oracle.causal(q, k, v, do, cu_seqlens_q=cuq, cu_seqlens_k=cuk, bottom_right=br)
+        for b in range(3):
+            a, e, ka, ke = int(cuq[b]), int(cuq[b + 1]), int(cuk[b]), int(cuk[b + 1])
+            sub = lambda x: x.permute(1, 0, 2).unsqueeze(0)
+            rb = oracle.causal(sub(q[a:e]), sub(k[ka:ke]), sub(v[ka:ke]), sub(do[a:e]), bottom_right=br)
+            np.testing.assert_allclose(r["o"][a:e], rb["o"][0].transpose(1, 0, 2), rtol=0, atol=1e-14)
+            np.testing.assert_allclose(r["dk"][ka:ke], rb["dk"][0].transpose(1, 0, 2), rtol=0, atol=1e-14)
+    B, T, bs = 2, 21, 4
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, seed=48)
+    ref = oracle.sel_bwd(q, k, v, inputs.make_dense_block_idx(B, Hkv, T, bs), do, bs, window=5)
+    for br in (False, True):
+        r = oracle.causal(q, k, v, do, bottom_right=br, window=5)
+        for name in ("o", "dq", "dk", "dv"):
+            np.testing.assert_allclose(r[name], ref[name], rtol=0, atol=1e-13, err_msg=name)
