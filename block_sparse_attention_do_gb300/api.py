@@ -31,6 +31,7 @@ SYMBOLS = (
     "nsa_trace_count", "nsa_trace_get", "nsa_build_inverse_index_noalloc",
     "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
     "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd", "nsa_debug_stall",
+    "nsa_causal_fwd_workspace_size", "nsa_causal_bwd_workspace_size", "nsa_causal_fwd", "nsa_causal_bwd",
 )
 
 
@@ -40,7 +41,9 @@ class Problem(C.Structure):
                 ("dtype", C.c_int32), ("layout", C.c_int32), ("total_tokens", C.c_int32),
                 ("scale", C.c_float), ("reserved", C.c_int32),
                 ("q_stride", C.c_int64 * 3), ("kv_stride", C.c_int64 * 3), ("o_stride", C.c_int64 * 3),
-                ("dq_stride", C.c_int64 * 3), ("dkv_stride", C.c_int64 * 3)]
+                ("dq_stride", C.c_int64 * 3), ("dkv_stride", C.c_int64 * 3),
+                ("Tk", C.c_int32), ("total_keys", C.c_int32), ("bottom_right", C.c_int32),
+                ("reserved2", C.c_int32)]
 
 
 def _bht_strides(t, thd):
@@ -116,6 +119,12 @@ def lib() -> C.CDLL:
         L.nsa_sink_fwd.argtypes = [pp, C.c_int32] + [_P] * 7 + [_P, C.c_size_t, _P]
         L.nsa_sink_bwd.argtypes = [pp, C.c_int32] + [_P] * 12 + [_P, C.c_size_t, _P]
         L.nsa_debug_stall.argtypes = [C.c_int32, C.c_int32]
+        L.nsa_causal_fwd_workspace_size.restype = C.c_size_t
+        L.nsa_causal_fwd_workspace_size.argtypes = [pp]
+        L.nsa_causal_bwd_workspace_size.restype = C.c_size_t
+        L.nsa_causal_bwd_workspace_size.argtypes = [pp]
+        L.nsa_causal_fwd.argtypes = [pp, C.c_int32] + [_P] * 7 + [_P, C.c_size_t, _P]
+        L.nsa_causal_bwd.argtypes = [pp, C.c_int32] + [_P] * 11 + [_P, C.c_size_t, _P]
         L.nsa_trace_enable.argtypes = [C.c_int32]
         L.nsa_trace_reset.restype = None
         L.nsa_trace_reset.argtypes = []
@@ -304,6 +313,74 @@ def sel_bwd(q, k, v, o, dO, lse, block_idx, block_size, scale=None, cu_seqlens=N
         s = L.nsa_sel_bwd(C.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                           _ptr(block_idx), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), st)
     _check(s, "nsa bwd")
+    return dq, dk, dv
+
+
+def _causal_problem(q, k, cu_q, cu_k, max_q, max_k, bottom_right, scale):
+    if cu_q is None:
+        B, Hq, T, D = q.shape
+        p = problem(B, Hq, k.shape[1], T, D, 64, 1, q.dtype, scale=scale)
+        p.Tk = k.shape[2]
+    else:
+        B = cu_q.numel() - 1
+        if max_q is None:
+            max_q = int((cu_q[1:] - cu_q[:-1]).max().item()) if B > 0 else 1
+        if max_k is None:
+            max_k = int((cu_k[1:] - cu_k[:-1]).max().item()) if B > 0 else 1
+        p = problem(B, q.shape[1], k.shape[1], max(1, max_q), q.shape[2], 64, 1, q.dtype, layout=LAYOUT_THD,
+                    total_tokens=q.shape[0], scale=scale)
+        p.Tk = max(1, max_k)
+        p.total_keys = k.shape[0]
+    p.bottom_right = int(bool(bottom_right))
+    return p
+
+
+def causal_fwd(q, k, v, block_size=64, window=0, bottom_right=False, cu_seqlens_q=None, cu_seqlens_k=None,
+               max_seqlen_q=None, max_seqlen_k=None, scale=None, ws=None, stream=None):
+    """Dense causal attention whose keys have their own lengths
+    (nsa_causal_fwd): the diagonal aligned top-left (row t sees keys <= t)
+    or bottom-right (keys <= t + Lk - Lq), with an optional window.
+    Returns (o, lse)."""
+    p = _causal_problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, bottom_right, scale)
+    p.block_size = block_size
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    _same_strides(k, v, "k and v")
+    declare_strides(p, cu_seqlens_q is not None, q=q, k=k, o=o)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    L = lib()
+    n = int(L.nsa_causal_fwd_workspace_size(C.byref(p)))
+    if n == 0:
+        raise NsaError(1, "nsa_causal_fwd_workspace_size")
+    ws = workspace(n, q.device, "fwd") if ws is None else ws
+    _check(L.nsa_causal_fwd(C.byref(p), int(window), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(q), _ptr(k),
+                            _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "nsa_causal_fwd")
+    return o, lse
+
+
+def causal_bwd(q, k, v, o, dO, lse, block_size=64, window=0, bottom_right=False, cu_seqlens_q=None,
+               cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, scale=None, ws=None, stream=None,
+               out=None):
+    """Backward of causal_fwd (nsa_causal_bwd): returns (dq, dk, dv)."""
+    p = _causal_problem(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, bottom_right, scale)
+    p.block_size = block_size
+    if out is None:
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+        dk = torch.empty(k.shape, dtype=k.dtype, device=k.device)
+        dv = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    else:
+        dq, dk, dv = out
+    _same_strides(k, v, "k and v")
+    _same_strides(o, dO, "o and dO")
+    _same_strides(dk, dv, "dk and dv")
+    declare_strides(p, cu_seqlens_q is not None, q=q, k=k, o=o, dq=dq, dk=dk)
+    L = lib()
+    n = int(L.nsa_causal_bwd_workspace_size(C.byref(p)))
+    if n == 0:
+        raise NsaError(1, "nsa_causal_bwd_workspace_size")
+    ws = workspace(n, q.device, "bwd") if ws is None else ws
+    _check(L.nsa_causal_bwd(C.byref(p), int(window), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(q), _ptr(k),
+                            _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                            ws.numel(), _stream(stream)), "nsa_causal_bwd")
     return dq, dk, dv
 
 

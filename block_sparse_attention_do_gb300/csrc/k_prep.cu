@@ -31,8 +31,8 @@ inline int grid_for(int64_t n, int per_block, int cap = 152 * 32)
 // blocks blk of nblk (grid-stride); each warp takes kDotU row groups per
 // step, so that 2 * kDotU 16-byte loads per thread are in flight
 constexpr int kDotU = 4;
-template <typename T>
-__device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ o, const T *__restrict__ dO,
+template <typename T, bool LIN>
+__device__ __forceinline__ void do_dot_rows(const Geo &g, const T *__restrict__ o, const T *__restrict__ dO,
                                             float *__restrict__ out, int64_t nrows, int D, int blk, int nblk)
 {
     constexpr int VEC = 16 / sizeof(T);
@@ -48,7 +48,7 @@ __device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ 
             const int64_t r = r0 + u * rpw + sub;
             a[u] = b[u] = make_uint4(0, 0, 0, 0);
             if (r < nrows) {
-                const int64_t off = qrow_off(g, g.so, r) + part * VEC;
+                const int64_t off = (LIN ? r * D : qrow_off(g, g.so, r)) + part * VEC;
                 a[u] = __ldcs(reinterpret_cast<const uint4 *>(o + off));
                 b[u] = __ldcs(reinterpret_cast<const uint4 *>(dO + off));
             }
@@ -68,6 +68,17 @@ __device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ 
                 out[r] = acc;
         }
     }
+}
+
+// dense o/dO (row r at r * D) take the branch-free loop, whose loads all stay in flight
+template <typename T>
+__device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ o, const T *__restrict__ dO,
+                                            float *__restrict__ out, int64_t nrows, int D, int blk, int nblk)
+{
+    if (g.o_lin)
+        do_dot_rows<T, true>(g, o, dO, out, nrows, D, blk, nblk);
+    else
+        do_dot_rows<T, false>(g, o, dO, out, nrows, D, blk, nblk);
 }
 
 template <typename T>
@@ -94,17 +105,6 @@ __device__ __forceinline__ void decode_idx_row(const Geo &g, int64_t lin, int &b
 }
 
 // 0 = use, 1 = padding, 2 = invalid (reported), 3 = repeat (reported)
-// dense mode: tokens attending block j form the run [j*bs, end) of the
-// sequence, end = L, or with a window the last token whose window still
-// reaches the block's last key: t <= (j+1)*bs - 1 + window - 1
-__device__ __forceinline__ int dense_count(const Geo &g, int L, int j)
-{
-    int end = L;
-    if (g.window > 0)
-        end = min(end, (j + 1) * g.bs + g.window - 1);
-    return j * g.bs < end ? end - j * g.bs : 0;
-}
-
 // slot s of an index row: 0 use it, 1 padding (-1), 2 out of range or in the
 // future, 3 a repeat of an earlier slot
 __device__ __forceinline__ int classify(const int *row, int s, int t, int bs, int nbmax)
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
             return 0;
         if (g.dense) {
             const int b = i / (g.Hkv * g.nbmax), j = i % g.nbmax;
-            return dense_count(g, seq_len(g, b), j);
+            return dense_count(g, b, j);
         }
         return counts[i];
     };
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int 
     if (nch == 1)
         return;  // written directly by the dK/dV kernel
     const int j = i % g.nbmax, kvh = (i / g.nbmax) % g.Hkv, b = i / (g.Hkv * g.nbmax);
-    const int L = seq_len(g, b);
+    const int L = seq_len_k(g, b);
     const int k0 = j * g.bs;
     if (k0 >= L)
         return;
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kThreads) sink_fwd_kernel(Geo g, const float *
             Ln = m + log1pf(expf(-fabsf(L - sk)));
             f = expf(L - Ln);
         }
-        T *row = o + qrow_off(g, g.so, i);
+        T *row = o + (g.o_lin ? i * g.D : qrow_off(g, g.so, i));
         for (int d = lane; d < g.D; d += 32)
             row[d] = from_f<T>(to_f(row[d]) * f);
         if (lane == 0)

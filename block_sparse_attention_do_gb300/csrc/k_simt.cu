@@ -39,17 +39,17 @@ __device__ __forceinline__ void decode_qrow(const Geo &g, int64_t r, int &b, int
     }
 }
 
-// decode a linear key-row number (k order) into (b, kvh, t)
+// decode a linear key-row number (k order) into (b, kvh, key)
 __device__ __forceinline__ void decode_krow(const Geo &g, int64_t r, int &b, int &kvh, int &t)
 {
     if (g.thd) {
         kvh = (int)(r % g.Hkv);
         const int tok = (int)(r / g.Hkv);
-        b = seq_of_token(g, tok);
-        t = tok - g.cu[b];
+        b = seq_of_key(g, tok);
+        t = tok - g.cuk[b];
     } else {
-        t = (int)(r % g.T);
-        const int64_t bh = r / g.T;
+        t = (int)(r % g.Tk);
+        const int64_t bh = r / g.Tk;
         kvh = (int)(bh % g.Hkv);
         b = (int)(bh / g.Hkv);
     }
@@ -65,7 +65,8 @@ __device__ __forceinline__ int slot_block(const Geo &g, const int *row, int s, i
     return (j >= 0 && j <= t / g.bs) ? j : -1;
 }
 
-__device__ __forceinline__ int n_slots(const Geo &g, int t) { return g.dense ? t / g.bs + 1 : g.S; }
+// slots to walk for a row whose last attended key is `hi` (dense: blocks 0 .. hi / bs)
+__device__ __forceinline__ int n_slots(const Geo &g, int hi) { return g.dense ? (hi >= 0 ? hi / g.bs + 1 : 0) : g.S; }
 
 template <typename T, int DPL>
 __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__restrict__ q,
@@ -90,13 +91,15 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(Geo g, const T *__re
         }
         float m = -INFINITY, l = 0.f;
         const int *row = g.dense ? nullptr : idx_row(g, idx, b, kvh, t);
-        const int ns = n_slots(g, t);
-        const int klo = key_lo(g, t);
+        // keys klo .. khi: the window's left edge up to the diagonal (and the keys' end)
+        const int c = kdiag(g, b, t), khi = min(c, seq_len_k(g, b) - 1);
+        const int klo = key_lo(g, c);
+        const int ns = n_slots(g, khi);
         for (int s = 0; s < ns; ++s) {
             const int j = slot_block(g, row, s, t);
             if (j < 0)
                 continue;
-            const int kend = min((j + 1) * g.bs, t + 1);
+            const int kend = min((j + 1) * g.bs, khi + 1);
             for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
                 const int64_t ko = kv_off(g, b, kvh, kk);
                 float part = 0.f;
@@ -153,13 +156,14 @@ __global__ void __launch_bounds__(kThreads) dq_simt_kernel(Geo g, const T *__res
         }
         if (L != -INFINITY) {
             const int *row = g.dense ? nullptr : idx_row(g, idx, b, kvh, t);
-            const int ns = n_slots(g, t);
-            const int klo = key_lo(g, t);
+            const int c = kdiag(g, b, t), khi = min(c, seq_len_k(g, b) - 1);
+            const int klo = key_lo(g, c);
+            const int ns = n_slots(g, khi);
             for (int s = 0; s < ns; ++s) {
                 const int j = slot_block(g, row, s, t);
                 if (j < 0)
                     continue;
-                const int kend = min((j + 1) * g.bs, t + 1);
+                const int kend = min((j + 1) * g.bs, khi + 1);
                 for (int kk = max(j * g.bs, klo); kk < kend; ++kk) {
                     const int64_t ko = kv_off(g, b, kvh, kk);
                     float ps = 0.f, pd = 0.f;
@@ -201,13 +205,12 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
                                                              T *__restrict__ dk, T *__restrict__ dv)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t nkeys = (int64_t)g.ntok * g.Hkv;
+    const int64_t nkeys = (int64_t)g.ntok_k * g.Hkv;
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < nkeys;
          r += (int64_t)gridDim.x * kWarps) {
         int b, kvh, kk;
         decode_krow(g, r, b, kvh, kk);
         const int j = kk / g.bs;
-        const int L = seq_len(g, b);
         const int64_t ko = kv_off(g, b, kvh, kk);
         float kv[DPL], vv[DPL], ak[DPL], av[DPL];
 #pragma unroll
@@ -222,8 +225,8 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
             n = 0;
             beg = 0;
         } else if (g.dense) {
-            beg = j * g.bs;
-            n = L - beg;
+            beg = dense_first(g, b, j);
+            n = dense_count(g, b, j);
         } else {
             const int bgj = ((b * g.Hkv) + kvh) * g.nbmax + j;
             beg = offsets[bgj];
@@ -231,9 +234,10 @@ __global__ void __launch_bounds__(kThreads) dkdv_simt_kernel(Geo g, const T *__r
         }
         for (int e = 0; e < n; ++e) {
             const int t = g.dense ? beg + e : rows[beg + e];
-            if (t < kk)
+            const int c = kdiag(g, b, t);
+            if (c < kk)
                 continue;
-            if (g.window > 0 && t - kk >= g.window)
+            if (g.window > 0 && c - kk >= g.window)
                 break;  // tokens ascend: the rest are past the window too
             for (int h = kvh * g.G; h < (kvh + 1) * g.G; ++h) {
                 const int64_t qo = q_off(g, b, h, t), oo = o_off(g, b, h, t);
@@ -322,7 +326,7 @@ cudaError_t launch_dkdv_simt(const Geo &g, const void *q, const void *k, const v
                              const int *offsets, const int *rows, void *dk, void *dv, int dtype,
                              cudaStream_t st)
 {
-    const int grid = rows_grid((int64_t)g.ntok * g.Hkv);
+    const int grid = rows_grid((int64_t)g.ntok_k * g.Hkv);
     if (dtype == NSA_DTYPE_BF16) {
         using T = __nv_bfloat16;
         NSA_DISPATCH_D(g.D, (dkdv_simt_kernel<T, DPL><<<grid, kThreads, 0, st>>>(

@@ -50,7 +50,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 }  // namespace
 
-bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s)
+bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s,
+               bool keys)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -63,7 +64,7 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
         rank = 3;
         dims[0] = g.D;
         dims[1] = H;
-        dims[2] = g.ntok;
+        dims[2] = keys ? g.ntok_k : g.ntok;
         strides[0] = (cuuint64_t)s.h * es;
         strides[1] = (cuuint64_t)s.t * es;
         box[0] = 64;
@@ -72,7 +73,7 @@ bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_
     } else {
         rank = 4;
         dims[0] = g.D;
-        dims[1] = g.T;
+        dims[1] = keys ? g.Tk : g.T;
         dims[2] = H;
         dims[3] = g.B;
         strides[0] = (cuuint64_t)s.t * es;

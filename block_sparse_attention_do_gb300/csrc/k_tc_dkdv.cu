@@ -92,7 +92,15 @@ __device__ __forceinline__ int unit_of(int k, int n_units)
     return ui < n_units ? (int)ui : -1;
 }
 
-template <bool GATHER_TMA>
+// How a tile's Q and dO rows arrive: one TMA box per token (its G heads,
+// both halves; G % 8 == 0), two TMA tile boxes per tensor (the dense
+// entries' units hold consecutive tokens; G % 8 != 0), or 16-byte cp.async
+// (selection, G % 8 != 0).  ROWS and CPASYNC fill the row-group layout
+// (rg_off); TILE fills one 64-column half after the other (rows head-major
+// for BHTD, token-major for THD).
+enum { LOAD_ROWS = 0, LOAD_TILE = 1, LOAD_CPASYNC = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_do,
                                                          const __grid_constant__ CUtensorMap tm_k,
@@ -116,12 +124,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         abort_flag[0] = 0;
         abort_flag[1] = p.wait_us;  // the wait limit (0: the default)
         for (int x = 0; x < NQ; ++x) {
-            mbar_init(&bars[B_QFULL0 + x], GATHER_TMA ? 1 : 32);
+            mbar_init(&bars[B_QFULL0 + x], MODE == LOAD_CPASYNC ? 32 : 1);
             mbar_init(&bars[B_QEMPTY0 + x], 1);  // dK^T's commit
             mbar_init(&bars[B_IDX0 + x], 32);
         }
         for (int x = 0; x < NDO; ++x) {
-            mbar_init(&bars[B_DOFULL0 + x], GATHER_TMA ? 1 : 32);
+            mbar_init(&bars[B_DOFULL0 + x], MODE == LOAD_CPASYNC ? 32 : 1);
             mbar_init(&bars[B_DOEMPTY0 + x], 2);  // dP's and dV^T's commits
         }
         mbar_init(&bars[B_KVFULL], 1);
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         uint64_t *pend = nullptr;             // cp.async gather: the tile whose release is still due
         // releases the pending cp.async tile (all of this lane's copies landed)
         auto flush = [&]() {
-            if (!GATHER_TMA && pend) {
+            if (MODE == LOAD_CPASYNC && pend) {
                 cp_async_wait<0>();
                 fence_async_smem();
                 mbar_arrive(pend);
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
                 for (int h = 0; h < 2; ++h) {
                     if (g.thd) {
-                        const int t0 = g.cu[b] + u.j * kKeys;
+                        const int t0 = g.cuk[b] + u.j * kKeys;
                         tma_load_3d(sm + OFF_K + h * kKvHalfBytes, &tm_k, &bars[B_KVFULL], h * 64, kvh, t0);
                         tma_load_3d(sm + OFF_V + h * kKvHalfBytes, &tm_v, &bars[B_KVFULL], h * 64, kvh, t0);
                     } else {
@@ -233,7 +241,24 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 }
                 const int ntok = min(Tt, u.count - ti * Tt);
                 const int *tok = tok_s + qs * kRows;
-                if (GATHER_TMA) {
+                if (MODE == LOAD_TILE) {
+                    // the tile's tokens are consecutive: one box per 64-column half
+                    uint64_t *full = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
+                    if (lane == 0) {
+                        last_tile = it;
+                        mbar_arrive_expect_tx(full, nrows * 256);
+                    }
+                    __syncwarp();
+                    if (lane < 2) {
+                        const int h = lane, t0 = tok[0];
+                        uint8_t *dst = sm + (tensor ? OFF_DO + ds * kTileBytes : OFF_Q + qs * kTileBytes) + h * kHalfBytes;
+                        const CUtensorMap *map = tensor ? &tm_do : &tm_q;
+                        if (g.thd)
+                            tma_load_3d(dst, map, full, h * 64, kvh * G, g.cu[b] + t0);
+                        else
+                            tma_load_4d(dst, map, full, h * 64, t0, kvh * G, b);
+                    }
+                } else if (MODE == LOAD_ROWS) {
                     uint64_t *full = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
                     if (lane == 0) {
                         last_tile = it;
@@ -298,7 +323,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         }
         if (okl && !*abort_flag)
             flush();
-        if (!GATHER_TMA)
+        if (MODE == LOAD_CPASYNC)
             cp_async_wait<0>();
         if (*abort_flag && lane == 0) {
             // let TMA copies still in flight land before the CTA exits
@@ -326,7 +351,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         int csr0 = 0, ntiles = 0;
         auto load_unit = [&]() {
             u = p.units[ui];
-            csr0 = g.dense ? 0 : p.offsets[u.bg * g.nbmax + u.j] + u.begin;
+            // dense: the block's tokens are one range from its first attending row
+            csr0 = g.dense ? dense_first(g, u.bg / g.Hkv, u.j) + u.begin : p.offsets[u.bg * g.nbmax + u.j] + u.begin;
             ntiles = (u.count + Tt - 1) / Tt;
         };
         int tok_r[4];
@@ -338,7 +364,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 tok_r[k4] = -1;
                 if (tl < ntok) {
                     const int pos = ti * Tt + tl;
-                    tok_r[k4] = g.dense ? u.j * g.bs + u.begin + pos : p.rows[csr0 + pos];
+                    tok_r[k4] = g.dense ? csr0 + pos : p.rows[csr0 + pos];
                 }
             }
         };
@@ -382,6 +408,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const uint32_t idV = idesc_bf16(128, 64, true, true);
             const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
             const uint32_t k_s = smem_u32(sm + OFF_K), v_s = smem_u32(sm + OFF_V);
+            // Q/dO tiles: 64-column halves and 8-row groups apart by these
+            const uint32_t qhalf = MODE == LOAD_TILE ? kHalfBytes : kRgHalf;
+            const uint32_t qsbo = MODE == LOAD_TILE ? 1024 : kRgStride;
             const uint32_t p_s = smem_u32(sm + OFF_P), ds_s = smem_u32(sm + OFF_DS);
             // S / dP: A = Q / dO (row-group tile), B = K_j / V_j
             const bool on_do = role == 1 || role == 2;
@@ -409,9 +438,9 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         tc_fence_after();
                         const uint32_t col = tmem + TM_S + tb * 128 + role * 64;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
-                            const uint32_t ao = (kk >> 2) * kRgHalf + (kk & 3) * 32;
+                            const uint32_t ao = (kk >> 2) * qhalf + (kk & 3) * 32;
                             const uint32_t bo = (kk >> 2) * kKvHalfBytes + (kk & 3) * 32;
-                            mma_bf16(col, sdesc_sw128(a_s + ao, 16, kRgStride), sdesc_sw128(b_s + bo, 16, 1024), idS,
+                            mma_bf16(col, sdesc_sw128(a_s + ao, 16, qsbo), sdesc_sw128(b_s + bo, 16, 1024), idS,
                                      kk > 0);
                         }
                         mma_commit(&bars[(role == 0 ? B_SFULL0 : B_DPFULL0) + tb]);
@@ -435,7 +464,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         const uint32_t pb = (role == 2 ? p_s : ds_s) + pbuf * (kRows * 128);
                         for (int kr = 0; kr < kRows / 16; ++kr)
                             // 16 rows = two row groups; LBO steps the 64-dim halves (M)
-                            mma_bf16(col, sdesc_sw128(a_s + kr * 2 * kRgStride, kRgHalf, kRgStride),
+                            mma_bf16(col, sdesc_sw128(a_s + kr * 2 * qsbo, qhalf, qsbo),
                                      sdesc_sw128(pb + kr * 2048, 8192, 1024), idV, (ti > 0 || kr > 0) ? 1u : 0u);
                         mma_commit(&bars[(role == 2 ? B_PFREE0 : B_DSFREE0) + pbuf]);
                         mma_commit(&bars[role == 2 ? B_DOEMPTY0 + st : B_QEMPTY0 + qs]);
@@ -462,6 +491,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         // ------------------------------------------------- softmax / epilogue
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // tile row = TMEM lane
+        // the row's token within the tile and head within the group
+        // (head-major rows for a BHTD tile box, token-major otherwise)
+        const bool head_major = MODE == LOAD_TILE && !g.thd;
+        const int my_tl = head_major ? r % Tt : r / G, my_hh = head_major ? r / Tt : r % G;
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t p_row = smem_u32(sm + OFF_P) + r * 128;
         const uint32_t ds_row = smem_u32(sm + OFF_DS) + r * 128;
@@ -479,11 +512,11 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const Unit nu = p.units[p_ui];
             if (!mbar_wait_warp(&bars[B_IDX0 + pq], pph, abort_flag))
                 return false;
-            ptok = r < nrows ? tok_s[pq * kRows + r / G] : -1;
+            ptok = r < nrows ? tok_s[pq * kRows + my_tl] : -1;
             plse = 0.f;
             pdlt = 0.f;
             if (ptok >= 0) {
-                const int64_t so = stat_off(g, nu.bg / g.Hkv, (nu.bg % g.Hkv) * G + r % G, ptok);
+                const int64_t so = stat_off(g, nu.bg / g.Hkv, (nu.bg % g.Hkv) * G + my_hh, ptok);
                 plse = p.lse[so];
                 pdlt = p.delta[so];
             }
@@ -503,7 +536,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         for (int ui; ok && (ui = unit_of(uc, n_units)) >= 0; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
-            const int L = seq_len(g, b);
+            const int L = seq_len_k(g, b);  // keys of the sequence
             const int k0 = u.j * kKeys;
             const int ntiles = (u.count + Tt - 1) / Tt;
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
@@ -514,9 +547,11 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                // keys k0 + c with lo <= c <= tok - k0 are attended (the token selected block j)
-                const int lim = tok < 0 ? -1 : tok - k0;
-                const int lo = tok < 0 ? 0 : key_lo(g, tok) - k0;  // window's left edge
+                // keys k0 + c with lo <= c <= lim are attended (the token selected block j):
+                // from the window's left edge to the row's diagonal and the keys' end
+                const int cdiag = tok < 0 ? -1 : kdiag(g, b, tok);
+                const int lim = tok < 0 ? -1 : min(cdiag, L - 1) - k0;
+                const int lo = tok < 0 ? 0 : key_lo(g, cdiag) - k0;  // window's left edge
                 // P from S while dP is still running
                 uint32_t pv[64];
                 tmem_ld64(lane_base + TM_S + tb * 128, pv);
@@ -681,11 +716,16 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
                            int *err, cudaStream_t st)
 {
     CUtensorMap tq, tdo, tk, tv;
-    const bool gather_tma = (g.G % 8) == 0;
-    const bool qmaps = gather_tma ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) &&
-                                        make_tmap_rows(&tdo, dO, g, g.Hq, g.G, g.so, g.o_bt)
-                                  : make_tmap(&tq, q, g, g.Hq, 1, 1, g.sq) && make_tmap(&tdo, dO, g, g.Hq, 1, 1, g.so);
-    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
+    const int mode = g.G % 8 == 0 ? LOAD_ROWS : g.dense ? LOAD_TILE : LOAD_CPASYNC;
+    const int Tt = g.G >= kRows ? 1 : kRows / g.G;
+    bool qmaps;
+    if (mode == LOAD_ROWS)
+        qmaps = make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) && make_tmap_rows(&tdo, dO, g, g.Hq, g.G, g.so, g.o_bt);
+    else if (mode == LOAD_TILE)
+        qmaps = make_tmap(&tq, q, g, g.Hq, Tt, g.G, g.sq) && make_tmap(&tdo, dO, g, g.Hq, Tt, g.G, g.so);
+    else
+        qmaps = make_tmap(&tq, q, g, g.Hq, 1, 1, g.sq) && make_tmap(&tdo, dO, g, g.Hq, 1, 1, g.so);
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv, true) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv, true))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;
@@ -709,13 +749,15 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
     if (grid < 1)
         grid = 1;
     // a programmatic dependent of the kernel before it (see the kernel's wait)
-    if (gather_tma) {
-        cudaFuncSetAttribute(dkdv_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        return launch_dependent(dkdv_tc_kernel<true>, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
-    } else {
-        cudaFuncSetAttribute(dkdv_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        return launch_dependent(dkdv_tc_kernel<false>, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
-    }
+    auto go = [&](auto kernel) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        return launch_dependent(kernel, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
+    };
+    if (mode == LOAD_ROWS)
+        return go(dkdv_tc_kernel<LOAD_ROWS>);
+    if (mode == LOAD_TILE)
+        return go(dkdv_tc_kernel<LOAD_TILE>);
+    return go(dkdv_tc_kernel<LOAD_CPASYNC>);
 }
 
 }  // namespace nsa

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                         uint8_t *dst = sm + (isv ? OFF_V : OFF_K) + st * kTileBytes + h * kHalfBytes + e * kKvHalfBytes;
                         const CUtensorMap *map = isv ? &tm_v : &tm_k;
                         if (g.thd)
-                            tma_load_3d(dst, map, full, h * 64, kvh, g.cu[b] + j * kKeys);
+                            tma_load_3d(dst, map, full, h * 64, kvh, g.cuk[b] + j * kKeys);
                         else
                             tma_load_4d(dst, map, full, h * 64, j * kKeys, kvh, b);
                     }
@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
             const int t = t0 + tl;
+            // the row's keys: from the window's left edge to its diagonal
+            const int cdiag = rvalid ? kdiag(g, b, t) : -1;
+            const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
             // the row's dQ columns e*64 .. e*64+63
             __nv_bfloat16 *dst = rvalid ? p.dq + dq_off(g, b, kvh * G + hh, t) + e * 64 : nullptr;
             const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
@@ -445,10 +448,10 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             for (int i = 0; i < npairs; ++i, ++gi) {
                 const int db = gi & 1;  // dP buffer
                 const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
-                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, klo, khi, j);
                 // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
-                const int lim = sel ? t - j * kKeys : -1;
-                const int lo = key_lo(g, t) - j * kKeys;
+                const int lim = sel ? khi - j * kKeys : -1;
+                const int lo = klo - j * kKeys;
                 // no row of the warp ends or starts inside the block: a row attends
                 // all of it or none; none gets a +inf bias (exp2(-inf) = 0)
                 const bool whole = __all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0));
@@ -644,7 +647,7 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
     const bool qmaps = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) &&
                                 make_tmap_rows(&tdo, dO, g, g.Hq, g.G, g.so, g.o_bt)
                           : make_tmap(&tq, q, g, g.Hq, Tq, g.G, g.sq) && make_tmap(&tdo, dO, g, g.Hq, Tq, g.G, g.so);
-    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
+    if (!qmaps || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv, true) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv, true))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                         uint8_t *dst = sm + (isv ? OFF_V : OFF_K) + st * kTileBytes + h * kHalfBytes + e * kKvHalfBytes;
                         const CUtensorMap *map = isv ? &tm_v : &tm_k;
                         if (g.thd)
-                            tma_load_3d(dst, map, full, h * 64, kvh, g.cu[b] + j * kKeys);
+                            tma_load_3d(dst, map, full, h * 64, kvh, g.cuk[b] + j * kKeys);
                         else
                             tma_load_4d(dst, map, full, h * 64, j * kKeys, kvh, b);
                     }
@@ -387,16 +387,19 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
             const int t = t0 + tl;
+            // the row's keys: from the window's left edge to its diagonal
+            const int cdiag = rvalid ? kdiag(g, b, t) : -1;
+            const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
             const uint32_t *my_mask = union_mask(u_buf(k)) + (rvalid ? tl : 0) * words;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int i = 0; i < npairs; ++i, ++gi) {
                 const int sb = gi & 1;
                 const int j = (2 * i + e < U) ? list[2 * i + e] : -1;
-                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, t, j);
+                const bool sel = rvalid && j >= 0 && qtile_selects(g, my_mask, klo, khi, j);
                 // the row attends keys j*64 + c, lo <= c <= lim (lim < 0: none)
-                const int lim = sel ? t - j * kKeys : -1;
-                const int lo = key_lo(g, t) - j * kKeys;
+                const int lim = sel ? khi - j * kKeys : -1;
+                const int lo = klo - j * kKeys;
                 const bool any = __any_sync(0xffffffffu, sel);
                 // no row of the warp ends or starts inside the block: a row attends
                 // all of it or none; none gets a -inf bias
@@ -588,7 +591,7 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
     CUtensorMap tq, tk, tv;
     const bool rg = !g.thd && (g.G % 8) == 0;  // row-group Q tile, one box per token
     const bool qmap = rg ? make_tmap_rows(&tq, q, g, g.Hq, g.G, g.sq, g.q_bt) : make_tmap(&tq, q, g, g.Hq, Tq, g.G, g.sq);
-    if (!qmap || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv))
+    if (!qmap || !make_tmap(&tk, k, g, g.Hkv, kKeys, 1, g.skv, true) || !make_tmap(&tv, v, g, g.Hkv, kKeys, 1, g.skv, true))
         return cudaErrorInvalidValue;
     Params p;
     p.g = g;

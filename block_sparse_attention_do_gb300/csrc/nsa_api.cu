@@ -18,17 +18,20 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-enum Mode { SPARSE = 0, DENSE = 1 };
+// SPARSE: selection; DENSE: every block up to the diagonal (queries and keys
+// of equal length); CAUSAL: dense with the keys' own lengths and the diagonal
+// aligned top-left or bottom-right (nsa_causal_*)
+enum Mode { SPARSE = 0, DENSE = 1, CAUSAL = 2 };
 
 // One tensor's declared (batch, head, token) strides into `out`: all zero
 // selects the dense layout with H heads; otherwise every stride in use must
 // be positive, a multiple of 16 bytes and below 2^40 bytes (the tensor-map
 // limits).  THD ignores the batch entry.
-bool take_strides(const int64_t in[3], const nsa_problem *p, bool thd, int H, Strides &out)
+bool take_strides(const int64_t in[3], const nsa_problem *p, bool thd, int H, int T, Strides &out)
 {
     const int64_t D = p->D, es = p->dtype == NSA_DTYPE_BF16 ? 2 : 4;
     if (in[0] == 0 && in[1] == 0 && in[2] == 0) {
-        out = thd ? Strides{0, D, (int64_t)H * D} : Strides{(int64_t)H * p->T * D, (int64_t)p->T * D, D};
+        out = thd ? Strides{0, D, (int64_t)H * D} : Strides{(int64_t)H * T * D, (int64_t)T * D, D};
         return true;
     }
     for (int i = thd ? 1 : 0; i < 3; ++i)
@@ -40,12 +43,19 @@ bool take_strides(const int64_t in[3], const nsa_problem *p, bool thd, int H, St
 
 // Checks the problem and fills the device geometry.  `want_thd` is the
 // layout the entry point requires.
-nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g, int window = 0)
+nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_t *cu, Geo &g, int window = 0,
+                    const int32_t *cuk = nullptr)
 {
-    if (window < 0 || (window > 0 && mode != DENSE))
+    if (window < 0 || (window > 0 && mode == SPARSE))
         return NSA_ERR_INVALID_ARG;
     if (!p)
         return NSA_ERR_INVALID_ARG;
+    // the keys' geometry: their own for the causal entries, else the queries'
+    const bool own_keys = mode == CAUSAL;
+    if (own_keys && (p->Tk < 0 || p->total_keys < 0 || (p->bottom_right != 0 && p->bottom_right != 1) ||
+                     (want_thd && (!cuk || p->total_keys < 1))))
+        return NSA_ERR_INVALID_ARG;
+    const int Tk = own_keys && p->Tk > 0 ? p->Tk : p->T;
     if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->T < 1)
         return NSA_ERR_INVALID_ARG;
     if (p->Hq % p->Hkv != 0)
@@ -71,8 +81,12 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
         return NSA_ERR_UNSUPPORTED;
     // the index-side sizes (list entries, per-block counters, work units) are
     // held in int: refuse problems whose counts would not fit
-    const int64_t nb = (p->T + p->block_size - 1) / p->block_size;
-    if (ntok >= INT32_MAX || ntok * p->Hq >= INT32_MAX || (int64_t)p->B * p->Hkv * nb >= INT32_MAX)
+    const int64_t ntok_k = !own_keys ? ntok : want_thd ? (int64_t)p->total_keys : (int64_t)p->B * Tk;
+    if (ntok_k * p->Hkv * (int64_t)p->D >= ((int64_t)1 << 40))
+        return NSA_ERR_UNSUPPORTED;
+    const int64_t nb = (Tk + p->block_size - 1) / p->block_size;
+    if (ntok >= INT32_MAX || ntok_k >= INT32_MAX || ntok * p->Hq >= INT32_MAX ||
+        (int64_t)p->B * p->Hkv * nb >= INT32_MAX)
         return NSA_ERR_UNSUPPORTED;
     if (mode == SPARSE && ntok * p->Hkv * p->S >= INT32_MAX)  // inverse-index entries
         return NSA_ERR_UNSUPPORTED;
@@ -84,18 +98,24 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     g.T = p->T;
     g.D = p->D;
     g.bs = p->block_size;
-    g.nbmax = (p->T + p->block_size - 1) / p->block_size;
-    g.S = mode == DENSE ? g.nbmax : p->S;
+    g.nbmax = (int)nb;  // key blocks of the longest key sequence
+    g.S = mode != SPARSE ? g.nbmax : p->S;
     g.ntok = (int)ntok;
     g.thd = want_thd ? 1 : 0;
-    g.dense = mode == DENSE ? 1 : 0;
+    g.dense = mode != SPARSE ? 1 : 0;
+    g.Tk = Tk;
+    g.ntok_k = (int)ntok_k;
+    g.cuk = own_keys && want_thd ? cuk : cu;
+    g.br = own_keys ? p->bottom_right : 0;
     g.window = window;
     g.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->D);
     g.scale_l2 = g.scale * 1.4426950408889634f;
     g.cu = cu;
-    if (!take_strides(p->q_stride, p, want_thd, p->Hq, g.sq) || !take_strides(p->kv_stride, p, want_thd, p->Hkv, g.skv) ||
-        !take_strides(p->o_stride, p, want_thd, p->Hq, g.so) || !take_strides(p->dq_stride, p, want_thd, p->Hq, g.sdq) ||
-        !take_strides(p->dkv_stride, p, want_thd, p->Hkv, g.sdkv))
+    if (!take_strides(p->q_stride, p, want_thd, p->Hq, p->T, g.sq) ||
+        !take_strides(p->kv_stride, p, want_thd, p->Hkv, Tk, g.skv) ||
+        !take_strides(p->o_stride, p, want_thd, p->Hq, p->T, g.so) ||
+        !take_strides(p->dq_stride, p, want_thd, p->Hq, p->T, g.sdq) ||
+        !take_strides(p->dkv_stride, p, want_thd, p->Hkv, Tk, g.sdkv))
         return NSA_ERR_INVALID_ARG;
     // the row-gather maps of q and o fold the batch into the token index when
     // it does not fold into the head index (a packed [B, T, H, D] tensor)
@@ -106,7 +126,7 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
     g.o_bt = bt(g.so, p->Hq);
     Strides dense_o;
     const int64_t zero[3] = {0, 0, 0};
-    take_strides(zero, p, want_thd, p->Hq, dense_o);
+    take_strides(zero, p, want_thd, p->Hq, p->T, dense_o);
     g.o_lin = (want_thd || g.so.b == dense_o.b) && g.so.h == dense_o.h && g.so.t == dense_o.t;
     return NSA_OK;
 }
@@ -131,8 +151,13 @@ PlanLayout plan_layout(const Geo &g)
     // kernel launched behind dK/dV takes the SMs its uneven end leaves)
     w.chunk = tiles_tokens(g) * 128;
     // upper bound on list entries; dense: a row of sequence-local token t
-    // attends t/bs + 1 <= nbmax/2 + 1 blocks on average over a sequence
-    const int64_t sel_total = g.dense ? (int64_t)g.ntok * g.Hkv * (g.nbmax / 2 + 1) : (int64_t)g.ntok * g.Hkv * g.S;
+    // attends t/bs + 1 <= nbmax/2 + 1 blocks on average over a sequence, or
+    // with keys of their own lengths (a short query run at the end of long
+    // keys) up to every block
+    const bool own_keys = g.br || g.Tk != g.T || g.cuk != g.cu;
+    const int64_t sel_total = !g.dense ? (int64_t)g.ntok * g.Hkv * g.S
+                              : own_keys ? (int64_t)g.ntok * g.Hkv * g.nbmax
+                                         : (int64_t)g.ntok * g.Hkv * (g.nbmax / 2 + 1);
     w.max_units = (int)(nbgj + (sel_total + w.chunk - 1) / w.chunk);
     size_t off = kAlign;  // header
     w.counts = off;
@@ -229,19 +254,24 @@ nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
     return NSA_OK;
 }
 
+// workspace bytes of a forward / backward of this mode (0: invalid problem)
+size_t fwd_ws_need(const nsa_problem *p, Mode mode);
+size_t bwd_ws_need(const nsa_problem *p, Mode mode);
+
 nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu, const void *q,
                    const void *k, const void *v, const int32_t *idx, void *o, float *lse,
-                   void *ws, size_t ws_bytes, void *stream, int window = 0, const float *sinks = nullptr)
+                   void *ws, size_t ws_bytes, void *stream, int window = 0, const float *sinks = nullptr,
+                   const int32_t *cuk = nullptr)
 {
     Geo g;
-    nsa_status s = make_geo(p, thd, mode, cu, g, window);
+    nsa_status s = make_geo(p, thd, mode, cu, g, window, cuk);
     if (s != NSA_OK)
         return s;
     if (!q || !k || !v || !o || !lse || (mode == SPARSE && !idx))
         return NSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return NSA_ERR_INVALID_ARG;
-    if ((s = check_ws(ws, ws_bytes, nsa_fwd_workspace_size(p))) != NSA_OK)
+    if ((s = check_ws(ws, ws_bytes, fwd_ws_need(p, mode))) != NSA_OK)
         return s;
     cudaStream_t st = (cudaStream_t)stream;
     WsHeader *hdr = (WsHeader *)ws;
@@ -311,10 +341,10 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
                    const int32_t *idx, const void *plan, void *dq, void *dk, void *dv, void *ws,
                    size_t ws_bytes, void *stream, int window = 0, const float *sinks = nullptr,
-                   float *dsinks = nullptr)
+                   float *dsinks = nullptr, const int32_t *cuk = nullptr)
 {
     Geo g;
-    nsa_status s = make_geo(p, thd, mode, cu, g, window);
+    nsa_status s = make_geo(p, thd, mode, cu, g, window, cuk);
     if (s != NSA_OK)
         return s;
     if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || (mode == SPARSE && !idx))
@@ -326,7 +356,7 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (plan && ((uintptr_t)plan & (kAlign - 1)))
         return NSA_ERR_INVALID_ARG;
     const BwdWs L = bwd_layout(g, p->dtype);
-    if ((s = check_ws(ws, ws_bytes, plan ? L.plan : nsa_bwd_workspace_size(p))) != NSA_OK)
+    if ((s = check_ws(ws, ws_bytes, plan ? L.plan : bwd_ws_need(p, mode))) != NSA_OK)
         return s;
     cudaStream_t st = (cudaStream_t)stream;
     char *w8 = (char *)ws;
@@ -377,6 +407,30 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 }
 
 WaitTest g_wait_test = {WAIT_TEST_NONE, 0};
+
+// stand-ins for device pointers in the size queries (never dereferenced):
+// distinct, so that a packed causal problem's keys count as their own
+const int32_t *const kFakeCuQ = (const int32_t *)16, *const kFakeCuK = (const int32_t *)32;
+
+size_t fwd_ws_need(const nsa_problem *p, Mode mode)
+{
+    if (mode != CAUSAL)
+        return nsa_fwd_workspace_size(p);
+    Geo g;
+    const bool thd = p && p->layout == NSA_LAYOUT_THD;
+    return make_geo(p, thd, CAUSAL, thd ? kFakeCuQ : nullptr, g, 0, thd ? kFakeCuK : nullptr) == NSA_OK ? kAlign : 0;
+}
+
+size_t bwd_ws_need(const nsa_problem *p, Mode mode)
+{
+    if (mode != CAUSAL)
+        return nsa_bwd_workspace_size(p);
+    Geo g;
+    const bool thd = p && p->layout == NSA_LAYOUT_THD;
+    if (make_geo(p, thd, CAUSAL, thd ? kFakeCuQ : nullptr, g, 0, thd ? kFakeCuK : nullptr) != NSA_OK)
+        return 0;
+    return bwd_layout(g, p->dtype).total;
+}
 
 }  // namespace
 
@@ -602,6 +656,37 @@ nsa_status nsa_sink_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_
         return NSA_ERR_INVALID_ARG;
     return run_bwd(p, thd, DENSE, cu_seqlens, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws, ws_bytes,
                    stream, window, sinks, dsinks);
+}
+
+size_t nsa_causal_fwd_workspace_size(const nsa_problem *p) { return fwd_ws_need(p, CAUSAL); }
+
+size_t nsa_causal_bwd_workspace_size(const nsa_problem *p) { return bwd_ws_need(p, CAUSAL); }
+
+nsa_status nsa_causal_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, const void *q, const void *k, const void *v, void *o,
+                          float *lse, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!p || window < 0)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens_q != nullptr) || thd != (cu_seqlens_k != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_fwd(p, thd, CAUSAL, cu_seqlens_q, q, k, v, nullptr, o, lse, ws, ws_bytes, stream, window, nullptr,
+                   cu_seqlens_k);
+}
+
+nsa_status nsa_causal_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, const void *q, const void *k, const void *v, const void *o,
+                          const void *dO, const float *lse, void *dq, void *dk, void *dv, void *ws,
+                          size_t ws_bytes, void *stream)
+{
+    if (!p || window < 0)
+        return NSA_ERR_INVALID_ARG;
+    const bool thd = p->layout == NSA_LAYOUT_THD;
+    if (thd != (cu_seqlens_q != nullptr) || thd != (cu_seqlens_k != nullptr))
+        return NSA_ERR_INVALID_ARG;
+    return run_bwd(p, thd, CAUSAL, cu_seqlens_q, q, k, v, o, dO, lse, nullptr, nullptr, dq, dk, dv, ws, ws_bytes,
+                   stream, window, nullptr, nullptr, cu_seqlens_k);
 }
 
 nsa_status nsa_do_dot(const nsa_problem *p, const int32_t *cu_seqlens, const void *o,

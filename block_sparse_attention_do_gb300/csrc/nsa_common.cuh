@@ -38,14 +38,30 @@ struct Geo {
     Strides sdkv;    // dk and dv
     int q_bt, o_bt;  // BHTD q / o: batch and token fold into one row index (b*T + t) for the row-gather maps
     int o_lin;       // o and dO are dense: query row r's vector sits at r * D
+    // keys (the causal entries may give them their own lengths; elsewhere
+    // they equal the queries'): BHTD key length, packed key count, cu_seqlens
+    // of the keys (THD), and the alignment of the causal diagonal
+    int Tk, ntok_k;
+    const int *cuk;
+    int br;          // 1: row t sits at key position t + Lk - Lq (bottom-right); 0: at t
 };
 
 __device__ __forceinline__ int seq_len(const Geo &g, int b) { return g.thd ? g.cu[b + 1] - g.cu[b] : g.T; }
 
-// first key row t may attend (the sliding window's left edge; 0 without one)
-__host__ __device__ __forceinline__ int key_lo(const Geo &g, int t)
+// keys of sequence b
+__device__ __forceinline__ int seq_len_k(const Geo &g, int b) { return g.thd ? g.cuk[b + 1] - g.cuk[b] : g.Tk; }
+
+// the key position of row t's diagonal: keys k <= kdiag (and k < Lk) are causal
+__device__ __forceinline__ int kdiag(const Geo &g, int b, int t)
 {
-    return (g.window > 0 && t - g.window + 1 > 0) ? t - g.window + 1 : 0;
+    return g.br ? t + seq_len_k(g, b) - seq_len(g, b) : t;
+}
+
+// first key a row whose diagonal sits at key position c may attend (the
+// sliding window's left edge; 0 without one)
+__host__ __device__ __forceinline__ int key_lo(const Geo &g, int c)
+{
+    return (g.window > 0 && c - g.window + 1 > 0) ? c - g.window + 1 : 0;
 }
 
 // element offset of the D-vector of (b, head h, token t) in a tensor with strides s
@@ -57,16 +73,21 @@ __device__ __forceinline__ int64_t vec_off(const Geo &g, const Strides &s, int b
 }
 __device__ __forceinline__ int64_t q_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sq, b, h, t); }
 __device__ __forceinline__ int64_t o_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.so, b, h, t); }
-__device__ __forceinline__ int64_t kv_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.skv, b, h, t); }
 __device__ __forceinline__ int64_t dq_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sdq, b, h, t); }
-__device__ __forceinline__ int64_t dkv_off(const Geo &g, int b, int h, int t) { return vec_off(g, g.sdkv, b, h, t); }
+// the same for key rows (packed by the keys' cu_seqlens)
+__device__ __forceinline__ int64_t vec_off_k(const Geo &g, const Strides &s, int b, int h, int k)
+{
+    if (g.thd)
+        return (int64_t)(g.cuk[b] + k) * s.t + (int64_t)h * s.h;
+    return (int64_t)b * s.b + (int64_t)h * s.h + (int64_t)k * s.t;
+}
+__device__ __forceinline__ int64_t kv_off(const Geo &g, int b, int h, int k) { return vec_off_k(g, g.skv, b, h, k); }
+__device__ __forceinline__ int64_t dkv_off(const Geo &g, int b, int h, int k) { return vec_off_k(g, g.sdkv, b, h, k); }
 
 // the D-vector of query row number r (the row order of lse and delta: BHTD
 // (b*Hq + h)*T + t, THD token*Hq + h) in a tensor with strides s
 __device__ __forceinline__ int64_t qrow_off(const Geo &g, const Strides &s, int64_t r)
 {
-    if (g.o_lin && &s == &g.so)
-        return r * g.D;
     if (g.thd)
         return (r / g.Hq) * s.t + (r % g.Hq) * s.h;
     const int64_t bh = r / g.T;
@@ -102,17 +123,56 @@ __device__ __forceinline__ int seq_of_token(const Geo &g, int tok)
     return lo;
 }
 
-// does row (b, kvh, t) select block j?  (dense: every block up to t/bs that
-// reaches into the window)
+// sequence holding packed key `tok` (THD); binary search over the keys' cu_seqlens
+__device__ __forceinline__ int seq_of_key(const Geo &g, int tok)
+{
+    int lo = 0, hi = g.B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (g.cuk[mid] <= tok)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// does row (b, kvh, t) select block j?  (dense: every block holding a key
+// between the window's left edge and the diagonal)
 __device__ __forceinline__ bool row_selects(const Geo &g, const int *idx, int b, int kvh, int t, int j)
 {
-    if (g.dense)
-        return j <= t / g.bs && j >= key_lo(g, t) / g.bs;
+    if (g.dense) {
+        const int c = kdiag(g, b, t), hi = min(c, seq_len_k(g, b) - 1);
+        const int lo = key_lo(g, c);
+        return lo <= hi && j <= hi / g.bs && j >= lo / g.bs;
+    }
     const int *r = idx_row(g, idx, b, kvh, t);
     for (int s = 0; s < g.S; ++s)
         if (r[s] == j)
             return true;
     return false;
+}
+
+// Dense entries: the tokens of sequence b that attend a key of block j form
+// one range, from dense_first (the first row whose diagonal reaches the
+// block) for dense_count tokens (up to the last row, or with a window the
+// last row whose window still reaches the block's last key).  0 for a block
+// past the keys' end.
+__device__ __forceinline__ int dense_first(const Geo &g, int b, int j)
+{
+    const int shift = g.br ? seq_len_k(g, b) - seq_len(g, b) : 0;
+    return max(0, j * g.bs - shift);
+}
+__device__ __forceinline__ int dense_count(const Geo &g, int b, int j)
+{
+    const int Lq = seq_len(g, b), Lk = seq_len_k(g, b);
+    if (j * g.bs >= Lk)
+        return 0;
+    const int shift = g.br ? Lk - Lq : 0;
+    int end = Lq;
+    if (g.window > 0)
+        end = min(end, (j + 1) * g.bs + g.window - 1 - shift);
+    return max(0, end - dense_first(g, b, j));
 }
 
 // The first error recorded wins; later ones are dropped.

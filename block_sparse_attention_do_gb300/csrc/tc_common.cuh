@@ -28,7 +28,9 @@ constexpr int kKvBytes = 2 * kKvHalfBytes;
 // `box_heads` heads x 64 columns; the smem result is box_tok*box_heads rows
 // of 128 bytes, 128B-swizzled, in (token-major for THD, head-major for BHTD)
 // order.
-bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s);
+// keys = true maps a key-side tensor (k, v): the key length / key count.
+bool make_tmap(CUtensorMap *map, const void *base, const Geo &g, int H, int box_tok, int box_heads, const Strides &s,
+               bool keys = false);
 
 // Row-group tile layout (gathered rows of the dK/dV kernel): the tile's
 // rows go in groups of 8; group R/8 occupies 2048 bytes, its 64-column half h
@@ -213,7 +215,9 @@ __device__ __forceinline__ void qtile_union_warp(const Geo &g, const int *idx, c
         ubits[x] = 0u;
     __syncwarp();
     if (g.dense) {
-        const int jmin = key_lo(g, t0) / g.bs, jmax = (t0 + nvalid - 1) / g.bs;
+        // from the first row's window edge to the last row's diagonal
+        const int hi = min(kdiag(g, b, t0 + nvalid - 1), seq_len_k(g, b) - 1);
+        const int jmin = key_lo(g, kdiag(g, b, t0)) / g.bs, jmax = hi >= 0 ? hi / g.bs : -1;
         for (int j = jmin + lane; j <= jmax; j += 32)
             atomicOr(&ubits[j >> 5], 1u << (j & 31));
     } else {
@@ -269,10 +273,11 @@ __device__ __forceinline__ void qtile_union_warp(const Geo &g, const int *idx, c
     __syncwarp();
 }
 
-// does the row's token select block j?  (valid rows only)
-__device__ __forceinline__ bool qtile_selects(const Geo &g, const uint32_t *my_mask, int t, int j)
+// does the row's token select block j?  (valid rows only; klo .. khi: the
+// row's attended key range, which decides for the dense entries)
+__device__ __forceinline__ bool qtile_selects(const Geo &g, const uint32_t *my_mask, int klo, int khi, int j)
 {
-    return g.dense ? (j <= t / g.bs && j >= key_lo(g, t) / g.bs) : (((my_mask[j >> 5] >> (j & 31)) & 1u) != 0);
+    return g.dense ? (klo <= khi && j <= khi / g.bs && j >= klo / g.bs) : (((my_mask[j >> 5] >> (j & 31)) & 1u) != 0);
 }
 
 }  // namespace nsa

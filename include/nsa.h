@@ -69,11 +69,12 @@ enum { NSA_DTYPE_F32 = 0, NSA_DTYPE_BF16 = 1 };
 /*
  * Layouts.  BHTD: q,o,dO,dq [B,Hq,T,D]; k,v,dk,dv [B,Hkv,T,D];
  * idx [B,Hkv,T,S]; lse [B,Hq,T].
- * THD (packed variable length, only through the *_varlen_* entry points):
- * q,o,dO,dq [total,Hq,D]; k,v,dk,dv [total,Hkv,D]; idx [total,Hkv,S] with
- * sequence-local block ids; lse [total,Hq]; cu_seqlens [B+1] int32 with
- * cu_seqlens[0] = 0 and cu_seqlens[B] = total.  Causality and block
- * numbering restart at every sequence (query and key lengths are equal).
+ * THD (packed variable length, through the entry points that take
+ * cu_seqlens): q,o,dO,dq [total,Hq,D]; k,v,dk,dv [total,Hkv,D]; idx
+ * [total,Hkv,S] with sequence-local block ids; lse [total,Hq]; cu_seqlens
+ * [B+1] int32 with cu_seqlens[0] = 0 and cu_seqlens[B] = total.  Causality
+ * and block numbering restart at every sequence.  Query and key lengths are
+ * equal except through nsa_causal_*, which take the keys' own cu_seqlens.
  */
 enum { NSA_LAYOUT_BHTD = 0, NSA_LAYOUT_THD = 1 };
 
@@ -109,6 +110,21 @@ typedef struct nsa_problem {
     int64_t o_stride[3];   /* o (written by the forward, read by the backward) and dO */
     int64_t dq_stride[3];  /* dq */
     int64_t dkv_stride[3]; /* dk and dv */
+    /*
+     * Keys with their own lengths -- read by the nsa_causal_* entry points
+     * only (every other entry point has keys and queries of equal length):
+     *   Tk           BHTD: key length of every sequence; THD: an upper bound
+     *                on every key length; 0 means T
+     *   total_keys   THD: cu_seqlens_k[B] (at least 1); ignored for BHTD
+     *   bottom_right 0: row t of a sequence sits at key position t (the
+     *                diagonal of the top-left corner); 1: at t + Lk - Lq
+     *                (the bottom-right corner, so the last query row sees
+     *                every key)
+     */
+    int32_t Tk;
+    int32_t total_keys;
+    int32_t bottom_right;
+    int32_t reserved2;     /* set to 0 */
 } nsa_problem;
 
 /* Workspace bytes needed by the forward / backward entry points (0 on an invalid problem). */
@@ -205,6 +221,36 @@ nsa_status nsa_sink_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_
                         const void *q, const void *k, const void *v, const void *o, const void *dO,
                         const float *lse, void *dq, void *dk, void *dv, float *dsinks, void *ws,
                         size_t ws_bytes, void *stream);
+
+/*
+ * Dense causal attention whose keys have lengths of their own (cuDNN-frontend
+ * page: the SDPA backward's THD path takes cum_seqlen_q and cum_seqlen_k,
+ * and its causal mask comes aligned to the top-left corner or, with
+ * causal_bottom_right, to the bottom-right one; both combine with the
+ * sliding window).  For a sequence with Lq query rows and Lk keys, row t
+ * sits at key position c_t = t (p->bottom_right = 0) or t + Lk - Lq
+ * (p->bottom_right = 1) and attends key k iff k <= c_t, k < Lk and, with
+ * window >= 1, c_t - k < window.  A row that attends nothing (bottom-right
+ * with Lq > Lk: the first Lq - Lk rows) gets O = 0, LSE = -inf and no
+ * gradient.
+ * Layouts: BHTD q, o, dO, dq [B,Hq,T,D], k, v, dk, dv [B,Hkv,Tk,D] (Tk =
+ * p->Tk, or T when 0), lse [B,Hq,T]; cu_seqlens_q and cu_seqlens_k NULL.
+ * THD: q [total_tokens,Hq,D], k [total_keys,Hkv,D], lse [total_tokens,Hq];
+ * cu_seqlens_q [B+1] (cu_seqlens_q[B] = p->total_tokens) and cu_seqlens_k
+ * [B+1] (cu_seqlens_k[B] = p->total_keys), both device int32; p->T and
+ * p->Tk bound every query and key length.  window = 0 is plain causal.
+ * The workspaces come from nsa_causal_{fwd,bwd}_workspace_size; p->S is
+ * ignored.  With Lq = Lk both alignments are the dense causal case.
+ */
+size_t nsa_causal_fwd_workspace_size(const nsa_problem *p);
+size_t nsa_causal_bwd_workspace_size(const nsa_problem *p);
+nsa_status nsa_causal_fwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, const void *q, const void *k, const void *v,
+                          void *o, float *lse, void *ws, size_t ws_bytes, void *stream);
+nsa_status nsa_causal_bwd(const nsa_problem *p, int32_t window, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, const void *q, const void *k, const void *v,
+                          const void *o, const void *dO, const float *lse, void *dq, void *dk,
+                          void *dv, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Reusable backward plan.  The pages build nothing like it: it is the inverse

@@ -170,3 +170,31 @@ def test_declared_strides_are_checked(lib):
     assert api.fwd_workspace_size(pt) == 0
     assert lib.nsa_sel_varlen_fwd(C.byref(pt), C.c_void_p(256), *([C.c_void_p(256)] * 6), ws, 1 << 30,
                                   None) == 1
+
+
+def test_causal_entries_check_their_arguments(lib):
+    """nsa_causal_*: the key geometry is validated before any launch."""
+    from block_sparse_attention_do_gb300 import api
+
+    p = _p(T=256)
+    p.Tk = 300
+    p.bottom_right = 1
+    n = lib.nsa_causal_bwd_workspace_size(C.byref(p))
+    assert n > 0
+    assert lib.nsa_causal_fwd_workspace_size(C.byref(p)) >= 256
+    p.bottom_right = 2
+    assert lib.nsa_causal_bwd_workspace_size(C.byref(p)) == 0
+    p.bottom_right = 0
+    p.Tk = -1
+    assert lib.nsa_causal_bwd_workspace_size(C.byref(p)) == 0
+    # packed layout: both cu_seqlens or neither, and total_keys >= 1
+    pt = api.problem(2, 4, 2, 256, 128, 64, 4, __import__("torch").bfloat16, layout=1, total_tokens=300)
+    assert lib.nsa_causal_bwd_workspace_size(C.byref(pt)) == 0  # total_keys = 0
+    pt.total_keys = 400
+    pt.Tk = 256
+    assert lib.nsa_causal_bwd_workspace_size(C.byref(pt)) > 0
+    dummy = C.c_void_p(256)
+    s = lib.nsa_causal_fwd(C.byref(pt), 0, dummy, None, *([dummy] * 5), dummy, 1 << 30, None)
+    assert s == 1
+    s = lib.nsa_causal_fwd(C.byref(p), -1, None, None, *([dummy] * 5), dummy, 1 << 30, None)
+    assert s == 1

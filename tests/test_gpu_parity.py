@@ -744,3 +744,41 @@ def test_declared_strides_packed_thd():
     torch.cuda.synchronize()
     ref = oracle.sel_bwd(xq, xk, xv, idx, do, bs, cu_seqlens=cu)
     _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, torch.bfloat16)
+
+
+# ---- dense causal attention with keys of their own lengths (nsa_causal_*):
+# top-left and bottom-right alignment of the diagonal, with a window
+
+
+CAUSAL_CASES = [
+    # dtype, (B, Hq, Hkv, D, bs), q lengths, k lengths (None: BHTD with Tq, Tk), bottom_right, window
+    (torch.bfloat16, (2, 16, 1, 128, 64), 200, 333, True, 0),     # tensor cores, G = 16, Lk > Lq
+    (torch.bfloat16, (1, 32, 2, 128, 64), 300, 130, True, 0),     # Lq > Lk: the first 170 rows see nothing
+    (torch.bfloat16, (1, 16, 2, 128, 64), 150, 260, False, 0),    # top-left: keys past Lq unused
+    (torch.bfloat16, (1, 8, 2, 128, 64), 300, 500, True, 100),    # G = 4 (cp.async gathers), window
+    (torch.float32, (2, 6, 2, 64, 32), 100, 150, True, 40),       # CUDA cores
+    (torch.bfloat16, (0, 8, 2, 128, 64), [130, 1, 64, 257], [200, 64, 1, 257], True, 70),   # THD
+    (torch.bfloat16, (0, 32, 2, 128, 64), [300, 90], [40, 300], True, 0),                   # THD, G = 16
+    (torch.float32, (0, 4, 2, 64, 32), [50, 7], [80, 3], False, 0),                          # THD, CUDA cores
+]
+
+
+@pytest.mark.parametrize("dtype,shape,lq,lk,br,window", CAUSAL_CASES)
+def test_causal_own_key_lengths(dtype, shape, lq, lk, br, window):
+    B, Hq, Hkv, D, bs = shape
+    if isinstance(lq, list):
+        cuq, cuk = inputs.cu_seqlens_from_lengths(lq), inputs.cu_seqlens_from_lengths(lk)
+        q, _, _, do = inputs.make_qkv_do(1, Hq, Hkv, sum(lq), D, dtype=dtype, seed=50, layout="thd")
+        _, k, v, _ = inputs.make_qkv_do(1, Hq, Hkv, sum(lk), D, dtype=dtype, seed=51, layout="thd")
+        gcq, gck = cuq.to(DEV), cuk.to(DEV)
+    else:
+        cuq = cuk = gcq = gck = None
+        q, _, _, do = inputs.make_qkv_do(B, Hq, Hkv, lq, D, dtype=dtype, seed=50)
+        _, k, v, _ = inputs.make_qkv_do(B, Hq, Hkv, lk, D, dtype=dtype, seed=51)
+    g = [x.to(DEV) for x in (q, k, v, do)]
+    kw = dict(block_size=bs, window=window, bottom_right=br, cu_seqlens_q=gcq, cu_seqlens_k=gck)
+    o, lse = api.causal_fwd(g[0], g[1], g[2], **kw)
+    dq, dk, dv = api.causal_bwd(g[0], g[1], g[2], o, g[3], lse, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.causal(q, k, v, do, cu_seqlens_q=cuq, cu_seqlens_k=cuk, window=window, bottom_right=br)
+    _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, dtype)
