@@ -195,6 +195,15 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         int it = 0, uc = 0, qs = 0, qph = 0;  // tile count; its Q stage and that stage's phase
         int last_tile = -1, last_kv = -1;     // newest TMA batches (for the abort path)
         uint64_t *pend = nullptr;             // cp.async gather: the tile whose release is still due
+        // cp.async gather: the swizzled destination of this lane's chunk in row
+        // 2u + (lane >> 4) of an 8-row group, and ceil(2^16 / G) for r / G
+        uint32_t dsto[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int rr = 2 * u + (lane >> 4), c = lane & 15;
+            dsto[u] = (c >> 3) * kRgHalf + rr * 128 + (((c & 7) ^ rr) << 4);
+        }
+        const int recipG = (65536 + G - 1) / G;
         // releases the pending cp.async tile (all of this lane's copies landed)
         auto flush = [&]() {
             if (MODE == LOAD_CPASYNC && pend) {
@@ -285,24 +294,22 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                     const __nv_bfloat16 *base = tensor ? p.dO : p.q;
                     const Strides &str = tensor ? g.so : g.sq;
                     const uint32_t tile_s = tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes;
-                    const int c = lane & 15;
-                    const int64_t hbase = (int64_t)(kvh * G) * str.h + c * 8;
-                    const int64_t cu_b = g.thd ? (int64_t)g.cu[b] : 0;
-                    // row r = token tl * G + head hh, stepped two rows at a time
-                    int tl = (lane >> 4) / G, hh = (lane >> 4) % G;
-                    for (int r = lane >> 4; r < kRows; r += 2, hh += 2) {
-                        while (hh >= G) {
-                            hh -= G;
-                            ++tl;
+                    // lane: chunk c of rows 8*grp + 2u + hi; its head 0 of the
+                    // group and its column, then per row token * stride_t + head * stride_h
+                    const int c = lane & 15, hi = lane >> 4;
+                    const __nv_bfloat16 *rowbase =
+                        base + (int64_t)(kvh * G) * str.h + c * 8 + (g.thd ? (int64_t)g.cu[b] * str.t : (int64_t)b * str.b);
+#pragma unroll 2
+                    for (int grp = 0; grp < kRows / 8; ++grp) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int r = grp * 8 + 2 * u + hi;
+                            const int tl = (r * recipG) >> 16, hh = r - tl * G;  // r / G, r % G (r < 128)
+                            const bool valid = r < nrows && tl < ntok;
+                            const __nv_bfloat16 *src =
+                                valid ? rowbase + (int64_t)tok[tl] * str.t + (int64_t)hh * str.h : base;
+                            cp_async_16(tile_s + grp * kRgStride + dsto[u], src, valid ? 16u : 0u);
                         }
-                        const bool valid = r < nrows && tl < ntok;
-                        const __nv_bfloat16 *src = base;
-                        if (valid) {
-                            const int64_t t = tok[tl];
-                            src = base + hbase + (int64_t)hh * str.h +
-                                  (g.thd ? (cu_b + t) * str.t : (int64_t)b * str.b + t * str.t);
-                        }
-                        cp_async_16(tile_s + rg_off(r, c >> 3) + (((c & 7) ^ (r & 7)) << 4), src, valid ? 16u : 0u);
                     }
                     cp_async_commit();
                     // the previous tile's rows have landed once only this
