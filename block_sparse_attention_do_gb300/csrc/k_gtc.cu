@@ -1,0 +1,746 @@
+// k_gtc.cu -- the forward, dQ and dK/dV on the tcgen05 tensor cores for the
+// shapes the specialised kernels (bf16, D = 128, 64-key blocks) do not take:
+// head dims 32, 64 and 128 with blocks of 16, 32 or 64 keys in bf16, and head
+// dims 32 and 64 in fp32.
+//
+// fp32 runs in split precision on the bf16 tensor cores: every fp32 operand x
+// is held as a bf16 high part h = bf16(x) and a bf16 low part l = bf16(x - h)
+// (|x - h - l| <= 2^-18 |x|), and every product A B^T is issued as three MMAs,
+// Ah Bh^T + Ah Bl^T + Al Bh^T, accumulated in fp32 (the dropped Al Bl^T and the
+// parts' rounding leave about 2^-16 of |A||B|).
+//
+// One CTA of 128 threads per work item -- a query tile (Tq tokens x the G
+// heads of a kv head) for the forward and dQ, a dK/dV unit of the inverse
+// index -- and thread r owns tile row r (TMEM lane r).  Thread 0 issues the
+// MMAs and commits them to one mbarrier, on which all threads wait (bounded).
+// Every operand is K-major in 128-byte-swizzled shared memory (the form every
+// N accepts); a product that needs a transposed operand (V^T and K^T for
+// P V and dS K, Q^T and dO^T for dK^T and dV^T, P^T and dS^T) reads a
+// transposed copy that the threads loading the data write beside the plain
+// one.  Head dims below 64 are zero-padded to 64; with them dV^T and dK^T are
+// one M = 128 product: [dO^T; Q^T] times [P^T; dS^T], whose diagonal blocks
+// are the two results.
+//
+// The forward takes two passes over the tile's blocks: the first finds each
+// row's maximum and sum (its LSE), the second forms P = exp(S - LSE) and
+// accumulates P V, so no accumulator is rescaled.
+#include <string.h>
+
+#include "tc_common.cuh"
+
+namespace nsa {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kThr = 128;    // threads per CTA = tile rows
+constexpr int kKeyPad = 64;  // key-dimension width of P, dS, K^T, V^T tiles
+
+struct GParams {
+    Geo g;
+    const void *q, *k, *v, *dO;
+    const float *lse, *delta;
+    const int *idx;
+    const int *offsets, *rows;
+    const Unit *units;
+    const WsHeader *hdr;
+    float *partials;
+    void *o, *dq, *dk, *dv;
+    float *lse_out;
+    int *err;
+    int Dp;       // head dim padded to 64 or 128
+    int ntiles;   // query tiles (forward / dQ)
+    int wait_us;  // bounded-wait limit in microseconds (0: the default)
+};
+
+// byte offset of element (r, c) of a K-major tile with R rows (a multiple of
+// 8) and 64-column chunks of 128-byte rows, 128-byte swizzle
+__device__ __forceinline__ uint32_t swz(int r, int c, int R)
+{
+    return (uint32_t)((c >> 6) * (R * 128) + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
+                      ((c & 7) << 1));
+}
+
+// descriptor of K-step kk (16 elements) of such a tile
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int R, int kk)
+{
+    return sdesc_sw128(tile + (kk >> 2) * (R * 128) + (kk & 3) * 32, 16, 1024);
+}
+
+__device__ __forceinline__ void st_u16(uint32_t addr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x)
+{
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&b);
+}
+
+// An operand value as stored: its high part, and (SPLIT) its low part
+template <bool SPLIT> struct Parts {
+    uint16_t hi, lo;
+};
+template <bool SPLIT> __device__ __forceinline__ Parts<SPLIT> split_of(float x)
+{
+    Parts<SPLIT> p;
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    p.hi = *reinterpret_cast<uint16_t *>(&h);
+    p.lo = SPLIT ? bf16_bits(x - __bfloat162float(h)) : (uint16_t)0;
+    return p;
+}
+
+// writes element (r, c) of a tile (and of its low-part copy, lo_off bytes on)
+template <bool SPLIT>
+__device__ __forceinline__ void put(uint32_t tile, int R, uint32_t lo_off, int r, int c, float x)
+{
+    const Parts<SPLIT> p = split_of<SPLIT>(x);
+    const uint32_t a = tile + swz(r, c, R);
+    st_u16(a, p.hi);
+    if (SPLIT)
+        st_u16(a + lo_off, p.lo);
+}
+
+// D (+)= A B^T over nk K-steps; SPLIT: three products of the parts.  A and B
+// are K-major tiles (A with Ra rows, B with Rb rows) whose low parts sit
+// alo / blo bytes after them.
+template <bool SPLIT>
+__device__ __forceinline__ void product(uint32_t d, uint32_t a, int Ra, uint32_t alo, uint32_t b, int Rb, uint32_t blo,
+                                        uint32_t idesc, int nk, bool acc)
+{
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint32_t on = (acc || kk > 0) ? 1u : 0u;
+        mma_bf16(d, kdesc(a, Ra, kk), kdesc(b, Rb, kk), idesc, on);
+        if (SPLIT) {
+            mma_bf16(d, kdesc(a, Ra, kk), kdesc(b + blo, Rb, kk), idesc, 1u);
+            mma_bf16(d, kdesc(a + alo, Ra, kk), kdesc(b, Rb, kk), idesc, 1u);
+        }
+    }
+}
+
+// element x of a row of the input (bf16 or fp32 by SPLIT)
+template <bool SPLIT> __device__ __forceinline__ float in_at(const void *base, int64_t off)
+{
+    if (SPLIT)
+        return ((const float *)base)[off];
+    return __bfloat162float(((const __nv_bfloat16 *)base)[off]);
+}
+
+template <bool SPLIT> __device__ __forceinline__ void out_at(void *base, int64_t off, float x)
+{
+    if (SPLIT)
+        ((float *)base)[off] = x;
+    else
+        ((__nv_bfloat16 *)base)[off] = __float2bfloat16_rn(x);
+}
+
+// Shared synchronisation of the CTA: the MMA barrier's phase and the wait
+// context (abort flag, limit).  issue_wait: thread 0 commits every MMA it
+// issued so far to the barrier, everyone waits for it; false (on every
+// thread) once a wait gave up.
+struct Sync {
+    uint64_t *bar;
+    volatile int *ctx;
+    uint32_t phase;
+};
+
+__device__ __forceinline__ bool commit_wait(Sync &s)
+{
+    if (threadIdx.x == 0)
+        mma_commit(s.bar);
+    bool ok = mbar_wait(s.bar, s.phase, s.ctx);
+    s.phase ^= 1;
+    ok = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+    return ok;
+}
+
+// every thread's shared-memory writes are visible to the tensor cores, and
+// every thread's TMEM reads are done, before thread 0 issues the next MMAs
+__device__ __forceinline__ void to_mma()
+{
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// The kernels' common start: the wait context, the MMA barrier and 256 TMEM
+// columns; the end: every MMA done, TMEM freed, a timeout reported.
+__device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Sync &s)
+{
+    uint64_t *bar = (uint64_t *)misc;
+    volatile int *ctx = (volatile int *)(misc + 16);
+    uint32_t *slot = (uint32_t *)(misc + 32);
+    if (threadIdx.x == 0) {
+        ctx[0] = 0;
+        ctx[1] = p.wait_us;
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x < 32) {
+        tmem_alloc(slot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    s.bar = bar;
+    s.ctx = ctx;
+    s.phase = 0;
+    return *slot;
+}
+
+__device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p)
+{
+    // MMAs still in flight (after a timeout) complete before TMEM is freed
+    if (threadIdx.x == 0) {
+        mma_commit(s.bar);
+        volatile int never[2] = {0, s.ctx[1]};
+        mbar_wait(s.bar, s.phase, never);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (s.ctx[0] && threadIdx.x == 0)
+        set_error(p.err, NSA_ERR_DEVICE_TIMEOUT);
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// loads key block j (keys k0 .. k0+bs-1 of sequence b, kv head kvh) of the
+// kv-shaped tensor src into a [bs][Dp] tile (transposed = false) or a
+// [Dp][64] tile (true); keys past the sequence's end and dims past D are 0.
+template <bool SPLIT>
+__device__ __forceinline__ void load_block(const Geo &g, const void *src, uint32_t tile, uint32_t lo_off, int Dp,
+                                           int b, int kvh, int k0, bool transposed)
+{
+    const int bs = g.bs, nk = min(bs, seq_len_k(g, b) - k0);
+    for (int e = threadIdx.x; e < bs * Dp; e += kThr) {
+        const int key = e / Dp, d = e % Dp;
+        float x = 0.f;
+        if (key < nk && d < g.D)
+            x = in_at<SPLIT>(src, kv_off(g, b, kvh, k0 + key) + d);
+        if (transposed)
+            put<SPLIT>(tile, Dp, lo_off, d, key, x);
+        else
+            put<SPLIT>(tile, bs, lo_off, key, d, x);
+    }
+}
+
+// row r of a query tile: token tl of the tile (rows token-major), head hh of the group
+__device__ __forceinline__ void qrow(int G, int r, int &tl, int &hh)
+{
+    tl = r / G;
+    hh = r % G;
+}
+
+// 16 consecutive TMEM columns of this thread's lane (row), as floats
+__device__ __forceinline__ void ld_cols(uint32_t tmem, int col, float *out, int n)
+{
+    const uint32_t base = tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + col;
+    for (int c0 = 0; c0 < n; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(base + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            out[c0 + i] = __uint_as_float(v[i]);
+    }
+}
+
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_ACC = 128, TM_ACC2 = 192;
+
+// zeroes n bytes of shared memory from p (16-byte multiples)
+__device__ __forceinline__ void zero_smem(uint8_t *p, int n)
+{
+    for (int i = threadIdx.x; i < n / 16; i += kThr)
+        ((uint4 *)p)[i] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------- forward
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Geo &g = p.g;
+    const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
+    const UnionBuf up = union_buf(g);
+    // plan: Q [128][Dp] | K [bs][Dp] | V^T [Dp][64] | P [128][64] (each with its
+    // low part right after it) | union buffer | barrier, wait context, TMEM slot
+    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, VB = Dp * kKeyPad * 2, PB = 128 * kKeyPad * 2;
+    uint8_t *q_t = sm, *k_t = q_t + parts * QB, *vt_t = k_t + parts * KB, *p_t = vt_t + parts * VB;
+    int *ubuf = (int *)(p_t + parts * PB);
+    uint8_t *misc = (uint8_t *)ubuf + up.bytes;
+    Sync sy;
+    const uint32_t tmem = g_start(misc, p, sy);
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+    qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
+    zero_smem(sm, parts * (QB + KB + VB + PB));
+    if (warp == 0 && nvalid > 0)
+        qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
+    __syncthreads();
+    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0;
+    const int *list = union_list(ubuf, up);
+    int tl, hh;
+    qrow(G, r, tl, hh);
+    const bool rvalid = r < nrows && tl < nvalid;
+    const int t = t0 + tl, words = (g.nbmax + 31) / 32;
+    const int cdiag = rvalid ? kdiag(g, b, t) : -1;
+    const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
+    const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
+    const uint32_t qs = smem_u32(q_t), ks = smem_u32(k_t), vts = smem_u32(vt_t), ps = smem_u32(p_t);
+    // the row's q (zero for rows past the tile's tokens)
+    if (rvalid) {
+        const int64_t qo = q_off(g, b, kvh * G + hh, t);
+        for (int d = 0; d < g.D; ++d)
+            put<SPLIT>(qs, 128, QB, r, d, in_at<SPLIT>(p.q, qo + d));
+    }
+    const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, false);
+    float sc[64];
+    bool ok = true;
+    // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
+    float m = -INFINITY, l = 0.f;
+    for (int i = 0; i < U && ok; ++i) {
+        const int j = list[i], k0 = j * bs;
+        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
+        to_mma();
+        if (r == 0)
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        if (!(ok = commit_wait(sy)))
+            break;
+        ld_cols(tmem, TM_S, sc, bs);
+        const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j);
+        for (int c = 0; c < bs; ++c) {
+            const int key = k0 + c;
+            if (sel && key >= klo && key <= khi) {
+                const float x = sc[c] * g.scale_l2, mn = fmaxf(m, x);
+                l = l * exp2f(m - mn) + exp2f(x - mn);
+                m = mn;
+            }
+        }
+    }
+    const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
+    // pass 2: P = exp2(scale_l2 s - lse2) on the row's keys, O += P V
+    for (int i = 0; i < U && ok; ++i) {
+        const int j = list[i], k0 = j * bs;
+        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
+        load_block<SPLIT>(g, p.v, vts, VB, Dp, b, kvh, k0, true);
+        to_mma();
+        if (r == 0)
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        if (!(ok = commit_wait(sy)))
+            break;
+        ld_cols(tmem, TM_S, sc, bs);
+        const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j) && lse2 != -INFINITY;
+        for (int c = 0; c < bs; ++c) {
+            const int key = k0 + c;
+            const float pv = (sel && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - lse2) : 0.f;
+            put<SPLIT>(ps, 128, PB, r, c, pv);
+        }
+        to_mma();
+        if (r == 0)
+            product<SPLIT>(tmem + TM_ACC, ps, 128, PB, vts, Dp, VB, idO, bs / 16, i > 0);
+        ok = commit_wait(sy);
+    }
+    // epilogue: O (already normalised) and the natural-log LSE.  Every lane
+    // runs the TMEM loads (warp-wide .sync.aligned); valid rows store.
+    if (ok) {
+        const int64_t oo = rvalid ? o_off(g, b, kvh * G + hh, t) : 0;
+        float acc[16];
+        for (int c0 = 0; c0 < g.D; c0 += 16) {
+            if (U > 0)
+                ld_cols(tmem, TM_ACC + c0, acc, 16);
+            if (rvalid)
+                for (int x = 0; x < 16 && c0 + x < g.D; ++x)
+                    out_at<SPLIT>(p.o, oo + c0 + x, (U > 0 && lse2 != -INFINITY) ? acc[x] : 0.f);
+        }
+        if (rvalid)
+            p.lse_out[stat_off(g, b, kvh * G + hh, t)] = lse2 == -INFINITY ? -INFINITY : lse2 * 0.6931471805599453f;
+    }
+    g_end(tmem, sy, p);
+}
+
+// --------------------------------------------------------------------- dQ
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Geo &g = p.g;
+    const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
+    const UnionBuf up = union_buf(g);
+    // plan: Q, dO [128][Dp] | K, V [bs][Dp] | K^T [Dp][64] | dS [128][64] | union | misc
+    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, TB = Dp * kKeyPad * 2, PB = 128 * kKeyPad * 2;
+    uint8_t *q_t = sm, *do_t = q_t + parts * QB, *k_t = do_t + parts * QB, *v_t = k_t + parts * KB;
+    uint8_t *kt_t = v_t + parts * KB, *ds_t = kt_t + parts * TB;
+    int *ubuf = (int *)(ds_t + parts * PB);
+    uint8_t *misc = (uint8_t *)ubuf + up.bytes;
+    Sync sy;
+    const uint32_t tmem = g_start(misc, p, sy);
+    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+    qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
+    zero_smem(sm, parts * (2 * QB + 2 * KB + TB + PB));
+    if (warp == 0 && nvalid > 0)
+        qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
+    __syncthreads();
+    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0;
+    const int *list = union_list(ubuf, up);
+    int tl, hh;
+    qrow(G, r, tl, hh);
+    const bool rvalid = r < nrows && tl < nvalid;
+    const int t = t0 + tl, words = (g.nbmax + 31) / 32;
+    const int cdiag = rvalid ? kdiag(g, b, t) : -1;
+    const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
+    const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
+    const uint32_t qs = smem_u32(q_t), dos = smem_u32(do_t), ks = smem_u32(k_t), vs = smem_u32(v_t);
+    const uint32_t kts = smem_u32(kt_t), dss = smem_u32(ds_t);
+    float l2 = -INFINITY, dl = 0.f;
+    if (rvalid) {
+        const int h = kvh * G + hh;
+        const int64_t qo = q_off(g, b, h, t), oo = o_off(g, b, h, t), so = stat_off(g, b, h, t);
+        for (int d = 0; d < g.D; ++d) {
+            put<SPLIT>(qs, 128, QB, r, d, in_at<SPLIT>(p.q, qo + d));
+            put<SPLIT>(dos, 128, QB, r, d, in_at<SPLIT>(p.dO, oo + d));
+        }
+        l2 = p.lse[so] * 1.4426950408889634f;
+        dl = p.delta[so];
+    }
+    const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, false);
+    float sc[64], dp[64];
+    bool ok = true;
+    for (int i = 0; i < U && ok; ++i) {
+        const int j = list[i], k0 = j * bs;
+        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
+        load_block<SPLIT>(g, p.v, vs, KB, Dp, b, kvh, k0, false);
+        load_block<SPLIT>(g, p.k, kts, TB, Dp, b, kvh, k0, true);
+        to_mma();
+        if (r == 0) {
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+            product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
+        }
+        if (!(ok = commit_wait(sy)))
+            break;
+        ld_cols(tmem, TM_S, sc, bs);
+        ld_cols(tmem, TM_DP, dp, bs);
+        const bool sel = rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
+        for (int c = 0; c < bs; ++c) {
+            const int key = k0 + c;
+            const float pv = (sel && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - l2) : 0.f;
+            put<SPLIT>(dss, 128, PB, r, c, pv * (dp[c] - dl));
+        }
+        to_mma();
+        if (r == 0)
+            product<SPLIT>(tmem + TM_ACC, dss, 128, PB, kts, Dp, TB, idQ, bs / 16, i > 0);
+        ok = commit_wait(sy);
+    }
+    if (ok) {
+        float acc[16];
+        const int64_t qo = rvalid ? dq_off(g, b, kvh * G + hh, t) : 0;
+        for (int c0 = 0; c0 < g.D; c0 += 16) {
+            if (U > 0)
+                ld_cols(tmem, TM_ACC + c0, acc, 16);
+            if (rvalid)
+                for (int x = 0; x < 16 && c0 + x < g.D; ++x)
+                    out_at<SPLIT>(p.dq, qo + c0 + x, U > 0 ? acc[x] * g.scale : 0.f);
+        }
+    }
+    g_end(tmem, sy, p);
+}
+
+// ------------------------------------------------------------------ dK/dV
+// One work unit (b, kv head, block j, a run of the block's token list) per
+// CTA.  Per tile of Tt tokens x G heads (128 rows):
+//   S = Q K_j^T, dP = dO V_j^T, P and dS per row, then
+//   Dp = 64:  [dV^T; dK^T-ish] += [dO^T; Q^T] [P^T; dS^T]^T  (one M = 128 product
+//             whose diagonal blocks are dV^T (lanes 0..63, columns 0..bs-1) and
+//             dK^T (lanes 64..127, columns bs..2bs-1))
+//   Dp = 128: dV^T += dO^T P, dK^T += Q^T dS (two M = 128 products)
+// accumulated in TMEM over the unit's tiles; then written out (a whole block)
+// or as fp32 partials of a split block.
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
+{
+    const int ui = blockIdx.x;
+    if (ui >= p.hdr->n_units)
+        return;  // uniform over the CTA: nothing allocated yet
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Geo &g = p.g;
+    const int Dp = p.Dp, bs = g.bs, G = g.G, parts = SPLIT ? 2 : 1;
+    const int Tt = tile_tokens(G), nrows = Tt * G;
+    const bool stacked = Dp == 64;
+    // plan: K, V [bs][Dp] | Q, dO [128][Dp] | transposed A: stacked [dO^T; Q^T]
+    // [128][128 rows], else dO^T and Q^T [128][128 rows] each | transposed B:
+    // stacked [P^T; dS^T] [2 bs][128 rows], else P^T and dS^T [bs][128 rows]
+    // each (low parts right after each) | misc
+    const uint32_t KB = bs * Dp * 2, QB = 128 * Dp * 2, AB = 128 * 128 * 2, BB = bs * 128 * 2;
+    uint8_t *k_t = sm, *v_t = k_t + parts * KB, *q_t = v_t + parts * KB, *do_t = q_t + parts * QB;
+    uint8_t *a_t = do_t + parts * QB;                                      // dO^T (stacked: [dO^T; Q^T])
+    uint8_t *a2_t = a_t + (stacked ? 0 : parts * AB);                      // Q^T (separate)
+    uint8_t *b_t = a_t + parts * AB * (stacked ? 1 : 2);                   // P^T (stacked: [P^T; dS^T])
+    uint8_t *b2_t = b_t + (stacked ? 0 : parts * BB);                      // dS^T (separate)
+    uint8_t *misc = b_t + parts * BB * 2;
+    const uint32_t ALO = stacked ? AB : AB, BLO = stacked ? 2 * BB : BB;  // low-part offsets
+    Sync sy;
+    const uint32_t tmem = g_start(misc, p, sy);
+    const int r = threadIdx.x, warp = r >> 5;
+    const Unit u = p.units[ui];
+    const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv, j = u.j, k0 = j * bs;
+    const int Lk = seq_len_k(g, b), nk = min(bs, Lk - k0);
+    zero_smem(sm, (int)(misc - sm));
+    __syncthreads();
+    const uint32_t ks = smem_u32(k_t), vs = smem_u32(v_t), qs = smem_u32(q_t), dos = smem_u32(do_t);
+    const uint32_t as_ = smem_u32(a_t), a2s = smem_u32(a2_t), bs_ = smem_u32(b_t), b2s = smem_u32(b2_t);
+    load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
+    load_block<SPLIT>(g, p.v, vs, KB, Dp, b, kvh, k0, false);
+    int tl, hh;
+    qrow(G, r, tl, hh);
+    const int csr0 = g.dense ? dense_first(g, b, j) + u.begin : p.offsets[u.bg * g.nbmax + j] + u.begin;
+    const uint32_t idS = idesc_bf16(128, bs, false, false);
+    const uint32_t idA = idesc_bf16(128, stacked ? 2 * bs : bs, false, false);
+    const int ntiles = (u.count + Tt - 1) / Tt;
+    float sc[64], dp[64];
+    bool ok = true;
+    for (int ti = 0; ti < ntiles && ok; ++ti) {
+        const int pos = ti * Tt + tl;
+        const bool rvalid = r < nrows && pos < u.count;
+        const int t = rvalid ? (g.dense ? csr0 + pos : p.rows[csr0 + pos]) : 0;
+        const int h = kvh * G + hh;
+        float l2 = 0.f, dl = 0.f;
+        // the row's q and dO, plain and transposed (zeros for rows past the list)
+        {
+            const int64_t qo = rvalid ? q_off(g, b, h, t) : 0, oo = rvalid ? o_off(g, b, h, t) : 0;
+            for (int d = 0; d < g.D; ++d) {
+                const float xq = rvalid ? in_at<SPLIT>(p.q, qo + d) : 0.f;
+                const float xo = rvalid ? in_at<SPLIT>(p.dO, oo + d) : 0.f;
+                put<SPLIT>(qs, 128, QB, r, d, xq);
+                put<SPLIT>(dos, 128, QB, r, d, xo);
+                if (stacked) {
+                    put<SPLIT>(as_, 128, ALO, d, r, xo);
+                    put<SPLIT>(as_, 128, ALO, 64 + d, r, xq);
+                } else {
+                    put<SPLIT>(as_, 128, ALO, d, r, xo);
+                    put<SPLIT>(a2s, 128, ALO, d, r, xq);
+                }
+            }
+            if (rvalid) {
+                const int64_t so = stat_off(g, b, h, t);
+                l2 = p.lse[so] * 1.4426950408889634f;
+                dl = p.delta[so];
+            }
+        }
+        to_mma();
+        if (r == 0) {
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+            product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
+        }
+        if (!(ok = commit_wait(sy)))
+            break;
+        ld_cols(tmem, TM_S, sc, bs);
+        ld_cols(tmem, TM_DP, dp, bs);
+        // the row's keys: from the window's left edge to its diagonal
+        const int cdiag = rvalid ? kdiag(g, b, t) : -1;
+        const int khi = rvalid ? min(cdiag, Lk - 1) : -1, klo = key_lo(g, cdiag);
+        const bool live = rvalid && l2 != -INFINITY;
+        for (int c = 0; c < bs; ++c) {
+            const int key = k0 + c;
+            const float pv = (live && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - l2) : 0.f;
+            const float dsv = pv * (dp[c] - dl);
+            if (stacked) {
+                put<SPLIT>(bs_, 2 * bs, BLO, c, r, pv);
+                put<SPLIT>(bs_, 2 * bs, BLO, bs + c, r, dsv);
+            } else {
+                put<SPLIT>(bs_, bs, BLO, c, r, pv);
+                put<SPLIT>(b2s, bs, BLO, c, r, dsv);
+            }
+        }
+        to_mma();
+        if (r == 0) {
+            if (stacked) {
+                product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, 2 * bs, BLO, idA, 128 / 16, ti > 0);
+            } else {
+                product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, bs, BLO, idA, 128 / 16, ti > 0);
+                product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
+            }
+        }
+        ok = commit_wait(sy);
+    }
+    // epilogue: lane r holds dim r of dV^T (stacked: lanes 0..63) and of dK^T
+    // (stacked: lanes 64..127, columns bs..2bs-1; else the second accumulator)
+    if (ok) {
+        const bool direct = u.slot < 0;
+        for (int which = 0; which < 2; ++which) {  // 0 dV, 1 dK
+            // warp-uniform columns: stacked warps 0-1 read dV's, 2-3 dK's
+            int col, d;
+            bool mine;
+            if (stacked) {
+                col = TM_ACC + (warp >= 2 ? bs : 0);
+                d = r & 63;
+                mine = (which == 0) == (warp < 2);
+            } else {
+                col = which == 0 ? TM_ACC : TM_ACC2;
+                d = r;
+                mine = true;
+            }
+            ld_cols(tmem, col, sc, bs);
+            if (!mine || d >= g.D)
+                continue;
+            const float mul = which == 1 ? g.scale : 1.f;
+            for (int c = 0; c < nk; ++c) {
+                const float x = sc[c] * mul;
+                if (direct)
+                    out_at<SPLIT>(which == 1 ? p.dk : p.dv, dkv_off(g, b, kvh, k0 + c) + d, x);
+                else
+                    p.partials[((int64_t)u.slot * 2 + which) * bs * g.D + c * g.D + d] = x;
+            }
+        }
+    }
+    g_end(tmem, sy, p);
+}
+
+constexpr int kSmemLimit = 232448;
+
+template <typename K> bool smem_ok(K kernel, size_t bytes)
+{
+    if (bytes > (size_t)kSmemLimit)
+        return false;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess;
+}
+
+size_t union_bytes(const Geo &g) { return union_buf(g).bytes; }
+
+GParams base_params(const Geo &g, int dtype)
+{
+    GParams p;
+    memset(&p, 0, sizeof(p));
+    p.g = g;
+    p.Dp = g.D <= 64 ? 64 : 128;
+    p.wait_us = wait_test().wait_us;
+    (void)dtype;
+    return p;
+}
+
+}  // namespace
+
+bool gtc_supported(const Geo &g, int dtype)
+{
+    if (g.G < 1 || g.G > kRows || !qtile_shape_ok(g))
+        return false;
+    if (g.bs != 16 && g.bs != 32 && g.bs != 64)
+        return false;
+    if (dtype == NSA_DTYPE_BF16)
+        return g.D == 32 || g.D == 64 || g.D == 128;
+    return g.D == 32 || g.D == 64;  // fp32: split precision
+}
+
+cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const void *v, const int *idx, void *o,
+                           float *lse, int dtype, int *err, cudaStream_t st)
+{
+    GParams p = base_params(g, dtype);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.idx = idx;
+    p.o = o;
+    p.lse_out = lse;
+    p.err = err;
+    const int Tq = tile_tokens(g.G);
+    p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
+    const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
+    const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + g.bs * p.Dp * 2 + p.Dp * kKeyPad * 2 + 128 * kKeyPad * 2) +
+                        union_bytes(g) + 64;
+    if (p.ntiles < 1)
+        return cudaSuccess;
+    if (dtype == NSA_DTYPE_F32) {
+        if (!smem_ok(fwd_gtc_kernel<true>, smem))
+            return cudaErrorInvalidValue;
+        fwd_gtc_kernel<true><<<p.ntiles, kThr, smem, st>>>(p);
+    } else {
+        if (!smem_ok(fwd_gtc_kernel<false>, smem))
+            return cudaErrorInvalidValue;
+        fwd_gtc_kernel<false><<<p.ntiles, kThr, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                          const float *lse, const float *delta, const int *idx, void *dq, int dtype, int *err,
+                          cudaStream_t st)
+{
+    GParams p = base_params(g, dtype);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.dO = dO;
+    p.lse = lse;
+    p.delta = delta;
+    p.idx = idx;
+    p.dq = dq;
+    p.err = err;
+    const int Tq = tile_tokens(g.G);
+    p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
+    const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
+    const size_t smem = 1024 +
+                        parts * (size_t)(2 * 128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + p.Dp * kKeyPad * 2 + 128 * kKeyPad * 2) +
+                        union_bytes(g) + 64;
+    if (p.ntiles < 1)
+        return cudaSuccess;
+    if (dtype == NSA_DTYPE_F32) {
+        if (!smem_ok(dq_gtc_kernel<true>, smem))
+            return cudaErrorInvalidValue;
+        dq_gtc_kernel<true><<<p.ntiles, kThr, smem, st>>>(p);
+    } else {
+        if (!smem_ok(dq_gtc_kernel<false>, smem))
+            return cudaErrorInvalidValue;
+        dq_gtc_kernel<false><<<p.ntiles, kThr, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                            const float *lse, const float *delta, const int *offsets, const int *rows,
+                            const Unit *units, const WsHeader *hdr, int max_units, float *partials, void *dk,
+                            void *dv, int dtype, int *err, cudaStream_t st)
+{
+    GParams p = base_params(g, dtype);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.dO = dO;
+    p.lse = lse;
+    p.delta = delta;
+    p.offsets = offsets;
+    p.rows = rows;
+    p.units = units;
+    p.hdr = hdr;
+    p.partials = partials;
+    p.dk = dk;
+    p.dv = dv;
+    p.err = err;
+    const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
+    const bool stacked = p.Dp == 64;
+    const size_t tiles = (size_t)2 * g.bs * p.Dp * 2 + 2 * 128 * p.Dp * 2 + (stacked ? 1 : 2) * 128 * 128 * 2 +
+                         2 * (size_t)g.bs * 128 * 2;
+    const size_t smem = 1024 + parts * tiles + 64;
+    if (max_units < 1)
+        return cudaSuccess;
+    if (dtype == NSA_DTYPE_F32) {
+        if (!smem_ok(dkdv_gtc_kernel<true>, smem))
+            return cudaErrorInvalidValue;
+        dkdv_gtc_kernel<true><<<max_units, kThr, smem, st>>>(p);
+    } else {
+        if (!smem_ok(dkdv_gtc_kernel<false>, smem))
+            return cudaErrorInvalidValue;
+        dkdv_gtc_kernel<false><<<max_units, kThr, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace nsa

@@ -68,6 +68,21 @@ cudaError_t launch_dkdv_simt(const Geo &g, const void *q, const void *k, const v
                              const int *offsets, const int *rows, void *dk, void *dv, int dtype,
                              cudaStream_t st);
 
+// ---- tensor-core kernels for the other shapes (k_gtc.cu): bf16 with D in
+// {32, 64, 128} and block_size in {16, 32, 64}, fp32 (split precision) with D
+// in {32, 64}; one CTA per query tile or dK/dV unit ----------------------------
+bool gtc_supported(const Geo &g, int dtype);
+cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const void *v, const int *idx, void *o,
+                           float *lse, int dtype, int *err, cudaStream_t st);
+cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                          const float *lse, const float *delta, const int *idx, void *dq, int dtype, int *err,
+                          cudaStream_t st);
+// max_units CTAs; those past the plan's unit count return at once
+cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
+                            const float *lse, const float *delta, const int *offsets, const int *rows,
+                            const Unit *units, const WsHeader *hdr, int max_units, float *partials, void *dk,
+                            void *dv, int dtype, int *err, cudaStream_t st);
+
 // ---- tensor-core kernels (bf16, D = 128, block_size = 64) -----------------
 bool tc_supported(const Geo &g, int dtype);
 // tile_next: a device int that is zero when the kernel starts (its work counter).

@@ -195,7 +195,7 @@ BwdWs bwd_layout(const Geo &g, int dtype)
     w.delta = off;
     off = align_up(off + sizeof(float) * (size_t)g.ntok * g.Hq);
     w.partials = off;
-    if (tc_supported(g, dtype))
+    if (tc_supported(g, dtype) || gtc_supported(g, dtype))
         off = align_up(off + sizeof(float) * 2 * (size_t)g.bs * g.D * (size_t)w.pl.max_units);
     w.utable = off;  // the dQ kernel's query-tile unions
     if (tc_supported(g, dtype))
@@ -288,6 +288,8 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         NSA_LAUNCH("fwd_tc",
                    launch_fwd_tc(g, q, k, v, idx, utable, o, lse, &hdr->err, &hdr->tile_next, mode == SPARSE, st));
     }
+    else if (gtc_supported(g, p->dtype))
+        NSA_LAUNCH("fwd_gtc", launch_fwd_gtc(g, q, k, v, idx, o, lse, p->dtype, &hdr->err, st));
     else
         NSA_LAUNCH("fwd_simt", launch_fwd_simt(g, q, k, v, idx, o, lse, p->dtype, st));
     if (sinks)
@@ -396,6 +398,12 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         // dQ right after dK/dV: it is that kernel's programmatic dependent
         NSA_LAUNCH("dq_tc",
                    launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, dq, &hdr->err, &hdr->tile_next, st));
+        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
+    } else if (gtc_supported(g, p->dtype)) {
+        NSA_LAUNCH("dkdv_gtc", launch_dkdv_gtc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
+                                               partials, dk, dv, p->dtype, &hdr->err, st));
+        NSA_LAUNCH("dq_gtc",
+                   launch_dq_gtc(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, &hdr->err, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else {
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));

@@ -782,3 +782,34 @@ def test_causal_own_key_lengths(dtype, shape, lq, lk, br, window):
     torch.cuda.synchronize()
     ref = oracle.causal(q, k, v, do, cu_seqlens_q=cuq, cu_seqlens_k=cuk, window=window, bottom_right=br)
     _compare(dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv), ref, dtype)
+
+
+# ---- the other shapes on tensor cores (k_gtc.cu): D 32/64/128 x blocks of
+# 16/32/64 in bf16, D 32/64 in fp32 by split precision
+
+
+@pytest.mark.parametrize("dtype,shape", [
+    (torch.float32, (2, 6, 2, 1024, 64, 32, 8)),    # the mid-size workload in fp32 (split precision)
+    (torch.bfloat16, (2, 6, 2, 1024, 64, 32, 8)),   # ... and in bf16
+    (torch.float32, (1, 2, 1, 128, 32, 16, 4)),     # the small fp32 fwd+bwd workload
+    (torch.bfloat16, (1, 16, 2, 300, 128, 32, 6)),  # D = 128, 32-key blocks
+    (torch.bfloat16, (2, 8, 1, 257, 32, 64, 3)),    # D = 32 (padded), 64-key blocks, G = 8
+])
+def test_other_shapes_run_on_tensor_cores(dtype, shape):
+    """These shapes launch the tensor-core kernels of k_gtc.cu (seen through
+    the library's per-launch tracer), not the CUDA-core ones, and match the
+    oracle."""
+    B, Hq, Hkv, T, D, bs, S = shape
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=dtype, seed=60)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=60)
+    api.trace_enable(64)
+    api.trace_reset()
+    try:
+        got = _run(q, k, v, do, idx, bs)
+        names = {n for n, _ in api.trace_records()}
+    finally:
+        api.trace_enable(0)
+    assert {"fwd_gtc", "dkdv_gtc", "dq_gtc"} <= names, names
+    assert not any(n.endswith("_simt") for n in names), names
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, dtype)
