@@ -120,14 +120,7 @@ __device__ __forceinline__ void product(uint32_t d, uint32_t a, int Ra, uint32_t
     }
 }
 
-// element x of a row of the input (bf16 or fp32 by SPLIT)
-template <bool SPLIT> __device__ __forceinline__ float in_at(const void *base, int64_t off)
-{
-    if (SPLIT)
-        return ((const float *)base)[off];
-    return __bfloat162float(((const __nv_bfloat16 *)base)[off]);
-}
-
+// output element (bf16 or fp32 by SPLIT)
 template <bool SPLIT> __device__ __forceinline__ void out_at(void *base, int64_t off, float x)
 {
     if (SPLIT)
@@ -211,23 +204,137 @@ __device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p)
     }
 }
 
-// loads key block j (keys k0 .. k0+bs-1 of sequence b, kv head kvh) of the
-// kv-shaped tensor src into a [bs][Dp] tile (transposed = false) or a
-// [Dp][64] tile (true); keys past the sequence's end and dims past D are 0.
-template <bool SPLIT>
-__device__ __forceinline__ void load_block(const Geo &g, const void *src, uint32_t tile, uint32_t lo_off, int Dp,
-                                           int b, int kvh, int k0, bool transposed)
+// 16-byte vectors of the input: 8 bf16 or 4 fp32 elements
+template <bool SPLIT> struct In {
+    static constexpr int VEC = SPLIT ? 4 : 8;
+    static constexpr int ES = SPLIT ? 4 : 2;
+};
+
+// the VEC values of a vector as floats
+template <bool SPLIT> __device__ __forceinline__ void unpack(const uint4 &w, float *x)
 {
-    const int bs = g.bs, nk = min(bs, seq_len_k(g, b) - k0);
-    for (int e = threadIdx.x; e < bs * Dp; e += kThr) {
-        const int key = e / Dp, d = e % Dp;
-        float x = 0.f;
-        if (key < nk && d < g.D)
-            x = in_at<SPLIT>(src, kv_off(g, b, kvh, k0 + key) + d);
-        if (transposed)
-            put<SPLIT>(tile, Dp, lo_off, d, key, x);
-        else
-            put<SPLIT>(tile, bs, lo_off, key, d, x);
+    if (SPLIT) {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    } else {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(u[i] << 16);
+            x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+    }
+}
+
+// a vector's VEC elements into row r, columns c .. c+VEC-1 of a tile (c a
+// multiple of VEC): one 16-byte store (bf16), or 8 bytes of high parts and 8
+// of low parts (SPLIT)
+template <bool SPLIT>
+__device__ __forceinline__ void put_vec(uint32_t tile, int R, uint32_t lo_off, int r, int c, const uint4 &w)
+{
+    const uint32_t a = tile + swz(r, c, R);
+    if (!SPLIT) {
+        st_shared_v4(a, w.x, w.y, w.z, w.w);
+        return;
+    }
+    float x[4];
+    unpack<true>(w, x);
+    uint32_t h[2], l[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const Parts<true> p0 = split_of<true>(x[2 * i]), p1 = split_of<true>(x[2 * i + 1]);
+        h[i] = (uint32_t)p0.hi | ((uint32_t)p1.hi << 16);
+        l[i] = (uint32_t)p0.lo | ((uint32_t)p1.lo << 16);
+    }
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(h[0]), "r"(h[1]) : "memory");
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a + lo_off), "r"(l[0]), "r"(l[1]) : "memory");
+}
+
+// A key block of a kv-shaped tensor in registers: this thread's vector i is
+// vector e = threadIdx.x + i * kThr of the block (key e / (D / VEC), columns
+// from (e % (D / VEC)) * VEC); keys past the sequence's end read as zeros.
+constexpr int kBlkVec = 8;  // bs * D / VEC <= 1024 vectors per block
+struct BlockRegs {
+    uint4 v[kBlkVec];
+};
+
+template <bool SPLIT>
+__device__ __forceinline__ void fetch_block(const Geo &g, const void *src, int b, int kvh, int k0, BlockRegs &R)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+    const int nv = g.D / VEC, n = g.bs * nv, nk = min(g.bs, seq_len_k(g, b) - k0);
+#pragma unroll
+    for (int i = 0; i < kBlkVec; ++i) {
+        const int e = threadIdx.x + i * kThr, key = e / nv, c = (e % nv) * VEC;
+        R.v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < n && key < nk)
+            R.v[i] = __ldg((const uint4 *)((const uint8_t *)src + (kv_off(g, b, kvh, k0 + key) + c) * In<SPLIT>::ES));
+    }
+}
+
+// the block into a [bs][Dp] tile (transposed = false) or a [Dp][64] tile
+template <bool SPLIT>
+__device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, uint32_t tile, uint32_t lo_off, int Dp,
+                                            bool transposed)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+    const int nv = g.D / VEC, n = g.bs * nv;
+#pragma unroll
+    for (int i = 0; i < kBlkVec; ++i) {
+        const int e = threadIdx.x + i * kThr, key = e / nv, c = (e % nv) * VEC;
+        if (e >= n)
+            continue;
+        if (!transposed) {
+            put_vec<SPLIT>(tile, g.bs, lo_off, key, c, R.v[i]);
+        } else {
+            float x[VEC];
+            unpack<SPLIT>(R.v[i], x);
+#pragma unroll
+            for (int z = 0; z < VEC; ++z)
+                put<SPLIT>(tile, Dp, lo_off, c + z, key, x[z]);
+        }
+    }
+}
+
+// One row of a q-shaped tensor (this thread's) in registers
+constexpr int kRowVec = 16;  // D * element bytes / 16 <= 16
+struct RowRegs {
+    uint4 v[kRowVec];
+};
+
+template <bool SPLIT>
+__device__ __forceinline__ void fetch_row(const Geo &g, const void *src, int64_t off, bool valid, RowRegs &R)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+        R.v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid && i * VEC < g.D)
+            R.v[i] = __ldg((const uint4 *)((const uint8_t *)src + (off + i * VEC) * In<SPLIT>::ES));
+    }
+}
+
+// the row into row r of a [128][Dp] tile, and (tr_tile != 0) into column r
+// of a transposed tile, rows tr_row0 + d
+template <bool SPLIT>
+__device__ __forceinline__ void store_row(const Geo &g, const RowRegs &R, uint32_t tile, uint32_t lo_off, int r,
+                                          uint32_t tr_tile, uint32_t tr_lo, int tr_row0)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+        if (i * VEC >= g.D)
+            break;
+        put_vec<SPLIT>(tile, 128, lo_off, r, i * VEC, R.v[i]);
+        if (tr_tile) {
+            float x[VEC];
+            unpack<SPLIT>(R.v[i], x);
+#pragma unroll
+            for (int z = 0; z < VEC; ++z)
+                put<SPLIT>(tr_tile, 128, tr_lo, tr_row0 + i * VEC + z, r, x[z]);
+        }
     }
 }
 
@@ -296,22 +403,27 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
     const uint32_t qs = smem_u32(q_t), ks = smem_u32(k_t), vts = smem_u32(vt_t), ps = smem_u32(p_t);
     // the row's q (zero for rows past the tile's tokens)
-    if (rvalid) {
-        const int64_t qo = q_off(g, b, kvh * G + hh, t);
-        for (int d = 0; d < g.D; ++d)
-            put<SPLIT>(qs, 128, QB, r, d, in_at<SPLIT>(p.q, qo + d));
+    {
+        RowRegs qr;
+        fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, kvh * G + hh, t) : 0, rvalid, qr);
+        store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
     }
     const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, false);
     float sc[64];
     bool ok = true;
     // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
     float m = -INFINITY, l = 0.f;
+    BlockRegs kr, vr;  // the next block's K (and V), fetched while the MMAs run
+    if (U > 0)
+        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
     for (int i = 0; i < U && ok; ++i) {
         const int j = list[i], k0 = j * bs;
-        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
+        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
         to_mma();
         if (r == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        if (i + 1 < U)
+            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
         if (!(ok = commit_wait(sy)))
             break;
         ld_cols(tmem, TM_S, sc, bs);
@@ -327,13 +439,21 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     }
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
     // pass 2: P = exp2(scale_l2 s - lse2) on the row's keys, O += P V
+    if (U > 0 && ok) {
+        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
+        fetch_block<SPLIT>(g, p.v, b, kvh, list[0] * bs, vr);
+    }
     for (int i = 0; i < U && ok; ++i) {
         const int j = list[i], k0 = j * bs;
-        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
-        load_block<SPLIT>(g, p.v, vts, VB, Dp, b, kvh, k0, true);
+        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
+        store_block<SPLIT>(g, vr, vts, VB, Dp, true);
         to_mma();
         if (r == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        if (i + 1 < U) {
+            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
+            fetch_block<SPLIT>(g, p.v, b, kvh, list[i + 1] * bs, vr);
+        }
         if (!(ok = commit_wait(sy)))
             break;
         ld_cols(tmem, TM_S, sc, bs);
@@ -402,28 +522,40 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     const uint32_t qs = smem_u32(q_t), dos = smem_u32(do_t), ks = smem_u32(k_t), vs = smem_u32(v_t);
     const uint32_t kts = smem_u32(kt_t), dss = smem_u32(ds_t);
     float l2 = -INFINITY, dl = 0.f;
-    if (rvalid) {
+    {
         const int h = kvh * G + hh;
-        const int64_t qo = q_off(g, b, h, t), oo = o_off(g, b, h, t), so = stat_off(g, b, h, t);
-        for (int d = 0; d < g.D; ++d) {
-            put<SPLIT>(qs, 128, QB, r, d, in_at<SPLIT>(p.q, qo + d));
-            put<SPLIT>(dos, 128, QB, r, d, in_at<SPLIT>(p.dO, oo + d));
+        RowRegs rr;
+        fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
+        store_row<SPLIT>(g, rr, qs, QB, r, 0, 0, 0);
+        fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
+        store_row<SPLIT>(g, rr, dos, QB, r, 0, 0, 0);
+        if (rvalid) {
+            const int64_t so = stat_off(g, b, h, t);
+            l2 = p.lse[so] * 1.4426950408889634f;
+            dl = p.delta[so];
         }
-        l2 = p.lse[so] * 1.4426950408889634f;
-        dl = p.delta[so];
     }
     const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, false);
     float sc[64], dp[64];
     bool ok = true;
+    BlockRegs kr, vr;  // the next block's K and V, fetched while the MMAs run
+    if (U > 0) {
+        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
+        fetch_block<SPLIT>(g, p.v, b, kvh, list[0] * bs, vr);
+    }
     for (int i = 0; i < U && ok; ++i) {
         const int j = list[i], k0 = j * bs;
-        load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
-        load_block<SPLIT>(g, p.v, vs, KB, Dp, b, kvh, k0, false);
-        load_block<SPLIT>(g, p.k, kts, TB, Dp, b, kvh, k0, true);
+        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
+        store_block<SPLIT>(g, vr, vs, KB, Dp, false);
+        store_block<SPLIT>(g, kr, kts, TB, Dp, true);
         to_mma();
         if (r == 0) {
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
+        }
+        if (i + 1 < U) {
+            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
+            fetch_block<SPLIT>(g, p.v, b, kvh, list[i + 1] * bs, vr);
         }
         if (!(ok = commit_wait(sy)))
             break;
@@ -498,8 +630,13 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     __syncthreads();
     const uint32_t ks = smem_u32(k_t), vs = smem_u32(v_t), qs = smem_u32(q_t), dos = smem_u32(do_t);
     const uint32_t as_ = smem_u32(a_t), a2s = smem_u32(a2_t), bs_ = smem_u32(b_t), b2s = smem_u32(b2_t);
-    load_block<SPLIT>(g, p.k, ks, KB, Dp, b, kvh, k0, false);
-    load_block<SPLIT>(g, p.v, vs, KB, Dp, b, kvh, k0, false);
+    {
+        BlockRegs kr;
+        fetch_block<SPLIT>(g, p.k, b, kvh, k0, kr);
+        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
+        fetch_block<SPLIT>(g, p.v, b, kvh, k0, kr);
+        store_block<SPLIT>(g, kr, vs, KB, Dp, false);
+    }
     int tl, hh;
     qrow(G, r, tl, hh);
     const int csr0 = g.dense ? dense_first(g, b, j) + u.begin : p.offsets[u.bg * g.nbmax + j] + u.begin;
@@ -516,20 +653,11 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
         float l2 = 0.f, dl = 0.f;
         // the row's q and dO, plain and transposed (zeros for rows past the list)
         {
-            const int64_t qo = rvalid ? q_off(g, b, h, t) : 0, oo = rvalid ? o_off(g, b, h, t) : 0;
-            for (int d = 0; d < g.D; ++d) {
-                const float xq = rvalid ? in_at<SPLIT>(p.q, qo + d) : 0.f;
-                const float xo = rvalid ? in_at<SPLIT>(p.dO, oo + d) : 0.f;
-                put<SPLIT>(qs, 128, QB, r, d, xq);
-                put<SPLIT>(dos, 128, QB, r, d, xo);
-                if (stacked) {
-                    put<SPLIT>(as_, 128, ALO, d, r, xo);
-                    put<SPLIT>(as_, 128, ALO, 64 + d, r, xq);
-                } else {
-                    put<SPLIT>(as_, 128, ALO, d, r, xo);
-                    put<SPLIT>(a2s, 128, ALO, d, r, xq);
-                }
-            }
+            RowRegs rr;
+            fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
+            store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
+            fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
+            store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
             if (rvalid) {
                 const int64_t so = stat_off(g, b, h, t);
                 l2 = p.lse[so] * 1.4426950408889634f;
