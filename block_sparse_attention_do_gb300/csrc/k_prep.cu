@@ -70,22 +70,14 @@ __device__ __forceinline__ void do_dot_rows(const Geo &g, const T *__restrict__ 
     }
 }
 
-// dense o/dO (row r at r * D) take the branch-free loop, whose loads all stay in flight
-template <typename T>
-__device__ __forceinline__ void do_dot_body(const Geo &g, const T *__restrict__ o, const T *__restrict__ dO,
-                                            float *__restrict__ out, int64_t nrows, int D, int blk, int nblk)
-{
-    if (g.o_lin)
-        do_dot_rows<T, true>(g, o, dO, out, nrows, D, blk, nblk);
-    else
-        do_dot_rows<T, false>(g, o, dO, out, nrows, D, blk, nblk);
-}
-
-template <typename T>
+// LIN: dense o/dO (row r at r * D), chosen on the host so that each kernel
+// holds one addressing scheme (the strided one's divisions would raise the
+// dense kernel's register count and cut the loads it keeps in flight)
+template <typename T, bool LIN>
 __global__ void __launch_bounds__(kThreads) do_dot_kernel(Geo g, const T *__restrict__ o, const T *__restrict__ dO,
                                                           float *__restrict__ out, int64_t nrows, int D)
 {
-    do_dot_body<T>(g, o, dO, out, nrows, D, blockIdx.x, gridDim.x);
+    do_dot_rows<T, LIN>(g, o, dO, out, nrows, D, blockIdx.x, gridDim.x);
 }
 
 // decode a linear index-row number into (b, kvh, t)
@@ -548,7 +540,7 @@ __global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const 
 // The chunk count and delta = rowsum(dO * O) in one launch: they are
 // independent, the first latency-bound and the second bandwidth-bound, so
 // the count's blocks (the first count_blocks) run under the dot's.
-template <typename T>
+template <typename T, bool LIN>
 __global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const int *__restrict__ idx,
                                                                    int *__restrict__ chunk_counts, int nchunks,
                                                                    int *err, int count_blocks, const T *__restrict__ o,
@@ -558,7 +550,7 @@ __global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const 
     if ((int)blockIdx.x < count_blocks)
         chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, count_blocks);
     else
-        do_dot_body<T>(g, o, dO, out, nrows, g.D, blockIdx.x - count_blocks, gridDim.x - count_blocks);
+        do_dot_rows<T, LIN>(g, o, dO, out, nrows, g.D, blockIdx.x - count_blocks, gridDim.x - count_blocks);
 }
 
 // one warp per (bg, j): exclusive prefix over chunks, list length in counts
@@ -701,12 +693,20 @@ cudaError_t launch_do_dot(const Geo &g, const void *o, const void *dO, float *de
     const int elems = dtype == NSA_DTYPE_BF16 ? 8 : 4;
     const int rpw = 32 / (g.D / elems);
     const int grid = grid_for(nrows, (kThreads / 32) * kDotU * rpw);
-    if (dtype == NSA_DTYPE_BF16)
-        do_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-            g, (const __nv_bfloat16 *)o, (const __nv_bfloat16 *)dO, delta, nrows, g.D);
-    else
-        do_dot_kernel<float><<<grid, kThreads, 0, st>>>(g, (const float *)o, (const float *)dO, delta,
-                                                        nrows, g.D);
+    using B16 = __nv_bfloat16;
+    if (dtype == NSA_DTYPE_BF16) {
+        if (g.o_lin)
+            do_dot_kernel<B16, true><<<grid, kThreads, 0, st>>>(g, (const B16 *)o, (const B16 *)dO, delta, nrows, g.D);
+        else
+            do_dot_kernel<B16, false><<<grid, kThreads, 0, st>>>(g, (const B16 *)o, (const B16 *)dO, delta, nrows, g.D);
+    } else {
+        if (g.o_lin)
+            do_dot_kernel<float, true><<<grid, kThreads, 0, st>>>(g, (const float *)o, (const float *)dO, delta, nrows,
+                                                                  g.D);
+        else
+            do_dot_kernel<float, false><<<grid, kThreads, 0, st>>>(g, (const float *)o, (const float *)dO, delta,
+                                                                   nrows, g.D);
+    }
     return cudaGetLastError();
 }
 
@@ -754,14 +754,21 @@ cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_coun
         const int elems = dot->dtype == NSA_DTYPE_BF16 ? 8 : 4;
         const int rpw = 32 / (g.D / elems);
         const int grid = cblocks + grid_for(nrows, (kThreads / 32) * kDotU * rpw);
-        if (dot->dtype == NSA_DTYPE_BF16)
-            chunk_count_dot_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-                g, idx, chunk_counts, nchunks, err, cblocks, (const __nv_bfloat16 *)dot->o,
-                (const __nv_bfloat16 *)dot->dO, dot->delta, nrows);
-        else
-            chunk_count_dot_kernel<float><<<grid, kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err, cblocks,
-                                                                     (const float *)dot->o, (const float *)dot->dO,
-                                                                     dot->delta, nrows);
+        using B16 = __nv_bfloat16;
+        auto go = [&](auto kernel, const auto *o, const auto *dO) {
+            kernel<<<grid, kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err, cblocks, o, dO, dot->delta, nrows);
+        };
+        if (dot->dtype == NSA_DTYPE_BF16) {
+            if (g.o_lin)
+                go(chunk_count_dot_kernel<B16, true>, (const B16 *)dot->o, (const B16 *)dot->dO);
+            else
+                go(chunk_count_dot_kernel<B16, false>, (const B16 *)dot->o, (const B16 *)dot->dO);
+        } else {
+            if (g.o_lin)
+                go(chunk_count_dot_kernel<float, true>, (const float *)dot->o, (const float *)dot->dO);
+            else
+                go(chunk_count_dot_kernel<float, false>, (const float *)dot->o, (const float *)dot->dO);
+        }
     } else {
         csr_chunk_count_kernel<<<cblocks, kThreads, 0, st>>>(g, idx, chunk_counts, nchunks, err);
     }

@@ -513,17 +513,24 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         int p_ui = unit_of(0, n_units);
         int ptok = -1;
         float plse = 0.f, pdlt = 0.f;
+        // The next tile's unit (its kv group and token count) stays in
+        // registers, read again only when the unit changes: reading it for
+        // every tile put a global load's latency on every tile's path.
+        int nu_bg = 0, nu_cnt = 0;
+        if (p_ui >= 0) {
+            nu_bg = p.units[p_ui].bg;
+            nu_cnt = p.units[p_ui].count;
+        }
         auto prefetch = [&]() -> bool {
             if (p_ui < 0)
                 return true;
-            const Unit nu = p.units[p_ui];
             if (!mbar_wait_warp(&bars[B_IDX0 + pq], pph, abort_flag))
                 return false;
             ptok = r < nrows ? tok_s[pq * kRows + my_tl] : -1;
             plse = 0.f;
             pdlt = 0.f;
             if (ptok >= 0) {
-                const int64_t so = stat_off(g, nu.bg / g.Hkv, (nu.bg % g.Hkv) * G + my_hh, ptok);
+                const int64_t so = stat_off(g, nu_bg / g.Hkv, (nu_bg % g.Hkv) * G + my_hh, ptok);
                 plse = p.lse[so];
                 pdlt = p.delta[so];
             }
@@ -531,9 +538,13 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 pq = 0;
                 pph ^= 1;
             }
-            if (++pti == (nu.count + Tt - 1) / Tt) {
+            if (++pti == (nu_cnt + Tt - 1) / Tt) {
                 pti = 0;
                 p_ui = unit_of(++pu, n_units);
+                if (p_ui >= 0) {
+                    nu_bg = p.units[p_ui].bg;
+                    nu_cnt = p.units[p_ui].count;
+                }
             }
             return true;
         };
