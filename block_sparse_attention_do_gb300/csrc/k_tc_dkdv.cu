@@ -15,8 +15,8 @@
 // Roles (11 warps):  warps 0 and 3 load (TMA for K_j/V_j; Q rows from warp 0
 // and dO rows from warp 3 by one TMA box per token -- its G heads, both
 // halves -- when G % 8 == 0; else by 16-byte cp.async, two whole rows per
-// warp instruction with the swizzle applied by hand, each tile released once
-// the next tile's copies are out); warp 1 resolves each tile's token ids a tile
+// warp instruction with the swizzle applied by hand, each lane's copies
+// arriving on the tile's barrier as they land); warp 1 resolves each tile's token ids a tile
 // ahead; warp 2 owns TMEM; one thread each of warps 2, 8, 9 and 10 issues the
 // S, dP, dV^T and dK^T MMAs; warps 4-7 compute P/dS for one row each (reading
 // the row's LSE and delta themselves) and run the epilogue.  Q has three
@@ -97,7 +97,8 @@ __device__ __forceinline__ int unit_of(int k, int n_units)
 // entries' units hold consecutive tokens; G % 8 != 0), or 16-byte cp.async
 // (selection, G % 8 != 0).  ROWS and CPASYNC fill the row-group layout
 // (rg_off); TILE fills one 64-column half after the other (rows head-major
-// for BHTD, token-major for THD).
+// for BHTD, token-major for THD).  (Token boxes for one tensor and cp.async
+// for the other measured three times slower than token boxes for both.)
 enum { LOAD_ROWS = 0, LOAD_TILE = 1, LOAD_CPASYNC = 2 };
 
 template <int MODE>
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         // issue, so two warps halve the time to the tile's last one); else
         // both by 16-byte cp.async from warp 0 with the swizzle applied by hand.
         const int tensor = warp == 3 ? 1 : 0;
+        constexpr bool cpa = MODE == LOAD_CPASYNC;
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -194,7 +196,6 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         }
         int it = 0, uc = 0, qs = 0, qph = 0;  // tile count; its Q stage and that stage's phase
         int last_tile = -1, last_kv = -1;     // newest TMA batches (for the abort path)
-        uint64_t *pend = nullptr;             // cp.async gather: the tile whose release is still due
         // cp.async gather: the swizzled destination of this lane's chunk in row
         // 2u + (lane >> 4) of an 8-row group, and ceil(2^16 / G) for r / G
         uint32_t dsto[4];
@@ -204,23 +205,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             dsto[u] = (c >> 3) * kRgHalf + rr * 128 + (((c & 7) ^ rr) << 4);
         }
         const int recipG = (65536 + G - 1) / G;
-        // releases the pending cp.async tile (all of this lane's copies landed)
-        auto flush = [&]() {
-            if (MODE == LOAD_CPASYNC && pend) {
-                cp_async_wait<0>();
-                fence_async_smem();
-                mbar_arrive(pend);
-                pend = nullptr;
-            }
-        };
         bool okl = true;
         for (int ui; (ui = unit_of(uc, n_units)) >= 0 && okl; ++uc) {
             const Unit u = p.units[ui];
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int ntiles = (u.count + Tt - 1) / Tt;
-            // the K/V stage frees once the previous unit's last S and dP have
-            // run, which needs that unit's last tile released first
-            flush();
+            // the K/V stage frees once the previous unit's last S and dP have run
             if (tensor == 0 && !mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
                 okl = false;
                 break;
@@ -267,7 +257,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                         else
                             tma_load_4d(dst, map, full, h * 64, t0, kvh * G, b);
                     }
-                } else if (MODE == LOAD_ROWS) {
+                } else if (!cpa) {
                     uint64_t *full = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
                     if (lane == 0) {
                         last_tile = it;
@@ -311,16 +301,10 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             cp_async_16(tile_s + grp * kRgStride + dsto[u], src, valid ? 16u : 0u);
                         }
                     }
-                    cp_async_commit();
-                    // the previous tile's rows have landed once only this
-                    // tile's group is outstanding: make them visible to the
-                    // tensor cores (async proxy), then release that tile
-                    if (pend) {
-                        cp_async_wait<1>();
-                        fence_async_smem();
-                        mbar_arrive(pend);
-                    }
-                    pend = tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs];
+                    // the tile's barrier takes this lane's arrival once its
+                    // copies have landed; the consumers fence them for the
+                    // tensor cores after their wait
+                    cp_async_mbar_arrive(tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs]);
                 }
                 if (++qs == NQ) {
                     qs = 0;
@@ -328,10 +312,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                 }
             }
         }
-        if (okl && !*abort_flag)
-            flush();
-        if (MODE == LOAD_CPASYNC)
-            cp_async_wait<0>();
+        if (cpa)
+            cp_async_wait<0>();  // every copy lands before the CTA may exit
         if (*abort_flag && lane == 0) {
             // let TMA copies still in flight land before the CTA exits
             volatile int never[2] = {0, abort_flag[1]};  // own limit, no abort
@@ -443,6 +425,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             break;
                         }
                         tc_fence_after();
+                        if (MODE == LOAD_CPASYNC)  // rows written by cp.async: order them for the tensor cores
+                            fence_async_smem();
                         const uint32_t col = tmem + TM_S + tb * 128 + role * 64;
                         for (int kk = 0; kk < kHead / 16; ++kk) {
                             const uint32_t ao = (kk >> 2) * qhalf + (kk & 3) * 32;
@@ -467,6 +451,8 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             break;
                         }
                         tc_fence_after();
+                        if (MODE == LOAD_CPASYNC)  // dO (dV^T) or Q (dK^T) written by cp.async
+                            fence_async_smem();
                         const uint32_t col = tmem + (role == 2 ? TM_DV : TM_DK);
                         const uint32_t pb = (role == 2 ? p_s : ds_s) + pbuf * (kRows * 128);
                         for (int kr = 0; kr < kRows / 16; ++kr)

@@ -152,6 +152,15 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// An arrive on bar once every cp.async this thread has issued so far has
+// landed (the barrier's count must include it: no pending-count increment).
+// A consumer then orders the rows for the tensor cores with fence_async_smem
+// after its wait.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <int N> __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
