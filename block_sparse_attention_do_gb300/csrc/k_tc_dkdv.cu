@@ -101,8 +101,15 @@ __device__ __forceinline__ int unit_of(int k, int n_units)
 // for the other measured three times slower than token boxes for both.)
 enum { LOAD_ROWS = 0, LOAD_TILE = 1, LOAD_CPASYNC = 2 };
 
+// Warps: 11, plus a third gather warp (warp 11) in the cp.async mode: one
+// warp's cp.async gather of a 32 KB tile takes ~6,300 cycles (about 100 cycles
+// per warp instruction), so three warps share both tensors' rows.  12 warps at
+// 168 registers still fit (3 warps per SM sub-partition).
+template <int MODE> constexpr int dkdv_threads() { return MODE == LOAD_CPASYNC ? 384 : 352; }
+constexpr int kGatherWarps = 3;  // warps 0, 3 and 11 in the cp.async mode
+
 template <int MODE>
-__global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_do,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v,
@@ -125,12 +132,12 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
         abort_flag[0] = 0;
         abort_flag[1] = p.wait_us;  // the wait limit (0: the default)
         for (int x = 0; x < NQ; ++x) {
-            mbar_init(&bars[B_QFULL0 + x], MODE == LOAD_CPASYNC ? 32 : 1);
+            mbar_init(&bars[B_QFULL0 + x], MODE == LOAD_CPASYNC ? 32 * kGatherWarps : 1);
             mbar_init(&bars[B_QEMPTY0 + x], 1);  // dK^T's commit
             mbar_init(&bars[B_IDX0 + x], 32);
         }
         for (int x = 0; x < NDO; ++x) {
-            mbar_init(&bars[B_DOFULL0 + x], MODE == LOAD_CPASYNC ? 32 : 1);
+            mbar_init(&bars[B_DOFULL0 + x], MODE == LOAD_CPASYNC ? 32 * kGatherWarps : 1);
             mbar_init(&bars[B_DOEMPTY0 + x], 2);  // dP's and dV^T's commits
         }
         mbar_init(&bars[B_KVFULL], 1);
@@ -176,16 +183,18 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
     // this kernel writes: let it take each SM as this kernel's CTA there ends.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0 || warp == 3) {
+    if (warp == 0 || warp == 3 || (MODE == LOAD_CPASYNC && warp == 11)) {
         // ------------------------------------------------------- tile loader
         // K_j / V_j once per unit (warp 0); per tile, once the indexer has
         // published the tile's tokens (it does so when the tile's Q stage is
         // free), the Q and dO rows: by TMA when G % 8 == 0, one box per token
         // (its G heads, both halves), warp 0 the Q boxes and warp 3 the dO
         // boxes once the tile's dO stage is free (a box takes ~85 cycles to
-        // issue, so two warps halve the time to the tile's last one); else
-        // both by 16-byte cp.async from warp 0 with the swizzle applied by hand.
+        // issue, so two warps halve the time to the tile's last one); else by
+        // 16-byte cp.async with the swizzle applied by hand, warps 0, 3 and
+        // 11 each taking every third 8-row group of Q and then of dO.
         const int tensor = warp == 3 ? 1 : 0;
+        const int gw = warp == 0 ? 0 : warp == 3 ? 1 : 2;  // cp.async: this warp's share of the row groups
         constexpr bool cpa = MODE == LOAD_CPASYNC;
         const uint32_t q_s = smem_u32(sm + OFF_Q), do_s = smem_u32(sm + OFF_DO);
         if (lane == 0) {
@@ -211,11 +220,11 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv;
             const int ntiles = (u.count + Tt - 1) / Tt;
             // the K/V stage frees once the previous unit's last S and dP have run
-            if (tensor == 0 && !mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
+            if (warp == 0 && !mbar_wait_warp(&bars[B_KVEMPTY], (uc & 1) ^ 1, abort_flag)) {
                 okl = false;
                 break;
             }
-            if (tensor == 0 && lane == 0) {
+            if (warp == 0 && lane == 0) {
                 last_kv = uc;
                 mbar_arrive_expect_tx(&bars[B_KVFULL], 2 * kKvBytes);
                 for (int h = 0; h < 2; ++h) {
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             for (int ti = 0; ti < ntiles; ++ti, ++it) {
                 const int ds = it & 1;  // dO stage
                 if (!mbar_wait_warp(&bars[B_IDX0 + qs], qph, abort_flag) ||
-                    (tensor == 1 && !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag))) {
+                    (!cpa && tensor == 1 && !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag))) {
                     okl = false;
                     break;
                 }
@@ -277,34 +286,41 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
                             tma_load_5d(dst, map, full, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t);
                     }
                 } else {
-                    // this warp's tensor: 128 rows x 16 chunks of 16 bytes, two
-                    // whole rows (256 contiguous bytes each) per warp
-                    // instruction; rows past the tile's tokens are zero-filled.
-                    // Each lane's arrival lands once its copies have.
-                    const __nv_bfloat16 *base = tensor ? p.dO : p.q;
-                    const Strides &str = tensor ? g.so : g.sq;
-                    const uint32_t tile_s = tensor ? do_s + ds * kTileBytes : q_s + qs * kTileBytes;
-                    // lane: chunk c of rows 8*grp + 2u + hi; its head 0 of the
-                    // group and its column, then per row token * stride_t + head * stride_h
+                    // cp.async: Q, then (once the tile's dO stage is free) dO; per
+                    // tensor 128 rows x 16 chunks of 16 bytes, two whole rows
+                    // (256 contiguous bytes each) per warp instruction, this warp
+                    // taking 8-row groups gw, gw + 3, ...; rows past the tile's
+                    // tokens are zero-filled.  Each lane's arrival on the
+                    // tile's barrier lands once its copies have; the consumers
+                    // fence them for the tensor cores after their wait.
                     const int c = lane & 15, hi = lane >> 4;
-                    const __nv_bfloat16 *rowbase =
-                        base + (int64_t)(kvh * G) * str.h + c * 8 + (g.thd ? (int64_t)g.cu[b] * str.t : (int64_t)b * str.b);
-#pragma unroll 2
-                    for (int grp = 0; grp < kRows / 8; ++grp) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int r = grp * 8 + 2 * u + hi;
-                            const int tl = (r * recipG) >> 16, hh = r - tl * G;  // r / G, r % G (r < 128)
-                            const bool valid = r < nrows && tl < ntok;
-                            const __nv_bfloat16 *src =
-                                valid ? rowbase + (int64_t)tok[tl] * str.t + (int64_t)hh * str.h : base;
-                            cp_async_16(tile_s + grp * kRgStride + dsto[u], src, valid ? 16u : 0u);
+                    for (int tn = 0; tn < 2; ++tn) {
+                        if (tn == 1 && !mbar_wait_warp(&bars[B_DOEMPTY0 + ds], ((it >> 1) & 1) ^ 1, abort_flag)) {
+                            okl = false;
+                            break;
                         }
+                        const __nv_bfloat16 *base = tn ? p.dO : p.q;
+                        const Strides &str = tn ? g.so : g.sq;
+                        const uint32_t tile_s = tn ? do_s + ds * kTileBytes : q_s + qs * kTileBytes;
+                        // lane: chunk c of rows 8*grp + 2u + hi; its head 0 of the
+                        // group and its column, then per row token * stride_t + head * stride_h
+                        const __nv_bfloat16 *rowbase = base + (int64_t)(kvh * G) * str.h + c * 8 +
+                                                       (g.thd ? (int64_t)g.cu[b] * str.t : (int64_t)b * str.b);
+                        for (int grp = gw; grp < kRows / 8; grp += kGatherWarps) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int r = grp * 8 + 2 * u + hi;
+                                const int tl = (r * recipG) >> 16, hh = r - tl * G;  // r / G, r % G (r < 128)
+                                const bool valid = r < nrows && tl < ntok;
+                                const __nv_bfloat16 *src =
+                                    valid ? rowbase + (int64_t)tok[tl] * str.t + (int64_t)hh * str.h : base;
+                                cp_async_16(tile_s + grp * kRgStride + dsto[u], src, valid ? 16u : 0u);
+                            }
+                        }
+                        cp_async_mbar_arrive(tn ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs]);
                     }
-                    // the tile's barrier takes this lane's arrival once its
-                    // copies have landed; the consumers fence them for the
-                    // tensor cores after their wait
-                    cp_async_mbar_arrive(tensor ? &bars[B_DOFULL0 + ds] : &bars[B_QFULL0 + qs]);
+                    if (!okl)
+                        break;
                 }
                 if (++qs == NQ) {
                     qs = 0;
@@ -383,7 +399,7 @@ __global__ void __launch_bounds__(352, 1) dkdv_tc_kernel(const __grid_constant__
             if (ui >= 0)
                 fetch();
         }
-    } else if (warp == 2 || warp >= 8) {
+    } else if (warp == 2 || (warp >= 8 && warp <= 10)) {
         // -------------------------------------------------------------- MMA
         // Four issuing threads in four warps (one thread issues a tcgen05 MMA
         // only every ~150 cycles): warp 2 issues S, warp 8 dP, warp 9 dV^T (as
@@ -753,15 +769,15 @@ cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const voi
     if (grid < 1)
         grid = 1;
     // a programmatic dependent of the kernel before it (see the kernel's wait)
-    auto go = [&](auto kernel) {
+    auto go = [&](auto kernel, int threads) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        return launch_dependent(kernel, dim3(grid), dim3(352), SMEM_BYTES, st, tq, tdo, tk, tv, p);
+        return launch_dependent(kernel, dim3(grid), dim3(threads), SMEM_BYTES, st, tq, tdo, tk, tv, p);
     };
     if (mode == LOAD_ROWS)
-        return go(dkdv_tc_kernel<LOAD_ROWS>);
+        return go(dkdv_tc_kernel<LOAD_ROWS>, dkdv_threads<LOAD_ROWS>());
     if (mode == LOAD_TILE)
-        return go(dkdv_tc_kernel<LOAD_TILE>);
-    return go(dkdv_tc_kernel<LOAD_CPASYNC>);
+        return go(dkdv_tc_kernel<LOAD_TILE>, dkdv_threads<LOAD_TILE>());
+    return go(dkdv_tc_kernel<LOAD_CPASYNC>, dkdv_threads<LOAD_CPASYNC>());
 }
 
 }  // namespace nsa
