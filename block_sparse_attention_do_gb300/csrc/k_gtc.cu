@@ -725,8 +725,8 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
                 const float x = sc[c] * mul;
                 if (direct)
                     out_at<SPLIT>(which == 1 ? p.dk : p.dv, dkv_off(g, b, kvh, k0 + c) + d, x);
-                else
-                    p.partials[((int64_t)u.slot * 2 + which) * bs * g.D + c * g.D + d] = x;
+                else  // a split block's partial: dK first, then dV (the reduction's order)
+                    p.partials[((int64_t)u.slot * 2 + (which == 1 ? 0 : 1)) * bs * g.D + c * g.D + d] = x;
             }
         }
     }

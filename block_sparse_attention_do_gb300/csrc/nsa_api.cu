@@ -148,8 +148,10 @@ PlanLayout plan_layout(const Geo &g)
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
     // tokens per dK/dV unit: 128 row tiles of the tensor-core kernel (longer
     // units mean fewer accumulator drains and split-block partials; the dQ
-    // kernel launched behind dK/dV takes the SMs its uneven end leaves)
-    w.chunk = tiles_tokens(g) * 128;
+    // kernel launched behind dK/dV takes the SMs its uneven end leaves); 4 row
+    // tiles for the other shapes' kernel, whose CTA walks its unit's tiles one
+    // after another (the longest unit sets its time)
+    w.chunk = tiles_tokens(g) * (g.D == 128 && g.bs == 64 ? 128 : 4);
     // upper bound on list entries; dense: a row of sequence-local token t
     // attends t/bs + 1 <= nbmax/2 + 1 blocks on average over a sequence, or
     // with keys of their own lengths (a short query run at the end of long
