@@ -103,6 +103,32 @@ __device__ __forceinline__ void put(uint32_t tile, int R, uint32_t lo_off, int r
         st_u16(a + lo_off, p.lo);
 }
 
+// descriptor of K-step kk (16 rows) of such a tile read as an MN-major
+// operand: its rows are the K index and its columns the N index (64-column
+// chunks R * 128 bytes apart)
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int R, int kk)
+{
+    return sdesc_sw128(tile + kk * 2048, R * 128, 1024);
+}
+
+// writes elements (r, c .. c+7) of a tile (c a multiple of 8: one 16-byte
+// chunk), and of its low-part copy lo_off bytes on
+template <bool SPLIT>
+__device__ __forceinline__ void put8(uint32_t tile, int R, uint32_t lo_off, int r, int c, const float *x)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const Parts<SPLIT> p0 = split_of<SPLIT>(x[2 * i]), p1 = split_of<SPLIT>(x[2 * i + 1]);
+        h[i] = (uint32_t)p0.hi | ((uint32_t)p1.hi << 16);
+        l[i] = (uint32_t)p0.lo | ((uint32_t)p1.lo << 16);
+    }
+    const uint32_t a = tile + swz(r, c, R);
+    st_shared_v4(a, h[0], h[1], h[2], h[3]);
+    if (SPLIT)
+        st_shared_v4(a + lo_off, l[0], l[1], l[2], l[3]);
+}
+
 // D (+)= A B^T over nk K-steps; SPLIT: three products of the parts.  A and B
 // are K-major tiles (A with Ra rows, B with Rb rows) whose low parts sit
 // alo / blo bytes after them.
@@ -116,6 +142,22 @@ __device__ __forceinline__ void product(uint32_t d, uint32_t a, int Ra, uint32_t
         if (SPLIT) {
             mma_bf16(d, kdesc(a, Ra, kk), kdesc(b + blo, Rb, kk), idesc, 1u);
             mma_bf16(d, kdesc(a + alo, Ra, kk), kdesc(b, Rb, kk), idesc, 1u);
+        }
+    }
+}
+
+// D (+)= A B over nk K-steps, B MN-major: a K-major tile of Rb rows (the K
+// index) read by columns (the N index), as mndesc; otherwise as product
+template <bool SPLIT>
+__device__ __forceinline__ void product_bmn(uint32_t d, uint32_t a, int Ra, uint32_t alo, uint32_t b, int Rb,
+                                            uint32_t blo, uint32_t idesc, int nk, bool acc)
+{
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint32_t on = (acc || kk > 0) ? 1u : 0u;
+        mma_bf16(d, kdesc(a, Ra, kk), mndesc(b, Rb, kk), idesc, on);
+        if (SPLIT) {
+            mma_bf16(d, kdesc(a, Ra, kk), mndesc(b + blo, Rb, kk), idesc, 1u);
+            mma_bf16(d, kdesc(a + alo, Ra, kk), mndesc(b, Rb, kk), idesc, 1u);
         }
     }
 }
@@ -377,10 +419,11 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     const Geo &g = p.g;
     const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
-    // plan: Q [128][Dp] | K [bs][Dp] | V^T [Dp][64] | P [128][64] (each with its
-    // low part right after it) | union buffer | barrier, wait context, TMEM slot
-    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, VB = Dp * kKeyPad * 2, PB = 128 * kKeyPad * 2;
-    uint8_t *q_t = sm, *k_t = q_t + parts * QB, *vt_t = k_t + parts * KB, *p_t = vt_t + parts * VB;
+    // plan: Q [128][Dp] | K [bs][Dp] | V [bs][Dp] (read MN-major by P V) |
+    // P [128][64] (each with its low part right after it) | union buffer |
+    // barrier, wait context, TMEM slot
+    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, VB = KB, PB = 128 * kKeyPad * 2;
+    uint8_t *q_t = sm, *k_t = q_t + parts * QB, *v_t = k_t + parts * KB, *p_t = v_t + parts * VB;
     int *ubuf = (int *)(p_t + parts * PB);
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
     Sync sy;
@@ -401,14 +444,14 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     const int cdiag = rvalid ? kdiag(g, b, t) : -1;
     const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
     const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
-    const uint32_t qs = smem_u32(q_t), ks = smem_u32(k_t), vts = smem_u32(vt_t), ps = smem_u32(p_t);
+    const uint32_t qs = smem_u32(q_t), ks = smem_u32(k_t), vs = smem_u32(v_t), ps = smem_u32(p_t);
     // the row's q (zero for rows past the tile's tokens)
     {
         RowRegs qr;
         fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, kvh * G + hh, t) : 0, rvalid, qr);
         store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
     }
-    const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, false);
+    const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, true);
     float sc[64];
     bool ok = true;
     // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
@@ -432,7 +475,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
             const int key = k0 + c;
             if (sel && key >= klo && key <= khi) {
                 const float x = sc[c] * g.scale_l2, mn = fmaxf(m, x);
-                l = l * exp2f(m - mn) + exp2f(x - mn);
+                l = l * ex2(m - mn) + ex2(x - mn);
                 m = mn;
             }
         }
@@ -446,7 +489,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     for (int i = 0; i < U && ok; ++i) {
         const int j = list[i], k0 = j * bs;
         store_block<SPLIT>(g, kr, ks, KB, Dp, false);
-        store_block<SPLIT>(g, vr, vts, VB, Dp, true);
+        store_block<SPLIT>(g, vr, vs, VB, Dp, false);
         to_mma();
         if (r == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
@@ -458,14 +501,18 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
             break;
         ld_cols(tmem, TM_S, sc, bs);
         const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j) && lse2 != -INFINITY;
-        for (int c = 0; c < bs; ++c) {
-            const int key = k0 + c;
-            const float pv = (sel && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - lse2) : 0.f;
-            put<SPLIT>(ps, 128, PB, r, c, pv);
+        for (int c0 = 0; c0 < bs; c0 += 8) {
+            float pv[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const int c = c0 + x, key = k0 + c;
+                pv[x] = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - lse2) : 0.f;
+            }
+            put8<SPLIT>(ps, 128, PB, r, c0, pv);
         }
         to_mma();
-        if (r == 0)
-            product<SPLIT>(tmem + TM_ACC, ps, 128, PB, vts, Dp, VB, idO, bs / 16, i > 0);
+        if (r == 0)  // O += P V, V read MN-major from its plain tile
+            product_bmn<SPLIT>(tmem + TM_ACC, ps, 128, PB, vs, bs, VB, idO, bs / 16, i > 0);
         ok = commit_wait(sy);
     }
     // epilogue: O (already normalised) and the natural-log LSE.  Every lane
@@ -495,10 +542,11 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     const Geo &g = p.g;
     const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
-    // plan: Q, dO [128][Dp] | K, V [bs][Dp] | K^T [Dp][64] | dS [128][64] | union | misc
-    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, TB = Dp * kKeyPad * 2, PB = 128 * kKeyPad * 2;
+    // plan: Q, dO [128][Dp] | K, V [bs][Dp] (K also read MN-major by dS K) |
+    // dS [128][64] | union | misc
+    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, PB = 128 * kKeyPad * 2;
     uint8_t *q_t = sm, *do_t = q_t + parts * QB, *k_t = do_t + parts * QB, *v_t = k_t + parts * KB;
-    uint8_t *kt_t = v_t + parts * KB, *ds_t = kt_t + parts * TB;
+    uint8_t *ds_t = v_t + parts * KB;
     int *ubuf = (int *)(ds_t + parts * PB);
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
     Sync sy;
@@ -506,7 +554,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
-    zero_smem(sm, parts * (2 * QB + 2 * KB + TB + PB));
+    zero_smem(sm, parts * (2 * QB + 2 * KB + PB));
     if (warp == 0 && nvalid > 0)
         qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
     __syncthreads();
@@ -520,7 +568,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
     const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
     const uint32_t qs = smem_u32(q_t), dos = smem_u32(do_t), ks = smem_u32(k_t), vs = smem_u32(v_t);
-    const uint32_t kts = smem_u32(kt_t), dss = smem_u32(ds_t);
+    const uint32_t dss = smem_u32(ds_t);
     float l2 = -INFINITY, dl = 0.f;
     {
         const int h = kvh * G + hh;
@@ -535,7 +583,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
             dl = p.delta[so];
         }
     }
-    const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, false);
+    const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, true);
     float sc[64], dp[64];
     bool ok = true;
     BlockRegs kr, vr;  // the next block's K and V, fetched while the MMAs run
@@ -547,7 +595,6 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         const int j = list[i], k0 = j * bs;
         store_block<SPLIT>(g, kr, ks, KB, Dp, false);
         store_block<SPLIT>(g, vr, vs, KB, Dp, false);
-        store_block<SPLIT>(g, kr, kts, TB, Dp, true);
         to_mma();
         if (r == 0) {
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
@@ -562,14 +609,19 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         ld_cols(tmem, TM_S, sc, bs);
         ld_cols(tmem, TM_DP, dp, bs);
         const bool sel = rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
-        for (int c = 0; c < bs; ++c) {
-            const int key = k0 + c;
-            const float pv = (sel && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - l2) : 0.f;
-            put<SPLIT>(dss, 128, PB, r, c, pv * (dp[c] - dl));
+        for (int c0 = 0; c0 < bs; c0 += 8) {
+            float dsv[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const int c = c0 + x, key = k0 + c;
+                const float pv = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
+                dsv[x] = pv * (dp[c] - dl);
+            }
+            put8<SPLIT>(dss, 128, PB, r, c0, dsv);
         }
         to_mma();
-        if (r == 0)
-            product<SPLIT>(tmem + TM_ACC, dss, 128, PB, kts, Dp, TB, idQ, bs / 16, i > 0);
+        if (r == 0)  // dQ += dS K, K read MN-major from its plain tile
+            product_bmn<SPLIT>(tmem + TM_ACC, dss, 128, PB, ks, bs, KB, idQ, bs / 16, i > 0);
         ok = commit_wait(sy);
     }
     if (ok) {
@@ -679,7 +731,7 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
         const bool live = rvalid && l2 != -INFINITY;
         for (int c = 0; c < bs; ++c) {
             const int key = k0 + c;
-            const float pv = (live && key >= klo && key <= khi) ? exp2f(sc[c] * g.scale_l2 - l2) : 0.f;
+            const float pv = (live && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
             const float dsv = pv * (dp[c] - dl);
             if (stacked) {
                 put<SPLIT>(bs_, 2 * bs, BLO, c, r, pv);
@@ -782,7 +834,7 @@ cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const voi
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + g.bs * p.Dp * 2 + p.Dp * kKeyPad * 2 + 128 * kKeyPad * 2) +
+    const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + 128 * kKeyPad * 2) +
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
@@ -815,8 +867,7 @@ cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 +
-                        parts * (size_t)(2 * 128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + p.Dp * kKeyPad * 2 + 128 * kKeyPad * 2) +
+    const size_t smem = 1024 + parts * (size_t)(2 * 128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + 128 * kKeyPad * 2) +
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
