@@ -175,6 +175,12 @@ template <bool SPLIT> __device__ __forceinline__ void out_at(void *base, int64_t
 // context (abort flag, limit).  issue_wait: thread 0 commits every MMA it
 // issued so far to the barrier, everyone waits for it; false (on every
 // thread) once a wait gave up.
+// A second MMA-issuing thread (warp 1's lane 0): one thread issues a tcgen05
+// MMA only every ~120 cycles, so S and dP go out from two threads at once.
+// Every commit_wait takes a commit from both (a commit with nothing
+// outstanding arrives at once).
+constexpr int kIssuer2 = 32;
+
 struct Sync {
     uint64_t *bar;
     volatile int *ctx;
@@ -183,7 +189,7 @@ struct Sync {
 
 __device__ __forceinline__ bool commit_wait(Sync &s)
 {
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 || threadIdx.x == 32)  // both issuing threads (see kIssuer2)
         mma_commit(s.bar);
     bool ok = mbar_wait(s.bar, s.phase, s.ctx);
     s.phase ^= 1;
@@ -212,7 +218,7 @@ __device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Syn
     if (threadIdx.x == 0) {
         ctx[0] = 0;
         ctx[1] = p.wait_us;
-        mbar_init(bar, 1);
+        mbar_init(bar, 2);  // commits from threads 0 and kIssuer2
         fence_barrier_init();
     }
     if (threadIdx.x < 32) {
@@ -231,8 +237,9 @@ __device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Syn
 __device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p)
 {
     // MMAs still in flight (after a timeout) complete before TMEM is freed
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 || threadIdx.x == 32)
         mma_commit(s.bar);
+    if (threadIdx.x == 0) {
         volatile int never[2] = {0, s.ctx[1]};
         mbar_wait(s.bar, s.phase, never);
     }
@@ -306,10 +313,11 @@ template <bool SPLIT>
 __device__ __forceinline__ void fetch_block(const Geo &g, const void *src, int b, int kvh, int k0, BlockRegs &R)
 {
     constexpr int VEC = In<SPLIT>::VEC;
-    const int nv = g.D / VEC, n = g.bs * nv, nk = min(g.bs, seq_len_k(g, b) - k0);
+    // vectors per key row: D / VEC, a power of two (D is 32, 64 or 128)
+    const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = g.bs * nv, nk = min(g.bs, seq_len_k(g, b) - k0);
 #pragma unroll
     for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr, key = e / nv, c = (e % nv) * VEC;
+        const int e = threadIdx.x + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
         R.v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (e < n && key < nk)
             R.v[i] = __ldg((const uint4 *)((const uint8_t *)src + (kv_off(g, b, kvh, k0 + key) + c) * In<SPLIT>::ES));
@@ -322,10 +330,10 @@ __device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, ui
                                             bool transposed)
 {
     constexpr int VEC = In<SPLIT>::VEC;
-    const int nv = g.D / VEC, n = g.bs * nv;
+    const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = g.bs * nv;
 #pragma unroll
     for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr, key = e / nv, c = (e % nv) * VEC;
+        const int e = threadIdx.x + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
         if (e >= n)
             continue;
         if (!transposed) {
@@ -596,10 +604,10 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         store_block<SPLIT>(g, kr, ks, KB, Dp, false);
         store_block<SPLIT>(g, vr, vs, KB, Dp, false);
         to_mma();
-        if (r == 0) {
+        if (r == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        else if (r == kIssuer2)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
-        }
         if (i + 1 < U) {
             fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
             fetch_block<SPLIT>(g, p.v, b, kvh, list[i + 1] * bs, vr);
@@ -717,10 +725,10 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
             }
         }
         to_mma();
-        if (r == 0) {
+        if (r == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+        else if (r == kIssuer2)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
-        }
         if (!(ok = commit_wait(sy)))
             break;
         ld_cols(tmem, TM_S, sc, bs);
@@ -743,12 +751,12 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
         }
         to_mma();
         if (r == 0) {
-            if (stacked) {
+            if (stacked)
                 product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, 2 * bs, BLO, idA, 128 / 16, ti > 0);
-            } else {
+            else
                 product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, bs, BLO, idA, 128 / 16, ti > 0);
-                product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
-            }
+        } else if (r == kIssuer2 && !stacked) {
+            product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
         }
         ok = commit_wait(sy);
     }
