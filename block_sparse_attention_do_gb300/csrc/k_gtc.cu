@@ -395,18 +395,30 @@ __device__ __forceinline__ void qrow(int G, int r, int &tl, int &hh)
     hh = r % G;
 }
 
-// 16 consecutive TMEM columns of this thread's lane (row), as floats
-__device__ __forceinline__ void ld_cols(uint32_t tmem, int col, float *out, int n)
+// N consecutive TMEM columns (a multiple of 16) of this thread's lane (row)
+// as floats, from col_a into a and (NB = N) from col_b into b: every load
+// goes out before the one wait
+template <int N, int NB = 0>
+__device__ __forceinline__ void ld_cols(uint32_t tmem, int col_a, float *a, int col_b = 0, float *b = nullptr)
 {
-    const uint32_t base = tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + col;
-    for (int c0 = 0; c0 < n; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(base + c0, v);
-        tmem_wait_ld();
+    static_assert(N % 16 == 0 && (NB == 0 || NB == N), "whole 16-column loads");
+    const uint32_t base = tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16);
+    uint32_t va[N / 16][16], vb[NB ? N / 16 : 1][16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            out[c0 + i] = __uint_as_float(v[i]);
+    for (int c = 0; c < N / 16; ++c) {
+        tmem_ld16(base + col_a + c * 16, va[c]);
+        if (NB)
+            tmem_ld16(base + col_b + c * 16, vb[c]);
     }
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            a[c * 16 + i] = __uint_as_float(va[c][i]);
+            if (NB)
+                b[c * 16 + i] = __uint_as_float(vb[c][i]);
+        }
 }
 
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_ACC = 128, TM_ACC2 = 192;
@@ -419,13 +431,14 @@ __device__ __forceinline__ void zero_smem(uint8_t *p, int n)
 }
 
 // ---------------------------------------------------------------- forward
-template <bool SPLIT>
+template <bool SPLIT, int BS>
 __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
-    const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
+    constexpr int bs = BS;  // keys per block (the launch picks the instance for g.bs)
+    const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
     // plan: Q [128][Dp] | K [bs][Dp] | V [bs][Dp] (read MN-major by P V) |
     // P [128][64] (each with its low part right after it) | union buffer |
@@ -460,7 +473,6 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
         store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
     }
     const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, true);
-    float sc[64];
     bool ok = true;
     // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
     float m = -INFINITY, l = 0.f;
@@ -477,15 +489,25 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
             fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
         if (!(ok = commit_wait(sy)))
             break;
-        ld_cols(tmem, TM_S, sc, bs);
+        float sc[bs];
+        ld_cols<bs>(tmem, TM_S, sc);
         const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j);
+        // the block's maximum first, then its terms against the new maximum
+        float bm = -INFINITY;
+#pragma unroll
         for (int c = 0; c < bs; ++c) {
             const int key = k0 + c;
-            if (sel && key >= klo && key <= khi) {
-                const float x = sc[c] * g.scale_l2, mn = fmaxf(m, x);
-                l = l * ex2(m - mn) + ex2(x - mn);
-                m = mn;
-            }
+            sc[c] = (sel && key >= klo && key <= khi) ? sc[c] * g.scale_l2 : -INFINITY;
+            bm = fmaxf(bm, sc[c]);
+        }
+        if (bm != -INFINITY) {
+            const float mn = fmaxf(m, bm);
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < bs; ++c)
+                sum += ex2(sc[c] - mn);  // exp2(-inf) = 0 off the row's keys
+            l = l * ex2(m - mn) + sum;
+            m = mn;
         }
     }
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
@@ -507,8 +529,10 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
         }
         if (!(ok = commit_wait(sy)))
             break;
-        ld_cols(tmem, TM_S, sc, bs);
+        float sc[bs];
+        ld_cols<bs>(tmem, TM_S, sc);
         const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j) && lse2 != -INFINITY;
+#pragma unroll
         for (int c0 = 0; c0 < bs; c0 += 8) {
             float pv[8];
 #pragma unroll
@@ -530,10 +554,12 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
         float acc[16];
         for (int c0 = 0; c0 < g.D; c0 += 16) {
             if (U > 0)
-                ld_cols(tmem, TM_ACC + c0, acc, 16);
+                ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
-                for (int x = 0; x < 16 && c0 + x < g.D; ++x)
-                    out_at<SPLIT>(p.o, oo + c0 + x, (U > 0 && lse2 != -INFINITY) ? acc[x] : 0.f);
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    if (c0 + x < g.D)
+                        out_at<SPLIT>(p.o, oo + c0 + x, (U > 0 && lse2 != -INFINITY) ? acc[x] : 0.f);
         }
         if (rvalid)
             p.lse_out[stat_off(g, b, kvh * G + hh, t)] = lse2 == -INFINITY ? -INFINITY : lse2 * 0.6931471805599453f;
@@ -542,13 +568,15 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
 }
 
 // --------------------------------------------------------------------- dQ
-template <bool SPLIT>
+template <bool SPLIT, int BS>
 __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
-    const int Dp = p.Dp, bs = g.bs, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
+    constexpr int bs = BS;
+    constexpr int kCh = bs < 32 ? bs : 32;  // S and dP columns read per TMEM wait
+    const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
     // plan: Q, dO [128][Dp] | K, V [bs][Dp] (K also read MN-major by dS K) |
     // dS [128][64] | union | misc
@@ -592,7 +620,6 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         }
     }
     const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, true);
-    float sc[64], dp[64];
     bool ok = true;
     BlockRegs kr, vr;  // the next block's K and V, fetched while the MMAs run
     if (U > 0) {
@@ -614,18 +641,22 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         }
         if (!(ok = commit_wait(sy)))
             break;
-        ld_cols(tmem, TM_S, sc, bs);
-        ld_cols(tmem, TM_DP, dp, bs);
         const bool sel = rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
-        for (int c0 = 0; c0 < bs; c0 += 8) {
-            float dsv[8];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const int c = c0 + x, key = k0 + c;
-                const float pv = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
-                dsv[x] = pv * (dp[c] - dl);
+        for (int c1 = 0; c1 < bs; c1 += kCh) {
+            float sc[kCh], dp[kCh];
+            ld_cols<kCh, kCh>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
+#pragma unroll
+            for (int c0 = 0; c0 < kCh; c0 += 8) {
+                float dsv[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int c = c0 + x, key = k0 + c1 + c;
+                    const float pv = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
+                    dsv[x] = pv * (dp[c] - dl);
+                }
+                put8<SPLIT>(dss, 128, PB, r, c1 + c0, dsv);
             }
-            put8<SPLIT>(dss, 128, PB, r, c0, dsv);
         }
         to_mma();
         if (r == 0)  // dQ += dS K, K read MN-major from its plain tile
@@ -637,10 +668,12 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
         const int64_t qo = rvalid ? dq_off(g, b, kvh * G + hh, t) : 0;
         for (int c0 = 0; c0 < g.D; c0 += 16) {
             if (U > 0)
-                ld_cols(tmem, TM_ACC + c0, acc, 16);
+                ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
-                for (int x = 0; x < 16 && c0 + x < g.D; ++x)
-                    out_at<SPLIT>(p.dq, qo + c0 + x, U > 0 ? acc[x] * g.scale : 0.f);
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    if (c0 + x < g.D)
+                        out_at<SPLIT>(p.dq, qo + c0 + x, U > 0 ? acc[x] * g.scale : 0.f);
         }
     }
     g_end(tmem, sy, p);
@@ -656,7 +689,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
 //   Dp = 128: dV^T += dO^T P, dK^T += Q^T dS (two M = 128 products)
 // accumulated in TMEM over the unit's tiles; then written out (a whole block)
 // or as fp32 partials of a split block.
-template <bool SPLIT>
+template <bool SPLIT, int BS>
 __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
 {
     const int ui = blockIdx.x;
@@ -665,7 +698,9 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
-    const int Dp = p.Dp, bs = g.bs, G = g.G, parts = SPLIT ? 2 : 1;
+    constexpr int bs = BS;
+    constexpr int kCh = bs < 32 ? bs : 32;  // S and dP columns read per TMEM wait
+    const int Dp = p.Dp, G = g.G, parts = SPLIT ? 2 : 1;
     const int Tt = tile_tokens(G), nrows = Tt * G;
     const bool stacked = Dp == 64;
     // plan: K, V [bs][Dp] | Q, dO [128][Dp] | transposed A: stacked [dO^T; Q^T]
@@ -703,7 +738,6 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     const uint32_t idS = idesc_bf16(128, bs, false, false);
     const uint32_t idA = idesc_bf16(128, stacked ? 2 * bs : bs, false, false);
     const int ntiles = (u.count + Tt - 1) / Tt;
-    float sc[64], dp[64];
     bool ok = true;
     for (int ti = 0; ti < ntiles && ok; ++ti) {
         const int pos = ti * Tt + tl;
@@ -731,22 +765,26 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
         if (!(ok = commit_wait(sy)))
             break;
-        ld_cols(tmem, TM_S, sc, bs);
-        ld_cols(tmem, TM_DP, dp, bs);
         // the row's keys: from the window's left edge to its diagonal
         const int cdiag = rvalid ? kdiag(g, b, t) : -1;
         const int khi = rvalid ? min(cdiag, Lk - 1) : -1, klo = key_lo(g, cdiag);
         const bool live = rvalid && l2 != -INFINITY;
-        for (int c = 0; c < bs; ++c) {
-            const int key = k0 + c;
-            const float pv = (live && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
-            const float dsv = pv * (dp[c] - dl);
-            if (stacked) {
-                put<SPLIT>(bs_, 2 * bs, BLO, c, r, pv);
-                put<SPLIT>(bs_, 2 * bs, BLO, bs + c, r, dsv);
-            } else {
-                put<SPLIT>(bs_, bs, BLO, c, r, pv);
-                put<SPLIT>(b2s, bs, BLO, c, r, dsv);
+#pragma unroll
+        for (int c1 = 0; c1 < bs; c1 += kCh) {
+            float sc[kCh], dp[kCh];
+            ld_cols<kCh, kCh>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
+#pragma unroll
+            for (int x = 0; x < kCh; ++x) {
+                const int c = c1 + x, key = k0 + c;
+                const float pv = (live && key >= klo && key <= khi) ? ex2(sc[x] * g.scale_l2 - l2) : 0.f;
+                const float dsv = pv * (dp[x] - dl);
+                if (stacked) {
+                    put<SPLIT>(bs_, 2 * bs, BLO, c, r, pv);
+                    put<SPLIT>(bs_, 2 * bs, BLO, bs + c, r, dsv);
+                } else {
+                    put<SPLIT>(bs_, bs, BLO, c, r, pv);
+                    put<SPLIT>(b2s, bs, BLO, c, r, dsv);
+                }
             }
         }
         to_mma();
@@ -777,16 +815,23 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
                 d = r;
                 mine = true;
             }
-            ld_cols(tmem, col, sc, bs);
-            if (!mine || d >= g.D)
-                continue;
             const float mul = which == 1 ? g.scale : 1.f;
-            for (int c = 0; c < nk; ++c) {
-                const float x = sc[c] * mul;
-                if (direct)
-                    out_at<SPLIT>(which == 1 ? p.dk : p.dv, dkv_off(g, b, kvh, k0 + c) + d, x);
-                else  // a split block's partial: dK first, then dV (the reduction's order)
-                    p.partials[((int64_t)u.slot * 2 + (which == 1 ? 0 : 1)) * bs * g.D + c * g.D + d] = x;
+            for (int c1 = 0; c1 < bs; c1 += 16) {
+                float ac[16];
+                ld_cols<16>(tmem, col + c1, ac);  // every lane: a warp-wide load
+                if (!mine || d >= g.D)
+                    continue;
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int c = c1 + x;
+                    if (c >= nk)
+                        break;
+                    const float v = ac[x] * mul;
+                    if (direct)
+                        out_at<SPLIT>(which == 1 ? p.dk : p.dv, dkv_off(g, b, kvh, k0 + c) + d, v);
+                    else  // a split block's partial: dK first, then dV (the reduction's order)
+                        p.partials[((int64_t)u.slot * 2 + (which == 1 ? 0 : 1)) * bs * g.D + c * g.D + d] = v;
+                }
             }
         }
     }
@@ -803,6 +848,32 @@ template <typename K> bool smem_ok(K kernel, size_t bytes)
 }
 
 size_t union_bytes(const Geo &g) { return union_buf(g).bytes; }
+
+// the instance of a kernel for the element type and the block size (16, 32 or 64)
+using GKernel = void (*)(const GParams);
+template <template <bool, int> class K> GKernel pick(int dtype, int bs)
+{
+    if (dtype == NSA_DTYPE_F32)
+        return bs == 16 ? K<true, 16>::fn : bs == 32 ? K<true, 32>::fn : K<true, 64>::fn;
+    return bs == 16 ? K<false, 16>::fn : bs == 32 ? K<false, 32>::fn : K<false, 64>::fn;
+}
+template <bool S, int B> struct FwdK {
+    static constexpr GKernel fn = fwd_gtc_kernel<S, B>;
+};
+template <bool S, int B> struct DqK {
+    static constexpr GKernel fn = dq_gtc_kernel<S, B>;
+};
+template <bool S, int B> struct DkdvK {
+    static constexpr GKernel fn = dkdv_gtc_kernel<S, B>;
+};
+
+cudaError_t launch_g(GKernel k, int grid, size_t smem, const GParams &p, cudaStream_t st)
+{
+    if (!smem_ok(k, smem))
+        return cudaErrorInvalidValue;
+    k<<<grid, kThr, smem, st>>>(p);
+    return cudaGetLastError();
+}
 
 GParams base_params(const Geo &g, int dtype)
 {
@@ -846,16 +917,7 @@ cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const voi
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
-    if (dtype == NSA_DTYPE_F32) {
-        if (!smem_ok(fwd_gtc_kernel<true>, smem))
-            return cudaErrorInvalidValue;
-        fwd_gtc_kernel<true><<<p.ntiles, kThr, smem, st>>>(p);
-    } else {
-        if (!smem_ok(fwd_gtc_kernel<false>, smem))
-            return cudaErrorInvalidValue;
-        fwd_gtc_kernel<false><<<p.ntiles, kThr, smem, st>>>(p);
-    }
-    return cudaGetLastError();
+    return launch_g(pick<FwdK>(dtype, g.bs), p.ntiles, smem, p, st);
 }
 
 cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
@@ -879,16 +941,7 @@ cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
-    if (dtype == NSA_DTYPE_F32) {
-        if (!smem_ok(dq_gtc_kernel<true>, smem))
-            return cudaErrorInvalidValue;
-        dq_gtc_kernel<true><<<p.ntiles, kThr, smem, st>>>(p);
-    } else {
-        if (!smem_ok(dq_gtc_kernel<false>, smem))
-            return cudaErrorInvalidValue;
-        dq_gtc_kernel<false><<<p.ntiles, kThr, smem, st>>>(p);
-    }
-    return cudaGetLastError();
+    return launch_g(pick<DqK>(dtype, g.bs), p.ntiles, smem, p, st);
 }
 
 cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
@@ -918,16 +971,7 @@ cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const vo
     const size_t smem = 1024 + parts * tiles + 64;
     if (max_units < 1)
         return cudaSuccess;
-    if (dtype == NSA_DTYPE_F32) {
-        if (!smem_ok(dkdv_gtc_kernel<true>, smem))
-            return cudaErrorInvalidValue;
-        dkdv_gtc_kernel<true><<<max_units, kThr, smem, st>>>(p);
-    } else {
-        if (!smem_ok(dkdv_gtc_kernel<false>, smem))
-            return cudaErrorInvalidValue;
-        dkdv_gtc_kernel<false><<<max_units, kThr, smem, st>>>(p);
-    }
-    return cudaGetLastError();
+    return launch_g(pick<DkdvK>(dtype, g.bs), max_units, smem, p, st);
 }
 
 }  // namespace nsa
