@@ -64,6 +64,12 @@ def lib():
         L.oracle_sel_keys_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5 + [_i64]
         L.oracle_sel_blocks_w.restype = None
         L.oracle_sel_blocks_w.argtypes = common + [_ptr] * 5 + [_i64] + [_ptr] * 5 + [_i64]
+        L.oracle_compress_mean.restype = None
+        L.oracle_compress_mean.argtypes = [_i64] * 6 + [_ptr] * 3
+        L.oracle_block_scores.restype = None
+        L.oracle_block_scores.argtypes = [_i64] * 7 + [_dbl] + [_ptr] * 4
+        L.oracle_select_topk.restype = None
+        L.oracle_select_topk.argtypes = [_i64] * 6 + [_ptr] * 3
         _lib = L
     return _lib
 
@@ -270,3 +276,65 @@ def causal(q, k, v, dO=None, scale=None, cu_seqlens_q=None, cu_seqlens_k=None, w
     L.oracle_causal(B, Hq, Hkv, Tq, Tk, D, scale, _p(cuq), _p(cuk), int(window), int(bool(bottom_right)),
                     _p(q), _p(k), _p(v), _p(dOa), _p(o), _p(lse), _p(dq), _p(dk), _p(dv))
     return out
+
+
+# ---------------------------------------------------------------- block selection
+# The step that produces idx (reading in nsa_oracle.c): compressed keys (mean
+# pooling stand-in), block scores = compressed-attention probabilities summed
+# over a kv group's heads, and the top-S selection with the own block first.
+
+
+def _nb(T, bs, cu):
+    maxlen = T if cu is None else (int(np.max(np.diff(cu))) if len(cu) > 1 else 0)
+    return (maxlen + bs - 1) // bs
+
+
+def compress_mean(k, bs, cu_seqlens=None, T=None):
+    """kc [B, Hkv, nb, D] fp64: the mean of each complete block's keys (zero
+    rows elsewhere).  THD: k [total, Hkv, D]; T (optional) fixes nb's length."""
+    k, cu = _f64(k), _i32(cu_seqlens)
+    if cu is None:
+        B, Hkv, Tt, D = k.shape
+    else:
+        Tt, Hkv, D = k.shape
+        B = len(cu) - 1
+    if cu is None:
+        nb = (Tt + bs - 1) // bs
+    else:  # the longest sequence's blocks, or ceil(T / bs) for a given length bound T
+        nb = _nb(None, bs, cu) if T is None else (T + bs - 1) // bs
+    kc = np.zeros((B, Hkv, nb, D), dtype=np.float64)
+    lib().oracle_compress_mean(B, Hkv, Tt, D, bs, nb, _p(cu), _p(k), _p(kc))
+    return kc
+
+
+def block_scores(q, kc, bs, scale=None, cu_seqlens=None):
+    """scores fp64, [B, Hkv, T, nb] (THD [total, Hkv, nb]), from q and kc [B, Hkv, nb, D]."""
+    q, kc, cu = _f64(q), _f64(kc), _i32(cu_seqlens)
+    B_, Hkv, nb, D = kc.shape
+    if cu is None:
+        B, Hq, T, _ = q.shape
+        shape = (B, Hkv, T, nb)
+    else:
+        T, Hq, _ = q.shape
+        B = len(cu) - 1
+        shape = (T, Hkv, nb)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.zeros(shape, dtype=np.float64)
+    lib().oracle_block_scores(B, Hq, Hkv, T, D, bs, nb, scale, _p(cu), _p(q), _p(kc), _p(out))
+    return out
+
+
+def select_topk(scores, bs, S, cu_seqlens=None):
+    """idx int32 [B, Hkv, T, S] (THD [total, Hkv, S]) from scores (any float
+    dtype; an fp32 input is compared exactly as fp32 since fp32 -> fp64 is exact)."""
+    sc, cu = _f64(scores), _i32(cu_seqlens)
+    if cu is None:
+        B, Hkv, T, nb = sc.shape
+        shape = (B, Hkv, T, S)
+    else:
+        T, Hkv, nb = sc.shape
+        B = len(cu) - 1
+        shape = (T, Hkv, S)
+    idx = np.full(shape, -1, dtype=np.int32)
+    lib().oracle_select_topk(B, Hkv, T, bs, S, nb, _p(cu), _p(sc), _p(idx))
+    return idx

@@ -781,3 +781,139 @@ void oracle_causal(int64_t B, int64_t Hq, int64_t Hkv, int64_t Tq, int64_t Tk, i
     }
     free(Dt);
 }
+
+/* ------------------------------------------------------------ block selection
+ *
+ * The step that produces idx.  The pages take the index as given (the
+ * gradcheck-gate page names "NSA selection" and builds idx with a helper it
+ * does not print), so this is the plainest reading of NSA's selection step,
+ * kept consistent with the index the pages' tests use (slot 0 is the row's
+ * own block):
+ *
+ *   block j of a sequence is complete at row t  iff  (j + 1) * bs - 1 <= t
+ *   kc_{g,j}      the compressed key of block j of kv head g -- an input,
+ *                 since NSA learns its compression; the stand-in provided
+ *                 is the mean of the block's bs keys (complete blocks only)
+ *   p_{h,t,j}     = exp(scale <q_{h,t}, kc_{g,j}>) / sum_{j' complete at t} exp(scale <q_{h,t}, kc_{g,j'}>)
+ *                   for j complete at t (h in group g)
+ *   score_{g,t,j} = sum_{h in group g} p_{h,t,j}    (0 where j is not complete at t)
+ *   idx_{g,t}     = [ t / bs,  then the S - 1 blocks j != t / bs complete at t
+ *                     with the largest scores, in decreasing order of score
+ *                     (equal scores: the smaller j first; a NaN score counts
+ *                     as -infinity),  then -1 for the slots left ]
+ *
+ * Layouts: kc [B, Hkv, nb, D], nb = ceil(T / bs) (THD: of the longest
+ * sequence), zero rows for blocks that are not complete; scores
+ * [B, Hkv, T, nb] (THD: [total, Hkv, nb]).
+ */
+
+static int64_t n_complete(int64_t t, int64_t bs) { return (t + 1) / bs; }
+
+static int64_t score_off(const prob_t *p, int64_t nb, int64_t b, int64_t g, int64_t t)
+{
+    if (p->cu)
+        return (((int64_t)p->cu[b] + t) * p->Hkv + g) * nb;
+    return ((b * p->Hkv + g) * p->T + t) * nb;
+}
+
+/* kc_{g,j} = (1 / bs) * sum of keys j*bs .. j*bs + bs - 1, for complete blocks */
+void oracle_compress_mean(int64_t B, int64_t Hkv, int64_t T, int64_t D, int64_t bs, int64_t nb,
+                          const int32_t *cu, const double *k, double *kc)
+{
+    prob_t p = mk(B, Hkv, Hkv, T, D, bs, 1, 1.0, cu);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t j = 0; j < nb; ++j) {
+                double *out = kc + ((b * Hkv + g) * nb + j) * D;
+                for (int64_t d = 0; d < D; ++d)
+                    out[d] = 0.0;
+                if ((j + 1) * bs > seq_len(&p, b))
+                    continue;  /* not complete in this sequence */
+                for (int64_t kk = j * bs; kk < (j + 1) * bs; ++kk) {
+                    const double *kr = k + row_off(&p, Hkv, b, g, kk);
+                    for (int64_t d = 0; d < D; ++d)
+                        out[d] += kr[d];
+                }
+                for (int64_t d = 0; d < D; ++d)
+                    out[d] /= (double)bs;
+            }
+}
+
+/* score_{g,t,j}: the compressed-attention probabilities of the group's heads, summed */
+void oracle_block_scores(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t bs, int64_t nb,
+                         double scale, const int32_t *cu, const double *q, const double *kc, double *scores)
+{
+    prob_t p = mk(B, Hq, Hkv, T, D, bs, 1, scale, cu);
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g) {
+            double *s = (double *)malloc(sizeof(double) * (nb > 0 ? nb : 1));
+            for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                double *out = scores + score_off(&p, nb, b, g, t);
+                for (int64_t j = 0; j < nb; ++j)
+                    out[j] = 0.0;
+                const int64_t nc = n_complete(t, bs);
+                for (int64_t h = g * G; h < (g + 1) * G; ++h) {
+                    const double *qt = q + row_off(&p, Hq, b, h, t);
+                    double m = -INFINITY, sum = 0.0;
+                    for (int64_t j = 0; j < nc; ++j) {
+                        s[j] = scale * dot(qt, kc + ((b * Hkv + g) * nb + j) * D, D);
+                        if (s[j] > m)
+                            m = s[j];
+                    }
+                    for (int64_t j = 0; j < nc; ++j)
+                        sum += exp(s[j] - m);
+                    for (int64_t j = 0; j < nc; ++j)
+                        out[j] += exp(s[j] - m) / sum;
+                }
+            }
+            free(s);
+        }
+}
+
+/* 1 if (x, i) comes before (y, j) in the selection order: larger score
+ * first, then smaller block id; NaN as -infinity */
+static int ranks_before(double x, int64_t i, double y, int64_t j)
+{
+    if (isnan(x))
+        x = -INFINITY;
+    if (isnan(y))
+        y = -INFINITY;
+    return x > y || (x == y && i < j);
+}
+
+/* idx rows from scores: the own block, then the S - 1 best complete blocks */
+void oracle_select_topk(int64_t B, int64_t Hkv, int64_t T, int64_t bs, int64_t S, int64_t nb,
+                        const int32_t *cu, const double *scores, int32_t *idx)
+{
+    prob_t p = mk(B, Hkv, Hkv, T, 1, bs, S, 1.0, cu);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t g = 0; g < Hkv; ++g)
+            for (int64_t t = 0; t < seq_len(&p, b); ++t) {
+                const double *sc = scores + score_off(&p, nb, b, g, t);
+                int32_t *row = (int32_t *)idx_row(&p, idx, b, g, t);
+                const int64_t own = t / bs, nc = n_complete(t, bs);
+                for (int64_t s = 0; s < S; ++s)
+                    row[s] = -1;
+                row[0] = (int32_t)own;
+                for (int64_t s = 1; s < S; ++s) {
+                    /* the best complete block not yet taken */
+                    int64_t best = -1;
+                    for (int64_t j = 0; j < nc; ++j) {
+                        if (j == own)
+                            continue;
+                        int taken = 0;
+                        for (int64_t u = 1; u < s; ++u)
+                            taken |= row[u] == j;
+                        if (taken)
+                            continue;
+                        if (best < 0 || ranks_before(sc[j], j, sc[best], best))
+                            best = j;
+                    }
+                    if (best < 0)
+                        break;
+                    row[s] = (int32_t)best;
+                }
+            }
+}
