@@ -451,6 +451,45 @@ def run_ours(args):
            "bwd_ms": sw_bwd / n_sw, "fwd_ms": sw_fwd / n_sw, "steps": n_sw,
            "scope": "nsa_swa_fwd + nsa_swa_bwd, same shapes, 10*D*pairs / backward time, L2 flushed"}
 
+    # ---- the step that produces the index (nsa_compress_keys_mean,
+    # nsa_block_scores, nsa_select_topk) on the same q and k: compressed keys,
+    # block scores on the tensor cores, the own block + S-1 best complete blocks
+    kc = api.compress_keys_mean(k, bs)
+    for _ in range(2):
+        sc_ = api.block_scores(q, kc, bs)
+        api.select_topk(sc_, bs, S)
+    n_se = max(3, min(K, 20))
+    s_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_se)]
+    for i in range(n_se):
+        flush.zero_()
+        s_ev[i][0].record(st)
+        kc = api.compress_keys_mean(k, bs)
+        s_ev[i][1].record(st)
+        sc_ = api.block_scores(q, kc, bs)
+        s_ev[i][2].record(st)
+        idx_sel = api.select_topk(sc_, bs, S)
+        s_ev[i][3].record(st)
+    torch.cuda.synchronize()
+    if api.get_error(api.workspace(1, dev, "select")):
+        raise RuntimeError("device error in the selection-step leg")
+    sel_ms = [sorted(e[j].elapsed_time(e[j + 1]) for e in s_ev)[n_se // 2] for j in range(3)]
+    nb_sel = (T + bs - 1) // bs
+    esz = 2
+    sc_bytes = B * Hq * T * D * esz + B * Hkv * nb_sel * D * esz + B * Hkv * T * nb_sel * 4
+    peak_hbm = peaks.get("hbm_gbs") if peaks else None
+    select = {
+        "ms": {"compress_mean": sel_ms[0], "block_scores": sel_ms[1], "select_topk": sel_ms[2]},
+        "step_ms": sum(sel_ms), "steps": n_se, "index_rows": B * Hkv * T,
+        "rows_per_s": B * Hkv * T / (sum(sel_ms) * 1e-3),
+        "roofline": {"kernel": "block_scores", "bound": "hbm", "unit": "GB/s",
+                     "achieved": sc_bytes / (sel_ms[1] * 1e-3) / 1e9, "peak": peak_hbm,
+                     "frac": (sc_bytes / (sel_ms[1] * 1e-3) / 1e9 / peak_hbm) if peak_hbm else None,
+                     "algorithmic_bytes": sc_bytes,
+                     "bytes_are": "read q and kc once, write fp32 scores [B,Hkv,T,nb] once"},
+        "scope": "median per kernel over the steps, L2 flushed before each step; same q and k as the headline",
+    }
+    del kc, sc_, idx_sel
+
     # ---- the pages' other workloads (single GPU only; rank 0 of a replica run
     # times them too, each rank on its own GPU)
     configs = {}
@@ -542,6 +581,7 @@ def run_ours(args):
                                      "around every launch (the library's tracer); the roofline uses it",
                              "bwd_ms": traced_bwd_ms},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "planned": planned, "swa": swa,
+            "select": select,
             "configs": configs,
             "gpu_launches": len(recs),
             "clocks": clocks,

@@ -32,6 +32,7 @@ SYMBOLS = (
     "nsa_plan_size", "nsa_plan_build", "nsa_bwd_planned_workspace_size", "nsa_sel_bwd_planned",
     "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd", "nsa_debug_stall",
     "nsa_causal_fwd_workspace_size", "nsa_causal_bwd_workspace_size", "nsa_causal_fwd", "nsa_causal_bwd",
+    "nsa_select_workspace_size", "nsa_compress_keys_mean", "nsa_block_scores", "nsa_select_topk",
 )
 
 
@@ -131,6 +132,11 @@ def lib() -> C.CDLL:
         L.nsa_trace_count.restype = C.c_int32
         L.nsa_trace_count.argtypes = []
         L.nsa_trace_get.argtypes = [C.c_int32, C.POINTER(C.c_char_p), C.POINTER(C.c_float)]
+        L.nsa_select_workspace_size.restype = C.c_size_t
+        L.nsa_select_workspace_size.argtypes = [pp]
+        L.nsa_compress_keys_mean.argtypes = [pp] + [_P] * 3 + [_P]
+        L.nsa_block_scores.argtypes = [pp] + [_P] * 4 + [_P, C.c_size_t, _P]
+        L.nsa_select_topk.argtypes = [pp] + [_P] * 3 + [_P]
         for name in SYMBOLS:
             fn = getattr(L, name)
             if fn.restype is C.c_int:  # default restype: status enums
@@ -472,3 +478,64 @@ def trace_records():
 
 def default_scale(D):
     return 1.0 / math.sqrt(D)
+
+
+# ---------------------------------------------------------------- block selection
+# The step that produces the index (include/nsa.h states the reading): block
+# scores from compressed keys, then the own block and the S - 1 best complete
+# blocks per index row.
+
+
+def _nb(T, block_size):
+    return (T + block_size - 1) // block_size
+
+
+def compress_keys_mean(k, block_size, cu_seqlens=None, max_seqlen=None, stream=None):
+    """kc [B, Hkv, nb, D] (k's dtype): the mean of each complete block's keys."""
+    p = problem_from(k, k, block_size, 1, None, cu_seqlens, max_seqlen)
+    declare_strides(p, cu_seqlens is not None, k=k)
+    B = p.B
+    kc = torch.empty(B, p.Hkv, _nb(p.T, block_size), p.D, dtype=k.dtype, device=k.device)
+    _check(lib().nsa_compress_keys_mean(C.byref(p), _ptr(cu_seqlens), _ptr(k), _ptr(kc), _stream(stream)),
+           "nsa_compress_keys_mean")
+    return kc
+
+
+def block_scores(q, kc, block_size, scale=None, cu_seqlens=None, max_seqlen=None, ws=None, stream=None):
+    """float32 block scores, [B, Hkv, T, nb] (THD [total, Hkv, nb])."""
+    p = problem_from(q, kc, block_size, 1, scale, cu_seqlens, max_seqlen)
+    declare_strides(p, cu_seqlens is not None, q=q)
+    nb = _nb(p.T, block_size)
+    if kc.shape[2] != nb or not kc.is_contiguous():
+        raise NsaError(1, "block_scores: kc must be a dense [B, Hkv, ceil(T / block_size), D] tensor")
+    shape = (p.B, p.Hkv, p.T, nb) if cu_seqlens is None else (q.shape[0], p.Hkv, nb)
+    scores = torch.empty(shape, dtype=torch.float32, device=q.device)
+    n = int(lib().nsa_select_workspace_size(C.byref(p)))
+    if n == 0:
+        raise NsaError(1, "nsa_select_workspace_size")
+    ws = workspace(n, q.device, "select") if ws is None else ws
+    _check(lib().nsa_block_scores(C.byref(p), _ptr(cu_seqlens), _ptr(q), _ptr(kc), _ptr(scores), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "nsa_block_scores")
+    return scores
+
+
+def select_topk(scores, block_size, S, cu_seqlens=None, max_seqlen=None, stream=None):
+    """int32 index rows from block scores: [B, Hkv, T, S] (THD [total, Hkv, S])."""
+    if cu_seqlens is None:
+        B, Hkv, T, nb = scores.shape
+        p = problem(B, Hkv, Hkv, T, 32, block_size, S, torch.float32)
+        shape = (B, Hkv, T, S)
+    else:
+        total, Hkv, nb = scores.shape
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 1
+        p = problem(B, Hkv, Hkv, max(1, max_seqlen), 32, block_size, S, torch.float32, layout=LAYOUT_THD,
+                    total_tokens=total)
+        shape = (total, Hkv, S)
+    if nb != _nb(p.T, block_size) or not scores.is_contiguous():
+        raise NsaError(1, "select_topk: scores must be dense with ceil(T / block_size) entries per row")
+    idx = torch.empty(shape, dtype=torch.int32, device=scores.device)
+    _check(lib().nsa_select_topk(C.byref(p), _ptr(cu_seqlens), _ptr(scores), _ptr(idx), _stream(stream)),
+           "nsa_select_topk")
+    return idx

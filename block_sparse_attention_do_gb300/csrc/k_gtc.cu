@@ -48,6 +48,7 @@ struct GParams {
     float *partials;
     void *o, *dq, *dk, *dv;
     float *lse_out;
+    float *scores;  // block scores (selection step)
     int *err;
     int Dp;       // head dim padded to 64 or 128
     int ntiles;   // query tiles (forward / dQ)
@@ -838,6 +839,166 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     g_end(tmem, sy, p);
 }
 
+// ------------------------------------------------------------ block scores
+// The selection step's scores: for row (b, query head h, t) and block j
+// complete at t ((j + 1) bs - 1 <= t), p = exp(scale <q, kc_j>) normalised
+// over the row's complete blocks; a token's score of block j is the sum of
+// p over the G heads of its kv head (0 for blocks not complete at t).
+// One CTA per query tile (Tq tokens x G heads): the compressed keys of the
+// blocks complete at the tile's last row go through shared memory in chunks
+// of 64 (the MMA's N); pass 1 keeps each row's running maximum and sum,
+// pass 2 forms p, stages it in shared memory (row stride 65 floats: column
+// writes by rows and row reads by columns are both conflict-free) and sums
+// each token's G rows.  S of up to 4 chunks stays in TMEM between the passes;
+// longer rows recompute it.
+constexpr int kScoreCh = 64;   // compressed keys per chunk
+constexpr int kPStride = 65;   // floats per staged row
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Geo &g = p.g;
+    constexpr int VEC = In<SPLIT>::VEC;
+    const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1, nb = g.nbmax;
+    // plan: Q [128][Dp] | compressed-key chunk [64][Dp] (each with its low
+    // part after it) | staged p [128][kPStride] fp32 | misc
+    const uint32_t QB = 128 * Dp * 2, CB = kScoreCh * Dp * 2;
+    uint8_t *q_t = sm, *c_t = q_t + parts * QB;
+    float *pbuf = (float *)(c_t + parts * CB);
+    uint8_t *misc = (uint8_t *)(pbuf + 128 * kPStride);
+    Sync sy;
+    const uint32_t tmem = g_start(misc, p, sy);
+    const int r = threadIdx.x;
+    int b = 0, kvh = 0, t0 = 0, nvalid = 0;
+    qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
+    zero_smem(sm, parts * (QB + CB));
+    int tl, hh;
+    qrow(G, r, tl, hh);
+    const bool rvalid = r < nrows && tl < nvalid;
+    const int t = t0 + tl;
+    const int nc = rvalid ? (t + 1) / g.bs : 0;                      // the row's complete blocks
+    const int ncmax = nvalid > 0 ? (t0 + nvalid) / g.bs : 0;           // ... of the tile's last row
+    const int nch = (ncmax + kScoreCh - 1) / kScoreCh;
+    const bool resident = nch <= 4;
+    const uint32_t qs = smem_u32(q_t), cs = smem_u32(c_t);
+    // the row's q, 16 vectors at a time
+    {
+        const int64_t qo = rvalid ? q_off(g, b, kvh * G + hh, t) : 0;
+        for (int i0 = 0; i0 * VEC < g.D; i0 += kRowVec) {
+            uint4 v[kRowVec];
+#pragma unroll
+            for (int i = 0; i < kRowVec; ++i) {
+                const int c = (i0 + i) * VEC;
+                v[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (rvalid && c < g.D)
+                    v[i] = __ldg((const uint4 *)((const uint8_t *)p.q + (qo + c) * In<SPLIT>::ES));
+            }
+#pragma unroll
+            for (int i = 0; i < kRowVec; ++i)
+                if ((i0 + i) * VEC < g.D)
+                    put_vec<SPLIT>(qs, 128, QB, r, (i0 + i) * VEC, v[i]);
+        }
+    }
+    const int nv = g.D / VEC, lnv = __ffs(nv) - 1, nvec = kScoreCh * nv;
+    const uint8_t *kc_bg = (const uint8_t *)p.k + (int64_t)(b * g.Hkv + kvh) * nb * g.D * In<SPLIT>::ES;
+    // chunk c of the compressed keys into the chunk tile, 8 vectors a thread at a time
+    auto load_chunk = [&](int c) {
+        for (int e0 = 0; e0 < nvec; e0 += kBlkVec * kThr) {
+            uint4 v[kBlkVec];
+#pragma unroll
+            for (int i = 0; i < kBlkVec; ++i) {
+                const int e = e0 + threadIdx.x + i * kThr, row = e >> lnv, j = c * kScoreCh + row;
+                v[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < nvec && j < nb)
+                    v[i] = __ldg((const uint4 *)(kc_bg + ((int64_t)j * g.D + (e & (nv - 1)) * VEC) * In<SPLIT>::ES));
+            }
+#pragma unroll
+            for (int i = 0; i < kBlkVec; ++i) {
+                const int e = e0 + threadIdx.x + i * kThr;
+                if (e < nvec)
+                    put_vec<SPLIT>(cs, kScoreCh, CB, e >> lnv, (e & (nv - 1)) * VEC, v[i]);
+            }
+        }
+    };
+    const uint32_t idS = idesc_bf16(128, kScoreCh, false, false);
+    bool ok = true;
+    // pass 1: the row's maximum m and sum l of exp2(scale_l2 s) over its complete blocks
+    float m = -INFINITY, l = 0.f;
+    for (int c = 0; c < nch && ok; ++c) {
+        const uint32_t col = resident ? c * kScoreCh : 0;
+        load_chunk(c);
+        to_mma();
+        if (r == 0)
+            product<SPLIT>(tmem + col, qs, 128, QB, cs, kScoreCh, CB, idS, Dp / 16, false);
+        if (!(ok = commit_wait(sy)))
+            break;
+#pragma unroll
+        for (int c1 = 0; c1 < kScoreCh; c1 += 32) {
+            float s[32];
+            ld_cols<32>(tmem, col + c1, s);
+            float bm = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                s[x] = c * kScoreCh + c1 + x < nc ? s[x] * g.scale_l2 : -INFINITY;
+                bm = fmaxf(bm, s[x]);
+            }
+            if (bm != -INFINITY) {
+                const float mn = fmaxf(m, bm);
+                float sum = 0.f;
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    sum += ex2(s[x] - mn);
+                l = l * ex2(m - mn) + sum;
+                m = mn;
+            }
+        }
+    }
+    const float lse2 = l > 0.f ? m + log2f(l) : INFINITY;  // +inf: no complete block, p = 0
+    // pass 2: p per row, staged; each token's G rows summed into its scores
+    for (int c = 0; c < nch && ok; ++c) {
+        uint32_t col = c * kScoreCh;
+        if (!resident) {
+            col = 0;
+            load_chunk(c);
+            to_mma();
+            if (r == 0)
+                product<SPLIT>(tmem, qs, 128, QB, cs, kScoreCh, CB, idS, Dp / 16, false);
+            if (!(ok = commit_wait(sy)))
+                break;
+        }
+#pragma unroll
+        for (int c1 = 0; c1 < kScoreCh; c1 += 32) {
+            float s[32];
+            ld_cols<32>(tmem, col + c1, s);
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+                pbuf[r * kPStride + c1 + x] = c * kScoreCh + c1 + x < nc ? ex2(s[x] * g.scale_l2 - lse2) : 0.f;
+        }
+        __syncthreads();
+        for (int o = threadIdx.x; o < nvalid * kScoreCh; o += kThr) {
+            const int tk = o / kScoreCh, jj = o % kScoreCh, j = c * kScoreCh + jj;
+            if (j >= nb)
+                continue;
+            float sum = 0.f;
+            for (int h2 = 0; h2 < G; ++h2)
+                sum += pbuf[(tk * G + h2) * kPStride + jj];
+            p.scores[index_row(g, b, kvh, t0 + tk) * nb + j] = sum;
+        }
+        tc_fence_before();  // this chunk's TMEM reads and staged rows are done before the next
+        __syncthreads();
+        tc_fence_after();
+    }
+    // zeros for the blocks past the tile's chunks
+    if (ok) {
+        const int j0 = nch * kScoreCh, rest = nb - j0;
+        for (int o = threadIdx.x; rest > 0 && o < nvalid * rest; o += kThr)
+            p.scores[index_row(g, b, kvh, t0 + o / rest) * nb + j0 + o % rest] = 0.f;
+    }
+    g_end(tmem, sy, p);
+}
+
 constexpr int kSmemLimit = 232448;
 
 template <typename K> bool smem_ok(K kernel, size_t bytes)
@@ -897,6 +1058,30 @@ bool gtc_supported(const Geo &g, int dtype)
     if (dtype == NSA_DTYPE_BF16)
         return g.D == 32 || g.D == 64 || g.D == 128;
     return g.D == 32 || g.D == 64;  // fp32: split precision
+}
+
+bool scores_gtc_supported(const Geo &g, int dtype)
+{
+    return g.G >= 1 && g.G <= kRows && (g.D == 32 || g.D == 64 || g.D == 128) &&
+           (dtype == NSA_DTYPE_BF16 || dtype == NSA_DTYPE_F32);
+}
+
+cudaError_t launch_scores_gtc(const Geo &g, const void *q, const void *kc, float *scores, int dtype, int *err,
+                              cudaStream_t st)
+{
+    GParams p = base_params(g, dtype);
+    p.q = q;
+    p.k = kc;
+    p.scores = scores;
+    p.err = err;
+    const int Tq = tile_tokens(g.G);
+    p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
+    const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
+    const size_t smem = 1024 + parts * (size_t)(128 + kScoreCh) * p.Dp * 2 + 128 * kPStride * 4 + 64;
+    if (p.ntiles < 1)
+        return cudaSuccess;
+    return launch_g(dtype == NSA_DTYPE_F32 ? scores_gtc_kernel<true> : scores_gtc_kernel<false>, p.ntiles, smem, p,
+                    st);
 }
 
 cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const void *v, const int *idx, void *o,

@@ -83,6 +83,18 @@ cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const vo
                             const Unit *units, const WsHeader *hdr, int max_units, float *partials, void *dk,
                             void *dv, int dtype, int *err, cudaStream_t st);
 
+// the selection step's block scores on the tensor cores (bf16, or fp32 by
+// split precision; D in {32, 64, 128}); kc [B, Hkv, nbmax, D] dense
+bool scores_gtc_supported(const Geo &g, int dtype);
+cudaError_t launch_scores_gtc(const Geo &g, const void *q, const void *kc, float *scores, int dtype, int *err,
+                              cudaStream_t st);
+
+// ---- the selection step's other kernels (k_select.cu) ---------------------
+// kc [B, Hkv, nbmax, D] dense: the mean of each complete block's keys, zero rows elsewhere
+cudaError_t launch_compress_mean(const Geo &g, const void *k, void *kc, int dtype, cudaStream_t st);
+// idx rows from block scores (rows as the index's; nbmax scores each)
+cudaError_t launch_select_topk(const Geo &g, const float *scores, int *idx, cudaStream_t st);
+
 // ---- tensor-core kernels (bf16, D = 128, block_size = 64) -----------------
 bool tc_supported(const Geo &g, int dtype);
 // tile_next: a device int that is zero when the kernel starts (its work counter).

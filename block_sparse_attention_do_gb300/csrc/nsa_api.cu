@@ -422,6 +422,15 @@ WaitTest g_wait_test = {WAIT_TEST_NONE, 0};
 // distinct, so that a packed causal problem's keys count as their own
 const int32_t *const kFakeCuQ = (const int32_t *)16, *const kFakeCuK = (const int32_t *)32;
 
+// The selection-step entries take either layout (THD when p->layout says so,
+// with cu_seqlens); index rows and block scores follow the index's layout.
+nsa_status select_geo(const nsa_problem *p, const int32_t *cu_seqlens, Geo &g, Mode mode)
+{
+    if (!p)
+        return NSA_ERR_INVALID_ARG;
+    return make_geo(p, p->layout == NSA_LAYOUT_THD, mode, cu_seqlens, g);
+}
+
 size_t fwd_ws_need(const nsa_problem *p, Mode mode)
 {
     if (mode != CAUSAL)
@@ -866,6 +875,69 @@ nsa_status nsa_trace_get(int32_t i, const char **name, float *ms)
     if (cudaEventElapsedTime(ms, g_trace[i].start, g_trace[i].stop) != cudaSuccess)
         return NSA_ERR_CUDA;
     *name = g_trace[i].name;
+    return NSA_OK;
+}
+
+// ---- the step that produces the index (block selection) -------------------
+
+size_t nsa_select_workspace_size(const nsa_problem *p)
+{
+    Geo g;
+    const bool thd = p && p->layout == NSA_LAYOUT_THD;
+    return select_geo(p, thd ? kFakeCuQ : nullptr, g, DENSE) == NSA_OK ? align_up(sizeof(WsHeader)) : 0;
+}
+
+nsa_status nsa_compress_keys_mean(const nsa_problem *p, const int32_t *cu_seqlens, const void *k, void *kc,
+                                  void *stream)
+{
+    Geo g;
+    nsa_status s = select_geo(p, cu_seqlens, g, DENSE);
+    if (s != NSA_OK)
+        return s;
+    if (!k || !kc || !aligned16(k) || !aligned16(kc))
+        return NSA_ERR_INVALID_ARG;
+    if (g.ntok == 0 || g.nbmax == 0)
+        return NSA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    NSA_LAUNCH("compress_mean", launch_compress_mean(g, k, kc, p->dtype, st));
+    return NSA_OK;
+}
+
+nsa_status nsa_block_scores(const nsa_problem *p, const int32_t *cu_seqlens, const void *q, const void *kc,
+                            float *scores, void *ws, size_t ws_bytes, void *stream)
+{
+    Geo g;
+    nsa_status s = select_geo(p, cu_seqlens, g, DENSE);
+    if (s != NSA_OK)
+        return s;
+    if (!q || !kc || !scores || !aligned16(q) || !aligned16(kc) || ((uintptr_t)scores & 3u))
+        return NSA_ERR_INVALID_ARG;
+    if (!scores_gtc_supported(g, p->dtype))
+        return NSA_ERR_UNSUPPORTED;
+    if ((s = check_ws(ws, ws_bytes, align_up(sizeof(WsHeader)))) != NSA_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    WsHeader *hdr = (WsHeader *)ws;
+    NSA_TRY(cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st));
+    if (g.ntok == 0)
+        return NSA_OK;
+    NSA_LAUNCH("block_scores", launch_scores_gtc(g, q, kc, scores, p->dtype, &hdr->err, st));
+    return NSA_OK;
+}
+
+nsa_status nsa_select_topk(const nsa_problem *p, const int32_t *cu_seqlens, const float *scores, int32_t *idx,
+                           void *stream)
+{
+    Geo g;
+    nsa_status s = select_geo(p, cu_seqlens, g, SPARSE);
+    if (s != NSA_OK)
+        return s;
+    if (!scores || !idx || ((uintptr_t)scores & 3u) || ((uintptr_t)idx & 3u))
+        return NSA_ERR_INVALID_ARG;
+    if (g.ntok == 0)
+        return NSA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    NSA_LAUNCH("select_topk", launch_select_topk(g, scores, idx, st));
     return NSA_OK;
 }
 

@@ -102,6 +102,15 @@ __device__ __forceinline__ int64_t stat_off(const Geo &g, int b, int h, int t)
     return ((int64_t)b * g.Hq + h) * g.T + t;
 }
 
+// the number of index row (b, kvh, t): BHTD (b*Hkv + kvh)*T + t, THD token*Hkv + kvh
+// (the block scores of the selection step use the same rows)
+__device__ __forceinline__ int64_t index_row(const Geo &g, int b, int kvh, int t)
+{
+    if (g.thd)
+        return (int64_t)(g.cu[b] + t) * g.Hkv + kvh;
+    return ((int64_t)b * g.Hkv + kvh) * g.T + t;
+}
+
 __device__ __forceinline__ const int *idx_row(const Geo &g, const int *idx, int b, int kvh, int t)
 {
     if (g.thd)

@@ -31,6 +31,8 @@ __all__ = [
     "make_varlen_block_idx",
     "cu_seqlens_from_lengths",
     "round_to_dtype",
+    "make_compressed_keys",
+    "make_block_scores",
 ]
 
 
@@ -130,3 +132,26 @@ def make_varlen_block_idx(lengths, Hkv, bs, S, seed=0) -> torch.Tensor:
             out[off : off + L, g, :] = _draw_rows(rng, L, bs, S)
         off += L
     return torch.from_numpy(out)
+
+
+def make_compressed_keys(B, Hkv, nb, D, dtype=torch.float32, seed=0) -> torch.Tensor:
+    """[B, Hkv, nb, D] CPU tensor in ``dtype``: standard normal draws standing
+    in for one compressed key per key block."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return round_to_dtype(torch.randn((B, Hkv, nb, D), generator=g, dtype=torch.float32), dtype)
+
+
+def make_block_scores(shape, seed=0, levels=0, nan_frac=0.0) -> torch.Tensor:
+    """fp32 CPU tensor of block scores: uniform in [0, 1), or (levels > 0)
+    one of ``levels`` evenly spaced values so that ties are common; a
+    fraction ``nan_frac`` of the entries is NaN."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    if levels > 0:
+        x = torch.randint(0, levels, shape, generator=g).float() / levels
+    else:
+        x = torch.rand(shape, generator=g, dtype=torch.float32)
+    if nan_frac > 0:
+        x[torch.rand(shape, generator=g) < nan_frac] = float("nan")
+    return x

@@ -357,6 +357,49 @@ nsa_status nsa_build_inverse_index_noalloc(const nsa_problem *p, const int32_t *
 nsa_status nsa_debug_stall(int32_t kernel, int32_t wait_limit_us);
 
 /*
+ * The step that PRODUCES the index: NSA's block selection.  The pages take
+ * idx as given (the gradcheck-gate page names "NSA selection" and builds
+ * idx with a helper it does not print), so this is the plainest reading of
+ * the selection step, consistent with the pages' tests (slot 0 = the row's
+ * own block):
+ *   block j of a sequence is complete at row t  iff  (j+1)*block_size - 1 <= t
+ *   p[h,t,j]    = softmax over the blocks j complete at t of scale*<q[h,t], kc[g,j]>
+ *   score[g,t,j] = sum over the G query heads h of kv head g of p[h,t,j]
+ *                  (0 for blocks not complete at t)
+ *   idx[g,t]    = [ t / block_size, then the S - 1 blocks other than it that
+ *                   are complete at t with the largest scores, in decreasing
+ *                   order (equal scores: smaller j first; NaN ranks as
+ *                   -infinity), then -1 for the slots left ]
+ * kc is one compressed key per block and kv head; NSA learns that
+ * compression, so kc is an input.  nsa_compress_keys_mean writes the
+ * weight-free stand-in (the mean of the block's keys).
+ *
+ * These entries take either layout: p->layout THD with cu_seqlens (block ids
+ * and causality local to each sequence), else BHTD with cu_seqlens NULL.
+ *   kc      [B, Hkv, nb, D] dense, the problem's dtype, nb = ceil(T /
+ *           block_size) (THD: T bounds every sequence length); rows of blocks
+ *           not complete in their sequence are zero (compress) or unused
+ *   scores  float, [B, Hkv, T, nb] (BHTD) or [total, Hkv, nb] (THD): the
+ *           index's rows, nb scores each
+ *   idx     int32, the index layout ([B, Hkv, T, S] / [total, Hkv, S])
+ * k honours p->kv_stride and q p->q_stride; kc, scores and idx are dense.
+ * Pointers are device pointers owned by the caller: q, k and kc 16-byte
+ * aligned, scores and idx 4-byte aligned.  Shape errors are returned before
+ * any launch.  nsa_block_scores runs on the tensor cores (bf16; fp32 by
+ * split precision; D in {32, 64, 128}) with bounded waits: its workspace
+ * (nsa_select_workspace_size bytes, 256-byte aligned) carries the device
+ * error word read by nsa_get_error.  nsa_compress_keys_mean and
+ * nsa_select_topk report no device errors and take no workspace.
+ */
+size_t nsa_select_workspace_size(const nsa_problem *p);
+nsa_status nsa_compress_keys_mean(const nsa_problem *p, const int32_t *cu_seqlens, const void *k, void *kc,
+                                  void *stream);
+nsa_status nsa_block_scores(const nsa_problem *p, const int32_t *cu_seqlens, const void *q, const void *kc,
+                            float *scores, void *ws, size_t ws_bytes, void *stream);
+nsa_status nsa_select_topk(const nsa_problem *p, const int32_t *cu_seqlens, const float *scores, int32_t *idx,
+                           void *stream);
+
+/*
  * Reads the device error word of a workspace used by the calls above,
  * after synchronising `stream`, into *out (an nsa_status value), and clears
  * it.  Returns NSA_ERR_CUDA if the read itself fails.

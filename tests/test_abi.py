@@ -198,3 +198,36 @@ def test_causal_entries_check_their_arguments(lib):
     assert s == 1
     s = lib.nsa_causal_fwd(C.byref(p), -1, None, None, *([dummy] * 5), dummy, 1 << 30, None)
     assert s == 1
+
+
+def test_selection_step_argument_checks(lib):
+    """The selection-step entries (block scores, top-S, compressed keys)
+    refuse bad arguments before any launch."""
+    import torch
+
+    from block_sparse_attention_do_gb300 import api
+
+    p = _p()
+    assert lib.nsa_select_workspace_size(C.byref(p)) == 256
+    assert lib.nsa_select_workspace_size(C.byref(_p(Hq=3))) == 0       # Hq % Hkv != 0
+    assert lib.nsa_select_workspace_size(C.byref(_p(D=96))) == 0       # unsupported head dim
+    pt = api.problem(2, 4, 2, 256, 64, 32, 4, torch.bfloat16, layout=1, total_tokens=300)
+    assert lib.nsa_select_workspace_size(C.byref(pt)) == 256           # THD sizes need no cu_seqlens
+    dev = C.c_void_p(256)
+    ws = C.c_void_p(256)
+    # null / misaligned tensors
+    assert lib.nsa_compress_keys_mean(C.byref(p), None, None, dev, None) == 1
+    assert lib.nsa_compress_keys_mean(C.byref(p), None, C.c_void_p(258), dev, None) == 1
+    assert lib.nsa_block_scores(C.byref(p), None, dev, dev, None, ws, 256, None) == 1
+    assert lib.nsa_block_scores(C.byref(p), None, dev, dev, C.c_void_p(258), ws, 256, None) == 1
+    assert lib.nsa_select_topk(C.byref(p), None, dev, None, None) == 1
+    assert lib.nsa_select_topk(C.byref(p), None, C.c_void_p(257), dev, None) == 1
+    # workspace too small or misaligned
+    assert lib.nsa_block_scores(C.byref(p), None, dev, dev, dev, ws, 16, None) == 6
+    assert lib.nsa_block_scores(C.byref(p), None, dev, dev, dev, C.c_void_p(272), 256, None) == 6
+    # shapes: block size, head dim, S
+    assert lib.nsa_block_scores(C.byref(_p(block_size=48)), None, dev, dev, dev, ws, 256, None) == 2
+    assert lib.nsa_select_topk(C.byref(_p(S=0)), None, dev, dev, None) == 1
+    assert lib.nsa_select_topk(C.byref(_p(S=300)), None, dev, dev, None) == 2
+    # THD without cu_seqlens
+    assert lib.nsa_select_topk(C.byref(pt), None, dev, dev, None) == 1
