@@ -211,7 +211,7 @@ __device__ __forceinline__ void to_mma()
 
 // The kernels' common start: the wait context, the MMA barrier and 256 TMEM
 // columns; the end: every MMA done, TMEM freed, a timeout reported.
-__device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Sync &s)
+__device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Sync &s, uint32_t cols = 256)
 {
     uint64_t *bar = (uint64_t *)misc;
     volatile int *ctx = (volatile int *)(misc + 16);
@@ -223,7 +223,7 @@ __device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Syn
         fence_barrier_init();
     }
     if (threadIdx.x < 32) {
-        tmem_alloc(slot, 256);
+        tmem_alloc(slot, cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -235,7 +235,7 @@ __device__ __forceinline__ uint32_t g_start(uint8_t *misc, const GParams &p, Syn
     return *slot;
 }
 
-__device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p)
+__device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p, uint32_t cols = 256)
 {
     // MMAs still in flight (after a timeout) complete before TMEM is freed
     if (threadIdx.x == 0 || threadIdx.x == 32)
@@ -250,7 +250,7 @@ __device__ __forceinline__ void g_end(uint32_t tmem, Sync &s, const GParams &p)
         set_error(p.err, NSA_ERR_DEVICE_TIMEOUT);
     if (threadIdx.x < 32) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, cols);
     }
 }
 
@@ -844,96 +844,201 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
 // complete at t ((j + 1) bs - 1 <= t), p = exp(scale <q, kc_j>) normalised
 // over the row's complete blocks; a token's score of block j is the sum of
 // p over the G heads of its kv head (0 for blocks not complete at t).
-// One CTA per query tile (Tq tokens x G heads): the compressed keys of the
-// blocks complete at the tile's last row go through shared memory in chunks
-// of 64 (the MMA's N); pass 1 keeps each row's running maximum and sum,
-// pass 2 forms p, stages it in shared memory (row stride 65 floats: column
-// writes by rows and row reads by columns are both conflict-free) and sums
-// each token's G rows.  S of up to 4 chunks stays in TMEM between the passes;
-// longer rows recompute it.
+// One CTA per query tile (Tq tokens x G heads).  The compressed keys of the
+// blocks complete at the tile's last row are read in chunks of 64 (the MMA's
+// N).  Up to 4 chunks (256 blocks) are resident: the q tile and every chunk
+// are loaded at once -- by TMA (bf16 with D a multiple of 64: the q tile as
+// boxes of G heads x Tq tokens, head-major rows for BHTD and token-major for
+// THD), else by per-thread copies -- all S products go out from two threads
+// and stay in TMEM; pass 1 takes each row's maximum and sum, pass 2 forms
+// p, stages it in shared memory (row stride 65 floats: writes by rows and
+// reads by columns are both conflict-free) and sums each token's G rows.
+// Longer rows walk the chunks one at a time and recompute S in pass 2.
 constexpr int kScoreCh = 64;   // compressed keys per chunk
+constexpr int kScoreBufs = 4;  // resident chunks at most
 constexpr int kPStride = 65;   // floats per staged row
 
-template <bool SPLIT>
-__global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
+__host__ __device__ inline int score_bufs(int nb)
 {
+    const int n = (nb + kScoreCh - 1) / kScoreCh;
+    return n < 1 ? 1 : n > kScoreBufs ? kScoreBufs : n;
+}
+
+// Shared-memory offsets and TMEM columns of the scores kernel.  With every
+// tile's chunks resident (nb <= 4 * 64) the staged p goes over the q and
+// chunk tiles, and the TMEM holds just the resident chunks' S.
+struct ScorePlan {
+    uint32_t pbuf_off, misc_off, tmem_cols;
+};
+__host__ __device__ inline ScorePlan score_plan(int nb, int parts, int Dp)
+{
+    const int nbuf = score_bufs(nb);
+    const bool all_resident = (nb + kScoreCh - 1) / kScoreCh <= nbuf;
+    const uint32_t tiles = (uint32_t)parts * (128 + nbuf * kScoreCh) * Dp * 2, pb = 128 * kPStride * 4;
+    ScorePlan s;
+    s.pbuf_off = all_resident && tiles >= pb ? 0u : tiles;
+    s.misc_off = s.pbuf_off + (s.pbuf_off ? pb : tiles);
+    s.tmem_cols = all_resident ? (uint32_t)(nbuf == 3 ? 256 : nbuf * kScoreCh) : (uint32_t)kScoreCh;
+    return s;
+}
+
+template <bool SPLIT, bool TMA>
+__global__ void __launch_bounds__(kThr, 1)
+    scores_gtc_kernel(const GParams p, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap kcmap)
+{
+    static_assert(!(SPLIT && TMA), "the TMA path moves bf16 tiles");
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // aligned by an offset into the shared array, so that plain accesses
+    // through these pointers stay shared-memory accesses
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const Geo &g = p.g;
-    constexpr int VEC = In<SPLIT>::VEC;
+    constexpr int VEC = In<SPLIT>::VEC, ES = In<SPLIT>::ES;
     const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1, nb = g.nbmax;
-    // plan: Q [128][Dp] | compressed-key chunk [64][Dp] (each with its low
-    // part after it) | staged p [128][kPStride] fp32 | misc
+    const int nbuf = score_bufs(nb);
+    // plan: Q [128][Dp] | nbuf chunk tiles [64][Dp] (each with its low part
+    // after it) | staged p [128][kPStride] fp32 -- over the tiles when every
+    // tile's chunks are resident (their products are done before p is
+    // staged) | misc (+48: the TMA barrier)
     const uint32_t QB = 128 * Dp * 2, CB = kScoreCh * Dp * 2;
+    const ScorePlan plan = score_plan(nb, parts, Dp);
     uint8_t *q_t = sm, *c_t = q_t + parts * QB;
-    float *pbuf = (float *)(c_t + parts * CB);
-    uint8_t *misc = (uint8_t *)(pbuf + 128 * kPStride);
+    float *pbuf = (float *)(sm + plan.pbuf_off);
+    uint8_t *misc = sm + plan.misc_off;
+    uint64_t *tbar = (uint64_t *)(misc + 48);
     Sync sy;
-    const uint32_t tmem = g_start(misc, p, sy);
+    if (TMA && threadIdx.x == 0) {
+        mbar_init(tbar, 1);
+        prefetch_tmap(&qmap);
+        prefetch_tmap(&kcmap);
+    }
+    const uint32_t tmem = g_start(misc, p, sy, plan.tmem_cols);  // (its barrier-init fence and sync cover tbar too)
+    uint32_t tphase = 0;
     const int r = threadIdx.x;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
-    zero_smem(sm, parts * (QB + CB));
+    if (g.D < Dp)  // zero padding columns (every other byte is written below)
+        zero_smem(sm, (int)(nbuf * parts * CB + parts * QB));
+    __syncthreads();
+    // the tile's rows: head-major (row = head * Tq + token) where the BHTD
+    // TMA box puts them, else token-major
+    const bool head_major = TMA && !g.thd;
     int tl, hh;
-    qrow(G, r, tl, hh);
+    if (head_major) {
+        tl = r % Tq;
+        hh = r / Tq;
+    } else {
+        qrow(G, r, tl, hh);
+    }
     const bool rvalid = r < nrows && tl < nvalid;
     const int t = t0 + tl;
-    const int nc = rvalid ? (t + 1) / g.bs : 0;                      // the row's complete blocks
-    const int ncmax = nvalid > 0 ? (t0 + nvalid) / g.bs : 0;           // ... of the tile's last row
+    const int nc = rvalid ? (t + 1) / g.bs : 0;               // the row's complete blocks
+    const int ncmax = nvalid > 0 ? (t0 + nvalid) / g.bs : 0;  // ... of the tile's last row
     const int nch = (ncmax + kScoreCh - 1) / kScoreCh;
-    const bool resident = nch <= 4;
+    const bool resident = nch <= nbuf;
     const uint32_t qs = smem_u32(q_t), cs = smem_u32(c_t);
-    // the row's q, 16 vectors at a time
-    {
-        const int64_t qo = rvalid ? q_off(g, b, kvh * G + hh, t) : 0;
-        for (int i0 = 0; i0 * VEC < g.D; i0 += kRowVec) {
-            uint4 v[kRowVec];
-#pragma unroll
-            for (int i = 0; i < kRowVec; ++i) {
-                const int c = (i0 + i) * VEC;
-                v[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (rvalid && c < g.D)
-                    v[i] = __ldg((const uint4 *)((const uint8_t *)p.q + (qo + c) * In<SPLIT>::ES));
-            }
-#pragma unroll
-            for (int i = 0; i < kRowVec; ++i)
-                if ((i0 + i) * VEC < g.D)
-                    put_vec<SPLIT>(qs, 128, QB, r, (i0 + i) * VEC, v[i]);
-        }
-    }
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, nvec = kScoreCh * nv;
-    const uint8_t *kc_bg = (const uint8_t *)p.k + (int64_t)(b * g.Hkv + kvh) * nb * g.D * In<SPLIT>::ES;
-    // chunk c of the compressed keys into the chunk tile, 8 vectors a thread at a time
-    auto load_chunk = [&](int c) {
-        for (int e0 = 0; e0 < nvec; e0 += kBlkVec * kThr) {
-            uint4 v[kBlkVec];
-#pragma unroll
-            for (int i = 0; i < kBlkVec; ++i) {
-                const int e = e0 + threadIdx.x + i * kThr, row = e >> lnv, j = c * kScoreCh + row;
-                v[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < nvec && j < nb)
-                    v[i] = __ldg((const uint4 *)(kc_bg + ((int64_t)j * g.D + (e & (nv - 1)) * VEC) * In<SPLIT>::ES));
+    const int halves = g.D / 64;  // TMA boxes per row (64 columns each)
+    const uint8_t *kc_bg = (const uint8_t *)p.k + (int64_t)(b * g.Hkv + kvh) * nb * g.D * ES;
+    // chunk c of the compressed keys into chunk tile `buf` (rows past nb read as zeros)
+    auto fetch_chunk = [&](int c, int buf) {
+        const uint32_t dst = cs + buf * parts * CB;
+        if constexpr (TMA) {
+            if (threadIdx.x == 0)
+                for (int h = 0; h < halves; ++h)
+                    tma_load_3d(c_t + buf * CB + h * (kScoreCh * 128), &kcmap, tbar, h * 64, c * kScoreCh,
+                                b * g.Hkv + kvh);
+        } else if constexpr (!SPLIT) {
+            for (int e = threadIdx.x; e < nvec; e += kThr) {
+                const int row = e >> lnv, j = c * kScoreCh + row, col = (e & (nv - 1)) * VEC;
+                cp_async_16(dst + swz(row, col, kScoreCh), kc_bg + ((int64_t)(j < nb ? j : 0) * g.D + col) * ES,
+                            j < nb ? 16u : 0u);
             }
+        } else {
+            for (int e0 = 0; e0 < nvec; e0 += kBlkVec * kThr) {
+                uint4 v[kBlkVec];
 #pragma unroll
-            for (int i = 0; i < kBlkVec; ++i) {
-                const int e = e0 + threadIdx.x + i * kThr;
-                if (e < nvec)
-                    put_vec<SPLIT>(cs, kScoreCh, CB, e >> lnv, (e & (nv - 1)) * VEC, v[i]);
+                for (int i = 0; i < kBlkVec; ++i) {
+                    const int e = e0 + threadIdx.x + i * kThr, j = c * kScoreCh + (e >> lnv);
+                    v[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (e < nvec && j < nb)
+                        v[i] = __ldg((const uint4 *)(kc_bg + ((int64_t)j * g.D + (e & (nv - 1)) * VEC) * ES));
+                }
+#pragma unroll
+                for (int i = 0; i < kBlkVec; ++i) {
+                    const int e = e0 + threadIdx.x + i * kThr;
+                    if (e < nvec)
+                        put_vec<SPLIT>(dst, kScoreCh, CB, e >> lnv, (e & (nv - 1)) * VEC, v[i]);
+                }
             }
         }
     };
-    const uint32_t idS = idesc_bf16(128, kScoreCh, false, false);
+    // thread 0 announces the bytes the TMA loads that follow will bring
+    bool tma_pending = false;  // (thread 0) loads announced and not yet seen landing
+    auto tma_expect = [&](int chunks, bool with_q) {
+        if (TMA && threadIdx.x == 0) {
+            mbar_arrive_expect_tx(tbar, (uint32_t)(halves * (chunks * kScoreCh * 128 + (with_q ? nrows * 128 : 0))));
+            tma_pending = true;
+        }
+    };
+    // every load issued so far has landed (bounded wait on the TMA barrier)
+    auto loads_done = [&]() -> bool {
+        if constexpr (TMA) {
+            const bool got = mbar_wait(tbar, tphase, sy.ctx);
+            if (got) {
+                tphase ^= 1;
+                tma_pending = false;
+            }
+            return __syncthreads_and(got) != 0;
+        } else {
+            if constexpr (!SPLIT) {
+                cp_async_commit();
+                cp_async_wait<0>();
+            }
+            return true;
+        }
+    };
     bool ok = true;
-    // pass 1: the row's maximum m and sum l of exp2(scale_l2 s) over its complete blocks
+    // the q tile (rows past the tile's tokens are zeros or unused)
+    if (resident)
+        tma_expect(nch, true);
+    else
+        tma_expect(1, true);
+    if constexpr (TMA) {
+        if (threadIdx.x == 0)
+            for (int h = 0; h < halves; ++h) {
+                if (g.thd)
+                    tma_load_3d(q_t + h * (128 * 128), &qmap, tbar, h * 64, kvh * G, g.cu[b] + t0);
+                else
+                    tma_load_4d(q_t + h * (128 * 128), &qmap, tbar, h * 64, t0, kvh * G, b);
+            }
+    } else {
+        const int64_t qo = rvalid ? q_off(g, b, kvh * G + hh, t) : 0;
+        if constexpr (!SPLIT) {
+            for (int c = 0; c < g.D; c += VEC)
+                cp_async_16(qs + swz(r, c, 128), (const uint8_t *)p.q + (qo + c) * ES, rvalid ? 16u : 0u);
+        } else {
+            for (int i0 = 0; i0 * VEC < g.D; i0 += kRowVec) {
+                uint4 v[kRowVec];
+#pragma unroll
+                for (int i = 0; i < kRowVec; ++i) {
+                    const int c = (i0 + i) * VEC;
+                    v[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (rvalid && c < g.D)
+                        v[i] = __ldg((const uint4 *)((const uint8_t *)p.q + (qo + c) * ES));
+                }
+#pragma unroll
+                for (int i = 0; i < kRowVec; ++i)
+                    if ((i0 + i) * VEC < g.D)
+                        put_vec<SPLIT>(qs, 128, QB, r, (i0 + i) * VEC, v[i]);
+            }
+        }
+    }
+    const uint32_t idS = idesc_bf16(128, kScoreCh, false, false);
     float m = -INFINITY, l = 0.f;
-    for (int c = 0; c < nch && ok; ++c) {
-        const uint32_t col = resident ? c * kScoreCh : 0;
-        load_chunk(c);
-        to_mma();
-        if (r == 0)
-            product<SPLIT>(tmem + col, qs, 128, QB, cs, kScoreCh, CB, idS, Dp / 16, false);
-        if (!(ok = commit_wait(sy)))
-            break;
+    // pass 1 on columns [col, col + 64) of TMEM holding chunk c: the row's
+    // running maximum m and sum l of exp2(scale_l2 s) over its complete blocks
+    auto stats = [&](int c, uint32_t col) {
 #pragma unroll
         for (int c1 = 0; c1 < kScoreCh; c1 += 32) {
             float s[32];
@@ -954,6 +1059,37 @@ __global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
                 m = mn;
             }
         }
+    };
+    // S of chunk c from chunk tile `buf` into TMEM columns [col, col + 64)
+    auto s_product = [&](int c, int buf, uint32_t col) {
+        product<SPLIT>(tmem + col, qs, 128, QB, cs + buf * parts * CB, kScoreCh, CB, idS, Dp / 16, false);
+    };
+    if (resident) {
+        for (int c = 0; c < nch; ++c)
+            fetch_chunk(c, c);
+        ok = loads_done();
+        to_mma();
+        if (ok && (r == 0 || r == kIssuer2))  // chunks split between the two issuing threads
+            for (int c = r == 0 ? 0 : 1; c < nch; c += 2)
+                s_product(c, c, c * kScoreCh);
+        ok = commit_wait(sy) && ok;
+        for (int c = 0; c < nch && ok; ++c)
+            stats(c, c * kScoreCh);
+    } else {
+        for (int c = 0; c < nch && ok; ++c) {
+            if (c > 0)
+                tma_expect(1, false);
+            fetch_chunk(c, 0);
+            ok = loads_done();
+            if (!ok)
+                break;
+            to_mma();
+            if (r == 0)
+                s_product(c, 0, 0);
+            ok = commit_wait(sy);
+            if (ok)
+                stats(c, 0);
+        }
     }
     const float lse2 = l > 0.f ? m + log2f(l) : INFINITY;  // +inf: no complete block, p = 0
     // pass 2: p per row, staged; each token's G rows summed into its scores
@@ -961,11 +1097,16 @@ __global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
         uint32_t col = c * kScoreCh;
         if (!resident) {
             col = 0;
-            load_chunk(c);
+            tma_expect(1, false);
+            fetch_chunk(c, 0);
+            ok = loads_done();
+            if (!ok)
+                break;
             to_mma();
             if (r == 0)
-                product<SPLIT>(tmem, qs, 128, QB, cs, kScoreCh, CB, idS, Dp / 16, false);
-            if (!(ok = commit_wait(sy)))
+                s_product(c, 0, 0);
+            ok = commit_wait(sy);
+            if (!ok)
                 break;
         }
 #pragma unroll
@@ -977,14 +1118,18 @@ __global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
                 pbuf[r * kPStride + c1 + x] = c * kScoreCh + c1 + x < nc ? ex2(s[x] * g.scale_l2 - lse2) : 0.f;
         }
         __syncthreads();
-        for (int o = threadIdx.x; o < nvalid * kScoreCh; o += kThr) {
-            const int tk = o / kScoreCh, jj = o % kScoreCh, j = c * kScoreCh + jj;
-            if (j >= nb)
-                continue;
-            float sum = 0.f;
-            for (int h2 = 0; h2 < G; ++h2)
-                sum += pbuf[(tk * G + h2) * kPStride + jj];
-            p.scores[index_row(g, b, kvh, t0 + tk) * nb + j] = sum;
+        {
+            // thread: column jj, tokens tk0, tk0 + 2, ...
+            const int jj = threadIdx.x % kScoreCh, j = c * kScoreCh + jj;
+            const int rs = head_major ? Tq : 1, ts = head_major ? 1 : G;  // row steps per head / token
+            if (j < nb)
+                for (int tk = threadIdx.x / kScoreCh; tk < nvalid; tk += kThr / kScoreCh) {
+                    const float *col = pbuf + tk * ts * kPStride + jj;
+                    float sum = 0.f;
+                    for (int h2 = 0; h2 < G; ++h2)
+                        sum += col[h2 * rs * kPStride];
+                    p.scores[index_row(g, b, kvh, t0 + tk) * nb + j] = sum;
+                }
         }
         tc_fence_before();  // this chunk's TMEM reads and staged rows are done before the next
         __syncthreads();
@@ -996,7 +1141,15 @@ __global__ void __launch_bounds__(kThr, 1) scores_gtc_kernel(const GParams p)
         for (int o = threadIdx.x; rest > 0 && o < nvalid * rest; o += kThr)
             p.scores[index_row(g, b, kvh, t0 + o / rest) * nb + j0 + o % rest] = 0.f;
     }
-    g_end(tmem, sy, p);
+    if constexpr (!TMA && !SPLIT)
+        cp_async_wait<0>();  // nothing left in flight after an early exit
+    if (TMA && tma_pending) {
+        // (thread 0, after a wait gave up) the TMA loads already issued land
+        // before the CTA exits, within the wait limit again
+        volatile int never[2] = {0, sy.ctx[1]};
+        mbar_wait(tbar, tphase, never);
+    }
+    g_end(tmem, sy, p, plan.tmem_cols);
 }
 
 constexpr int kSmemLimit = 232448;
@@ -1077,11 +1230,29 @@ cudaError_t launch_scores_gtc(const Geo &g, const void *q, const void *kc, float
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 + parts * (size_t)(128 + kScoreCh) * p.Dp * 2 + 128 * kPStride * 4 + 64;
+    const size_t smem = 1024 + (size_t)score_plan(g.nbmax, parts, p.Dp).misc_off + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
-    return launch_g(dtype == NSA_DTYPE_F32 ? scores_gtc_kernel<true> : scores_gtc_kernel<false>, p.ntiles, smem, p,
-                    st);
+    CUtensorMap qmap, kcmap;
+    memset(&qmap, 0, sizeof(qmap));
+    memset(&kcmap, 0, sizeof(kcmap));
+    // TMA tiles for bf16 with D a multiple of 64: the q tile as one box of
+    // G heads x Tq tokens per 64 columns, a chunk of 64 compressed keys
+    bool tma = dtype == NSA_DTYPE_BF16 && g.D % 64 == 0;
+    if (tma) {
+        const uint64_t dims[3] = {(uint64_t)g.D, (uint64_t)g.nbmax, (uint64_t)g.B * g.Hkv};
+        const uint64_t strides[2] = {(uint64_t)g.D * 2, (uint64_t)g.nbmax * g.D * 2};
+        const uint32_t box[3] = {64, (uint32_t)kScoreCh, 1};
+        tma = make_tmap(&qmap, q, g, g.Hq, Tq, g.G, g.sq) && make_tmap_3d(&kcmap, kc, dims, strides, box);
+    }
+    void (*k)(const GParams, const CUtensorMap, const CUtensorMap) =
+        dtype == NSA_DTYPE_F32 ? scores_gtc_kernel<true, false>
+        : tma                  ? scores_gtc_kernel<false, true>
+                               : scores_gtc_kernel<false, false>;
+    if (!smem_ok(k, smem))
+        return cudaErrorInvalidValue;
+    k<<<p.ntiles, kThr, smem, st>>>(p, qmap, kcmap);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const void *v, const int *idx, void *o,

@@ -24,7 +24,7 @@ int grid_of(int64_t n, int per_block, int cap)
     return (int)(b < 1 ? 1 : b > cap ? cap : b);
 }
 
-// 16-byte vectors of the element type: 8 bf16 or 4 fp32
+// 16-byte vectors of the element type (8 bf16 or 4 fp32), added into fp32 sums
 template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
@@ -37,16 +37,6 @@ template <> struct Vec<__nv_bfloat16> {
             acc[2 * i + 1] += __uint_as_float(u[i] & 0xffff0000u);
         }
     }
-    static __device__ __forceinline__ uint4 pack(const float *x)
-    {
-        uint32_t u[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-            u[i] = *reinterpret_cast<const uint32_t *>(&h);
-        }
-        return make_uint4(u[0], u[1], u[2], u[3]);
-    }
 };
 template <> struct Vec<float> {
     static constexpr int N = 4;
@@ -57,53 +47,67 @@ template <> struct Vec<float> {
         acc[2] += __uint_as_float(w.z);
         acc[3] += __uint_as_float(w.w);
     }
-    static __device__ __forceinline__ uint4 pack(const float *x)
-    {
-        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
-    }
 };
 
 // kc[b, g, j, :] = the mean of keys j*bs .. j*bs + bs - 1 of sequence b, kv
 // head g, for blocks complete in the sequence; zero rows for the others.  One
-// thread per 16-byte vector of kc (consecutive threads: consecutive vectors
-// of a row, so a warp reads whole key rows).
+// CTA per block: thread (group, v) sums 16-byte vector v of the rows group,
+// group + groups, ... (all its loads in flight), then the groups' partial
+// sums meet in shared memory.
 template <typename T> __global__ void __launch_bounds__(kThreads) compress_mean_kernel(const Geo g, const T *k, T *kc)
 {
     constexpr int N = Vec<T>::N;
-    const int nv = g.D / N, nb = g.nbmax;
-    const int64_t total = (int64_t)g.B * g.Hkv * nb * nv;
+    __shared__ float part[kThreads * N];
+    const int nv = g.D / N, groups = kThreads / nv;  // nv divides kThreads (D / N is 4 .. 32)
+    const int v = threadIdx.x % nv, grp = threadIdx.x / nv;
+    const int nb = g.nbmax;
+    const int64_t nrows = (int64_t)g.B * g.Hkv * nb;
     const float inv = 1.0f / (float)g.bs;  // bs is a power of two: exact
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int v = (int)(e % nv);
-        const int64_t row = e / nv;  // (b * Hkv + kvh) * nb + j
+    for (int64_t row = blockIdx.x; row < nrows; row += gridDim.x) {  // row = (b * Hkv + kvh) * nb + j
         const int j = (int)(row % nb), bg = (int)(row / nb), b = bg / g.Hkv, kvh = bg % g.Hkv;
+        const bool complete = (int64_t)(j + 1) * g.bs <= seq_len(g, b);
         float acc[N];
 #pragma unroll
         for (int i = 0; i < N; ++i)
             acc[i] = 0.f;
-        if ((int64_t)(j + 1) * g.bs <= seq_len(g, b)) {
-            for (int i = 0; i < g.bs; ++i)
+        if (complete) {
+#pragma unroll 4
+            for (int i = grp; i < g.bs; i += groups)
                 Vec<T>::add(__ldg((const uint4 *)(k + kv_off(g, b, kvh, j * g.bs + i) + v * N)), acc);
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-                acc[i] *= inv;
         }
-        *(uint4 *)(kc + row * g.D + v * N) = Vec<T>::pack(acc);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            part[(grp * nv + v) * N + i] = acc[i];
+        __syncthreads();
+        if (threadIdx.x < g.D) {  // element d: vector d / N, lane d % N of it
+            const int d = threadIdx.x;
+            float sum = 0.f;
+            for (int q = 0; q < groups; ++q)
+                sum += part[(q * nv + d / N) * N + d % N];
+            kc[row * g.D + d] = (T)(sum * inv);
+        }
+        __syncthreads();
     }
 }
 
-// (x, i) ranks before (y, j): larger score first, then smaller block id;
-// NaN scores were mapped to -infinity by the caller
-__device__ __forceinline__ bool ranks_before(float x, int i, float y, int j) { return x > y || (x == y && i < j); }
+// The selection order as one unsigned key: a larger score gives a larger
+// key; NaN counts as -infinity and -0 as +0 (they compare equal); every key
+// is above 0, which stands for "no block".
+__device__ __forceinline__ uint32_t order_key(float x)
+{
+    x = isnan(x) ? -INFINITY : x + 0.0f;  // -0 + 0 = +0
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
-__device__ __forceinline__ float rank_key(float x) { return isnan(x) ? -INFINITY : x; }
+constexpr int kTopRegs = 8;  // scores a lane holds in registers: rows of up to 256 blocks
 
 // One warp per index row R (the index's own row order: BHTD (b*Hkv + kvh)*T
 // + t, THD token*Hkv + kvh; the scores use the same rows, nb = nbmax each).
-// Each of the S - 1 rounds takes the best complete block that ranks after
-// the previous round's pick (a strict total order, so no block is taken
-// twice): every lane scans its blocks j = lane, lane + 32, ..., then a
-// butterfly of shuffles keeps the best.
+// Round s takes the best complete block (largest key, then smallest id) that
+// ranks after round s-1's pick -- a strict total order, so no block is taken
+// twice: each lane finds its own best, then a warp max of the keys and a
+// warp min of the ids among the lanes holding that key.
 __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, const float *scores, int *idx)
 {
     const int lane = threadIdx.x & 31;
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, cons
         int t;
         if (g.thd) {
             const int tok = (int)(R / g.Hkv);
-            int lo = 0, hi = g.B - 1;  // the sequence holding token tok: cu[lo] <= tok < cu[lo + 1]
+            int lo = 0, hi = g.B - 1;  // the sequence holding token tok: the last b with cu[b] <= tok
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (g.cu[mid] <= tok)
@@ -130,37 +134,49 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, cons
         const float *sc = scores + R * nb;
         int *out = idx + R * S;
         const int own = t / g.bs, nc = (t + 1) / g.bs;
+        const bool in_regs = nc <= 32 * kTopRegs;
+        uint32_t key[kTopRegs];
+#pragma unroll
+        for (int i = 0; i < kTopRegs; ++i) {
+            const int j = lane + 32 * i;
+            key[i] = (in_regs && j < nc && j != own) ? order_key(__ldg(sc + j)) : 0u;
+        }
         if (lane == 0)
             out[0] = own;
-        float pv = INFINITY;  // the previous pick; (+inf, -1) ranks before every block
+        uint32_t pk = 0xffffffffu;  // the previous pick: above every key
         int pj = -1, filled = 1;
         for (int s = 1; s < S; ++s) {
-            float bv = -INFINITY;
-            int bj = -1;
-            for (int j = lane; j < nc; j += 32) {
-                if (j == own)
-                    continue;
-                const float v = rank_key(__ldg(sc + j));
-                if (ranks_before(pv, pj, v, j) && (bj < 0 || ranks_before(v, j, bv, bj))) {
-                    bv = v;
-                    bj = j;
-                }
-            }
+            uint32_t bk = 0u;
+            int bj = 0x7fffffff;
+            if (in_regs) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
-                if (oj >= 0 && (bj < 0 || ranks_before(ov, oj, bv, bj))) {
-                    bv = ov;
-                    bj = oj;
+                for (int i = 0; i < kTopRegs; ++i) {  // ids ascend with i: the first of equal keys wins
+                    const int j = lane + 32 * i;
+                    const uint32_t kk = key[i];
+                    if (kk > bk && (kk < pk || (kk == pk && j > pj))) {
+                        bk = kk;
+                        bj = j;
+                    }
+                }
+            } else {
+                for (int j = lane; j < nc; j += 32) {
+                    if (j == own)
+                        continue;
+                    const uint32_t kk = order_key(__ldg(sc + j));
+                    if (kk > bk && (kk < pk || (kk == pk && j > pj))) {
+                        bk = kk;
+                        bj = j;
+                    }
                 }
             }
-            if (bj < 0)  // warp-uniform after the butterfly: no complete block left
+            const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+            if (wk == 0u)  // no complete block left (warp-uniform)
                 break;
+            const int wj = (int)__reduce_min_sync(0xffffffffu, (unsigned)(bk == wk ? bj : 0x7fffffff));
             if (lane == 0)
-                out[s] = bj;
-            pv = bv;
-            pj = bj;
+                out[s] = wj;
+            pk = wk;
+            pj = wj;
             filled = s + 1;
         }
         for (int s = filled + lane; s < S; s += 32)
@@ -172,8 +188,7 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, cons
 
 cudaError_t launch_compress_mean(const Geo &g, const void *k, void *kc, int dtype, cudaStream_t st)
 {
-    const int64_t total = (int64_t)g.B * g.Hkv * g.nbmax * (g.D / (dtype == NSA_DTYPE_BF16 ? 8 : 4));
-    const int grid = grid_of(total, kThreads, 152 * 16);
+    const int grid = grid_of((int64_t)g.B * g.Hkv * g.nbmax, 1, 152 * 8);
     if (dtype == NSA_DTYPE_BF16)
         compress_mean_kernel<__nv_bfloat16>
             <<<grid, kThreads, 0, st>>>(g, (const __nv_bfloat16 *)k, (__nv_bfloat16 *)kc);

@@ -131,4 +131,18 @@ bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d(CUtensorMap *map, const void *base, const uint64_t dims[3], const uint64_t strides_bytes[2],
+                  const uint32_t box[3])
+{
+    auto fn = encode_fn();
+    if (!fn || dims[0] == 0 || dims[1] == 0 || dims[2] == 0)
+        return false;
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]}, st[2] = {strides_bytes[0], strides_bytes[1]};
+    cuuint32_t bx[3] = {box[0], box[1], box[2]}, estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, st, bx, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace nsa

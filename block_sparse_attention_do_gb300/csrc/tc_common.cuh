@@ -50,6 +50,11 @@ __host__ __device__ inline int rg_off(int r, int half) { return (r >> 3) * kRgSt
 // folded, needs s.b = T * s.t) or the packed row (THD).
 bool make_tmap_rows(CUtensorMap *map, const void *base, const Geo &g, int H, int G, const Strides &s, int bt);
 
+// A plain 3-D bf16 tensor map, 128B-swizzled (dims and box innermost first,
+// byte strides of dims 1 and 2); rows past an end read as zeros.
+bool make_tmap_3d(CUtensorMap *map, const void *base, const uint64_t dims[3], const uint64_t strides_bytes[2],
+                  const uint32_t box[3]);
+
 // Whether the row-gather map of a BHTD tensor with these strides can be
 // built, and in which form (bt: batch folded into the token index).
 inline bool rows_map_form(const Geo &g, int H, const Strides &s, int &bt)
