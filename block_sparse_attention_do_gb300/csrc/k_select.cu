@@ -100,25 +100,26 @@ __device__ __forceinline__ uint32_t order_key(float x)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kTopRegs = 8;  // scores a lane holds in registers: rows of up to 256 blocks
-
 // One warp per index row R (the index's own row order: BHTD (b*Hkv + kvh)*T
 // + t, THD token*Hkv + kvh; the scores use the same rows, nb = nbmax each).
 // Round s takes the best complete block (largest key, then smallest id) that
 // ranks after round s-1's pick -- a strict total order, so no block is taken
 // twice: each lane finds its own best, then a warp max of the keys and a
-// warp min of the ids among the lanes holding that key.
-__global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, const float *scores, int *idx)
+// warp min of the ids among the lanes holding that key.  Rows of up to
+// 32 * REGS blocks keep their keys in registers (REGS per lane, block
+// lane + 32 i); REGS = 0 reads every round's keys from memory.
+template <int REGS> __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, const float *scores, int *idx)
 {
+    constexpr int R = REGS > 0 ? REGS : 1;
     const int lane = threadIdx.x & 31;
     const int64_t nrows = (int64_t)g.ntok * g.Hkv;
     const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int nb = g.nbmax, S = g.S;
-    for (int64_t R = warp0; R < nrows; R += nwarps) {
+    for (int64_t row = warp0; row < nrows; row += nwarps) {
         int t;
         if (g.thd) {
-            const int tok = (int)(R / g.Hkv);
+            const int tok = (int)(row / g.Hkv);
             int lo = 0, hi = g.B - 1;  // the sequence holding token tok: the last b with cu[b] <= tok
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -129,17 +130,16 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, cons
             }
             t = tok - g.cu[lo];
         } else {
-            t = (int)(R % g.T);
+            t = (int)(row % g.T);
         }
-        const float *sc = scores + R * nb;
-        int *out = idx + R * S;
+        const float *sc = scores + row * nb;
+        int *out = idx + row * S;
         const int own = t / g.bs, nc = (t + 1) / g.bs;
-        const bool in_regs = nc <= 32 * kTopRegs;
-        uint32_t key[kTopRegs];
+        uint32_t key[R];
 #pragma unroll
-        for (int i = 0; i < kTopRegs; ++i) {
+        for (int i = 0; i < R; ++i) {
             const int j = lane + 32 * i;
-            key[i] = (in_regs && j < nc && j != own) ? order_key(__ldg(sc + j)) : 0u;
+            key[i] = (REGS > 0 && j < nc && j != own) ? order_key(__ldg(sc + j)) : 0u;
         }
         if (lane == 0)
             out[0] = own;
@@ -148,9 +148,9 @@ __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, cons
         for (int s = 1; s < S; ++s) {
             uint32_t bk = 0u;
             int bj = 0x7fffffff;
-            if (in_regs) {
+            if constexpr (REGS > 0) {
 #pragma unroll
-                for (int i = 0; i < kTopRegs; ++i) {  // ids ascend with i: the first of equal keys wins
+                for (int i = 0; i < R; ++i) {  // ids ascend with i: the first of equal keys wins
                     const int j = lane + 32 * i;
                     const uint32_t kk = key[i];
                     if (kk > bk && (kk < pk || (kk == pk && j > pj))) {
@@ -201,7 +201,18 @@ cudaError_t launch_select_topk(const Geo &g, const float *scores, int *idx, cuda
 {
     const int64_t rows = (int64_t)g.ntok * g.Hkv;
     const int grid = grid_of(rows, kThreads / 32, 152 * 16);
-    select_topk_kernel<<<grid, kThreads, 0, st>>>(g, scores, idx);
+    // a row's complete blocks number at most nbmax: the smallest register set that holds them
+    const int nb = g.nbmax;
+    if (nb <= 32)
+        select_topk_kernel<1><<<grid, kThreads, 0, st>>>(g, scores, idx);
+    else if (nb <= 64)
+        select_topk_kernel<2><<<grid, kThreads, 0, st>>>(g, scores, idx);
+    else if (nb <= 128)
+        select_topk_kernel<4><<<grid, kThreads, 0, st>>>(g, scores, idx);
+    else if (nb <= 256)
+        select_topk_kernel<8><<<grid, kThreads, 0, st>>>(g, scores, idx);
+    else
+        select_topk_kernel<0><<<grid, kThreads, 0, st>>>(g, scores, idx);
     return cudaGetLastError();
 }
 

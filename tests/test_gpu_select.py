@@ -150,6 +150,16 @@ def test_select_topk_bit_exact(S, levels, nan_frac):
     np.testing.assert_array_equal(got, ref)
 
 
+@pytest.mark.parametrize("T", [900, 3000])  # rows of up to 57 and 188 blocks
+def test_select_topk_row_lengths(T):
+    B, Hkv, bs, S = 1, 2, 16, 16
+    nb = (T + bs - 1) // bs
+    sc = inputs.make_block_scores((B, Hkv, T, nb), seed=31, levels=8, nan_frac=0.02)
+    got = api.select_topk(sc.to(DEV), bs, S).cpu().numpy()
+    ref = oracle.select_topk(sc, bs, S)
+    np.testing.assert_array_equal(got, ref)
+
+
 def test_select_topk_packed_and_long_rows():
     lens = [1000, 3, 64, 4200]
     Hkv, bs, S = 2, 16, 24  # up to 263 blocks a row
