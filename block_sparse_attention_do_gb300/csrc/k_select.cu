@@ -102,12 +102,13 @@ __device__ __forceinline__ uint32_t order_key(float x)
 
 // One warp per index row R (the index's own row order: BHTD (b*Hkv + kvh)*T
 // + t, THD token*Hkv + kvh; the scores use the same rows, nb = nbmax each).
-// Round s takes the best complete block (largest key, then smallest id) that
-// ranks after round s-1's pick -- a strict total order, so no block is taken
-// twice: each lane finds its own best, then a warp max of the keys and a
-// warp min of the ids among the lanes holding that key.  Rows of up to
-// 32 * REGS blocks keep their keys in registers (REGS per lane, block
-// lane + 32 i); REGS = 0 reads every round's keys from memory.
+// Round s takes the best complete block left (largest key, then smallest
+// id): a warp max of the lanes' best keys and a warp min of the ids among
+// the lanes holding that key.  Rows of up to 32 * REGS blocks keep their
+// keys in registers (REGS per lane, block lane + 32 i; a taken block's key
+// is cleared); REGS = 0 reads every round's keys from memory and takes the
+// best block that ranks after the previous round's pick (a strict total
+// order, so no block is taken twice).
 template <int REGS> __global__ void __launch_bounds__(kThreads) select_topk_kernel(const Geo g, const float *scores, int *idx)
 {
     constexpr int R = REGS > 0 ? REGS : 1;
@@ -143,22 +144,46 @@ template <int REGS> __global__ void __launch_bounds__(kThreads) select_topk_kern
         }
         if (lane == 0)
             out[0] = own;
-        uint32_t pk = 0xffffffffu;  // the previous pick: above every key
-        int pj = -1, filled = 1;
-        for (int s = 1; s < S; ++s) {
+        int filled = 1;
+        if constexpr (REGS > 0) {
+            // each lane's best remaining key (ids ascend with i, so the first
+            // of equal keys -- the smallest id -- wins); only the lane whose
+            // block was taken looks again
             uint32_t bk = 0u;
             int bj = 0x7fffffff;
-            if constexpr (REGS > 0) {
+            auto lane_best = [&]() {
+                bk = 0u;
+                bj = 0x7fffffff;
 #pragma unroll
-                for (int i = 0; i < R; ++i) {  // ids ascend with i: the first of equal keys wins
-                    const int j = lane + 32 * i;
-                    const uint32_t kk = key[i];
-                    if (kk > bk && (kk < pk || (kk == pk && j > pj))) {
-                        bk = kk;
-                        bj = j;
+                for (int i = 0; i < R; ++i)
+                    if (key[i] > bk) {
+                        bk = key[i];
+                        bj = lane + 32 * i;
                     }
+            };
+            lane_best();
+            for (int s = 1; s < S; ++s) {
+                const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+                if (wk == 0u)  // no complete block left (warp-uniform)
+                    break;
+                const int wj = (int)__reduce_min_sync(0xffffffffu, (unsigned)(bk == wk ? bj : 0x7fffffff));
+                if (lane == 0)
+                    out[s] = wj;
+                filled = s + 1;
+                if (lane == (wj & 31)) {
+#pragma unroll
+                    for (int i = 0; i < R; ++i)
+                        if (i == (wj >> 5))
+                            key[i] = 0u;
+                    lane_best();
                 }
-            } else {
+            }
+        } else {
+            uint32_t pk = 0xffffffffu;  // the previous pick: above every key
+            int pj = -1;
+            for (int s = 1; s < S; ++s) {
+                uint32_t bk = 0u;
+                int bj = 0x7fffffff;
                 for (int j = lane; j < nc; j += 32) {
                     if (j == own)
                         continue;
@@ -168,16 +193,16 @@ template <int REGS> __global__ void __launch_bounds__(kThreads) select_topk_kern
                         bj = j;
                     }
                 }
+                const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+                if (wk == 0u)
+                    break;
+                const int wj = (int)__reduce_min_sync(0xffffffffu, (unsigned)(bk == wk ? bj : 0x7fffffff));
+                if (lane == 0)
+                    out[s] = wj;
+                pk = wk;
+                pj = wj;
+                filled = s + 1;
             }
-            const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
-            if (wk == 0u)  // no complete block left (warp-uniform)
-                break;
-            const int wj = (int)__reduce_min_sync(0xffffffffu, (unsigned)(bk == wk ? bj : 0x7fffffff));
-            if (lane == 0)
-                out[s] = wj;
-            pk = wk;
-            pj = wj;
-            filled = s + 1;
         }
         for (int s = filled + lane; s < S; s += 32)
             out[s] = -1;
