@@ -539,23 +539,75 @@ def run_ours(args):
         h2d = sum(x.numel() * x.element_size() for x in host_in)
         d2h = sum(x.numel() * x.element_size() for x in host_out)
         n_e2e = max(3, min(K, 20))
+        # (1) one step at a time on one stream: copy in, backward, copy out
         e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(n_e2e + 2)]
         for i in range(n_e2e + 2):
             e_ev[i][0].record(st)
             for hsrc, ddst in zip(host_in, dev_in):
                 ddst.copy_(hsrc, non_blocking=True)
-            dq_, dk_, dv_ = api.sel_bwd(*dev_in[:6], dev_in[6], bs, ws=ws_b, out=outs)
+            api.sel_bwd(*dev_in[:6], dev_in[6], bs, ws=ws_b, out=outs)
             for dsrc, hdst in zip(outs, host_out):
                 hdst.copy_(dsrc, non_blocking=True)
             e_ev[i][1].record(st)
         torch.cuda.synchronize()
-        e_ms = sum(a.elapsed_time(b) for a, b in e_ev[2:])  # first two are warm-up
+        serial_ms = sum(a.elapsed_time(b) for a, b in e_ev[2:]) / n_e2e  # first two are warm-up
+        # (2) the same steps as a pipeline: step i's inputs go in on a copy
+        # stream while step i-1 computes and step i-2's gradients come out on
+        # another; two sets of device buffers alternate.  Every step still
+        # copies all its inputs in and its gradients out inside the timed region.
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        dev_in2 = [dev_in, [torch.empty_like(x) for x in dev_in]]
+        outs2 = [list(outs), [torch.empty_like(x) for x in outs]]
+        host_out2 = [host_out, [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]]
+
+        def pipeline(n):
+            done_c = [None, None]  # per buffer set: the compute that last read / wrote it
+            done_o = [None, None]  # per buffer set: the copy-out that last read its gradients
+            for i in range(n):
+                j = i % 2
+                ev_in = torch.cuda.Event()
+                with torch.cuda.stream(s_in):
+                    if done_c[j] is not None:
+                        s_in.wait_event(done_c[j])
+                    for hsrc, ddst in zip(host_in, dev_in2[j]):
+                        ddst.copy_(hsrc, non_blocking=True)
+                    ev_in.record(s_in)
+                st.wait_event(ev_in)
+                if done_o[j] is not None:
+                    st.wait_event(done_o[j])
+                api.sel_bwd(*dev_in2[j][:6], dev_in2[j][6], bs, ws=ws_b, out=outs2[j])
+                done_c[j] = torch.cuda.Event()
+                done_c[j].record(st)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done_c[j])
+                    for dsrc, hdst in zip(outs2[j], host_out2[j]):
+                        hdst.copy_(dsrc, non_blocking=True)
+                    done_o[j] = torch.cuda.Event()
+                    done_o[j].record(s_out)
+            st.wait_stream(s_in)
+            st.wait_stream(s_out)
+
+        pipeline(2)
+        torch.cuda.synchronize()
+        p_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        p_ev[0].record(st)
+        s_in.wait_stream(st)
+        s_out.wait_stream(st)
+        pipeline(n_e2e)
+        p_ev[1].record(st)
+        torch.cuda.synchronize()
+        if api.get_error(ws_b):
+            raise RuntimeError("device error in the end-to-end leg")
+        e_ms = p_ev[0].elapsed_time(p_ev[1])
         e_ms_max, e_flop = aggregate(e_ms, bwd_flop * n_e2e, dev)
         e2e = {"value": e_flop / (e_ms_max * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e2e,
-               "scope": "H2D of the backward's inputs (q,k,v,o,dO,lse,idx) from pinned memory, "
-                        "nsa_sel_bwd, D2H of dq,dk,dv to pinned memory"}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e2e, "steps": n_e2e,
+               "serial_ms_per_step": serial_ms,
+               "scope": "per step: H2D of the backward's inputs (q,k,v,o,dO,lse,idx) from pinned memory, "
+                        "nsa_sel_bwd, D2H of dq,dk,dv to pinned memory; steps pipelined over a copy-in "
+                        "stream, the compute stream and a copy-out stream with two buffer sets "
+                        "(serial_ms_per_step: the same step alone on one stream)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
