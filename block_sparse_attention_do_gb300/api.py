@@ -33,6 +33,7 @@ SYMBOLS = (
     "nsa_swa_fwd", "nsa_swa_bwd", "nsa_sink_fwd", "nsa_sink_bwd", "nsa_debug_stall",
     "nsa_causal_fwd_workspace_size", "nsa_causal_bwd_workspace_size", "nsa_causal_fwd", "nsa_causal_bwd",
     "nsa_select_workspace_size", "nsa_compress_keys_mean", "nsa_block_scores", "nsa_select_topk",
+    "nsa_sel_fwd_workspace_size", "nsa_sel_bwd_workspace_size",
 )
 
 
@@ -132,6 +133,9 @@ def lib() -> C.CDLL:
         L.nsa_trace_count.restype = C.c_int32
         L.nsa_trace_count.argtypes = []
         L.nsa_trace_get.argtypes = [C.c_int32, C.POINTER(C.c_char_p), C.POINTER(C.c_float)]
+        for name in ("nsa_sel_fwd_workspace_size", "nsa_sel_bwd_workspace_size"):
+            getattr(L, name).restype = C.c_size_t
+            getattr(L, name).argtypes = [pp]
         L.nsa_select_workspace_size.restype = C.c_size_t
         L.nsa_select_workspace_size.argtypes = [pp]
         L.nsa_compress_keys_mean.argtypes = [pp] + [_P] * 3 + [_P]

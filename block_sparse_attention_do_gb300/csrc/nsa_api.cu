@@ -523,6 +523,9 @@ size_t nsa_bwd_workspace_size(const nsa_problem *p)
     return 0;
 }
 
+size_t nsa_sel_fwd_workspace_size(const nsa_problem *p) { return nsa_fwd_workspace_size(p); }
+size_t nsa_sel_bwd_workspace_size(const nsa_problem *p) { return nsa_bwd_workspace_size(p); }
+
 nsa_status nsa_sel_fwd(const nsa_problem *p, const void *q, const void *k, const void *v,
                        const int32_t *block_idx, void *o, float *lse, void *ws, size_t ws_bytes,
                        void *stream)

@@ -127,9 +127,13 @@ typedef struct nsa_problem {
     int32_t reserved2;     /* set to 0 */
 } nsa_problem;
 
-/* Workspace bytes needed by the forward / backward entry points (0 on an invalid problem). */
+/* Workspace bytes needed by the forward / backward entry points (0 on an invalid problem).
+ * nsa_sel_fwd_workspace_size / nsa_sel_bwd_workspace_size are the same functions under
+ * the selection entries' names. */
 size_t nsa_fwd_workspace_size(const nsa_problem *p);
 size_t nsa_bwd_workspace_size(const nsa_problem *p);
+size_t nsa_sel_fwd_workspace_size(const nsa_problem *p);
+size_t nsa_sel_bwd_workspace_size(const nsa_problem *p);
 
 /*
  * Selection forward (gradcheck-gate page: the selection forward called in

@@ -55,6 +55,8 @@ def test_workspace_sizes_and_validation(lib):
 
     p = _p()
     assert api.fwd_workspace_size(p) >= 256
+    assert lib.nsa_sel_fwd_workspace_size(C.byref(p)) == api.fwd_workspace_size(p)
+    assert lib.nsa_sel_bwd_workspace_size(C.byref(p)) == api.bwd_workspace_size(p)
     assert api.bwd_workspace_size(p) > 256 + 4 * 256 * 4
     assert api.bwd_workspace_size(_p(Hq=3)) == 0          # Hq % Hkv != 0
     assert api.bwd_workspace_size(_p(D=96)) == 0          # unsupported head dim
