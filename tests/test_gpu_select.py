@@ -105,6 +105,7 @@ SCORE_CASES = [
     (1, 128, 1, 70, 64, 16, torch.bfloat16),   # G = 128: one token per tile
     (1, 3, 3, 4200, 64, 16, torch.bfloat16),   # 263 blocks: S recomputed in pass 2
     (1, 2, 1, 10, 64, 16, torch.float32),      # T < block size: no complete block
+    (1, 4, 2, 150, 32, 16, torch.bfloat16),    # bf16 D = 32: per-thread copies, not TMA
 ]
 
 
@@ -124,9 +125,9 @@ def test_block_scores(B, Hq, Hkv, T, D, bs, dtype):
     assert np.all(got.numpy()[..., (j + 1) * bs - 1 > t] == 0.0)
 
 
-def test_block_scores_packed_sequences():
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 2, 64, 32), (32, 2, 128, 64)])
+def test_block_scores_packed_sequences(Hq, Hkv, D, bs):
     lens = [100, 7, 260, 33]
-    Hq, Hkv, D, bs = 8, 2, 64, 32
     cu = inputs.cu_seqlens_from_lengths(lens)
     total = sum(lens)
     q, _, _, _ = inputs.make_qkv_do(1, Hq, Hkv, total, D, dtype=torch.bfloat16, seed=25, layout="thd")
