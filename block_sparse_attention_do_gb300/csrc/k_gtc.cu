@@ -349,6 +349,44 @@ __device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, ui
     }
 }
 
+// A group of 64 keys: the 64 / BS union blocks list[i0 ..] (fewer at the
+// list's end), block list[i0 + r / BS]'s key r % BS in row r.  The query-tile
+// kernels walk their blocks a group at a time, so that each step's fixed
+// costs (stores, barriers, MMA latencies) are paid once per 64 keys.
+constexpr int kGroupKeys = 64;
+
+template <bool SPLIT, int BS>
+__device__ __forceinline__ void fetch_group(const Geo &g, const void *src, int b, int kvh, const int *list, int i0,
+                                            int U, BlockRegs &R)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+    const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = kGroupKeys * nv, Lk = seq_len_k(g, b);
+#pragma unroll
+    for (int i = 0; i < kBlkVec; ++i) {
+        const int e = threadIdx.x + i * kThr, row = e >> lnv, c = (e & (nv - 1)) * VEC, gi = i0 + row / BS;
+        R.v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < n && gi < U) {
+            const int key = list[gi] * BS + row % BS;
+            if (key < Lk)
+                R.v[i] = __ldg((const uint4 *)((const uint8_t *)src + (kv_off(g, b, kvh, key) + c) * In<SPLIT>::ES));
+        }
+    }
+}
+
+// the group into a [64][Dp] tile
+template <bool SPLIT>
+__device__ __forceinline__ void store_group(const Geo &g, const BlockRegs &R, uint32_t tile, uint32_t lo_off)
+{
+    constexpr int VEC = In<SPLIT>::VEC;
+    const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = kGroupKeys * nv;
+#pragma unroll
+    for (int i = 0; i < kBlkVec; ++i) {
+        const int e = threadIdx.x + i * kThr;
+        if (e < n)
+            put_vec<SPLIT>(tile, kGroupKeys, lo_off, e >> lnv, (e & (nv - 1)) * VEC, R.v[i]);
+    }
+}
+
 // One row of a q-shaped tensor (this thread's) in registers
 constexpr int kRowVec = 16;  // D * element bytes / 16 <= 16
 struct RowRegs {
@@ -438,13 +476,15 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
-    constexpr int bs = BS;  // keys per block (the launch picks the instance for g.bs)
+    constexpr int bs = BS;                     // keys per block (the launch picks the instance for g.bs)
+    constexpr int GB = kGroupKeys / BS;        // blocks per group
+    constexpr int NK = kGroupKeys;             // keys per group: the products' N (S) and K (P V)
     const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
-    // plan: Q [128][Dp] | K [bs][Dp] | V [bs][Dp] (read MN-major by P V) |
+    // plan: Q [128][Dp] | K [64][Dp] | V [64][Dp] (read MN-major by P V) |
     // P [128][64] (each with its low part right after it) | union buffer |
     // barrier, wait context, TMEM slot
-    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, VB = KB, PB = 128 * kKeyPad * 2;
+    const uint32_t QB = 128 * Dp * 2, KB = NK * Dp * 2, VB = KB, PB = 128 * kKeyPad * 2;
     uint8_t *q_t = sm, *k_t = q_t + parts * QB, *v_t = k_t + parts * KB, *p_t = v_t + parts * VB;
     int *ubuf = (int *)(p_t + parts * PB);
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
@@ -457,7 +497,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     if (warp == 0 && nvalid > 0)
         qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
     __syncthreads();
-    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0;
+    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0, NG = (U + GB - 1) / GB;
     const int *list = union_list(ubuf, up);
     int tl, hh;
     qrow(G, r, tl, hh);
@@ -473,39 +513,51 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
         fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, kvh * G + hh, t) : 0, rvalid, qr);
         store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
     }
-    const uint32_t idS = idesc_bf16(128, bs, false, false), idO = idesc_bf16(128, Dp, false, true);
+    const uint32_t idS = idesc_bf16(128, NK, false, false), idO = idesc_bf16(128, Dp, false, true);
+    // the first key of each block of group gi (-1 past the list's end) and
+    // whether the row takes that block
+    auto group_blocks = [&](int gi, int *k0s, bool *sel) {
+#pragma unroll
+        for (int e = 0; e < GB; ++e) {
+            const int li = gi * GB + e;
+            const int j = li < U ? list[li] : -1;
+            k0s[e] = j * bs;
+            sel[e] = j >= 0 && rvalid && qtile_selects(g, my_mask, klo, khi, j);
+        }
+    };
     bool ok = true;
     // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
     float m = -INFINITY, l = 0.f;
-    BlockRegs kr, vr;  // the next block's K (and V), fetched while the MMAs run
-    if (U > 0)
-        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
-    for (int i = 0; i < U && ok; ++i) {
-        const int j = list[i], k0 = j * bs;
-        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
+    BlockRegs kr, vr;  // the next group's K (and V), fetched while the MMAs run
+    if (NG > 0)
+        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
+    for (int gi = 0; gi < NG && ok; ++gi) {
+        store_group<SPLIT>(g, kr, ks, KB);
         to_mma();
         if (r == 0)
-            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
-        if (i + 1 < U)
-            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
+        if (gi + 1 < NG)
+            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
         if (!(ok = commit_wait(sy)))
             break;
-        float sc[bs];
-        ld_cols<bs>(tmem, TM_S, sc);
-        const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j);
-        // the block's maximum first, then its terms against the new maximum
+        int k0s[GB];
+        bool sel[GB];
+        group_blocks(gi, k0s, sel);
+        float sc[NK];
+        ld_cols<NK>(tmem, TM_S, sc);
+        // the group's maximum first, then its terms against the new maximum
         float bm = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < bs; ++c) {
-            const int key = k0 + c;
-            sc[c] = (sel && key >= klo && key <= khi) ? sc[c] * g.scale_l2 : -INFINITY;
+        for (int c = 0; c < NK; ++c) {
+            const int key = k0s[c / bs] + c % bs;
+            sc[c] = (sel[c / bs] && key >= klo && key <= khi) ? sc[c] * g.scale_l2 : -INFINITY;
             bm = fmaxf(bm, sc[c]);
         }
         if (bm != -INFINITY) {
             const float mn = fmaxf(m, bm);
             float sum = 0.f;
 #pragma unroll
-            for (int c = 0; c < bs; ++c)
+            for (int c = 0; c < NK; ++c)
                 sum += ex2(sc[c] - mn);  // exp2(-inf) = 0 off the row's keys
             l = l * ex2(m - mn) + sum;
             m = mn;
@@ -513,39 +565,45 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     }
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
     // pass 2: P = exp2(scale_l2 s - lse2) on the row's keys, O += P V
-    if (U > 0 && ok) {
-        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
-        fetch_block<SPLIT>(g, p.v, b, kvh, list[0] * bs, vr);
+    if (NG > 0 && ok) {
+        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
+        fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, 0, U, vr);
     }
-    for (int i = 0; i < U && ok; ++i) {
-        const int j = list[i], k0 = j * bs;
-        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
-        store_block<SPLIT>(g, vr, vs, VB, Dp, false);
+    for (int gi = 0; gi < NG && ok; ++gi) {
+        store_group<SPLIT>(g, kr, ks, KB);
+        store_group<SPLIT>(g, vr, vs, VB);
         to_mma();
         if (r == 0)
-            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
-        if (i + 1 < U) {
-            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
-            fetch_block<SPLIT>(g, p.v, b, kvh, list[i + 1] * bs, vr);
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
+        if (gi + 1 < NG) {
+            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
+            fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
         }
         if (!(ok = commit_wait(sy)))
             break;
-        float sc[bs];
-        ld_cols<bs>(tmem, TM_S, sc);
-        const bool sel = rvalid && qtile_selects(g, my_mask, klo, khi, j) && lse2 != -INFINITY;
+        int k0s[GB];
+        bool sel[GB];
+        group_blocks(gi, k0s, sel);
 #pragma unroll
-        for (int c0 = 0; c0 < bs; c0 += 8) {
-            float pv[8];
+        for (int c1 = 0; c1 < NK; c1 += 32) {
+            float sc[32];
+            ld_cols<32>(tmem, TM_S + c1, sc);
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const int c = c0 + x, key = k0 + c;
-                pv[x] = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - lse2) : 0.f;
+            for (int c0 = 0; c0 < 32; c0 += 8) {
+                float pv[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int c = c1 + c0 + x, key = k0s[c / bs] + c % bs;
+                    pv[x] = (sel[c / bs] && lse2 != -INFINITY && key >= klo && key <= khi)
+                                ? ex2(sc[c0 + x] * g.scale_l2 - lse2)
+                                : 0.f;
+                }
+                put8<SPLIT>(ps, 128, PB, r, c1 + c0, pv);
             }
-            put8<SPLIT>(ps, 128, PB, r, c0, pv);
         }
         to_mma();
         if (r == 0)  // O += P V, V read MN-major from its plain tile
-            product_bmn<SPLIT>(tmem + TM_ACC, ps, 128, PB, vs, bs, VB, idO, bs / 16, i > 0);
+            product_bmn<SPLIT>(tmem + TM_ACC, ps, 128, PB, vs, NK, VB, idO, NK / 16, gi > 0);
         ok = commit_wait(sy);
     }
     // epilogue: O (already normalised) and the natural-log LSE.  Every lane
@@ -576,12 +634,13 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
     constexpr int bs = BS;
-    constexpr int kCh = bs < 32 ? bs : 32;  // S and dP columns read per TMEM wait
+    constexpr int GB = kGroupKeys / BS;  // blocks per group
+    constexpr int NK = kGroupKeys;       // keys per group: the products' N (S, dP) and K (dS K)
     const int Dp = p.Dp, G = g.G, Tq = tile_tokens(G), nrows = Tq * G, parts = SPLIT ? 2 : 1;
     const UnionBuf up = union_buf(g);
-    // plan: Q, dO [128][Dp] | K, V [bs][Dp] (K also read MN-major by dS K) |
+    // plan: Q, dO [128][Dp] | K, V [64][Dp] (K also read MN-major by dS K) |
     // dS [128][64] | union | misc
-    const uint32_t QB = 128 * Dp * 2, KB = bs * Dp * 2, PB = 128 * kKeyPad * 2;
+    const uint32_t QB = 128 * Dp * 2, KB = NK * Dp * 2, PB = 128 * kKeyPad * 2;
     uint8_t *q_t = sm, *do_t = q_t + parts * QB, *k_t = do_t + parts * QB, *v_t = k_t + parts * KB;
     uint8_t *ds_t = v_t + parts * KB;
     int *ubuf = (int *)(ds_t + parts * PB);
@@ -595,7 +654,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     if (warp == 0 && nvalid > 0)
         qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
     __syncthreads();
-    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0;
+    const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0, NG = (U + GB - 1) / GB;
     const int *list = union_list(ubuf, up);
     int tl, hh;
     qrow(G, r, tl, hh);
@@ -620,48 +679,57 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
             dl = p.delta[so];
         }
     }
-    const uint32_t idS = idesc_bf16(128, bs, false, false), idQ = idesc_bf16(128, Dp, false, true);
+    const uint32_t idS = idesc_bf16(128, NK, false, false), idQ = idesc_bf16(128, Dp, false, true);
     bool ok = true;
-    BlockRegs kr, vr;  // the next block's K and V, fetched while the MMAs run
-    if (U > 0) {
-        fetch_block<SPLIT>(g, p.k, b, kvh, list[0] * bs, kr);
-        fetch_block<SPLIT>(g, p.v, b, kvh, list[0] * bs, vr);
+    BlockRegs kr, vr;  // the next group's K and V, fetched while the MMAs run
+    if (NG > 0) {
+        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
+        fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, 0, U, vr);
     }
-    for (int i = 0; i < U && ok; ++i) {
-        const int j = list[i], k0 = j * bs;
-        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
-        store_block<SPLIT>(g, vr, vs, KB, Dp, false);
+    for (int gi = 0; gi < NG && ok; ++gi) {
+        store_group<SPLIT>(g, kr, ks, KB);
+        store_group<SPLIT>(g, vr, vs, KB);
         to_mma();
         if (r == 0)
-            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
+            product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
         else if (r == kIssuer2)
-            product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
-        if (i + 1 < U) {
-            fetch_block<SPLIT>(g, p.k, b, kvh, list[i + 1] * bs, kr);
-            fetch_block<SPLIT>(g, p.v, b, kvh, list[i + 1] * bs, vr);
+            product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, NK, KB, idS, Dp / 16, false);
+        if (gi + 1 < NG) {
+            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
+            fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
         }
         if (!(ok = commit_wait(sy)))
             break;
-        const bool sel = rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
+        // the first key of each block of the group, and whether the row takes it
+        int k0s[GB];
+        bool sel[GB];
 #pragma unroll
-        for (int c1 = 0; c1 < bs; c1 += kCh) {
-            float sc[kCh], dp[kCh];
-            ld_cols<kCh, kCh>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
+        for (int e = 0; e < GB; ++e) {
+            const int li = gi * GB + e;
+            const int j = li < U ? list[li] : -1;
+            k0s[e] = j * bs;
+            sel[e] = j >= 0 && rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
+        }
 #pragma unroll
-            for (int c0 = 0; c0 < kCh; c0 += 8) {
+        for (int c1 = 0; c1 < NK; c1 += 32) {
+            float sc[32], dp[32];
+            ld_cols<32, 32>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 8) {
                 float dsv[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
-                    const int c = c0 + x, key = k0 + c1 + c;
-                    const float pv = (sel && key >= klo && key <= khi) ? ex2(sc[c] * g.scale_l2 - l2) : 0.f;
-                    dsv[x] = pv * (dp[c] - dl);
+                    const int c = c1 + c0 + x, key = k0s[c / bs] + c % bs;
+                    const float pv =
+                        (sel[c / bs] && key >= klo && key <= khi) ? ex2(sc[c0 + x] * g.scale_l2 - l2) : 0.f;
+                    dsv[x] = pv * (dp[c0 + x] - dl);
                 }
                 put8<SPLIT>(dss, 128, PB, r, c1 + c0, dsv);
             }
         }
         to_mma();
         if (r == 0)  // dQ += dS K, K read MN-major from its plain tile
-            product_bmn<SPLIT>(tmem + TM_ACC, dss, 128, PB, ks, bs, KB, idQ, bs / 16, i > 0);
+            product_bmn<SPLIT>(tmem + TM_ACC, dss, 128, PB, ks, NK, KB, idQ, NK / 16, gi > 0);
         ok = commit_wait(sy);
     }
     if (ok) {
@@ -1269,7 +1337,7 @@ cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const voi
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + 128 * kKeyPad * 2) +
+    const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + 2 * kGroupKeys * p.Dp * 2 + 128 * kKeyPad * 2) +
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
@@ -1293,7 +1361,8 @@ cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 + parts * (size_t)(2 * 128 * p.Dp * 2 + 2 * g.bs * p.Dp * 2 + 128 * kKeyPad * 2) +
+    const size_t smem = 1024 +
+                        parts * (size_t)(2 * 128 * p.Dp * 2 + 2 * kGroupKeys * p.Dp * 2 + 128 * kKeyPad * 2) +
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
