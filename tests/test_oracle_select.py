@@ -217,3 +217,15 @@ def test_selection_pipeline_gives_a_valid_index():
     assert oracle.validate_index(torch.from_numpy(idx), bs) == 0
     o, lse = oracle.sel_fwd(q, k, k, torch.from_numpy(idx), bs)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def test_planted_mistake_in_scores_is_caught():
+    """Scores summed over the wrong heads (head h counted in kv group h % Hkv
+    instead of h // G) must fail the pin against causal attention."""
+    B, Hq, Hkv, T, D, bs = 1, 4, 2, 40, 16, 4
+    q = _rand((B, Hq, T, D), 13)
+    kc = oracle.compress_mean(_rand((B, Hkv, T, D), 14), bs)
+    want = _scores_via_causal_attention(q.numpy(), kc, bs, 0.5)
+    perm = [h for r in range(Hkv) for h in range(r, Hq, Hkv)]  # plant: h -> group h % Hkv
+    bad = oracle.block_scores(q[:, perm], kc, bs, scale=0.5)
+    assert np.max(np.abs(bad - want)) > 1e-3
