@@ -12,14 +12,16 @@
 // several units writes fp32 partials that a separate kernel adds in unit
 // order; a block held by one unit writes dK/dV directly.
 //
-// Roles (11 warps):  warps 0 and 3 load (TMA for K_j/V_j; Q rows from warp 0
+// Roles (15 warps; 16 with the third cp.async gather warp):  warps 0 and 3 load (TMA for K_j/V_j; Q rows from warp 0
 // and dO rows from warp 3 by one TMA box per token -- its G heads, both
 // halves -- when G % 8 == 0; else by 16-byte cp.async, two whole rows per
 // warp instruction with the swizzle applied by hand, each lane's copies
 // arriving on the tile's barrier as they land); warp 1 resolves each tile's token ids a tile
 // ahead; warp 2 owns TMEM; one thread each of warps 2, 8, 9 and 10 issues the
-// S, dP, dV^T and dK^T MMAs; warps 4-7 compute P/dS for one row each (reading
-// the row's LSE and delta themselves) and run the epilogue.  Q has three
+// S, dP, dV^T and dK^T MMAs; two softmax warpgroups (warps 4-7 and 11-14, or
+// 12-15 where warp 11 gathers) compute P/dS for one row each, keys 0..31 and
+// 32..63 of the block (reading the row's LSE and delta themselves), and split
+// the epilogue's columns the same way.  Q has three
 // stages and dO two (row-group layout, so that a token's box is contiguous):
 // a tile's Q is held from its load until dK^T has read it, its dO only from
 // its load until dV^T has, so the dO ring refills later and needs fewer
@@ -105,8 +107,11 @@ enum { LOAD_ROWS = 0, LOAD_TILE = 1, LOAD_CPASYNC = 2 };
 // warp's cp.async gather of a 32 KB tile takes ~6,300 cycles (about 100 cycles
 // per warp instruction), so three warps share both tensors' rows.  12 warps at
 // 168 registers still fit (3 warps per SM sub-partition).
-template <int MODE> constexpr int dkdv_threads() { return MODE == LOAD_CPASYNC ? 384 : 352; }
+template <int MODE> constexpr int dkdv_threads() { return MODE == LOAD_CPASYNC ? 512 : 480; }
 constexpr int kGatherWarps = 3;  // warps 0, 3 and 11 in the cp.async mode
+// the second softmax warpgroup (keys 32..63 of every tile; the first, warps
+// 4-7, takes keys 0..31): warps 11-14, or 12-15 in the cp.async mode
+template <int MODE> constexpr int softmax1_warp0() { return MODE == LOAD_CPASYNC ? 12 : 11; }
 
 template <int MODE>
 __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -145,18 +150,18 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
         for (int x = 0; x < NSB; ++x) {
             mbar_init(&bars[B_SFULL0 + x], 1);
             mbar_init(&bars[B_DPFULL0 + x], 1);
-            mbar_init(&bars[B_SFREE0 + x], kRows);
+            mbar_init(&bars[B_SFREE0 + x], 2 * kRows);  // both softmax warpgroups
         }
         for (int x = 0; x < NPB; ++x) {
-            mbar_init(&bars[B_PFULL0 + x], kRows);
+            mbar_init(&bars[B_PFULL0 + x], 2 * kRows);
             mbar_init(&bars[B_PFREE0 + x], 1);
-            mbar_init(&bars[B_DSFULL0 + x], kRows);
+            mbar_init(&bars[B_DSFULL0 + x], 2 * kRows);
             mbar_init(&bars[B_DSFREE0 + x], 1);
         }
         mbar_init(&bars[B_ACCFULL], 2);
-        mbar_init(&bars[B_ACCEMPTY], kRows);
-        mbar_init(&bars[B_STAGED], kRows);
-        mbar_init(&bars[B_COPIED], kRows);
+        mbar_init(&bars[B_ACCEMPTY], 2 * kRows);
+        mbar_init(&bars[B_STAGED], 2 * kRows);
+        mbar_init(&bars[B_COPIED], 2 * kRows);
         for (int x = 0; x < 4; ++x)
             mbar_init(&bars[B_DONE0 + x], 1);
         fence_barrier_init();
@@ -496,8 +501,11 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
             mbar_wait(&bars[B_DONE0 + role], 0, never);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || (warp >= softmax1_warp0<MODE>() && warp < softmax1_warp0<MODE>() + 4)) {
         // ------------------------------------------------- softmax / epilogue
+        // two warpgroups, one row per thread each: keys (and, in the
+        // epilogue, dK/dV columns) cb .. cb + 31
+        const int half = warp >= 8 ? 1 : 0, cb = half * 32;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // tile row = TMEM lane
         // the row's token within the tile and head within the group
@@ -572,9 +580,9 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                 const int cdiag = tok < 0 ? -1 : kdiag(g, b, tok);
                 const int lim = tok < 0 ? -1 : min(cdiag, L - 1) - k0;
                 const int lo = tok < 0 ? 0 : key_lo(g, cdiag) - k0;  // window's left edge
-                // P from S while dP is still running
-                uint32_t pv[64];
-                tmem_ld64(lane_base + TM_S + tb * 128, pv);
+                // P from S while dP is still running (this warpgroup's 32 keys)
+                uint32_t pv[32];
+                tmem_ld32(lane_base + TM_S + tb * 128 + cb, pv);
                 tmem_wait_ld();
                 if (__all_sync(0xffffffffu, lim < 0 || (lim >= kKeys - 1 && lo <= 0))) {
                     // no row of the warp ends or starts inside the block: a row
@@ -582,7 +590,7 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     const float bias = lim >= 0 ? l2 : __int_as_float(0x7f800000);
                     const uint64_t sc2 = f2(g.scale_l2, g.scale_l2), nb2 = f2(-bias, -bias);
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
+                    for (int c = 0; c < 32; c += 2) {
                         float x0, x1;
                         f2_split(f2_fma(f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), sc2, nb2), x0, x1);
                         pv[c] = __float_as_uint(ex2(x0));
@@ -590,15 +598,16 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        pv[c] = __float_as_uint((c <= lim && c >= lo) ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
-                                                                      : 0.f);
+                    for (int c = 0; c < 32; ++c)
+                        pv[c] = __float_as_uint((cb + c <= lim && cb + c >= lo)
+                                                    ? ex2(__uint_as_float(pv[c]) * g.scale_l2 - l2)
+                                                    : 0.f);
                 }
                 // P (bf16) to shared memory as soon as the dV product of the
                 // previous tile has read it: dV^T += dO^T P starts while dS forms
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2)
+                for (int c = 0; c < 32; c += 2)
                     pk[c >> 1] = pack_bf16(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
                 const int pbuf = it % NPB;  // this tile's P / dS buffer
                 if (!mbar_wait_warp(&bars[B_PFREE0 + pbuf], ((it / NPB) & 1) ^ 1, abort_flag)) {
@@ -606,9 +615,9 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     break;
                 }
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(p_row + pbuf * (kRows * 128) + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1],
-                                 pk[4 * c + 2], pk[4 * c + 3]);
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(p_row + pbuf * (kRows * 128) + (((cb / 8 + c) ^ (r & 7)) << 4), pk[4 * c],
+                                 pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 fence_async_smem();
                 mbar_arrive(&bars[B_PFULL0 + pbuf]);
                 if (!prefetch()) {
@@ -621,8 +630,8 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     break;
                 }
                 tc_fence_after();
-                uint32_t dv_[64];
-                tmem_ld64(lane_base + TM_S + tb * 128 + 64, dv_);
+                uint32_t dv_[32];
+                tmem_ld32(lane_base + TM_S + tb * 128 + 64 + cb, dv_);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars[B_SFREE0 + tb]);
@@ -630,10 +639,10 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     tb = 0;
                     tph ^= 1;
                 }
-                uint32_t dk_[32];
+                uint32_t dk_[16];
                 const uint64_t nd2 = f2(-dl, -dl);
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
+                for (int c = 0; c < 32; c += 2) {
                     float d0, d1;
                     const uint64_t pp = f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1]));
                     f2_split(f2_mul(pp, f2_add(f2(__uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1])), nd2)), d0, d1);
@@ -644,9 +653,9 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                     break;
                 }
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(ds_row + pbuf * (kRows * 128) + ((c ^ (r & 7)) << 4), dk_[4 * c], dk_[4 * c + 1], dk_[4 * c + 2],
-                                 dk_[4 * c + 3]);
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(ds_row + pbuf * (kRows * 128) + (((cb / 8 + c) ^ (r & 7)) << 4), dk_[4 * c],
+                                 dk_[4 * c + 1], dk_[4 * c + 2], dk_[4 * c + 3]);
                 fence_async_smem();
                 mbar_arrive(&bars[B_DSFULL0 + pbuf]);
             }
@@ -666,24 +675,22 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
             const int d = r;
             const int nk = min(kKeys, L - k0);
             const bool direct = u.slot < 0;
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? TM_DK : TM_DV;
+            for (int which = 0; which < 2; ++which) {  // this warpgroup's keys cb .. cb + 31
+                const uint32_t col = (which == 0 ? TM_DK : TM_DV) + cb;
                 const float mul = which == 0 ? g.scale : 1.f;
-                uint32_t a[64];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld16(lane_base + col + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&a[c * 16]));
+                uint32_t a[32];
+                tmem_ld32(lane_base + col, a);
                 tmem_wait_ld();
                 if (!direct) {
-                    float *dst = p.partials + ((int64_t)u.slot * 2 + which) * kKeys * kHead + d;
+                    float *dst = p.partials + ((int64_t)u.slot * 2 + which) * kKeys * kHead + cb * kHead + d;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < 32; ++c)
                         dst[c * kHead] = __uint_as_float(a[c]) * mul;
                 } else {
                     // dS buffer holds dK, P buffer dV: [64 keys][128 dims] bf16
-                    __nv_bfloat16 *stage = (__nv_bfloat16 *)(sm + (which == 0 ? OFF_DS : OFF_P)) + d;
+                    __nv_bfloat16 *stage = (__nv_bfloat16 *)(sm + (which == 0 ? OFF_DS : OFF_P)) + cb * kHead + d;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < 32; ++c)
                         stage[c * kHead] = __float2bfloat16_rn(__uint_as_float(a[c]) * mul);
                 }
             }
@@ -697,7 +704,7 @@ __global__ void __launch_bounds__(dkdv_threads<MODE>(), 1) dkdv_tc_kernel(const 
                 // distance between consecutive keys (elements)
                 const int64_t kstride = g.sdkv.t;
 #pragma unroll 4
-                for (int q = r; q < 2 * kKeys * 16; q += kRows) {
+                for (int q = r + half * kRows; q < 2 * kKeys * 16; q += 2 * kRows) {
                     const int which = q / (kKeys * 16), c = (q >> 4) & (kKeys - 1), ch = q & 15;
                     if (c < nk) {
                         __nv_bfloat16 *out = (which == 0 ? p.dk : p.dv) + dkv_off(g, b, kvh, k0) + c * kstride;
