@@ -912,7 +912,8 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
 // complete at t ((j + 1) bs - 1 <= t), p = exp(scale <q, kc_j>) normalised
 // over the row's complete blocks; a token's score of block j is the sum of
 // p over the G heads of its kv head (0 for blocks not complete at t).
-// One CTA per query tile (Tq tokens x G heads).  The compressed keys of the
+// One CTA of two threads per tile row (each takes 32 of a chunk's 64
+// columns) per query tile (Tq tokens x G heads).  The compressed keys of the
 // blocks complete at the tile's last row are read in chunks of 64 (the MMA's
 // N).  Up to 4 chunks (256 blocks) are resident: the q tile and every chunk
 // are loaded at once -- by TMA (bf16 with D a multiple of 64: the q tile as
@@ -922,6 +923,7 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
 // p, stages it in shared memory (row stride 65 floats: writes by rows and
 // reads by columns are both conflict-free) and sums each token's G rows.
 // Longer rows walk the chunks one at a time and recompute S in pass 2.
+constexpr int kScoreThr = 256;  // two threads per tile row
 constexpr int kScoreCh = 64;   // compressed keys per chunk
 constexpr int kScoreBufs = 4;  // resident chunks at most
 constexpr int kPStride = 65;   // floats per staged row
@@ -951,7 +953,7 @@ __host__ __device__ inline ScorePlan score_plan(int nb, int parts, int Dp)
 }
 
 template <bool SPLIT, bool TMA>
-__global__ void __launch_bounds__(kThr, 1)
+__global__ void __launch_bounds__(kScoreThr, 3)
     scores_gtc_kernel(const GParams p, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kcmap)
 {
@@ -974,6 +976,7 @@ __global__ void __launch_bounds__(kThr, 1)
     float *pbuf = (float *)(sm + plan.pbuf_off);
     uint8_t *misc = sm + plan.misc_off;
     uint64_t *tbar = (uint64_t *)(misc + 48);
+    float *xchg = (float *)(misc + 64);  // [2 halves][2 (m, l)][128 rows]: the rows' statistics
     Sync sy;
     if (TMA && threadIdx.x == 0) {
         mbar_init(tbar, 1);
@@ -982,7 +985,10 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     const uint32_t tmem = g_start(misc, p, sy, plan.tmem_cols);  // (its barrier-init fence and sync cover tbar too)
     uint32_t tphase = 0;
-    const int r = threadIdx.x;
+    // two threads per row: thread (hc, r) takes columns hc*32 .. hc*32+31 of
+    // every chunk; warp w reads TMEM lanes 32*(w%4) ..
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, colh = hc * 32;
+    const uint32_t lane_base = tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16);
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
     if (g.D < Dp)  // zero padding columns (every other byte is written below)
@@ -1017,24 +1023,24 @@ __global__ void __launch_bounds__(kThr, 1)
                     tma_load_3d(c_t + buf * CB + h * (kScoreCh * 128), &kcmap, tbar, h * 64, c * kScoreCh,
                                 b * g.Hkv + kvh);
         } else if constexpr (!SPLIT) {
-            for (int e = threadIdx.x; e < nvec; e += kThr) {
+            for (int e = threadIdx.x; e < nvec; e += kScoreThr) {
                 const int row = e >> lnv, j = c * kScoreCh + row, col = (e & (nv - 1)) * VEC;
                 cp_async_16(dst + swz(row, col, kScoreCh), kc_bg + ((int64_t)(j < nb ? j : 0) * g.D + col) * ES,
                             j < nb ? 16u : 0u);
             }
         } else {
-            for (int e0 = 0; e0 < nvec; e0 += kBlkVec * kThr) {
+            for (int e0 = 0; e0 < nvec; e0 += kBlkVec * kScoreThr) {
                 uint4 v[kBlkVec];
 #pragma unroll
                 for (int i = 0; i < kBlkVec; ++i) {
-                    const int e = e0 + threadIdx.x + i * kThr, j = c * kScoreCh + (e >> lnv);
+                    const int e = e0 + threadIdx.x + i * kScoreThr, j = c * kScoreCh + (e >> lnv);
                     v[i] = make_uint4(0u, 0u, 0u, 0u);
                     if (e < nvec && j < nb)
                         v[i] = __ldg((const uint4 *)(kc_bg + ((int64_t)j * g.D + (e & (nv - 1)) * VEC) * ES));
                 }
 #pragma unroll
                 for (int i = 0; i < kBlkVec; ++i) {
-                    const int e = e0 + threadIdx.x + i * kThr;
+                    const int e = e0 + threadIdx.x + i * kScoreThr;
                     if (e < nvec)
                         put_vec<SPLIT>(dst, kScoreCh, CB, e >> lnv, (e & (nv - 1)) * VEC, v[i]);
                 }
@@ -1080,7 +1086,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 else
                     tma_load_4d(q_t + h * (128 * 128), &qmap, tbar, h * 64, t0, kvh * G, b);
             }
-    } else {
+    } else if (hc == 0) {
         const int64_t qo = rvalid ? q_off(g, b, kvh * G + hh, t) : 0;
         if constexpr (!SPLIT) {
             for (int c = 0; c < g.D; c += VEC)
@@ -1106,15 +1112,23 @@ __global__ void __launch_bounds__(kThr, 1)
     float m = -INFINITY, l = 0.f;
     // pass 1 on columns [col, col + 64) of TMEM holding chunk c: the row's
     // running maximum m and sum l of exp2(scale_l2 s) over its complete blocks
-    auto stats = [&](int c, uint32_t col) {
+    // this thread's 32 columns of TMEM column block col, as floats
+    auto ld32 = [&](uint32_t col, float *out) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + col + colh, v);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c1 = 0; c1 < kScoreCh; c1 += 32) {
+        for (int x = 0; x < 32; ++x)
+            out[x] = __uint_as_float(v[x]);
+    };
+    auto stats = [&](int c, uint32_t col) {
+        {
             float s[32];
-            ld_cols<32>(tmem, col + c1, s);
+            ld32(col, s);
             float bm = -INFINITY;
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
-                s[x] = c * kScoreCh + c1 + x < nc ? s[x] * g.scale_l2 : -INFINITY;
+                s[x] = c * kScoreCh + colh + x < nc ? s[x] * g.scale_l2 : -INFINITY;
                 bm = fmaxf(bm, s[x]);
             }
             if (bm != -INFINITY) {
@@ -1137,8 +1151,8 @@ __global__ void __launch_bounds__(kThr, 1)
             fetch_chunk(c, c);
         ok = loads_done();
         to_mma();
-        if (ok && (r == 0 || r == kIssuer2))  // chunks split between the two issuing threads
-            for (int c = r == 0 ? 0 : 1; c < nch; c += 2)
+        if (ok && (threadIdx.x == 0 || threadIdx.x == kIssuer2))  // chunks split between the two issuing threads
+            for (int c = threadIdx.x == 0 ? 0 : 1; c < nch; c += 2)
                 s_product(c, c, c * kScoreCh);
         ok = commit_wait(sy) && ok;
         for (int c = 0; c < nch && ok; ++c)
@@ -1152,11 +1166,23 @@ __global__ void __launch_bounds__(kThr, 1)
             if (!ok)
                 break;
             to_mma();
-            if (r == 0)
+            if (threadIdx.x == 0)
                 s_product(c, 0, 0);
             ok = commit_wait(sy);
             if (ok)
                 stats(c, 0);
+        }
+    }
+    // the row's statistics over both halves of its columns
+    xchg[(hc * 2) * kThr + r] = m;
+    xchg[(hc * 2 + 1) * kThr + r] = l;
+    __syncthreads();
+    {
+        const float mo = xchg[((1 - hc) * 2) * kThr + r], lo = xchg[((1 - hc) * 2 + 1) * kThr + r];
+        const float mn = fmaxf(m, mo);
+        if (mn != -INFINITY) {
+            l = (m != -INFINITY ? l * ex2(m - mn) : 0.f) + (mo != -INFINITY ? lo * ex2(mo - mn) : 0.f);
+            m = mn;
         }
     }
     const float lse2 = l > 0.f ? m + log2f(l) : INFINITY;  // +inf: no complete block, p = 0
@@ -1171,19 +1197,18 @@ __global__ void __launch_bounds__(kThr, 1)
             if (!ok)
                 break;
             to_mma();
-            if (r == 0)
+            if (threadIdx.x == 0)
                 s_product(c, 0, 0);
             ok = commit_wait(sy);
             if (!ok)
                 break;
         }
-#pragma unroll
-        for (int c1 = 0; c1 < kScoreCh; c1 += 32) {
+        {
             float s[32];
-            ld_cols<32>(tmem, col + c1, s);
+            ld32(col, s);
 #pragma unroll
             for (int x = 0; x < 32; ++x)
-                pbuf[r * kPStride + c1 + x] = c * kScoreCh + c1 + x < nc ? ex2(s[x] * g.scale_l2 - lse2) : 0.f;
+                pbuf[r * kPStride + colh + x] = c * kScoreCh + colh + x < nc ? ex2(s[x] * g.scale_l2 - lse2) : 0.f;
         }
         __syncthreads();
         {
@@ -1191,7 +1216,7 @@ __global__ void __launch_bounds__(kThr, 1)
             const int jj = threadIdx.x % kScoreCh, j = c * kScoreCh + jj;
             const int rs = head_major ? Tq : 1, ts = head_major ? 1 : G;  // row steps per head / token
             if (j < nb)
-                for (int tk = threadIdx.x / kScoreCh; tk < nvalid; tk += kThr / kScoreCh) {
+                for (int tk = threadIdx.x / kScoreCh; tk < nvalid; tk += kScoreThr / kScoreCh) {
                     const float *col = pbuf + tk * ts * kPStride + jj;
                     float sum = 0.f;
                     for (int h2 = 0; h2 < G; ++h2)
@@ -1206,7 +1231,7 @@ __global__ void __launch_bounds__(kThr, 1)
     // zeros for the blocks past the tile's chunks
     if (ok) {
         const int j0 = nch * kScoreCh, rest = nb - j0;
-        for (int o = threadIdx.x; rest > 0 && o < nvalid * rest; o += kThr)
+        for (int o = threadIdx.x; rest > 0 && o < nvalid * rest; o += kScoreThr)
             p.scores[index_row(g, b, kvh, t0 + o / rest) * nb + j0 + o % rest] = 0.f;
     }
     if constexpr (!TMA && !SPLIT)
@@ -1298,7 +1323,7 @@ cudaError_t launch_scores_gtc(const Geo &g, const void *q, const void *kc, float
     const int Tq = tile_tokens(g.G);
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
-    const size_t smem = 1024 + (size_t)score_plan(g.nbmax, parts, p.Dp).misc_off + 64;
+    const size_t smem = 1024 + (size_t)score_plan(g.nbmax, parts, p.Dp).misc_off + 64 + 4 * kThr * 4;
     if (p.ntiles < 1)
         return cudaSuccess;
     CUtensorMap qmap, kcmap;
@@ -1319,7 +1344,7 @@ cudaError_t launch_scores_gtc(const Geo &g, const void *q, const void *kc, float
                                : scores_gtc_kernel<false, false>;
     if (!smem_ok(k, smem))
         return cudaErrorInvalidValue;
-    k<<<p.ntiles, kThr, smem, st>>>(p, qmap, kcmap);
+    k<<<p.ntiles, kScoreThr, smem, st>>>(p, qmap, kcmap);
     return cudaGetLastError();
 }
 
