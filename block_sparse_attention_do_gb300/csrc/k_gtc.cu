@@ -355,15 +355,15 @@ __device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, ui
 // costs (stores, barriers, MMA latencies) are paid once per 64 keys.
 constexpr int kGroupKeys = 64;
 
-template <bool SPLIT, int BS>
+template <bool SPLIT, int BS, int NT = kThr>
 __device__ __forceinline__ void fetch_group(const Geo &g, const void *src, int b, int kvh, const int *list, int i0,
                                             int U, BlockRegs &R)
 {
     constexpr int VEC = In<SPLIT>::VEC;
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = kGroupKeys * nv, Lk = seq_len_k(g, b);
 #pragma unroll
-    for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr, row = e >> lnv, c = (e & (nv - 1)) * VEC, gi = i0 + row / BS;
+    for (int i = 0; i < kBlkVec * kThr / NT; ++i) {
+        const int e = threadIdx.x + i * NT, row = e >> lnv, c = (e & (nv - 1)) * VEC, gi = i0 + row / BS;
         R.v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (e < n && gi < U) {
             const int key = list[gi] * BS + row % BS;
@@ -374,14 +374,14 @@ __device__ __forceinline__ void fetch_group(const Geo &g, const void *src, int b
 }
 
 // the group into a [64][Dp] tile
-template <bool SPLIT>
+template <bool SPLIT, int NT = kThr>
 __device__ __forceinline__ void store_group(const Geo &g, const BlockRegs &R, uint32_t tile, uint32_t lo_off)
 {
     constexpr int VEC = In<SPLIT>::VEC;
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = kGroupKeys * nv;
 #pragma unroll
-    for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr;
+    for (int i = 0; i < kBlkVec * kThr / NT; ++i) {
+        const int e = threadIdx.x + i * NT;
         if (e < n)
             put_vec<SPLIT>(tile, kGroupKeys, lo_off, e >> lnv, (e & (nv - 1)) * VEC, R.v[i]);
     }
@@ -441,7 +441,7 @@ template <int N, int NB = 0>
 __device__ __forceinline__ void ld_cols(uint32_t tmem, int col_a, float *a, int col_b = 0, float *b = nullptr)
 {
     static_assert(N % 16 == 0 && (NB == 0 || NB == N), "whole 16-column loads");
-    const uint32_t base = tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16);
+    const uint32_t base = tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16);  // warp w: lanes 32*(w%4)..
     uint32_t va[N / 16][16], vb[NB ? N / 16 : 1][16];
 #pragma unroll
     for (int c = 0; c < N / 16; ++c) {
@@ -465,13 +465,18 @@ constexpr uint32_t TM_S = 0, TM_DP = 64, TM_ACC = 128, TM_ACC2 = 192;
 // zeroes n bytes of shared memory from p (16-byte multiples)
 __device__ __forceinline__ void zero_smem(uint8_t *p, int n)
 {
-    for (int i = threadIdx.x; i < n / 16; i += kThr)
+    for (int i = threadIdx.x; i < n / 16; i += blockDim.x)
         ((uint4 *)p)[i] = make_uint4(0, 0, 0, 0);
 }
 
+// The query-tile kernels (forward, dQ) run two threads per tile row (256
+// threads): thread r + 128 hc takes key columns 32 hc .. 32 hc + 31 of row
+// r's S, P and dS, and output columns 16 hc + 32 i.
+constexpr int kRowThr = 2 * kThr;
+
 // ---------------------------------------------------------------- forward
 template <bool SPLIT, int BS>
-__global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
+__global__ void __launch_bounds__(kRowThr, 1) fwd_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -483,14 +488,15 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     const UnionBuf up = union_buf(g);
     // plan: Q [128][Dp] | K [64][Dp] | V [64][Dp] (read MN-major by P V) |
     // P [128][64] (each with its low part right after it) | union buffer |
-    // barrier, wait context, TMEM slot
+    // barrier, wait context, TMEM slot | the halves' row statistics
     const uint32_t QB = 128 * Dp * 2, KB = NK * Dp * 2, VB = KB, PB = 128 * kKeyPad * 2;
     uint8_t *q_t = sm, *k_t = q_t + parts * QB, *v_t = k_t + parts * KB, *p_t = v_t + parts * VB;
     int *ubuf = (int *)(p_t + parts * PB);
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
     Sync sy;
+    float *xchg = (float *)(misc + 64);  // [2 halves][m, l][128 rows]
     const uint32_t tmem = g_start(misc, p, sy);
-    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
     zero_smem(sm, parts * (QB + KB + VB + PB));
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     const uint32_t *my_mask = union_mask(ubuf) + (rvalid ? tl : 0) * words;
     const uint32_t qs = smem_u32(q_t), ks = smem_u32(k_t), vs = smem_u32(v_t), ps = smem_u32(p_t);
     // the row's q (zero for rows past the tile's tokens)
-    {
+    if (hc == 0) {
         RowRegs qr;
         fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, kvh * G + hh, t) : 0, rvalid, qr);
         store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
@@ -526,66 +532,77 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
         }
     };
     bool ok = true;
-    // pass 1: the row's maximum m and sum l of exp2(scale_l2 * s), over its keys
+    // pass 1: the maximum m and sum l of exp2(scale_l2 * s) over the row's
+    // keys in this thread's columns, then the two halves' combined
     float m = -INFINITY, l = 0.f;
     BlockRegs kr, vr;  // the next group's K (and V), fetched while the MMAs run
     if (NG > 0)
-        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
+        fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, 0, U, kr);
     for (int gi = 0; gi < NG && ok; ++gi) {
-        store_group<SPLIT>(g, kr, ks, KB);
+        store_group<SPLIT, kRowThr>(g, kr, ks, KB);
         to_mma();
-        if (r == 0)
+        if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
         if (gi + 1 < NG)
-            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
+            fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
         if (!(ok = commit_wait(sy)))
             break;
         int k0s[GB];
         bool sel[GB];
         group_blocks(gi, k0s, sel);
-        float sc[NK];
-        ld_cols<NK>(tmem, TM_S, sc);
+        constexpr int NH = NK / 2;
+        const int c1 = hc * NH;
+        float sc[NH];
+        ld_cols<NH>(tmem, TM_S + c1, sc);
         // the group's maximum first, then its terms against the new maximum
         float bm = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < NK; ++c) {
-            const int key = k0s[c / bs] + c % bs;
-            sc[c] = (sel[c / bs] && key >= klo && key <= khi) ? sc[c] * g.scale_l2 : -INFINITY;
-            bm = fmaxf(bm, sc[c]);
+        for (int x = 0; x < NH; ++x) {
+            const int c = c1 + x, key = k0s[c / bs] + c % bs;
+            sc[x] = (sel[c / bs] && key >= klo && key <= khi) ? sc[x] * g.scale_l2 : -INFINITY;
+            bm = fmaxf(bm, sc[x]);
         }
         if (bm != -INFINITY) {
             const float mn = fmaxf(m, bm);
             float sum = 0.f;
 #pragma unroll
-            for (int c = 0; c < NK; ++c)
-                sum += ex2(sc[c] - mn);  // exp2(-inf) = 0 off the row's keys
+            for (int x = 0; x < NH; ++x)
+                sum += ex2(sc[x] - mn);  // exp2(-inf) = 0 off the row's keys
             l = l * ex2(m - mn) + sum;
             m = mn;
         }
     }
+    xchg[(hc * 2) * kThr + r] = m;
+    xchg[(hc * 2 + 1) * kThr + r] = l;
+    __syncthreads();
+    {  // both halves combine the same two pairs in the same order
+        const float m0 = xchg[r], l0 = xchg[kThr + r], m1 = xchg[2 * kThr + r], l1 = xchg[3 * kThr + r];
+        m = fmaxf(m0, m1);
+        l = m == -INFINITY ? 0.f : l0 * ex2(m0 - m) + l1 * ex2(m1 - m);
+    }
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
     // pass 2: P = exp2(scale_l2 s - lse2) on the row's keys, O += P V
     if (NG > 0 && ok) {
-        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
-        fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, 0, U, vr);
+        fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, 0, U, kr);
+        fetch_group<SPLIT, BS, kRowThr>(g, p.v, b, kvh, list, 0, U, vr);
     }
     for (int gi = 0; gi < NG && ok; ++gi) {
-        store_group<SPLIT>(g, kr, ks, KB);
-        store_group<SPLIT>(g, vr, vs, VB);
+        store_group<SPLIT, kRowThr>(g, kr, ks, KB);
+        store_group<SPLIT, kRowThr>(g, vr, vs, VB);
         to_mma();
-        if (r == 0)
+        if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
         if (gi + 1 < NG) {
-            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
-            fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
+            fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
+            fetch_group<SPLIT, BS, kRowThr>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
         }
         if (!(ok = commit_wait(sy)))
             break;
         int k0s[GB];
         bool sel[GB];
         group_blocks(gi, k0s, sel);
-#pragma unroll
-        for (int c1 = 0; c1 < NK; c1 += 32) {
+        {
+            const int c1 = hc * 32;
             float sc[32];
             ld_cols<32>(tmem, TM_S + c1, sc);
 #pragma unroll
@@ -602,7 +619,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
             }
         }
         to_mma();
-        if (r == 0)  // O += P V, V read MN-major from its plain tile
+        if (threadIdx.x == 0)  // O += P V, V read MN-major from its plain tile
             product_bmn<SPLIT>(tmem + TM_ACC, ps, 128, PB, vs, NK, VB, idO, NK / 16, gi > 0);
         ok = commit_wait(sy);
     }
@@ -611,7 +628,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
     if (ok) {
         const int64_t oo = rvalid ? o_off(g, b, kvh * G + hh, t) : 0;
         float acc[16];
-        for (int c0 = 0; c0 < g.D; c0 += 16) {
+        for (int c0 = hc * 16; c0 < g.D; c0 += 32) {
             if (U > 0)
                 ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
@@ -620,7 +637,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
                     if (c0 + x < g.D)
                         out_at<SPLIT>(p.o, oo + c0 + x, (U > 0 && lse2 != -INFINITY) ? acc[x] : 0.f);
         }
-        if (rvalid)
+        if (rvalid && hc == 0)
             p.lse_out[stat_off(g, b, kvh * G + hh, t)] = lse2 == -INFINITY ? -INFINITY : lse2 * 0.6931471805599453f;
     }
     g_end(tmem, sy, p);
@@ -628,7 +645,7 @@ __global__ void __launch_bounds__(kThr, 1) fwd_gtc_kernel(const GParams p)
 
 // --------------------------------------------------------------------- dQ
 template <bool SPLIT, int BS>
-__global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
+__global__ void __launch_bounds__(kRowThr, 1) dq_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -647,7 +664,7 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
     Sync sy;
     const uint32_t tmem = g_start(misc, p, sy);
-    const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
     zero_smem(sm, parts * (2 * QB + 2 * KB + PB));
@@ -668,11 +685,9 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     float l2 = -INFINITY, dl = 0.f;
     {
         const int h = kvh * G + hh;
-        RowRegs rr;
-        fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
-        store_row<SPLIT>(g, rr, qs, QB, r, 0, 0, 0);
-        fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
-        store_row<SPLIT>(g, rr, dos, QB, r, 0, 0, 0);
+        RowRegs rr;  // the row of Q (hc = 0) or of dO (hc = 1)
+        fetch_row<SPLIT>(g, hc ? p.dO : p.q, !rvalid ? 0 : hc ? o_off(g, b, h, t) : q_off(g, b, h, t), rvalid, rr);
+        store_row<SPLIT>(g, rr, hc ? dos : qs, QB, r, 0, 0, 0);
         if (rvalid) {
             const int64_t so = stat_off(g, b, h, t);
             l2 = p.lse[so] * 1.4426950408889634f;
@@ -683,20 +698,20 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
     bool ok = true;
     BlockRegs kr, vr;  // the next group's K and V, fetched while the MMAs run
     if (NG > 0) {
-        fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, 0, U, kr);
-        fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, 0, U, vr);
+        fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, 0, U, kr);
+        fetch_group<SPLIT, BS, kRowThr>(g, p.v, b, kvh, list, 0, U, vr);
     }
     for (int gi = 0; gi < NG && ok; ++gi) {
-        store_group<SPLIT>(g, kr, ks, KB);
-        store_group<SPLIT>(g, vr, vs, KB);
+        store_group<SPLIT, kRowThr>(g, kr, ks, KB);
+        store_group<SPLIT, kRowThr>(g, vr, vs, KB);
         to_mma();
-        if (r == 0)
+        if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, NK, KB, idS, Dp / 16, false);
-        else if (r == kIssuer2)
+        else if (threadIdx.x == kIssuer2)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, NK, KB, idS, Dp / 16, false);
         if (gi + 1 < NG) {
-            fetch_group<SPLIT, BS>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
-            fetch_group<SPLIT, BS>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
+            fetch_group<SPLIT, BS, kRowThr>(g, p.k, b, kvh, list, (gi + 1) * GB, U, kr);
+            fetch_group<SPLIT, BS, kRowThr>(g, p.v, b, kvh, list, (gi + 1) * GB, U, vr);
         }
         if (!(ok = commit_wait(sy)))
             break;
@@ -710,8 +725,8 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
             k0s[e] = j * bs;
             sel[e] = j >= 0 && rvalid && l2 != -INFINITY && qtile_selects(g, my_mask, klo, khi, j);
         }
-#pragma unroll
-        for (int c1 = 0; c1 < NK; c1 += 32) {
+        {
+            const int c1 = hc * 32;
             float sc[32], dp[32];
             ld_cols<32, 32>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
 #pragma unroll
@@ -728,14 +743,14 @@ __global__ void __launch_bounds__(kThr, 1) dq_gtc_kernel(const GParams p)
             }
         }
         to_mma();
-        if (r == 0)  // dQ += dS K, K read MN-major from its plain tile
+        if (threadIdx.x == 0)  // dQ += dS K, K read MN-major from its plain tile
             product_bmn<SPLIT>(tmem + TM_ACC, dss, 128, PB, ks, NK, KB, idQ, NK / 16, gi > 0);
         ok = commit_wait(sy);
     }
     if (ok) {
         float acc[16];
         const int64_t qo = rvalid ? dq_off(g, b, kvh * G + hh, t) : 0;
-        for (int c0 = 0; c0 < g.D; c0 += 16) {
+        for (int c0 = hc * 16; c0 < g.D; c0 += 32) {
             if (U > 0)
                 ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
@@ -1274,11 +1289,11 @@ template <bool S, int B> struct DkdvK {
     static constexpr GKernel fn = dkdv_gtc_kernel<S, B>;
 };
 
-cudaError_t launch_g(GKernel k, int grid, size_t smem, const GParams &p, cudaStream_t st)
+cudaError_t launch_g(GKernel k, int grid, size_t smem, const GParams &p, cudaStream_t st, int threads = kThr)
 {
     if (!smem_ok(k, smem))
         return cudaErrorInvalidValue;
-    k<<<grid, kThr, smem, st>>>(p);
+    k<<<grid, threads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1363,10 +1378,10 @@ cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const voi
     p.ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
     const size_t smem = 1024 + parts * (size_t)(128 * p.Dp * 2 + 2 * kGroupKeys * p.Dp * 2 + 128 * kKeyPad * 2) +
-                        union_bytes(g) + 64;
+                        union_bytes(g) + 64 + 4 * kThr * 4;
     if (p.ntiles < 1)
         return cudaSuccess;
-    return launch_g(pick<FwdK>(dtype, g.bs), p.ntiles, smem, p, st);
+    return launch_g(pick<FwdK>(dtype, g.bs), p.ntiles, smem, p, st, kRowThr);
 }
 
 cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
@@ -1391,7 +1406,7 @@ cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
-    return launch_g(pick<DqK>(dtype, g.bs), p.ntiles, smem, p, st);
+    return launch_g(pick<DqK>(dtype, g.bs), p.ntiles, smem, p, st, kRowThr);
 }
 
 cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
