@@ -303,7 +303,8 @@ __device__ __forceinline__ void put_vec(uint32_t tile, int R, uint32_t lo_off, i
 }
 
 // A key block of a kv-shaped tensor in registers: this thread's vector i is
-// vector e = threadIdx.x + i * kThr of the block (key e / (D / VEC), columns
+// vector e = (threadIdx.x % kThr) + i * kThr of the block (each 128 threads
+// of a larger CTA cover the whole block) (key e / (D / VEC), columns
 // from (e % (D / VEC)) * VEC); keys past the sequence's end read as zeros.
 constexpr int kBlkVec = 8;  // bs * D / VEC <= 1024 vectors per block
 struct BlockRegs {
@@ -318,7 +319,7 @@ __device__ __forceinline__ void fetch_block(const Geo &g, const void *src, int b
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = g.bs * nv, nk = min(g.bs, seq_len_k(g, b) - k0);
 #pragma unroll
     for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
+        const int e = (threadIdx.x & (kThr - 1)) + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
         R.v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (e < n && key < nk)
             R.v[i] = __ldg((const uint4 *)((const uint8_t *)src + (kv_off(g, b, kvh, k0 + key) + c) * In<SPLIT>::ES));
@@ -334,7 +335,7 @@ __device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, ui
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = g.bs * nv;
 #pragma unroll
     for (int i = 0; i < kBlkVec; ++i) {
-        const int e = threadIdx.x + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
+        const int e = (threadIdx.x & (kThr - 1)) + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
         if (e >= n)
             continue;
         if (!transposed) {
@@ -471,12 +472,14 @@ __device__ __forceinline__ void zero_smem(uint8_t *p, int n)
 
 // The query-tile kernels (forward, dQ) run two threads per tile row (256
 // threads): thread r + 128 hc takes key columns 32 hc .. 32 hc + 31 of row
-// r's S, P and dS, and output columns 16 hc + 32 i.
+// r's S, P and dS, and output columns 16 hc + 32 i.  MINB = 1 gives each
+// thread the registers of one CTA per SM (grids of at most one tile per SM);
+// MINB = 2 caps them for two resident CTAs (larger grids).
 constexpr int kRowThr = 2 * kThr;
 
 // ---------------------------------------------------------------- forward
-template <bool SPLIT, int BS>
-__global__ void __launch_bounds__(kRowThr, 1) fwd_gtc_kernel(const GParams p)
+template <bool SPLIT, int BS, int MINB>
+__global__ void __launch_bounds__(kRowThr, MINB) fwd_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -644,8 +647,8 @@ __global__ void __launch_bounds__(kRowThr, 1) fwd_gtc_kernel(const GParams p)
 }
 
 // --------------------------------------------------------------------- dQ
-template <bool SPLIT, int BS>
-__global__ void __launch_bounds__(kRowThr, 1) dq_gtc_kernel(const GParams p)
+template <bool SPLIT, int BS, int MINB>
+__global__ void __launch_bounds__(kRowThr, MINB) dq_gtc_kernel(const GParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -765,7 +768,8 @@ __global__ void __launch_bounds__(kRowThr, 1) dq_gtc_kernel(const GParams p)
 
 // ------------------------------------------------------------------ dK/dV
 // One work unit (b, kv head, block j, a run of the block's token list) per
-// CTA.  Per tile of Tt tokens x G heads (128 rows):
+// CTA of two threads per tile row, two CTAs per SM.  Per tile of Tt tokens x
+// G heads (128 rows):
 //   S = Q K_j^T, dP = dO V_j^T, P and dS per row, then
 //   Dp = 64:  [dV^T; dK^T-ish] += [dO^T; Q^T] [P^T; dS^T]^T  (one M = 128 product
 //             whose diagonal blocks are dV^T (lanes 0..63, columns 0..bs-1) and
@@ -774,7 +778,7 @@ __global__ void __launch_bounds__(kRowThr, 1) dq_gtc_kernel(const GParams p)
 // accumulated in TMEM over the unit's tiles; then written out (a whole block)
 // or as fp32 partials of a split block.
 template <bool SPLIT, int BS>
-__global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
+__global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
 {
     const int ui = blockIdx.x;
     if (ui >= p.hdr->n_units)
@@ -783,7 +787,10 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Geo &g = p.g;
     constexpr int bs = BS;
-    constexpr int kCh = bs < 32 ? bs : 32;  // S and dP columns read per TMEM wait
+    // two threads per tile row: thread r + 128 hc forms P and dS for keys
+    // hc bs/2 .. hc bs/2 + bs/2 - 1 of row r, reading 16 columns of S and dP
+    // at a time (with 16-key blocks both threads read the block's 16)
+    constexpr int NH = bs / 2, kCh = NH < 16 ? 16 : NH;
     const int Dp = p.Dp, G = g.G, parts = SPLIT ? 2 : 1;
     const int Tt = tile_tokens(G), nrows = Tt * G;
     const bool stacked = Dp == 64;
@@ -801,7 +808,7 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     const uint32_t ALO = stacked ? AB : AB, BLO = stacked ? 2 * BB : BB;  // low-part offsets
     Sync sy;
     const uint32_t tmem = g_start(misc, p, sy);
-    const int r = threadIdx.x, warp = r >> 5;
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, wq = r >> 5;
     const Unit u = p.units[ui];
     const int b = u.bg / g.Hkv, kvh = u.bg % g.Hkv, j = u.j, k0 = j * bs;
     const int Lk = seq_len_k(g, b), nk = min(bs, Lk - k0);
@@ -809,12 +816,10 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
     __syncthreads();
     const uint32_t ks = smem_u32(k_t), vs = smem_u32(v_t), qs = smem_u32(q_t), dos = smem_u32(do_t);
     const uint32_t as_ = smem_u32(a_t), a2s = smem_u32(a2_t), bs_ = smem_u32(b_t), b2s = smem_u32(b2_t);
-    {
+    {  // K (hc = 0) or V (hc = 1)
         BlockRegs kr;
-        fetch_block<SPLIT>(g, p.k, b, kvh, k0, kr);
-        store_block<SPLIT>(g, kr, ks, KB, Dp, false);
-        fetch_block<SPLIT>(g, p.v, b, kvh, k0, kr);
-        store_block<SPLIT>(g, kr, vs, KB, Dp, false);
+        fetch_block<SPLIT>(g, hc ? p.v : p.k, b, kvh, k0, kr);
+        store_block<SPLIT>(g, kr, hc ? vs : ks, KB, Dp, false);
     }
     int tl, hh;
     qrow(G, r, tl, hh);
@@ -829,13 +834,17 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
         const int t = rvalid ? (g.dense ? csr0 + pos : p.rows[csr0 + pos]) : 0;
         const int h = kvh * G + hh;
         float l2 = 0.f, dl = 0.f;
-        // the row's q and dO, plain and transposed (zeros for rows past the list)
+        // the row's dO (hc = 0) or q (hc = 1), plain and transposed (zeros
+        // for rows past the list)
         {
             RowRegs rr;
-            fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
-            store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
-            fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
-            store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
+            if (hc == 0) {
+                fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
+                store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
+            } else {
+                fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
+                store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
+            }
             if (rvalid) {
                 const int64_t so = stat_off(g, b, h, t);
                 l2 = p.lse[so] * 1.4426950408889634f;
@@ -843,9 +852,9 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
             }
         }
         to_mma();
-        if (r == 0)
+        if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
-        else if (r == kIssuer2)
+        else if (threadIdx.x == kIssuer2)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
         if (!(ok = commit_wait(sy)))
             break;
@@ -853,12 +862,14 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
         const int cdiag = rvalid ? kdiag(g, b, t) : -1;
         const int khi = rvalid ? min(cdiag, Lk - 1) : -1, klo = key_lo(g, cdiag);
         const bool live = rvalid && l2 != -INFINITY;
-#pragma unroll
-        for (int c1 = 0; c1 < bs; c1 += kCh) {
+        {
+            const int c1 = NH < 16 ? 0 : hc * NH;
             float sc[kCh], dp[kCh];
             ld_cols<kCh, kCh>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
 #pragma unroll
             for (int x = 0; x < kCh; ++x) {
+                if (NH < 16 && x / NH != hc)  // x stays a compile-time register index
+                    continue;
                 const int c = c1 + x, key = k0 + c;
                 const float pv = (live && key >= klo && key <= khi) ? ex2(sc[x] * g.scale_l2 - l2) : 0.f;
                 const float dsv = pv * (dp[x] - dl);
@@ -872,28 +883,29 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
             }
         }
         to_mma();
-        if (r == 0) {
+        if (threadIdx.x == 0) {
             if (stacked)
                 product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, 2 * bs, BLO, idA, 128 / 16, ti > 0);
             else
                 product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, bs, BLO, idA, 128 / 16, ti > 0);
-        } else if (r == kIssuer2 && !stacked) {
+        } else if (threadIdx.x == kIssuer2 && !stacked) {
             product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
         }
         ok = commit_wait(sy);
     }
     // epilogue: lane r holds dim r of dV^T (stacked: lanes 0..63) and of dK^T
-    // (stacked: lanes 64..127, columns bs..2bs-1; else the second accumulator)
+    // (stacked: lanes 64..127, columns bs..2bs-1; else the second accumulator);
+    // the two threads of a lane take alternate 16-column pieces of (dV, dK)
     if (ok) {
         const bool direct = u.slot < 0;
         for (int which = 0; which < 2; ++which) {  // 0 dV, 1 dK
-            // warp-uniform columns: stacked warps 0-1 read dV's, 2-3 dK's
+            // warp-uniform columns: stacked lane quarters 0-1 read dV's, 2-3 dK's
             int col, d;
             bool mine;
             if (stacked) {
-                col = TM_ACC + (warp >= 2 ? bs : 0);
+                col = TM_ACC + (wq >= 2 ? bs : 0);
                 d = r & 63;
-                mine = (which == 0) == (warp < 2);
+                mine = (which == 0) == (wq < 2);
             } else {
                 col = which == 0 ? TM_ACC : TM_ACC2;
                 d = r;
@@ -901,6 +913,8 @@ __global__ void __launch_bounds__(kThr, 1) dkdv_gtc_kernel(const GParams p)
             }
             const float mul = which == 1 ? g.scale : 1.f;
             for (int c1 = 0; c1 < bs; c1 += 16) {
+                if (((which * (bs / 16) + c1 / 16) & 1) != hc)
+                    continue;
                 float ac[16];
                 ld_cols<16>(tmem, col + c1, ac);  // every lane: a warp-wide load
                 if (!mine || d >= g.D)
@@ -1279,11 +1293,17 @@ template <template <bool, int> class K> GKernel pick(int dtype, int bs)
         return bs == 16 ? K<true, 16>::fn : bs == 32 ? K<true, 32>::fn : K<true, 64>::fn;
     return bs == 16 ? K<false, 16>::fn : bs == 32 ? K<false, 32>::fn : K<false, 64>::fn;
 }
-template <bool S, int B> struct FwdK {
-    static constexpr GKernel fn = fwd_gtc_kernel<S, B>;
+template <bool S, int B> struct FwdK1 {
+    static constexpr GKernel fn = fwd_gtc_kernel<S, B, 1>;
 };
-template <bool S, int B> struct DqK {
-    static constexpr GKernel fn = dq_gtc_kernel<S, B>;
+template <bool S, int B> struct FwdK2 {
+    static constexpr GKernel fn = fwd_gtc_kernel<S, B, 2>;
+};
+template <bool S, int B> struct DqK1 {
+    static constexpr GKernel fn = dq_gtc_kernel<S, B, 1>;
+};
+template <bool S, int B> struct DqK2 {
+    static constexpr GKernel fn = dq_gtc_kernel<S, B, 2>;
 };
 template <bool S, int B> struct DkdvK {
     static constexpr GKernel fn = dkdv_gtc_kernel<S, B>;
@@ -1381,7 +1401,11 @@ cudaError_t launch_fwd_gtc(const Geo &g, const void *q, const void *k, const voi
                         union_bytes(g) + 64 + 4 * kThr * 4;
     if (p.ntiles < 1)
         return cudaSuccess;
-    return launch_g(pick<FwdK>(dtype, g.bs), p.ntiles, smem, p, st, kRowThr);
+    // two CTAs per SM once the grid has more tiles than SMs (measured: T = 8192
+    // bf16 D = 64 forward 1.16 -> 0.75 ms; at one tile per SM the full
+    // register budget is the faster)
+    const GKernel kern = p.ntiles > num_sms() ? pick<FwdK2>(dtype, g.bs) : pick<FwdK1>(dtype, g.bs);
+    return launch_g(kern, p.ntiles, smem, p, st, kRowThr);
 }
 
 cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
@@ -1406,7 +1430,11 @@ cudaError_t launch_dq_gtc(const Geo &g, const void *q, const void *k, const void
                         union_bytes(g) + 64;
     if (p.ntiles < 1)
         return cudaSuccess;
-    return launch_g(pick<DqK>(dtype, g.bs), p.ntiles, smem, p, st, kRowThr);
+    // as the forward, but split precision keeps one CTA per SM: its register
+    // cap for two spills and measured slower at every size
+    const bool two = dtype == NSA_DTYPE_BF16 && p.ntiles > num_sms();
+    const GKernel kern = two ? pick<DqK2>(dtype, g.bs) : pick<DqK1>(dtype, g.bs);
+    return launch_g(kern, p.ntiles, smem, p, st, kRowThr);
 }
 
 cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
@@ -1436,7 +1464,7 @@ cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const vo
     const size_t smem = 1024 + parts * tiles + 64;
     if (max_units < 1)
         return cudaSuccess;
-    return launch_g(pick<DkdvK>(dtype, g.bs), max_units, smem, p, st);
+    return launch_g(pick<DkdvK>(dtype, g.bs), max_units, smem, p, st, kRowThr);
 }
 
 }  // namespace nsa

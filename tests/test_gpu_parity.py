@@ -794,6 +794,10 @@ def test_causal_own_key_lengths(dtype, shape, lq, lk, br, window):
     (torch.float32, (1, 2, 1, 128, 32, 16, 4)),     # the small fp32 fwd+bwd workload
     (torch.bfloat16, (1, 16, 2, 300, 128, 32, 6)),  # D = 128, 32-key blocks
     (torch.bfloat16, (2, 8, 1, 257, 32, 64, 3)),    # D = 32 (padded), 64-key blocks, G = 8
+    # 175 query tiles of 8 tokens, more than the GPU has SMs: the launches that
+    # keep two CTAs per SM (forward in both types, dQ in bf16)
+    (torch.bfloat16, (1, 16, 1, 1400, 64, 32, 6)),
+    (torch.float32, (1, 16, 1, 1400, 64, 32, 6)),
 ])
 def test_other_shapes_run_on_tensor_cores(dtype, shape):
     """These shapes launch the tensor-core kernels of k_gtc.cu (seen through
