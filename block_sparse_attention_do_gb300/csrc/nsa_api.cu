@@ -1,10 +1,13 @@
 // nsa_api.cu -- the C ABI of libnsa.so (include/nsa.h): argument checks,
 // workspace carving and the launch sequence of each entry point.  No entry
-// point allocates memory or synchronises; all work goes on the caller's
-// stream.
+// point allocates memory or synchronises; all work is ordered on the
+// caller's stream (a launch that may run beside it goes on a helper stream
+// forked from and joined back to it by events).
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "launch.h"
 
@@ -249,6 +252,74 @@ struct TraceScope {
         NSA_TRY(expr);                                 \
     } while (0)
 
+// ---- a helper stream per device, for a launch that can run beside the
+// ones that follow it on the caller's stream (the other-shapes dQ needs
+// only delta, so it runs beside the index build and dK/dV).  Created on
+// first use; kept for the process.
+struct Helper {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;  // held from a fork to its join: the two events are shared
+};
+constexpr int kMaxDevices = 64;
+Helper g_helpers[kMaxDevices];
+std::mutex g_helpers_mu;
+
+Helper *helper_of_current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_helpers_mu);
+    Helper &h = g_helpers[dev];
+    if (!h.s) {
+        cudaStream_t s = nullptr;
+        cudaEvent_t a = nullptr, b = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+            if (s)
+                cudaStreamDestroy(s);
+            if (a)
+                cudaEventDestroy(a);
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        h.fork = a;
+        h.join = b;
+        h.s = s;
+    }
+    return &h;
+}
+
+// begin(): work launched on side() from here on starts after everything
+// enqueued on st so far; at scope exit st waits for it.  Without a helper
+// (or before begin) side() is st itself: the launches stay in order.
+struct Fork {
+    cudaStream_t st;
+    Helper *h = nullptr;
+    bool forked = false;
+    std::unique_lock<std::mutex> lk;
+    explicit Fork(cudaStream_t s) : st(s) {}
+    void begin()
+    {
+        if (forked || !(h = helper_of_current_device()))
+            return;
+        lk = std::unique_lock<std::mutex>(h->mu);
+        forked = cudaEventRecord(h->fork, st) == cudaSuccess && cudaStreamWaitEvent(h->s, h->fork, 0) == cudaSuccess;
+        if (!forked) {
+            (void)cudaGetLastError();
+            lk.unlock();
+        }
+    }
+    cudaStream_t side() const { return forked ? h->s : st; }
+    ~Fork()
+    {
+        if (forked && (cudaEventRecord(h->join, h->s) != cudaSuccess || cudaStreamWaitEvent(st, h->join, 0) != cudaSuccess))
+            cudaStreamSynchronize(h->s);  // the join failed: order by waiting instead
+    }
+};
+
 nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 {
     if (!ws || ((uintptr_t)ws & (kAlign - 1)) || ws_bytes < need)
@@ -304,14 +375,18 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 // and an ordered per-chunk fill; otherwise one atomic count pass and one
 // ordered walk per block list.  Both give the same canonical lists.
 // dot (nullable, chunked build only): delta computed in the count's launch
+// fork (nullable, with dot): begun once the count's launch (and so delta)
+// is enqueued
 nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
                      Unit *units, int *nchunk, int *slot, WsHeader *hdr, int *err, int chunk, cudaStream_t st,
-                     int *chunk_counts = nullptr, const DotArgs *dot = nullptr)
+                     int *chunk_counts = nullptr, const DotArgs *dot = nullptr, Fork *fork = nullptr)
 {
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     if (!g.dense && chunk_counts && csr_chunked_ok(g)) {
         NSA_LAUNCH(dot ? "do_dot+csr_count" : "csr_count",
                    launch_csr_chunk_count(g, idx, chunk_counts, counts, err, st, dot));
+        if (dot && fork)
+            fork->begin();
         NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
         NSA_LAUNCH("csr_fill", launch_csr_chunk_fill(g, idx, chunk_counts, offsets, rows, st));
         return NSA_OK;
@@ -329,13 +404,13 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
 // Builds the plan of `idx` at `plan8` (layout L); index errors go to *err.
 // With dot, delta is computed in the same pass (see build_csr).
 nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanLayout &L, int *err, cudaStream_t st,
-                      const DotArgs *dot = nullptr)
+                      const DotArgs *dot = nullptr, Fork *fork = nullptr)
 {
     WsHeader *phdr = (WsHeader *)plan8;
     NSA_TRY(cudaMemsetAsync(phdr, 0, sizeof(WsHeader), st));
     return build_csr(g, idx, (int *)(plan8 + L.counts), (int *)(plan8 + L.offsets), (int *)(plan8 + L.rows),
                      (Unit *)(plan8 + L.units), (int *)(plan8 + L.nchunk), (int *)(plan8 + L.slot), phdr, err,
-                     L.chunk, st, (int *)(plan8 + L.chunkc), dot);
+                     L.chunk, st, (int *)(plan8 + L.chunkc), dot, fork);
 }
 
 // whether build_plan takes the chunked path (which can carry the dot)
@@ -385,9 +460,17 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     // built here by chunks, else on its own
     const DotArgs dot{o, dO, delta, p->dtype};
     const bool fused = !plan && plan_is_chunked(g);
+    // the other-shapes dQ reads only delta (not the inverse index): it runs
+    // on a helper stream beside the index build and dK/dV, which leave SMs
+    // free (one CTA of ~170 registers a thread per query tile)
+    const bool gtc = !tc_supported(g, p->dtype) && gtc_supported(g, p->dtype);
+    Fork fork(st);
     if (!fused)
         NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
-    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr)) != NSA_OK)
+    if (gtc && !fused)
+        fork.begin();
+    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr, gtc ? &fork : nullptr)) !=
+                     NSA_OK)
         return s;
     if (tc_supported(g, p->dtype)) {
         // the query-tile unions (sparse only): alongside the kernel before,
@@ -401,11 +484,13 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         NSA_LAUNCH("dq_tc",
                    launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, dq, &hdr->err, &hdr->tile_next, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
-    } else if (gtc_supported(g, p->dtype)) {
+    } else if (gtc) {
+        {
+            const cudaStream_t st = fork.side();
+            NSA_LAUNCH("dq_gtc", launch_dq_gtc(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, &hdr->err, st));
+        }
         NSA_LAUNCH("dkdv_gtc", launch_dkdv_gtc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                                partials, dk, dv, p->dtype, &hdr->err, st));
-        NSA_LAUNCH("dq_gtc",
-                   launch_dq_gtc(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, &hdr->err, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else {
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));

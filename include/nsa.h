@@ -32,6 +32,11 @@
  *    declares (dense when they are 0), 16-byte aligned.  The library
  *    never allocates or frees memory and never synchronises: work is
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *    A launch that can run beside the ones after it (the other-shapes dQ
+ *    of a backward) goes on a helper stream the library keeps per device,
+ *    forked from `stream` and joined back to it by events: it starts after
+ *    the work enqueued on `stream` before the call and ends before the work
+ *    enqueued after it, also inside a CUDA-graph capture of `stream`.
  *  - Shape, dtype and layout errors are returned synchronously before any
  *    launch.  Errors found on the device (a bad index entry, a wait that
  *    timed out) are recorded in the workspace and read back with

@@ -290,6 +290,64 @@ def test_runs_on_the_callers_stream():
         assert torch.equal(x, ref[name]), f"{name} differs between streams (must be deterministic)"
 
 
+def test_other_shapes_ordered_on_the_callers_stream():
+    """The other-shapes backward runs its dQ on a helper stream forked from
+    the caller's: it must start after the caller's earlier work (dO written
+    there behind a GPU wait) and end before the caller's later work (a copy
+    of dq), and give the same bits as the same call on the default stream."""
+    B, Hq, Hkv, T, D, bs, S = 2, 6, 2, 1024, 64, 32, 8
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=61)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=61)
+    ref = _run(q, k, v, do, idx, bs)
+    g = [x.to(DEV) for x in (q, k, v, do, idx)]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    do_late = torch.zeros_like(g[3])
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(20_000_000)  # ~10 ms of GPU time before dO exists
+        do_late.copy_(g[3])
+        dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], ref["o"], do_late, ref["lse"], g[4], bs, stream=s)
+        after = [x.clone() for x in (dq, dk, dv)]
+    s.synchronize()
+    for name, x in zip(("dq", "dk", "dv"), after):
+        assert torch.equal(x, ref[name]), f"{name}: not ordered on the caller's stream"
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 4, 1, 256, 128, 64, 4),   # tensor-core kernels for D = 128, 64-key blocks
+    (2, 6, 2, 1024, 64, 32, 8),   # the other shapes (dQ on the helper stream)
+])
+def test_backward_captured_in_a_cuda_graph(shape):
+    """Forward and backward captured once into a CUDA graph and replayed on
+    new inputs give the same bits as direct calls."""
+    B, Hq, Hkv, T, D, bs, S = shape
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=62)
+    idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=62)
+    q2, k2, v2, do2 = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=63)
+    ref = _run(q2, k2, v2, do2, idx, bs)
+    bufs = [x.to(DEV) for x in (q, k, v, do)]
+    gi = idx.to(DEV)
+
+    def step():
+        o, lse = api.sel_fwd(bufs[0], bufs[1], bufs[2], gi, bs)
+        return (o, lse) + tuple(api.sel_bwd(bufs[0], bufs[1], bufs[2], o, bufs[3], lse, gi, bs))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture (workspaces, kernel attributes)
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        outs = step()
+    for dst, src in zip(bufs, (q2, k2, v2, do2)):
+        dst.copy_(src.to(DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    for name, x in zip(("o", "lse", "dq", "dk", "dv"), outs):
+        assert torch.equal(x, ref[name]), f"{name} differs under graph replay"
+
+
 def test_count_pairs():
     B, Hq, Hkv, T, bs, S = 2, 6, 2, 500, 32, 6
     idx = inputs.make_block_idx(B, Hkv, T, bs, S, seed=6)
