@@ -41,6 +41,7 @@ WORKLOAD_NAME = ("NSA selection fwd+bwd, bf16: B=1 Hq=32 Hkv=2 (G=16) T=8192 D=1
                  "block_size=64 S=16, own block + 15 uniform earlier blocks per token")
 # FLOP per selected (query row, key) pair of each kernel's algorithmic work
 ALG_FLOP_PER_PAIR_PER_D = {"dkdv_tc": 8, "dq_tc": 6, "fwd_tc": 4,
+                           "dkdv_gtc": 8, "dq_gtc": 6, "fwd_gtc": 4,
                            "dkdv_simt": 8, "dq_simt": 6, "fwd_simt": 4}
 FLUSH_BYTES = 256 << 20  # > the 129 MB L2
 SWA_WINDOW = 512  # sliding-window leg: keys (t - 512, t]
@@ -504,6 +505,12 @@ def run_ours(args):
         idx2 = inputs.make_block_idx(2, 2, 1024, 32, 8, seed=rank)
         configs["mid_bf16"] = bench_extra(
             "NSA selection bwd, bf16: B=2 Hq=6 Hkv=2 (G=3) T=1024 D=64 block_size=32 S=8",
+            *(x.to(dev) for x in (q2, k2, v2, do2, idx2)), 32, flush, st, n_x, peaks)
+        # ... and in fp32 (split precision: three bf16 products per fp32 product;
+        # the roofline still counts the fp32 work against the bf16 peak)
+        q2, k2, v2, do2 = inputs.make_qkv_do(2, 6, 2, 1024, 64, dtype=torch.float32, seed=rank)
+        configs["mid_fp32"] = bench_extra(
+            "NSA selection bwd, fp32: B=2 Hq=6 Hkv=2 (G=3) T=1024 D=64 block_size=32 S=8",
             *(x.to(dev) for x in (q2, k2, v2, do2, idx2)), 32, flush, st, n_x, peaks)
         del q2, k2, v2, do2, idx2
         # config 4: dense causal B=2 Hq=32 Hkv=8 T=4096 D=128 block 64 (nsa_dense_causal_*)
