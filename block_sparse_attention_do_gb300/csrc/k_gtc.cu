@@ -172,6 +172,24 @@ template <bool SPLIT> __device__ __forceinline__ void out_at(void *base, int64_t
         ((__nv_bfloat16 *)base)[off] = __float2bfloat16_rn(x);
 }
 
+// 16 consecutive output elements x[i] * mul (zeros without `any`) as 16-byte
+// stores: rows start 16-byte aligned and off is a multiple of 16 from a row's
+// start (D is a multiple of 16)
+template <bool SPLIT>
+__device__ __forceinline__ void out16(void *base, int64_t off, const float *x, float mul, bool any)
+{
+    uint32_t w[SPLIT ? 16 : 8];
+#pragma unroll
+    for (int i = 0; i < (SPLIT ? 16 : 8); ++i)
+        w[i] = SPLIT ? __float_as_uint(any ? x[i] * mul : 0.f)
+                     : (uint32_t)bf16_bits(any ? x[2 * i] * mul : 0.f) |
+                           ((uint32_t)bf16_bits(any ? x[2 * i + 1] * mul : 0.f) << 16);
+    uint4 *d = SPLIT ? (uint4 *)((float *)base + off) : (uint4 *)((__nv_bfloat16 *)base + off);
+#pragma unroll
+    for (int i = 0; i < (SPLIT ? 4 : 2); ++i)
+        d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
 // Shared synchronisation of the CTA: the MMA barrier's phase and the wait
 // context (abort flag, limit).  issue_wait: thread 0 commits every MMA it
 // issued so far to the barrier, everyone waits for it; false (on every
@@ -428,6 +446,73 @@ __device__ __forceinline__ void store_row(const Geo &g, const RowRegs &R, uint32
     }
 }
 
+// The query tile's union (as qtile_union_warp builds it) from the whole CTA:
+// every thread reads its share of the tile's index entries at once (one
+// round of loads for a tile of up to 4 entries a thread), then one warp
+// compacts the list.  Holds three CTA-wide barriers; nvalid > 0.
+__device__ __forceinline__ void qtile_union_cta(const Geo &g, const int *idx, const UnionBuf &u, int *buf, int b,
+                                                int kvh, int t0, int nvalid)
+{
+    const int words = (g.nbmax + 31) / 32, tid = threadIdx.x, nt = blockDim.x;
+    uint32_t *mask = union_mask(buf), *ubits = mask + u.mask_words;
+    for (int x = tid; x < u.mask_words + words; x += nt)  // the tokens' bitmaps, then the union's
+        mask[x] = 0u;
+    __syncthreads();
+    if (g.dense) {
+        const int hi = min(kdiag(g, b, t0 + nvalid - 1), seq_len_k(g, b) - 1);
+        const int jmin = key_lo(g, kdiag(g, b, t0)) / g.bs, jmax = hi >= 0 ? hi / g.bs : -1;
+        for (int j = jmin + tid; j <= jmax; j += nt)
+            atomicOr(&ubits[j >> 5], 1u << (j & 31));
+    } else {
+        const int n = nvalid * g.S;
+        for (int x0 = 0; x0 < n; x0 += 4 * nt) {
+            int jv[4];
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int x = x0 + u4 * nt + tid;
+                jv[u4] = x < n ? idx_row(g, idx, b, kvh, t0 + x / g.S)[x % g.S] : -1;
+            }
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                const int x = x0 + u4 * nt + tid;
+                const int tl = x / g.S, t = t0 + tl, j = jv[u4];
+                if (x < n && j >= 0 && j <= t / g.bs && j < g.nbmax) {
+                    atomicOr(&mask[tl * words + (j >> 5)], 1u << (j & 31));
+                    atomicOr(&ubits[j >> 5], 1u << (j & 31));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < 32) {  // ordered compaction
+        const int lane = tid;
+        int *list = union_list(buf, u);
+        int base = 0;
+        for (int w0 = 0; w0 < words; w0 += 32) {
+            const uint32_t bits = (w0 + lane < words) ? ubits[w0 + lane] : 0u;
+            const int cnt = __popc(bits);
+            int incl = cnt;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            int pos = base + incl - cnt;
+            for (uint32_t bb = bits; bb; bb &= bb - 1)
+                list[pos++] = (w0 + lane) * 32 + __ffs(bb) - 1;
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            buf[UH_B] = b;
+            buf[UH_KVH] = kvh;
+            buf[UH_T0] = t0;
+            buf[UH_NVALID] = nvalid;
+            buf[UH_COUNT] = base;
+        }
+    }
+    __syncthreads();
+}
+
 // row r of a query tile: token tl of the tile (rows token-major), head hh of the group
 __device__ __forceinline__ void qrow(int G, int r, int &tl, int &hh)
 {
@@ -499,12 +584,12 @@ __global__ void __launch_bounds__(kRowThr, MINB) fwd_gtc_kernel(const GParams p)
     Sync sy;
     float *xchg = (float *)(misc + 64);  // [2 halves][m, l][128 rows]
     const uint32_t tmem = g_start(misc, p, sy);
-    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
     zero_smem(sm, parts * (QB + KB + VB + PB));
-    if (warp == 0 && nvalid > 0)
-        qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
+    if (nvalid > 0)
+        qtile_union_cta(g, p.idx, up, ubuf, b, kvh, t0, nvalid);
     __syncthreads();
     const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0, NG = (U + GB - 1) / GB;
     const int *list = union_list(ubuf, up);
@@ -635,10 +720,7 @@ __global__ void __launch_bounds__(kRowThr, MINB) fwd_gtc_kernel(const GParams p)
             if (U > 0)
                 ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
-#pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    if (c0 + x < g.D)
-                        out_at<SPLIT>(p.o, oo + c0 + x, (U > 0 && lse2 != -INFINITY) ? acc[x] : 0.f);
+                out16<SPLIT>(p.o, oo + c0, acc, 1.f, U > 0 && lse2 != -INFINITY);
         }
         if (rvalid && hc == 0)
             p.lse_out[stat_off(g, b, kvh * G + hh, t)] = lse2 == -INFINITY ? -INFINITY : lse2 * 0.6931471805599453f;
@@ -667,12 +749,12 @@ __global__ void __launch_bounds__(kRowThr, MINB) dq_gtc_kernel(const GParams p)
     uint8_t *misc = (uint8_t *)ubuf + up.bytes;
     Sync sy;
     const uint32_t tmem = g_start(misc, p, sy);
-    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7;
     int b = 0, kvh = 0, t0 = 0, nvalid = 0;
     qtile_of(g, blockIdx.x, b, kvh, t0, nvalid);
     zero_smem(sm, parts * (2 * QB + 2 * KB + PB));
-    if (warp == 0 && nvalid > 0)
-        qtile_union_warp(g, p.idx, up, ubuf, b, kvh, t0, nvalid, lane);
+    if (nvalid > 0)
+        qtile_union_cta(g, p.idx, up, ubuf, b, kvh, t0, nvalid);
     __syncthreads();
     const int U = nvalid > 0 ? ubuf[UH_COUNT] : 0, NG = (U + GB - 1) / GB;
     const int *list = union_list(ubuf, up);
@@ -757,10 +839,7 @@ __global__ void __launch_bounds__(kRowThr, MINB) dq_gtc_kernel(const GParams p)
             if (U > 0)
                 ld_cols<16>(tmem, TM_ACC + c0, acc);
             if (rvalid)
-#pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    if (c0 + x < g.D)
-                        out_at<SPLIT>(p.dq, qo + c0 + x, U > 0 ? acc[x] * g.scale : 0.f);
+                out16<SPLIT>(p.dq, qo + c0, acc, g.scale, U > 0);
         }
     }
     g_end(tmem, sy, p);
