@@ -900,6 +900,11 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
         fetch_block<SPLIT>(g, hc ? p.v : p.k, b, kvh, k0, kr);
         store_block<SPLIT>(g, kr, hc ? vs : ks, KB, Dp, false);
     }
+    // Launched (selection) as a programmatic dependent of the kernel before
+    // it (the inverse index's fill, or delta with a prebuilt plan): the
+    // set-up above read only the unit list, which a launch before that kernel
+    // wrote; the token rows and delta are read after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int tl, hh;
     qrow(G, r, tl, hh);
     const int csr0 = g.dense ? dense_first(g, b, j) + u.begin : p.offsets[u.bg * g.nbmax + j] + u.begin;
@@ -1388,10 +1393,13 @@ template <bool S, int B> struct DkdvK {
     static constexpr GKernel fn = dkdv_gtc_kernel<S, B>;
 };
 
-cudaError_t launch_g(GKernel k, int grid, size_t smem, const GParams &p, cudaStream_t st, int threads = kThr)
+cudaError_t launch_g(GKernel k, int grid, size_t smem, const GParams &p, cudaStream_t st, int threads = kThr,
+                     bool dependent = false)
 {
     if (!smem_ok(k, smem))
         return cudaErrorInvalidValue;
+    if (dependent)
+        return launch_dependent(k, dim3(grid), dim3(threads), smem, st, p);
     k<<<grid, threads, smem, st>>>(p);
     return cudaGetLastError();
 }
@@ -1543,7 +1551,10 @@ cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const vo
     const size_t smem = 1024 + parts * tiles + 64;
     if (max_units < 1)
         return cudaSuccess;
-    return launch_g(pick<DkdvK>(dtype, g.bs), max_units, smem, p, st, kRowThr);
+    // a programmatic dependent of the inverse index's fill (or, with a plan,
+    // of delta); the dense entry's unit list comes from the kernel just
+    // before (the scan), so that launch waits for it in full
+    return launch_g(pick<DkdvK>(dtype, g.bs), max_units, smem, p, st, kRowThr, !g.dense);
 }
 
 }  // namespace nsa
