@@ -911,35 +911,59 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     const uint32_t idS = idesc_bf16(128, bs, false, false);
     const uint32_t idA = idesc_bf16(128, stacked ? 2 * bs : bs, false, false);
     const int ntiles = (u.count + Tt - 1) / Tt;
+    const int h = kvh * G + hh;
+    // The row's token in tile ti (-1 past the list), and its dO (hc = 0) or
+    // q (hc = 1) row with its LSE and delta: tile ti + 1's token is read
+    // while tile ti's S and dP products run, its row while the dV and dK
+    // products run, so the loads' latency stays off the tile's chain.  (With
+    // 64-key blocks the row is read at the tile's start instead: held across
+    // the tile, its registers would spill.)
+    constexpr bool kRowAhead = BS < 64;
+    auto token_of = [&](int ti) -> int {
+        const int pos = ti * Tt + tl;
+        return (r < nrows && pos < u.count) ? (g.dense ? csr0 + pos : p.rows[csr0 + pos]) : -1;
+    };
+    RowRegs rr;
+    float lse_raw = 0.f, dl = 0.f;
+    auto fetch_row_of = [&](int tk) {
+        const bool v = tk >= 0;
+        if (hc == 0)
+            fetch_row<SPLIT>(g, p.dO, v ? o_off(g, b, h, tk) : 0, v, rr);
+        else
+            fetch_row<SPLIT>(g, p.q, v ? q_off(g, b, h, tk) : 0, v, rr);
+    };
+    auto fetch_tile = [&](int tk) {
+        const bool v = tk >= 0;
+        if (kRowAhead)
+            fetch_row_of(tk);
+        lse_raw = 0.f;
+        dl = 0.f;
+        if (v) {
+            const int64_t so = stat_off(g, b, h, tk);
+            lse_raw = p.lse[so];
+            dl = p.delta[so];
+        }
+    };
+    int t = ntiles > 0 ? token_of(0) : -1;
+    if (ntiles > 0)
+        fetch_tile(t);
     bool ok = true;
     for (int ti = 0; ti < ntiles && ok; ++ti) {
-        const int pos = ti * Tt + tl;
-        const bool rvalid = r < nrows && pos < u.count;
-        const int t = rvalid ? (g.dense ? csr0 + pos : p.rows[csr0 + pos]) : 0;
-        const int h = kvh * G + hh;
-        float l2 = 0.f, dl = 0.f;
-        // the row's dO (hc = 0) or q (hc = 1), plain and transposed (zeros
-        // for rows past the list)
-        {
-            RowRegs rr;
-            if (hc == 0) {
-                fetch_row<SPLIT>(g, p.dO, rvalid ? o_off(g, b, h, t) : 0, rvalid, rr);
-                store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
-            } else {
-                fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, h, t) : 0, rvalid, rr);
-                store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
-            }
-            if (rvalid) {
-                const int64_t so = stat_off(g, b, h, t);
-                l2 = p.lse[so] * 1.4426950408889634f;
-                dl = p.delta[so];
-            }
-        }
+        const bool rvalid = t >= 0;
+        const float l2 = rvalid ? lse_raw * 1.4426950408889634f : 0.f;
+        // the rows, plain and transposed (zeros for rows past the list)
+        if (!kRowAhead)
+            fetch_row_of(t);
+        if (hc == 0)
+            store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
+        else
+            store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
         to_mma();
         if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
         else if (threadIdx.x == kIssuer2)
             product<SPLIT>(tmem + TM_DP, dos, 128, QB, vs, bs, KB, idS, Dp / 16, false);
+        const int tn = ti + 1 < ntiles ? token_of(ti + 1) : -1;
         if (!(ok = commit_wait(sy)))
             break;
         // the row's keys: from the window's left edge to its diagonal
@@ -975,6 +999,9 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
         } else if (threadIdx.x == kIssuer2 && !stacked) {
             product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
         }
+        if (ti + 1 < ntiles)
+            fetch_tile(tn);
+        t = tn;
         ok = commit_wait(sy);
     }
     // epilogue: lane r holds dim r of dV^T (stacked: lanes 0..63) and of dK^T
