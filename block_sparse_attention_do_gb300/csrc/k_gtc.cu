@@ -163,6 +163,24 @@ __device__ __forceinline__ void product_bmn(uint32_t d, uint32_t a, int Ra, uint
     }
 }
 
+// D (+)= A B over nk K-steps, both operands MN-major: A a K-major tile read
+// by columns whose 64-column chunks (the M index) lie a_lbo bytes apart
+// (within one tile, or two tiles placed that far apart), B as product_bmn
+template <bool SPLIT>
+__device__ __forceinline__ void product_mn(uint32_t d, uint32_t a, uint32_t a_lbo, uint32_t alo, uint32_t b, int Rb,
+                                           uint32_t blo, uint32_t idesc, int nk, bool acc)
+{
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint32_t on = (acc || kk > 0) ? 1u : 0u;
+        const uint64_t ad = sdesc_sw128(a + kk * 2048, a_lbo, 1024);
+        mma_bf16(d, ad, mndesc(b, Rb, kk), idesc, on);
+        if (SPLIT) {
+            mma_bf16(d, ad, mndesc(b + blo, Rb, kk), idesc, 1u);
+            mma_bf16(d, sdesc_sw128(a + alo + kk * 2048, a_lbo, 1024), mndesc(b, Rb, kk), idesc, 1u);
+        }
+    }
+}
+
 // output element (bf16 or fp32 by SPLIT)
 template <bool SPLIT> __device__ __forceinline__ void out_at(void *base, int64_t off, float x)
 {
@@ -846,6 +864,9 @@ __global__ void __launch_bounds__(kRowThr, MINB) dq_gtc_kernel(const GParams p)
 }
 
 // ------------------------------------------------------------------ dK/dV
+// width (columns) of the stacked P / dS tile for blocks of bs keys
+constexpr int stacked_pw(int bs) { return 2 * bs <= 64 ? 64 : 2 * bs; }
+
 // One work unit (b, kv head, block j, a run of the block's token list) per
 // CTA of two threads per tile row, two CTAs per SM.  Per tile of Tt tokens x
 // G heads (128 rows):
@@ -873,18 +894,19 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     const int Dp = p.Dp, G = g.G, parts = SPLIT ? 2 : 1;
     const int Tt = tile_tokens(G), nrows = Tt * G;
     const bool stacked = Dp == 64;
-    // plan: K, V [bs][Dp] | Q, dO [128][Dp] | transposed A: stacked [dO^T; Q^T]
-    // [128][128 rows], else dO^T and Q^T [128][128 rows] each | transposed B:
-    // stacked [P^T; dS^T] [2 bs][128 rows], else P^T and dS^T [bs][128 rows]
-    // each (low parts right after each) | misc
-    const uint32_t KB = bs * Dp * 2, QB = 128 * Dp * 2, AB = 128 * 128 * 2, BB = bs * 128 * 2;
-    uint8_t *k_t = sm, *v_t = k_t + parts * KB, *q_t = v_t + parts * KB, *do_t = q_t + parts * QB;
-    uint8_t *a_t = do_t + parts * QB;                                      // dO^T (stacked: [dO^T; Q^T])
-    uint8_t *a2_t = a_t + (stacked ? 0 : parts * AB);                      // Q^T (separate)
-    uint8_t *b_t = a_t + parts * AB * (stacked ? 1 : 2);                   // P^T (stacked: [P^T; dS^T])
-    uint8_t *b2_t = b_t + (stacked ? 0 : parts * BB);                      // dS^T (separate)
-    uint8_t *misc = b_t + parts * BB * 2;
-    const uint32_t ALO = stacked ? AB : AB, BLO = stacked ? 2 * BB : BB;  // low-part offsets
+    // plan: K, V [bs][Dp] | dO, Q [128][Dp] | P and dS: stacked one [128][PW]
+    // tile (row r: P's bs keys, then dS's), else a [128][64] tile each (low
+    // parts right after each) | misc.  dO and Q are the K-major A operands of
+    // S and dP and, read by columns (MN-major), the A operands of dV^T and
+    // dK^T; P and dS are read by columns as their B operands.  Stacked, Q
+    // sits right after dO, so [dO^T; Q^T] is one M = 128 operand of two
+    // 64-dim chunks parts * QB bytes apart.
+    constexpr int PW = stacked_pw(BS);  // stacked P / dS tile width: 2 bs columns, padded to a 64-column chunk
+    const uint32_t KB = bs * Dp * 2, QB = 128 * Dp * 2, PB = 128 * (stacked ? PW : kKeyPad) * 2;
+    uint8_t *k_t = sm, *v_t = k_t + parts * KB, *do_t = v_t + parts * KB, *q_t = do_t + parts * QB;
+    uint8_t *p_t = q_t + parts * QB;                       // P (stacked: P and dS)
+    uint8_t *ds_t = p_t + (stacked ? 0 : parts * PB);      // dS (separate)
+    uint8_t *misc = p_t + parts * PB * (stacked ? 1 : 2);
     Sync sy;
     const uint32_t tmem = g_start(misc, p, sy);
     const int r = threadIdx.x & (kThr - 1), hc = threadIdx.x >> 7, wq = r >> 5;
@@ -894,7 +916,7 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     zero_smem(sm, (int)(misc - sm));
     __syncthreads();
     const uint32_t ks = smem_u32(k_t), vs = smem_u32(v_t), qs = smem_u32(q_t), dos = smem_u32(do_t);
-    const uint32_t as_ = smem_u32(a_t), a2s = smem_u32(a2_t), bs_ = smem_u32(b_t), b2s = smem_u32(b2_t);
+    const uint32_t ps = smem_u32(p_t), dss = smem_u32(ds_t);
     {  // K (hc = 0) or V (hc = 1)
         BlockRegs kr;
         fetch_block<SPLIT>(g, hc ? p.v : p.k, b, kvh, k0, kr);
@@ -909,7 +931,7 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     qrow(G, r, tl, hh);
     const int csr0 = g.dense ? dense_first(g, b, j) + u.begin : p.offsets[u.bg * g.nbmax + j] + u.begin;
     const uint32_t idS = idesc_bf16(128, bs, false, false);
-    const uint32_t idA = idesc_bf16(128, stacked ? 2 * bs : bs, false, false);
+    const uint32_t idA = idesc_bf16(128, stacked ? 2 * bs : bs, true, true);
     const int ntiles = (u.count + Tt - 1) / Tt;
     const int h = kvh * G + hh;
     // The row's token in tile ti (-1 past the list), and its dO (hc = 0) or
@@ -951,13 +973,10 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     for (int ti = 0; ti < ntiles && ok; ++ti) {
         const bool rvalid = t >= 0;
         const float l2 = rvalid ? lse_raw * 1.4426950408889634f : 0.f;
-        // the rows, plain and transposed (zeros for rows past the list)
+        // the rows (zeros for rows past the list)
         if (!kRowAhead)
             fetch_row_of(t);
-        if (hc == 0)
-            store_row<SPLIT>(g, rr, dos, QB, r, as_, ALO, 0);
-        else
-            store_row<SPLIT>(g, rr, qs, QB, r, stacked ? as_ : a2s, ALO, stacked ? 64 : 0);
+        store_row<SPLIT>(g, rr, hc == 0 ? dos : qs, QB, r, 0, 0, 0);
         to_mma();
         if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);
@@ -974,31 +993,30 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
             const int c1 = NH < 16 ? 0 : hc * NH;
             float sc[kCh], dp[kCh];
             ld_cols<kCh, kCh>(tmem, TM_S + c1, sc, TM_DP + c1, dp);
+            // P and dS of this thread's keys, 8 columns per 16-byte store
 #pragma unroll
-            for (int x = 0; x < kCh; ++x) {
-                if (NH < 16 && x / NH != hc)  // x stays a compile-time register index
+            for (int x0 = 0; x0 < kCh; x0 += 8) {
+                if (NH < 16 && x0 / NH != hc)  // x stays a compile-time register index
                     continue;
-                const int c = c1 + x, key = k0 + c;
-                const float pv = (live && key >= klo && key <= khi) ? ex2(sc[x] * g.scale_l2 - l2) : 0.f;
-                const float dsv = pv * (dp[x] - dl);
-                if (stacked) {
-                    put<SPLIT>(bs_, 2 * bs, BLO, c, r, pv);
-                    put<SPLIT>(bs_, 2 * bs, BLO, bs + c, r, dsv);
-                } else {
-                    put<SPLIT>(bs_, bs, BLO, c, r, pv);
-                    put<SPLIT>(b2s, bs, BLO, c, r, dsv);
+                float pv[8], dsv[8];
+#pragma unroll
+                for (int z = 0; z < 8; ++z) {
+                    const int x = x0 + z, key = k0 + c1 + x;
+                    pv[z] = (live && key >= klo && key <= khi) ? ex2(sc[x] * g.scale_l2 - l2) : 0.f;
+                    dsv[z] = pv[z] * (dp[x] - dl);
                 }
+                put8<SPLIT>(ps, 128, PB, r, c1 + x0, pv);
+                put8<SPLIT>(stacked ? ps : dss, 128, PB, r, (stacked ? bs : 0) + c1 + x0, dsv);
             }
         }
         to_mma();
-        if (threadIdx.x == 0) {
-            if (stacked)
-                product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, 2 * bs, BLO, idA, 128 / 16, ti > 0);
-            else
-                product<SPLIT>(tmem + TM_ACC, as_, 128, ALO, bs_, bs, BLO, idA, 128 / 16, ti > 0);
-        } else if (threadIdx.x == kIssuer2 && !stacked) {
-            product<SPLIT>(tmem + TM_ACC2, a2s, 128, ALO, b2s, bs, BLO, idA, 128 / 16, ti > 0);
-        }
+        // [dV^T; dK^T] += [dO^T; Q^T] [P dS] (stacked), else dV^T += dO^T P
+        // and dK^T += Q^T dS; K = the tile's 128 rows
+        if (threadIdx.x == 0)
+            product_mn<SPLIT>(tmem + TM_ACC, dos, stacked ? parts * QB : 128 * 128, QB, ps, 128, PB, idA, 128 / 16,
+                              ti > 0);
+        else if (threadIdx.x == kIssuer2 && !stacked)
+            product_mn<SPLIT>(tmem + TM_ACC2, qs, 128 * 128, QB, dss, 128, PB, idA, 128 / 16, ti > 0);
         if (ti + 1 < ntiles)
             fetch_tile(tn);
         t = tn;
@@ -1573,8 +1591,8 @@ cudaError_t launch_dkdv_gtc(const Geo &g, const void *q, const void *k, const vo
     p.err = err;
     const int parts = dtype == NSA_DTYPE_F32 ? 2 : 1;
     const bool stacked = p.Dp == 64;
-    const size_t tiles = (size_t)2 * g.bs * p.Dp * 2 + 2 * 128 * p.Dp * 2 + (stacked ? 1 : 2) * 128 * 128 * 2 +
-                         2 * (size_t)g.bs * 128 * 2;
+    const size_t tiles = (size_t)2 * g.bs * p.Dp * 2 + 2 * 128 * p.Dp * 2 +
+                         (stacked ? (size_t)128 * stacked_pw(g.bs) * 2 : (size_t)2 * 128 * kKeyPad * 2);
     const size_t smem = 1024 + parts * tiles + 64;
     if (max_units < 1)
         return cudaSuccess;
