@@ -9,17 +9,17 @@
 // Ah Bh^T + Ah Bl^T + Al Bh^T, accumulated in fp32 (the dropped Al Bl^T and the
 // parts' rounding leave about 2^-16 of |A||B|).
 //
-// One CTA of 128 threads per work item -- a query tile (Tq tokens x the G
+// One CTA of 256 threads per work item -- a query tile (Tq tokens x the G
 // heads of a kv head) for the forward and dQ, a dK/dV unit of the inverse
-// index -- and thread r owns tile row r (TMEM lane r).  Thread 0 issues the
-// MMAs and commits them to one mbarrier, on which all threads wait (bounded).
-// Every operand is K-major in 128-byte-swizzled shared memory (the form every
-// N accepts); a product that needs a transposed operand (V^T and K^T for
-// P V and dS K, Q^T and dO^T for dK^T and dV^T, P^T and dS^T) reads a
-// transposed copy that the threads loading the data write beside the plain
-// one.  Head dims below 64 are zero-padded to 64; with them dV^T and dK^T are
-// one M = 128 product: [dO^T; Q^T] times [P^T; dS^T], whose diagonal blocks
-// are the two results.
+// index -- and two threads own each tile row r (TMEM lane r), each taking
+// half of the row's keys and output columns.  Thread 0 issues the MMAs and
+// commits them to one mbarrier, on which all threads wait (bounded).  Every
+// tile is stored once, K-major in 128-byte-swizzled shared memory, as the
+// threads that load or compute it write it; a product that needs the tile
+// transposed (V and K in P V and dS K, dO and Q in dV^T and dK^T, P and dS)
+// reads it by columns, as an MN-major operand.  Head dims below 64 are
+// zero-padded to 64; with them dV^T and dK^T are one M = 128 product:
+// [dO^T; Q^T] times [P dS], whose diagonal blocks are the two results.
 //
 // The forward takes two passes over the tile's blocks: the first finds each
 // row's maximum and sum (its LSE), the second forms P = exp(S - LSE) and
@@ -69,11 +69,6 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int R, int kk)
     return sdesc_sw128(tile + (kk >> 2) * (R * 128) + (kk & 3) * 32, 16, 1024);
 }
 
-__device__ __forceinline__ void st_u16(uint32_t addr, uint16_t v)
-{
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
 __device__ __forceinline__ uint16_t bf16_bits(float x)
 {
     __nv_bfloat16 b = __float2bfloat16_rn(x);
@@ -91,17 +86,6 @@ template <bool SPLIT> __device__ __forceinline__ Parts<SPLIT> split_of(float x)
     p.hi = *reinterpret_cast<uint16_t *>(&h);
     p.lo = SPLIT ? bf16_bits(x - __bfloat162float(h)) : (uint16_t)0;
     return p;
-}
-
-// writes element (r, c) of a tile (and of its low-part copy, lo_off bytes on)
-template <bool SPLIT>
-__device__ __forceinline__ void put(uint32_t tile, int R, uint32_t lo_off, int r, int c, float x)
-{
-    const Parts<SPLIT> p = split_of<SPLIT>(x);
-    const uint32_t a = tile + swz(r, c, R);
-    st_u16(a, p.hi);
-    if (SPLIT)
-        st_u16(a + lo_off, p.lo);
 }
 
 // descriptor of K-step kk (16 rows) of such a tile read as an MN-major
@@ -296,24 +280,6 @@ template <bool SPLIT> struct In {
     static constexpr int ES = SPLIT ? 4 : 2;
 };
 
-// the VEC values of a vector as floats
-template <bool SPLIT> __device__ __forceinline__ void unpack(const uint4 &w, float *x)
-{
-    if (SPLIT) {
-        x[0] = __uint_as_float(w.x);
-        x[1] = __uint_as_float(w.y);
-        x[2] = __uint_as_float(w.z);
-        x[3] = __uint_as_float(w.w);
-    } else {
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[2 * i] = __uint_as_float(u[i] << 16);
-            x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-        }
-    }
-}
-
 // a vector's VEC elements into row r, columns c .. c+VEC-1 of a tile (c a
 // multiple of VEC): one 16-byte store (bf16), or 8 bytes of high parts and 8
 // of low parts (SPLIT)
@@ -325,8 +291,7 @@ __device__ __forceinline__ void put_vec(uint32_t tile, int R, uint32_t lo_off, i
         st_shared_v4(a, w.x, w.y, w.z, w.w);
         return;
     }
-    float x[4];
-    unpack<true>(w, x);
+    const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
     uint32_t h[2], l[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -362,27 +327,17 @@ __device__ __forceinline__ void fetch_block(const Geo &g, const void *src, int b
     }
 }
 
-// the block into a [bs][Dp] tile (transposed = false) or a [Dp][64] tile
+// the block into a [bs][Dp] tile
 template <bool SPLIT>
-__device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, uint32_t tile, uint32_t lo_off, int Dp,
-                                            bool transposed)
+__device__ __forceinline__ void store_block(const Geo &g, const BlockRegs &R, uint32_t tile, uint32_t lo_off)
 {
     constexpr int VEC = In<SPLIT>::VEC;
     const int nv = g.D / VEC, lnv = __ffs(nv) - 1, n = g.bs * nv;
 #pragma unroll
     for (int i = 0; i < kBlkVec; ++i) {
-        const int e = (threadIdx.x & (kThr - 1)) + i * kThr, key = e >> lnv, c = (e & (nv - 1)) * VEC;
-        if (e >= n)
-            continue;
-        if (!transposed) {
-            put_vec<SPLIT>(tile, g.bs, lo_off, key, c, R.v[i]);
-        } else {
-            float x[VEC];
-            unpack<SPLIT>(R.v[i], x);
-#pragma unroll
-            for (int z = 0; z < VEC; ++z)
-                put<SPLIT>(tile, Dp, lo_off, c + z, key, x[z]);
-        }
+        const int e = (threadIdx.x & (kThr - 1)) + i * kThr;
+        if (e < n)
+            put_vec<SPLIT>(tile, g.bs, lo_off, e >> lnv, (e & (nv - 1)) * VEC, R.v[i]);
     }
 }
 
@@ -442,11 +397,9 @@ __device__ __forceinline__ void fetch_row(const Geo &g, const void *src, int64_t
     }
 }
 
-// the row into row r of a [128][Dp] tile, and (tr_tile != 0) into column r
-// of a transposed tile, rows tr_row0 + d
+// the row into row r of a [128][Dp] tile
 template <bool SPLIT>
-__device__ __forceinline__ void store_row(const Geo &g, const RowRegs &R, uint32_t tile, uint32_t lo_off, int r,
-                                          uint32_t tr_tile, uint32_t tr_lo, int tr_row0)
+__device__ __forceinline__ void store_row(const Geo &g, const RowRegs &R, uint32_t tile, uint32_t lo_off, int r)
 {
     constexpr int VEC = In<SPLIT>::VEC;
 #pragma unroll
@@ -454,13 +407,6 @@ __device__ __forceinline__ void store_row(const Geo &g, const RowRegs &R, uint32
         if (i * VEC >= g.D)
             break;
         put_vec<SPLIT>(tile, 128, lo_off, r, i * VEC, R.v[i]);
-        if (tr_tile) {
-            float x[VEC];
-            unpack<SPLIT>(R.v[i], x);
-#pragma unroll
-            for (int z = 0; z < VEC; ++z)
-                put<SPLIT>(tr_tile, 128, tr_lo, tr_row0 + i * VEC + z, r, x[z]);
-        }
     }
 }
 
@@ -623,7 +569,7 @@ __global__ void __launch_bounds__(kRowThr, MINB) fwd_gtc_kernel(const GParams p)
     if (hc == 0) {
         RowRegs qr;
         fetch_row<SPLIT>(g, p.q, rvalid ? q_off(g, b, kvh * G + hh, t) : 0, rvalid, qr);
-        store_row<SPLIT>(g, qr, qs, QB, r, 0, 0, 0);
+        store_row<SPLIT>(g, qr, qs, QB, r);
     }
     const uint32_t idS = idesc_bf16(128, NK, false, false), idO = idesc_bf16(128, Dp, false, true);
     // the first key of each block of group gi (-1 past the list's end) and
@@ -790,7 +736,7 @@ __global__ void __launch_bounds__(kRowThr, MINB) dq_gtc_kernel(const GParams p)
         const int h = kvh * G + hh;
         RowRegs rr;  // the row of Q (hc = 0) or of dO (hc = 1)
         fetch_row<SPLIT>(g, hc ? p.dO : p.q, !rvalid ? 0 : hc ? o_off(g, b, h, t) : q_off(g, b, h, t), rvalid, rr);
-        store_row<SPLIT>(g, rr, hc ? dos : qs, QB, r, 0, 0, 0);
+        store_row<SPLIT>(g, rr, hc ? dos : qs, QB, r);
         if (rvalid) {
             const int64_t so = stat_off(g, b, h, t);
             l2 = p.lse[so] * 1.4426950408889634f;
@@ -920,13 +866,15 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
     {  // K (hc = 0) or V (hc = 1)
         BlockRegs kr;
         fetch_block<SPLIT>(g, hc ? p.v : p.k, b, kvh, k0, kr);
-        store_block<SPLIT>(g, kr, hc ? vs : ks, KB, Dp, false);
+        store_block<SPLIT>(g, kr, hc ? vs : ks, KB);
     }
     // Launched (selection) as a programmatic dependent of the kernel before
     // it (the inverse index's fill, or delta with a prebuilt plan): the
     // set-up above read only the unit list, which a launch before that kernel
     // wrote; the token rows and delta are read after this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the split-block sum launched next may start (it waits for this kernel)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int tl, hh;
     qrow(G, r, tl, hh);
     const int csr0 = g.dense ? dense_first(g, b, j) + u.begin : p.offsets[u.bg * g.nbmax + j] + u.begin;
@@ -976,7 +924,7 @@ __global__ void __launch_bounds__(kRowThr, 2) dkdv_gtc_kernel(const GParams p)
         // the rows (zeros for rows past the list)
         if (!kRowAhead)
             fetch_row_of(t);
-        store_row<SPLIT>(g, rr, hc == 0 ? dos : qs, QB, r, 0, 0, 0);
+        store_row<SPLIT>(g, rr, hc == 0 ? dos : qs, QB, r);
         to_mma();
         if (threadIdx.x == 0)
             product<SPLIT>(tmem + TM_S, qs, 128, QB, ks, bs, KB, idS, Dp / 16, false);

@@ -7,6 +7,7 @@
 //   * the fixed-order reduction of split dK/dV blocks;
 //   * the (query row, key) pair count used for effective-FLOP reporting.
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace nsa {
 
@@ -240,6 +241,12 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
                                                         int *__restrict__ blk_slot, WsHeader *hdr,
                                                         int chunk)
 {
+    // The index-build kernels (count, prefix, scan, fill) launch as
+    // programmatic dependents of the kernel before each and let the next one
+    // launch at once: each waits here, before reading anything, for the one
+    // before it to complete, so only the launches overlap.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Tails (each block's last, partial chunk) go after the full chunks,
     // longest first by kTailBins bins (stable within a bin), so that the
     // dK/dV kernel's snake assignment of units to CTAs balances their work.
@@ -421,6 +428,9 @@ __global__ void __launch_bounds__(kThreads) dkdv_reduce_kernel(Geo g, const int 
                                                                const float *__restrict__ partials,
                                                                T *__restrict__ dk, T *__restrict__ dv)
 {
+    // (other shapes) a programmatic dependent of the dK/dV kernel: nothing is
+    // read before it completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int i = blockIdx.x >> 2, quarter = blockIdx.x & 3;
     const int nch = nchunk[i];
     if (nch == 1)
@@ -537,6 +547,7 @@ __global__ void __launch_bounds__(kThreads) csr_chunk_count_kernel(Geo g, const 
                                                                    int *__restrict__ chunk_counts, int nchunks,
                                                                    int *err)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the prefix may launch (it waits)
     chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, gridDim.x);
 }
 
@@ -550,6 +561,7 @@ __global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const 
                                                                    const T *__restrict__ dO, float *__restrict__ out,
                                                                    int64_t nrows)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the prefix may launch (it waits)
     if ((int)blockIdx.x < count_blocks)
         chunk_count_body(g, idx, chunk_counts, nchunks, err, blockIdx.x, count_blocks);
     else
@@ -560,6 +572,9 @@ __global__ void __launch_bounds__(kThreads) chunk_count_dot_kernel(Geo g, const 
 __global__ void __launch_bounds__(kThreads) csr_chunk_prefix_kernel(Geo g, int *__restrict__ chunk_counts,
                                                                     int nchunks, int *__restrict__ counts)
 {
+    // a programmatic dependent of the count, and the scan's primary (see csr_scan_kernel)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int n = g.B * g.Hkv * g.nbmax;
     for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += (gridDim.x * blockDim.x) >> 5) {
@@ -589,7 +604,10 @@ __global__ void __launch_bounds__(kFillWarps * 32) csr_chunk_fill_kernel(Geo g, 
                                                                          int nchunks, const int *__restrict__ offsets,
                                                                          int *__restrict__ rows)
 {
-    // the dK/dV kernel launched next may start its set-up (it waits before reading the index)
+    // this kernel waits for the scan (see csr_scan_kernel); then the kernel
+    // launched next may start its set-up, which reads the scan's unit list
+    // but not this kernel's lists (it waits for this kernel before those)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned mask_all[];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -731,8 +749,8 @@ cudaError_t launch_csr_scan(const Geo &g, const int *counts, int *offsets, Unit 
                             int *blk_nchunk, int *blk_slot, WsHeader *hdr, int chunk,
                             cudaStream_t st)
 {
-    csr_scan_kernel<<<1, 1024, 0, st>>>(g, counts, offsets, units, blk_nchunk, blk_slot, hdr, chunk);
-    return cudaGetLastError();
+    return launch_dependent(csr_scan_kernel, dim3(1), dim3(1024), 0, st, g, counts, offsets, units, blk_nchunk,
+                            blk_slot, hdr, chunk);
 }
 
 int csr_nchunks(const Geo &g) { return (g.T + kChunkTok - 1) / kChunkTok; }
@@ -777,8 +795,8 @@ cudaError_t launch_csr_chunk_count(const Geo &g, const int *idx, int *chunk_coun
     }
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    csr_chunk_prefix_kernel<<<grid_for(nbgj * 32, kThreads), kThreads, 0, st>>>(g, chunk_counts, nchunks, counts);
-    return cudaGetLastError();
+    return launch_dependent(csr_chunk_prefix_kernel, dim3(grid_for(nbgj * 32, kThreads)), dim3(kThreads), 0, st, g,
+                            chunk_counts, nchunks, counts);
 }
 
 cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk_prefix, const int *offsets,
@@ -788,8 +806,8 @@ cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk
     const int items = g.B * g.Hkv * nchunks;
     const int grid = grid_for(items, kFillWarps);
     const size_t smem = sizeof(unsigned) * kFillWarps * g.nbmax;
-    csr_chunk_fill_kernel<<<grid, kFillWarps * 32, smem, st>>>(g, idx, chunk_prefix, nchunks, offsets, rows);
-    return cudaGetLastError();
+    return launch_dependent(csr_chunk_fill_kernel, dim3(grid), dim3(kFillWarps * 32), smem, st, g, idx, chunk_prefix,
+                            nchunks, offsets, rows);
 }
 
 cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, int *rows,
@@ -804,18 +822,21 @@ cudaError_t launch_csr_fill(const Geo &g, const int *idx, const int *offsets, in
 
 cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *blk_slot,
                                const float *partials, void *dk, void *dv, int dtype,
-                               cudaStream_t st)
+                               cudaStream_t st, bool dependent)
 {
     const int n = g.B * g.Hkv * g.nbmax;
     if (n == 0)
         return cudaSuccess;
+    auto go = [&](auto kernel, auto *k_out, auto *v_out) -> cudaError_t {
+        if (dependent)
+            return launch_dependent(kernel, dim3(4 * n), dim3(kThreads), 0, st, g, blk_nchunk, blk_slot, partials,
+                                    k_out, v_out);
+        kernel<<<4 * n, kThreads, 0, st>>>(g, blk_nchunk, blk_slot, partials, k_out, v_out);
+        return cudaGetLastError();
+    };
     if (dtype == NSA_DTYPE_BF16)
-        dkdv_reduce_kernel<__nv_bfloat16><<<4 * n, kThreads, 0, st>>>(
-            g, blk_nchunk, blk_slot, partials, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv);
-    else
-        dkdv_reduce_kernel<float><<<4 * n, kThreads, 0, st>>>(g, blk_nchunk, blk_slot, partials,
-                                                              (float *)dk, (float *)dv);
-    return cudaGetLastError();
+        return go(dkdv_reduce_kernel<__nv_bfloat16>, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv);
+    return go(dkdv_reduce_kernel<float>, (float *)dk, (float *)dv);
 }
 
 cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cudaStream_t st)

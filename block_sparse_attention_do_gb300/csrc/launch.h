@@ -49,7 +49,7 @@ cudaError_t launch_csr_chunk_fill(const Geo &g, const int *idx, const int *chunk
 // sums the fp32 partials of split blocks into dk/dv and zeroes unselected blocks
 cudaError_t launch_dkdv_reduce(const Geo &g, const int *blk_nchunk, const int *blk_slot,
                                const float *partials, void *dk, void *dv, int dtype,
-                               cudaStream_t st);
+                               cudaStream_t st, bool dependent = false);
 cudaError_t launch_count_pairs(const Geo &g, const int *idx, long long *out, cudaStream_t st);
 // attention sinks: fold sinks[h] into the forward's o and lse in place; and
 // dsinks[h] = -sum over head h's rows of exp(sinks[h] - lse) * delta

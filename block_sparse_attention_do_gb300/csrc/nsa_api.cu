@@ -491,7 +491,8 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         }
         NSA_LAUNCH("dkdv_gtc", launch_dkdv_gtc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                                partials, dk, dv, p->dtype, &hdr->err, st));
-        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
+        // a programmatic dependent of dK/dV (it waits for it before reading)
+        NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st, true));
     } else {
         NSA_LAUNCH("dkdv_simt", launch_dkdv_simt(g, q, k, v, dO, lse, delta, offsets, rows, dk, dv, p->dtype, st));
         NSA_LAUNCH("dq_simt", launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, p->dtype, st));
