@@ -244,8 +244,12 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(Geo g, const int *__rest
     // The index-build kernels (count, prefix, scan, fill) launch as
     // programmatic dependents of the kernel before each and let the next one
     // launch at once: each waits here, before reading anything, for the one
-    // before it to complete, so only the launches overlap.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // before it to complete, so only the launches overlap.  The dense
+    // entries follow the scan with the persistent dK/dV kernel, whose CTA on
+    // this kernel's SM would then start late and end the last: there the next
+    // kernel launches when this one ends.
+    if (!g.dense)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // Tails (each block's last, partial chunk) go after the full chunks,
     // longest first by kTailBins bins (stable within a bin), so that the
