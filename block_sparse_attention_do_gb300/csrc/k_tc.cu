@@ -11,7 +11,8 @@ bool tc_supported(const Geo &g, int dtype)
     if (!(dtype == NSA_DTYPE_BF16 && g.D == kHead && g.bs == kKeys && g.G >= 1 && g.G <= kRows))
         return false;
     // the row-gather maps (G % 8 == 0) fold the batch index into the head or
-    // the token index: strides where neither folds go to the CUDA-core kernels
+    // the token index: strides where neither folds go to the other-shapes
+    // kernels (k_gtc.cu)
     int bt;
     return g.G % 8 != 0 || (rows_map_form(g, g.Hq, g.sq, bt) && rows_map_form(g, g.Hq, g.so, bt));
 }

@@ -190,7 +190,7 @@ def test_varlen(dtype, Hq):
     (torch.bfloat16, (1, 16, 1, 300, 128, 64, 1), 64),   # window = one block
     (torch.bfloat16, (2, 32, 2, 200, 128, 64, 1), 1),    # own key only
     (torch.bfloat16, (1, 16, 1, 300, 128, 64, 1), 1000), # wider than T: dense causal
-    (torch.float32, (2, 6, 2, 150, 64, 32, 1), 45),      # SIMT
+    (torch.float32, (2, 6, 2, 150, 64, 32, 1), 45),      # other shapes: split-precision tensor cores
     (torch.bfloat16, (1, 4, 1, 150, 128, 64, 1), 70),    # G = 4: head-major tiles, cp.async gathers
 ])
 def test_sliding_window(dtype, shape, W):
@@ -758,8 +758,8 @@ def _packed_views(x_q, x_k, x_v, thd, pad_tokens=0):
 @pytest.mark.parametrize("dtype,shape,pad", [
     (torch.bfloat16, (2, 32, 2, 300, 128, 64, 4), 0),  # tensor cores, row-gather maps (batch folded into tokens)
     (torch.bfloat16, (2, 8, 2, 200, 128, 64, 3), 0),   # tensor cores, G = 4: tile maps and cp.async gathers
-    (torch.float32, (2, 6, 2, 150, 64, 32, 3), 0),     # CUDA cores
-    (torch.bfloat16, (2, 16, 1, 130, 128, 64, 3), 8),  # padded token capacity: batch folds nowhere (CUDA cores)
+    (torch.float32, (2, 6, 2, 150, 64, 32, 3), 0),     # other shapes: split-precision tensor cores
+    (torch.bfloat16, (2, 16, 1, 130, 128, 64, 3), 8),  # padded token capacity: batch folds nowhere (other shapes)
 ])
 def test_declared_strides_packed_qkv(dtype, shape, pad):
     """q, k, v are views of one packed [B, T, Hq + 2 Hkv, D] tensor and
@@ -814,10 +814,10 @@ CAUSAL_CASES = [
     (torch.bfloat16, (1, 32, 2, 128, 64), 300, 130, True, 0),     # Lq > Lk: the first 170 rows see nothing
     (torch.bfloat16, (1, 16, 2, 128, 64), 150, 260, False, 0),    # top-left: keys past Lq unused
     (torch.bfloat16, (1, 8, 2, 128, 64), 300, 500, True, 100),    # G = 4 (cp.async gathers), window
-    (torch.float32, (2, 6, 2, 64, 32), 100, 150, True, 40),       # CUDA cores
+    (torch.float32, (2, 6, 2, 64, 32), 100, 150, True, 40),       # other shapes, split precision
     (torch.bfloat16, (0, 8, 2, 128, 64), [130, 1, 64, 257], [200, 64, 1, 257], True, 70),   # THD
     (torch.bfloat16, (0, 32, 2, 128, 64), [300, 90], [40, 300], True, 0),                   # THD, G = 16
-    (torch.float32, (0, 4, 2, 64, 32), [50, 7], [80, 3], False, 0),                          # THD, CUDA cores
+    (torch.float32, (0, 4, 2, 64, 32), [50, 7], [80, 3], False, 0),                          # THD, other shapes
 ]
 
 
