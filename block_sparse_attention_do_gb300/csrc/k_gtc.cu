@@ -471,6 +471,7 @@ __device__ __forceinline__ void qtile_union_cta(const Geo &g, const int *idx, co
             buf[UH_KVH] = kvh;
             buf[UH_T0] = t0;
             buf[UH_NVALID] = nvalid;
+            buf[UH_GROUPED] = 0;
             buf[UH_COUNT] = base;
         }
     }

@@ -82,6 +82,9 @@ struct Params {
     int stall;    // self-test: the S-product issuer stays idle (see wait_test)
 };
 
+// GROUPED: the union table's tiles are grouped by shared blocks (each row's
+// token is read from the tile's record); else a tile's row tl has token T0 + tl
+template <bool GROUPED>
 __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                        const __grid_constant__ CUtensorMap tm_do,
                                                        const __grid_constant__ CUtensorMap tm_k,
@@ -231,9 +234,11 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
                 if (rg) {  // token box: G heads x both halves, contiguous in the row-group layout
                     for (int tl = lane; tl < Tq; tl += 32)
                         if (tensor ? g.o_bt : g.q_bt)  // batch folded into the token index
-                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, kvh * G / 8, b * g.T + t0 + tl);
+                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, kvh * G / 8,
+                                        b * g.T + (GROUPED ? qtile_token(u_hdr(k), tl) : t0 + tl));
                         else
-                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, (b * g.Hq + kvh * G) / 8, t0 + tl);
+                            tma_load_5d(base + tl * G * 256, map, bar, 0, 0, 0, (b * g.Hq + kvh * G) / 8,
+                                        GROUPED ? qtile_token(u_hdr(k), tl) : t0 + tl);
                 } else if (lane < 2) {
                     const int h = lane;
                     if (g.thd)
@@ -424,7 +429,8 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const volatile int *hdr = u_hdr(k);
             nU = hdr[UH_COUNT];
             if (nU >= 0 && r < nrows && tl < hdr[UH_NVALID]) {
-                const int64_t so = stat_off(g, hdr[UH_B], hdr[UH_KVH] * G + hh, hdr[UH_T0] + tl);
+                const int64_t so =
+                    stat_off(g, hdr[UH_B], hdr[UH_KVH] * G + hh, GROUPED ? qtile_token(hdr, tl) : hdr[UH_T0] + tl);
                 nl2 = p.lse[so];  // scaled by log2(e) at use, so the load does not stall here
                 ndl = p.delta[so];
             }
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(384, 1) dq_tc_kernel(const __grid_constant__ C
             const int *list = union_list(u_buf(k), up);
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
-            const int t = t0 + tl;
+            const int t = GROUPED ? qtile_token(hdr, tl) : t0 + tl;  // the row's token
             // the row's keys: from the window's left edge to its diagonal
             const int cdiag = rvalid ? kdiag(g, b, t) : -1;
             const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
@@ -595,7 +601,196 @@ __global__ void __launch_bounds__(256) qtile_union_kernel(Geo g, const int *__re
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Tiles grouped by shared blocks.  The tokens of Wt consecutive tiles (a
+// window of W = Wt * Tq <= 64 tokens of one (b, kv head)) are dealt into
+// the same number of tiles greedily: a tile starts with the window's first
+// free token and takes, Tq - 1 times, the free token that adds the fewest
+// blocks to its union (ties to the lower token).  A tile need not hold
+// consecutive tokens, and tokens that share blocks make smaller unions: on
+// uniformly drawn selections the block pairs a tile walks drop by ~13%; on
+// selections that cluster, by more.  One warp per window: lane l holds the
+// block bitmaps of tokens l and l + 32 in registers (every index entry of
+// both read at once), and a pick is one warp-wide minimum of (cost, token).
+// The union records go where qtile_union_kernel puts them, with UH_GROUPED
+// set and the tokens as offsets from the window's start.  For tiles of
+// 2 .. kGroupMaxTq tokens whose Q (and dO) rows the kernels load by token
+// (row-group layout).
+constexpr int kGroupWindow = 64;  // tokens a window holds at most
+constexpr int kGroupWords = 8;    // block bitmap words a grouped window may need (nbmax <= 256)
+
+// WORDS: the block bitmap's words, (nbmax + 31) / 32 rounded up to 1, 2, 4 or 8
+template <int WORDS>
+__global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__restrict__ idx, UnionBuf up,
+                                                          int *__restrict__ utable)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int words = (g.nbmax + 31) / 32;
+    const int Tq = tile_tokens(g.G), Wt = kGroupWindow / Tq, W = Wt * Tq;
+    const int nbg = g.B * g.Hkv, per_seq = (g.T + Tq - 1) / Tq, nwin = (per_seq + Wt - 1) / Wt;
+    const bool vec = (g.S & 3) == 0 && ((uintptr_t)idx & 15) == 0;  // index rows in 16-byte pieces
+    for (int item = blockIdx.x * (blockDim.x >> 5) + w; item < nbg * nwin; item += gridDim.x * (blockDim.x >> 5)) {
+        const int bg = item % nbg, win = item / nbg;
+        const int b = bg / g.Hkv, kvh = bg % g.Hkv;
+        const int t0 = win * W, ntok = min(W, g.T - t0);
+        // lane l holds window tokens l + 32 q (q < 2): their block bitmaps,
+        // and bit q of avail while the token is free
+        uint32_t m[2][WORDS];
+        uint32_t avail = 0u;
+        int tq[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+            for (int x = 0; x < WORDS; ++x)
+                m[q][x] = 0u;
+            if (lane + 32 * q < ntok)
+                avail |= 1u << q;
+            tq[q] = t0 + min(lane + 32 * q, ntok - 1);  // a token past the window reads a valid row, unused
+        }
+        // the tokens' index entries: every load of a round issued before any is used
+        for (int s0 = 0; s0 < g.S; s0 += 8) {
+            int jv[2][8];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int *row = idx_row(g, idx, b, kvh, tq[q]);
+                if (vec) {
+#pragma unroll
+                    for (int u = 0; u < 8; u += 4) {
+                        const int4 v4 = __ldg((const int4 *)(row + min(s0 + u, g.S - 4)));
+                        jv[q][u] = v4.x;
+                        jv[q][u + 1] = v4.y;
+                        jv[q][u + 2] = v4.z;
+                        jv[q][u + 3] = v4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        jv[q][u] = __ldg(row + min(s0 + u, g.S - 1));
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int t = tq[q];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int j = jv[q][u];
+                    const bool use = s0 + u < g.S && j >= 0 && j <= t / g.bs && j < g.nbmax;
+                    const uint32_t bit = use ? 1u << (j & 31) : 0u;
+#pragma unroll
+                    for (int x = 0; x < WORDS; ++x)
+                        m[q][x] |= (j >> 5) == x ? bit : 0u;
+                }
+            }
+        }
+        const int ntiles_w = (ntok + Tq - 1) / Tq;
+        for (int k = 0; k < ntiles_w; ++k) {
+            const int nk = min(Tq, ntok - k * Tq);
+            const int tile = win * Wt + k;
+            int *dst = utable + (int64_t)((per_seq - 1 - tile) * nbg + bg) * (up.bytes / 4);
+            uint32_t *mask = (uint32_t *)(dst + UH_INTS), *ubits = mask + up.mask_words;
+            int *list = dst + UH_INTS + up.mask_words + up.ubits_words;
+            uint32_t cur[WORDS];
+#pragma unroll
+            for (int x = 0; x < WORDS; ++x)
+                cur[x] = 0u;
+            uint32_t packed[kGroupMaxTq / 4] = {0u, 0u, 0u, 0u};
+            int slot0 = -1, slot1 = -1;  // the tile row each of this lane's tokens took
+            for (int pick = 0; pick < nk; ++pick) {
+                // key = cost << 8 | token: the free token adding the fewest
+                // blocks (for the first pick every cost is 0: the lowest token)
+                unsigned key = 0xffffffffu;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    unsigned cost = 0u;
+#pragma unroll
+                    for (int x = 0; x < WORDS; ++x)
+                        cost += __popc(m[q][x] & ~cur[x]);
+                    if ((avail >> q) & 1u)
+                        key = min(key, (cost << 8) | (unsigned)(lane + 32 * q));
+                }
+                key = __reduce_min_sync(0xffffffffu, key);
+                if (key == 0xffffffffu)
+                    break;  // (never: a window's tiles take exactly its tokens)
+                const int best = (int)(key & 0xffu), owner = best & 31, qb = best >> 5;
+                // the token's bitmap from its lane into the union
+#pragma unroll
+                for (int x = 0; x < WORDS; ++x)
+                    cur[x] |= __shfl_sync(0xffffffffu, qb == 0 ? m[0][x] : m[1][x], owner);
+                if (lane == owner) {
+                    avail &= ~(1u << qb);
+                    if (qb == 0)
+                        slot0 = pick;
+                    else
+                        slot1 = pick;
+                }
+#pragma unroll
+                for (int x = 0; x < kGroupMaxTq / 4; ++x)
+                    if ((pick >> 2) == x)
+                        packed[x] |= (uint32_t)best << ((pick & 3) * 8);
+            }
+            // the tile's rows: each token's bitmap by its lane, then empty
+            // bitmaps for rows past the tile's tokens
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int sl = q == 0 ? slot0 : slot1;
+                if (sl >= 0)
+#pragma unroll
+                    for (int x = 0; x < WORDS; ++x)
+                        if (x < words)
+                            mask[sl * words + x] = m[q][x];
+            }
+            for (int x = nk * words + lane; x < up.mask_words; x += 32)
+                mask[x] = 0u;
+            // the union bitmap, and its blocks in ascending order (lane x <
+            // words takes word x)
+            uint32_t bits = 0u;
+#pragma unroll
+            for (int x = 0; x < WORDS; ++x)
+                if (lane == x)
+                    bits = cur[x];
+            for (int x = lane; x < up.ubits_words; x += 32)
+                ubits[x] = x < words ? bits : 0u;
+            const int cnt = __popc(bits);
+            int incl = cnt;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            int pos = incl - cnt;
+            for (uint32_t bb = bits; bb; bb &= bb - 1u)
+                list[pos++] = lane * 32 + __ffs(bb) - 1;
+            const int total = __shfl_sync(0xffffffffu, incl, 31);  // every lane takes part
+            if (lane < kGroupMaxTq / 4) {
+                uint32_t pw = 0u;
+#pragma unroll
+                for (int x = 0; x < kGroupMaxTq / 4; ++x)
+                    if (lane == x)
+                        pw = packed[x];
+                dst[UH_TOK + lane] = (int)pw;
+            }
+            if (lane == 0) {
+                dst[UH_B] = b;
+                dst[UH_KVH] = kvh;
+                dst[UH_T0] = t0;
+                dst[UH_NVALID] = nk;
+                dst[UH_COUNT] = total;
+                dst[UH_GROUPED] = 1;
+            }
+            __syncwarp();
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace
+
+bool qtile_groupable(const Geo &g)
+{
+    const int Tq = tile_tokens(g.G);
+    return !g.dense && !g.thd && g.G % 8 == 0 && Tq >= 2 && Tq <= kGroupMaxTq && g.nbmax <= 32 * kGroupWords &&
+           qtile_shape_ok(g);
+}
 
 size_t qtile_union_table_bytes(const Geo &g)
 {
@@ -605,13 +800,23 @@ size_t qtile_union_table_bytes(const Geo &g)
     return (size_t)((g.T + Tq - 1) / Tq) * g.B * g.Hkv * union_buf(g).bytes;
 }
 
-cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st)
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group)
 {
     if (qtile_union_table_bytes(g) == 0)
         return cudaSuccess;
     const int Tq = tile_tokens(g.G);
     const int ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const UnionBuf up = union_buf(g);
+    if (group && qtile_groupable(g)) {
+        const int Wt = kGroupWindow / Tq, nwin = ((g.T + Tq - 1) / Tq + Wt - 1) / Wt;
+        const int items = g.B * g.Hkv * nwin, grid = (items + 3) / 4;
+        if (grid < 1)
+            return cudaSuccess;
+        const int words = (g.nbmax + 31) / 32;
+        auto kern = words <= 1 ? qtile_group_kernel<1> : words <= 2 ? qtile_group_kernel<2>
+                  : words <= 4 ? qtile_group_kernel<4> : qtile_group_kernel<8>;
+        return launch_dependent(kern, dim3(grid), dim3(128), 0, st, g, idx, up, utable);
+    }
     const int grid = (ntiles + 7) / 8;
     if (grid < 1)
         return cudaSuccess;
@@ -622,8 +827,8 @@ cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaS
 }
 
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v, const void *dO,
-                         const float *lse, const float *delta, const int *idx, const int *utable, void *dq,
-                         int *err, int *tile_next, cudaStream_t st)
+                         const float *lse, const float *delta, const int *idx, const int *utable, bool grouped,
+                         void *dq, int *err, int *tile_next, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_dq_simt(g, q, k, v, dO, lse, delta, idx, dq, NSA_DTYPE_BF16, st);
@@ -670,11 +875,12 @@ cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void 
         grid = p.ntiles;
     if (grid < 1)
         return cudaSuccess;
-    cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kernel = grouped && utable ? dq_tc_kernel<true> : dq_tc_kernel<false>;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     // a programmatic dependent of the kernel before it on the stream (the dK/dV
     // kernel, whose outputs it does not read): its CTAs start as that kernel's
     // CTAs end; everything it reads was written by earlier, completed launches
-    return launch_dependent(dq_tc_kernel, dim3(grid), dim3(384), smem, st, tq, tdo, tk, tv, p);
+    return launch_dependent(kernel, dim3(grid), dim3(384), smem, st, tq, tdo, tk, tv, p);
 }
 
 }  // namespace nsa

@@ -85,6 +85,9 @@ struct Params {
     int stall;    // self-test: the S-product issuer stays idle (see wait_test)
 };
 
+// GROUPED: the union table's tiles are grouped by shared blocks (each row's
+// token is read from the tile's record); else a tile's row tl has token T0 + tl
+template <bool GROUPED>
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
                                                         const __grid_constant__ CUtensorMap tm_v,
@@ -219,10 +222,10 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
                 for (int tl = lane; tl < Tq; tl += 32) {
                     if (g.q_bt)  // batch folded into the token index
                         tma_load_5d(sm + OFF_Q + tl * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, kvh * G / 8,
-                                    b * g.T + t0 + tl);
+                                    b * g.T + (GROUPED ? qtile_token(u_hdr(k), tl) : t0 + tl));
                     else
                         tma_load_5d(sm + OFF_Q + tl * G * 256, &tm_q, &bars[B_QFULL], 0, 0, 0, (b * g.Hq + kvh * G) / 8,
-                                    t0 + tl);
+                                    GROUPED ? qtile_token(u_hdr(k), tl) : t0 + tl);
                 }
             } else if (lane < 2) {
                 const int h = lane;
@@ -386,7 +389,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
             const int *list = union_list(u_buf(k), up);
             const int npairs = (U + 1) >> 1;
             const bool rvalid = r < nrows && tl < nvalid;
-            const int t = t0 + tl;
+            const int t = GROUPED ? qtile_token(hdr, tl) : t0 + tl;  // the row's token
             // the row's keys: from the window's left edge to its diagonal
             const int cdiag = rvalid ? kdiag(g, b, t) : -1;
             const int khi = rvalid ? min(cdiag, seq_len_k(g, b) - 1) : -1, klo = key_lo(g, cdiag);
@@ -576,8 +579,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(const __grid_constant__ 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v, const int *idx,
-                          const int *utable, void *o, float *lse, int *err, int *tile_next, bool after_kernel,
-                          cudaStream_t st)
+                          const int *utable, bool grouped, void *o, float *lse, int *err, int *tile_next,
+                          bool after_kernel, cudaStream_t st)
 {
     if (!qtile_shape_ok(g))
         return launch_fwd_simt(g, q, k, v, idx, o, lse, NSA_DTYPE_BF16, st);
@@ -612,12 +615,13 @@ cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void
         grid = p.ntiles;
     if (grid < 1)
         return cudaSuccess;
-    cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto fwd_tc = grouped && utable ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+    cudaFuncSetAttribute(fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     // After the index validation, a programmatic dependent of it (the check
     // only reports errors; this kernel skips invalid entries by itself).
     if (after_kernel)
-        return launch_dependent(fwd_tc_kernel, dim3(grid), dim3(384), smem, st, tq, tk, tv, p);
-    fwd_tc_kernel<<<grid, 384, smem, st>>>(tq, tk, tv, p);
+        return launch_dependent(fwd_tc, dim3(grid), dim3(384), smem, st, tq, tk, tv, p);
+    fwd_tc<<<grid, 384, smem, st>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

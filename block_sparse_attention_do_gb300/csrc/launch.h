@@ -103,18 +103,24 @@ bool tc_supported(const Geo &g, int dtype);
 // this library (the index validation or the union build) and becomes its
 // programmatic dependent (it waits for it before reading utable)
 cudaError_t launch_fwd_tc(const Geo &g, const void *q, const void *k, const void *v,
-                          const int *idx, const int *utable, void *o, float *lse, int *err, int *tile_next,
-                          bool after_kernel, cudaStream_t st);
+                          const int *idx, const int *utable, bool grouped, void *o, float *lse, int *err,
+                          int *tile_next, bool after_kernel, cudaStream_t st);
 // every query tile's block union for the dQ kernel, into utable
 // (qtile_union_table_bytes(g) bytes; 0, and no launch, for the dense entries,
 // whose unions are block ranges the dQ kernel builds itself); a
 // programmatic dependent of the kernel before it on st
 size_t qtile_union_table_bytes(const Geo &g);
-cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st);
-// utable: the union table launch_qtile_unions wrote, or null (dense entries)
+// whether the table's tiles are grouped by shared blocks rather than made of
+// consecutive tokens (qtile_group_kernel)
+bool qtile_groupable(const Geo &g);
+// group: tiles grouped by shared blocks where qtile_groupable, else
+// consecutive tokens
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group);
+// utable: the union table launch_qtile_unions wrote, or null (dense
+// entries); grouped: its tiles are grouped by shared blocks
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,
                          const void *dO, const float *lse, const float *delta, const int *idx,
-                         const int *utable, void *dq, int *err, int *tile_next, cudaStream_t st);
+                         const int *utable, bool grouped, void *dq, int *err, int *tile_next, cudaStream_t st);
 cudaError_t launch_dkdv_tc(const Geo &g, const void *q, const void *k, const void *v,
                            const void *dO, const float *lse, const float *delta,
                            const int *offsets, const int *rows, const Unit *units,

@@ -139,13 +139,16 @@ nsa_status make_geo(const nsa_problem *p, bool want_thd, Mode mode, const int32_
 // header | counts | offsets | unit list | per-block chunk count and partial
 // slot | per-chunk histograms (chunked build) | token lists (sparse only).
 struct PlanLayout {
-    size_t counts, offsets, units, nchunk, slot, chunkc, rows, total;
+    size_t counts, offsets, units, nchunk, slot, chunkc, rows, utable, total;
     int chunk, max_units;
+    bool has_utable;  // the plan also holds the query-tile unions, tiles grouped by shared blocks
 };
 
 int tiles_tokens(const Geo &g) { return g.G >= 128 ? 1 : 128 / g.G; }
 
-PlanLayout plan_layout(const Geo &g)
+// dtype >= 0 (a plan built by nsa_plan_build): where the tensor-core kernels
+// take a grouped union table, the plan ends with one
+PlanLayout plan_layout(const Geo &g, int dtype = -1)
 {
     PlanLayout w;
     const int64_t nbgj = (int64_t)g.B * g.Hkv * g.nbmax;
@@ -181,6 +184,11 @@ PlanLayout plan_layout(const Geo &g)
     w.rows = off;
     if (!g.dense)
         off = align_up(off + sizeof(int) * (size_t)g.ntok * g.Hkv * g.S);
+    w.utable = off;
+    w.has_utable = dtype >= 0 && !g.dense && tc_supported(g, dtype) && qtile_groupable(g) &&
+                   qtile_union_table_bytes(g) > 0;
+    if (w.has_utable)
+        off = align_up(off + qtile_union_table_bytes(g));
     w.total = off;
     return w;
 }
@@ -357,9 +365,10 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         // the query-tile unions (sparse only), alongside the validation
         int *utable = mode == SPARSE && qtile_union_table_bytes(g) ? (int *)((char *)ws + kAlign) : nullptr;
         if (utable)
-            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st));
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st, true));
         NSA_LAUNCH("fwd_tc",
-                   launch_fwd_tc(g, q, k, v, idx, utable, o, lse, &hdr->err, &hdr->tile_next, mode == SPARSE, st));
+                   launch_fwd_tc(g, q, k, v, idx, utable, utable && qtile_groupable(g), o, lse, &hdr->err,
+                                 &hdr->tile_next, mode == SPARSE, st));
     }
     else if (gtc_supported(g, p->dtype))
         NSA_LAUNCH("fwd_gtc", launch_fwd_gtc(g, q, k, v, idx, o, lse, p->dtype, &hdr->err, st));
@@ -442,6 +451,8 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     WsHeader *hdr = (WsHeader *)ws;
     char *pl8 = plan ? (char *)plan : w8 + L.plan;
     const PlanLayout &P = L.pl;
+    // a plan built by nsa_plan_build may end with the grouped union table
+    const PlanLayout PP = plan ? plan_layout(g, p->dtype) : L.pl;
     float *delta = (float *)(w8 + L.delta);
     float *partials = (float *)(w8 + L.partials);
     const int *offsets = (const int *)(pl8 + P.offsets);
@@ -475,14 +486,19 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     if (tc_supported(g, p->dtype)) {
         // the query-tile unions (sparse only): alongside the kernel before,
         // since they read only the index
+        // (consecutive tokens: grouping tiles by shared blocks costs more here
+        // than it saves dQ; a plan's table, built once, has them grouped)
         int *utable = qtile_union_table_bytes(g) ? (int *)(w8 + L.utable) : nullptr;
-        if (utable)
-            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st));
+        if (PP.has_utable)
+            utable = (int *)(pl8 + PP.utable);
+        else if (utable)
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st, false));
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                partials, dk, dv, &hdr->err, st));
         // dQ right after dK/dV: it is that kernel's programmatic dependent
         NSA_LAUNCH("dq_tc",
-                   launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, dq, &hdr->err, &hdr->tile_next, st));
+                   launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, PP.has_utable, dq, &hdr->err,
+                                &hdr->tile_next, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else if (gtc) {
         {
@@ -667,7 +683,7 @@ size_t nsa_plan_size(const nsa_problem *p)
     const bool thd = p->layout == NSA_LAYOUT_THD;
     if (make_geo(p, thd, SPARSE, thd ? (const int32_t *)16 : nullptr, g) != NSA_OK)
         return 0;
-    return plan_layout(g).total;
+    return plan_layout(g, p->dtype).total;
 }
 
 size_t nsa_bwd_planned_workspace_size(const nsa_problem *p)
@@ -693,11 +709,16 @@ nsa_status nsa_plan_build(const nsa_problem *p, const int32_t *cu_seqlens, const
         return s;
     if (!block_idx)
         return NSA_ERR_INVALID_ARG;
-    const PlanLayout L = plan_layout(g);
+    const PlanLayout L = plan_layout(g, p->dtype);
     if ((s = check_ws(plan, plan_bytes, L.total)) != NSA_OK)
         return s;
     char *pl8 = (char *)plan;
-    return build_plan(g, block_idx, pl8, L, &((WsHeader *)pl8)->err, (cudaStream_t)stream);
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((s = build_plan(g, block_idx, pl8, L, &((WsHeader *)pl8)->err, st)) != NSA_OK)
+        return s;
+    if (L.has_utable)  // the dQ kernel's query-tile unions, tiles grouped by shared blocks
+        NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, block_idx, (int *)(pl8 + L.utable), st, true));
+    return NSA_OK;
 }
 
 nsa_status nsa_sel_bwd_planned(const nsa_problem *p, const int32_t *cu_seqlens, const void *q, const void *k,

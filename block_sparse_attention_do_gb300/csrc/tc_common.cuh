@@ -131,8 +131,18 @@ __device__ __forceinline__ void qtile_row(const Geo &g, int Tq, int r, int &tl, 
 
 // A union buffer: UH_INTS header ints (the tile's coordinates and the list
 // length; a negative length ends the walk), the per-token block bitmaps, the
-// union bitmap and the ascending list.
-enum { UH_B = 0, UH_KVH, UH_T0, UH_NVALID, UH_COUNT, UH_INTS = 8 };
+// union bitmap and the ascending list.  The tile's token tl is T0 + tl, or
+// with UH_GROUPED set T0 + byte tl of the words from UH_TOK (a tile of at
+// most 16 tokens grouped from a window that starts at T0; see
+// qtile_group_kernel).
+enum { UH_B = 0, UH_KVH, UH_T0, UH_NVALID, UH_COUNT, UH_GROUPED, UH_TOK = 8, UH_INTS = 12 };
+constexpr int kGroupMaxTq = 16;  // tokens a grouped tile names (4 words of bytes)
+
+// the tile's token tl (sequence-local)
+__device__ __forceinline__ int qtile_token(const volatile int *hdr, int tl)
+{
+    return hdr[UH_T0] + (hdr[UH_GROUPED] ? (hdr[UH_TOK + (tl >> 2)] >> ((tl & 3) * 8)) & 0xff : tl);
+}
 struct UnionBuf {
     int mask_words, ubits_words, list_ints, bytes;
 };
@@ -273,6 +283,7 @@ __device__ __forceinline__ void qtile_union_warp(const Geo &g, const int *idx, c
         buf[UH_KVH] = kvh;
         buf[UH_T0] = t0;
         buf[UH_NVALID] = nvalid;
+        buf[UH_GROUPED] = 0;
         buf[UH_COUNT] = base;
     }
     __syncwarp();

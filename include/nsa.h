@@ -274,7 +274,13 @@ nsa_status nsa_causal_bwd(const nsa_problem *p, int32_t window, const int32_t *c
  *  - nsa_plan_build: checks the arguments, then on `stream` validates
  *    block_idx and writes the plan.  cu_seqlens is NULL for BHTD (p->layout
  *    NSA_LAYOUT_BHTD) and the packed-row offsets for THD.  Index errors are
- *    read with nsa_get_error(plan, ...); bad entries are left out.
+ *    read with nsa_get_error(plan, ...); bad entries are left out.  Where
+ *    the dQ tensor-core kernel runs (bf16, D = 128, 64-key blocks, G a
+ *    multiple of 8, BHTD) the plan also holds its query tiles' block unions
+ *    with the tiles' tokens grouped by shared blocks (a tile need not hold
+ *    consecutive tokens: fewer blocks per tile), which the planned backward
+ *    reads instead of building consecutive-token unions; the forward groups
+ *    its tiles the same way on every call.
  *  - nsa_bwd_planned_workspace_size / nsa_sel_bwd_planned: the selection
  *    backward (nsa_sel_bwd, or nsa_sel_varlen_bwd when p->layout is THD and
  *    cu_seqlens is given) taking the index from `plan`, which must have been

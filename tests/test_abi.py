@@ -86,7 +86,7 @@ def test_offsets_len(lib):
 
 def test_forward_workspace_holds_the_union_table(lib):
     """The selection forward's workspace: a 256-byte header, then (bf16 on the
-    tensor-core kernels) one union record per 128-row query tile: 8 header
+    tensor-core kernels) one union record per 128-row query tile: 12 header
     ints, a block bitmap per token, the union bitmap (words rounded up to 4)
     and the block list (rounded up to 4 ints), 128-byte rounded."""
     import torch
@@ -97,7 +97,7 @@ def test_forward_workspace_holds_the_union_table(lib):
         G, nb = Hq // Hkv, -(-T // bs)
         words = -(-nb // 32)
         tq = 128 // G
-        ints = 8 + tq * words + (words + 3) // 4 * 4 + (nb + 3) // 4 * 4
+        ints = 12 + tq * words + (words + 3) // 4 * 4 + (nb + 3) // 4 * 4
         rec = -(-ints * 4 // 128) * 128
         table = B * Hkv * -(-T // tq) * rec
         return 256 + -(-table // 256) * 256
