@@ -301,12 +301,13 @@ Helper *helper_of_current_device()
 }
 
 // begin(): work launched on side() from here on starts after everything
-// enqueued on st so far; at scope exit st waits for it.  Without a helper
-// (or before begin) side() is st itself: the launches stay in order.
+// enqueued on st so far; join() (or scope exit) makes what st enqueues next
+// wait for it.  Without a helper (or before begin) side() is st itself: the
+// launches stay in order.
 struct Fork {
     cudaStream_t st;
     Helper *h = nullptr;
-    bool forked = false;
+    bool forked = false, joined = false;
     std::unique_lock<std::mutex> lk;
     explicit Fork(cudaStream_t s) : st(s) {}
     void begin()
@@ -320,12 +321,17 @@ struct Fork {
             lk.unlock();
         }
     }
-    cudaStream_t side() const { return forked ? h->s : st; }
-    ~Fork()
+    cudaStream_t side() const { return forked && !joined ? h->s : st; }
+    void join()
     {
-        if (forked && (cudaEventRecord(h->join, h->s) != cudaSuccess || cudaStreamWaitEvent(st, h->join, 0) != cudaSuccess))
+        if (!forked || joined)
+            return;
+        if (cudaEventRecord(h->join, h->s) != cudaSuccess || cudaStreamWaitEvent(st, h->join, 0) != cudaSuccess)
             cudaStreamSynchronize(h->s);  // the join failed: order by waiting instead
+        joined = true;
+        lk.unlock();
     }
+    ~Fork() { join(); }
 };
 
 nsa_status check_ws(void *ws, size_t ws_bytes, size_t need)
@@ -385,10 +391,11 @@ nsa_status run_fwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
 // ordered walk per block list.  Both give the same canonical lists.
 // dot (nullable, chunked build only): delta computed in the count's launch
 // fork (nullable, with dot): begun once the count's launch (and so delta)
-// is enqueued
+// is enqueued; join (nullable): joined before the fill
 nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets, int *rows,
                      Unit *units, int *nchunk, int *slot, WsHeader *hdr, int *err, int chunk, cudaStream_t st,
-                     int *chunk_counts = nullptr, const DotArgs *dot = nullptr, Fork *fork = nullptr)
+                     int *chunk_counts = nullptr, const DotArgs *dot = nullptr, Fork *fork = nullptr,
+                     Fork *join = nullptr)
 {
     const size_t nbgj = (size_t)g.B * g.Hkv * g.nbmax;
     if (!g.dense && chunk_counts && csr_chunked_ok(g)) {
@@ -397,6 +404,8 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
         if (dot && fork)
             fork->begin();
         NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
+        if (join)
+            join->join();
         NSA_LAUNCH("csr_fill", launch_csr_chunk_fill(g, idx, chunk_counts, offsets, rows, st));
         return NSA_OK;
     }
@@ -405,6 +414,8 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
         NSA_LAUNCH("csr_count", launch_csr_count(g, idx, counts, err, st));
     }
     NSA_LAUNCH("csr_scan", launch_csr_scan(g, counts, offsets, units, nchunk, slot, hdr, chunk, st));
+    if (join)
+        join->join();
     if (!g.dense)
         NSA_LAUNCH("csr_fill", launch_csr_fill(g, idx, offsets, rows, st));
     return NSA_OK;
@@ -413,13 +424,13 @@ nsa_status build_csr(const Geo &g, const int32_t *idx, int *counts, int *offsets
 // Builds the plan of `idx` at `plan8` (layout L); index errors go to *err.
 // With dot, delta is computed in the same pass (see build_csr).
 nsa_status build_plan(const Geo &g, const int32_t *idx, char *plan8, const PlanLayout &L, int *err, cudaStream_t st,
-                      const DotArgs *dot = nullptr, Fork *fork = nullptr)
+                      const DotArgs *dot = nullptr, Fork *fork = nullptr, Fork *join = nullptr)
 {
     WsHeader *phdr = (WsHeader *)plan8;
     NSA_TRY(cudaMemsetAsync(phdr, 0, sizeof(WsHeader), st));
     return build_csr(g, idx, (int *)(plan8 + L.counts), (int *)(plan8 + L.offsets), (int *)(plan8 + L.rows),
                      (Unit *)(plan8 + L.units), (int *)(plan8 + L.nchunk), (int *)(plan8 + L.slot), phdr, err,
-                     L.chunk, st, (int *)(plan8 + L.chunkc), dot, fork);
+                     L.chunk, st, (int *)(plan8 + L.chunkc), dot, fork, join);
 }
 
 // whether build_plan takes the chunked path (which can carry the dot)
@@ -476,28 +487,43 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
     // free (one CTA of ~170 registers a thread per query tile)
     const bool gtc = !tc_supported(g, p->dtype) && gtc_supported(g, p->dtype);
     Fork fork(st);
+    // The dQ tensor-core kernel's union table with tiles grouped by shared
+    // blocks: built on the helper stream beside delta and the index build
+    // (it reads only the index), joined before the fill; its table is read
+    // only by dQ, after dK/dV.
+    Fork gfork(st);
+    bool grouped = false;
+    if (tc_supported(g, p->dtype) && !plan && mode == SPARSE && qtile_groupable(g) && qtile_union_table_bytes(g)) {
+        gfork.begin();
+        if (gfork.forked) {
+            const cudaStream_t st = gfork.side();
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, (int *)(w8 + L.utable), st, true));
+            grouped = true;
+        }
+    }
     if (!fused)
         NSA_LAUNCH("do_dot", launch_do_dot(g, o, dO, delta, p->dtype, st));
     if (gtc && !fused)
         fork.begin();
-    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr, gtc ? &fork : nullptr)) !=
-                     NSA_OK)
+    if (!plan && (s = build_plan(g, idx, pl8, P, &hdr->err, st, fused ? &dot : nullptr, gtc ? &fork : nullptr,
+                                 grouped ? &gfork : nullptr)) != NSA_OK)
         return s;
+    gfork.join();
     if (tc_supported(g, p->dtype)) {
         // the query-tile unions (sparse only): alongside the kernel before,
         // since they read only the index
-        // (consecutive tokens: grouping tiles by shared blocks costs more here
-        // than it saves dQ; a plan's table, built once, has them grouped)
+        // (grouped and built above, or a plan's, built once; else consecutive
+        // tokens, built here)
         int *utable = qtile_union_table_bytes(g) ? (int *)(w8 + L.utable) : nullptr;
         if (PP.has_utable)
             utable = (int *)(pl8 + PP.utable);
-        else if (utable)
+        else if (utable && !grouped)
             NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, utable, st, false));
         NSA_LAUNCH("dkdv_tc", launch_dkdv_tc(g, q, k, v, dO, lse, delta, offsets, rows, units, phdr, P.max_units,
                                partials, dk, dv, &hdr->err, st));
         // dQ right after dK/dV: it is that kernel's programmatic dependent
         NSA_LAUNCH("dq_tc",
-                   launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, PP.has_utable, dq, &hdr->err,
+                   launch_dq_tc(g, q, k, v, dO, lse, delta, idx, utable, PP.has_utable || grouped, dq, &hdr->err,
                                 &hdr->tile_next, st));
         NSA_LAUNCH("dkdv_reduce", launch_dkdv_reduce(g, nchunk, slot, partials, dk, dv, p->dtype, st));
     } else if (gtc) {
