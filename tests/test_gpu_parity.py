@@ -419,6 +419,46 @@ def test_planned_backward_is_the_same_backward(dtype, shape):
         _compare(dict(o=ref["o"], lse=ref["lse"], dq=dq, dk=dk, dv=dv), want, dtype)
 
 
+def _clustered_block_idx(B, Hkv, T, bs, S, seed):
+    """Each token: its own block, then up to S - 1 distinct earlier blocks
+    drawn from a few shared sets (every token of a set of consecutive tokens
+    draws from the same 6 blocks), -1 padding.  Tokens share most of their
+    blocks, so tile grouping meets many equal costs."""
+    g = np.random.default_rng(seed)
+    idx = np.full((B, Hkv, T, S), -1, dtype=np.int32)
+    for b in range(B):
+        for h in range(Hkv):
+            for t0 in range(0, T, 24):
+                own0 = t0 // bs
+                pool = g.choice(max(own0, 1), size=min(6, max(own0, 1)), replace=False) if own0 else np.array([], int)
+                for t in range(t0, min(T, t0 + 24)):
+                    own = t // bs
+                    cand = [int(j) for j in pool if j < own]
+                    picks = g.permutation(cand)[: S - 1] if cand else []
+                    row = [own] + [int(j) for j in picks]
+                    idx[b, h, t, : len(row)] = row
+    return torch.from_numpy(idx)
+
+
+def test_grouped_query_tiles_clustered_selection():
+    """Clustered selections on the tensor-core path (G = 16, BHTD), where the
+    forward, the backward and a plan group the query tiles by shared blocks:
+    forward, backward and planned backward against the oracle."""
+    B, Hq, Hkv, T, D, bs, S = 1, 32, 2, 700, 128, 64, 5
+    q, k, v, do = inputs.make_qkv_do(B, Hq, Hkv, T, D, dtype=torch.bfloat16, seed=70)
+    idx = _clustered_block_idx(B, Hkv, T, bs, S, seed=70)
+    assert oracle.validate_index(idx, bs) == 0
+    got = _run(q, k, v, do, idx, bs)
+    ref = oracle.sel_bwd(q, k, v, idx, do, bs)
+    _compare(got, ref, torch.bfloat16)
+    g = [x.to(DEV) for x in (q, k, v, do, idx)]
+    plan = api.build_plan(g[0], g[1], g[4], bs)
+    dq, dk, dv = api.sel_bwd(g[0], g[1], g[2], got["o"], g[3], got["lse"], g[4], bs, plan=plan)
+    torch.cuda.synchronize()
+    assert api.get_error(plan) == 0
+    _compare(dict(o=got["o"], lse=got["lse"], dq=dq, dk=dk, dv=dv), ref, torch.bfloat16)
+
+
 def test_planned_backward_varlen_and_bad_index():
     Hq, Hkv, D, bs, S = 8, 2, 128, 64, 6
     lengths = [130, 64, 257]
