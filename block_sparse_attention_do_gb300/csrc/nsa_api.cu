@@ -510,10 +510,10 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         return s;
     gfork.join();
     if (tc_supported(g, p->dtype)) {
-        // the query-tile unions (sparse only): alongside the kernel before,
-        // since they read only the index
-        // (grouped and built above, or a plan's, built once; else consecutive
-        // tokens, built here)
+        // the query-tile unions (sparse only): grouped and built beside the
+        // index build above, or a plan's (built once), or else of consecutive
+        // tokens, built here alongside the kernel before (they read only the
+        // index)
         int *utable = qtile_union_table_bytes(g) ? (int *)(w8 + L.utable) : nullptr;
         if (PP.has_utable)
             utable = (int *)(pl8 + PP.utable);
