@@ -693,7 +693,6 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
 #pragma unroll
             for (int x = 0; x < WORDS; ++x)
                 cur[x] = 0u;
-            uint32_t packed[kGroupMaxTq / 4] = {0u, 0u, 0u, 0u};
             int slot0 = -1, slot1 = -1;  // the tile row each of this lane's tokens took
             for (int pick = 0; pick < nk; ++pick) {
                 // key = cost << 8 | token: the free token adding the fewest
@@ -716,17 +715,11 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
 #pragma unroll
                 for (int x = 0; x < WORDS; ++x)
                     cur[x] |= __shfl_sync(0xffffffffu, qb == 0 ? m[0][x] : m[1][x], owner);
-                if (lane == owner) {
-                    avail &= ~(1u << qb);
-                    if (qb == 0)
-                        slot0 = pick;
-                    else
-                        slot1 = pick;
-                }
-#pragma unroll
-                for (int x = 0; x < kGroupMaxTq / 4; ++x)
-                    if ((pick >> 2) == x)
-                        packed[x] |= (uint32_t)best << ((pick & 3) * 8);
+                // the owner's bookkeeping as selects: no divergent branch on the chain
+                const bool mine = lane == owner;
+                avail &= mine ? ~(1u << qb) : 0xffffffffu;
+                slot0 = mine && qb == 0 ? pick : slot0;
+                slot1 = mine && qb == 1 ? pick : slot1;
             }
             // the tile's rows: each token's bitmap by its lane, then empty
             // bitmaps for rows past the tile's tokens
@@ -761,13 +754,17 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
             for (uint32_t bb = bits; bb; bb &= bb - 1u)
                 list[pos++] = lane * 32 + __ffs(bb) - 1;
             const int total = __shfl_sync(0xffffffffu, incl, 31);  // every lane takes part
-            if (lane < kGroupMaxTq / 4) {
-                uint32_t pw = 0u;
+            // the tile's tokens, byte r of the words = row r's offset in the window
 #pragma unroll
-                for (int x = 0; x < kGroupMaxTq / 4; ++x)
-                    if (lane == x)
-                        pw = packed[x];
-                dst[UH_TOK + lane] = (int)pw;
+            for (int x = 0; x < kGroupMaxTq / 4; ++x) {
+                uint32_t part = 0u;
+                if (slot0 >= 0 && (slot0 >> 2) == x)
+                    part |= (uint32_t)lane << ((slot0 & 3) * 8);
+                if (slot1 >= 0 && (slot1 >> 2) == x)
+                    part |= (uint32_t)(lane + 32) << ((slot1 & 3) * 8);
+                part = __reduce_or_sync(0xffffffffu, part);
+                if (lane == x)
+                    dst[UH_TOK + x] = (int)part;
             }
             if (lane == 0) {
                 dst[UH_B] = b;
