@@ -602,44 +602,46 @@ __global__ void __launch_bounds__(256) qtile_union_kernel(Geo g, const int *__re
 }
 
 // Tiles grouped by shared blocks.  The tokens of Wt consecutive tiles (a
-// window of W = Wt * Tq <= 64 tokens of one (b, kv head)) are dealt into
-// the same number of tiles greedily: a tile starts with the window's first
+// window of W = Wt * Tq <= 64 or 128 tokens of one (b, kv head)) are dealt
+// into the same number of tiles greedily: a tile starts with the window's first
 // free token and takes, Tq - 1 times, the free token that adds the fewest
 // blocks to its union (ties to the lower token).  A tile need not hold
 // consecutive tokens, and tokens that share blocks make smaller unions: on
-// uniformly drawn selections the block pairs a tile walks drop by ~13%; on
-// selections that cluster, by more.  One warp per window: lane l holds the
-// block bitmaps of tokens l and l + 32 in registers (every index entry of
-// both read at once), and a pick is one warp-wide minimum of (cost, token).
+// uniformly drawn selections the block pairs a tile walks drop by ~13%
+// (64-token windows) or ~16% (128); on selections that cluster, by more.
+// One warp per window: lane l holds the block bitmaps of tokens l + 32 q in
+// registers (every index entry read at once), and a pick is one warp-wide
+// minimum of (cost, token).
 // The union records go where qtile_union_kernel puts them, with UH_GROUPED
 // set and the tokens as offsets from the window's start.  For tiles of
 // 2 .. kGroupMaxTq tokens whose Q (and dO) rows the kernels load by token
 // (row-group layout).
-constexpr int kGroupWindow = 64;  // tokens a window holds at most
-constexpr int kGroupWords = 8;    // block bitmap words a grouped window may need (nbmax <= 256)
+constexpr int kGroupWords = 8;  // block bitmap words a grouped window may need (nbmax <= 256)
 
-// WORDS: the block bitmap's words, (nbmax + 31) / 32 rounded up to 1, 2, 4 or 8
-template <int WORDS>
+// WORDS: the block bitmap's words, (nbmax + 31) / 32 rounded up to 1, 2, 4 or
+// 8; TPL: tokens a lane holds, so a window holds up to 32 TPL tokens (64 or
+// 128: the larger groups better and takes about twice as long)
+template <int WORDS, int TPL>
 __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__restrict__ idx, UnionBuf up,
                                                           int *__restrict__ utable)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int words = (g.nbmax + 31) / 32;
-    const int Tq = tile_tokens(g.G), Wt = kGroupWindow / Tq, W = Wt * Tq;
+    const int Tq = tile_tokens(g.G), Wt = 32 * TPL / Tq, W = Wt * Tq;
     const int nbg = g.B * g.Hkv, per_seq = (g.T + Tq - 1) / Tq, nwin = (per_seq + Wt - 1) / Wt;
     const bool vec = (g.S & 3) == 0 && ((uintptr_t)idx & 15) == 0;  // index rows in 16-byte pieces
     for (int item = blockIdx.x * (blockDim.x >> 5) + w; item < nbg * nwin; item += gridDim.x * (blockDim.x >> 5)) {
         const int bg = item % nbg, win = item / nbg;
         const int b = bg / g.Hkv, kvh = bg % g.Hkv;
         const int t0 = win * W, ntok = min(W, g.T - t0);
-        // lane l holds window tokens l + 32 q (q < 2): their block bitmaps,
+        // lane l holds window tokens l + 32 q (q < TPL): their block bitmaps,
         // and bit q of avail while the token is free
-        uint32_t m[2][WORDS];
+        uint32_t m[TPL][WORDS];
         uint32_t avail = 0u;
-        int tq[2];
+        int tq[TPL];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < TPL; ++q) {
 #pragma unroll
             for (int x = 0; x < WORDS; ++x)
                 m[q][x] = 0u;
@@ -649,9 +651,9 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
         }
         // the tokens' index entries: every load of a round issued before any is used
         for (int s0 = 0; s0 < g.S; s0 += 8) {
-            int jv[2][8];
+            int jv[TPL][8];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < TPL; ++q) {
                 const int *row = idx_row(g, idx, b, kvh, tq[q]);
                 if (vec) {
 #pragma unroll
@@ -669,7 +671,7 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < TPL; ++q) {
                 const int t = tq[q];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -693,13 +695,16 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
 #pragma unroll
             for (int x = 0; x < WORDS; ++x)
                 cur[x] = 0u;
-            int slot0 = -1, slot1 = -1;  // the tile row each of this lane's tokens took
+            int slot[TPL];  // the tile row each of this lane's tokens took
+#pragma unroll
+            for (int q = 0; q < TPL; ++q)
+                slot[q] = -1;
             for (int pick = 0; pick < nk; ++pick) {
                 // key = cost << 8 | token: the free token adding the fewest
                 // blocks (for the first pick every cost is 0: the lowest token)
                 unsigned key = 0xffffffffu;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < TPL; ++q) {
                     unsigned cost = 0u;
 #pragma unroll
                     for (int x = 0; x < WORDS; ++x)
@@ -713,19 +718,25 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
                 const int best = (int)(key & 0xffu), owner = best & 31, qb = best >> 5;
                 // the token's bitmap from its lane into the union
 #pragma unroll
-                for (int x = 0; x < WORDS; ++x)
-                    cur[x] |= __shfl_sync(0xffffffffu, qb == 0 ? m[0][x] : m[1][x], owner);
+                for (int x = 0; x < WORDS; ++x) {
+                    uint32_t v = m[0][x];
+#pragma unroll
+                    for (int q = 1; q < TPL; ++q)
+                        v = qb == q ? m[q][x] : v;
+                    cur[x] |= __shfl_sync(0xffffffffu, v, owner);
+                }
                 // the owner's bookkeeping as selects: no divergent branch on the chain
                 const bool mine = lane == owner;
                 avail &= mine ? ~(1u << qb) : 0xffffffffu;
-                slot0 = mine && qb == 0 ? pick : slot0;
-                slot1 = mine && qb == 1 ? pick : slot1;
+#pragma unroll
+                for (int q = 0; q < TPL; ++q)
+                    slot[q] = mine && qb == q ? pick : slot[q];
             }
             // the tile's rows: each token's bitmap by its lane, then empty
             // bitmaps for rows past the tile's tokens
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int sl = q == 0 ? slot0 : slot1;
+            for (int q = 0; q < TPL; ++q) {
+                const int sl = slot[q];
                 if (sl >= 0)
 #pragma unroll
                     for (int x = 0; x < WORDS; ++x)
@@ -758,10 +769,10 @@ __global__ void __launch_bounds__(128) qtile_group_kernel(Geo g, const int *__re
 #pragma unroll
             for (int x = 0; x < kGroupMaxTq / 4; ++x) {
                 uint32_t part = 0u;
-                if (slot0 >= 0 && (slot0 >> 2) == x)
-                    part |= (uint32_t)lane << ((slot0 & 3) * 8);
-                if (slot1 >= 0 && (slot1 >> 2) == x)
-                    part |= (uint32_t)(lane + 32) << ((slot1 & 3) * 8);
+#pragma unroll
+                for (int q = 0; q < TPL; ++q)
+                    if (slot[q] >= 0 && (slot[q] >> 2) == x)
+                        part |= (uint32_t)(lane + 32 * q) << ((slot[q] & 3) * 8);
                 part = __reduce_or_sync(0xffffffffu, part);
                 if (lane == x)
                     dst[UH_TOK + x] = (int)part;
@@ -797,7 +808,7 @@ size_t qtile_union_table_bytes(const Geo &g)
     return (size_t)((g.T + Tq - 1) / Tq) * g.B * g.Hkv * union_buf(g).bytes;
 }
 
-cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group)
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group, bool wide)
 {
     if (qtile_union_table_bytes(g) == 0)
         return cudaSuccess;
@@ -805,13 +816,17 @@ cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaS
     const int ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const UnionBuf up = union_buf(g);
     if (group && qtile_groupable(g)) {
-        const int Wt = kGroupWindow / Tq, nwin = ((g.T + Tq - 1) / Tq + Wt - 1) / Wt;
+        const int Wt = (wide ? 128 : 64) / Tq, nwin = ((g.T + Tq - 1) / Tq + Wt - 1) / Wt;
         const int items = g.B * g.Hkv * nwin, grid = (items + 3) / 4;
         if (grid < 1)
             return cudaSuccess;
         const int words = (g.nbmax + 31) / 32;
-        auto kern = words <= 1 ? qtile_group_kernel<1> : words <= 2 ? qtile_group_kernel<2>
-                  : words <= 4 ? qtile_group_kernel<4> : qtile_group_kernel<8>;
+        auto pick = [&](auto tpl) {
+            constexpr int T_ = decltype(tpl)::value;
+            return words <= 1 ? qtile_group_kernel<1, T_> : words <= 2 ? qtile_group_kernel<2, T_>
+                 : words <= 4 ? qtile_group_kernel<4, T_> : qtile_group_kernel<8, T_>;
+        };
+        auto kern = wide ? pick(std::integral_constant<int, 4>()) : pick(std::integral_constant<int, 2>());
         return launch_dependent(kern, dim3(grid), dim3(128), 0, st, g, idx, up, utable);
     }
     const int grid = (ntiles + 7) / 8;

@@ -114,8 +114,10 @@ size_t qtile_union_table_bytes(const Geo &g);
 // consecutive tokens (qtile_group_kernel)
 bool qtile_groupable(const Geo &g);
 // group: tiles grouped by shared blocks where qtile_groupable, else
-// consecutive tokens
-cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group);
+// consecutive tokens; wide: grouped over 128-token windows instead of 64
+// (fewer blocks per tile, about twice the time)
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group,
+                                bool wide = false);
 // utable: the union table launch_qtile_unions wrote, or null (dense
 // entries); grouped: its tiles are grouped by shared blocks
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,

@@ -497,7 +497,8 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         gfork.begin();
         if (gfork.forked) {
             const cudaStream_t st = gfork.side();
-            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, (int *)(w8 + L.utable), st, true));
+            // (64-token windows: the 128-token grouping outlasts the work it runs beside)
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, (int *)(w8 + L.utable), st, true, false));
             grouped = true;
         }
     }
@@ -743,7 +744,8 @@ nsa_status nsa_plan_build(const nsa_problem *p, const int32_t *cu_seqlens, const
     if ((s = build_plan(g, block_idx, pl8, L, &((WsHeader *)pl8)->err, st)) != NSA_OK)
         return s;
     if (L.has_utable)  // the dQ kernel's query-tile unions, tiles grouped by shared blocks
-        NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, block_idx, (int *)(pl8 + L.utable), st, true));
+        // over 128-token windows: a plan is built once, so the better grouping's time is paid once
+        NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, block_idx, (int *)(pl8 + L.utable), st, true, true));
     return NSA_OK;
 }
 
