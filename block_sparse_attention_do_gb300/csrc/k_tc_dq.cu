@@ -808,7 +808,7 @@ size_t qtile_union_table_bytes(const Geo &g)
     return (size_t)((g.T + Tq - 1) / Tq) * g.B * g.Hkv * union_buf(g).bytes;
 }
 
-cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group, bool wide)
+cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group, int tpl)
 {
     if (qtile_union_table_bytes(g) == 0)
         return cudaSuccess;
@@ -816,7 +816,8 @@ cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaS
     const int ntiles = ((g.T + Tq - 1) / Tq) * g.B * g.Hkv;
     const UnionBuf up = union_buf(g);
     if (group && qtile_groupable(g)) {
-        const int Wt = (wide ? 128 : 64) / Tq, nwin = ((g.T + Tq - 1) / Tq + Wt - 1) / Wt;
+        tpl = tpl < 2 ? 2 : tpl > 4 ? 4 : tpl;
+        const int Wt = 32 * tpl / Tq, nwin = ((g.T + Tq - 1) / Tq + Wt - 1) / Wt;
         const int items = g.B * g.Hkv * nwin, grid = (items + 3) / 4;
         if (grid < 1)
             return cudaSuccess;
@@ -826,7 +827,8 @@ cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaS
             return words <= 1 ? qtile_group_kernel<1, T_> : words <= 2 ? qtile_group_kernel<2, T_>
                  : words <= 4 ? qtile_group_kernel<4, T_> : qtile_group_kernel<8, T_>;
         };
-        auto kern = wide ? pick(std::integral_constant<int, 4>()) : pick(std::integral_constant<int, 2>());
+        auto kern = tpl == 4 ? pick(std::integral_constant<int, 4>())
+                  : tpl == 3 ? pick(std::integral_constant<int, 3>()) : pick(std::integral_constant<int, 2>());
         return launch_dependent(kern, dim3(grid), dim3(128), 0, st, g, idx, up, utable);
     }
     const int grid = (ntiles + 7) / 8;

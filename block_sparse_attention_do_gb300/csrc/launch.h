@@ -114,10 +114,11 @@ size_t qtile_union_table_bytes(const Geo &g);
 // consecutive tokens (qtile_group_kernel)
 bool qtile_groupable(const Geo &g);
 // group: tiles grouped by shared blocks where qtile_groupable, else
-// consecutive tokens; wide: grouped over 128-token windows instead of 64
-// (fewer blocks per tile, about twice the time)
+// consecutive tokens; tpl: tokens per lane of the grouping warp (2, 3 or 4:
+// windows of 64, 96 or 128 tokens; a wider window groups better and takes
+// longer)
 cudaError_t launch_qtile_unions(const Geo &g, const int *idx, int *utable, cudaStream_t st, bool group,
-                                bool wide = false);
+                                int tpl = 2);
 // utable: the union table launch_qtile_unions wrote, or null (dense
 // entries); grouped: its tiles are grouped by shared blocks
 cudaError_t launch_dq_tc(const Geo &g, const void *q, const void *k, const void *v,

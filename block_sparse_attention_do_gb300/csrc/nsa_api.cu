@@ -497,8 +497,9 @@ nsa_status run_bwd(const nsa_problem *p, bool thd, Mode mode, const int32_t *cu,
         gfork.begin();
         if (gfork.forked) {
             const cudaStream_t st = gfork.side();
-            // (64-token windows: the 128-token grouping outlasts the work it runs beside)
-            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, (int *)(w8 + L.utable), st, true, false));
+            // (64-token windows: grouping over 96 or 128 outlasts the work it runs
+            // beside and delays the fill)
+            NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, idx, (int *)(w8 + L.utable), st, true, 2));
             grouped = true;
         }
     }
@@ -745,7 +746,7 @@ nsa_status nsa_plan_build(const nsa_problem *p, const int32_t *cu_seqlens, const
         return s;
     if (L.has_utable)  // the dQ kernel's query-tile unions, tiles grouped by shared blocks
         // over 128-token windows: a plan is built once, so the better grouping's time is paid once
-        NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, block_idx, (int *)(pl8 + L.utable), st, true, true));
+        NSA_LAUNCH("qtile_unions", launch_qtile_unions(g, block_idx, (int *)(pl8 + L.utable), st, true, 4));
     return NSA_OK;
 }
 
